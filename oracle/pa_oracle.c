@@ -1,0 +1,428 @@
+/*
+ * pa_oracle.c -- plain, slow, CPU reference for paged-KV decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This library exists to check the CUDA path; it is
+ * never part of it.  Only the test suite, the smoke check in __graft_entry__ and
+ * the CPU-baseline / reference legs of bench.py may load it.  It shares no code,
+ * header, table or constant with the CUDA library, and it includes nothing from
+ * the package.
+ *
+ * Every function computes the plain definition of its step, in double precision
+ * unless the step itself fixes another precision (the FP8 writer is defined in
+ * fp32 arithmetic, see oracle_reshape_and_cache_fp8).  No blocking, fusion,
+ * online softmax or reordering beyond what the definition states.
+ *
+ * Sources (web pages this method is described on):
+ *   [P1] "appendonly" (rajatmohan.com), sections "Paging, because contiguous
+ *        allocation is a disaster" and "Prefix sharing is where the real win lives".
+ *   [P3] "KV Cache Engineering for LLM Serving" (dailydoseofds), sections
+ *        1 "GQA and MQA cache fewer heads", 8 "Quantization", 10 "Paging".
+ *   [P4] "Taming the Token Torrent" (architects-blueprint), sections
+ *        "The Block Table Logic" and "Custom PagedAttention Kernels".
+ *   OCP 8-bit Floating Point Specification (OFP8), E4M3 format.
+ *
+ * Layouts (all row-major):
+ *   q            [B, Hq, D]                 bf16 bit patterns (uint16)
+ *   k/v pool     [nblocks, bs, Hkv, D]      bf16 bit patterns, or E4M3 codes (uint8)
+ *   k/v scale    [nblocks, Hkv]             fp32 (FP8 pools only)
+ *   block_tables [B, max_blocks]            int32
+ *   seq_lens     [B]                        int32 (tokens in the cache, incl. this step's)
+ *   slot_mapping [T]                        int64 (slot = block * bs + offset; < 0 = skip)
+ *   out          [B, Hq, D]                 double
+ *
+ * Parity status of each function is listed in the header comment of
+ * oracle/__init__.py together with the tests that pin it.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* Scalar formats                                                             */
+/* ------------------------------------------------------------------------- */
+
+/* bf16 is the upper half of an IEEE binary32. */
+static float bf16_bits_to_float(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+double oracle_bf16_to_double(uint16_t h) { return (double)bf16_bits_to_float(h); }
+
+/*
+ * OFP8 E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits.
+ *   exponent field 0      : subnormal, |x| = 2^-6 * (m / 8)
+ *   exponent field 1..15  : normal,    |x| = 2^(e-7) * (1 + m / 8)
+ *   S.1111.111            : NaN (the only non-finite encoding; no infinities)
+ * Largest finite magnitude: S.1111.110 = 448.
+ */
+double oracle_e4m3_to_double(uint8_t c)
+{
+    int s = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 0x7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/*
+ * Round a float to E4M3, to nearest with ties to the even code, saturating
+ * finite values of magnitude >= 448 to +-448 ("satfinite").  NaN maps to the
+ * NaN code.  The sign of the input is kept, so values that round to zero give
+ * +0 (0x00) or -0 (0x80).
+ *
+ * Written as the definition: scan the 127 non-negative finite codes (their
+ * magnitudes increase with the code), take the two that bracket |x| and pick the
+ * nearer one, comparing against their exact midpoint.
+ */
+uint8_t oracle_e4m3_from_float(float x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a, lo_v, hi_v, mid;
+    int hi;
+    if (isnan(x))
+        return 0x7F;
+    a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    hi = 0;
+    while (oracle_e4m3_to_double((uint8_t)hi) < a)
+        hi++;                                   /* stops at <= 0x7E since a < 448 */
+    hi_v = oracle_e4m3_to_double((uint8_t)hi);
+    if (hi_v == a || hi == 0)
+        return (uint8_t)(sign | hi);
+    lo_v = oracle_e4m3_to_double((uint8_t)(hi - 1));
+    mid = 0.5 * (lo_v + hi_v);                  /* exact: both have few significant bits */
+    if (a < mid)
+        return (uint8_t)(sign | (hi - 1));
+    if (a > mid)
+        return (uint8_t)(sign | hi);
+    return (uint8_t)(sign | (((hi & 1) == 0) ? hi : hi - 1));   /* tie: even code */
+}
+
+/* Array forms of the two E4M3 conversions (same definitions, element by element). */
+void oracle_e4m3_to_double_array(const uint8_t *c, long long n, double *out)
+{
+    long long i;
+    for (i = 0; i < n; i++)
+        out[i] = oracle_e4m3_to_double(c[i]);
+}
+
+void oracle_e4m3_from_float_array(const float *x, long long n, uint8_t *out)
+{
+    long long i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < n; i++)
+        out[i] = oracle_e4m3_from_float(x[i]);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Small definitions pinned by the pages' printed examples                   */
+/* ------------------------------------------------------------------------- */
+
+/* [P3] section 1: query head h reads KV head h / (Hq / Hkv); a group of Hq/Hkv
+ * consecutive query heads shares one KV head. */
+int oracle_kv_head(int h, int Hq, int Hkv) { return h / (Hq / Hkv); }
+
+/* [P3] "The cache formula" / section 1: scalars cached = 2 (K and V) x KV heads
+ * x tokens x head size, per layer. */
+long long oracle_cached_scalars(int layers, int Hkv, long long tokens, int D)
+{
+    return 2LL * layers * Hkv * tokens * D;
+}
+
+/*
+ * [P3] section 8: absmax quantiser onto signed integer codes.
+ *   scale = max|x| / largest_code, largest_code = 2^(bits-1) - 1
+ *   code  = clip(rint(x / scale), -largest_code, largest_code)   (rint: ties to even)
+ *   restored = code * scale
+ * Double precision, as in the page's example.  A zero absmax gives scale 0 and
+ * all-zero codes.
+ */
+void oracle_quantize_absmax_int(const double *x, int n, int bits, int *codes,
+                                double *restored, double *scale_out)
+{
+    int i, largest = (1 << (bits - 1)) - 1;
+    double amax = 0.0, scale;
+    for (i = 0; i < n; i++)
+        if (fabs(x[i]) > amax)
+            amax = fabs(x[i]);
+    scale = amax / (double)largest;
+    for (i = 0; i < n; i++) {
+        double c = (scale == 0.0) ? 0.0 : nearbyint(x[i] / scale);
+        if (c > largest) c = largest;
+        if (c < -largest) c = -largest;
+        codes[i] = (int)c;
+        restored[i] = c * scale;
+    }
+    *scale_out = scale;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Cache write (reshape_and_cache)                                            */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * [P4] "How Paging Works": a new token goes into a physical block taken from
+ * the pool; [P4] "The Block Table Logic": logical index -> (block, offset).
+ * Slot s addresses row (s / bs, s % bs) of the pool.  For each token t with
+ * slot_mapping[t] >= 0 the K/V vectors of all KV heads are copied bit for bit:
+ *   pool[s / bs][s % bs][h][:] = new[t][h][:]
+ * Negative slots are padding and write nothing.
+ */
+void oracle_reshape_and_cache_bf16(int T, int Hkv, int D, int bs,
+                                   const uint16_t *k_new, const uint16_t *v_new,
+                                   uint16_t *k_pool, uint16_t *v_pool,
+                                   const int64_t *slot_mapping)
+{
+    int t, h, d;
+    for (t = 0; t < T; t++) {
+        int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        for (h = 0; h < Hkv; h++)
+            for (d = 0; d < D; d++) {
+                size_t dst = (((size_t)(s / bs) * bs + (size_t)(s % bs)) * Hkv + h) * D + d;
+                size_t src = ((size_t)t * Hkv + h) * D + d;
+                k_pool[dst] = k_new[src];
+                v_pool[dst] = v_new[src];
+            }
+    }
+}
+
+/*
+ * One (block, kv head) of an FP8 pool receives the token vector x[0..D) at
+ * offset off.  Reading of [P3] section 8 for a paged cache with one fp32 scale
+ * per (block, kv head):
+ *   - the scale is absmax / 448 over every value ever written into this
+ *     (block, head) since its offset 0 was written (448 = largest E4M3 code),
+ *     computed as an fp32 IEEE division.  Writing offset 0 starts afresh.
+ *   - code = E4M3(x / scale), fp32 IEEE division, ties-to-even, saturating.
+ *   - when a write raises the scale, the codes already stored at offsets
+ *     0..off-1 are re-encoded from their restored values:
+ *       restored = float(E4M3 value) * old_scale   (one fp32 product)
+ *       code'    = E4M3(restored / new_scale)
+ *   - a zero scale stores +0 codes.
+ * Because fp32 division is monotone, keeping max(old, absmax_new / 448) equals
+ * absmax_over_all / 448.
+ */
+static void fp8_write_row(uint8_t *pool, float *scale, int Hkv, int D, int bs,
+                          int64_t blk, int off, int h, const uint16_t *x)
+{
+    float amax = 0.0f, cand, old, s_new;
+    int d, r;
+    float *sp = &scale[blk * Hkv + h];
+    for (d = 0; d < D; d++) {
+        float v = fabsf(bf16_bits_to_float(x[d]));
+        if (v > amax)
+            amax = v;
+    }
+    cand = amax / 448.0f;
+    old = *sp;
+    s_new = (off == 0 || cand > old) ? cand : old;
+    if (off > 0 && s_new > old) {
+        for (r = 0; r < off; r++)
+            for (d = 0; d < D; d++) {
+                uint8_t *c = &pool[(((size_t)blk * bs + r) * Hkv + h) * D + d];
+                float restored = (float)oracle_e4m3_to_double(*c) * old;
+                *c = (s_new == 0.0f) ? 0x00 : oracle_e4m3_from_float(restored / s_new);
+            }
+    }
+    for (d = 0; d < D; d++) {
+        float v = bf16_bits_to_float(x[d]);
+        pool[(((size_t)blk * bs + off) * Hkv + h) * D + d] =
+            (s_new == 0.0f) ? 0x00 : oracle_e4m3_from_float(v / s_new);
+    }
+    *sp = s_new;
+}
+
+/* FP8 variant of the cache write: the slot mapping of oracle_reshape_and_cache_bf16
+ * and the per-(block, head) quantiser of fp8_write_row.  Tokens are applied in
+ * index order. */
+void oracle_reshape_and_cache_fp8(int T, int Hkv, int D, int bs,
+                                  const uint16_t *k_new, const uint16_t *v_new,
+                                  uint8_t *k_pool, uint8_t *v_pool,
+                                  float *k_scale, float *v_scale,
+                                  const int64_t *slot_mapping)
+{
+    int t, h;
+    for (t = 0; t < T; t++) {
+        int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        for (h = 0; h < Hkv; h++) {
+            fp8_write_row(k_pool, k_scale, Hkv, D, bs, s / bs, (int)(s % bs), h,
+                          &k_new[((size_t)t * Hkv + h) * D]);
+            fp8_write_row(v_pool, v_scale, Hkv, D, bs, s / bs, (int)(s % bs), h,
+                          &v_new[((size_t)t * Hkv + h) * D]);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Decode attention                                                           */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    int Hq, Hkv, D, bs, max_blocks, kv_fp8;
+    const void *k_pool, *v_pool;
+    const float *k_scale, *v_scale;
+    const int32_t *block_tables;
+} paged_kv;
+
+/* Gather: element d of the key (or value) of logical token t of sequence b, KV
+ * head kvh ([P4] "The Block Table Logic"; [P1] "Paging"):
+ *   block = block_tables[b][t / bs], row = pool[block][t % bs][kvh][d]
+ * FP8 pools are restored as code value * scale[block][kvh], exactly in double. */
+static double kv_elem(const paged_kv *p, int is_v, int b, int t, int kvh, int d)
+{
+    int32_t blk = p->block_tables[(size_t)b * p->max_blocks + t / p->bs];
+    size_t idx = (((size_t)blk * p->bs + (size_t)(t % p->bs)) * p->Hkv + kvh) * p->D + d;
+    const void *pool = is_v ? p->v_pool : p->k_pool;
+    if (!p->kv_fp8)
+        return oracle_bf16_to_double(((const uint16_t *)pool)[idx]);
+    {
+        const float *sc = is_v ? p->v_scale : p->k_scale;
+        return oracle_e4m3_to_double(((const uint8_t *)pool)[idx]) *
+               (double)sc[(size_t)blk * p->Hkv + kvh];
+    }
+}
+
+/*
+ * Textbook attention of one query head over tokens [t0, t1) of sequence b:
+ *   s_t = sm_scale * <q, K_t>,   w_t = exp(s_t - max_t s_t)
+ *   o   = sum_t w_t V_t / sum_t w_t,   lse = max_t s_t + ln(sum_t w_t)
+ * An empty range gives o = 0 and lse = -inf.
+ */
+static void attend_range(const paged_kv *p, const uint16_t *q_row, int b, int h,
+                         int t0, int t1, double sm_scale, double *o, double *lse)
+{
+    int kvh = oracle_kv_head(h, p->Hq, p->Hkv);
+    int n = t1 - t0, t, d;
+    double mx = -INFINITY, sum = 0.0;
+    double *s;
+    for (d = 0; d < p->D; d++)
+        o[d] = 0.0;
+    if (n <= 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    s = (double *)malloc(sizeof(double) * (size_t)n);
+    for (t = 0; t < n; t++) {
+        double acc = 0.0;
+        for (d = 0; d < p->D; d++)
+            acc += oracle_bf16_to_double(q_row[d]) * kv_elem(p, 0, b, t0 + t, kvh, d);
+        s[t] = sm_scale * acc;
+        if (s[t] > mx)
+            mx = s[t];
+    }
+    for (t = 0; t < n; t++) {
+        s[t] = exp(s[t] - mx);
+        sum += s[t];
+    }
+    for (t = 0; t < n; t++)
+        for (d = 0; d < p->D; d++)
+            o[d] += s[t] * kv_elem(p, 1, b, t0 + t, kvh, d);
+    for (d = 0; d < p->D; d++)
+        o[d] /= sum;
+    *lse = mx + log(sum);
+    free(s);
+}
+
+/*
+ * Decode attention for a batch: out[b][h] = softmax(sm_scale * q[b,h] K_b^T) V_b
+ * over the L_b = seq_lens[b] tokens of sequence b, gathered through its block
+ * table ([P4] "Custom PagedAttention Kernels": grid over (sequence, head),
+ * walk the block table, load K and V, scaled dot-product attention).
+ * With rows == NULL every (b, h) is computed into out[B][Hq][D]; otherwise only
+ * the nrows pairs (rows_b[i], rows_h[i]) into out[nrows][D].
+ * Parallel over rows with OpenMP when nthreads > 1 (each row is independent).
+ */
+void oracle_paged_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks, int kv_fp8,
+                         const uint16_t *q, const void *k_pool, const void *v_pool,
+                         const float *k_scale, const float *v_scale,
+                         const int32_t *block_tables, const int32_t *seq_lens,
+                         double sm_scale, int nrows, const int32_t *rows_b,
+                         const int32_t *rows_h, double *out, int nthreads)
+{
+    paged_kv p;
+    long long i, n;
+    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_fp8 = kv_fp8;
+    p.k_pool = k_pool; p.v_pool = v_pool; p.k_scale = k_scale; p.v_scale = v_scale;
+    p.block_tables = block_tables;
+    n = rows_b ? (long long)nrows : (long long)B * Hq;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+    for (i = 0; i < n; i++) {
+        int b = rows_b ? rows_b[i] : (int)(i / Hq);
+        int h = rows_b ? rows_h[i] : (int)(i % Hq);
+        double lse;
+        attend_range(&p, &q[((size_t)b * Hq + h) * D], b, h, 0, seq_lens[b], sm_scale,
+                     &out[(size_t)i * D], &lse);
+    }
+}
+
+/*
+ * Split-KV partials of one (b, h): split i covers logical blocks
+ * [blk_begin[i], blk_begin[i+1]) of the sequence, clipped to its length.
+ * Each split is attended on its own (attend_range), giving o_i (normalised) and
+ * lse_i (natural log).  Empty splits give o_i = 0, lse_i = -inf.
+ */
+void oracle_split_partials(int Hq, int Hkv, int D, int bs, int max_blocks, int kv_fp8,
+                           const uint16_t *q, const void *k_pool, const void *v_pool,
+                           const float *k_scale, const float *v_scale,
+                           const int32_t *block_tables, const int32_t *seq_lens,
+                           double sm_scale, int b, int h, int nsplit,
+                           const int32_t *blk_begin, double *o_parts, double *lse)
+{
+    paged_kv p;
+    int i, L = seq_lens[b];
+    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_fp8 = kv_fp8;
+    p.k_pool = k_pool; p.v_pool = v_pool; p.k_scale = k_scale; p.v_scale = v_scale;
+    p.block_tables = block_tables;
+    for (i = 0; i < nsplit; i++) {
+        int t0 = blk_begin[i] * bs, t1 = blk_begin[i + 1] * bs;
+        if (t1 > L) t1 = L;
+        if (t0 > L) t0 = L;
+        attend_range(&p, &q[((size_t)b * Hq + h) * D], b, h, t0, t1, sm_scale,
+                     &o_parts[(size_t)i * D], &lse[i]);
+    }
+}
+
+/*
+ * Log-sum-exp merge of split partials of one head:
+ *   M = max_i lse_i,  w_i = exp(lse_i - M),  out = sum_i w_i o_i / sum_i w_i
+ * Splits with lse_i = -inf carry no weight; if all are -inf the output is 0.
+ */
+void oracle_merge_lse(int nsplit, int D, const double *o_parts, const double *lse, double *out)
+{
+    int i, d;
+    double M = -INFINITY, wsum = 0.0;
+    for (d = 0; d < D; d++)
+        out[d] = 0.0;
+    for (i = 0; i < nsplit; i++)
+        if (lse[i] > M)
+            M = lse[i];
+    if (M == -INFINITY)
+        return;
+    for (i = 0; i < nsplit; i++) {
+        double w;
+        if (lse[i] == -INFINITY)
+            continue;
+        w = exp(lse[i] - M);
+        wsum += w;
+        for (d = 0; d < D; d++)
+            out[d] += w * o_parts[(size_t)i * D + d];
+    }
+    for (d = 0; d < D; d++)
+        out[d] /= wsum;
+}

@@ -1,0 +1,409 @@
+"""Pins of the CPU oracle against facts fixed outside it (CPU only).
+
+Each test checks the oracle against something it does not compute itself:
+values printed in the pages' worked examples (tests/golden/*.json, each with
+its source), closed forms, invariants, an independent numpy/scipy restatement
+of textbook attention on contiguous K/V, and torch's float8_e4m3fn conversion.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import softmax
+
+import oracle
+from paged_kv_cache_28_gb300 import workload as wl
+
+
+def _golden(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- page examples
+
+def test_gqa_mapping_and_cached_scalars(golden_dir):
+    g = _golden(golden_dir, "gqa_mapping.json")
+    for name, lay in g["layouts"].items():
+        mapping = [oracle.kv_head(h, g["query_heads"], lay["kv_heads"])
+                   for h in range(g["query_heads"])]
+        assert mapping == lay["mapping"], name
+        assert oracle.cached_scalars(1, lay["kv_heads"], g["tokens"], g["head_size"]) == \
+            lay["cached_scalars"], name
+
+
+def test_kv_capacity_figures(golden_dir):
+    g = _golden(golden_dir, "kv_capacity.json")
+    per_tok16 = oracle.cached_scalars(g["layers"], g["kv_heads"], 1, g["head_dim"]) * \
+        g["bytes_per_value_16bit"]
+    per_tok8 = oracle.cached_scalars(g["layers"], g["kv_heads"], 1, g["head_dim"]) * \
+        g["bytes_per_value_8bit"]
+    assert per_tok16 == g["bytes_per_token_16bit"]
+    assert g["pool_bytes"] // per_tok16 == g["tokens_in_pool_16bit"]
+    assert g["pool_bytes"] // per_tok8 == g["tokens_in_pool_8bit"]
+    # one layer of the 70B-class shape: 4,096 bytes per token (the bench's unit)
+    assert oracle.cached_scalars(1, 8, 1, 128) * 2 == 4096
+
+
+def test_quantizer_4bit_example(golden_dir):
+    g = _golden(golden_dir, "quant4_absmax.json")
+    codes, restored, scale = oracle.quantize_absmax_int(g["values"], g["bits"])
+    assert codes.tolist() == g["codes"]
+    assert np.round(restored, 3).tolist() == g["restored_3dp"]
+    assert scale == pytest.approx(1.0 / 7.0, rel=0, abs=1e-15)
+
+
+def test_quantizer_ties_to_even_and_zero():
+    # x/scale = 2.5 and 3.5 with scale 1 (absmax 7): rint gives 2 and 4
+    codes, _, _ = oracle.quantize_absmax_int([2.5, 3.5, -2.5, 7.0], 4)
+    assert codes.tolist() == [2, 4, -2, 7]
+    codes, restored, scale = oracle.quantize_absmax_int([0.0, 0.0], 4)
+    assert codes.tolist() == [0, 0] and scale == 0.0 and restored.tolist() == [0.0, 0.0]
+
+
+def test_allocator_example(golden_dir):
+    g = _golden(golden_dir, "paging_allocation.json")
+    alloc = wl.BlockAllocator(g["initial_free"])
+    a = alloc.allocate(3)
+    b = alloc.allocate(2)
+    alloc.release(a)
+    free_after = list(alloc.free)
+    c = alloc.allocate(2)
+    assert (a, b, free_after, c) == (g["request_a"], g["request_b"],
+                                     g["free_after_a_finishes"], g["request_c"])
+
+
+# ---------------------------------------------------------------- E4M3 format
+
+def test_e4m3_decode_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_to_double(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.array_equal(mine[~np.isnan(mine)], ref[~np.isnan(ref)])
+    assert np.isnan(mine[0x7F]) and np.isnan(mine[0xFF])
+    assert mine[0x7E] == 448.0 and mine[0xFE] == -448.0
+    assert mine[0x01] == 2.0 ** -9 and mine[0x08] == 2.0 ** -6 and mine[0x38] == 1.0
+    finite = mine[:0x7F]
+    assert np.all(np.diff(finite) > 0)          # magnitudes increase with the code
+
+
+def _torch_e4m3_satfinite(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.clip(x, -448.0, 448.0).astype(np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("scale", [1.0, 1.0 / 448.0, 3.0 / 448.0, 0.0173, 7.25, 1e-3])
+def test_e4m3_encode_every_bf16(scale):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = wl.bf16_to_float(bits)
+    x = x[np.isfinite(x)]
+    with np.errstate(over="ignore"):
+        y = (x / np.float32(scale)).astype(np.float32)      # overflow -> inf saturates too
+    assert np.array_equal(oracle.e4m3_from_float(y), _torch_e4m3_satfinite(y))
+
+
+def test_e4m3_encode_ties_and_saturation():
+    x = np.array([2.0 ** -10, 1.5 * 2.0 ** -9, 1.0625, 1.1875, 448.0, 464.0, 1e30, -1e30,
+                  -1e-9, np.nan], dtype=np.float32)
+    got = oracle.e4m3_from_float(x).tolist()
+    assert got[:4] == [0x00, 0x02, 0x38, 0x3A]      # ties go to the even code
+    assert got[4:8] == [0x7E, 0x7E, 0x7E, 0xFE]     # saturation to +-448
+    assert got[8] == 0x80                           # sign kept on underflow
+    assert got[9] == 0x7F
+
+
+# ---------------------------------------------------------------- cache write
+
+def test_reshape_and_cache_bf16_canary():
+    rng = np.random.default_rng(5)
+    nblocks, bs, Hkv, D, T = 9, 16, 2, 64, 7
+    k_pool = np.full((nblocks, bs, Hkv, D), 0xBEEF, np.uint16)
+    v_pool = np.full((nblocks, bs, Hkv, D), 0xCAFE, np.uint16)
+    k_new = rng.integers(0, 65536, (T, Hkv, D)).astype(np.uint16)
+    v_new = rng.integers(0, 65536, (T, Hkv, D)).astype(np.uint16)
+    slots = np.array([0, 17, -1, 143, 5, -7, 100], np.int64)
+    ek, ev = k_pool.copy(), v_pool.copy()
+    for t, s in enumerate(slots):
+        if s >= 0:
+            ek[s // bs, s % bs] = k_new[t]
+            ev[s // bs, s % bs] = v_new[t]
+    oracle.reshape_and_cache_bf16(k_new, v_new, k_pool, v_pool, slots, bs)
+    assert np.array_equal(k_pool, ek) and np.array_equal(v_pool, ev)
+
+
+def _fp8_setup(D=8, bs=4, nblocks=3, Hkv=1):
+    k_pool = np.zeros((nblocks, bs, Hkv, D), np.uint8)
+    v_pool = np.zeros((nblocks, bs, Hkv, D), np.uint8)
+    k_scale = np.full((nblocks, Hkv), 123.0, np.float32)
+    v_scale = np.full((nblocks, Hkv), 123.0, np.float32)
+    return k_pool, v_pool, k_scale, v_scale
+
+
+def _write(vals, slot, pools):
+    kp, vp, ks, vs = pools
+    x = wl.bf16_bits(np.asarray(vals, np.float32)).reshape(1, 1, -1)
+    oracle.reshape_and_cache_fp8(x, x, kp, vp, ks, vs, np.array([slot], np.int64),
+                                 kp.shape[1])
+
+
+def test_fp8_write_first_token_sets_scale():
+    pools = _fp8_setup()
+    vals = [1.0, -0.5, 0.25, 3.0, -3.0, 0.0, 0.1, 2.0]
+    _write(vals, 4, pools)          # block 1, offset 0: a fresh scale
+    kp, vp, ks, vs = pools
+    scale = np.float32(3.0) / np.float32(448.0)
+    assert ks[1, 0] == scale and vs[1, 0] == scale and ks[0, 0] == 123.0
+    xf = wl.bf16_to_float(wl.bf16_bits(np.asarray(vals, np.float32)))
+    assert np.array_equal(kp[1, 0, 0], _torch_e4m3_satfinite(xf / scale))
+    assert kp[1, 0, 0, 3] == 0x7E and kp[1, 0, 0, 4] == 0xFE       # absmax -> +-448
+    assert np.array_equal(kp, vp)
+
+
+def test_fp8_write_smaller_keeps_scale_larger_requantises():
+    pools = _fp8_setup()
+    kp, vp, ks, vs = pools
+    _write([1.0, 0.5, -0.25, 0.0, 0, 0, 0, 0], 0, pools)
+    s0 = np.float32(1.0) / np.float32(448.0)
+    row0 = kp[0, 0, 0].copy()
+    _write([0.5, 0.125, 0, 0, 0, 0, 0, 0], 1, pools)        # smaller: scale unchanged
+    assert ks[0, 0] == s0 and np.array_equal(kp[0, 0, 0], row0)
+    assert kp[0, 1, 0, 0] == _torch_e4m3_satfinite(np.array([np.float32(0.5) / s0]))[0]
+    _write([2.0, 0, 0, 0, 0, 0, 0, 0], 2, pools)            # larger: rows 0, 1 re-encoded
+    s1 = np.float32(2.0) / np.float32(448.0)
+    assert ks[0, 0] == s1
+    restored0 = (torch.from_numpy(row0).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+                 * s0).astype(np.float32)
+    assert np.array_equal(kp[0, 0, 0], _torch_e4m3_satfinite(restored0 / s1))
+    # the value 1.0 now sits at code 224 (half the range), 2.0 at 448
+    assert kp[0, 0, 0, 0] == _torch_e4m3_satfinite(np.array([224.0], np.float32))[0]
+    assert kp[0, 2, 0, 0] == 0x7E
+    # scale equals absmax over everything written / 448
+    assert ks[0, 0] == np.float32(2.0) / np.float32(448.0)
+
+
+def test_fp8_write_offset0_resets_and_zero_scale():
+    pools = _fp8_setup()
+    kp, vp, ks, vs = pools
+    _write([4.0] * 8, 8, pools)
+    _write([0.0] * 8, 8, pools)                 # offset 0 again: fresh, zero scale
+    assert ks[2, 0] == 0.0 and np.all(kp[2, 0] == 0)
+    _write([1.0] * 8, 9, pools)                 # grows from 0: old codes stay 0
+    assert ks[2, 0] == np.float32(1.0) / np.float32(448.0)
+    assert np.all(kp[2, 0] == 0) and np.all(kp[2, 1] == 0x7E)
+    _write([5.0] * 8, -1, pools)                # padding slot writes nothing
+    assert ks[2, 0] == np.float32(1.0) / np.float32(448.0)
+
+
+def test_fp8_write_error_bound_random():
+    rng = np.random.default_rng(11)
+    pools = _fp8_setup(D=32, bs=16, nblocks=1)
+    kp, vp, ks, vs = pools
+    xs = []
+    for off in range(16):
+        v = rng.standard_normal(32).astype(np.float32) * np.float32(rng.uniform(0.1, 3))
+        xs.append(wl.bf16_to_float(wl.bf16_bits(v)))
+        _write(v, off, pools)
+    xs = np.array(xs)
+    assert ks[0, 0] == np.float32(np.abs(xs).max()) / np.float32(448.0)
+    restored = oracle.e4m3_to_double(kp[0, :, 0]) * float(ks[0, 0])
+    # each requantisation adds at most half an E4M3 step (relative 2^-4) plus the
+    # subnormal spacing; 16 writes bound the drift well below 6 steps
+    step = np.maximum(np.abs(xs) * 2.0 ** -3, 2.0 ** -9 * float(ks[0, 0]))
+    assert np.all(np.abs(restored - xs) <= 6 * step)
+
+
+# ---------------------------------------------------------------- decode attention
+
+def _contiguous_reference(batch):
+    """Independent restatement: gather each sequence's K/V into contiguous
+    arrays with numpy fancy indexing and apply scipy's softmax."""
+    B, Hq, Hkv, D, bs = batch.B, batch.Hq, batch.Hkv, batch.D, batch.block_size
+    G = Hq // Hkv
+    q = wl.bf16_to_float(batch.q).astype(np.float64)
+    if batch.kv_dtype == "fp8_e4m3":
+        lut = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(
+            torch.float64).numpy()
+        kf = lut[batch.k_pool] * batch.k_scale.astype(np.float64)[:, None, :, None]
+        vf = lut[batch.v_pool] * batch.v_scale.astype(np.float64)[:, None, :, None]
+    else:
+        kf = wl.bf16_to_float(batch.k_pool).astype(np.float64)
+        vf = wl.bf16_to_float(batch.v_pool).astype(np.float64)
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        L = int(batch.seq_lens[b])
+        if L == 0:
+            continue
+        t = np.arange(L)
+        blocks = batch.block_tables[b, t // bs]
+        K = kf[blocks, t % bs]          # [L, Hkv, D]
+        V = vf[blocks, t % bs]
+        for h in range(Hq):
+            s = batch.sm_scale * (K[:, h // G, :] @ q[b, h])
+            out[b, h] = softmax(s) @ V[:, h // G, :]
+    return out
+
+
+def _oracle(batch, **kw):
+    return oracle.paged_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                               batch.seq_lens, batch.sm_scale, Hkv=batch.Hkv,
+                               block_size=batch.block_size, k_scale=batch.k_scale,
+                               v_scale=batch.v_scale, **kw)
+
+
+def test_decode_tiny_config_vs_contiguous_numpy():
+    batch = wl.make("tiny")
+    assert np.allclose(_oracle(batch), _contiguous_reference(batch), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(8, 8, 64, 16), (8, 1, 64, 32), (16, 4, 128, 16),
+                                         (12, 3, 64, 32)])
+def test_decode_random_shapes_vs_contiguous_numpy(Hq, Hkv, D, bs):
+    batch = wl.build_batch("t", [0, 1, 15, 16, 17, 40, 97], Hq=Hq, Hkv=Hkv, D=D,
+                           block_size=bs, seed=Hq * 7 + bs)
+    assert np.allclose(_oracle(batch), _contiguous_reference(batch), rtol=1e-12, atol=1e-13)
+
+
+def test_decode_fp8_vs_contiguous_numpy():
+    batch = wl.build_batch("t", [3, 16, 33, 70], Hq=8, Hkv=2, D=64, block_size=16, seed=3,
+                           kv_dtype="fp8_e4m3")
+    assert np.allclose(_oracle(batch), _contiguous_reference(batch), rtol=1e-12, atol=1e-13)
+
+
+def test_decode_rows_subset_matches_full():
+    batch = wl.build_batch("t", [5, 30, 64], Hq=8, Hkv=2, D=64, block_size=16, seed=9)
+    full = _oracle(batch)
+    rows = np.array([[2, 7], [0, 0], [1, 3]])
+    part = _oracle(batch, rows=rows)
+    for i, (b, h) in enumerate(rows):
+        assert np.array_equal(part[i], full[b, h])
+
+
+def test_decode_length_one_returns_v_exactly():
+    batch = wl.build_batch("t", [1, 1], Hq=8, Hkv=2, D=64, block_size=16, seed=4)
+    out = _oracle(batch)
+    vf = wl.bf16_to_float(batch.v_pool).astype(np.float64)
+    for b in range(2):
+        blk = batch.block_tables[b, 0]
+        for h in range(8):
+            assert np.array_equal(out[b, h], vf[blk, 0, h // 4])
+
+
+def test_decode_zero_query_gives_mean_of_v():
+    batch = wl.build_batch("t", [37], Hq=4, Hkv=1, D=64, block_size=16, seed=6)
+    batch.q[:] = 0
+    out = _oracle(batch)
+    vf = wl.bf16_to_float(batch.v_pool).astype(np.float64)
+    t = np.arange(37)
+    V = vf[batch.block_tables[0, t // 16], t % 16, 0]
+    assert np.allclose(out[0], V.mean(axis=0)[None, :], rtol=1e-13, atol=1e-14)
+
+
+def test_decode_two_tokens_logistic_closed_form():
+    batch = wl.build_batch("t", [2], Hq=2, Hkv=1, D=64, block_size=16, seed=8)
+    out = _oracle(batch)
+    kf = wl.bf16_to_float(batch.k_pool).astype(np.float64)
+    vf = wl.bf16_to_float(batch.v_pool).astype(np.float64)
+    q = wl.bf16_to_float(batch.q).astype(np.float64)
+    blk = batch.block_tables[0, 0]
+    for h in range(2):
+        s0 = batch.sm_scale * kf[blk, 0, 0] @ q[0, h]
+        s1 = batch.sm_scale * kf[blk, 1, 0] @ q[0, h]
+        w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+        expect = w0 * vf[blk, 0, 0] + (1.0 - w0) * vf[blk, 1, 0]
+        assert np.allclose(out[0, h], expect, rtol=1e-13, atol=1e-14)
+
+
+def test_decode_needle():
+    batch = wl.build_batch("t", [50], Hq=1, Hkv=1, D=64, block_size=16, seed=12)
+    q = wl.bf16_to_float(batch.q[0, 0]).astype(np.float32)
+    blk, off = batch.block_tables[0, 23 // 16], 23 % 16
+    batch.k_pool[blk, off, 0] = wl.bf16_bits(q * np.float32(100.0 / np.linalg.norm(q)) * 8)
+    out = _oracle(batch)
+    v = wl.bf16_to_float(batch.v_pool[blk, off, 0]).astype(np.float64)
+    assert np.allclose(out[0, 0], v, atol=1e-6)
+
+
+def _permute_blocks(batch, perm):
+    """Relabel physical block i as perm[i] (moving its rows): the logical cache is unchanged."""
+    k = np.empty_like(batch.k_pool)
+    v = np.empty_like(batch.v_pool)
+    k[perm] = batch.k_pool
+    v[perm] = batch.v_pool
+    tables = batch.block_tables.copy()
+    used = tables >= 0
+    tables[used] = perm[tables[used]]
+    return k, v, tables
+
+
+def test_decode_block_permutation_invariance_bitwise():
+    batch = wl.build_batch("t", [3, 40, 77, 16], Hq=8, Hkv=2, D=64, block_size=16, seed=13)
+    ref = _oracle(batch)
+    perm = np.random.default_rng(1).permutation(batch.nblocks)
+    k, v, tables = _permute_blocks(batch, perm)
+    out = oracle.paged_decode(batch.q, k, v, tables, batch.seq_lens, batch.sm_scale,
+                              Hkv=batch.Hkv, block_size=batch.block_size)
+    assert np.array_equal(out, ref)
+
+
+def test_decode_shared_vs_duplicated_prefix_bitwise():
+    groups = ((40, [0, 1, 2]),)                # 2 full shared blocks + a copied 8-row tail
+    batch = wl.build_batch("t", [45, 90, 41], Hq=8, Hkv=2, D=64, block_size=16, seed=14,
+                           prefix_groups=groups, pool_factor=2.0)
+    assert batch.block_tables[0, 0] == batch.block_tables[1, 0] == batch.block_tables[2, 0]
+    ref = _oracle(batch)
+    # duplicate the shared blocks into free blocks for sequences 1 and 2
+    used = set(batch.block_tables[batch.block_tables >= 0].tolist())
+    free = [i for i in range(batch.nblocks) if i not in used]
+    tables = batch.block_tables.copy()
+    k, v = batch.k_pool.copy(), batch.v_pool.copy()
+    for b in (1, 2):
+        for j in range(2):
+            dst = free.pop()
+            k[dst], v[dst] = k[tables[b, j]], v[tables[b, j]]
+            tables[b, j] = dst
+    out = oracle.paged_decode(batch.q, k, v, tables, batch.seq_lens, batch.sm_scale,
+                              Hkv=batch.Hkv, block_size=batch.block_size)
+    assert np.array_equal(out, ref)
+
+
+def test_decode_gqa_group_shares_kv():
+    # identical queries within a group give identical outputs; across groups they differ
+    batch = wl.build_batch("t", [33], Hq=8, Hkv=2, D=64, block_size=16, seed=15)
+    batch.q[0, :] = batch.q[0, 0]
+    out = _oracle(batch)
+    for h in range(4):
+        assert np.array_equal(out[0, h], out[0, 0])
+        assert np.array_equal(out[0, 4 + h], out[0, 4])
+    assert not np.array_equal(out[0, 0], out[0, 4])
+
+
+# ---------------------------------------------------------------- split + merge
+
+def test_split_merge_identity_random():
+    batch = wl.build_batch("t", [1, 33, 200, 0], Hq=8, Hkv=2, D=64, block_size=16, seed=16)
+    full = _oracle(batch)
+    rng = np.random.default_rng(2)
+    for b in range(batch.B):
+        nb = (int(batch.seq_lens[b]) + 15) // 16
+        for h in (0, 5):
+            for S in (1, 2, 5):
+                cuts = np.sort(rng.integers(0, nb + 1, S - 1)) if S > 1 else np.array([], int)
+                beg = np.concatenate([[0], cuts, [nb]]).astype(np.int32)
+                o, lse = oracle.split_partials(batch.q, batch.k_pool, batch.v_pool,
+                                               batch.block_tables, batch.seq_lens,
+                                               batch.sm_scale, b, h, beg, Hkv=2, block_size=16)
+                merged = oracle.merge_lse(o, lse)
+                assert np.allclose(merged, full[b, h], rtol=1e-12, atol=1e-13)
+                if S == 1:
+                    assert np.array_equal(o[0], full[b, h])
+
+
+def test_merge_empty_splits_carry_no_weight():
+    o = np.array([[1.0, 2.0], [np.nan, np.nan], [3.0, 4.0]])
+    lse = np.array([0.0, -np.inf, math.log(3.0)])
+    assert np.allclose(oracle.merge_lse(o, lse), [(1 + 9) / 4, (2 + 12) / 4], rtol=1e-15)
+    assert np.array_equal(oracle.merge_lse(o[1:2], lse[1:2]), [0.0, 0.0])
