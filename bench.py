@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Decode-attention benchmark: one JSON line on rank 0.
+
+A step is one pass of the whole hot path over one decode batch of the
+70B-class layer workload (B=64, Hq=64, Hkv=8, D=128, bf16, 16-token blocks,
+lognormal lengths with median 2,400 / p95 ~18,000): the slot-mapped cache
+write of the step's new K/V, split-KV paged decode attention, and the
+log-sum-exp merge.  Inputs are resident in HBM when the timed region starts;
+the KV read per step (~1.3 GB) is far larger than L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+With N > 1 it runs under torch.distributed.run, one rank per GPU; each rank
+decodes its own batch (weak scaling, no collective on the data path) and the
+time is the max over ranks.  --impl reference times the CPU oracle (plain fp64
+C) on this host's cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic per decode launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum), with
+# the hash of the kernel sources it was measured on; reported only while they still match.
+TRAFFIC = {}
+
+
+# ----------------------------------------------------------------------------
+# distributed helpers (one process per GPU; no collective on the data path)
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank decodes its own batch drawn with its own seed (weak scaling)."""
+    return base_seed + 1009 * rank
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            lines = [ln for ln in out.splitlines() if ln.strip()]
+        if not lines:     # the timed region was shorter than one sample: take one now
+            try:
+                lines = subprocess.run(
+                    ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_QUERY}",
+                     "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                    timeout=10).stdout.splitlines()
+            except (OSError, subprocess.TimeoutExpired):
+                lines = []
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_28_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def cpu_baseline(batch, cores: int) -> dict:
+    """The oracle, as it stands, on this host's cores: cache write + decode of the
+    whole batch, once."""
+    import oracle
+    t0 = time.perf_counter()
+    kp, vp = batch.k_pool.copy(), batch.v_pool.copy()
+    if batch.kv_dtype == "fp8_e4m3":
+        ks, vs = batch.k_scale.copy(), batch.v_scale.copy()
+        oracle.reshape_and_cache_fp8(batch.k_new, batch.v_new, kp, vp, ks, vs,
+                                     batch.slot_mapping, batch.block_size)
+    else:
+        ks = vs = None
+        oracle.reshape_and_cache_bf16(batch.k_new, batch.v_new, kp, vp, batch.slot_mapping,
+                                      batch.block_size)
+    oracle.paged_decode(batch.q, kp, vp, batch.block_tables, batch.seq_lens, batch.sm_scale,
+                        Hkv=batch.Hkv, block_size=batch.block_size, k_scale=ks, v_scale=vs,
+                        nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": batch.B / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"one full step of the same batch (write + decode of all {batch.B} "
+                      f"sequences x {batch.Hq} heads), fp64 C with OpenMP, {dt:.2f} s wall"}
+
+
+def run_ours(args):
+    import torch
+
+    from paged_kv_cache_28_gb300 import _lib
+    from paged_kv_cache_28_gb300 import workload as wl
+    from paged_kv_cache_28_gb300.device import DeviceBatch, default_num_splits, to_device_bf16
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev_id = torch.device("cuda", local)
+    if not os.path.exists(_lib.LIB_PATH):
+        from paged_kv_cache_28_gb300 import build
+        build.build()
+    _lib.load()
+
+    seed = rank_seed(wl.DEFAULT_SEEDS[args.config], rank)
+    batch = wl.make(args.config, seed=seed)
+    dev = DeviceBatch(batch, device=dev_id)
+    ns = args.num_splits or default_num_splits(dev.shape, dev_id)
+    dev.ensure_workspace(ns)
+    stream = torch.cuda.current_stream(dev_id)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+
+    def step(i=None):
+        dev.reshape_and_cache(stream)
+        if i is not None:
+            ev[i][0].record(stream)
+        _lib.pa_decode_splitkv(dev.shape, dev.out, dev.workspace, ns, dev.q, dev.k_pool,
+                               dev.v_pool, dev.k_scale, dev.v_scale, dev.block_tables,
+                               dev.seq_lens, batch.sm_scale, dev.err, stream)
+        if i is not None:
+            ev[i][1].record(stream)
+        _lib.pa_merge_lse(dev.shape, dev.out, dev.workspace, ns, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dev.read_err():
+        raise RuntimeError("device error flag set during warm-up")
+
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier(world)
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = reduce_max(ms_total, world, dev_id)
+    ms_per_step = ms_total / args.steps
+    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    decode_ms = reduce_max(decode_ms, world, dev_id)
+
+    # ---- end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {name: getattr(dev, name).cpu().pin_memory()
+                for name in ("q", "k_new", "v_new", "slot_mapping", "seq_lens", "block_tables")}
+        out_host = torch.empty(dev.out.shape, dtype=dev.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for name, t in host.items():
+                getattr(dev, name).copy_(t, non_blocking=True)
+            step()
+            out_host.copy_(dev.out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        barrier(world)
+        t0 = time.perf_counter()
+        n_e2e = max(3, min(args.steps, 200))
+        for _ in range(n_e2e):
+            e2e_step()
+        e2e_s = reduce_max((time.perf_counter() - t0) / n_e2e, world, dev_id)
+        e2e = {"value": world * batch.B / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    if dev.read_err():
+        raise RuntimeError("device error flag set during the timed steps")
+
+    unique_tokens = batch.unique_kv_tokens()
+    kv_bytes = unique_tokens * batch.kv_bytes_per_token()
+    if batch.kv_dtype == "fp8_e4m3":
+        kv_bytes += sum(int(n) for n in (batch.seq_lens + batch.block_size - 1)
+                        // batch.block_size) * batch.scale_bytes_per_block()
+    peak, peak_kind = measured_peak_hbm()
+    achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
+    tr = TRAFFIC.get(args.config)
+    traffic = tr["bytes"] if tr and tr.get("kernel_hash") == kernel_source_hash() else None
+    result = {
+        "metric": METRIC,
+        "value": world * batch.B / (ms_per_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3" if batch.kv_dtype == "fp8_e4m3" else "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": args.config,
+            "B": batch.B, "Hq": batch.Hq, "Hkv": batch.Hkv, "D": batch.D,
+            "block_size": batch.block_size, "seq_len_sum": batch.logical_tokens,
+            "seq_len_max": int(batch.seq_lens.max()),
+            "unique_kv_tokens": unique_tokens, "num_splits": ns,
+            "l2": f"no flush: {kv_bytes / 1e9:.2f} GB of KV read per step >> 129 MB L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single",
+            "step": "pa_reshape_and_cache + pa_decode_splitkv + pa_merge_lse",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "kernel": "pa_decode_splitkv call (plan kernels + decode_segment_kernel)",
+            "kernel_ms": decode_ms,
+            "algorithmic_bytes": kv_bytes,
+            "peak_kind": peak_kind,
+        },
+        "gpu_launches": 5 * args.steps,
+        "clocks": clock_info,
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(batch, os.cpu_count() or 1)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the CPU oracle on this host's cores
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_cache_28_gb300 import workload as wl
+    oracle.build()
+    batch = wl.make(args.config)
+    cores = os.cpu_count() or 1
+    # each step decodes a bounded sample of (sequence, head) rows, sized so that the
+    # whole --steps/--warmup run takes about REF_BUDGET_S; the time is scaled to the
+    # whole batch by the KV tokens the sample reads
+    REF_BUDGET_S = 90.0
+    rng = np.random.default_rng(0)
+    all_rows = np.array([(b, h) for b in range(batch.B) for h in range(batch.Hq)], np.int32)
+    rng.shuffle(all_rows)
+    row_tokens = batch.seq_lens[all_rows[:, 0]].astype(np.int64)
+    total_token_heads = int(batch.seq_lens.astype(np.int64).sum()) * batch.Hq
+
+    def time_rows(rows):
+        t0 = time.perf_counter()
+        oracle.paged_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                            batch.seq_lens, batch.sm_scale, Hkv=batch.Hkv,
+                            block_size=batch.block_size, k_scale=batch.k_scale,
+                            v_scale=batch.v_scale, rows=rows, nthreads=cores)
+        return time.perf_counter() - t0
+
+    calib = all_rows[:4 * cores]
+    s_per_token_head = time_rows(calib) / max(1, int(row_tokens[:len(calib)].sum()))
+    per_step = REF_BUDGET_S / (args.steps + args.warmup)
+    want = per_step / max(s_per_token_head, 1e-12)
+    n = int(np.searchsorted(np.cumsum(row_tokens), want)) + 1
+    n = max(cores, min(n, len(all_rows)))
+    rows = np.ascontiguousarray(all_rows[:n])
+    sample_token_heads = int(row_tokens[:n].sum())
+    frac = sample_token_heads / total_token_heads
+    idx = np.unique(rows[:, 0])
+
+    def ref_step():
+        # the cache write touches only this step's B rows; the sample's decode reads them
+        time_rows(rows)
+
+    for _ in range(args.warmup):
+        ref_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ref_step()
+    dt = (time.perf_counter() - t0) / args.steps
+    full_step_s = dt / frac
+    value = batch.B / full_step_s
+    result = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": full_step_s * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.config, "B": batch.B, "Hq": batch.Hq, "Hkv": batch.Hkv,
+                   "D": batch.D, "block_size": batch.block_size,
+                   "seq_len_sum": batch.logical_tokens},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} random (sequence, head) rows of {batch.B * batch.Hq} "
+                                   f"({frac:.2%} of the KV token-heads) per step, decoded by "
+                                   f"the fp64 oracle; time scaled to the whole batch by "
+                                   f"KV token-heads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama70b_layer",
+                    choices=["tiny", "llama70b_layer", "prefix_sharing", "long_context",
+                             "fp8_mixed"])
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+/*
+ * pa.h -- C ABI of the paged-KV decode attention library (libpa.so, sm_103a).
+ *
+ * The library implements the data-parallel hot path of paged KV-cache LLM
+ * decoding: the slot-mapped write of each step's new K/V into a block pool,
+ * and single-token grouped-query attention over that pool through per-sequence
+ * block tables.
+ *
+ * Sources of the operations (web pages the method is described on):
+ *   [P1] "appendonly" (rajatmohan.com): "What is actually being cached"
+ *        (K and V per token, 8 KV heads x 128 dims), "Paging, because contiguous
+ *        allocation is a disaster" (fixed 16/32-token blocks, per-sequence block
+ *        table, lazy allocation), "Prefix sharing is where the real win lives"
+ *        (sequences point at the same physical blocks).
+ *   [P3] "KV Cache Engineering for LLM Serving" (dailydoseofds): section 1
+ *        (GQA: query head h reads KV head h / (Hq/Hkv)), section 8
+ *        (absmax-scaled low-bit cache, restored = code * scale; FP8 cache),
+ *        section 10 (PagedAttention block pool).
+ *   [P4] "Taming the Token Torrent" (architects-blueprint): "How Paging Works in
+ *        the LLM Context" (new tokens go to a block taken from a free pool),
+ *        "The Block Table Logic" (logical index -> physical block + offset),
+ *        "Custom PagedAttention Kernels" (grid over (sequence, head), walk the
+ *        block table, stage each block in shared memory, attend, move on),
+ *        "The Metadata Bottleneck" (block tables live on the GPU).
+ * Split-KV with a log-sum-exp merge is not on the pages; it is the standard
+ * flash-decoding extension, defined below by what it computes.
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions common to every entry point
+ * ---------------------------------------------------------------------------
+ *  - All array arguments are caller-owned DEVICE memory of the current CUDA
+ *    device, row-major, 16-byte aligned.  The library allocates nothing, frees
+ *    nothing and keeps no state between calls.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and is asynchronous: no call synchronises.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns PA_ERR_INVALID_ARG or PA_ERR_UNSUPPORTED and launches
+ *    nothing.  A failed launch returns PA_ERR_CUDA.
+ *  - Errors that depend on device data (a block id outside the pool, a
+ *    sequence longer than its block table, a slot outside the pool, two FP8
+ *    writes into one block) are reported through `err_flag`: a device int32
+ *    that the kernels OR a PA_DEVERR_* bit into.  The affected unit is skipped
+ *    (or reads zeros), nothing traps.  The flag is sticky; the caller zeroes it
+ *    and reads it after synchronising (see pa_read_error_flag).  err_flag may
+ *    be NULL only if the caller vouches that the data is valid.
+ *  - Shapes: B sequences (or tokens, for the cache write), Hq query heads,
+ *    Hkv KV heads (Hq % Hkv == 0, G = Hq / Hkv <= 16), head dim D in {64, 128},
+ *    block_size in {16, 32}.  FP8 pools need D = 128.
+ *  - Layouts:
+ *      q            [B, Hq, D]                  bf16
+ *      out          [B, Hq, D]                  fp32
+ *      k/v pool     [nblocks, block_size, Hkv, D] bf16, or E4M3 codes (uint8)
+ *      k/v scale    [nblocks, Hkv]              fp32 (FP8 pools only, else NULL)
+ *      block_tables [B, max_blocks]             int32 physical block ids
+ *      seq_lens     [B]                         int32 tokens in the cache,
+ *                                               including this step's token
+ *      slot_mapping [B]                         int64 slot = block * block_size
+ *                                               + offset; negative = skip
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pa_stream_t;   /* same type as cudaStream_t */
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or workspace */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but not built: D, block_size, G, dtype */
+    PA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed */
+    PA_ERR_DEVICE = 4         /* pa_read_error_flag found a PA_DEVERR_* bit */
+} pa_status;
+
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+
+/* Device error bits ORed into *err_flag. */
+#define PA_DEVERR_BLOCK_ID     1   /* block table entry outside [0, nblocks)        */
+#define PA_DEVERR_SEQ_LEN      2   /* seq_len < 0 or > max_blocks * block_size      */
+#define PA_DEVERR_SLOT         4   /* slot_mapping entry >= nblocks * block_size    */
+#define PA_DEVERR_FP8_CONFLICT 8   /* two tokens of one FP8 write hit one block     */
+#define PA_DEVERR_TIMEOUT      16  /* an internal pipeline wait gave up             */
+
+typedef struct {
+    int32_t B;            /* sequences (decode) or tokens to write (cache write) */
+    int32_t Hq;           /* query heads */
+    int32_t Hkv;          /* KV heads */
+    int32_t D;            /* head dimension */
+    int32_t block_size;   /* tokens per physical block */
+    int32_t nblocks;      /* physical blocks in each pool */
+    int32_t max_blocks;   /* columns of block_tables */
+    int32_t kv_dtype;     /* pa_kv_dtype */
+} pa_shape;
+
+/*
+ * pa_reshape_and_cache -- write this step's K/V into the block pools.
+ * [P4] "How Paging Works in the LLM Context" and "The Block Table Logic";
+ * [P1] "Paging".  For every token t < shape->B with s = slot_mapping[t] >= 0
+ * and every KV head h:
+ *     pool[s / block_size][s % block_size][h][:] = new[t][h][:]
+ * k_new, v_new: [B, Hkv, D] bf16.  shape->Hq is ignored.
+ *
+ * BF16 pools: a bit-exact copy.  Two tokens with the same slot race (one wins).
+ *
+ * FP8 pools (kv_dtype = PA_KV_FP8_E4M3, k_scale/v_scale required), after
+ * [P3] section 8, per (block, kv head) and separately for K and V:
+ *   - scale = absmax of every value written into the (block, head) since its
+ *     offset 0 was written, / 448 (fp32 IEEE division); writing offset 0
+ *     starts a new scale;
+ *   - code = E4M3(x / scale): fp32 IEEE division, round to nearest even,
+ *     saturating to +-448; a zero scale stores +0 codes;
+ *   - a write that raises the scale re-encodes the codes at offsets below it:
+ *     code' = E4M3((E4M3 value of code * old scale) / new scale), fp32 product
+ *     and division.
+ *   Two tokens of one call that land in the same block set
+ *   PA_DEVERR_FP8_CONFLICT and neither is written.
+ * A slot beyond the pool sets PA_DEVERR_SLOT and is skipped.
+ */
+pa_status pa_reshape_and_cache(const pa_shape *shape, const void *k_new, const void *v_new,
+                               void *k_pool, void *v_pool, float *k_scale, float *v_scale,
+                               const int64_t *slot_mapping, int32_t *err_flag,
+                               pa_stream_t stream);
+
+/*
+ * pa_decode -- single-token decode attention over the paged cache, one CTA per
+ * (sequence, KV head) serving the whole query group.
+ * [P4] "Custom PagedAttention Kernels" (grid over sequence and head, block-table
+ * walk, block staged in shared memory); [P3] section 1 (GQA grouping).
+ *     out[b][h][:] = sum_t softmax_t(sm_scale * <q[b][h], K_b[t]>) V_b[t]
+ * over t < seq_lens[b], where K_b[t] = k_pool[block_tables[b][t / bs]][t % bs]
+ * [h / G] (same for V) and FP8 codes are restored as value * scale[block][kvh].
+ * seq_lens[b] = 0 gives zeros.  out is fp32 [B, Hq, D].
+ */
+pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void *k_pool,
+                    const void *v_pool, const float *k_scale, const float *v_scale,
+                    const int32_t *block_tables, const int32_t *seq_lens, float sm_scale,
+                    int32_t *err_flag, pa_stream_t stream);
+
+/*
+ * Bytes of device workspace pa_decode_splitkv / pa_merge_lse need for this
+ * shape and num_splits; 0 if the arguments are invalid.  Host only.
+ */
+size_t pa_splitkv_workspace_bytes(const pa_shape *shape, int32_t num_splits);
+
+/*
+ * A good num_splits for this shape on a GPU with sm_count SMs: the number of
+ * split workers that are resident at once.  Host only, no CUDA call.
+ */
+int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count);
+
+/*
+ * pa_decode_splitkv -- the same attention as pa_decode, with the KV of each
+ * (sequence, KV head) split across SMs (flash-decoding).  Partition: the
+ * 16-token tiles of all (b, kvh) pairs, in (b, kvh, position) order, are cut
+ * into num_splits contiguous segments of ceil(total / num_splits) tiles; each
+ * segment is one split worker.  A pair that lies inside one segment is finished
+ * there and written to out.  A pair cut by segment boundaries leaves one
+ * partial per piece in the workspace:
+ *     o_i = sum_t e^(s_t - m_i) V_t / l_i,  lse_i = m_i + ln l_i  (natural log)
+ * and pa_merge_lse completes it.  out is complete only after pa_merge_lse on
+ * the same stream with the same shape, workspace and num_splits.
+ * workspace: device memory of at least pa_splitkv_workspace_bytes(shape,
+ * num_splits) bytes, 256-byte aligned, owned by the caller, not shared with
+ * concurrent calls.  1 <= num_splits <= 65536.
+ */
+pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
+                            size_t workspace_bytes, int32_t num_splits, const void *q,
+                            const void *k_pool, const void *v_pool, const float *k_scale,
+                            const float *v_scale, const int32_t *block_tables,
+                            const int32_t *seq_lens, float sm_scale, int32_t *err_flag,
+                            pa_stream_t stream);
+
+/*
+ * pa_merge_lse -- log-sum-exp merge of the split partials left by
+ * pa_decode_splitkv, per query head:
+ *     M = max_i lse_i,  w_i = e^(lse_i - M),  out = sum_i w_i o_i / sum_i w_i
+ * Pairs with seq_len 0 get zeros; pairs finished inside one segment are left
+ * untouched.
+ */
+pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,
+                       int32_t num_splits, pa_stream_t stream);
+
+/* Human-readable name of a status. */
+const char *pa_status_string(pa_status status);
+
+/*
+ * Synchronise `stream`, copy the device int32 *err_flag to *host_value and
+ * return PA_ERR_DEVICE if it is nonzero, PA_OK otherwise.
+ */
+pa_status pa_read_error_flag(const int32_t *err_flag, int32_t *host_value, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -280,21 +280,25 @@ typedef struct {
     const int32_t *block_tables;
 } paged_kv;
 
-/* Gather: element d of the key (or value) of logical token t of sequence b, KV
- * head kvh ([P4] "The Block Table Logic"; [P1] "Paging"):
- *   block = block_tables[b][t / bs], row = pool[block][t % bs][kvh][d]
- * FP8 pools are restored as code value * scale[block][kvh], exactly in double. */
-static double kv_elem(const paged_kv *p, int is_v, int b, int t, int kvh, int d)
+/* Gather: the key (or value) row of logical token t of sequence b, KV head kvh
+ * ([P4] "The Block Table Logic"; [P1] "Paging"):
+ *   block = block_tables[b][t / bs], row = pool[block][t % bs][kvh][:]
+ * written into dst[0..D) as doubles.  FP8 pools are restored as
+ * code value * scale[block][kvh], exactly in double. */
+static void kv_row(const paged_kv *p, int is_v, int b, int t, int kvh, double *dst)
 {
     int32_t blk = p->block_tables[(size_t)b * p->max_blocks + t / p->bs];
-    size_t idx = (((size_t)blk * p->bs + (size_t)(t % p->bs)) * p->Hkv + kvh) * p->D + d;
+    size_t idx = (((size_t)blk * p->bs + (size_t)(t % p->bs)) * p->Hkv + kvh) * p->D;
     const void *pool = is_v ? p->v_pool : p->k_pool;
-    if (!p->kv_fp8)
-        return oracle_bf16_to_double(((const uint16_t *)pool)[idx]);
-    {
+    int d;
+    if (!p->kv_fp8) {
+        for (d = 0; d < p->D; d++)
+            dst[d] = oracle_bf16_to_double(((const uint16_t *)pool)[idx + d]);
+    } else {
         const float *sc = is_v ? p->v_scale : p->k_scale;
-        return oracle_e4m3_to_double(((const uint8_t *)pool)[idx]) *
-               (double)sc[(size_t)blk * p->Hkv + kvh];
+        double scale = (double)sc[(size_t)blk * p->Hkv + kvh];
+        for (d = 0; d < p->D; d++)
+            dst[d] = oracle_e4m3_to_double(((const uint8_t *)pool)[idx + d]) * scale;
     }
 }
 
@@ -310,7 +314,7 @@ static void attend_range(const paged_kv *p, const uint16_t *q_row, int b, int h,
     int kvh = oracle_kv_head(h, p->Hq, p->Hkv);
     int n = t1 - t0, t, d;
     double mx = -INFINITY, sum = 0.0;
-    double *s;
+    double *s, *row, *q;
     for (d = 0; d < p->D; d++)
         o[d] = 0.0;
     if (n <= 0) {
@@ -318,10 +322,15 @@ static void attend_range(const paged_kv *p, const uint16_t *q_row, int b, int h,
         return;
     }
     s = (double *)malloc(sizeof(double) * (size_t)n);
+    row = (double *)malloc(sizeof(double) * (size_t)p->D);
+    q = (double *)malloc(sizeof(double) * (size_t)p->D);
+    for (d = 0; d < p->D; d++)
+        q[d] = oracle_bf16_to_double(q_row[d]);
     for (t = 0; t < n; t++) {
         double acc = 0.0;
+        kv_row(p, 0, b, t0 + t, kvh, row);
         for (d = 0; d < p->D; d++)
-            acc += oracle_bf16_to_double(q_row[d]) * kv_elem(p, 0, b, t0 + t, kvh, d);
+            acc += q[d] * row[d];
         s[t] = sm_scale * acc;
         if (s[t] > mx)
             mx = s[t];
@@ -330,13 +339,17 @@ static void attend_range(const paged_kv *p, const uint16_t *q_row, int b, int h,
         s[t] = exp(s[t] - mx);
         sum += s[t];
     }
-    for (t = 0; t < n; t++)
+    for (t = 0; t < n; t++) {
+        kv_row(p, 1, b, t0 + t, kvh, row);
         for (d = 0; d < p->D; d++)
-            o[d] += s[t] * kv_elem(p, 1, b, t0 + t, kvh, d);
+            o[d] += s[t] * row[d];
+    }
     for (d = 0; d < p->D; d++)
         o[d] /= sum;
     *lse = mx + log(sum);
     free(s);
+    free(row);
+    free(q);
 }
 
 /*

@@ -1,0 +1,162 @@
+"""ctypes binding of libpa.so (include/pa.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and passes torch
+tensors through as raw device pointers; all computation happens in the CUDA
+kernels.  Loading fails loudly when libpa.so is missing or no CUDA device is
+present: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpa.so")
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE = range(5)
+PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+PA_DEVERR_BLOCK_ID, PA_DEVERR_SEQ_LEN, PA_DEVERR_SLOT = 1, 2, 4
+PA_DEVERR_FP8_CONFLICT, PA_DEVERR_TIMEOUT = 8, 16
+
+EXPORTED = ("pa_reshape_and_cache", "pa_decode", "pa_splitkv_workspace_bytes",
+            "pa_default_num_splits", "pa_decode_splitkv", "pa_merge_lse", "pa_status_string",
+            "pa_read_error_flag")
+
+
+class pa_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("nblocks", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32)]
+
+
+class PAError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{fn} -> {status_string(status)}{(': ' + detail) if detail else ''}")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpa.so (no CUDA call is made by loading)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it with "
+                              "`python -m paged_kv_cache_28_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(path)
+        P, I32, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+        S = ctypes.POINTER(pa_shape)
+        sig = {
+            "pa_reshape_and_cache": (I32, [S, P, P, P, P, P, P, P, P, P]),
+            "pa_decode": (I32, [S, P, P, P, P, P, P, P, P, F, P, P]),
+            "pa_splitkv_workspace_bytes": (ctypes.c_size_t, [S, I32]),
+            "pa_default_num_splits": (I32, [S, I32]),
+            "pa_decode_splitkv": (I32, [S, P, P, ctypes.c_size_t, I32, P, P, P, P, P, P, P, F,
+                                        P, P]),
+            "pa_merge_lse": (I32, [S, P, P, I32, P]),
+            "pa_status_string": (ctypes.c_char_p, [I32]),
+            "pa_read_error_flag": (I32, [P, ctypes.POINTER(I32), P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().pa_status_string(status).decode()
+
+
+# ----------------------------------------------------------------------------
+# marshalling helpers
+# ----------------------------------------------------------------------------
+
+def _ptr(t):
+    """Device pointer of a CUDA tensor (None -> NULL).  Plain ints pass through."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("libpa takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libpa takes contiguous tensors only")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def make_shape(B, Hq, Hkv, D, block_size, nblocks, max_blocks, kv_dtype=PA_KV_BF16) -> pa_shape:
+    return pa_shape(int(B), int(Hq), int(Hkv), int(D), int(block_size), int(nblocks),
+                    int(max_blocks), int(kv_dtype))
+
+
+def _check(name: str, status: int):
+    if status != PA_OK:
+        raise PAError(name, status)
+
+
+# ----------------------------------------------------------------------------
+# entry points
+# ----------------------------------------------------------------------------
+
+def pa_reshape_and_cache(shape: pa_shape, k_new, v_new, k_pool, v_pool, k_scale, v_scale,
+                         slot_mapping, err_flag=None, stream=None) -> None:
+    lib = load()
+    _check("pa_reshape_and_cache", lib.pa_reshape_and_cache(
+        ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+        _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), _ptr(err_flag), _stream(stream)))
+
+
+def pa_decode(shape: pa_shape, out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
+              seq_lens, sm_scale: float, err_flag=None, stream=None) -> None:
+    lib = load()
+    _check("pa_decode", lib.pa_decode(
+        ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), float(sm_scale), _ptr(err_flag),
+        _stream(stream)))
+
+
+def pa_splitkv_workspace_bytes(shape: pa_shape, num_splits: int) -> int:
+    return int(load().pa_splitkv_workspace_bytes(ctypes.byref(shape), int(num_splits)))
+
+
+def pa_default_num_splits(shape: pa_shape, sm_count: int) -> int:
+    return int(load().pa_default_num_splits(ctypes.byref(shape), int(sm_count)))
+
+
+def pa_decode_splitkv(shape: pa_shape, out, workspace, num_splits: int, q, k_pool, v_pool,
+                      k_scale, v_scale, block_tables, seq_lens, sm_scale: float, err_flag=None,
+                      stream=None) -> None:
+    lib = load()
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("pa_decode_splitkv", lib.pa_decode_splitkv(
+        ctypes.byref(shape), _ptr(out), _ptr(workspace), nbytes, int(num_splits), _ptr(q),
+        _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+        _ptr(seq_lens), float(sm_scale), _ptr(err_flag), _stream(stream)))
+
+
+def pa_merge_lse(shape: pa_shape, out, workspace, num_splits: int, stream=None) -> None:
+    lib = load()
+    _check("pa_merge_lse", lib.pa_merge_lse(ctypes.byref(shape), _ptr(out), _ptr(workspace),
+                                            int(num_splits), _stream(stream)))
+
+
+def pa_read_error_flag(err_flag, stream=None) -> int:
+    """Synchronise the stream and return the device error bits (0 = none)."""
+    lib = load()
+    v = ctypes.c_int32(0)
+    st = lib.pa_read_error_flag(_ptr(err_flag), ctypes.byref(v), _stream(stream))
+    if st not in (PA_OK, PA_ERR_DEVICE):
+        raise PAError("pa_read_error_flag", st)
+    return int(v.value)

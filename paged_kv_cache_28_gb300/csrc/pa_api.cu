@@ -1,0 +1,157 @@
+// pa_api.cu -- the extern "C" entry points declared in include/pa.h: host-side
+// argument checks, then the launches in pa_cache.cu / pa_decode.cu.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <initializer_list>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks common to every call.  need_q: Hq matters (decode).
+pa_status check_shape(const pa_shape *s, bool need_q) {
+  if (!s) return PA_ERR_INVALID_ARG;
+  if (s->B < 0 || s->Hkv <= 0 || s->D <= 0 || s->block_size <= 0 || s->nblocks <= 0 ||
+      s->max_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (s->kv_dtype != PA_KV_BF16 && s->kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  if (need_q) {
+    if (s->Hq <= 0 || s->Hq % s->Hkv != 0) return PA_ERR_INVALID_ARG;
+    if (s->Hq / s->Hkv > 16) return PA_ERR_UNSUPPORTED;
+  }
+  if (s->D != 64 && s->D != 128) return PA_ERR_UNSUPPORTED;
+  if (s->block_size != 16 && s->block_size != 32) return PA_ERR_UNSUPPORTED;
+  if (s->kv_dtype == PA_KV_FP8_E4M3 && s->D != 128) return PA_ERR_UNSUPPORTED;
+  // every row index and tile count below must fit in int32
+  if (static_cast<int64_t>(s->nblocks) * s->block_size >= (int64_t(1) << 31))
+    return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(s->B) * s->max_blocks >= (int64_t(1) << 31)) return PA_ERR_INVALID_ARG;
+  const int64_t max_tiles = (static_cast<int64_t>(s->max_blocks) * s->block_size + 15) / 16;
+  if (static_cast<int64_t>(s->B) * s->Hkv * max_tiles >= (int64_t(1) << 31))
+    return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+pa_status check_ptrs(std::initializer_list<const void *> ptrs) {
+  for (const void *p : ptrs)
+    if (!p || !aligned16(p)) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+pa_status check_decode_args(const pa_shape *shape, const float *out, const void *q,
+                            const void *k_pool, const void *v_pool, const float *k_scale,
+                            const float *v_scale, const int32_t *bt, const int32_t *sl) {
+  pa_status st = check_shape(shape, true);
+  if (st != PA_OK) return st;
+  st = check_ptrs({out, q, k_pool, v_pool, bt, sl});
+  if (st != PA_OK) return st;
+  if (shape->kv_dtype == PA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+constexpr int kMaxSplits = 65536;
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_reshape_and_cache(const pa_shape *shape, const void *k_new, const void *v_new,
+                               void *k_pool, void *v_pool, float *k_scale, float *v_scale,
+                               const int64_t *slot_mapping, int32_t *err_flag,
+                               pa_stream_t stream) {
+  pa_status st = check_shape(shape, false);
+  if (st != PA_OK) return st;
+  if (shape->B == 0) return PA_OK;
+  st = check_ptrs({k_new, v_new, k_pool, v_pool, slot_mapping});
+  if (st != PA_OK) return st;
+  if (shape->kv_dtype == PA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  return pa::run_reshape_and_cache(*shape, k_new, v_new, k_pool, v_pool, k_scale, v_scale,
+                                   slot_mapping, err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void *k_pool,
+                    const void *v_pool, const float *k_scale, const float *v_scale,
+                    const int32_t *block_tables, const int32_t *seq_lens, float sm_scale,
+                    int32_t *err_flag, pa_stream_t stream) {
+  if (!shape) return PA_ERR_INVALID_ARG;
+  if (shape->B == 0) return check_shape(shape, true);
+  pa_status st = check_decode_args(shape, out, q, k_pool, v_pool, k_scale, v_scale,
+                                   block_tables, seq_lens);
+  if (st != PA_OK) return st;
+  return pa::run_decode(*shape, out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
+                        sm_scale, err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t pa_splitkv_workspace_bytes(const pa_shape *shape, int32_t num_splits) {
+  if (check_shape(shape, true) != PA_OK || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return pa::splitkv_layout(*shape, num_splits).total;
+}
+
+int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count) {
+  if (check_shape(shape, true) != PA_OK || sm_count <= 0) return 1;
+  // resident split workers: CTAs per SM by shared memory (228 KB per SM, 1 KB
+  // reserved per CTA), capped by the 2048-thread limit, times warps per CTA
+  const int per_cta = pa::decode_smem_bytes(*shape) + 1024;
+  const int warps = pa::decode_warps_per_cta();
+  int ctas = (228 * 1024) / per_cta;
+  if (ctas > 2048 / (32 * warps)) ctas = 2048 / (32 * warps);
+  if (ctas < 1) ctas = 1;
+  const int64_t n = static_cast<int64_t>(sm_count) * ctas * warps;
+  return static_cast<int32_t>(n > kMaxSplits ? kMaxSplits : n);
+}
+
+pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
+                            size_t workspace_bytes, int32_t num_splits, const void *q,
+                            const void *k_pool, const void *v_pool, const float *k_scale,
+                            const float *v_scale, const int32_t *block_tables,
+                            const int32_t *seq_lens, float sm_scale, int32_t *err_flag,
+                            pa_stream_t stream) {
+  if (!shape) return PA_ERR_INVALID_ARG;
+  if (shape->B == 0) return check_shape(shape, true);
+  pa_status st = check_decode_args(shape, out, q, k_pool, v_pool, k_scale, v_scale,
+                                   block_tables, seq_lens);
+  if (st != PA_OK) return st;
+  if (num_splits < 1 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < pa::splitkv_layout(*shape, num_splits).total) return PA_ERR_INVALID_ARG;
+  return pa::run_decode_splitkv(*shape, out, workspace, num_splits, q, k_pool, v_pool, k_scale,
+                                v_scale, block_tables, seq_lens, sm_scale, err_flag,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,
+                       int32_t num_splits, pa_stream_t stream) {
+  pa_status st = check_shape(shape, true);
+  if (st != PA_OK) return st;
+  if (shape->B == 0) return PA_OK;
+  if (!out || !aligned16(out) || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARG;
+  return pa::run_merge(*shape, out, workspace, num_splits, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_DEVICE: return "PA_ERR_DEVICE";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+pa_status pa_read_error_flag(const int32_t *err_flag, int32_t *host_value, pa_stream_t stream) {
+  if (!err_flag || !host_value) return PA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemcpy(host_value, err_flag, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return *host_value ? PA_ERR_DEVICE : PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,987 @@
+// pa_decode.cu -- paged decode attention for sm_103a.
+//
+// What is computed ("Taming the Token Torrent", section "Custom PagedAttention
+// Kernels"; "KV Cache Engineering for LLM Serving", section 1): for every
+// sequence b and query head h,
+//     out[b][h] = softmax_t(sm_scale * <q[b][h], K_b[t]>) V_b[t],  t < seq_lens[b],
+// where K_b / V_b are gathered through the block table and query head h reads KV
+// head h / G.
+//
+// How (GB300 design):
+//  * The unit of work is a 16-token tile of one (sequence, KV head) pair.  A
+//    warp streams its tiles through a private ring of shared-memory stages.
+//    Each stage is filled by TMA (two or one 128-byte-swizzled boxes for K, the
+//    same for V) plus, when a new pair starts, a bulk copy of the pair's G query
+//    rows; completion is tracked by one mbarrier per stage.
+//  * The whole query group of a KV head is served at once with warp-level
+//    tensor-core mma (m16n8k16): S^T = K Q^T (tokens x heads, the group is the
+//    n = 8 side), online softmax in fp32 registers with warp shuffles, then
+//    O^T += V^T P^T with P split into a high and a low 16-bit part so that the
+//    weights keep ~16 significant bits.
+//  * FP8 (E4M3) pools are converted to f16 in registers (exact); the per-block
+//    K scale folds into the score scale and the V scale into the running
+//    rescale factor, so dequantisation costs no per-element multiply.
+//  * pa_decode: one CTA per (sequence, KV head); its warps take interleaved
+//    tiles and merge their softmax states in shared memory at the end.
+//  * pa_decode_splitkv: the tiles of all pairs, laid end to end, are cut into
+//    equal segments, one per warp (flash-decoding with exact load balance).
+//    Pairs inside a segment are finished in place; cut pairs leave (o, lse)
+//    partials that pa_merge_lse combines.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// ----------------------------------------------------------------------------
+// configuration
+// ----------------------------------------------------------------------------
+
+template <int D_, int NT_, bool FP8_>
+struct Cfg {
+  static constexpr int D = D_;
+  static constexpr int NT = NT_;            // 8-head n-tiles (G <= 8 * NT)
+  static constexpr bool FP8 = FP8_;
+  static constexpr int KS = D / 16;         // QK k-steps of 16 elements
+  static constexpr int DT = D / 16;         // PV 16-row output tiles
+  static constexpr int EB = FP8 ? 1 : 2;    // bytes per cached element
+  static constexpr int ROW = D * EB;        // bytes of one token's head vector
+  static constexpr int HALVES = ROW / 128;  // 128-byte swizzle spans per row
+  static constexpr int BOX_X = 128 / EB;    // TMA box width in elements
+  static constexpr int KV_BYTES = kTile * ROW;
+  static constexpr int Q_BYTES = 8 * NT * D * 2;
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
+  static constexpr int STAGES = 2;
+  static constexpr int WARPS = 4;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int META_BYTES = 32;     // int4 unit + k/v scale
+  static constexpr int SMEM = 1024 + WARPS * STAGES * (STAGE_BYTES + 8 + META_BYTES);
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(KV_BYTES % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
+};
+
+struct Params {
+  float *out;
+  const uint16_t *q;
+  const float *k_scale;
+  const float *v_scale;
+  const int32_t *block_tables;
+  const int32_t *seq_lens;
+  int32_t *err;
+  int B, Hq, Hkv, G, bs, nblocks, max_blocks;
+  float sl2;  // sm_scale * log2(e)
+  // split-KV
+  const int4 *units;
+  const int32_t *prefix;
+  float *o_part;
+  float *lse_part;
+  int num_splits;
+};
+
+// ----------------------------------------------------------------------------
+// per-warp softmax state
+// ----------------------------------------------------------------------------
+
+template <class C>
+struct State {
+  float acc[C::NT][C::DT][4];   // O^T fragments (d x heads)
+  float m[C::NT][2];            // running max, log2 domain, heads 2q, 2q+1 of each n-tile
+  float l[C::NT][2];            // this thread's share of the running sum
+  uint32_t qf[C::NT][C::KS][2]; // Q^T B-fragments
+  float qshift;                 // FP8: 2^-k undoing the power-of-two scaling of q
+  float vs;                     // FP8: V scale the accumulator is expressed in
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt) {
+#pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][dt][i] = 0.f;
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
+    }
+    qshift = 1.f;
+    vs = 1.f;
+  }
+};
+
+// Output row (d) of accumulator element i of d-tile dt for this lane.
+template <class C>
+__device__ __forceinline__ int acc_d(int dt, int i, int lane) {
+  if constexpr (C::FP8)
+    return dt * 16 + 2 * (lane >> 2) + (i >> 1);
+  else
+    return dt * 16 + (lane >> 2) + (i >> 1) * 8;
+}
+
+// Load the group's Q^T fragments from the stage's Q slot ([8*NT rows][D] bf16).
+template <class C>
+__device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint16_t *qslot_ptr,
+                                       int lane) {
+  if constexpr (!C::FP8) {
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int ks = 0; ks < C::KS; ks += 2) {
+        uint32_t r[4];
+        const int g = nt * 8 + (lane & 7);
+        const int chunk = ks * 2 + (lane >> 3);
+        ldsm_x4(r, qslot + g * (C::D * 2) + chunk * 16);
+        st.qf[nt][ks][0] = r[0];
+        st.qf[nt][ks][1] = r[1];
+        st.qf[nt][ks + 1][0] = r[2];
+        st.qf[nt][ks + 1][1] = r[3];
+      }
+  } else {
+    // K codes arrive in a permuted order (see process_tile): k-step ks, lane (r, q)
+    // pairs Q[g=r][16ks + 4q + {0,1}] and Q[g=r][16ks + 4q + {2,3}].  q is scaled by
+    // 2^k so that its largest magnitude sits just below 2^15 (exact in f16).
+    const int r = lane >> 2, qd = lane & 3;
+    uint2 raw[C::NT][C::KS];
+    float amax = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int ks = 0; ks < C::KS; ++ks) {
+        raw[nt][ks] = *reinterpret_cast<const uint2 *>(qslot_ptr + (nt * 8 + r) * C::D +
+                                                       ks * 16 + qd * 4);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(raw[nt][ks].x)), fabsf(bf16_hi(raw[nt][ks].x))),
+                                 fmaxf(fabsf(bf16_lo(raw[nt][ks].y)), fabsf(bf16_hi(raw[nt][ks].y)))));
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int k = 0;
+    if (amax > 0.f) {
+      const int e = ((__float_as_uint(amax) >> 23) & 0xFF) - 126;   // amax < 2^e
+      k = min(max(15 - e, -100), 100);
+    }
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+    st.qshift = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int ks = 0; ks < C::KS; ++ks) {
+        const uint2 v = raw[nt][ks];
+        st.qf[nt][ks][0] = pack_f16(bf16_lo(v.x) * up, bf16_hi(v.x) * up);
+        st.qf[nt][ks][1] = pack_f16(bf16_lo(v.y) * up, bf16_hi(v.y) * up);
+      }
+  }
+}
+
+// One 16-token tile: scores, online-softmax update, P V accumulation.
+// sscale: factor from raw mma scores to log2-domain scores; vs: FP8 V scale.
+template <class C>
+__device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint32_t vtile,
+                                             int nvalid, float sscale, float vs, int lane) {
+  const int r = lane >> 2, qd = lane & 3;
+  float s[C::NT][4];
+#pragma unroll
+  for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
+
+  // ---- S^T = K Q^T
+  if constexpr (!C::FP8) {
+    const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ++ks) {
+      const int c = ((ks & 3) << 1) + (lane >> 4);
+      uint32_t a[4];
+      ldsm_x4(a, ktile + (ks >> 2) * (kTile * 128) + row * 128 + ((c ^ (row & 7)) << 4));
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt) mma_bf16(s[nt], a, st.qf[nt][ks][0], st.qf[nt][ks][1]);
+    }
+  } else {
+    // ldmatrix on byte pairs: lane (r, q) receives codes 4q..4q+3 of a 16-code chunk;
+    // the mma's k order is permuted accordingly (load_q applies the same order to q).
+    const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+    for (int kk = 0; kk < C::D / 32; ++kk) {
+      const int c = 2 * kk + (lane >> 4);
+      uint32_t R[4];
+      ldsm_x4(R, ktile + row * 128 + ((c ^ (row & 7)) << 4));
+      const uint32_t a0[4] = {e4m3x2_to_f16x2(R[0]), e4m3x2_to_f16x2(R[1]),
+                              e4m3x2_to_f16x2(R[0] >> 16), e4m3x2_to_f16x2(R[1] >> 16)};
+      const uint32_t a1[4] = {e4m3x2_to_f16x2(R[2]), e4m3x2_to_f16x2(R[3]),
+                              e4m3x2_to_f16x2(R[2] >> 16), e4m3x2_to_f16x2(R[3] >> 16)};
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt) {
+        mma_f16(s[nt], a0, st.qf[nt][2 * kk][0], st.qf[nt][2 * kk][1]);
+        mma_f16(s[nt], a1, st.qf[nt][2 * kk + 1][0], st.qf[nt][2 * kk + 1][1]);
+      }
+    }
+  }
+
+  // ---- online softmax (log2 domain); element i: token r + 8*(i>>1), head 2q + (i&1)
+  float p[C::NT][4];
+  float corr[C::NT][2];
+#pragma unroll
+  for (int nt = 0; nt < C::NT; ++nt) {
+    float x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = r + ((i >> 1) << 3);
+      x[i] = (t < nvalid) ? s[nt][i] * sscale : -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float mx = fmaxf(x[j], x[j + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mnew = fmaxf(st.m[nt][j], mx);
+      const float alpha = ex2(st.m[nt][j] - mnew);
+      st.m[nt][j] = mnew;
+      p[nt][j] = ex2(x[j] - mnew);
+      p[nt][j + 2] = ex2(x[j + 2] - mnew);
+      st.l[nt][j] = st.l[nt][j] * alpha + (p[nt][j] + p[nt][j + 2]);
+      corr[nt][j] = C::FP8 ? alpha * (st.vs / vs) : alpha;
+    }
+#pragma unroll
+    for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) st.acc[nt][dt][i] *= corr[nt][i & 1];
+  }
+  if constexpr (C::FP8) st.vs = vs;
+
+  // ---- P^T fragments: hi + lo 16-bit parts, transposed in registers
+  uint32_t bh[C::NT][2], bl[C::NT][2];
+#pragma unroll
+  for (int nt = 0; nt < C::NT; ++nt) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float p0 = p[nt][2 * h], p1 = p[nt][2 * h + 1];
+      uint32_t hi, lo;
+      if constexpr (!C::FP8) {
+        hi = pack_bf16(p0, p1);
+        lo = pack_bf16(p0 - bf16_lo(hi), p1 - bf16_hi(hi));
+      } else {
+        hi = pack_f16(p0, p1);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+        lo = pack_f16(p0 - hf.x, p1 - hf.y);
+      }
+      bh[nt][h] = movmatrix_trans(hi);
+      bl[nt][h] = movmatrix_trans(lo);
+    }
+  }
+
+  // ---- O^T += V^T P^T; rows of V beyond nvalid are zeroed in registers (the pool
+  // may hold stale or non-finite values there)
+  uint32_t m01 = 0xFFFFFFFFu, m23 = 0xFFFFFFFFu;
+  if (nvalid < kTile) {
+    m01 = (2 * qd < nvalid ? 0x0000FFFFu : 0u) | (2 * qd + 1 < nvalid ? 0xFFFF0000u : 0u);
+    m23 = (2 * qd + 8 < nvalid ? 0x0000FFFFu : 0u) | (2 * qd + 9 < nvalid ? 0xFFFF0000u : 0u);
+  }
+  if constexpr (!C::FP8) {
+    const int t = (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+    for (int dt = 0; dt < C::DT; ++dt) {
+      const int c = ((dt & 3) << 1) + ((lane >> 3) & 1);
+      uint32_t a[4];
+      ldsm_x4_trans(a, vtile + (dt >> 2) * (kTile * 128) + t * 128 + ((c ^ (t & 7)) << 4));
+      a[0] &= m01;
+      a[1] &= m01;
+      a[2] &= m23;
+      a[3] &= m23;
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt) {
+        mma_bf16(st.acc[nt][dt], a, bh[nt][0], bh[nt][1]);
+        mma_bf16(st.acc[nt][dt], a, bl[nt][0], bl[nt][1]);
+      }
+    }
+  } else {
+    // ldmatrix.trans on byte pairs gives lane (r, q): bytes (t=2q: d=2r, 2r+1) and
+    // (t=2q+1: d=2r, 2r+1); regrouping by d yields V^T rows d = 2r (even) and 2r+1
+    // (odd) -- the tile's 16 output rows in the order (2r, 2r+1).
+    const int t = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+    for (int cc = 0; cc < C::D / 32; ++cc) {
+      const int c = 2 * cc + (lane >> 4);
+      uint32_t R[4];
+      ldsm_x4_trans(R, vtile + t * 128 + ((c ^ (t & 7)) << 4));
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t lo8 = R[2 * hh], hi8 = R[2 * hh + 1];
+        uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(lo8, 0, 0x4420)),
+                         e4m3x2_to_f16x2(__byte_perm(lo8, 0, 0x4431)),
+                         e4m3x2_to_f16x2(__byte_perm(hi8, 0, 0x4420)),
+                         e4m3x2_to_f16x2(__byte_perm(hi8, 0, 0x4431))};
+        a[0] &= m01;
+        a[1] &= m01;
+        a[2] &= m23;
+        a[3] &= m23;
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+          mma_f16(st.acc[nt][2 * cc + hh], a, bh[nt][0], bh[nt][1]);
+          mma_f16(st.acc[nt][2 * cc + hh], a, bl[nt][0], bl[nt][1]);
+        }
+      }
+    }
+  }
+}
+
+// Sum l over the 8 lanes that share a head pair; returns the per-head total.
+template <class C>
+__device__ __forceinline__ void reduce_l(const State<C> &st, float (&ltot)[C::NT][2]) {
+#pragma unroll
+  for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float v = st.l[nt][j];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      ltot[nt][j] = v;
+    }
+}
+
+// Write o = acc / l (normalised) for heads < G to dst[g * D + d]; and lse if requested.
+template <class C>
+__device__ __forceinline__ void write_normalised(const State<C> &st, float *dst, float *lse_dst,
+                                                 int G, int lane) {
+  float ltot[C::NT][2];
+  reduce_l<C>(st, ltot);
+  const int qd = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int g = nt * 8 + 2 * qd + j;
+      if (g >= G) continue;
+      const float f = (C::FP8 ? st.vs : 1.f) / ltot[nt][j];
+#pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt) {
+        dst[g * C::D + acc_d<C>(dt, j, lane)] = st.acc[nt][dt][j] * f;
+        dst[g * C::D + acc_d<C>(dt, j + 2, lane)] = st.acc[nt][dt][j + 2] * f;
+      }
+      if (lse_dst && (lane >> 2) == 0) lse_dst[g] = (st.m[nt][j] + __log2f(ltot[nt][j])) * kLn2;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// unit sources: which tiles a warp processes, in order
+// ----------------------------------------------------------------------------
+
+// Tiles w, w + NW, ... of one (b, kvh) pair, read straight from the block table.
+struct PairSource {
+  const int32_t *row;
+  int32_t *err;
+  int pair, L, ntiles, w, nw, bs, nblocks;
+  int base;
+  int4 cur, nxt;
+
+  __device__ __forceinline__ int count() const {
+    return ntiles > w ? (ntiles - w + nw - 1) / nw : 0;
+  }
+  __device__ __forceinline__ int4 load(int i) const {
+    const int tile = w + i * nw;
+    if (tile >= ntiles) return make_int4(kInvalidPhys, 0, 0, 0);
+    int phys = __ldg(row + (tile * kTile) / bs);
+    if (phys < 0 || phys >= nblocks) {
+      set_err(err, PA_DEVERR_BLOCK_ID);
+      phys = kInvalidPhys;
+    }
+    int info = min(kTile, L - tile * kTile);
+    if (tile == 0) info |= kFirstOfPair;
+    if (tile == ntiles - 1) info |= kLastOfPair;
+    if (i == 0) info |= kPieceStart;
+    if (tile + nw >= ntiles) info |= kPieceEnd;
+    return make_int4(phys, pair, tile, info);
+  }
+  __device__ __forceinline__ void init(int lane) {
+    base = 0;
+    cur = load(lane);
+    nxt = load(32 + lane);
+  }
+  __device__ __forceinline__ int4 get(int i, int lane) {
+    while (i >= base + 32) {
+      cur = nxt;
+      base += 32;
+      nxt = load(base + 32 + lane);
+    }
+    return shfl_int4(cur, i - base);
+  }
+};
+
+// A contiguous segment [begin, end) of the precomputed unit list.
+struct SegmentSource {
+  const int4 *units;
+  int begin, end;
+  int base;
+  int4 cur, nxt;
+
+  __device__ __forceinline__ int count() const { return end - begin; }
+  __device__ __forceinline__ int4 load(int i) const {
+    const int f = begin + i;
+    if (f >= end) return make_int4(kInvalidPhys, 0, 0, 0);
+    int4 u = __ldg(units + f);
+    if (i == 0 || (u.w & kFirstOfPair)) u.w |= kPieceStart;
+    if (f == end - 1 || (u.w & kLastOfPair)) u.w |= kPieceEnd;
+    return u;
+  }
+  __device__ __forceinline__ void init(int lane) {
+    base = 0;
+    cur = load(lane);
+    nxt = load(32 + lane);
+  }
+  __device__ __forceinline__ int4 get(int i, int lane) {
+    while (i >= base + 32) {
+      cur = nxt;
+      base += 32;
+      nxt = load(base + 32 + lane);
+    }
+    return shfl_int4(cur, i - base);
+  }
+};
+
+// ----------------------------------------------------------------------------
+// the per-warp pipeline
+// ----------------------------------------------------------------------------
+
+struct WarpSmem {
+  uint8_t *stage;     // STAGES * STAGE_BYTES, 1024-aligned
+  uint64_t *bar;      // STAGES mbarriers
+  int4 *meta;         // STAGES * 2 int4: unit, then (k scale, v scale) as floats
+};
+
+template <class C>
+__device__ __forceinline__ void issue(const WarpSmem &ws, int s, int4 u, const Params &p,
+                                      const CUtensorMap *tmK, const CUtensorMap *tmV, int lane) {
+  if (lane != 0) return;
+  uint8_t *stage = ws.stage + s * C::STAGE_BYTES;
+  const uint32_t bar = smem_u32(&ws.bar[s]);
+  const int phys = u.x, pair = u.y, tile = u.z;
+  const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
+  ws.meta[2 * s] = u;
+  if constexpr (C::FP8) {
+    float *sc = reinterpret_cast<float *>(&ws.meta[2 * s + 1]);
+    if (phys != kInvalidPhys) {
+      cp_async_4(smem_u32(sc), p.k_scale + static_cast<size_t>(phys) * p.Hkv + kvh);
+      cp_async_4(smem_u32(sc + 1), p.v_scale + static_cast<size_t>(phys) * p.Hkv + kvh);
+    } else {
+      sc[0] = 0.f;
+      sc[1] = 0.f;
+    }
+    cp_async_arrive(bar);
+  }
+  const bool with_q = (u.w & kPieceStart) != 0;
+  const uint32_t bytes = 2 * C::KV_BYTES + (with_q ? p.G * C::D * 2 : 0);
+  const int y = (phys == kInvalidPhys) ? p.nblocks * p.bs : phys * p.bs + (tile * kTile) % p.bs;
+  const uint32_t dst = smem_u32(stage);
+  fence_proxy_async();
+  mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+  for (int h = 0; h < C::HALVES; ++h) {
+    const int x = kvh * C::D + h * C::BOX_X;
+    tma_load_2d(dst + h * (kTile * 128), tmK, x, y, bar);
+    tma_load_2d(dst + C::KV_BYTES + h * (kTile * 128), tmV, x, y, bar);
+  }
+  if (with_q)
+    bulk_load(dst + 2 * C::KV_BYTES, p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D,
+              p.G * C::D * 2, bar);
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  const bool ok = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Runs all units of `src` through the warp's ring.  on_piece_end(u, first_tile, st)
+// is called after the last tile of every piece.  Returns false after a wait timeout.
+template <class C, class Src, class OnEnd>
+__device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> &st,
+                                         const Params &p, const CUtensorMap *tmK,
+                                         const CUtensorMap *tmV, OnEnd &&on_piece_end,
+                                         int lane) {
+  const int n = src.count();
+  src.init(lane);
+#pragma unroll
+  for (int s = 0; s < C::STAGES; ++s)
+    if (s < n) issue<C>(ws, s, src.get(s, lane), p, tmK, tmV, lane);
+  int first_tile = 0;
+  for (int i = 0; i < n; ++i) {
+    const int s = i % C::STAGES;
+    const uint32_t bar = smem_u32(&ws.bar[s]);
+    if (!warp_wait(bar, (i / C::STAGES) & 1)) {
+      set_err(lane == 0 ? p.err : nullptr, PA_DEVERR_TIMEOUT);
+      for (int j = i; j < n && j < i + C::STAGES; ++j)
+        mbar_wait(smem_u32(&ws.bar[j % C::STAGES]), (j / C::STAGES) & 1);
+      return false;
+    }
+    const int4 u = ws.meta[2 * s];
+    uint8_t *stage = ws.stage + s * C::STAGE_BYTES;
+    const uint32_t ktile = smem_u32(stage);
+    float sscale = p.sl2, vs = 1.f;
+    if (u.w & kPieceStart) {
+      st.reset();
+      load_q<C>(st, ktile + 2 * C::KV_BYTES,
+                reinterpret_cast<const uint16_t *>(stage + 2 * C::KV_BYTES), lane);
+      first_tile = u.z;
+    }
+    if constexpr (C::FP8) {
+      const float4 sc = *reinterpret_cast<const float4 *>(&ws.meta[2 * s + 1]);
+      sscale = p.sl2 * sc.x * st.qshift;
+      vs = sc.y;
+      if (u.w & kPieceStart) st.vs = vs;
+    }
+    process_tile<C>(st, ktile, ktile + C::KV_BYTES, u.w & 0xFF, sscale, vs, lane);
+    if (u.w & kPieceEnd) on_piece_end(u, first_tile, st);
+    __syncwarp();
+    if (i + C::STAGES < n) issue<C>(ws, s, src.get(i + C::STAGES, lane), p, tmK, tmV, lane);
+  }
+  return true;
+}
+
+template <class C>
+__device__ __forceinline__ WarpSmem setup_smem(uint8_t *raw, int warp, int G, int lane) {
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  WarpSmem ws;
+  ws.stage = base + warp * C::STAGES * C::STAGE_BYTES;
+  uint8_t *tail = base + C::WARPS * C::STAGES * C::STAGE_BYTES;
+  ws.bar = reinterpret_cast<uint64_t *>(tail) + warp * C::STAGES;
+  ws.meta = reinterpret_cast<int4 *>(tail + C::WARPS * C::STAGES * 8) + warp * C::STAGES * 2;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(smem_u32(&ws.bar[s]), C::FP8 ? 2 : 1);
+    fence_mbar_init();
+  }
+  // query rows G..8*NT-1 of every Q slot stay zero (the bulk copy writes G rows)
+  const int pad = (8 * C::NT - G) * C::D * 2;
+  for (int s = 0; s < C::STAGES; ++s) {
+    uint8_t *qs = ws.stage + s * C::STAGE_BYTES + 2 * C::KV_BYTES + G * C::D * 2;
+    for (int o = lane * 16; o < pad; o += 32 * 16) *reinterpret_cast<uint4 *>(qs + o) = make_uint4(0, 0, 0, 0);
+  }
+  __syncwarp();
+  return ws;
+}
+
+// ----------------------------------------------------------------------------
+// pa_decode: one CTA per (sequence, KV head)
+// ----------------------------------------------------------------------------
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS)
+    decode_pair_kernel(const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const int pair = blockIdx.x;
+  const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int L = p.seq_lens[b];
+  const int cap = p.max_blocks * p.bs;
+  if (L < 0 || L > cap) {
+    if (threadIdx.x == 0 && kvh == 0) set_err(p.err, PA_DEVERR_SEQ_LEN);
+    L = min(max(L, 0), cap);
+  }
+  const int ntiles = (L + kTile - 1) / kTile;
+
+  WarpSmem ws = setup_smem<C>(smem_raw, warp, p.G, lane);
+  State<C> st;
+  st.reset();
+  PairSource src;
+  src.row = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
+  src.err = p.err;
+  src.pair = pair;
+  src.L = L;
+  src.ntiles = ntiles;
+  src.w = warp;
+  src.nw = C::WARPS;
+  src.bs = p.bs;
+  src.nblocks = p.nblocks;
+  run_warp<C>(src, ws, st, p, &tmK, &tmV, [](int4, int, State<C> &) {}, lane);
+
+  // ---- merge the warps' states: warp w leaves m, l, acc (in absolute units)
+  __syncthreads();
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  constexpr int GP = 8 * C::NT;
+  float *sm_m = reinterpret_cast<float *>(base);                 // [WARPS][GP]
+  float *sm_l = sm_m + C::WARPS * GP;                            // [WARPS][GP]
+  float *sm_acc = sm_l + C::WARPS * GP;                          // [WARPS][GP][D]
+  {
+    float ltot[C::NT][2];
+    reduce_l<C>(st, ltot);
+    const int qd = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int g = nt * 8 + 2 * qd + j;
+        if ((lane >> 2) == 0) {
+          sm_m[warp * GP + g] = st.m[nt][j];
+          sm_l[warp * GP + g] = ltot[nt][j];
+        }
+        const float f = C::FP8 ? st.vs : 1.f;
+#pragma unroll
+        for (int dt = 0; dt < C::DT; ++dt) {
+          sm_acc[(warp * GP + g) * C::D + acc_d<C>(dt, j, lane)] = st.acc[nt][dt][j] * f;
+          sm_acc[(warp * GP + g) * C::D + acc_d<C>(dt, j + 2, lane)] = st.acc[nt][dt][j + 2] * f;
+        }
+      }
+  }
+  __syncthreads();
+  float *out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D;
+  for (int e = threadIdx.x; e < p.G * C::D; e += C::THREADS) {
+    const int g = e / C::D, d = e - g * C::D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < C::WARPS; ++w) M = fmaxf(M, sm_m[w * GP + g]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < C::WARPS; ++w) {
+        const float mw = sm_m[w * GP + g];
+        if (mw == -INFINITY) continue;
+        const float f = ex2(mw - M);
+        num += f * sm_acc[(w * GP + g) * C::D + d];
+        den += f * sm_l[w * GP + g];
+      }
+    }
+    out[e] = den > 0.f ? num / den : 0.f;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// pa_decode_splitkv: plan (scan + unit list), segmented decode, merge
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ int clamp_len(int L, int cap) { return min(max(L, 0), cap); }
+
+// prefix[b] = Hkv * sum_{b' < b} ntiles(b'), prefix[B] = total.  One CTA.
+__global__ void __launch_bounds__(1024) plan_scan_kernel(const int32_t *seq_lens, int B, int Hkv,
+                                                         int cap, int32_t *prefix, int32_t *err) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry_s = 0;
+  __syncthreads();
+  for (int base = 0; base < B; base += 1024) {
+    const int i = base + tid;
+    int v = 0;
+    if (i < B) {
+      const int L = seq_lens[i];
+      if (L < 0 || L > cap) set_err(err, PA_DEVERR_SEQ_LEN);
+      v = Hkv * ((clamp_len(L, cap) + kTile - 1) / kTile);
+    }
+    int x = v;   // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;   // inclusive over warps
+    }
+    __syncthreads();
+    const int carry = carry_s;
+    const int excl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+    if (i < B) prefix[i] = excl;
+    __syncthreads();
+    if (tid == 1023) carry_s = excl + v;
+    __syncthreads();
+  }
+  if (tid == 0) prefix[B] = carry_s;
+}
+
+// units[prefix[b] + kvh * nt + j] for tile j of (b, kvh).  One CTA per sequence.
+__global__ void __launch_bounds__(256) plan_units_kernel(const int32_t *seq_lens,
+                                                         const int32_t *block_tables,
+                                                         const int32_t *prefix, int Hkv,
+                                                         int bs, int nblocks, int max_blocks,
+                                                         int4 *units, int32_t *err) {
+  const int b = blockIdx.x;
+  const int start = prefix[b];
+  const int cnt = prefix[b + 1] - start;
+  if (cnt == 0) return;
+  const int nt = cnt / Hkv;
+  const int L = clamp_len(seq_lens[b], max_blocks * bs);
+  const int32_t *row = block_tables + static_cast<size_t>(b) * max_blocks;
+  for (int k = threadIdx.x; k < cnt; k += blockDim.x) {
+    const int kvh = k / nt, j = k - kvh * nt;
+    int phys = __ldg(row + (j * kTile) / bs);
+    if (phys < 0 || phys >= nblocks) {
+      set_err(err, PA_DEVERR_BLOCK_ID);
+      phys = kInvalidPhys;
+    }
+    int info = min(kTile, L - j * kTile);
+    if (j == 0) info |= kFirstOfPair;
+    if (j == nt - 1) info |= kLastOfPair;
+    units[start + k] = make_int4(phys, b * Hkv + kvh, j, info);
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS)
+    decode_segment_kernel(const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = blockIdx.x * C::WARPS + warp;
+  const int total = p.prefix[p.B];
+  const int W = max(1, (total + p.num_splits - 1) / p.num_splits);
+  WarpSmem ws = setup_smem<C>(smem_raw, warp, p.G, lane);
+  SegmentSource src;
+  src.units = p.units;
+  src.begin = min(seg * W, total);
+  src.end = (seg < p.num_splits) ? min(src.begin + W, total) : src.begin;
+  State<C> st;
+  st.reset();
+  run_warp<C>(
+      src, ws, st, p, &tmK, &tmV,
+      [&](int4 u, int first_tile, State<C> &s) {
+        const int b = u.y / p.Hkv, kvh = u.y - b * p.Hkv;
+        if (first_tile == 0 && (u.w & kLastOfPair)) {
+          write_normalised<C>(s, p.out + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D,
+                              nullptr, p.G, lane);
+        } else {
+          const size_t slot = static_cast<size_t>(seg) * 2 + (first_tile == 0 ? 1 : 0);
+          write_normalised<C>(s, p.o_part + slot * p.G * C::D, p.lse_part + slot * p.G, p.G,
+                              lane);
+        }
+      },
+      lane);
+}
+
+// One CTA per (b, kvh) pair; threads over (head, 4 consecutive d).
+__global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *prefix,
+                                                    const float *o_part, const float *lse_part,
+                                                    int B, int Hq, int Hkv, int G, int D,
+                                                    int num_splits) {
+  const int pair = blockIdx.x;
+  const int b = pair / Hkv, kvh = pair - b * Hkv;
+  const int start_b = prefix[b];
+  const int nt = (prefix[b + 1] - start_b) / Hkv;
+  const int total = prefix[B];
+  const int W = max(1, (total + num_splits - 1) / num_splits);
+  float *o = out + (static_cast<size_t>(b) * Hq + kvh * G) * D;
+  const int D4 = D / 4;
+  if (nt == 0) {
+    for (int e = threadIdx.x; e < G * D4; e += blockDim.x)
+      reinterpret_cast<float4 *>(o)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const int start = start_b + kvh * nt, end = start + nt;
+  const int p0 = start / W, p1 = (end - 1) / W;
+  if (p0 == p1) return;
+  for (int e = threadIdx.x; e < G * D4; e += blockDim.x) {
+    const int g = e / D4, d4 = e - g * D4;
+    float M = -INFINITY;
+    for (int s = p0; s <= p1; ++s)
+      M = fmaxf(M, lse_part[(static_cast<size_t>(s) * 2 + (s == p0)) * G + g]);
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    for (int s = p0; s <= p1; ++s) {
+      const size_t slot = static_cast<size_t>(s) * 2 + (s == p0);
+      const float w = expf(lse_part[slot * G + g] - M);
+      const float4 v = reinterpret_cast<const float4 *>(o_part + (slot * G + g) * D)[d4];
+      num.x += w * v.x;
+      num.y += w * v.y;
+      num.z += w * v.z;
+      num.w += w * v.w;
+      den += w;
+    }
+    const float inv = 1.f / den;
+    reinterpret_cast<float4 *>(o)[e] = make_float4(num.x * inv, num.y * inv, num.z * inv,
+                                                   num.w * inv);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2D view of a pool: rows = nblocks * bs tokens, columns = Hkv * D elements;
+// box = 16 rows x 128 bytes, 128-byte swizzle.
+static bool make_pool_map(CUtensorMap *map, const void *pool, const pa_shape &s) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
+  const int eb = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.Hkv) * s.D,
+                        static_cast<cuuint64_t>(s.nblocks) * s.block_size};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(s.Hkv) * s.D * eb};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(kTile)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void *>(pool), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Opt the kernel in to the dynamic shared memory it needs (per call: cheap, and
+// correct whichever device is current).
+template <class C, class K>
+static cudaError_t prep_kernel(K kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+}
+
+static Params make_params(const pa_shape &s, float *out, const void *q, const float *k_scale,
+                          const float *v_scale, const int32_t *bt, const int32_t *sl,
+                          float sm_scale, int32_t *err) {
+  Params p{};
+  p.out = out;
+  p.q = static_cast<const uint16_t *>(q);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.block_tables = bt;
+  p.seq_lens = sl;
+  p.err = err;
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.G = s.Hq / s.Hkv;
+  p.bs = s.block_size;
+  p.nblocks = s.nblocks;
+  p.max_blocks = s.max_blocks;
+  p.sl2 = sm_scale * kLog2e;
+  return p;
+}
+
+template <class C>
+static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
+                             cudaStream_t stream) {
+  if (prep_kernel<C>(decode_pair_kernel<C>) != cudaSuccess) return PA_ERR_CUDA;
+  decode_pair_kernel<C><<<p.B * p.Hkv, C::THREADS, C::SMEM, stream>>>(mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+template <class C>
+static pa_status launch_segments(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
+                                 cudaStream_t stream) {
+  if (prep_kernel<C>(decode_segment_kernel<C>) != cudaSuccess) return PA_ERR_CUDA;
+  const int grid = (p.num_splits + C::WARPS - 1) / C::WARPS;
+  decode_segment_kernel<C><<<grid, C::THREADS, C::SMEM, stream>>>(mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Dispatch on (D, n-tiles, dtype).
+#define PA_DISPATCH(D_, NT_, FP8_, FN, ...)                                   \
+  if (s.D == D_ && nt == NT_ && fp8 == FP8_) return FN<Cfg<D_, NT_, FP8_>>(__VA_ARGS__);
+
+static pa_status dispatch_pair(const pa_shape &s, const Params &p, const CUtensorMap &mk,
+                               const CUtensorMap &mv, cudaStream_t st) {
+  const int nt = (p.G + 7) / 8;
+  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
+  PA_DISPATCH(128, 1, false, launch_pair, p, mk, mv, st)
+  PA_DISPATCH(128, 2, false, launch_pair, p, mk, mv, st)
+  PA_DISPATCH(64, 1, false, launch_pair, p, mk, mv, st)
+  PA_DISPATCH(64, 2, false, launch_pair, p, mk, mv, st)
+  PA_DISPATCH(128, 1, true, launch_pair, p, mk, mv, st)
+  PA_DISPATCH(128, 2, true, launch_pair, p, mk, mv, st)
+  return PA_ERR_UNSUPPORTED;
+}
+
+static pa_status dispatch_segments(const pa_shape &s, const Params &p, const CUtensorMap &mk,
+                                   const CUtensorMap &mv, cudaStream_t st) {
+  const int nt = (p.G + 7) / 8;
+  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
+  PA_DISPATCH(128, 1, false, launch_segments, p, mk, mv, st)
+  PA_DISPATCH(128, 2, false, launch_segments, p, mk, mv, st)
+  PA_DISPATCH(64, 1, false, launch_segments, p, mk, mv, st)
+  PA_DISPATCH(64, 2, false, launch_segments, p, mk, mv, st)
+  PA_DISPATCH(128, 1, true, launch_segments, p, mk, mv, st)
+  PA_DISPATCH(128, 2, true, launch_segments, p, mk, mv, st)
+  return PA_ERR_UNSUPPORTED;
+}
+
+int decode_smem_bytes(const pa_shape &s) {
+  const int nt = (s.Hq / s.Hkv + 7) / 8;
+  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
+  if (fp8) return nt == 1 ? Cfg<128, 1, true>::SMEM : Cfg<128, 2, true>::SMEM;
+  if (s.D == 64) return nt == 1 ? Cfg<64, 1, false>::SMEM : Cfg<64, 2, false>::SMEM;
+  return nt == 1 ? Cfg<128, 1, false>::SMEM : Cfg<128, 2, false>::SMEM;
+}
+
+int decode_warps_per_cta() { return Cfg<128, 1, false>::WARPS; }
+
+WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits) {
+  WorkspaceLayout w{};
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t G = static_cast<size_t>(s.Hq / s.Hkv);
+  const size_t max_tiles = (static_cast<size_t>(s.max_blocks) * s.block_size + kTile - 1) / kTile;
+  w.prefix = 0;
+  w.units = up(w.prefix + (static_cast<size_t>(s.B) + 1) * 4);
+  w.lse = up(w.units + static_cast<size_t>(s.B) * s.Hkv * max_tiles * 16);
+  w.o_part = up(w.lse + static_cast<size_t>(num_splits) * 2 * G * 4);
+  w.total = up(w.o_part + static_cast<size_t>(num_splits) * 2 * G * s.D * 4);
+  return w;
+}
+
+pa_status run_decode(const pa_shape &s, float *out, const void *q, const void *k_pool,
+                     const void *v_pool, const float *k_scale, const float *v_scale,
+                     const int32_t *bt, const int32_t *sl, float sm_scale, int32_t *err,
+                     cudaStream_t stream) {
+  CUtensorMap mk, mv;
+  if (!make_pool_map(&mk, k_pool, s) || !make_pool_map(&mv, v_pool, s)) return PA_ERR_CUDA;
+  Params p = make_params(s, out, q, k_scale, v_scale, bt, sl, sm_scale, err);
+  return dispatch_pair(s, p, mk, mv, stream);
+}
+
+pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int num_splits,
+                             const void *q, const void *k_pool, const void *v_pool,
+                             const float *k_scale, const float *v_scale, const int32_t *bt,
+                             const int32_t *sl, float sm_scale, int32_t *err,
+                             cudaStream_t stream) {
+  const WorkspaceLayout w = splitkv_layout(s, num_splits);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int32_t *prefix = reinterpret_cast<int32_t *>(ws + w.prefix);
+  int4 *units = reinterpret_cast<int4 *>(ws + w.units);
+  plan_scan_kernel<<<1, 1024, 0, stream>>>(sl, s.B, s.Hkv, s.max_blocks * s.block_size, prefix,
+                                           err);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  plan_units_kernel<<<s.B, 256, 0, stream>>>(sl, bt, prefix, s.Hkv, s.block_size, s.nblocks,
+                                             s.max_blocks, units, err);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  CUtensorMap mk, mv;
+  if (!make_pool_map(&mk, k_pool, s) || !make_pool_map(&mv, v_pool, s)) return PA_ERR_CUDA;
+  Params p = make_params(s, out, q, k_scale, v_scale, bt, sl, sm_scale, err);
+  p.units = units;
+  p.prefix = prefix;
+  p.lse_part = reinterpret_cast<float *>(ws + w.lse);
+  p.o_part = reinterpret_cast<float *>(ws + w.o_part);
+  p.num_splits = num_splits;
+  return dispatch_segments(s, p, mk, mv, stream);
+}
+
+pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int num_splits,
+                    cudaStream_t stream) {
+  const WorkspaceLayout w = splitkv_layout(s, num_splits);
+  const uint8_t *ws = static_cast<const uint8_t *>(workspace);
+  const int G = s.Hq / s.Hkv;
+  const int threads = min(256, max(32, ((G * s.D / 4) + 31) / 32 * 32));
+  merge_kernel<<<s.B * s.Hkv, threads, 0, stream>>>(
+      out, reinterpret_cast<const int32_t *>(ws + w.prefix),
+      reinterpret_cast<const float *>(ws + w.o_part), reinterpret_cast<const float *>(ws + w.lse),
+      s.B, s.Hq, s.Hkv, G, s.D, num_splits);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa

@@ -1,0 +1,44 @@
+// pa_internal.h -- host-side interfaces between the C ABI (pa_api.cu) and the
+// kernel files.  Arguments reaching these functions are already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Byte offsets of the split-KV workspace regions (each 256-byte aligned):
+//   prefix  int32 [B + 1]        tile-count prefix over sequences (x Hkv)
+//   units   int4  [B*Hkv*max_tiles]  (phys block, pair, tile, info) per 16-token tile
+//   lse     fp32  [num_splits][2][G]
+//   o_part  fp32  [num_splits][2][G][D]
+struct WorkspaceLayout {
+  size_t prefix, units, lse, o_part, total;
+};
+
+WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits);
+int decode_smem_bytes(const pa_shape &s);
+int decode_warps_per_cta();
+
+pa_status run_reshape_and_cache(const pa_shape &s, const void *k_new, const void *v_new,
+                                void *k_pool, void *v_pool, float *k_scale, float *v_scale,
+                                const int64_t *slot_mapping, int32_t *err, cudaStream_t stream);
+
+pa_status run_decode(const pa_shape &s, float *out, const void *q, const void *k_pool,
+                     const void *v_pool, const float *k_scale, const float *v_scale,
+                     const int32_t *bt, const int32_t *sl, float sm_scale, int32_t *err,
+                     cudaStream_t stream);
+
+pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int num_splits,
+                             const void *q, const void *k_pool, const void *v_pool,
+                             const float *k_scale, const float *v_scale, const int32_t *bt,
+                             const int32_t *sl, float sm_scale, int32_t *err,
+                             cudaStream_t stream);
+
+pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int num_splits,
+                    cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,101 @@
+"""Device-side buffers for a decode batch and the calls that run on them.
+
+DeviceBatch uploads a workload.Batch (numpy) to the GPU as torch tensors in the
+layouts of include/pa.h and calls the C ABI through the binding.  It only moves
+data and passes pointers; every step of the hot path runs in libpa.so.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _lib
+from .workload import Batch
+
+
+def to_device_bf16(bits: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(
+        torch.bfloat16)
+
+
+class DeviceBatch:
+    def __init__(self, batch: Batch, device="cuda", pools=None):
+        """pools: optional (k_pool, v_pool, k_scale, v_scale) device tensors to use
+        instead of uploading batch.k_pool / batch.v_pool (for large generated pools)."""
+        self.batch = batch
+        self.device = torch.device(device)
+        fp8 = batch.kv_dtype == "fp8_e4m3"
+        self.fp8 = fp8
+        self.shape = _lib.make_shape(batch.B, batch.Hq, batch.Hkv, batch.D, batch.block_size,
+                                     batch.nblocks, batch.max_blocks,
+                                     _lib.PA_KV_FP8_E4M3 if fp8 else _lib.PA_KV_BF16)
+        self.q = to_device_bf16(batch.q, self.device)
+        self.k_new = to_device_bf16(batch.k_new, self.device)
+        self.v_new = to_device_bf16(batch.v_new, self.device)
+        self.block_tables = torch.from_numpy(batch.block_tables).to(self.device)
+        self.seq_lens = torch.from_numpy(batch.seq_lens).to(self.device)
+        self.slot_mapping = torch.from_numpy(batch.slot_mapping).to(self.device)
+        if pools is not None:
+            self.k_pool, self.v_pool, self.k_scale, self.v_scale = pools
+        elif fp8:
+            self.k_pool = torch.from_numpy(batch.k_pool).to(self.device)
+            self.v_pool = torch.from_numpy(batch.v_pool).to(self.device)
+            self.k_scale = torch.from_numpy(batch.k_scale).to(self.device)
+            self.v_scale = torch.from_numpy(batch.v_scale).to(self.device)
+        else:
+            self.k_pool = to_device_bf16(batch.k_pool, self.device)
+            self.v_pool = to_device_bf16(batch.v_pool, self.device)
+            self.k_scale = self.v_scale = None
+        self.out = torch.zeros((batch.B, batch.Hq, batch.D), dtype=torch.float32,
+                               device=self.device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.workspace = None
+        self.num_splits = None
+
+    # -- calls -----------------------------------------------------------------
+
+    def reshape_and_cache(self, stream=None):
+        _lib.pa_reshape_and_cache(self.shape, self.k_new, self.v_new, self.k_pool, self.v_pool,
+                                  self.k_scale, self.v_scale, self.slot_mapping, self.err,
+                                  stream)
+
+    def decode(self, stream=None):
+        _lib.pa_decode(self.shape, self.out, self.q, self.k_pool, self.v_pool, self.k_scale,
+                       self.v_scale, self.block_tables, self.seq_lens, self.batch.sm_scale,
+                       self.err, stream)
+
+    def ensure_workspace(self, num_splits: int):
+        nbytes = _lib.pa_splitkv_workspace_bytes(self.shape, num_splits)
+        if nbytes == 0:
+            raise ValueError("invalid shape or num_splits for split-KV")
+        if self.workspace is None or self.workspace.numel() < nbytes:
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        self.num_splits = num_splits
+
+    def decode_splitkv(self, num_splits: int | None = None, stream=None):
+        if num_splits is None:
+            num_splits = default_num_splits(self.shape, self.device)
+        if self.workspace is None or self.num_splits != num_splits:
+            self.ensure_workspace(num_splits)
+        _lib.pa_decode_splitkv(self.shape, self.out, self.workspace, num_splits, self.q,
+                               self.k_pool, self.v_pool, self.k_scale, self.v_scale,
+                               self.block_tables, self.seq_lens, self.batch.sm_scale, self.err,
+                               stream)
+        _lib.pa_merge_lse(self.shape, self.out, self.workspace, num_splits, stream)
+
+    def read_err(self, stream=None) -> int:
+        return _lib.pa_read_error_flag(self.err, stream)
+
+    # -- host copies for checking ------------------------------------------------
+
+    def pools_numpy(self):
+        if self.fp8:
+            return (self.k_pool.cpu().numpy(), self.v_pool.cpu().numpy(),
+                    self.k_scale.cpu().numpy(), self.v_scale.cpu().numpy())
+        return (self.k_pool.view(torch.int16).cpu().numpy().view(np.uint16),
+                self.v_pool.view(torch.int16).cpu().numpy().view(np.uint16), None, None)
+
+
+def default_num_splits(shape, device=None) -> int:
+    sms = torch.cuda.get_device_properties(device or 0).multi_processor_count
+    return _lib.pa_default_num_splits(shape, sms)

@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
 from collections import deque
 
 import numpy as np
@@ -118,23 +119,44 @@ class Batch:
 # value draws
 # --------------------------------------------------------------------------
 
-def _normal_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 25) -> np.ndarray:
+_CHUNK = 1 << 22
+
+
+def _chunked(rng: np.random.Generator, n: int, fill) -> None:
+    """Run fill(child_rng, start, end) over fixed 4M-element chunks in threads.
+
+    Each chunk has its own generator spawned from one draw of `rng`, so the
+    result depends only on the seed (not on the thread count)."""
+    import concurrent.futures
+    ss = np.random.SeedSequence(int(rng.integers(0, 2 ** 63)))
+    starts = list(range(0, n, _CHUNK))
+    children = ss.spawn(len(starts))
+    work = [(np.random.default_rng(c), s, min(n, s + _CHUNK)) for c, s in zip(children, starts)]
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+        list(ex.map(lambda w: fill(*w), work))
+
+
+def _normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
-    for s in range(0, n, chunk):
-        e = min(n, s + chunk)
-        out[s:e] = bf16_bits(rng.standard_normal(e - s, dtype=np.float32))
+
+    def fill(g, s, e):
+        out[s:e] = bf16_bits(g.standard_normal(e - s, dtype=np.float32))
+
+    _chunked(rng, n, fill)
     return out.reshape(shape)
 
 
-def _fp8_codes(rng: np.random.Generator, shape, chunk: int = 1 << 25) -> np.ndarray:
+def _fp8_codes(rng: np.random.Generator, shape) -> np.ndarray:
     import torch  # float8_e4m3fn rounding of the drawn values (input format only)
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint8)
-    for s in range(0, n, chunk):
-        e = min(n, s + chunk)
-        x = np.clip(rng.standard_normal(e - s, dtype=np.float32) * np.float32(112.0), -448, 448)
+
+    def fill(g, s, e):
+        x = np.clip(g.standard_normal(e - s, dtype=np.float32) * np.float32(112.0), -448, 448)
         out[s:e] = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+    _chunked(rng, n, fill)
     return out.reshape(shape)
 
 

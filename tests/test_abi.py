@@ -1,0 +1,121 @@
+"""The C ABI without a GPU: libpa.so loads, exports every entry point that
+include/pa.h declares, and rejects bad arguments on the host before any CUDA
+call."""
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_28_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_28_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = header_functions()
+    assert declared == sorted(_lib.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert _lib.status_string(s).startswith("PA_")
+
+
+def shape(**kw):
+    base = dict(B=4, Hq=8, Hkv=2, D=64, block_size=16, nblocks=64, max_blocks=8,
+                kv_dtype=_lib.PA_KV_BF16)
+    base.update(kw)
+    return _lib.make_shape(**base)
+
+
+FAKE = 1 << 20      # a 16-byte aligned non-null address: never dereferenced on these paths
+
+
+def _decode(lib, s, **ptr):
+    p = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, ks=None, vs=None, bt=FAKE, sl=FAKE)
+    p.update(ptr)
+    return lib.pa_decode(s, p["out"], p["q"], p["k"], p["v"], p["ks"], p["vs"], p["bt"], p["sl"],
+                         0.125, None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=6, Hkv=4), _lib.PA_ERR_INVALID_ARG),        # Hq % Hkv != 0
+    (dict(Hq=64, Hkv=2), _lib.PA_ERR_UNSUPPORTED),        # G = 32 > 16
+    (dict(D=96), _lib.PA_ERR_UNSUPPORTED),
+    (dict(block_size=8), _lib.PA_ERR_UNSUPPORTED),
+    (dict(kv_dtype=_lib.PA_KV_FP8_E4M3), _lib.PA_ERR_UNSUPPORTED),   # FP8 needs D = 128
+    (dict(kv_dtype=7), _lib.PA_ERR_INVALID_ARG),
+    (dict(nblocks=0), _lib.PA_ERR_INVALID_ARG),
+    (dict(B=-1), _lib.PA_ERR_INVALID_ARG),
+    (dict(nblocks=1 << 27, block_size=32), _lib.PA_ERR_INVALID_ARG),   # rows overflow int32
+])
+def test_decode_rejects_bad_shapes(lib, kw, status):
+    import ctypes
+    assert _decode(lib, ctypes.byref(shape(**kw))) == status
+
+
+def test_decode_rejects_bad_pointers(lib):
+    import ctypes
+    s = ctypes.byref(shape())
+    assert _decode(lib, s, q=None) == _lib.PA_ERR_INVALID_ARG
+    assert _decode(lib, s, k=FAKE + 4) == _lib.PA_ERR_INVALID_ARG     # misaligned
+    fp8 = ctypes.byref(shape(D=128, kv_dtype=_lib.PA_KV_FP8_E4M3))
+    assert _decode(lib, fp8) == _lib.PA_ERR_INVALID_ARG                # scales missing
+    assert lib.pa_decode(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 0.1, None,
+                         None) == _lib.PA_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(lib):
+    import ctypes
+    assert _decode(lib, ctypes.byref(shape(B=0)), q=None) == _lib.PA_OK
+
+
+def test_splitkv_host_checks(lib):
+    import ctypes
+    s = shape(B=64, Hq=64, Hkv=8, D=128, max_blocks=2048, nblocks=30000)
+    nbytes = _lib.pa_splitkv_workspace_bytes(s, 1216)
+    G = 8
+    max_tiles = 2048
+    expect_min = (65 * 4) + 64 * 8 * max_tiles * 16 + 1216 * 2 * G * 4 + 1216 * 2 * G * 128 * 4
+    assert expect_min <= nbytes <= expect_min + 4 * 256
+    assert _lib.pa_splitkv_workspace_bytes(s, 0) == 0
+    assert _lib.pa_splitkv_workspace_bytes(s, 70000) == 0
+    args = [ctypes.byref(s), FAKE, FAKE, nbytes - 1, 1216, FAKE, FAKE, FAKE, None, None, FAKE,
+            FAKE, 0.1, None, None]
+    assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # workspace too small
+    args[3] = nbytes
+    args[2] = FAKE + 16
+    assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # workspace not 256-aligned
+    assert lib.pa_merge_lse(ctypes.byref(s), FAKE, FAKE, 0, None) == _lib.PA_ERR_INVALID_ARG
+
+
+def test_default_num_splits_is_resident_warps(lib):
+    s = shape(B=64, Hq=64, Hkv=8, D=128, max_blocks=2048, nblocks=30000)
+    n = _lib.pa_default_num_splits(s, 152)
+    assert n % 152 == 0 and 152 * 4 <= n <= 152 * 16
+    assert _lib.pa_default_num_splits(s, 0) == 1
+
+
+def test_reshape_rejects_bad_args(lib):
+    import ctypes
+    s = ctypes.byref(shape(B=4))
+    assert lib.pa_reshape_and_cache(s, FAKE, None, FAKE, FAKE, None, None, FAKE, None,
+                                    None) == _lib.PA_ERR_INVALID_ARG
+    fp8 = ctypes.byref(shape(D=128, kv_dtype=_lib.PA_KV_FP8_E4M3))
+    assert lib.pa_reshape_and_cache(fp8, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None,
+                                    None) == _lib.PA_ERR_INVALID_ARG

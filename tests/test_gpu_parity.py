@@ -1,0 +1,385 @@
+"""Parity of the CUDA path (libpa.so through its C ABI) with the CPU oracle.
+
+Every test here needs a GB300.  The bar: bit-exact for the cache write and for
+indexing invariants; |gpu - oracle| <= 1e-3 + 1e-3 |oracle| elementwise for
+bf16 caches and <= 2e-2 + 2e-2 |oracle| for FP8 caches (the oracle reads the
+same codes and scales).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_28_gb300 import _lib
+from paged_kv_cache_28_gb300 import workload as wl
+from paged_kv_cache_28_gb300.device import DeviceBatch, default_num_splits
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = (1e-3, 1e-3)   # (atol, rtol)
+TOL_FP8 = (2e-2, 2e-2)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    _lib.load()
+
+
+def _tol(batch):
+    return TOL_FP8 if batch.kv_dtype == "fp8_e4m3" else TOL_BF16
+
+
+def assert_close(gpu, ref, batch, what=""):
+    atol, rtol = _tol(batch)
+    gpu = np.asarray(gpu, dtype=np.float64)
+    err = np.abs(gpu - ref)
+    bound = atol + rtol * np.abs(ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.where(bad, err - bound, -np.inf)), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {err.size} outside tolerance; worst at {i}:"
+                             f" gpu={gpu[i]!r} oracle={ref[i]!r}")
+
+
+def oracle_after_write(batch, rows=None, write=True):
+    """Oracle output after applying this step's cache write to host copies of the pools."""
+    kp, vp = batch.k_pool.copy(), batch.v_pool.copy()
+    ks = None if batch.k_scale is None else batch.k_scale.copy()
+    vs = None if batch.v_scale is None else batch.v_scale.copy()
+    if write:
+        if batch.kv_dtype == "fp8_e4m3":
+            oracle.reshape_and_cache_fp8(batch.k_new, batch.v_new, kp, vp, ks, vs,
+                                         batch.slot_mapping, batch.block_size)
+        else:
+            oracle.reshape_and_cache_bf16(batch.k_new, batch.v_new, kp, vp, batch.slot_mapping,
+                                          batch.block_size)
+    out = oracle.paged_decode(batch.q, kp, vp, batch.block_tables, batch.seq_lens,
+                              batch.sm_scale, Hkv=batch.Hkv, block_size=batch.block_size,
+                              k_scale=ks, v_scale=vs, rows=rows)
+    return out, (kp, vp, ks, vs)
+
+
+def run_gpu(dev, mode, num_splits=None):
+    dev.out.fill_(float("nan"))
+    if mode == "decode":
+        dev.decode()
+    else:
+        dev.decode_splitkv(num_splits)
+    torch.cuda.synchronize()
+    return dev.out.cpu().numpy()
+
+
+MODES = [("decode", None), ("split", 1), ("split", 3), ("split", 7), ("split", 64),
+         ("split", 1000), ("split", "default")]
+
+
+def _modes_run(dev, batch, ref, label):
+    for mode, ns in MODES:
+        if ns == "default":
+            ns = default_num_splits(dev.shape)
+        out = run_gpu(dev, mode, ns)
+        assert_close(out, ref, batch, f"{label} {mode} num_splits={ns}")
+    assert dev.read_err() == 0
+
+
+# ---------------------------------------------------------------- cache write
+
+def test_reshape_and_cache_bf16_bit_exact():
+    batch = wl.make("tiny")
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    _, (kp, vp, _, _) = oracle_after_write(batch)
+    gk, gv, _, _ = dev.pools_numpy()
+    assert np.array_equal(gk, kp) and np.array_equal(gv, vp)
+    assert dev.read_err() == 0
+
+
+def test_reshape_and_cache_bf16_canary_and_padding():
+    rng = np.random.default_rng(3)
+    T, Hkv, D, bs, nblocks = 37, 4, 128, 32, 11
+    k_pool = np.full((nblocks, bs, Hkv, D), 0xBEEF, np.uint16)
+    v_pool = np.full((nblocks, bs, Hkv, D), 0xCAFE, np.uint16)
+    slots = rng.choice(nblocks * bs, T, replace=False).astype(np.int64)
+    slots[::5] = -1
+    k_new = rng.integers(0, 65536, (T, Hkv, D)).astype(np.uint16)
+    v_new = rng.integers(0, 65536, (T, Hkv, D)).astype(np.uint16)
+    dk = torch.from_numpy(k_pool.view(np.int16)).cuda()
+    dv = torch.from_numpy(v_pool.view(np.int16)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    shape = _lib.make_shape(T, Hkv, Hkv, D, bs, nblocks, 1)
+    _lib.pa_reshape_and_cache(shape, torch.from_numpy(k_new.view(np.int16)).cuda(),
+                              torch.from_numpy(v_new.view(np.int16)).cuda(), dk, dv, None, None,
+                              torch.from_numpy(slots).cuda(), err)
+    oracle.reshape_and_cache_bf16(k_new, v_new, k_pool, v_pool, slots, bs)
+    assert np.array_equal(dk.cpu().numpy().view(np.uint16), k_pool)
+    assert np.array_equal(dv.cpu().numpy().view(np.uint16), v_pool)
+    assert _lib.pa_read_error_flag(err) == 0
+
+
+def _fp8_write_case(seed, T, Hkv, bs, nblocks, steps):
+    """Several write calls; each writes one token into each of T distinct blocks at
+    increasing offsets, so scales grow and rows get re-encoded."""
+    rng = np.random.default_rng(seed)
+    D = 128
+    k_pool = rng.integers(0, 256, (nblocks, bs, Hkv, D)).astype(np.uint8)
+    k_pool[k_pool == 0x7F] = 0
+    k_pool[k_pool == 0xFF] = 0
+    v_pool = k_pool.copy()
+    k_scale = rng.uniform(0.001, 0.01, (nblocks, Hkv)).astype(np.float32)
+    v_scale = k_scale.copy()
+    dk, dv = torch.from_numpy(k_pool).cuda(), torch.from_numpy(v_pool).cuda()
+    dks, dvs = torch.from_numpy(k_scale).cuda(), torch.from_numpy(v_scale).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    blocks = rng.choice(nblocks, T, replace=False)
+    shape = _lib.make_shape(T, Hkv, Hkv, D, bs, nblocks, 1, _lib.PA_KV_FP8_E4M3)
+    for step in range(steps):
+        scale = rng.uniform(0.05, 4.0, (T, 1, 1)).astype(np.float32)
+        x = rng.standard_normal((T, Hkv, D)).astype(np.float32) * scale
+        if step == 1:
+            x[0] = 0.0                               # all-zero token
+        k_new = wl.bf16_bits(x)
+        v_new = wl.bf16_bits(x[::-1].copy())
+        slots = (blocks * bs + step).astype(np.int64)
+        slots[1] = -1                                # padding row
+        _lib.pa_reshape_and_cache(shape, torch.from_numpy(k_new.view(np.int16)).cuda(),
+                                  torch.from_numpy(v_new.view(np.int16)).cuda(), dk, dv, dks, dvs,
+                                  torch.from_numpy(slots).cuda(), err)
+        oracle.reshape_and_cache_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, slots, bs)
+    torch.cuda.synchronize()
+    assert _lib.pa_read_error_flag(err) == 0
+    return (dk.cpu().numpy(), dv.cpu().numpy(), dks.cpu().numpy(), dvs.cpu().numpy()), \
+        (k_pool, v_pool, k_scale, v_scale)
+
+
+@pytest.mark.parametrize("seed,T,Hkv,bs,steps", [(0, 5, 2, 16, 16), (1, 64, 8, 16, 6),
+                                                  (2, 9, 1, 32, 32)])
+def test_reshape_and_cache_fp8_bit_exact(seed, T, Hkv, bs, steps):
+    got, want = _fp8_write_case(seed, T, Hkv, bs, 3 * T + 2, steps)
+    for g, w, name in zip(got, want, ("k_pool", "v_pool", "k_scale", "v_scale")):
+        assert np.array_equal(g.view(np.uint8) if g.dtype != np.float32 else g.view(np.uint32),
+                              w.view(np.uint8) if w.dtype != np.float32 else w.view(np.uint32)), name
+
+
+def test_reshape_and_cache_fp8_conflict_flagged():
+    nblocks, bs, Hkv, D = 4, 16, 1, 128
+    dk = torch.zeros((nblocks, bs, Hkv, D), dtype=torch.uint8, device="cuda")
+    dv = torch.zeros_like(dk)
+    ks = torch.zeros((nblocks, Hkv), dtype=torch.float32, device="cuda")
+    vs = torch.zeros_like(ks)
+    x = torch.ones((3, Hkv, D), dtype=torch.bfloat16, device="cuda")
+    slots = torch.tensor([0, 1, 40], dtype=torch.int64, device="cuda")   # 0, 1 share block 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    shape = _lib.make_shape(3, Hkv, Hkv, D, bs, nblocks, 1, _lib.PA_KV_FP8_E4M3)
+    _lib.pa_reshape_and_cache(shape, x, x, dk, dv, ks, vs, slots, err)
+    assert _lib.pa_read_error_flag(err) == _lib.PA_DEVERR_FP8_CONFLICT
+    assert torch.all(dk[0] == 0) and ks[0, 0].item() == 0.0       # neither written
+    assert torch.all(dk[2, 8] == 0x7E) and ks[2, 0].item() == np.float32(1.0) / np.float32(448)
+
+
+# ---------------------------------------------------------------- decode parity
+
+def test_tiny_config_all_modes():
+    batch = wl.make("tiny")
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch)
+    _modes_run(dev, batch, ref, "tiny")
+
+
+SHAPES = [
+    # Hq, Hkv, D, bs, lens
+    (8, 2, 64, 16, [1, 17, 33, 100]),
+    (64, 8, 128, 16, [1, 15, 16, 17, 31, 32, 33, 250, 1000, 3]),
+    (64, 8, 128, 32, [0, 1, 47, 64, 65, 700]),
+    (16, 16, 64, 16, [5, 300, 0, 129]),           # MHA (G = 1)
+    (32, 2, 128, 16, [77, 1, 500]),               # G = 16 (two n-tiles)
+    (12, 1, 64, 32, [33, 2, 90]),                  # MQA, G = 12
+    (24, 4, 128, 16, [129, 4, 1]),                 # G = 6 (padded group)
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs,lens", SHAPES)
+def test_random_shapes_all_modes(Hq, Hkv, D, bs, lens):
+    batch = wl.build_batch("t", lens, Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seed=Hq + bs + D,
+                           max_blocks=(max(lens) + bs - 1) // bs + 3)
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch)
+    _modes_run(dev, batch, ref, f"Hq={Hq} Hkv={Hkv} D={D} bs={bs}")
+
+
+def test_fp8_small_all_modes():
+    batch = wl.build_batch("t", [1, 16, 17, 200, 33, 0, 1000], Hq=64, Hkv=8, D=128, block_size=16,
+                           seed=21, kv_dtype="fp8_e4m3")
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch)
+    _modes_run(dev, batch, ref, "fp8")
+
+
+def test_fp8_g16_and_bs32():
+    batch = wl.build_batch("t", [3, 64, 65, 400], Hq=32, Hkv=2, D=128, block_size=32, seed=22,
+                           kv_dtype="fp8_e4m3")
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch)
+    _modes_run(dev, batch, ref, "fp8 G=16 bs=32")
+
+
+# ---------------------------------------------------------------- invariants
+
+def _bits(x):
+    return np.asarray(x, dtype=np.float32).view(np.uint32)
+
+
+def test_length_one_returns_v_bitwise():
+    batch = wl.build_batch("t", [1, 1, 1], Hq=64, Hkv=8, D=128, block_size=16, seed=31)
+    dev = DeviceBatch(batch)
+    vf = wl.bf16_to_float(batch.v_pool)
+    for mode, ns in (("decode", None), ("split", 5)):
+        out = run_gpu(dev, mode, ns)
+        for b in range(3):
+            blk = batch.block_tables[b, 0]
+            for h in range(64):
+                assert np.array_equal(_bits(out[b, h]), _bits(vf[blk, 0, h // 8])), (mode, b, h)
+
+
+def _permuted(batch, perm):
+    k = np.empty_like(batch.k_pool)
+    v = np.empty_like(batch.v_pool)
+    k[perm] = batch.k_pool
+    v[perm] = batch.v_pool
+    t = batch.block_tables.copy()
+    t[t >= 0] = perm[t[t >= 0]]
+    return k, v, t
+
+
+def test_block_permutation_invariance_bitwise():
+    batch = wl.build_batch("t", [3, 400, 77, 1600, 16], Hq=64, Hkv=8, D=128, block_size=16,
+                           seed=32)
+    dev = DeviceBatch(batch)
+    outs = [run_gpu(dev, "decode"), run_gpu(dev, "split", 37)]
+    perm = np.random.default_rng(0).permutation(batch.nblocks)
+    k, v, t = _permuted(batch, perm)
+    batch2 = wl.Batch(**{**batch.__dict__, "k_pool": k, "v_pool": v, "block_tables": t})
+    dev2 = DeviceBatch(batch2)
+    outs2 = [run_gpu(dev2, "decode"), run_gpu(dev2, "split", 37)]
+    for a, b in zip(outs, outs2):
+        assert np.array_equal(_bits(a), _bits(b))
+
+
+def test_shared_vs_duplicated_prefix_bitwise():
+    groups = ((900, [0, 1, 2, 3]),)
+    batch = wl.build_batch("t", [950, 2000, 901, 1500], Hq=64, Hkv=8, D=128, block_size=16,
+                           seed=33, prefix_groups=groups, pool_factor=2.0)
+    dev = DeviceBatch(batch)
+    outs = [run_gpu(dev, "decode"), run_gpu(dev, "split", 29)]
+    used = set(batch.block_tables[batch.block_tables >= 0].tolist())
+    free = [i for i in range(batch.nblocks) if i not in used]
+    tables = batch.block_tables.copy()
+    k, v = batch.k_pool.copy(), batch.v_pool.copy()
+    for b in (1, 2, 3):
+        for j in range(900 // 16):
+            dst = free.pop()
+            k[dst], v[dst] = k[tables[b, j]], v[tables[b, j]]
+            tables[b, j] = dst
+    batch2 = wl.Batch(**{**batch.__dict__, "k_pool": k, "v_pool": v, "block_tables": tables})
+    dev2 = DeviceBatch(batch2)
+    outs2 = [run_gpu(dev2, "decode"), run_gpu(dev2, "split", 29)]
+    for a, b in zip(outs, outs2):
+        assert np.array_equal(_bits(a), _bits(b))
+
+
+def test_zero_query_gives_mean_of_v():
+    batch = wl.build_batch("t", [333, 16], Hq=8, Hkv=1, D=128, block_size=16, seed=34)
+    batch.q[:] = 0
+    dev = DeviceBatch(batch)
+    vf = wl.bf16_to_float(batch.v_pool).astype(np.float64)
+    for mode, ns in (("decode", None), ("split", 9)):
+        out = run_gpu(dev, mode, ns)
+        for b, L in enumerate(batch.seq_lens):
+            t = np.arange(L)
+            mean = vf[batch.block_tables[b, t // 16], t % 16, 0].mean(axis=0)
+            assert_close(out[b], np.broadcast_to(mean, out[b].shape), batch, "q=0")
+
+
+def test_repeatable_bitwise():
+    batch = wl.build_batch("t", [1200, 5, 3000], Hq=64, Hkv=8, D=128, block_size=16, seed=35)
+    dev = DeviceBatch(batch)
+    a = run_gpu(dev, "split", 111)
+    b = run_gpu(dev, "split", 111)
+    assert np.array_equal(_bits(a), _bits(b))
+
+
+def test_empty_batch_rows_and_all_empty():
+    batch = wl.build_batch("t", [0, 0, 40, 0], Hq=8, Hkv=2, D=64, block_size=16, seed=36)
+    dev = DeviceBatch(batch)
+    ref, _ = oracle_after_write(batch, write=False)
+    for mode, ns in (("decode", None), ("split", 4)):
+        out = run_gpu(dev, mode, ns)
+        assert np.all(out[[0, 1, 3]] == 0.0)
+        assert_close(out, ref, batch, mode)
+    empty = wl.build_batch("t", [0, 0], Hq=8, Hkv=2, D=64, block_size=16, seed=37)
+    dev = DeviceBatch(empty)
+    for mode, ns in (("decode", None), ("split", 4)):
+        assert np.all(run_gpu(dev, mode, ns) == 0.0)
+
+
+# ---------------------------------------------------------------- device error flags
+
+def test_bad_block_id_flagged():
+    batch = wl.build_batch("t", [40, 40], Hq=8, Hkv=2, D=64, block_size=16, seed=38)
+    batch.block_tables[1, 1] = batch.nblocks + 5
+    dev = DeviceBatch(batch)
+    for mode, ns in (("decode", None), ("split", 3)):
+        dev.err.zero_()
+        out = run_gpu(dev, mode, ns)
+        assert dev.read_err() & _lib.PA_DEVERR_BLOCK_ID
+        ref, _ = oracle_after_write(wl.Batch(**{**batch.__dict__, "seq_lens": batch.seq_lens[:1],
+                                                "q": batch.q[:1], "B": 1}), write=False)
+        assert_close(out[:1], ref, batch, "untouched sequence")
+
+
+def test_bad_seq_len_and_slot_flagged():
+    batch = wl.build_batch("t", [20, 20], Hq=8, Hkv=2, D=64, block_size=16, seed=39)
+    batch.seq_lens[0] = batch.max_blocks * 16 + 1
+    dev = DeviceBatch(batch)
+    for mode, ns in (("decode", None), ("split", 3)):
+        dev.err.zero_()
+        run_gpu(dev, mode, ns)
+        assert dev.read_err() & _lib.PA_DEVERR_SEQ_LEN
+    dev.err.zero_()
+    dev.slot_mapping[0] = batch.nblocks * 16 + 3
+    dev.reshape_and_cache()
+    assert dev.read_err() & _lib.PA_DEVERR_SLOT
+
+
+# ---------------------------------------------------------------- full-size configs
+
+def _sample_rows(batch, rng, n_random=192):
+    lens = batch.seq_lens
+    pick = {int(np.argmax(lens)), int(np.argmin(lens))}
+    pick.update(int(b) for b in rng.choice(batch.B, min(batch.B, 3), replace=False))
+    rows = [(b, h) for b in sorted(pick) for h in range(batch.Hq)]
+    rows += [(int(rng.integers(batch.B)), int(rng.integers(batch.Hq))) for _ in range(n_random)]
+    return np.array(rows, dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", ["llama70b_layer", "prefix_sharing", "long_context", "fp8_mixed"])
+def test_full_size_config_sampled(name):
+    """The bench's launch configuration (split-KV, default num_splits) at full size;
+    every head of the longest, shortest and three random sequences plus 192
+    random (b, h) rows are compared with the oracle."""
+    batch = wl.make(name)
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    out = run_gpu(dev, "split", default_num_splits(dev.shape))
+    assert dev.read_err() == 0
+    rows = _sample_rows(batch, np.random.default_rng(7))
+    ref, _ = oracle_after_write(batch, rows=rows)
+    assert_close(out[rows[:, 0], rows[:, 1]], ref, batch, name)
+    if name == "fp8_mixed":      # unsplit kernel too, on the same rows
+        out2 = run_gpu(dev, "decode")
+        assert_close(out2[rows[:, 0], rows[:, 1]], ref, batch, name + " decode")
