@@ -30,7 +30,8 @@
  * ---------------------------------------------------------------------------
  *  - All array arguments are caller-owned DEVICE memory of the current CUDA
  *    device, row-major, 16-byte aligned.  The library allocates nothing, frees
- *    nothing and keeps no state between calls.
+ *    nothing and keeps no state between calls (pa_decode_splitkv_noalloc, at
+ *    the end, is the one call with a library-owned scratch array).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *    stream) and is asynchronous: no call synchronises.
  *  - Arguments are checked on the host before anything is launched; a bad
@@ -184,6 +185,42 @@ pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
  */
 pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,
                        int32_t num_splits, pa_stream_t stream);
+
+/*
+ * pa_decode_splitkv_noalloc -- pa_decode_splitkv followed by pa_merge_lse, for
+ * callers that cannot allocate device memory.  The pages describe no such
+ * call; it exists for users of this library who may not call cudaMalloc: a
+ * plugin inside a host framework that owns all device memory through its own
+ * pool, a latency-critical path where cudaMalloc's implicit device-wide
+ * synchronisation is not acceptable, or a deployment whose memory budget is
+ * fixed at start-up.
+ *
+ * Instead of a caller workspace it uses a scratch array of
+ * PA_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library: every GPU that
+ * loads libpa.so holds that array until the process exits.  The call allocates
+ * nothing and frees nothing.  Arguments and results are those of
+ * pa_decode_splitkv + pa_merge_lse: out [B, Hq, D] is complete when the work
+ * enqueued on `stream` has finished.
+ *
+ * Limits and sharing:
+ *   - returns PA_ERR_INVALID_ARG (launching nothing) when
+ *     pa_splitkv_workspace_bytes(shape, num_splits) exceeds
+ *     PA_NOALLOC_SCRATCH_BYTES, or for any argument pa_decode_splitkv rejects;
+ *   - the first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress) and caches it; make that first call before
+ *     any stream capture;
+ *   - all calls share the one array per device and it keeps the last call's
+ *     contents (nothing in it needs to start at zero); calls whose work
+ *     overlaps on the GPU -- on different streams, or from different threads --
+ *     race on it and must be serialised by the caller.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+pa_status pa_decode_splitkv_noalloc(const pa_shape *shape, float *out, int32_t num_splits,
+                                    const void *q, const void *k_pool, const void *v_pool,
+                                    const float *k_scale, const float *v_scale,
+                                    const int32_t *block_tables, const int32_t *seq_lens,
+                                    float sm_scale, int32_t *err_flag, pa_stream_t stream);
 
 /* Human-readable name of a status. */
 const char *pa_status_string(pa_status status);

@@ -20,7 +20,8 @@ PA_DEVERR_FP8_CONFLICT, PA_DEVERR_TIMEOUT = 8, 16
 
 EXPORTED = ("pa_reshape_and_cache", "pa_decode", "pa_splitkv_workspace_bytes",
             "pa_default_num_splits", "pa_decode_splitkv", "pa_merge_lse", "pa_status_string",
-            "pa_read_error_flag")
+            "pa_read_error_flag", "pa_decode_splitkv_noalloc")
+PA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class pa_shape(ctypes.Structure):
@@ -59,6 +60,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "pa_merge_lse": (I32, [S, P, P, I32, P]),
             "pa_status_string": (ctypes.c_char_p, [I32]),
             "pa_read_error_flag": (I32, [P, ctypes.POINTER(I32), P]),
+            "pa_decode_splitkv_noalloc": (I32, [S, P, I32, P, P, P, P, P, P, P, F, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -160,3 +162,15 @@ def pa_read_error_flag(err_flag, stream=None) -> int:
     if st not in (PA_OK, PA_ERR_DEVICE):
         raise PAError("pa_read_error_flag", st)
     return int(v.value)
+
+
+def pa_decode_splitkv_noalloc(shape: pa_shape, out, num_splits: int, q, k_pool, v_pool,
+                              k_scale, v_scale, block_tables, seq_lens, sm_scale: float,
+                              err_flag=None, stream=None) -> None:
+    """Split-KV decode + merge with the library's own fixed scratch array, for
+    callers that may not allocate device memory (see include/pa.h)."""
+    lib = load()
+    _check("pa_decode_splitkv_noalloc", lib.pa_decode_splitkv_noalloc(
+        ctypes.byref(shape), _ptr(out), int(num_splits), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), float(sm_scale),
+        _ptr(err_flag), _stream(stream)))
