@@ -167,7 +167,9 @@ int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count);
  * the same stream with the same shape, workspace and num_splits.
  * workspace: device memory of at least pa_splitkv_workspace_bytes(shape,
  * num_splits) bytes, 256-byte aligned, owned by the caller, not shared with
- * concurrent calls.  1 <= num_splits <= 65536.
+ * concurrent calls; nothing in it needs initialising.  1 <= num_splits <= 65536.
+ * Batches of more than 16384 sequences return PA_ERR_UNSUPPORTED (each CTA
+ * scans the sequence lengths in shared memory).
  */
 pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
                             size_t workspace_bytes, int32_t num_splits, const void *q,

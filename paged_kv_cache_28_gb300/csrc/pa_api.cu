@@ -95,7 +95,7 @@ int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count) {
   if (check_shape(shape, true) != PA_OK || sm_count <= 0) return 1;
   // resident split workers: CTAs per SM by shared memory (228 KB per SM, 1 KB
   // reserved per CTA), capped by the 2048-thread limit, times warps per CTA
-  const int per_cta = pa::decode_smem_bytes(*shape) + 1024;
+  const int per_cta = pa::splitkv_smem_bytes(*shape) + 1024;
   const int warps = pa::decode_warps_per_cta();
   int ctas = (228 * 1024) / per_cta;
   if (ctas > 2048 / (32 * warps)) ctas = 2048 / (32 * warps);
@@ -116,6 +116,7 @@ pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
                                    block_tables, seq_lens);
   if (st != PA_OK) return st;
   if (num_splits < 1 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARG;
+  if (shape->B > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
   if (workspace_bytes < pa::splitkv_layout(*shape, num_splits).total) return PA_ERR_INVALID_ARG;
   return pa::run_decode_splitkv(*shape, out, workspace, num_splits, q, k_pool, v_pool, k_scale,

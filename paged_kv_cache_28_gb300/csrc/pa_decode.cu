@@ -74,8 +74,7 @@ struct Params {
   int B, Hq, Hkv, G, bs, nblocks, max_blocks;
   float sl2;  // sm_scale * log2(e)
   // split-KV
-  const int4 *units;
-  const int32_t *prefix;
+  int32_t *prefix_out;   // workspace copy of the tile prefix, read by the merge
   float *o_part;
   float *lse_part;
   int num_splits;
@@ -407,9 +406,15 @@ struct PairSource {
   }
 };
 
-// A contiguous segment [begin, end) of the precomputed unit list.
+// A contiguous segment [begin, end) of the tile stream: position f belongs to the
+// sequence b with prefix[b] <= f < prefix[b + 1] (binary search in shared memory),
+// then to KV head (f - prefix[b]) / ntiles(b) and tile (f - prefix[b]) % ntiles(b).
 struct SegmentSource {
-  const int4 *units;
+  const int32_t *prefix;     // shared: [B + 1]
+  const uint8_t *lastn;      // shared: [B] valid tokens in each sequence's last tile
+  const int32_t *block_tables;
+  int32_t *err;
+  int B, Hkv, bs, nblocks, max_blocks;
   int begin, end;
   int base;
   int4 cur, nxt;
@@ -418,10 +423,26 @@ struct SegmentSource {
   __device__ __forceinline__ int4 load(int i) const {
     const int f = begin + i;
     if (f >= end) return make_int4(kInvalidPhys, 0, 0, 0);
-    int4 u = __ldg(units + f);
-    if (i == 0 || (u.w & kFirstOfPair)) u.w |= kPieceStart;
-    if (f == end - 1 || (u.w & kLastOfPair)) u.w |= kPieceEnd;
-    return u;
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= f) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo, start = prefix[b];
+    const int nt = (prefix[b + 1] - start) / Hkv;
+    const int r = f - start;
+    const int kvh = r / nt, tile = r - kvh * nt;
+    int phys = __ldg(block_tables + static_cast<size_t>(b) * max_blocks + (tile * kTile) / bs);
+    if (phys < 0 || phys >= nblocks) {
+      set_err(err, PA_DEVERR_BLOCK_ID);
+      phys = kInvalidPhys;
+    }
+    int info = (tile == nt - 1) ? lastn[b] : kTile;
+    if (tile == 0) info |= kFirstOfPair | kPieceStart;
+    if (tile == nt - 1) info |= kLastOfPair | kPieceEnd;
+    if (i == 0) info |= kPieceStart;
+    if (f == end - 1) info |= kPieceEnd;
+    return make_int4(phys, b * Hkv + kvh, tile, info);
   }
   __device__ __forceinline__ void init(int lane) {
     base = 0;
@@ -560,6 +581,20 @@ __device__ __forceinline__ WarpSmem setup_smem(uint8_t *raw, int warp, int G, in
   return ws;
 }
 
+// First byte after the per-warp stages, barriers and metadata (16-byte aligned).
+template <class C>
+__device__ __forceinline__ uint8_t *split_tail(uint8_t *raw) {
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  return base + C::WARPS * C::STAGES * (C::STAGE_BYTES + 8 + C::META_BYTES);
+}
+
+// Dynamic shared memory of the split kernel: stages plus the length scan.
+template <class C>
+__host__ __device__ constexpr int split_smem(int B) {
+  return C::SMEM + ((B + 1) * 4 + B + 15) / 16 * 16;
+}
+
 // ----------------------------------------------------------------------------
 // pa_decode: one CTA per (sequence, KV head)
 // ----------------------------------------------------------------------------
@@ -652,23 +687,30 @@ __global__ void __launch_bounds__(C::THREADS)
 
 __device__ __forceinline__ int clamp_len(int L, int cap) { return min(max(L, 0), cap); }
 
-// prefix[b] = Hkv * sum_{b' < b} ntiles(b'), prefix[B] = total.  One CTA.
-__global__ void __launch_bounds__(1024) plan_scan_kernel(const int32_t *seq_lens, int B, int Hkv,
-                                                         int cap, int32_t *prefix, int32_t *err) {
-  __shared__ int warp_sums[32];
+// Block-wide scan of the sequence lengths into shared memory:
+//   prefix[b] = Hkv * sum_{b' < b} ntiles(b'),  prefix[B] = total tiles,
+//   lastn[b]  = valid tokens in the last 16-token tile of sequence b.
+// Out-of-range lengths are clamped (and reported once, by CTA 0).
+template <int THREADS>
+__device__ void scan_lengths(const Params &p, int32_t *prefix, uint8_t *lastn) {
+  __shared__ int warp_sums[THREADS / 32];
   __shared__ int carry_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cap = p.max_blocks * p.bs;
   if (tid == 0) carry_s = 0;
   __syncthreads();
-  for (int base = 0; base < B; base += 1024) {
+  for (int base = 0; base < p.B; base += THREADS) {
     const int i = base + tid;
     int v = 0;
-    if (i < B) {
-      const int L = seq_lens[i];
-      if (L < 0 || L > cap) set_err(err, PA_DEVERR_SEQ_LEN);
-      v = Hkv * ((clamp_len(L, cap) + kTile - 1) / kTile);
+    if (i < p.B) {
+      const int L0 = p.seq_lens[i];
+      if ((L0 < 0 || L0 > cap) && blockIdx.x == 0) set_err(p.err, PA_DEVERR_SEQ_LEN);
+      const int L = clamp_len(L0, cap);
+      const int nt = (L + kTile - 1) / kTile;
+      v = p.Hkv * nt;
+      lastn[i] = static_cast<uint8_t>(nt ? L - (nt - 1) * kTile : 0);
     }
-    int x = v;   // inclusive warp scan
+    int x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -676,51 +718,15 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(const int32_t *seq_lens
     }
     if (lane == 31) warp_sums[warp] = x;
     __syncthreads();
-    if (warp == 0) {
-      int w = warp_sums[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
-      }
-      warp_sums[lane] = w;   // inclusive over warps
-    }
+    int before = carry_s;
+    for (int w = 0; w < warp; ++w) before += warp_sums[w];
+    if (i < p.B) prefix[i] = before + x - v;
     __syncthreads();
-    const int carry = carry_s;
-    const int excl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
-    if (i < B) prefix[i] = excl;
-    __syncthreads();
-    if (tid == 1023) carry_s = excl + v;
+    if (tid == THREADS - 1) carry_s = before + x;
     __syncthreads();
   }
-  if (tid == 0) prefix[B] = carry_s;
-}
-
-// units[prefix[b] + kvh * nt + j] for tile j of (b, kvh).  One CTA per sequence.
-__global__ void __launch_bounds__(256) plan_units_kernel(const int32_t *seq_lens,
-                                                         const int32_t *block_tables,
-                                                         const int32_t *prefix, int Hkv,
-                                                         int bs, int nblocks, int max_blocks,
-                                                         int4 *units, int32_t *err) {
-  const int b = blockIdx.x;
-  const int start = prefix[b];
-  const int cnt = prefix[b + 1] - start;
-  if (cnt == 0) return;
-  const int nt = cnt / Hkv;
-  const int L = clamp_len(seq_lens[b], max_blocks * bs);
-  const int32_t *row = block_tables + static_cast<size_t>(b) * max_blocks;
-  for (int k = threadIdx.x; k < cnt; k += blockDim.x) {
-    const int kvh = k / nt, j = k - kvh * nt;
-    int phys = __ldg(row + (j * kTile) / bs);
-    if (phys < 0 || phys >= nblocks) {
-      set_err(err, PA_DEVERR_BLOCK_ID);
-      phys = kInvalidPhys;
-    }
-    int info = min(kTile, L - j * kTile);
-    if (j == 0) info |= kFirstOfPair;
-    if (j == nt - 1) info |= kLastOfPair;
-    units[start + k] = make_int4(phys, b * Hkv + kvh, j, info);
-  }
+  if (tid == 0) prefix[p.B] = carry_s;
+  __syncthreads();
 }
 
 template <class C>
@@ -729,12 +735,25 @@ __global__ void __launch_bounds__(C::THREADS)
                           const __grid_constant__ CUtensorMap tmV, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = blockIdx.x * C::WARPS + warp;
-  const int total = p.prefix[p.B];
-  const int W = max(1, (total + p.num_splits - 1) / p.num_splits);
   WarpSmem ws = setup_smem<C>(smem_raw, warp, p.G, lane);
+  int32_t *prefix = reinterpret_cast<int32_t *>(split_tail<C>(smem_raw));
+  uint8_t *lastn = reinterpret_cast<uint8_t *>(prefix + p.B + 1);
+  scan_lengths<C::THREADS>(p, prefix, lastn);
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= p.B; i += C::THREADS) p.prefix_out[i] = prefix[i];
+  const int seg = blockIdx.x * C::WARPS + warp;
+  const int total = prefix[p.B];
+  const int W = max(1, (total + p.num_splits - 1) / p.num_splits);
   SegmentSource src;
-  src.units = p.units;
+  src.prefix = prefix;
+  src.lastn = lastn;
+  src.block_tables = p.block_tables;
+  src.err = p.err;
+  src.B = p.B;
+  src.Hkv = p.Hkv;
+  src.bs = p.bs;
+  src.nblocks = p.nblocks;
+  src.max_blocks = p.max_blocks;
   src.begin = min(seg * W, total);
   src.end = (seg < p.num_splits) ? min(src.begin + W, total) : src.begin;
   State<C> st;
@@ -755,7 +774,8 @@ __global__ void __launch_bounds__(C::THREADS)
       lane);
 }
 
-// One CTA per (b, kvh) pair; threads over (head, 4 consecutive d).
+// One CTA per (b, kvh) pair; threads over (head, 4 consecutive d).  The pieces of a
+// pair are visited eight at a time with their loads issued together.
 __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *prefix,
                                                     const float *o_part, const float *lse_part,
                                                     int B, int Hq, int Hkv, int G, int D,
@@ -776,22 +796,40 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
   const int start = start_b + kvh * nt, end = start + nt;
   const int p0 = start / W, p1 = (end - 1) / W;
   if (p0 == p1) return;
+  constexpr int U = 8;
   for (int e = threadIdx.x; e < G * D4; e += blockDim.x) {
     const int g = e / D4, d4 = e - g * D4;
+    auto slot = [&](int s) { return static_cast<size_t>(s) * 2 + (s == p0 ? 1 : 0); };
     float M = -INFINITY;
-    for (int s = p0; s <= p1; ++s)
-      M = fmaxf(M, lse_part[(static_cast<size_t>(s) * 2 + (s == p0)) * G + g]);
+    for (int s0 = p0; s0 <= p1; s0 += U) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        v[u] = (s0 + u <= p1) ? __ldg(lse_part + slot(s0 + u) * G + g) : -INFINITY;
+#pragma unroll
+      for (int u = 0; u < U; ++u) M = fmaxf(M, v[u]);
+    }
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
-    for (int s = p0; s <= p1; ++s) {
-      const size_t slot = static_cast<size_t>(s) * 2 + (s == p0);
-      const float w = expf(lse_part[slot * G + g] - M);
-      const float4 v = reinterpret_cast<const float4 *>(o_part + (slot * G + g) * D)[d4];
-      num.x += w * v.x;
-      num.y += w * v.y;
-      num.z += w * v.z;
-      num.w += w * v.w;
-      den += w;
+    for (int s0 = p0; s0 <= p1; s0 += U) {
+      float l[U];
+      float4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const bool ok = s0 + u <= p1;
+        l[u] = ok ? __ldg(lse_part + slot(s0 + u) * G + g) : -INFINITY;
+        x[u] = ok ? __ldg(reinterpret_cast<const float4 *>(o_part + (slot(s0 + u) * G + g) * D) + d4)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float w = expf(l[u] - M);
+        num.x += w * x[u].x;
+        num.y += w * x[u].y;
+        num.z += w * x[u].z;
+        num.w += w * x[u].w;
+        den += w;
+      }
     }
     const float inv = 1.f / den;
     reinterpret_cast<float4 *>(o)[e] = make_float4(num.x * inv, num.y * inv, num.z * inv,
@@ -876,9 +914,12 @@ static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUten
 template <class C>
 static pa_status launch_segments(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
                                  cudaStream_t stream) {
-  if (prep_kernel<C>(decode_segment_kernel<C>) != cudaSuccess) return PA_ERR_CUDA;
+  const int smem = split_smem<C>(p.B);
+  if (cudaFuncSetAttribute(decode_segment_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return PA_ERR_CUDA;
   const int grid = (p.num_splits + C::WARPS - 1) / C::WARPS;
-  decode_segment_kernel<C><<<grid, C::THREADS, C::SMEM, stream>>>(mk, mv, p);
+  decode_segment_kernel<C><<<grid, C::THREADS, smem, stream>>>(mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -912,12 +953,13 @@ static pa_status dispatch_segments(const pa_shape &s, const Params &p, const CUt
   return PA_ERR_UNSUPPORTED;
 }
 
-int decode_smem_bytes(const pa_shape &s) {
+int splitkv_smem_bytes(const pa_shape &s) {
   const int nt = (s.Hq / s.Hkv + 7) / 8;
   const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
-  if (fp8) return nt == 1 ? Cfg<128, 1, true>::SMEM : Cfg<128, 2, true>::SMEM;
-  if (s.D == 64) return nt == 1 ? Cfg<64, 1, false>::SMEM : Cfg<64, 2, false>::SMEM;
-  return nt == 1 ? Cfg<128, 1, false>::SMEM : Cfg<128, 2, false>::SMEM;
+  if (fp8) return nt == 1 ? split_smem<Cfg<128, 1, true>>(s.B) : split_smem<Cfg<128, 2, true>>(s.B);
+  if (s.D == 64)
+    return nt == 1 ? split_smem<Cfg<64, 1, false>>(s.B) : split_smem<Cfg<64, 2, false>>(s.B);
+  return nt == 1 ? split_smem<Cfg<128, 1, false>>(s.B) : split_smem<Cfg<128, 2, false>>(s.B);
 }
 
 int decode_warps_per_cta() { return Cfg<128, 1, false>::WARPS; }
@@ -926,10 +968,8 @@ WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits) {
   WorkspaceLayout w{};
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t G = static_cast<size_t>(s.Hq / s.Hkv);
-  const size_t max_tiles = (static_cast<size_t>(s.max_blocks) * s.block_size + kTile - 1) / kTile;
   w.prefix = 0;
-  w.units = up(w.prefix + (static_cast<size_t>(s.B) + 1) * 4);
-  w.lse = up(w.units + static_cast<size_t>(s.B) * s.Hkv * max_tiles * 16);
+  w.lse = up(w.prefix + (static_cast<size_t>(s.B) + 1) * 4);
   w.o_part = up(w.lse + static_cast<size_t>(num_splits) * 2 * G * 4);
   w.total = up(w.o_part + static_cast<size_t>(num_splits) * 2 * G * s.D * 4);
   return w;
@@ -952,19 +992,10 @@ pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int
                              cudaStream_t stream) {
   const WorkspaceLayout w = splitkv_layout(s, num_splits);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  int32_t *prefix = reinterpret_cast<int32_t *>(ws + w.prefix);
-  int4 *units = reinterpret_cast<int4 *>(ws + w.units);
-  plan_scan_kernel<<<1, 1024, 0, stream>>>(sl, s.B, s.Hkv, s.max_blocks * s.block_size, prefix,
-                                           err);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-  plan_units_kernel<<<s.B, 256, 0, stream>>>(sl, bt, prefix, s.Hkv, s.block_size, s.nblocks,
-                                             s.max_blocks, units, err);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   CUtensorMap mk, mv;
   if (!make_pool_map(&mk, k_pool, s) || !make_pool_map(&mv, v_pool, s)) return PA_ERR_CUDA;
   Params p = make_params(s, out, q, k_scale, v_scale, bt, sl, sm_scale, err);
-  p.units = units;
-  p.prefix = prefix;
+  p.prefix_out = reinterpret_cast<int32_t *>(ws + w.prefix);
   p.lse_part = reinterpret_cast<float *>(ws + w.lse);
   p.o_part = reinterpret_cast<float *>(ws + w.o_part);
   p.num_splits = num_splits;

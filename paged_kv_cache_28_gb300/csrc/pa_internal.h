@@ -12,15 +12,17 @@ namespace pa {
 
 // Byte offsets of the split-KV workspace regions (each 256-byte aligned):
 //   prefix  int32 [B + 1]        tile-count prefix over sequences (x Hkv)
-//   units   int4  [B*Hkv*max_tiles]  (phys block, pair, tile, info) per 16-token tile
 //   lse     fp32  [num_splits][2][G]
 //   o_part  fp32  [num_splits][2][G][D]
 struct WorkspaceLayout {
-  size_t prefix, units, lse, o_part, total;
+  size_t prefix, lse, o_part, total;
 };
 
+// Largest batch the split-KV kernel accepts (its length scan lives in shared memory).
+constexpr int kMaxSplitBatch = 16384;
+
 WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits);
-int decode_smem_bytes(const pa_shape &s);
+int splitkv_smem_bytes(const pa_shape &s);
 int decode_warps_per_cta();
 
 pa_status run_reshape_and_cache(const pa_shape &s, const void *k_new, const void *v_new,

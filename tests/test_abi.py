@@ -90,9 +90,8 @@ def test_splitkv_host_checks(lib):
     s = shape(B=64, Hq=64, Hkv=8, D=128, max_blocks=2048, nblocks=30000)
     nbytes = _lib.pa_splitkv_workspace_bytes(s, 1216)
     G = 8
-    max_tiles = 2048
-    expect_min = (65 * 4) + 64 * 8 * max_tiles * 16 + 1216 * 2 * G * 4 + 1216 * 2 * G * 128 * 4
-    assert expect_min <= nbytes <= expect_min + 4 * 256
+    expect_min = (65 * 4) + 1216 * 2 * G * 4 + 1216 * 2 * G * 128 * 4
+    assert expect_min <= nbytes <= expect_min + 3 * 256
     assert _lib.pa_splitkv_workspace_bytes(s, 0) == 0
     assert _lib.pa_splitkv_workspace_bytes(s, 70000) == 0
     args = [ctypes.byref(s), FAKE, FAKE, nbytes - 1, 1216, FAKE, FAKE, FAKE, None, None, FAKE,
@@ -102,6 +101,11 @@ def test_splitkv_host_checks(lib):
     args[2] = FAKE + 16
     assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # workspace not 256-aligned
     assert lib.pa_merge_lse(ctypes.byref(s), FAKE, FAKE, 0, None) == _lib.PA_ERR_INVALID_ARG
+    big = _lib.make_shape(16385, 8, 8, 128, 16, 30000, 4)
+    args[0] = ctypes.byref(big)
+    args[3] = _lib.pa_splitkv_workspace_bytes(big, 1216)
+    args[2] = FAKE
+    assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_UNSUPPORTED      # B > 16384
 
 
 def test_default_num_splits_is_resident_warps(lib):

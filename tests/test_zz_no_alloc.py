@@ -56,10 +56,10 @@ def test_noalloc_matches_workspace_entry_points_on_consecutive_calls():
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = _lib.load()
-    # 256 sequences x 8 KV heads x 2048 tiles of unit records need more than the array holds
+    # 65536 split workers' partials need more than the array holds
     s = _lib.make_shape(256, 64, 8, 128, 16, 60000, 2048)
-    assert _lib.pa_splitkv_workspace_bytes(s, 1216) > _lib.PA_NOALLOC_SCRATCH_BYTES
-    st = lib.pa_decode_splitkv_noalloc(ctypes.byref(s), 1 << 20, 1216, 1 << 20, 1 << 20, 1 << 20,
+    assert _lib.pa_splitkv_workspace_bytes(s, 65536) > _lib.PA_NOALLOC_SCRATCH_BYTES
+    st = lib.pa_decode_splitkv_noalloc(ctypes.byref(s), 1 << 20, 65536, 1 << 20, 1 << 20, 1 << 20,
                                        None, None, 1 << 20, 1 << 20, ctypes.c_float(0.1), None,
                                        None)
     assert st == _lib.PA_ERR_INVALID_ARG
