@@ -93,12 +93,13 @@ size_t pa_splitkv_workspace_bytes(const pa_shape *shape, int32_t num_splits) {
 
 int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count) {
   if (check_shape(shape, true) != PA_OK || sm_count <= 0) return 1;
-  // resident split workers: CTAs per SM by shared memory (228 KB per SM, 1 KB
-  // reserved per CTA), capped by the 2048-thread limit, times warps per CTA
+  // resident split workers: CTAs per SM by shared memory (227 KB usable per SM,
+  // 1 KB reserved per CTA), capped by what the kernel's register budget was
+  // compiled for, times warps per CTA
   const int per_cta = pa::splitkv_smem_bytes(*shape) + 1024;
   const int warps = pa::decode_warps_per_cta();
-  int ctas = (228 * 1024) / per_cta;
-  if (ctas > 2048 / (32 * warps)) ctas = 2048 / (32 * warps);
+  int ctas = (227 * 1024) / per_cta;
+  if (ctas > pa::splitkv_min_blocks(*shape)) ctas = pa::splitkv_min_blocks(*shape);
   if (ctas < 1) ctas = 1;
   const int64_t n = static_cast<int64_t>(sm_count) * ctas * warps;
   return static_cast<int32_t>(n > kMaxSplits ? kMaxSplits : n);

@@ -15,6 +15,8 @@ namespace pa {
 __global__ void __launch_bounds__(128) cache_write_bf16_kernel(
     const uint4 *k_new, const uint4 *v_new, uint4 *k_pool, uint4 *v_pool,
     const int64_t *slot_mapping, int bs, int nblocks, int row16, int32_t *err) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const int64_t slot = slot_mapping[t];
   if (slot < 0) return;
@@ -36,6 +38,8 @@ __global__ void __launch_bounds__(256) cache_write_fp8_kernel(
     const uint16_t *k_new, const uint16_t *v_new, uint8_t *k_pool, uint8_t *v_pool,
     float *k_scale, float *v_scale, const int64_t *slot_mapping, int T, int Hkv, int bs,
     int nblocks, int32_t *err) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int D = 128;
   const int t = blockIdx.x;
   const int64_t slot = slot_mapping[t];
@@ -102,19 +106,20 @@ __global__ void __launch_bounds__(256) cache_write_fp8_kernel(
 pa_status run_reshape_and_cache(const pa_shape &s, const void *k_new, const void *v_new,
                                 void *k_pool, void *v_pool, float *k_scale, float *v_scale,
                                 const int64_t *slot_mapping, int32_t *err, cudaStream_t stream) {
+  cudaError_t e;
   if (s.kv_dtype == PA_KV_FP8_E4M3) {
-    cache_write_fp8_kernel<<<s.B, 256, 0, stream>>>(
-        static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
-        static_cast<uint8_t *>(k_pool), static_cast<uint8_t *>(v_pool), k_scale, v_scale,
-        slot_mapping, s.B, s.Hkv, s.block_size, s.nblocks, err);
+    e = launch_pdl(cache_write_fp8_kernel, dim3(s.B), dim3(256), 0, stream,
+                   static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
+                   static_cast<uint8_t *>(k_pool), static_cast<uint8_t *>(v_pool), k_scale,
+                   v_scale, slot_mapping, s.B, s.Hkv, s.block_size, s.nblocks, err);
   } else {
     const int row16 = s.Hkv * s.D * 2 / 16;
-    cache_write_bf16_kernel<<<s.B, 128, 0, stream>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
-        static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), slot_mapping,
-        s.block_size, s.nblocks, row16, err);
+    e = launch_pdl(cache_write_bf16_kernel, dim3(s.B), dim3(128), 0, stream,
+                   static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+                   static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), slot_mapping,
+                   s.block_size, s.nblocks, row16, err);
   }
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa

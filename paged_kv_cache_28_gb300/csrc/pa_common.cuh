@@ -99,6 +99,18 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Wait until the grid this one depends on (the previous kernel in the stream) has
+// completed and its writes are visible.  Returns at once when there is none.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel in the stream be scheduled before this grid finishes.  The
+// next kernel still runs pdl_wait() before it touches anything this grid touches.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ fragments
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {

@@ -59,6 +59,10 @@ struct Cfg {
   static constexpr int THREADS = WARPS * 32;
   static constexpr int META_BYTES = 32;     // int4 unit + k/v scale
   static constexpr int SMEM = 1024 + WARPS * STAGES * (STAGE_BYTES + 8 + META_BYTES);
+  // CTAs per SM that shared memory allows (227 KB usable, 1 KB reserved per CTA, 4 KB
+  // left for the split kernel's length scan); the register budget is held to it
+  static constexpr int MIN_BLOCKS_RAW = (227 * 1024) / (SMEM + 1024 + 4096);
+  static constexpr int MIN_BLOCKS = MIN_BLOCKS_RAW < 1 ? 1 : (MIN_BLOCKS_RAW > 4 ? 4 : MIN_BLOCKS_RAW);
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(KV_BYTES % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
 };
@@ -259,12 +263,12 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
         hi = pack_bf16(p0, p1);
         lo = pack_bf16(p0 - bf16_lo(hi), p1 - bf16_hi(hi));
       } else {
+        // f16 keeps 11 significant bits of p: one term is enough for the FP8 tolerance
         hi = pack_f16(p0, p1);
-        const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
-        lo = pack_f16(p0 - hf.x, p1 - hf.y);
+        lo = 0;
       }
       bh[nt][h] = movmatrix_trans(hi);
-      bl[nt][h] = movmatrix_trans(lo);
+      if constexpr (!C::FP8) bl[nt][h] = movmatrix_trans(lo);
     }
   }
 
@@ -282,10 +286,12 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
       const int c = ((dt & 3) << 1) + ((lane >> 3) & 1);
       uint32_t a[4];
       ldsm_x4_trans(a, vtile + (dt >> 2) * (kTile * 128) + t * 128 + ((c ^ (t & 7)) << 4));
-      a[0] &= m01;
-      a[1] &= m01;
-      a[2] &= m23;
-      a[3] &= m23;
+      if (nvalid < kTile) {
+        a[0] &= m01;
+        a[1] &= m01;
+        a[2] &= m23;
+        a[3] &= m23;
+      }
 #pragma unroll
       for (int nt = 0; nt < C::NT; ++nt) {
         mma_bf16(st.acc[nt][dt], a, bh[nt][0], bh[nt][1]);
@@ -309,15 +315,14 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
                          e4m3x2_to_f16x2(__byte_perm(lo8, 0, 0x4431)),
                          e4m3x2_to_f16x2(__byte_perm(hi8, 0, 0x4420)),
                          e4m3x2_to_f16x2(__byte_perm(hi8, 0, 0x4431))};
-        a[0] &= m01;
-        a[1] &= m01;
-        a[2] &= m23;
-        a[3] &= m23;
-#pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt) {
-          mma_f16(st.acc[nt][2 * cc + hh], a, bh[nt][0], bh[nt][1]);
-          mma_f16(st.acc[nt][2 * cc + hh], a, bl[nt][0], bl[nt][1]);
+        if (nvalid < kTile) {
+          a[0] &= m01;
+          a[1] &= m01;
+          a[2] &= m23;
+          a[3] &= m23;
         }
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) mma_f16(st.acc[nt][2 * cc + hh], a, bh[nt][0], bh[nt][1]);
       }
     }
   }
@@ -511,7 +516,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, ok);
 }
 
-// Runs all units of `src` through the warp's ring.  on_piece_end(u, first_tile, st)
+// Runs all units of `src` (already init()ed) through the warp's ring.  on_piece_end(u, first_tile, st)
 // is called after the last tile of every piece.  Returns false after a wait timeout.
 template <class C, class Src, class OnEnd>
 __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> &st,
@@ -519,7 +524,6 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
                                          const CUtensorMap *tmV, OnEnd &&on_piece_end,
                                          int lane) {
   const int n = src.count();
-  src.init(lane);
 #pragma unroll
   for (int s = 0; s < C::STAGES; ++s)
     if (s < n) issue<C>(ws, s, src.get(s, lane), p, tmK, tmV, lane);
@@ -600,7 +604,7 @@ __host__ __device__ constexpr int split_smem(int B) {
 // ----------------------------------------------------------------------------
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS)
+__global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -628,6 +632,7 @@ __global__ void __launch_bounds__(C::THREADS)
   src.nw = C::WARPS;
   src.bs = p.bs;
   src.nblocks = p.nblocks;
+  src.init(lane);
   run_warp<C>(src, ws, st, p, &tmK, &tmV, [](int4, int, State<C> &) {}, lane);
 
   // ---- merge the warps' states: warp w leaves m, l, acc (in absolute units)
@@ -730,17 +735,16 @@ __device__ void scan_lengths(const Params &p, int32_t *prefix, uint8_t *lastn) {
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS)
+__global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     decode_segment_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   WarpSmem ws = setup_smem<C>(smem_raw, warp, p.G, lane);
   int32_t *prefix = reinterpret_cast<int32_t *>(split_tail<C>(smem_raw));
   uint8_t *lastn = reinterpret_cast<uint8_t *>(prefix + p.B + 1);
   scan_lengths<C::THREADS>(p, prefix, lastn);
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i <= p.B; i += C::THREADS) p.prefix_out[i] = prefix[i];
   const int seg = blockIdx.x * C::WARPS + warp;
   const int total = prefix[p.B];
   const int W = max(1, (total + p.num_splits - 1) / p.num_splits);
@@ -756,6 +760,13 @@ __global__ void __launch_bounds__(C::THREADS)
   src.max_blocks = p.max_blocks;
   src.begin = min(seg * W, total);
   src.end = (seg < p.num_splits) ? min(src.begin + W, total) : src.begin;
+  src.init(lane);
+  // everything above reads only caller inputs (lengths, block tables); the pools
+  // (written by the cache write) and the workspace (read by the previous merge)
+  // are touched only after the previous grid has finished
+  pdl_wait();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= p.B; i += C::THREADS) p.prefix_out[i] = prefix[i];
   State<C> st;
   st.reset();
   run_warp<C>(
@@ -780,6 +791,8 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
                                                     const float *o_part, const float *lse_part,
                                                     int B, int Hq, int Hkv, int G, int D,
                                                     int num_splits) {
+  pdl_trigger();
+  pdl_wait();
   const int pair = blockIdx.x;
   const int b = pair / Hkv, kvh = pair - b * Hkv;
   const int start_b = prefix[b];
@@ -870,15 +883,23 @@ static bool make_pool_map(CUtensorMap *map, const void *pool, const pa_shape &s)
   CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                   const_cast<void *>(pool), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  // promote L2 fills to one head row: 256 B for bf16 D = 128, else 128 B
+                  // (a wider fill would pull in the neighbouring KV head's row)
+                  s.D * eb >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                  : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 // Opt the kernel in to the dynamic shared memory it needs (per call: cheap, and
 // correct whichever device is current).
-template <class C, class K>
-static cudaError_t prep_kernel(K kernel) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+template <class K>
+static cudaError_t prep_kernel(K kernel, int smem) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
 }
 
 static Params make_params(const pa_shape &s, float *out, const void *q, const float *k_scale,
@@ -906,7 +927,7 @@ static Params make_params(const pa_shape &s, float *out, const void *q, const fl
 template <class C>
 static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
                              cudaStream_t stream) {
-  if (prep_kernel<C>(decode_pair_kernel<C>) != cudaSuccess) return PA_ERR_CUDA;
+  if (prep_kernel(decode_pair_kernel<C>, C::SMEM) != cudaSuccess) return PA_ERR_CUDA;
   decode_pair_kernel<C><<<p.B * p.Hkv, C::THREADS, C::SMEM, stream>>>(mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -915,12 +936,12 @@ template <class C>
 static pa_status launch_segments(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
                                  cudaStream_t stream) {
   const int smem = split_smem<C>(p.B);
-  if (cudaFuncSetAttribute(decode_segment_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem) != cudaSuccess)
-    return PA_ERR_CUDA;
+  if (prep_kernel(decode_segment_kernel<C>, smem) != cudaSuccess) return PA_ERR_CUDA;
   const int grid = (p.num_splits + C::WARPS - 1) / C::WARPS;
-  decode_segment_kernel<C><<<grid, C::THREADS, smem, stream>>>(mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return launch_pdl(decode_segment_kernel<C>, dim3(grid), dim3(C::THREADS), smem, stream, mk, mv,
+                    p) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 // Dispatch on (D, n-tiles, dtype).
@@ -963,6 +984,14 @@ int splitkv_smem_bytes(const pa_shape &s) {
 }
 
 int decode_warps_per_cta() { return Cfg<128, 1, false>::WARPS; }
+
+int splitkv_min_blocks(const pa_shape &s) {
+  const int nt = (s.Hq / s.Hkv + 7) / 8;
+  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
+  if (fp8) return nt == 1 ? Cfg<128, 1, true>::MIN_BLOCKS : Cfg<128, 2, true>::MIN_BLOCKS;
+  if (s.D == 64) return nt == 1 ? Cfg<64, 1, false>::MIN_BLOCKS : Cfg<64, 2, false>::MIN_BLOCKS;
+  return nt == 1 ? Cfg<128, 1, false>::MIN_BLOCKS : Cfg<128, 2, false>::MIN_BLOCKS;
+}
 
 WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits) {
   WorkspaceLayout w{};
@@ -1008,11 +1037,13 @@ pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int nu
   const uint8_t *ws = static_cast<const uint8_t *>(workspace);
   const int G = s.Hq / s.Hkv;
   const int threads = min(256, max(32, ((G * s.D / 4) + 31) / 32 * 32));
-  merge_kernel<<<s.B * s.Hkv, threads, 0, stream>>>(
-      out, reinterpret_cast<const int32_t *>(ws + w.prefix),
-      reinterpret_cast<const float *>(ws + w.o_part), reinterpret_cast<const float *>(ws + w.lse),
-      s.B, s.Hq, s.Hkv, G, s.D, num_splits);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return launch_pdl(merge_kernel, dim3(s.B * s.Hkv), dim3(threads), 0, stream, out,
+                    reinterpret_cast<const int32_t *>(ws + w.prefix),
+                    reinterpret_cast<const float *>(ws + w.o_part),
+                    reinterpret_cast<const float *>(ws + w.lse), s.B, s.Hq, s.Hkv, G, s.D,
+                    num_splits) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 }  // namespace pa

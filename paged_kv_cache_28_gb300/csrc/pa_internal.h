@@ -6,9 +6,30 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pa.h"
 
 namespace pa {
+
+// Launch `kernel` on `stream` so that it may start before the previous kernel in the
+// stream has finished (programmatic dependent launch); every kernel launched this
+// way calls pdl_wait() before it reads or writes memory an earlier kernel may use.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Byte offsets of the split-KV workspace regions (each 256-byte aligned):
 //   prefix  int32 [B + 1]        tile-count prefix over sequences (x Hkv)
@@ -24,6 +45,8 @@ constexpr int kMaxSplitBatch = 16384;
 WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits);
 int splitkv_smem_bytes(const pa_shape &s);
 int decode_warps_per_cta();
+// CTAs per SM the split kernel is compiled for (registers capped accordingly).
+int splitkv_min_blocks(const pa_shape &s);
 
 pa_status run_reshape_and_cache(const pa_shape &s, const void *k_new, const void *v_new,
                                 void *k_pool, void *v_pool, float *k_scale, float *v_scale,
