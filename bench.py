@@ -215,7 +215,8 @@ def run_ours(args):
             ev[i][0].record(stream)
         _lib.pa_decode_splitkv(dev.shape, dev.out, dev.workspace, ns, dev.q, dev.k_pool,
                                dev.v_pool, dev.k_scale, dev.v_scale, dev.block_tables,
-                               dev.seq_lens, batch.sm_scale, dev.err, stream)
+                               dev.seq_lens, batch.sm_scale, dev.err, stream,
+                               dev.shared_prefix_lens)
         if i is not None:
             ev[i][1].record(stream)
         _lib.pa_merge_lse(dev.shape, dev.out, dev.workspace, ns, stream)

@@ -168,6 +168,14 @@ int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count);
  * workspace: device memory of at least pa_splitkv_workspace_bytes(shape,
  * num_splits) bytes, 256-byte aligned, owned by the caller, not shared with
  * concurrent calls; nothing in it needs initialising.  1 <= num_splits <= 65536.
+ *
+ * shared_prefix_lens (optional, [B] int32, may be NULL) is a speed hint for
+ * batches with prefix sharing ("appendonly", "Prefix sharing is where the real
+ * win lives"): the number of leading tokens of sequence b that lie in blocks
+ * other sequences of the batch also reference.  Whole 16-token tiles inside
+ * that prefix are fetched with an L2 evict-last policy and all other tiles with
+ * evict-first, so a shared block stays in L2 for its other readers.  Any value
+ * gives the same result, bit for bit.
  * Batches of more than 16384 sequences return PA_ERR_UNSUPPORTED (each CTA
  * scans the sequence lengths in shared memory).
  */
@@ -175,8 +183,8 @@ pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
                             size_t workspace_bytes, int32_t num_splits, const void *q,
                             const void *k_pool, const void *v_pool, const float *k_scale,
                             const float *v_scale, const int32_t *block_tables,
-                            const int32_t *seq_lens, float sm_scale, int32_t *err_flag,
-                            pa_stream_t stream);
+                            const int32_t *seq_lens, const int32_t *shared_prefix_lens,
+                            float sm_scale, int32_t *err_flag, pa_stream_t stream);
 
 /*
  * pa_merge_lse -- log-sum-exp merge of the split partials left by

@@ -55,8 +55,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "pa_decode": (I32, [S, P, P, P, P, P, P, P, P, F, P, P]),
             "pa_splitkv_workspace_bytes": (ctypes.c_size_t, [S, I32]),
             "pa_default_num_splits": (I32, [S, I32]),
-            "pa_decode_splitkv": (I32, [S, P, P, ctypes.c_size_t, I32, P, P, P, P, P, P, P, F,
-                                        P, P]),
+            "pa_decode_splitkv": (I32, [S, P, P, ctypes.c_size_t, I32, P, P, P, P, P, P, P, P,
+                                        F, P, P]),
             "pa_merge_lse": (I32, [S, P, P, I32, P]),
             "pa_status_string": (ctypes.c_char_p, [I32]),
             "pa_read_error_flag": (I32, [P, ctypes.POINTER(I32), P]),
@@ -139,13 +139,14 @@ def pa_default_num_splits(shape: pa_shape, sm_count: int) -> int:
 
 def pa_decode_splitkv(shape: pa_shape, out, workspace, num_splits: int, q, k_pool, v_pool,
                       k_scale, v_scale, block_tables, seq_lens, sm_scale: float, err_flag=None,
-                      stream=None) -> None:
+                      stream=None, shared_prefix_lens=None) -> None:
     lib = load()
     nbytes = workspace.numel() * workspace.element_size()
     _check("pa_decode_splitkv", lib.pa_decode_splitkv(
         ctypes.byref(shape), _ptr(out), _ptr(workspace), nbytes, int(num_splits), _ptr(q),
         _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
-        _ptr(seq_lens), float(sm_scale), _ptr(err_flag), _stream(stream)))
+        _ptr(seq_lens), _ptr(shared_prefix_lens), float(sm_scale), _ptr(err_flag),
+        _stream(stream)))
 
 
 def pa_merge_lse(shape: pa_shape, out, workspace, num_splits: int, stream=None) -> None:

@@ -109,8 +109,8 @@ pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
                             size_t workspace_bytes, int32_t num_splits, const void *q,
                             const void *k_pool, const void *v_pool, const float *k_scale,
                             const float *v_scale, const int32_t *block_tables,
-                            const int32_t *seq_lens, float sm_scale, int32_t *err_flag,
-                            pa_stream_t stream) {
+                            const int32_t *seq_lens, const int32_t *shared_prefix_lens,
+                            float sm_scale, int32_t *err_flag, pa_stream_t stream) {
   if (!shape) return PA_ERR_INVALID_ARG;
   if (shape->B == 0) return check_shape(shape, true);
   pa_status st = check_decode_args(shape, out, q, k_pool, v_pool, k_scale, v_scale,
@@ -120,9 +120,10 @@ pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
   if (shape->B > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
   if (workspace_bytes < pa::splitkv_layout(*shape, num_splits).total) return PA_ERR_INVALID_ARG;
+  if (shared_prefix_lens && !aligned16(shared_prefix_lens)) return PA_ERR_INVALID_ARG;
   return pa::run_decode_splitkv(*shape, out, workspace, num_splits, q, k_pool, v_pool, k_scale,
-                                v_scale, block_tables, seq_lens, sm_scale, err_flag,
-                                reinterpret_cast<cudaStream_t>(stream));
+                                v_scale, block_tables, seq_lens, shared_prefix_lens, sm_scale,
+                                err_flag, reinterpret_cast<cudaStream_t>(stream));
 }
 
 pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,

@@ -22,6 +22,8 @@ constexpr int kFirstOfPair = 1 << 8;
 constexpr int kLastOfPair = 1 << 9;
 constexpr int kPieceStart = 1 << 10;
 constexpr int kPieceEnd = 1 << 11;
+constexpr int kHintShared = 1 << 12;   // tile lies in a prefix other sequences share
+constexpr int kHintPrivate = 1 << 13;  // tile is private (hints given, not shared)
 constexpr int kInvalidPhys = -1;
 
 __device__ __forceinline__ void set_err(int32_t *flag, int bits) {
@@ -76,6 +78,29 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// The same with an L2 eviction-priority policy (from make_l2_policy) for the box.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, int x,
+                                                 int y, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// L2 policies: keep a line as long as possible (data many readers will reuse) or
+// evict it first (data read once).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // Plain bulk copy global -> shared (16-byte aligned, size multiple of 16).

@@ -74,6 +74,7 @@ struct Params {
   const float *v_scale;
   const int32_t *block_tables;
   const int32_t *seq_lens;
+  const int32_t *shared_prefix_lens;   // optional L2 hint per sequence (split kernel)
   int32_t *err;
   int B, Hq, Hkv, G, bs, nblocks, max_blocks;
   float sl2;  // sm_scale * log2(e)
@@ -418,6 +419,7 @@ struct SegmentSource {
   const int32_t *prefix;     // shared: [B + 1]
   const uint8_t *lastn;      // shared: [B] valid tokens in each sequence's last tile
   const int32_t *block_tables;
+  const int32_t *shared_prefix_lens;   // may be null
   int32_t *err;
   int B, Hkv, bs, nblocks, max_blocks;
   int begin, end;
@@ -447,6 +449,8 @@ struct SegmentSource {
     if (tile == nt - 1) info |= kLastOfPair | kPieceEnd;
     if (i == 0) info |= kPieceStart;
     if (f == end - 1) info |= kPieceEnd;
+    if (shared_prefix_lens)
+      info |= ((tile + 1) * kTile <= __ldg(shared_prefix_lens + b)) ? kHintShared : kHintPrivate;
     return make_int4(phys, b * Hkv + kvh, tile, info);
   }
   __device__ __forceinline__ void init(int lane) {
@@ -500,11 +504,21 @@ __device__ __forceinline__ void issue(const WarpSmem &ws, int s, int4 u, const P
   const uint32_t dst = smem_u32(stage);
   fence_proxy_async();
   mbar_arrive_expect_tx(bar, bytes);
+  if (u.w & (kHintShared | kHintPrivate)) {
+    const uint64_t pol = (u.w & kHintShared) ? l2_policy_evict_last() : l2_policy_evict_first();
 #pragma unroll
-  for (int h = 0; h < C::HALVES; ++h) {
-    const int x = kvh * C::D + h * C::BOX_X;
-    tma_load_2d(dst + h * (kTile * 128), tmK, x, y, bar);
-    tma_load_2d(dst + C::KV_BYTES + h * (kTile * 128), tmV, x, y, bar);
+    for (int h = 0; h < C::HALVES; ++h) {
+      const int x = kvh * C::D + h * C::BOX_X;
+      tma_load_2d_hint(dst + h * (kTile * 128), tmK, x, y, bar, pol);
+      tma_load_2d_hint(dst + C::KV_BYTES + h * (kTile * 128), tmV, x, y, bar, pol);
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < C::HALVES; ++h) {
+      const int x = kvh * C::D + h * C::BOX_X;
+      tma_load_2d(dst + h * (kTile * 128), tmK, x, y, bar);
+      tma_load_2d(dst + C::KV_BYTES + h * (kTile * 128), tmV, x, y, bar);
+    }
   }
   if (with_q)
     bulk_load(dst + 2 * C::KV_BYTES, p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D,
@@ -752,6 +766,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.prefix = prefix;
   src.lastn = lastn;
   src.block_tables = p.block_tables;
+  src.shared_prefix_lens = p.shared_prefix_lens;
   src.err = p.err;
   src.B = p.B;
   src.Hkv = p.Hkv;
@@ -1017,13 +1032,14 @@ pa_status run_decode(const pa_shape &s, float *out, const void *q, const void *k
 pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int num_splits,
                              const void *q, const void *k_pool, const void *v_pool,
                              const float *k_scale, const float *v_scale, const int32_t *bt,
-                             const int32_t *sl, float sm_scale, int32_t *err,
-                             cudaStream_t stream) {
+                             const int32_t *sl, const int32_t *shared_prefix_lens, float sm_scale,
+                             int32_t *err, cudaStream_t stream) {
   const WorkspaceLayout w = splitkv_layout(s, num_splits);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   CUtensorMap mk, mv;
   if (!make_pool_map(&mk, k_pool, s) || !make_pool_map(&mv, v_pool, s)) return PA_ERR_CUDA;
   Params p = make_params(s, out, q, k_scale, v_scale, bt, sl, sm_scale, err);
+  p.shared_prefix_lens = shared_prefix_lens;
   p.prefix_out = reinterpret_cast<int32_t *>(ws + w.prefix);
   p.lse_part = reinterpret_cast<float *>(ws + w.lse);
   p.o_part = reinterpret_cast<float *>(ws + w.o_part);

@@ -35,6 +35,8 @@ class DeviceBatch:
         self.block_tables = torch.from_numpy(batch.block_tables).to(self.device)
         self.seq_lens = torch.from_numpy(batch.seq_lens).to(self.device)
         self.slot_mapping = torch.from_numpy(batch.slot_mapping).to(self.device)
+        self.shared_prefix_lens = (None if batch.shared_prefix_lens is None else
+                                   torch.from_numpy(batch.shared_prefix_lens).to(self.device))
         if pools is not None:
             self.k_pool, self.v_pool, self.k_scale, self.v_scale = pools
         elif fp8:
@@ -72,7 +74,8 @@ class DeviceBatch:
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
         self.num_splits = num_splits
 
-    def decode_splitkv(self, num_splits: int | None = None, stream=None):
+    def decode_splitkv(self, num_splits: int | None = None, stream=None, hints: bool = True):
+        """Split-KV decode + merge; hints: pass the batch's shared-prefix lengths (if any)."""
         if num_splits is None:
             num_splits = default_num_splits(self.shape, self.device)
         if self.workspace is None or self.num_splits != num_splits:
@@ -80,7 +83,7 @@ class DeviceBatch:
         _lib.pa_decode_splitkv(self.shape, self.out, self.workspace, num_splits, self.q,
                                self.k_pool, self.v_pool, self.k_scale, self.v_scale,
                                self.block_tables, self.seq_lens, self.batch.sm_scale, self.err,
-                               stream)
+                               stream, self.shared_prefix_lens if hints else None)
         _lib.pa_merge_lse(self.shape, self.out, self.workspace, num_splits, stream)
 
     def read_err(self, stream=None) -> int:

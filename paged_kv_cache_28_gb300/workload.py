@@ -85,6 +85,7 @@ class Batch:
     v_scale: np.ndarray | None
     sm_scale: float
     seed: int
+    shared_prefix_lens: np.ndarray | None = None   # int32 [B]: tokens in blocks shared with others
 
     @property
     def elem_bytes(self) -> int:
@@ -250,11 +251,17 @@ def build_batch(name: str, seq_lens, *, Hq: int, Hkv: int, D: int, block_size: i
                 v_scale[dst] = v_scale[src]
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
+    shared = None
+    if prefix_groups:
+        shared = np.zeros(B, dtype=np.int32)
+        for plen, seqs in prefix_groups:
+            for b in seqs:
+                shared[b] = (plen // bs) * bs        # the copied tail block is private
     return Batch(name=name, B=B, Hq=Hq, Hkv=Hkv, D=D, block_size=bs, nblocks=nblocks,
                  max_blocks=max_blocks, kv_dtype=kv_dtype, seq_lens=seq_lens,
                  block_tables=tables, slot_mapping=slot, q=q, k_new=k_new, v_new=v_new,
                  k_pool=k_pool, v_pool=v_pool, k_scale=k_scale, v_scale=v_scale,
-                 sm_scale=float(sm_scale), seed=seed)
+                 sm_scale=float(sm_scale), seed=seed, shared_prefix_lens=shared)
 
 
 def lognormal_lens(rng, n: int, median: float, lo: int, hi: int) -> np.ndarray:

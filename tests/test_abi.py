@@ -95,11 +95,15 @@ def test_splitkv_host_checks(lib):
     assert _lib.pa_splitkv_workspace_bytes(s, 0) == 0
     assert _lib.pa_splitkv_workspace_bytes(s, 70000) == 0
     args = [ctypes.byref(s), FAKE, FAKE, nbytes - 1, 1216, FAKE, FAKE, FAKE, None, None, FAKE,
-            FAKE, 0.1, None, None]
+            FAKE, None, 0.1, None, None]
     assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # workspace too small
     args[3] = nbytes
     args[2] = FAKE + 16
     assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # workspace not 256-aligned
+    args[2] = FAKE
+    args[12] = FAKE + 4
+    assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # hint array misaligned
+    args[12] = None
     assert lib.pa_merge_lse(ctypes.byref(s), FAKE, FAKE, 0, None) == _lib.PA_ERR_INVALID_ARG
     big = _lib.make_shape(16385, 8, 8, 128, 16, 30000, 4)
     args[0] = ctypes.byref(big)

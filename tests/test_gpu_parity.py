@@ -292,6 +292,32 @@ def test_shared_vs_duplicated_prefix_bitwise():
         assert np.array_equal(_bits(a), _bits(b))
 
 
+def test_shared_prefix_hint_changes_nothing_bitwise():
+    groups = ((900, list(range(12))), (3000, [12, 13, 14]))
+    lens = [950, 2000, 901, 1500, 3000, 905, 1000, 2500, 4000, 999, 1200, 960, 3100, 5000, 3001]
+    batch = wl.build_batch("t", lens, Hq=64, Hkv=8, D=128, block_size=16, seed=40,
+                           prefix_groups=groups)
+    assert batch.shared_prefix_lens is not None
+    dev = DeviceBatch(batch)
+    ref, _ = oracle_after_write(batch, write=False)
+    outs = []
+    for hints in (False, True):
+        dev.out.fill_(float("nan"))
+        dev.decode_splitkv(23, hints=hints)
+        torch.cuda.synchronize()
+        outs.append(dev.out.cpu().numpy())
+        assert_close(outs[-1], ref, batch, f"hints={hints}")
+    assert np.array_equal(_bits(outs[0]), _bits(outs[1]))
+    # any hint values (here: random, including past the end) give the same bits
+    dev.shared_prefix_lens = torch.from_numpy(
+        np.random.default_rng(1).integers(0, 6000, batch.B).astype(np.int32)).cuda()
+    dev.out.fill_(float("nan"))
+    dev.decode_splitkv(23)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(dev.out.cpu().numpy()), _bits(outs[0]))
+    assert dev.read_err() == 0
+
+
 def test_zero_query_gives_mean_of_v():
     batch = wl.build_batch("t", [333, 16], Hq=8, Hkv=1, D=128, block_size=16, seed=34)
     batch.q[:] = 0
