@@ -33,6 +33,10 @@ paged_decode                   numpy/scipy softmax attention on contiguous
                                L=2 logistic closed form; needle; block
                                permutation and shared-vs-copied prefix
                                invariance; GQA grouping
+window_positions               the four-token window trace printed in
+                               "KV Cache Engineering", sec. 3
+paged_decode(window=W)         numpy/scipy attention over the last W rows of
+                               the contiguous K/V; W >= L equals no window
 split_partials / merge_lse     merge(split(x)) == unsplit(x) to 1e-12 for
                                random splits; one split is the identity;
                                empty splits carry no weight
@@ -100,7 +104,9 @@ def _load():
             lib.oracle_reshape_and_cache_fp8.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
             lib.oracle_paged_decode.restype = None
             lib.oracle_paged_decode.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, D,
-                                                I, P, P, P, I]
+                                                I, I, P, P, P, I]
+            lib.oracle_window_positions.restype = I
+            lib.oracle_window_positions.argtypes = [I, I, P]
             lib.oracle_split_partials.restype = None
             lib.oracle_split_partials.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, D,
                                                   I, I, I, P, P, P]
@@ -199,14 +205,22 @@ def reshape_and_cache_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, slot_m
 # decode attention
 # --------------------------------------------------------------------------
 
+def window_positions(length: int, window: int) -> list[int]:
+    lib = _load()
+    out = np.zeros(max(length, 1), dtype=np.int32)
+    n = lib.oracle_window_positions(int(length), int(window), _ptr(out))
+    return out[:n].tolist()
+
+
 def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, *, Hkv: int,
                  block_size: int, k_scale=None, v_scale=None, rows=None,
-                 nthreads: int | None = None) -> np.ndarray:
+                 nthreads: int | None = None, window: int = 0) -> np.ndarray:
     """Decode attention in fp64.
 
     q: uint16 [B, Hq, D] (bf16 bits).  Pools: uint16 (bf16) or uint8 (E4M3 codes, then
     k_scale / v_scale float32 [nblocks, Hkv] are required), shape [nblocks, bs, Hkv, D].
     rows: optional int array [n, 2] of (b, h); then the result is [n, D], else [B, Hq, D].
+    window: > 0 attends over the last `window` positions of each sequence only.
     """
     lib = _load()
     q = _c(q, np.uint16)
@@ -223,7 +237,7 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, *, 
         out = np.zeros((B, Hq, D), dtype=np.float64)
         lib.oracle_paged_decode(B, Hq, Hkv, D, block_size, bt.shape[1], int(fp8), _ptr(q),
                                 _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl),
-                                float(sm_scale), 0, None, None, _ptr(out), nthreads)
+                                float(sm_scale), int(window), 0, None, None, _ptr(out), nthreads)
         return out
     rows = np.asarray(rows, dtype=np.int32).reshape(-1, 2)
     rb = np.ascontiguousarray(rows[:, 0])
@@ -231,7 +245,7 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, *, 
     out = np.zeros((rows.shape[0], D), dtype=np.float64)
     lib.oracle_paged_decode(B, Hq, Hkv, D, block_size, bt.shape[1], int(fp8), _ptr(q), _ptr(kp),
                             _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl), float(sm_scale),
-                            rows.shape[0], _ptr(rb), _ptr(rh), _ptr(out), nthreads)
+                            int(window), rows.shape[0], _ptr(rb), _ptr(rh), _ptr(out), nthreads)
     return out
 
 

@@ -142,6 +142,21 @@ long long oracle_cached_scalars(int layers, int Hkv, long long tokens, int D)
 }
 
 /*
+ * [P3] section 3: a sliding-window layer keeps only the most recent `window`
+ * positions.  After a sequence of `len` tokens it retains positions
+ * [max(0, len - window), len); window <= 0 means no window (all positions).
+ * Writes the retained positions to out and returns how many there are.
+ */
+int oracle_window_positions(int len, int window, int *out)
+{
+    int first = (window > 0 && len > window) ? len - window : 0;
+    int t, n = 0;
+    for (t = first; t < len; t++)
+        out[n++] = t;
+    return n;
+}
+
+/*
  * [P3] section 8: absmax quantiser onto signed integer codes.
  *   scale = max|x| / largest_code, largest_code = 2^(bits-1) - 1
  *   code  = clip(rint(x / scale), -largest_code, largest_code)   (rint: ties to even)
@@ -356,7 +371,9 @@ static void attend_range(const paged_kv *p, const uint16_t *q_row, int b, int h,
  * Decode attention for a batch: out[b][h] = softmax(sm_scale * q[b,h] K_b^T) V_b
  * over the L_b = seq_lens[b] tokens of sequence b, gathered through its block
  * table ([P4] "Custom PagedAttention Kernels": grid over (sequence, head),
- * walk the block table, load K and V, scaled dot-product attention).
+ * walk the block table, load K and V, scaled dot-product attention).  With
+ * window > 0 only the positions oracle_window_positions retains are attended
+ * ([P3] section 3).
  * With rows == NULL every (b, h) is computed into out[B][Hq][D]; otherwise only
  * the nrows pairs (rows_b[i], rows_h[i]) into out[nrows][D].
  * Parallel over rows with OpenMP when nthreads > 1 (each row is independent).
@@ -365,7 +382,7 @@ void oracle_paged_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks, 
                          const uint16_t *q, const void *k_pool, const void *v_pool,
                          const float *k_scale, const float *v_scale,
                          const int32_t *block_tables, const int32_t *seq_lens,
-                         double sm_scale, int nrows, const int32_t *rows_b,
+                         double sm_scale, int window, int nrows, const int32_t *rows_b,
                          const int32_t *rows_h, double *out, int nthreads)
 {
     paged_kv p;
@@ -379,7 +396,9 @@ void oracle_paged_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks, 
         int b = rows_b ? rows_b[i] : (int)(i / Hq);
         int h = rows_b ? rows_h[i] : (int)(i % Hq);
         double lse;
-        attend_range(&p, &q[((size_t)b * Hq + h) * D], b, h, 0, seq_lens[b], sm_scale,
+        int L = seq_lens[b];
+        int first = (window > 0 && L > window) ? L - window : 0;
+        attend_range(&p, &q[((size_t)b * Hq + h) * D], b, h, first, L, sm_scale,
                      &out[(size_t)i * D], &lse);
     }
 }

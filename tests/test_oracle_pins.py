@@ -218,9 +218,10 @@ def test_fp8_write_error_bound_random():
 
 # ---------------------------------------------------------------- decode attention
 
-def _contiguous_reference(batch):
+def _contiguous_reference(batch, window=0):
     """Independent restatement: gather each sequence's K/V into contiguous
-    arrays with numpy fancy indexing and apply scipy's softmax."""
+    arrays with numpy fancy indexing and apply scipy's softmax (over the last
+    `window` rows when window > 0)."""
     B, Hq, Hkv, D, bs = batch.B, batch.Hq, batch.Hkv, batch.D, batch.block_size
     G = Hq // Hkv
     q = wl.bf16_to_float(batch.q).astype(np.float64)
@@ -238,6 +239,8 @@ def _contiguous_reference(batch):
         if L == 0:
             continue
         t = np.arange(L)
+        if window > 0:
+            t = t[-window:]
         blocks = batch.block_tables[b, t // bs]
         K = kf[blocks, t % bs]          # [L, Hkv, D]
         V = vf[blocks, t % bs]
@@ -271,6 +274,33 @@ def test_decode_fp8_vs_contiguous_numpy():
     batch = wl.build_batch("t", [3, 16, 33, 70], Hq=8, Hkv=2, D=64, block_size=16, seed=3,
                            kv_dtype="fp8_e4m3")
     assert np.allclose(_oracle(batch), _contiguous_reference(batch), rtol=1e-12, atol=1e-13)
+
+
+def test_window_positions_page_trace(golden_dir):
+    g = _golden(golden_dir, "sliding_window.json")
+    for token, want in enumerate(g["retained_after_token"]):
+        assert oracle.window_positions(token + 1, g["window"]) == want
+    assert max(len(oracle.window_positions(n, g["window"])) for n in range(1, 50)) == \
+        g["maximum_retained"]
+    assert oracle.window_positions(7, 0) == list(range(7))          # no window
+
+
+@pytest.mark.parametrize("window", [1, 4, 16, 17, 50, 1000])
+def test_decode_window_vs_contiguous_numpy(window):
+    batch = wl.build_batch("t", [1, 15, 16, 17, 40, 97, 0], Hq=8, Hkv=2, D=64, block_size=16,
+                           seed=60 + window)
+    got = _oracle(batch, window=window)
+    assert np.allclose(got, _contiguous_reference(batch, window), rtol=1e-12, atol=1e-13)
+    if window >= batch.seq_lens.max():
+        assert np.array_equal(got, _oracle(batch))
+
+
+def test_decode_window_ignores_blocks_before_it():
+    batch = wl.build_batch("t", [100, 70], Hq=8, Hkv=2, D=64, block_size=16, seed=66)
+    ref = _oracle(batch, window=20)
+    batch.block_tables[0, :4] = 10 ** 6        # blocks wholly before position 80: never read
+    batch.block_tables[1, :3] = -5             # before position 50
+    assert np.array_equal(_oracle(batch, window=20), ref)
 
 
 def test_decode_rows_subset_matches_full():
