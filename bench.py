@@ -216,7 +216,7 @@ def run_ours(args):
         _lib.pa_decode_splitkv(dev.shape, dev.out, dev.workspace, ns, dev.q, dev.k_pool,
                                dev.v_pool, dev.k_scale, dev.v_scale, dev.block_tables,
                                dev.seq_lens, batch.sm_scale, dev.err, stream,
-                               dev.shared_prefix_lens)
+                               dev.shared_prefix_lens, args.window)
         if i is not None:
             ev[i][1].record(stream)
         _lib.pa_merge_lse(dev.shape, dev.out, dev.workspace, ns, stream)
@@ -275,14 +275,14 @@ def run_ours(args):
     if dev.read_err():
         raise RuntimeError("device error flag set during the timed steps")
 
-    unique_tokens = batch.unique_kv_tokens()
+    unique_tokens = batch.unique_kv_tokens(args.window)
     kv_bytes = unique_tokens * batch.kv_bytes_per_token()
     if batch.kv_dtype == "fp8_e4m3":
         kv_bytes += sum(int(n) for n in (batch.seq_lens + batch.block_size - 1)
                         // batch.block_size) * batch.scale_bytes_per_block()
     peak, peak_kind = measured_peak_hbm()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
-    tr = TRAFFIC.get(args.config)
+    tr = TRAFFIC.get(args.config) if args.window == 0 else None
     traffic = tr["bytes"] if tr and tr.get("kernel_hash") == kernel_source_hash() else None
     result = {
         "metric": METRIC,
@@ -303,6 +303,7 @@ def run_ours(args):
             "block_size": batch.block_size, "seq_len_sum": batch.logical_tokens,
             "seq_len_max": int(batch.seq_lens.max()),
             "unique_kv_tokens": unique_tokens, "num_splits": ns,
+            "window": args.window,
             "l2": f"no flush: {kv_bytes / 1e9:.2f} GB of KV read per step >> 129 MB L2",
             "parallelism": f"replicas x{world}" if world > 1 else "single",
             "step": "pa_reshape_and_cache + pa_decode_splitkv + pa_merge_lse",
@@ -425,6 +426,8 @@ def main(argv=None):
                     choices=["tiny", "llama70b_layer", "prefix_sharing", "long_context",
                              "fp8_mixed"])
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding-window layer: attend over the last W positions (0 = all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

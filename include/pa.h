@@ -99,6 +99,28 @@ typedef struct {
 } pa_shape;
 
 /*
+ * Optional settings of a decode call (pass NULL for the defaults).
+ *   window: > 0 attends over the last `window` positions of each sequence only,
+ *     [max(0, L - window), L) -- a sliding-window layer ("KV Cache Engineering
+ *     for LLM Serving", section 3).  Block-table entries of blocks wholly before
+ *     the window are never read (they may be freed and hold any value).  0 = all.
+ *   reserved: must be 0.
+ *   shared_prefix_lens: pa_decode_splitkv only (ignored by pa_decode); optional
+ *     [B] int32 device array, a speed hint for batches with prefix sharing
+ *     ("appendonly", "Prefix sharing is where the real win lives"): the number
+ *     of leading tokens of sequence b that lie in blocks other sequences of the
+ *     batch also reference.  Whole 16-token tiles inside that prefix are
+ *     fetched with an L2 evict-last policy, all other tiles evict-first, so a
+ *     shared block stays in L2 for its other readers.  Any value gives the same
+ *     result, bit for bit.
+ */
+typedef struct {
+    int32_t window;
+    int32_t reserved;
+    const int32_t *shared_prefix_lens;
+} pa_decode_opts;
+
+/*
  * pa_reshape_and_cache -- write this step's K/V into the block pools.
  * [P4] "How Paging Works in the LLM Context" and "The Block Table Logic";
  * [P1] "Paging".  For every token t < shape->B with s = slot_mapping[t] >= 0
@@ -135,12 +157,13 @@ pa_status pa_reshape_and_cache(const pa_shape *shape, const void *k_new, const v
  *     out[b][h][:] = sum_t softmax_t(sm_scale * <q[b][h], K_b[t]>) V_b[t]
  * over t < seq_lens[b], where K_b[t] = k_pool[block_tables[b][t / bs]][t % bs]
  * [h / G] (same for V) and FP8 codes are restored as value * scale[block][kvh].
- * seq_lens[b] = 0 gives zeros.  out is fp32 [B, Hq, D].
+ * seq_lens[b] = 0 gives zeros.  out is fp32 [B, Hq, D].  opts: see pa_decode_opts.
  */
 pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void *k_pool,
                     const void *v_pool, const float *k_scale, const float *v_scale,
-                    const int32_t *block_tables, const int32_t *seq_lens, float sm_scale,
-                    int32_t *err_flag, pa_stream_t stream);
+                    const int32_t *block_tables, const int32_t *seq_lens,
+                    const pa_decode_opts *opts, float sm_scale, int32_t *err_flag,
+                    pa_stream_t stream);
 
 /*
  * Bytes of device workspace pa_decode_splitkv / pa_merge_lse need for this
@@ -168,14 +191,8 @@ int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count);
  * workspace: device memory of at least pa_splitkv_workspace_bytes(shape,
  * num_splits) bytes, 256-byte aligned, owned by the caller, not shared with
  * concurrent calls; nothing in it needs initialising.  1 <= num_splits <= 65536.
- *
- * shared_prefix_lens (optional, [B] int32, may be NULL) is a speed hint for
- * batches with prefix sharing ("appendonly", "Prefix sharing is where the real
- * win lives"): the number of leading tokens of sequence b that lie in blocks
- * other sequences of the batch also reference.  Whole 16-token tiles inside
- * that prefix are fetched with an L2 evict-last policy and all other tiles with
- * evict-first, so a shared block stays in L2 for its other readers.  Any value
- * gives the same result, bit for bit.
+ * opts (may be NULL): the window and the shared-prefix L2 hint, see
+ * pa_decode_opts; with a window the partition runs over the attended tiles only.
  * Batches of more than 16384 sequences return PA_ERR_UNSUPPORTED (each CTA
  * scans the sequence lengths in shared memory).
  */
@@ -183,7 +200,7 @@ pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
                             size_t workspace_bytes, int32_t num_splits, const void *q,
                             const void *k_pool, const void *v_pool, const float *k_scale,
                             const float *v_scale, const int32_t *block_tables,
-                            const int32_t *seq_lens, const int32_t *shared_prefix_lens,
+                            const int32_t *seq_lens, const pa_decode_opts *opts,
                             float sm_scale, int32_t *err_flag, pa_stream_t stream);
 
 /*
@@ -209,8 +226,8 @@ pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,
  * PA_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library: every GPU that
  * loads libpa.so holds that array until the process exits.  The call allocates
  * nothing and frees nothing.  Arguments and results are those of
- * pa_decode_splitkv + pa_merge_lse: out [B, Hq, D] is complete when the work
- * enqueued on `stream` has finished.
+ * pa_decode_splitkv (with opts = NULL: full attention, no hint) + pa_merge_lse:
+ * out [B, Hq, D] is complete when the work enqueued on `stream` has finished.
  *
  * Limits and sharing:
  *   - returns PA_ERR_INVALID_ARG (launching nothing) when

@@ -31,6 +31,18 @@ class pa_shape(ctypes.Structure):
                 ("kv_dtype", ctypes.c_int32)]
 
 
+class pa_decode_opts(ctypes.Structure):
+    _fields_ = [("window", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("shared_prefix_lens", ctypes.c_void_p)]
+
+
+def _opts(window: int = 0, shared_prefix_lens=None):
+    """A pa_decode_opts by reference, or None when every setting is the default."""
+    if not window and shared_prefix_lens is None:
+        return None
+    return ctypes.byref(pa_decode_opts(int(window), 0, _ptr(shared_prefix_lens)))
+
+
 class PAError(RuntimeError):
     def __init__(self, fn: str, status: int, detail: str = ""):
         self.status = status
@@ -52,7 +64,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         S = ctypes.POINTER(pa_shape)
         sig = {
             "pa_reshape_and_cache": (I32, [S, P, P, P, P, P, P, P, P, P]),
-            "pa_decode": (I32, [S, P, P, P, P, P, P, P, P, F, P, P]),
+            "pa_decode": (I32, [S, P, P, P, P, P, P, P, P, P, F, P, P]),
             "pa_splitkv_workspace_bytes": (ctypes.c_size_t, [S, I32]),
             "pa_default_num_splits": (I32, [S, I32]),
             "pa_decode_splitkv": (I32, [S, P, P, ctypes.c_size_t, I32, P, P, P, P, P, P, P, P,
@@ -121,12 +133,12 @@ def pa_reshape_and_cache(shape: pa_shape, k_new, v_new, k_pool, v_pool, k_scale,
 
 
 def pa_decode(shape: pa_shape, out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
-              seq_lens, sm_scale: float, err_flag=None, stream=None) -> None:
+              seq_lens, sm_scale: float, err_flag=None, stream=None, window: int = 0) -> None:
     lib = load()
     _check("pa_decode", lib.pa_decode(
         ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
-        _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), float(sm_scale), _ptr(err_flag),
-        _stream(stream)))
+        _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), _opts(window), float(sm_scale),
+        _ptr(err_flag), _stream(stream)))
 
 
 def pa_splitkv_workspace_bytes(shape: pa_shape, num_splits: int) -> int:
@@ -139,13 +151,13 @@ def pa_default_num_splits(shape: pa_shape, sm_count: int) -> int:
 
 def pa_decode_splitkv(shape: pa_shape, out, workspace, num_splits: int, q, k_pool, v_pool,
                       k_scale, v_scale, block_tables, seq_lens, sm_scale: float, err_flag=None,
-                      stream=None, shared_prefix_lens=None) -> None:
+                      stream=None, shared_prefix_lens=None, window: int = 0) -> None:
     lib = load()
     nbytes = workspace.numel() * workspace.element_size()
     _check("pa_decode_splitkv", lib.pa_decode_splitkv(
         ctypes.byref(shape), _ptr(out), _ptr(workspace), nbytes, int(num_splits), _ptr(q),
         _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
-        _ptr(seq_lens), _ptr(shared_prefix_lens), float(sm_scale), _ptr(err_flag),
+        _ptr(seq_lens), _opts(window, shared_prefix_lens), float(sm_scale), _ptr(err_flag),
         _stream(stream)))
 
 

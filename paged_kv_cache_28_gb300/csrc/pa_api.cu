@@ -44,12 +44,17 @@ pa_status check_ptrs(std::initializer_list<const void *> ptrs) {
 
 pa_status check_decode_args(const pa_shape *shape, const float *out, const void *q,
                             const void *k_pool, const void *v_pool, const float *k_scale,
-                            const float *v_scale, const int32_t *bt, const int32_t *sl) {
+                            const float *v_scale, const int32_t *bt, const int32_t *sl,
+                            const pa_decode_opts *opts) {
   pa_status st = check_shape(shape, true);
   if (st != PA_OK) return st;
   st = check_ptrs({out, q, k_pool, v_pool, bt, sl});
   if (st != PA_OK) return st;
   if (shape->kv_dtype == PA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  if (opts) {
+    if (opts->window < 0 || opts->reserved != 0) return PA_ERR_INVALID_ARG;
+    if (opts->shared_prefix_lens && !aligned16(opts->shared_prefix_lens)) return PA_ERR_INVALID_ARG;
+  }
   return PA_OK;
 }
 
@@ -75,15 +80,16 @@ pa_status pa_reshape_and_cache(const pa_shape *shape, const void *k_new, const v
 
 pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void *k_pool,
                     const void *v_pool, const float *k_scale, const float *v_scale,
-                    const int32_t *block_tables, const int32_t *seq_lens, float sm_scale,
-                    int32_t *err_flag, pa_stream_t stream) {
+                    const int32_t *block_tables, const int32_t *seq_lens,
+                    const pa_decode_opts *opts, float sm_scale, int32_t *err_flag,
+                    pa_stream_t stream) {
   if (!shape) return PA_ERR_INVALID_ARG;
   if (shape->B == 0) return check_shape(shape, true);
   pa_status st = check_decode_args(shape, out, q, k_pool, v_pool, k_scale, v_scale,
-                                   block_tables, seq_lens);
+                                   block_tables, seq_lens, opts);
   if (st != PA_OK) return st;
   return pa::run_decode(*shape, out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
-                        sm_scale, err_flag, reinterpret_cast<cudaStream_t>(stream));
+                        opts, sm_scale, err_flag, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t pa_splitkv_workspace_bytes(const pa_shape *shape, int32_t num_splits) {
@@ -109,21 +115,20 @@ pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
                             size_t workspace_bytes, int32_t num_splits, const void *q,
                             const void *k_pool, const void *v_pool, const float *k_scale,
                             const float *v_scale, const int32_t *block_tables,
-                            const int32_t *seq_lens, const int32_t *shared_prefix_lens,
+                            const int32_t *seq_lens, const pa_decode_opts *opts,
                             float sm_scale, int32_t *err_flag, pa_stream_t stream) {
   if (!shape) return PA_ERR_INVALID_ARG;
   if (shape->B == 0) return check_shape(shape, true);
   pa_status st = check_decode_args(shape, out, q, k_pool, v_pool, k_scale, v_scale,
-                                   block_tables, seq_lens);
+                                   block_tables, seq_lens, opts);
   if (st != PA_OK) return st;
   if (num_splits < 1 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARG;
   if (shape->B > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
   if (workspace_bytes < pa::splitkv_layout(*shape, num_splits).total) return PA_ERR_INVALID_ARG;
-  if (shared_prefix_lens && !aligned16(shared_prefix_lens)) return PA_ERR_INVALID_ARG;
   return pa::run_decode_splitkv(*shape, out, workspace, num_splits, q, k_pool, v_pool, k_scale,
-                                v_scale, block_tables, seq_lens, shared_prefix_lens, sm_scale,
-                                err_flag, reinterpret_cast<cudaStream_t>(stream));
+                                v_scale, block_tables, seq_lens, opts, sm_scale, err_flag,
+                                reinterpret_cast<cudaStream_t>(stream));
 }
 
 pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,

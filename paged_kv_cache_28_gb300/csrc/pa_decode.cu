@@ -75,6 +75,7 @@ struct Params {
   const int32_t *block_tables;
   const int32_t *seq_lens;
   const int32_t *shared_prefix_lens;   // optional L2 hint per sequence (split kernel)
+  int window;                          // > 0: attend over the last `window` positions only
   int32_t *err;
   int B, Hq, Hkv, G, bs, nblocks, max_blocks;
   float sl2;  // sm_scale * log2(e)
@@ -176,11 +177,37 @@ __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint1
   }
 }
 
+// The 16-token tiles a sequence of L cached tokens is attended over: with a window
+// ("KV Cache Engineering for LLM Serving", section 3) only positions
+// [max(0, L - window), L) count, so whole tiles before that are skipped and the
+// first kept tile may start part-way.
+struct SeqTiles {
+  int first;       // absolute index of the first tile
+  int count;       // tiles attended
+  int last_valid;  // valid tokens in the last tile (1..16)
+  int first_skip;  // tokens before the window in the first tile (0..15)
+};
+
+__device__ __forceinline__ SeqTiles seq_tiles(int L, int window) {
+  const int start = (window > 0 && L > window) ? L - window : 0;
+  const int end_tiles = (L + kTile - 1) / kTile;
+  SeqTiles t;
+  t.first = start / kTile;
+  t.count = end_tiles - t.first;
+  t.last_valid = L - (end_tiles - 1) * kTile;
+  t.first_skip = start - t.first * kTile;
+  return t;
+}
+
+constexpr int kLoShift = 16;   // unit info bits 16..19: first valid token of the tile
+
 // One 16-token tile: scores, online-softmax update, P V accumulation.
 // sscale: factor from raw mma scores to log2-domain scores; vs: FP8 V scale.
 template <class C>
 __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint32_t vtile,
-                                             int nvalid, float sscale, float vs, int lane) {
+                                             int lo, int nvalid, float sscale, float vs,
+                                             int lane) {
+  // tokens lo <= t < nvalid of the tile are attended
   const int r = lane >> 2, qd = lane & 3;
   float s[C::NT][4];
 #pragma unroll
@@ -229,7 +256,7 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int t = r + ((i >> 1) << 3);
-      x[i] = (t < nvalid) ? s[nt][i] * sscale : -INFINITY;
+      x[i] = (t >= lo && t < nvalid) ? s[nt][i] * sscale : -INFINITY;
     }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -275,10 +302,12 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
 
   // ---- O^T += V^T P^T; rows of V beyond nvalid are zeroed in registers (the pool
   // may hold stale or non-finite values there)
+  const bool partial = nvalid < kTile || lo > 0;
   uint32_t m01 = 0xFFFFFFFFu, m23 = 0xFFFFFFFFu;
-  if (nvalid < kTile) {
-    m01 = (2 * qd < nvalid ? 0x0000FFFFu : 0u) | (2 * qd + 1 < nvalid ? 0xFFFF0000u : 0u);
-    m23 = (2 * qd + 8 < nvalid ? 0x0000FFFFu : 0u) | (2 * qd + 9 < nvalid ? 0xFFFF0000u : 0u);
+  if (partial) {
+    auto in = [&](int t) { return t >= lo && t < nvalid; };
+    m01 = (in(2 * qd) ? 0x0000FFFFu : 0u) | (in(2 * qd + 1) ? 0xFFFF0000u : 0u);
+    m23 = (in(2 * qd + 8) ? 0x0000FFFFu : 0u) | (in(2 * qd + 9) ? 0xFFFF0000u : 0u);
   }
   if constexpr (!C::FP8) {
     const int t = (lane & 7) + ((lane >> 4) << 3);
@@ -287,7 +316,7 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
       const int c = ((dt & 3) << 1) + ((lane >> 3) & 1);
       uint32_t a[4];
       ldsm_x4_trans(a, vtile + (dt >> 2) * (kTile * 128) + t * 128 + ((c ^ (t & 7)) << 4));
-      if (nvalid < kTile) {
+      if (partial) {
         a[0] &= m01;
         a[1] &= m01;
         a[2] &= m23;
@@ -316,7 +345,7 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
                          e4m3x2_to_f16x2(__byte_perm(lo8, 0, 0x4431)),
                          e4m3x2_to_f16x2(__byte_perm(hi8, 0, 0x4420)),
                          e4m3x2_to_f16x2(__byte_perm(hi8, 0, 0x4431))};
-        if (nvalid < kTile) {
+        if (partial) {
           a[0] &= m01;
           a[1] &= m01;
           a[2] &= m23;
@@ -371,30 +400,33 @@ __device__ __forceinline__ void write_normalised(const State<C> &st, float *dst,
 // unit sources: which tiles a warp processes, in order
 // ----------------------------------------------------------------------------
 
-// Tiles w, w + NW, ... of one (b, kvh) pair, read straight from the block table.
+// Tiles w, w + NW, ... of one (b, kvh) pair's attended tiles, read straight from
+// the block table.
 struct PairSource {
   const int32_t *row;
   int32_t *err;
-  int pair, L, ntiles, w, nw, bs, nblocks;
+  int pair, w, nw, bs, nblocks;
+  SeqTiles geo;
   int base;
   int4 cur, nxt;
 
   __device__ __forceinline__ int count() const {
-    return ntiles > w ? (ntiles - w + nw - 1) / nw : 0;
+    return geo.count > w ? (geo.count - w + nw - 1) / nw : 0;
   }
   __device__ __forceinline__ int4 load(int i) const {
-    const int tile = w + i * nw;
-    if (tile >= ntiles) return make_int4(kInvalidPhys, 0, 0, 0);
+    const int j = w + i * nw;
+    if (j >= geo.count) return make_int4(kInvalidPhys, 0, 0, 0);
+    const int tile = geo.first + j;
     int phys = __ldg(row + (tile * kTile) / bs);
     if (phys < 0 || phys >= nblocks) {
       set_err(err, PA_DEVERR_BLOCK_ID);
       phys = kInvalidPhys;
     }
-    int info = min(kTile, L - tile * kTile);
-    if (tile == 0) info |= kFirstOfPair;
-    if (tile == ntiles - 1) info |= kLastOfPair;
+    int info = (j == geo.count - 1) ? geo.last_valid : kTile;
+    if (j == 0) info |= kFirstOfPair | (geo.first_skip << kLoShift);
+    if (j == geo.count - 1) info |= kLastOfPair;
     if (i == 0) info |= kPieceStart;
-    if (tile + nw >= ntiles) info |= kPieceEnd;
+    if (j + nw >= geo.count) info |= kPieceEnd;
     return make_int4(phys, pair, tile, info);
   }
   __device__ __forceinline__ void init(int lane) {
@@ -414,14 +446,14 @@ struct PairSource {
 
 // A contiguous segment [begin, end) of the tile stream: position f belongs to the
 // sequence b with prefix[b] <= f < prefix[b + 1] (binary search in shared memory),
-// then to KV head (f - prefix[b]) / ntiles(b) and tile (f - prefix[b]) % ntiles(b).
+// then to KV head (f - prefix[b]) / count(b) and attended tile (f - prefix[b]) % count(b).
 struct SegmentSource {
   const int32_t *prefix;     // shared: [B + 1]
-  const uint8_t *lastn;      // shared: [B] valid tokens in each sequence's last tile
+  const int32_t *seq_lens;
   const int32_t *block_tables;
   const int32_t *shared_prefix_lens;   // may be null
   int32_t *err;
-  int B, Hkv, bs, nblocks, max_blocks;
+  int B, Hkv, bs, nblocks, max_blocks, window;
   int begin, end;
   int base;
   int4 cur, nxt;
@@ -438,15 +470,18 @@ struct SegmentSource {
     const int b = lo, start = prefix[b];
     const int nt = (prefix[b + 1] - start) / Hkv;
     const int r = f - start;
-    const int kvh = r / nt, tile = r - kvh * nt;
+    const int kvh = r / nt, j = r - kvh * nt;
+    const int L = min(max(__ldg(seq_lens + b), 0), max_blocks * bs);
+    const SeqTiles geo = seq_tiles(L, window);
+    const int tile = geo.first + j;
     int phys = __ldg(block_tables + static_cast<size_t>(b) * max_blocks + (tile * kTile) / bs);
     if (phys < 0 || phys >= nblocks) {
       set_err(err, PA_DEVERR_BLOCK_ID);
       phys = kInvalidPhys;
     }
-    int info = (tile == nt - 1) ? lastn[b] : kTile;
-    if (tile == 0) info |= kFirstOfPair | kPieceStart;
-    if (tile == nt - 1) info |= kLastOfPair | kPieceEnd;
+    int info = (j == nt - 1) ? geo.last_valid : kTile;
+    if (j == 0) info |= kFirstOfPair | kPieceStart | (geo.first_skip << kLoShift);
+    if (j == nt - 1) info |= kLastOfPair | kPieceEnd;
     if (i == 0) info |= kPieceStart;
     if (f == end - 1) info |= kPieceEnd;
     if (shared_prefix_lens)
@@ -530,8 +565,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, ok);
 }
 
-// Runs all units of `src` (already init()ed) through the warp's ring.  on_piece_end(u, first_tile, st)
-// is called after the last tile of every piece.  Returns false after a wait timeout.
+// Runs all units of `src` (already init()ed) through the warp's ring.
+// on_piece_end(u, piece_has_pair_start, st) is called after the last tile of every
+// piece.  Returns false after a wait timeout.
 template <class C, class Src, class OnEnd>
 __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> &st,
                                          const Params &p, const CUtensorMap *tmK,
@@ -541,7 +577,7 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
 #pragma unroll
   for (int s = 0; s < C::STAGES; ++s)
     if (s < n) issue<C>(ws, s, src.get(s, lane), p, tmK, tmV, lane);
-  int first_tile = 0;
+  bool piece_first = false;
   for (int i = 0; i < n; ++i) {
     const int s = i % C::STAGES;
     const uint32_t bar = smem_u32(&ws.bar[s]);
@@ -559,7 +595,7 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
       st.reset();
       load_q<C>(st, ktile + 2 * C::KV_BYTES,
                 reinterpret_cast<const uint16_t *>(stage + 2 * C::KV_BYTES), lane);
-      first_tile = u.z;
+      piece_first = (u.w & kFirstOfPair) != 0;
     }
     if constexpr (C::FP8) {
       const float4 sc = *reinterpret_cast<const float4 *>(&ws.meta[2 * s + 1]);
@@ -567,8 +603,9 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
       vs = sc.y;
       if (u.w & kPieceStart) st.vs = vs;
     }
-    process_tile<C>(st, ktile, ktile + C::KV_BYTES, u.w & 0xFF, sscale, vs, lane);
-    if (u.w & kPieceEnd) on_piece_end(u, first_tile, st);
+    process_tile<C>(st, ktile, ktile + C::KV_BYTES, (u.w >> kLoShift) & 0xF, u.w & 0xFF, sscale,
+                    vs, lane);
+    if (u.w & kPieceEnd) on_piece_end(u, piece_first, st);
     __syncwarp();
     if (i + C::STAGES < n) issue<C>(ws, s, src.get(i + C::STAGES, lane), p, tmK, tmV, lane);
   }
@@ -610,7 +647,7 @@ __device__ __forceinline__ uint8_t *split_tail(uint8_t *raw) {
 // Dynamic shared memory of the split kernel: stages plus the length scan.
 template <class C>
 __host__ __device__ constexpr int split_smem(int B) {
-  return C::SMEM + ((B + 1) * 4 + B + 15) / 16 * 16;
+  return C::SMEM + ((B + 1) * 4 + 15) / 16 * 16;
 }
 
 // ----------------------------------------------------------------------------
@@ -631,8 +668,6 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     if (threadIdx.x == 0 && kvh == 0) set_err(p.err, PA_DEVERR_SEQ_LEN);
     L = min(max(L, 0), cap);
   }
-  const int ntiles = (L + kTile - 1) / kTile;
-
   WarpSmem ws = setup_smem<C>(smem_raw, warp, p.G, lane);
   State<C> st;
   st.reset();
@@ -640,14 +675,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.row = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
   src.err = p.err;
   src.pair = pair;
-  src.L = L;
-  src.ntiles = ntiles;
+  src.geo = seq_tiles(L, p.window);
   src.w = warp;
   src.nw = C::WARPS;
   src.bs = p.bs;
   src.nblocks = p.nblocks;
   src.init(lane);
-  run_warp<C>(src, ws, st, p, &tmK, &tmV, [](int4, int, State<C> &) {}, lane);
+  run_warp<C>(src, ws, st, p, &tmK, &tmV, [](int4, bool, State<C> &) {}, lane);
 
   // ---- merge the warps' states: warp w leaves m, l, acc (in absolute units)
   __syncthreads();
@@ -707,11 +741,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 __device__ __forceinline__ int clamp_len(int L, int cap) { return min(max(L, 0), cap); }
 
 // Block-wide scan of the sequence lengths into shared memory:
-//   prefix[b] = Hkv * sum_{b' < b} ntiles(b'),  prefix[B] = total tiles,
-//   lastn[b]  = valid tokens in the last 16-token tile of sequence b.
+//   prefix[b] = Hkv * sum_{b' < b} count(b'),  prefix[B] = total tiles,
+// where count(b) is the number of 16-token tiles sequence b attends over.
 // Out-of-range lengths are clamped (and reported once, by CTA 0).
 template <int THREADS>
-__device__ void scan_lengths(const Params &p, int32_t *prefix, uint8_t *lastn) {
+__device__ void scan_lengths(const Params &p, int32_t *prefix) {
   __shared__ int warp_sums[THREADS / 32];
   __shared__ int carry_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -724,10 +758,7 @@ __device__ void scan_lengths(const Params &p, int32_t *prefix, uint8_t *lastn) {
     if (i < p.B) {
       const int L0 = p.seq_lens[i];
       if ((L0 < 0 || L0 > cap) && blockIdx.x == 0) set_err(p.err, PA_DEVERR_SEQ_LEN);
-      const int L = clamp_len(L0, cap);
-      const int nt = (L + kTile - 1) / kTile;
-      v = p.Hkv * nt;
-      lastn[i] = static_cast<uint8_t>(nt ? L - (nt - 1) * kTile : 0);
+      v = p.Hkv * seq_tiles(clamp_len(L0, cap), p.window).count;
     }
     int x = v;
 #pragma unroll
@@ -757,14 +788,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   pdl_trigger();
   WarpSmem ws = setup_smem<C>(smem_raw, warp, p.G, lane);
   int32_t *prefix = reinterpret_cast<int32_t *>(split_tail<C>(smem_raw));
-  uint8_t *lastn = reinterpret_cast<uint8_t *>(prefix + p.B + 1);
-  scan_lengths<C::THREADS>(p, prefix, lastn);
+  scan_lengths<C::THREADS>(p, prefix);
   const int seg = blockIdx.x * C::WARPS + warp;
   const int total = prefix[p.B];
   const int W = max(1, (total + p.num_splits - 1) / p.num_splits);
   SegmentSource src;
   src.prefix = prefix;
-  src.lastn = lastn;
+  src.seq_lens = p.seq_lens;
   src.block_tables = p.block_tables;
   src.shared_prefix_lens = p.shared_prefix_lens;
   src.err = p.err;
@@ -773,6 +803,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.bs = p.bs;
   src.nblocks = p.nblocks;
   src.max_blocks = p.max_blocks;
+  src.window = p.window;
   src.begin = min(seg * W, total);
   src.end = (seg < p.num_splits) ? min(src.begin + W, total) : src.begin;
   src.init(lane);
@@ -786,13 +817,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   st.reset();
   run_warp<C>(
       src, ws, st, p, &tmK, &tmV,
-      [&](int4 u, int first_tile, State<C> &s) {
+      [&](int4 u, bool piece_first, State<C> &s) {
         const int b = u.y / p.Hkv, kvh = u.y - b * p.Hkv;
-        if (first_tile == 0 && (u.w & kLastOfPair)) {
+        if (piece_first && (u.w & kLastOfPair)) {
           write_normalised<C>(s, p.out + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D,
                               nullptr, p.G, lane);
         } else {
-          const size_t slot = static_cast<size_t>(seg) * 2 + (first_tile == 0 ? 1 : 0);
+          const size_t slot = static_cast<size_t>(seg) * 2 + (piece_first ? 1 : 0);
           write_normalised<C>(s, p.o_part + slot * p.G * C::D, p.lse_part + slot * p.G, p.G,
                               lane);
         }
@@ -919,8 +950,9 @@ static cudaError_t prep_kernel(K kernel, int smem) {
 
 static Params make_params(const pa_shape &s, float *out, const void *q, const float *k_scale,
                           const float *v_scale, const int32_t *bt, const int32_t *sl,
-                          float sm_scale, int32_t *err) {
+                          const pa_decode_opts *opts, float sm_scale, int32_t *err) {
   Params p{};
+  p.window = opts ? opts->window : 0;
   p.out = out;
   p.q = static_cast<const uint16_t *>(q);
   p.k_scale = k_scale;
@@ -1021,25 +1053,25 @@ WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits) {
 
 pa_status run_decode(const pa_shape &s, float *out, const void *q, const void *k_pool,
                      const void *v_pool, const float *k_scale, const float *v_scale,
-                     const int32_t *bt, const int32_t *sl, float sm_scale, int32_t *err,
-                     cudaStream_t stream) {
+                     const int32_t *bt, const int32_t *sl, const pa_decode_opts *opts,
+                     float sm_scale, int32_t *err, cudaStream_t stream) {
   CUtensorMap mk, mv;
   if (!make_pool_map(&mk, k_pool, s) || !make_pool_map(&mv, v_pool, s)) return PA_ERR_CUDA;
-  Params p = make_params(s, out, q, k_scale, v_scale, bt, sl, sm_scale, err);
+  Params p = make_params(s, out, q, k_scale, v_scale, bt, sl, opts, sm_scale, err);
   return dispatch_pair(s, p, mk, mv, stream);
 }
 
 pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int num_splits,
                              const void *q, const void *k_pool, const void *v_pool,
                              const float *k_scale, const float *v_scale, const int32_t *bt,
-                             const int32_t *sl, const int32_t *shared_prefix_lens, float sm_scale,
+                             const int32_t *sl, const pa_decode_opts *opts, float sm_scale,
                              int32_t *err, cudaStream_t stream) {
   const WorkspaceLayout w = splitkv_layout(s, num_splits);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   CUtensorMap mk, mv;
   if (!make_pool_map(&mk, k_pool, s) || !make_pool_map(&mv, v_pool, s)) return PA_ERR_CUDA;
-  Params p = make_params(s, out, q, k_scale, v_scale, bt, sl, sm_scale, err);
-  p.shared_prefix_lens = shared_prefix_lens;
+  Params p = make_params(s, out, q, k_scale, v_scale, bt, sl, opts, sm_scale, err);
+  p.shared_prefix_lens = opts ? opts->shared_prefix_lens : nullptr;
   p.prefix_out = reinterpret_cast<int32_t *>(ws + w.prefix);
   p.lse_part = reinterpret_cast<float *>(ws + w.lse);
   p.o_part = reinterpret_cast<float *>(ws + w.o_part);

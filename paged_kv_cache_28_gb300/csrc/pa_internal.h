@@ -54,13 +54,13 @@ pa_status run_reshape_and_cache(const pa_shape &s, const void *k_new, const void
 
 pa_status run_decode(const pa_shape &s, float *out, const void *q, const void *k_pool,
                      const void *v_pool, const float *k_scale, const float *v_scale,
-                     const int32_t *bt, const int32_t *sl, float sm_scale, int32_t *err,
-                     cudaStream_t stream);
+                     const int32_t *bt, const int32_t *sl, const pa_decode_opts *opts,
+                     float sm_scale, int32_t *err, cudaStream_t stream);
 
 pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int num_splits,
                              const void *q, const void *k_pool, const void *v_pool,
                              const float *k_scale, const float *v_scale, const int32_t *bt,
-                             const int32_t *sl, const int32_t *shared_prefix_lens, float sm_scale,
+                             const int32_t *sl, const pa_decode_opts *opts, float sm_scale,
                              int32_t *err, cudaStream_t stream);
 
 pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int num_splits,

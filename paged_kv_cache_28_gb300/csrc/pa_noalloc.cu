@@ -62,7 +62,7 @@ extern "C" pa_status pa_decode_splitkv_noalloc(const pa_shape *shape, float *out
   if (scratch_address(&scratch) != cudaSuccess) return PA_ERR_CUDA;
   pa_status st = pa_decode_splitkv(shape, out, scratch, PA_NOALLOC_SCRATCH_BYTES, num_splits, q,
                                    k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
-                                   nullptr, sm_scale, err_flag, stream);
+                                   /*opts=*/nullptr, sm_scale, err_flag, stream);
   if (st != PA_OK) return st;
   return pa_merge_lse(shape, out, scratch, num_splits, stream);
 }

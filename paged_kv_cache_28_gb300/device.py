@@ -61,10 +61,10 @@ class DeviceBatch:
                                   self.k_scale, self.v_scale, self.slot_mapping, self.err,
                                   stream)
 
-    def decode(self, stream=None):
+    def decode(self, stream=None, window: int = 0):
         _lib.pa_decode(self.shape, self.out, self.q, self.k_pool, self.v_pool, self.k_scale,
                        self.v_scale, self.block_tables, self.seq_lens, self.batch.sm_scale,
-                       self.err, stream)
+                       self.err, stream, window)
 
     def ensure_workspace(self, num_splits: int):
         nbytes = _lib.pa_splitkv_workspace_bytes(self.shape, num_splits)
@@ -74,7 +74,8 @@ class DeviceBatch:
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
         self.num_splits = num_splits
 
-    def decode_splitkv(self, num_splits: int | None = None, stream=None, hints: bool = True):
+    def decode_splitkv(self, num_splits: int | None = None, stream=None, hints: bool = True,
+                       window: int = 0):
         """Split-KV decode + merge; hints: pass the batch's shared-prefix lengths (if any)."""
         if num_splits is None:
             num_splits = default_num_splits(self.shape, self.device)
@@ -83,7 +84,7 @@ class DeviceBatch:
         _lib.pa_decode_splitkv(self.shape, self.out, self.workspace, num_splits, self.q,
                                self.k_pool, self.v_pool, self.k_scale, self.v_scale,
                                self.block_tables, self.seq_lens, self.batch.sm_scale, self.err,
-                               stream, self.shared_prefix_lens if hints else None)
+                               stream, self.shared_prefix_lens if hints else None, window)
         _lib.pa_merge_lse(self.shape, self.out, self.workspace, num_splits, stream)
 
     def read_err(self, stream=None) -> int:

@@ -95,18 +95,18 @@ class Batch:
     def logical_tokens(self) -> int:
         return int(self.seq_lens.astype(np.int64).sum())
 
-    def unique_kv_tokens(self) -> int:
-        """Tokens stored in distinct physical blocks that some sequence reads."""
-        best: dict[int, int] = {}
+    def unique_kv_tokens(self, window: int = 0) -> int:
+        """Distinct (physical block, row) token slots that some sequence reads; with a
+        window only the last `window` positions of each sequence count."""
+        rows: dict[int, set] = {}
         bs = self.block_size
         for b in range(self.B):
             L = int(self.seq_lens[b])
-            for j in range((L + bs - 1) // bs):
-                n = min(bs, L - j * bs)
-                blk = int(self.block_tables[b, j])
-                if best.get(blk, 0) < n:
-                    best[blk] = n
-        return sum(best.values())
+            first = L - window if (window > 0 and L > window) else 0
+            for j in range(first // bs, (L + bs - 1) // bs):
+                lo, hi = max(first, j * bs) - j * bs, min(L, (j + 1) * bs) - j * bs
+                rows.setdefault(int(self.block_tables[b, j]), set()).update(range(lo, hi))
+        return sum(len(r) for r in rows.values())
 
     def kv_bytes_per_token(self) -> int:
         """K and V of every KV head for one token of one layer."""

@@ -50,7 +50,7 @@ def _decode(lib, s, **ptr):
     p = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, ks=None, vs=None, bt=FAKE, sl=FAKE)
     p.update(ptr)
     return lib.pa_decode(s, p["out"], p["q"], p["k"], p["v"], p["ks"], p["vs"], p["bt"], p["sl"],
-                         0.125, None, None)
+                         p.get("opts"), 0.125, None, None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -76,8 +76,12 @@ def test_decode_rejects_bad_pointers(lib):
     assert _decode(lib, s, k=FAKE + 4) == _lib.PA_ERR_INVALID_ARG     # misaligned
     fp8 = ctypes.byref(shape(D=128, kv_dtype=_lib.PA_KV_FP8_E4M3))
     assert _decode(lib, fp8) == _lib.PA_ERR_INVALID_ARG                # scales missing
-    assert lib.pa_decode(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 0.1, None,
+    assert lib.pa_decode(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, None, 0.1, None,
                          None) == _lib.PA_ERR_INVALID_ARG
+    bad = _lib.pa_decode_opts(-1, 0, None)
+    assert _decode(lib, s, opts=ctypes.byref(bad)) == _lib.PA_ERR_INVALID_ARG   # window < 0
+    bad = _lib.pa_decode_opts(8, 1, None)
+    assert _decode(lib, s, opts=ctypes.byref(bad)) == _lib.PA_ERR_INVALID_ARG   # reserved != 0
 
 
 def test_empty_batch_is_a_no_op(lib):
@@ -101,7 +105,7 @@ def test_splitkv_host_checks(lib):
     args[2] = FAKE + 16
     assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # workspace not 256-aligned
     args[2] = FAKE
-    args[12] = FAKE + 4
+    args[12] = ctypes.byref(_lib.pa_decode_opts(0, 0, FAKE + 4))
     assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # hint array misaligned
     args[12] = None
     assert lib.pa_merge_lse(ctypes.byref(s), FAKE, FAKE, 0, None) == _lib.PA_ERR_INVALID_ARG

@@ -43,7 +43,7 @@ def assert_close(gpu, ref, batch, what=""):
                              f" gpu={gpu[i]!r} oracle={ref[i]!r}")
 
 
-def oracle_after_write(batch, rows=None, write=True):
+def oracle_after_write(batch, rows=None, write=True, window=0):
     """Oracle output after applying this step's cache write to host copies of the pools."""
     kp, vp = batch.k_pool.copy(), batch.v_pool.copy()
     ks = None if batch.k_scale is None else batch.k_scale.copy()
@@ -57,16 +57,16 @@ def oracle_after_write(batch, rows=None, write=True):
                                           batch.block_size)
     out = oracle.paged_decode(batch.q, kp, vp, batch.block_tables, batch.seq_lens,
                               batch.sm_scale, Hkv=batch.Hkv, block_size=batch.block_size,
-                              k_scale=ks, v_scale=vs, rows=rows)
+                              k_scale=ks, v_scale=vs, rows=rows, window=window)
     return out, (kp, vp, ks, vs)
 
 
-def run_gpu(dev, mode, num_splits=None):
+def run_gpu(dev, mode, num_splits=None, window=0):
     dev.out.fill_(float("nan"))
     if mode == "decode":
-        dev.decode()
+        dev.decode(window=window)
     else:
-        dev.decode_splitkv(num_splits)
+        dev.decode_splitkv(num_splits, window=window)
     torch.cuda.synchronize()
     return dev.out.cpu().numpy()
 
@@ -226,6 +226,44 @@ def test_fp8_g16_and_bs32():
     dev.reshape_and_cache()
     ref, _ = oracle_after_write(batch)
     _modes_run(dev, batch, ref, "fp8 G=16 bs=32")
+
+
+# ---------------------------------------------------------------- sliding window
+
+@pytest.mark.parametrize("kv_dtype,bs", [("bf16", 16), ("bf16", 32), ("fp8_e4m3", 16)])
+def test_window_all_modes(kv_dtype, bs):
+    lens = [1, 15, 16, 17, 40, 97, 333, 1200, 0, 64]
+    batch = wl.build_batch("t", lens, Hq=64, Hkv=8, D=128, block_size=bs, seed=70 + bs,
+                           kv_dtype=kv_dtype)
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    for window in (1, 4, 16, 17, 100, 5000):
+        ref, _ = oracle_after_write(batch, window=window)
+        for mode, ns in (("decode", None), ("split", 1), ("split", 9), ("split", 300)):
+            out = run_gpu(dev, mode, ns, window)
+            assert_close(out, ref, batch, f"window={window} {mode} {ns}")
+    assert dev.read_err() == 0
+
+
+def test_window_one_returns_last_v_and_skips_old_blocks():
+    batch = wl.build_batch("t", [100, 37, 1], Hq=64, Hkv=8, D=128, block_size=16, seed=75)
+    vf = wl.bf16_to_float(batch.v_pool)
+    # blocks wholly before a 20-token window are never read: sequence 0 (L=100)
+    # attends from position 80 (block 5), sequence 1 (L=37) from 17 (block 1)
+    batch.block_tables[0, :5] = -1
+    batch.block_tables[1, :1] = batch.nblocks + 100
+    dev = DeviceBatch(batch)
+    for mode, ns in (("decode", None), ("split", 5)):
+        out = run_gpu(dev, mode, ns, window=1)
+        for b, L in enumerate(batch.seq_lens):
+            t = L - 1
+            blk = batch.block_tables[b, t // 16]
+            for h in range(64):
+                assert np.array_equal(_bits(out[b, h]), _bits(vf[blk, t % 16, h // 8])), (mode, b)
+        out = run_gpu(dev, mode, ns, window=20)
+        ref, _ = oracle_after_write(batch, write=False, window=20)
+        assert_close(out, ref, batch, f"window 20 {mode}")
+    assert dev.read_err() == 0
 
 
 # ---------------------------------------------------------------- invariants
