@@ -28,6 +28,10 @@ reshape_and_cache_bf16         canary-filled pools: exactly the addressed
                                rows change, byte for byte
 reshape_and_cache_fp8          closed-form scale/requantisation cases built by
                                hand from the reading in pa_oracle.c
+reshape_and_cache_int4         the 4-bit codes and restored values printed in
+                               "KV Cache Engineering", sec. 8, through the
+                               writer; closed-form growth/requantisation cases
+int4_restore                   closed form (nibble - 8) * scale
 paged_decode                   numpy/scipy softmax attention on contiguous
                                (unpaged) K/V; L=1 -> V; q=0 -> mean(V);
                                L=2 logistic closed form; needle; block
@@ -102,6 +106,10 @@ def _load():
             lib.oracle_reshape_and_cache_bf16.argtypes = [I, I, I, I, P, P, P, P, P]
             lib.oracle_reshape_and_cache_fp8.restype = None
             lib.oracle_reshape_and_cache_fp8.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
+            lib.oracle_reshape_and_cache_int4.restype = None
+            lib.oracle_reshape_and_cache_int4.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
+            lib.oracle_int4_restore.restype = None
+            lib.oracle_int4_restore.argtypes = [P, I, ctypes.c_float, P]
             lib.oracle_paged_decode.restype = None
             lib.oracle_paged_decode.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, D,
                                                 I, I, P, P, P, I]
@@ -201,9 +209,39 @@ def reshape_and_cache_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, slot_m
                                      _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(sm))
 
 
+def reshape_and_cache_int4(k_new, v_new, k_pool, v_pool, k_scale, v_scale, slot_mapping,
+                           block_size: int):
+    """In place on uint8 pools [nblocks, bs, Hkv, D/2] (two offset-binary nibbles per
+    byte) and float32 scales [nblocks, Hkv]."""
+    lib = _load()
+    for a, dt in ((k_pool, np.uint8), (v_pool, np.uint8), (k_scale, np.float32),
+                  (v_scale, np.float32)):
+        assert a.dtype == dt and a.flags.c_contiguous
+    T, Hkv, D = k_new.shape
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    sm = _c(slot_mapping, np.int64)
+    lib.oracle_reshape_and_cache_int4(T, Hkv, D, block_size, _ptr(kn), _ptr(vn), _ptr(k_pool),
+                                      _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(sm))
+
+
+def int4_restore(row, scale: float) -> np.ndarray:
+    lib = _load()
+    r = _c(row, np.uint8)
+    out = np.zeros(r.size * 2, dtype=np.float64)
+    lib.oracle_int4_restore(_ptr(r), r.size * 2, float(scale), _ptr(out))
+    return out
+
+
 # --------------------------------------------------------------------------
 # decode attention
 # --------------------------------------------------------------------------
+
+def _kv_kind(pool, D: int) -> int:
+    """0: bf16 (uint16) pool, 1: E4M3 (uint8, D per row), 2: 4-bit (uint8, D/2 per row)."""
+    if pool.dtype == np.uint16:
+        return 0
+    return 2 if pool.shape[-1] * 2 == D else 1
+
 
 def window_positions(length: int, window: int) -> list[int]:
     lib = _load()
@@ -217,15 +255,17 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, *, 
                  nthreads: int | None = None, window: int = 0) -> np.ndarray:
     """Decode attention in fp64.
 
-    q: uint16 [B, Hq, D] (bf16 bits).  Pools: uint16 (bf16) or uint8 (E4M3 codes, then
-    k_scale / v_scale float32 [nblocks, Hkv] are required), shape [nblocks, bs, Hkv, D].
+    q: uint16 [B, Hq, D] (bf16 bits).  Pools: uint16 (bf16) [nblocks, bs, Hkv, D], uint8
+    E4M3 codes [nblocks, bs, Hkv, D] or uint8 4-bit nibble pairs [nblocks, bs, Hkv, D/2]
+    (the last two need k_scale / v_scale float32 [nblocks, Hkv]).
     rows: optional int array [n, 2] of (b, h); then the result is [n, D], else [B, Hq, D].
     window: > 0 attends over the last `window` positions of each sequence only.
     """
     lib = _load()
     q = _c(q, np.uint16)
     B, Hq, D = q.shape
-    fp8 = k_pool.dtype == np.uint8
+    kind = _kv_kind(k_pool, D)
+    fp8 = kind != 0
     kp = np.ascontiguousarray(k_pool)
     vp = np.ascontiguousarray(v_pool)
     ks = _c(k_scale, np.float32) if fp8 else None
@@ -235,7 +275,7 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, *, 
     nthreads = nthreads or os.cpu_count() or 1
     if rows is None:
         out = np.zeros((B, Hq, D), dtype=np.float64)
-        lib.oracle_paged_decode(B, Hq, Hkv, D, block_size, bt.shape[1], int(fp8), _ptr(q),
+        lib.oracle_paged_decode(B, Hq, Hkv, D, block_size, bt.shape[1], kind, _ptr(q),
                                 _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl),
                                 float(sm_scale), int(window), 0, None, None, _ptr(out), nthreads)
         return out
@@ -243,7 +283,7 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, *, 
     rb = np.ascontiguousarray(rows[:, 0])
     rh = np.ascontiguousarray(rows[:, 1])
     out = np.zeros((rows.shape[0], D), dtype=np.float64)
-    lib.oracle_paged_decode(B, Hq, Hkv, D, block_size, bt.shape[1], int(fp8), _ptr(q), _ptr(kp),
+    lib.oracle_paged_decode(B, Hq, Hkv, D, block_size, bt.shape[1], kind, _ptr(q), _ptr(kp),
                             _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl), float(sm_scale),
                             int(window), rows.shape[0], _ptr(rb), _ptr(rh), _ptr(out), nthreads)
     return out
@@ -255,7 +295,8 @@ def split_partials(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, b
     lib = _load()
     q = _c(q, np.uint16)
     B, Hq, D = q.shape
-    fp8 = k_pool.dtype == np.uint8
+    kind = _kv_kind(k_pool, D)
+    fp8 = kind != 0
     kp = np.ascontiguousarray(k_pool)
     vp = np.ascontiguousarray(v_pool)
     ks = _c(k_scale, np.float32) if fp8 else None
@@ -266,7 +307,7 @@ def split_partials(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, b
     S = beg.size - 1
     o = np.zeros((S, D), dtype=np.float64)
     lse = np.zeros(S, dtype=np.float64)
-    lib.oracle_split_partials(Hq, Hkv, D, block_size, bt.shape[1], int(fp8), _ptr(q), _ptr(kp),
+    lib.oracle_split_partials(Hq, Hkv, D, block_size, bt.shape[1], kind, _ptr(q), _ptr(kp),
                               _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl), float(sm_scale),
                               b, h, S, _ptr(beg), _ptr(o), _ptr(lse))
     return o, lse

@@ -284,12 +284,109 @@ void oracle_reshape_and_cache_fp8(int T, int Hkv, int D, int bs,
     }
 }
 
+/*
+ * 4-bit variant of the cache write ([P3] section 8 with bits = 4, largest code
+ * 7), per (block, kv head) and separately for K and V, with the same reading as
+ * the FP8 writer:
+ *   scale = absmax of all values written since offset 0 / 7 (fp32 division);
+ *   code  = clip(rint(x / scale), -7, 7) (fp32 division, ties to even);
+ *   a write that raises the scale re-encodes rows 0..off-1 from
+ *   restored = code * old_scale (fp32 product); a zero scale stores code 0.
+ * Storage: a code is kept as the nibble code + 8 (offset binary, 1..15); the
+ * byte at column j of a row holds elements 2j (low nibble) and 2j + 1 (high).
+ */
+static int int4_get(const uint8_t *row, int d)
+{
+    int nib = (d & 1) ? (row[d >> 1] >> 4) : (row[d >> 1] & 0xF);
+    return nib - 8;
+}
+
+static void int4_put(uint8_t *row, int d, int code)
+{
+    uint8_t nib = (uint8_t)(code + 8);
+    if (d & 1)
+        row[d >> 1] = (uint8_t)((row[d >> 1] & 0x0F) | (nib << 4));
+    else
+        row[d >> 1] = (uint8_t)((row[d >> 1] & 0xF0) | nib);
+}
+
+static int int4_code(float x, float scale)
+{
+    float c;
+    if (scale == 0.0f)
+        return 0;
+    c = nearbyintf(x / scale);
+    if (c > 7.0f) c = 7.0f;
+    if (c < -7.0f) c = -7.0f;
+    return (int)c;
+}
+
+static void int4_write_row(uint8_t *pool, float *scale, int Hkv, int D, int bs,
+                           int64_t blk, int off, int h, const uint16_t *x)
+{
+    float amax = 0.0f, cand, old, s_new;
+    int d, r;
+    float *sp = &scale[blk * Hkv + h];
+    size_t rowb = (size_t)D / 2;
+    for (d = 0; d < D; d++) {
+        float v = fabsf(bf16_bits_to_float(x[d]));
+        if (v > amax)
+            amax = v;
+    }
+    cand = amax / 7.0f;
+    old = *sp;
+    s_new = (off == 0 || cand > old) ? cand : old;
+    if (off > 0 && s_new > old) {
+        for (r = 0; r < off; r++) {
+            uint8_t *row = &pool[(((size_t)blk * bs + r) * Hkv + h) * rowb];
+            for (d = 0; d < D; d++) {
+                float restored = (float)int4_get(row, d) * old;
+                int4_put(row, d, int4_code(restored, s_new));
+            }
+        }
+    }
+    {
+        uint8_t *row = &pool[(((size_t)blk * bs + off) * Hkv + h) * rowb];
+        for (d = 0; d < D; d++)
+            int4_put(row, d, int4_code(bf16_bits_to_float(x[d]), s_new));
+    }
+    *sp = s_new;
+}
+
+void oracle_reshape_and_cache_int4(int T, int Hkv, int D, int bs,
+                                   const uint16_t *k_new, const uint16_t *v_new,
+                                   uint8_t *k_pool, uint8_t *v_pool,
+                                   float *k_scale, float *v_scale,
+                                   const int64_t *slot_mapping)
+{
+    int t, h;
+    for (t = 0; t < T; t++) {
+        int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        for (h = 0; h < Hkv; h++) {
+            int4_write_row(k_pool, k_scale, Hkv, D, bs, s / bs, (int)(s % bs), h,
+                           &k_new[((size_t)t * Hkv + h) * D]);
+            int4_write_row(v_pool, v_scale, Hkv, D, bs, s / bs, (int)(s % bs), h,
+                           &v_new[((size_t)t * Hkv + h) * D]);
+        }
+    }
+}
+
+/* Restored values of one 4-bit row: (nibble - 8) * scale, exactly in double. */
+void oracle_int4_restore(const uint8_t *row, int D, float scale, double *out)
+{
+    int d;
+    for (d = 0; d < D; d++)
+        out[d] = (double)int4_get(row, d) * (double)scale;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Decode attention                                                           */
 /* ------------------------------------------------------------------------- */
 
 typedef struct {
-    int Hq, Hkv, D, bs, max_blocks, kv_fp8;
+    int Hq, Hkv, D, bs, max_blocks, kv_kind;
     const void *k_pool, *v_pool;
     const float *k_scale, *v_scale;
     const int32_t *block_tables;
@@ -298,17 +395,22 @@ typedef struct {
 /* Gather: the key (or value) row of logical token t of sequence b, KV head kvh
  * ([P4] "The Block Table Logic"; [P1] "Paging"):
  *   block = block_tables[b][t / bs], row = pool[block][t % bs][kvh][:]
- * written into dst[0..D) as doubles.  FP8 pools are restored as
- * code value * scale[block][kvh], exactly in double. */
+ * written into dst[0..D) as doubles.  FP8 and 4-bit pools are restored as
+ * code value * scale[block][kvh], exactly in double (kv_kind: 0 bf16, 1 E4M3,
+ * 2 4-bit). */
 static void kv_row(const paged_kv *p, int is_v, int b, int t, int kvh, double *dst)
 {
     int32_t blk = p->block_tables[(size_t)b * p->max_blocks + t / p->bs];
     size_t idx = (((size_t)blk * p->bs + (size_t)(t % p->bs)) * p->Hkv + kvh) * p->D;
     const void *pool = is_v ? p->v_pool : p->k_pool;
     int d;
-    if (!p->kv_fp8) {
+    if (p->kv_kind == 0) {
         for (d = 0; d < p->D; d++)
             dst[d] = oracle_bf16_to_double(((const uint16_t *)pool)[idx + d]);
+    } else if (p->kv_kind == 2) {
+        const float *sc = is_v ? p->v_scale : p->k_scale;
+        oracle_int4_restore(&((const uint8_t *)pool)[idx / 2], p->D,
+                            sc[(size_t)blk * p->Hkv + kvh], dst);
     } else {
         const float *sc = is_v ? p->v_scale : p->k_scale;
         double scale = (double)sc[(size_t)blk * p->Hkv + kvh];
@@ -378,7 +480,7 @@ static void attend_range(const paged_kv *p, const uint16_t *q_row, int b, int h,
  * the nrows pairs (rows_b[i], rows_h[i]) into out[nrows][D].
  * Parallel over rows with OpenMP when nthreads > 1 (each row is independent).
  */
-void oracle_paged_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks, int kv_fp8,
+void oracle_paged_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks, int kv_kind,
                          const uint16_t *q, const void *k_pool, const void *v_pool,
                          const float *k_scale, const float *v_scale,
                          const int32_t *block_tables, const int32_t *seq_lens,
@@ -387,7 +489,7 @@ void oracle_paged_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks, 
 {
     paged_kv p;
     long long i, n;
-    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_fp8 = kv_fp8;
+    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_kind = kv_kind;
     p.k_pool = k_pool; p.v_pool = v_pool; p.k_scale = k_scale; p.v_scale = v_scale;
     p.block_tables = block_tables;
     n = rows_b ? (long long)nrows : (long long)B * Hq;
@@ -409,7 +511,7 @@ void oracle_paged_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks, 
  * Each split is attended on its own (attend_range), giving o_i (normalised) and
  * lse_i (natural log).  Empty splits give o_i = 0, lse_i = -inf.
  */
-void oracle_split_partials(int Hq, int Hkv, int D, int bs, int max_blocks, int kv_fp8,
+void oracle_split_partials(int Hq, int Hkv, int D, int bs, int max_blocks, int kv_kind,
                            const uint16_t *q, const void *k_pool, const void *v_pool,
                            const float *k_scale, const float *v_scale,
                            const int32_t *block_tables, const int32_t *seq_lens,
@@ -418,7 +520,7 @@ void oracle_split_partials(int Hq, int Hkv, int D, int bs, int max_blocks, int k
 {
     paged_kv p;
     int i, L = seq_lens[b];
-    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_fp8 = kv_fp8;
+    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_kind = kv_kind;
     p.k_pool = k_pool; p.v_pool = v_pool; p.k_scale = k_scale; p.v_scale = v_scale;
     p.block_tables = block_tables;
     for (i = 0; i < nsplit; i++) {

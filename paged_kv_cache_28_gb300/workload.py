@@ -16,8 +16,9 @@ of "KV Cache Engineering for LLM Serving", section 10 (Paging).
 Every array is numpy.  Values are drawn with numpy's PCG64 generator, which
 gives the same numbers on every platform.  K/V/Q are N(0, 1) rounded to bf16.
 FP8 pools hold E4M3 codes drawn as RNE(N(0,1) * 112) clipped to +-448 with
-per-(block, head) scales 4/448 * U(0.8, 1.2); this is a random input of the
-right format, not the product's quantiser.
+per-(block, head) scales 4/448 * U(0.8, 1.2); 4-bit pools hold codes
+clip(rint(N(0,1) * 7/3), -7, 7) with scales 3/7 * U(0.8, 1.2).  These are
+random inputs of the right format, not the product's quantiser.
 """
 from __future__ import annotations
 
@@ -72,14 +73,14 @@ class Batch:
     block_size: int
     nblocks: int
     max_blocks: int
-    kv_dtype: str                      # "bf16" or "fp8_e4m3"
+    kv_dtype: str                      # "bf16", "fp8_e4m3" or "int4"
     seq_lens: np.ndarray               # int32 [B]
     block_tables: np.ndarray           # int32 [B, max_blocks] (unused entries -1)
     slot_mapping: np.ndarray           # int64 [B]: slot of position seq_len-1 (this step's token)
     q: np.ndarray                      # uint16 [B, Hq, D] (bf16 bits)
     k_new: np.ndarray                  # uint16 [B, Hkv, D]
     v_new: np.ndarray                  # uint16 [B, Hkv, D]
-    k_pool: np.ndarray | None          # uint16 / uint8 [nblocks, bs, Hkv, D]
+    k_pool: np.ndarray | None          # uint16 / uint8 [nblocks, bs, Hkv, D] (int4: D / 2)
     v_pool: np.ndarray | None
     k_scale: np.ndarray | None         # float32 [nblocks, Hkv] (fp8 only)
     v_scale: np.ndarray | None
@@ -88,8 +89,12 @@ class Batch:
     shared_prefix_lens: np.ndarray | None = None   # int32 [B]: tokens in blocks shared with others
 
     @property
-    def elem_bytes(self) -> int:
-        return 1 if self.kv_dtype == "fp8_e4m3" else 2
+    def quantized(self) -> bool:
+        return self.kv_dtype in ("fp8_e4m3", "int4")
+
+    @property
+    def elem_bytes(self) -> float:
+        return {"bf16": 2, "fp8_e4m3": 1, "int4": 0.5}[self.kv_dtype]
 
     @property
     def logical_tokens(self) -> int:
@@ -110,10 +115,10 @@ class Batch:
 
     def kv_bytes_per_token(self) -> int:
         """K and V of every KV head for one token of one layer."""
-        return 2 * self.Hkv * self.D * self.elem_bytes
+        return int(2 * self.Hkv * self.D * self.elem_bytes)
 
     def scale_bytes_per_block(self) -> int:
-        return 2 * self.Hkv * 4 if self.kv_dtype == "fp8_e4m3" else 0
+        return 2 * self.Hkv * 4 if self.quantized else 0
 
 
 # --------------------------------------------------------------------------
@@ -143,6 +148,21 @@ def _normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
 
     def fill(g, s, e):
         out[s:e] = bf16_bits(g.standard_normal(e - s, dtype=np.float32))
+
+    _chunked(rng, n, fill)
+    return out.reshape(shape)
+
+
+def _int4_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    """Packed 4-bit codes: clip(rint(N(0,1) * 7 / 3), -7, 7) + 8 per element, two per byte
+    (element 2j in the low nibble); shape's last dim is D / 2."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint8)
+
+    def fill(g, s, e):
+        c = np.clip(np.rint(g.standard_normal(2 * (e - s), dtype=np.float32) * np.float32(7 / 3)),
+                    -7, 7).astype(np.int16) + 8
+        out[s:e] = (c[0::2] | (c[1::2] << 4)).astype(np.uint8)
 
     _chunked(rng, n, fill)
     return out.reshape(shape)
@@ -240,6 +260,14 @@ def build_batch(name: str, seq_lens, *, Hq: int, Hkv: int, D: int, block_size: i
                        rng.uniform(0.8, 1.2, (nblocks, Hkv)).astype(np.float32))
             v_scale = (np.float32(4.0 / 448.0) *
                        rng.uniform(0.8, 1.2, (nblocks, Hkv)).astype(np.float32))
+        elif kv_dtype == "int4":
+            shape4 = (nblocks, bs, Hkv, D // 2)
+            k_pool = _int4_codes(rng, shape4)
+            v_pool = _int4_codes(rng, shape4)
+            k_scale = (np.float32(3.0 / 7.0) *
+                       rng.uniform(0.8, 1.2, (nblocks, Hkv)).astype(np.float32))
+            v_scale = (np.float32(3.0 / 7.0) *
+                       rng.uniform(0.8, 1.2, (nblocks, Hkv)).astype(np.float32))
         else:
             k_pool = _normal_bf16(rng, shape)
             v_pool = _normal_bf16(rng, shape)
@@ -273,7 +301,8 @@ def lognormal_lens(rng, n: int, median: float, lo: int, hi: int) -> np.ndarray:
 # the five named workloads
 # --------------------------------------------------------------------------
 
-CONFIGS = ("tiny", "llama70b_layer", "prefix_sharing", "long_context", "fp8_mixed")
+CONFIGS = ("tiny", "llama70b_layer", "prefix_sharing", "long_context", "fp8_mixed",
+           "int4_mixed")
 
 
 def config_seq_lens(name: str, seed: int):
@@ -294,14 +323,15 @@ def config_seq_lens(name: str, seed: int):
     if name == "long_context":
         return (np.full(8, 131072, np.int32), (),
                 dict(Hq=64, Hkv=8, D=128, block_size=32, max_blocks=4096))
-    if name == "fp8_mixed":
+    if name in ("fp8_mixed", "int4_mixed"):
         return (rng.integers(1, 4097, 512).astype(np.int32), (),
-                dict(Hq=64, Hkv=8, D=128, block_size=16, max_blocks=256, kv_dtype="fp8_e4m3"))
+                dict(Hq=64, Hkv=8, D=128, block_size=16, max_blocks=256,
+                     kv_dtype="fp8_e4m3" if name == "fp8_mixed" else "int4"))
     raise KeyError(name)
 
 
 DEFAULT_SEEDS = {"tiny": 0, "llama70b_layer": 1, "prefix_sharing": 2, "long_context": 3,
-                 "fp8_mixed": 4}
+                 "fp8_mixed": 4, "int4_mixed": 5}
 
 
 def make(name: str, seed: int | None = None, with_pools: bool = True) -> Batch:

@@ -216,6 +216,86 @@ def test_fp8_write_error_bound_random():
     assert np.all(np.abs(restored - xs) <= 6 * step)
 
 
+# ---------------------------------------------------------------- 4-bit cache write
+
+def _int4_setup(D=8, bs=4, nblocks=3, Hkv=1):
+    k_pool = np.zeros((nblocks, bs, Hkv, D // 2), np.uint8)
+    v_pool = np.zeros((nblocks, bs, Hkv, D // 2), np.uint8)
+    k_scale = np.full((nblocks, Hkv), 123.0, np.float32)
+    v_scale = np.full((nblocks, Hkv), 123.0, np.float32)
+    return k_pool, v_pool, k_scale, v_scale
+
+
+def _write4(vals, slot, pools):
+    kp, vp, ks, vs = pools
+    x = wl.bf16_bits(np.asarray(vals, np.float32)).reshape(1, 1, -1)
+    oracle.reshape_and_cache_int4(x, x, kp, vp, ks, vs, np.array([slot], np.int64), kp.shape[1])
+
+
+def _unpack4(row):
+    """Independent unpacking: element 2j in the low nibble of byte j, offset by 8."""
+    row = np.asarray(row, np.uint8)
+    out = np.empty(row.size * 2, np.int64)
+    out[0::2] = (row & 0xF).astype(np.int64) - 8
+    out[1::2] = (row >> 4).astype(np.int64) - 8
+    return out
+
+
+def test_int4_writer_reproduces_page_example(golden_dir):
+    g = _golden(golden_dir, "quant4_absmax.json")
+    pools = _int4_setup(D=6, bs=2, nblocks=1)
+    _write4(g["values"], 0, pools)
+    kp, vp, ks, vs = pools
+    assert _unpack4(kp[0, 0, 0]).tolist() == g["codes"]
+    restored = oracle.int4_restore(kp[0, 0, 0], float(ks[0, 0]))
+    assert np.round(restored, 3).tolist() == g["restored_3dp"]
+    assert ks[0, 0] == np.float32(1.0) / np.float32(7.0)
+
+
+def test_int4_writer_growth_requantises():
+    pools = _int4_setup()
+    kp, vp, ks, vs = pools
+    _write4([1.0, 0.3, -0.5 / 7, 0, 0, 0, 0, 0], 0, pools)   # codes 7, 2, 0 (-0.499 -> 0)
+    assert _unpack4(kp[0, 0, 0])[:3].tolist() == [7, 2, 0]
+    _write4([0.5, 0, 0, 0, 0, 0, 0, 0], 1, pools)             # smaller: scale kept
+    assert ks[0, 0] == np.float32(1.0) / np.float32(7.0)
+    # fp32: 0.5 / fl(1/7) = 3.4999999, just below the tie, so the code is 3
+    assert _unpack4(kp[0, 1, 0])[0] == 3
+    _write4([2.4 / 7, 0, 0, 0, 0, 0, 0, 0], 3, pools)         # bf16(2.4/7) / fl(1/7) = 2.40 -> 2
+    assert _unpack4(kp[0, 3, 0])[0] == 2
+    _write4([-3.0, 0, 0, 0, 0, 0, 0, 0], 2, pools)            # larger: rows 0, 1 re-encoded
+    assert ks[0, 0] == np.float32(3.0) / np.float32(7.0)
+    assert _unpack4(kp[0, 0, 0])[:2].tolist() == [2, 1]       # 1.0 -> 2.33 -> 2; 0.29 -> 0.67 -> 1
+    assert _unpack4(kp[0, 1, 0])[0] == 1                      # 0.43 -> 1.0 -> 1
+    assert _unpack4(kp[0, 2, 0])[0] == -7
+    _write4([0.0] * 8, 4, pools)                              # block 1 offset 0: zero scale
+    assert ks[1, 0] == 0.0 and np.all(_unpack4(kp[1, 0, 0]) == 0)
+
+
+def test_int4_writer_scale_is_block_absmax_random():
+    rng = np.random.default_rng(12)
+    pools = _int4_setup(D=32, bs=16, nblocks=1)
+    kp, vp, ks, vs = pools
+    xs = []
+    for off in range(16):
+        v = rng.standard_normal(32).astype(np.float32) * np.float32(rng.uniform(0.1, 3))
+        xs.append(wl.bf16_to_float(wl.bf16_bits(v)))
+        _write4(v, off, pools)
+    xs = np.array(xs)
+    assert ks[0, 0] == np.float32(np.abs(xs).max()) / np.float32(7.0)
+    codes = np.array([_unpack4(kp[0, r, 0]) for r in range(16)])
+    assert np.all(np.abs(codes) <= 7)
+    restored = codes * float(ks[0, 0])
+    # each requantisation moves a value by at most half a step of the scale it used
+    assert np.all(np.abs(restored - xs) <= 16 * 0.5 * float(ks[0, 0]) + 1e-7)
+
+
+def test_int4_restore_closed_form():
+    row = np.array([0x8F, 0x18, 0x77], np.uint8)          # nibbles (low, high): 15,8 8,1 7,7
+    got = oracle.int4_restore(row, 0.5)
+    assert got.tolist() == [3.5, 0.0, 0.0, -3.5, -0.5, -0.5]
+
+
 # ---------------------------------------------------------------- decode attention
 
 def _contiguous_reference(batch, window=0):
@@ -230,6 +310,14 @@ def _contiguous_reference(batch, window=0):
             torch.float64).numpy()
         kf = lut[batch.k_pool] * batch.k_scale.astype(np.float64)[:, None, :, None]
         vf = lut[batch.v_pool] * batch.v_scale.astype(np.float64)[:, None, :, None]
+    elif batch.kv_dtype == "int4":
+        def unpack(pool):
+            out = np.empty(pool.shape[:-1] + (pool.shape[-1] * 2,), np.float64)
+            out[..., 0::2] = (pool & 0xF).astype(np.float64) - 8
+            out[..., 1::2] = (pool >> 4).astype(np.float64) - 8
+            return out
+        kf = unpack(batch.k_pool) * batch.k_scale.astype(np.float64)[:, None, :, None]
+        vf = unpack(batch.v_pool) * batch.v_scale.astype(np.float64)[:, None, :, None]
     else:
         kf = wl.bf16_to_float(batch.k_pool).astype(np.float64)
         vf = wl.bf16_to_float(batch.v_pool).astype(np.float64)
@@ -301,6 +389,12 @@ def test_decode_window_ignores_blocks_before_it():
     batch.block_tables[0, :4] = 10 ** 6        # blocks wholly before position 80: never read
     batch.block_tables[1, :3] = -5             # before position 50
     assert np.array_equal(_oracle(batch, window=20), ref)
+
+
+def test_decode_int4_vs_contiguous_numpy():
+    batch = wl.build_batch("t", [3, 16, 33, 70, 0], Hq=8, Hkv=2, D=64, block_size=16, seed=5,
+                           kv_dtype="int4")
+    assert np.allclose(_oracle(batch), _contiguous_reference(batch), rtol=1e-12, atol=1e-13)
 
 
 def test_decode_rows_subset_matches_full():
