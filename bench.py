@@ -160,10 +160,11 @@ def cpu_baseline(batch, cores: int) -> dict:
     import oracle
     t0 = time.perf_counter()
     kp, vp = batch.k_pool.copy(), batch.v_pool.copy()
-    if batch.kv_dtype == "fp8_e4m3":
+    if batch.quantized:
         ks, vs = batch.k_scale.copy(), batch.v_scale.copy()
-        oracle.reshape_and_cache_fp8(batch.k_new, batch.v_new, kp, vp, ks, vs,
-                                     batch.slot_mapping, batch.block_size)
+        write = (oracle.reshape_and_cache_fp8 if batch.kv_dtype == "fp8_e4m3"
+                 else oracle.reshape_and_cache_int4)
+        write(batch.k_new, batch.v_new, kp, vp, ks, vs, batch.slot_mapping, batch.block_size)
     else:
         ks = vs = None
         oracle.reshape_and_cache_bf16(batch.k_new, batch.v_new, kp, vp, batch.slot_mapping,
@@ -277,7 +278,7 @@ def run_ours(args):
 
     unique_tokens = batch.unique_kv_tokens(args.window)
     kv_bytes = unique_tokens * batch.kv_bytes_per_token()
-    if batch.kv_dtype == "fp8_e4m3":
+    if batch.quantized:
         kv_bytes += sum(int(n) for n in (batch.seq_lens + batch.block_size - 1)
                         // batch.block_size) * batch.scale_bytes_per_block()
     peak, peak_kind = measured_peak_hbm()
@@ -295,7 +296,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3" if batch.kv_dtype == "fp8_e4m3" else "bf16",
+        "dtype": batch.kv_dtype,
         "data": "synthetic",
         "config": {
             "workload": args.config,
@@ -424,7 +425,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="llama70b_layer",
                     choices=["tiny", "llama70b_layer", "prefix_sharing", "long_context",
-                             "fp8_mixed"])
+                             "fp8_mixed", "int4_mixed"])
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--window", type=int, default=0,
                     help="sliding-window layer: attend over the last W positions (0 = all)")

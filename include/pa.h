@@ -46,12 +46,13 @@
  *    be NULL only if the caller vouches that the data is valid.
  *  - Shapes: B sequences (or tokens, for the cache write), Hq query heads,
  *    Hkv KV heads (Hq % Hkv == 0, G = Hq / Hkv <= 16), head dim D in {64, 128},
- *    block_size in {16, 32}.  FP8 pools need D = 128.
+ *    block_size in {16, 32}.  FP8 and 4-bit pools need D = 128.
  *  - Layouts:
  *      q            [B, Hq, D]                  bf16
  *      out          [B, Hq, D]                  fp32
- *      k/v pool     [nblocks, block_size, Hkv, D] bf16, or E4M3 codes (uint8)
- *      k/v scale    [nblocks, Hkv]              fp32 (FP8 pools only, else NULL)
+ *      k/v pool     [nblocks, block_size, Hkv, D] bf16, or E4M3 codes (uint8),
+ *                   or [nblocks, block_size, Hkv, D/2] packed 4-bit codes
+ *      k/v scale    [nblocks, Hkv]              fp32 (code pools only, else NULL)
  *      block_tables [B, max_blocks]             int32 physical block ids
  *      seq_lens     [B]                         int32 tokens in the cache,
  *                                               including this step's token
@@ -78,9 +79,13 @@ typedef enum {
     PA_ERR_DEVICE = 4         /* pa_read_error_flag found a PA_DEVERR_* bit */
 } pa_status;
 
-typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+/* Cached element formats.  PA_KV_INT4: signed 4-bit codes in [-7, 7] stored as
+ * offset-binary nibbles (code + 8), two per byte -- element 2j in the low nibble of
+ * byte j -- so a pool row is D / 2 bytes. */
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1, PA_KV_INT4 = 2 } pa_kv_dtype;
 
-/* Device error bits ORed into *err_flag. */
+/* Device error bits ORed into *err_flag (PA_DEVERR_FP8_CONFLICT also covers 4-bit
+ * pools: two tokens of one write call in one block). */
 #define PA_DEVERR_BLOCK_ID     1   /* block table entry outside [0, nblocks)        */
 #define PA_DEVERR_SEQ_LEN      2   /* seq_len < 0 or > max_blocks * block_size      */
 #define PA_DEVERR_SLOT         4   /* slot_mapping entry >= nblocks * block_size    */
@@ -150,13 +155,22 @@ pa_status pa_reshape_and_cache(const pa_shape *shape, const void *k_new, const v
                                pa_stream_t stream);
 
 /*
+ * 4-bit pools (kv_dtype = PA_KV_INT4, D = 128) are written the same way with
+ * largest code 7 ("KV Cache Engineering for LLM Serving", section 8, bits = 4):
+ *   scale = absmax since offset 0 / 7 (fp32 division); code = clip(rint(x /
+ *   scale), -7, 7) (fp32 division, ties to even); a growing scale re-encodes the
+ *   earlier rows from code * old scale (fp32 product); a zero scale stores 0.
+ */
+
+/*
  * pa_decode -- single-token decode attention over the paged cache, one CTA per
  * (sequence, KV head) serving the whole query group.
  * [P4] "Custom PagedAttention Kernels" (grid over sequence and head, block-table
  * walk, block staged in shared memory); [P3] section 1 (GQA grouping).
  *     out[b][h][:] = sum_t softmax_t(sm_scale * <q[b][h], K_b[t]>) V_b[t]
  * over t < seq_lens[b], where K_b[t] = k_pool[block_tables[b][t / bs]][t % bs]
- * [h / G] (same for V) and FP8 codes are restored as value * scale[block][kvh].
+ * [h / G] (same for V) and FP8 / 4-bit codes are restored as value *
+ * scale[block][kvh].
  * seq_lens[b] = 0 gives zeros.  out is fp32 [B, Hq, D].  opts: see pa_decode_opts.
  */
 pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void *k_pool,

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libpa.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE = range(5)
-PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+PA_KV_BF16, PA_KV_FP8_E4M3, PA_KV_INT4 = 0, 1, 2
 PA_DEVERR_BLOCK_ID, PA_DEVERR_SEQ_LEN, PA_DEVERR_SLOT = 1, 2, 4
 PA_DEVERR_FP8_CONFLICT, PA_DEVERR_TIMEOUT = 8, 16
 

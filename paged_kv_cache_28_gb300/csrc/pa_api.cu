@@ -18,14 +18,15 @@ pa_status check_shape(const pa_shape *s, bool need_q) {
   if (s->B < 0 || s->Hkv <= 0 || s->D <= 0 || s->block_size <= 0 || s->nblocks <= 0 ||
       s->max_blocks <= 0)
     return PA_ERR_INVALID_ARG;
-  if (s->kv_dtype != PA_KV_BF16 && s->kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  if (s->kv_dtype != PA_KV_BF16 && s->kv_dtype != PA_KV_FP8_E4M3 && s->kv_dtype != PA_KV_INT4)
+    return PA_ERR_INVALID_ARG;
   if (need_q) {
     if (s->Hq <= 0 || s->Hq % s->Hkv != 0) return PA_ERR_INVALID_ARG;
     if (s->Hq / s->Hkv > 16) return PA_ERR_UNSUPPORTED;
   }
   if (s->D != 64 && s->D != 128) return PA_ERR_UNSUPPORTED;
   if (s->block_size != 16 && s->block_size != 32) return PA_ERR_UNSUPPORTED;
-  if (s->kv_dtype == PA_KV_FP8_E4M3 && s->D != 128) return PA_ERR_UNSUPPORTED;
+  if (s->kv_dtype != PA_KV_BF16 && s->D != 128) return PA_ERR_UNSUPPORTED;
   // every row index and tile count below must fit in int32
   if (static_cast<int64_t>(s->nblocks) * s->block_size >= (int64_t(1) << 31))
     return PA_ERR_INVALID_ARG;
@@ -50,7 +51,7 @@ pa_status check_decode_args(const pa_shape *shape, const float *out, const void 
   if (st != PA_OK) return st;
   st = check_ptrs({out, q, k_pool, v_pool, bt, sl});
   if (st != PA_OK) return st;
-  if (shape->kv_dtype == PA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  if (shape->kv_dtype != PA_KV_BF16 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
   if (opts) {
     if (opts->window < 0 || opts->reserved != 0) return PA_ERR_INVALID_ARG;
     if (opts->shared_prefix_lens && !aligned16(opts->shared_prefix_lens)) return PA_ERR_INVALID_ARG;
@@ -73,7 +74,7 @@ pa_status pa_reshape_and_cache(const pa_shape *shape, const void *k_new, const v
   if (shape->B == 0) return PA_OK;
   st = check_ptrs({k_new, v_new, k_pool, v_pool, slot_mapping});
   if (st != PA_OK) return st;
-  if (shape->kv_dtype == PA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  if (shape->kv_dtype != PA_KV_BF16 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
   return pa::run_reshape_and_cache(*shape, k_new, v_new, k_pool, v_pool, k_scale, v_scale,
                                    slot_mapping, err_flag, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -40,21 +40,29 @@ namespace pa {
 // configuration
 // ----------------------------------------------------------------------------
 
-template <int D_, int NT_, bool FP8_>
+// Cached element kinds.
+constexpr int kKindBf16 = 0;
+constexpr int kKindFp8 = 1;   // E4M3 codes, one per byte
+constexpr int kKindInt4 = 2;  // 4-bit codes, two per byte (offset binary)
+
+template <int D_, int NT_, int KIND_>
 struct Cfg {
   static constexpr int D = D_;
   static constexpr int NT = NT_;            // 8-head n-tiles (G <= 8 * NT)
-  static constexpr bool FP8 = FP8_;
+  static constexpr int KIND = KIND_;
+  static constexpr bool FP8 = KIND == kKindFp8;
+  static constexpr bool INT4 = KIND == kKindInt4;
+  static constexpr bool QUANT = KIND != kKindBf16;   // codes x per-(block, head) scale
   static constexpr int KS = D / 16;         // QK k-steps of 16 elements
   static constexpr int DT = D / 16;         // PV 16-row output tiles
-  static constexpr int EB = FP8 ? 1 : 2;    // bytes per cached element
-  static constexpr int ROW = D * EB;        // bytes of one token's head vector
-  static constexpr int HALVES = ROW / 128;  // 128-byte swizzle spans per row
-  static constexpr int BOX_X = 128 / EB;    // TMA box width in elements
+  static constexpr int ROW = INT4 ? D / 2 : (FP8 ? D : 2 * D);  // bytes of one token's head row
+  static constexpr int BOX_BYTES = ROW < 128 ? ROW : 128;        // TMA box width (swizzle span)
+  static constexpr int BOXES = ROW / BOX_BYTES;                  // boxes per tile row
+  static constexpr int BOX_X = BOX_BYTES / (KIND == kKindBf16 ? 2 : 1);  // box width in elements
   static constexpr int KV_BYTES = kTile * ROW;
   static constexpr int Q_BYTES = 8 * NT * D * 2;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = INT4 ? 4 : 2;
   static constexpr int WARPS = 4;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int META_BYTES = 32;     // int4 unit + k/v scale
@@ -117,17 +125,30 @@ struct State {
 // Output row (d) of accumulator element i of d-tile dt for this lane.
 template <class C>
 __device__ __forceinline__ int acc_d(int dt, int i, int lane) {
-  if constexpr (C::FP8)
+  if constexpr (C::INT4)   // d-tile (chunk c = dt/2, half dt%2): rows 4r + 2 half + {0, 1}
+    return (dt >> 1) * 32 + 4 * (lane >> 2) + 2 * (dt & 1) + (i >> 1);
+  else if constexpr (C::FP8)
     return dt * 16 + 2 * (lane >> 2) + (i >> 1);
   else
     return dt * 16 + (lane >> 2) + (i >> 1) * 8;
+}
+
+// Four signed 4-bit codes stored as offset-binary nibbles at bits 4i.. and 4i+16..
+// of w (after w >> 4i): as f16 bits 0x6400 | u the halves are exactly 1024 + u, so
+// subtracting 1032 leaves the code.  Returns {nibble i, nibble i + 4} as f16x2.
+__device__ __forceinline__ uint32_t int4_pair_f16(uint32_t w, int i) {
+  uint32_t h;
+  const uint32_t x = w >> (4 * i);
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(x), "r"(0x000F000Fu), "r"(0x64006400u));
+  const __half2 v = __hsub2(*reinterpret_cast<const __half2 *>(&h), __floats2half2_rn(1032.f, 1032.f));
+  return *reinterpret_cast<const uint32_t *>(&v);
 }
 
 // Load the group's Q^T fragments from the stage's Q slot ([8*NT rows][D] bf16).
 template <class C>
 __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint16_t *qslot_ptr,
                                        int lane) {
-  if constexpr (!C::FP8) {
+  if constexpr (!C::QUANT) {
 #pragma unroll
     for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
@@ -142,9 +163,11 @@ __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint1
         st.qf[nt][ks + 1][1] = r[3];
       }
   } else {
-    // K codes arrive in a permuted order (see process_tile): k-step ks, lane (r, q)
-    // pairs Q[g=r][16ks + 4q + {0,1}] and Q[g=r][16ks + 4q + {2,3}].  q is scaled by
-    // 2^k so that its largest magnitude sits just below 2^15 (exact in f16).
+    // K codes arrive in a permuted order (see process_tile).  FP8: k-step ks, lane
+    // (r, q) pairs Q[g=r][16ks + 4q + {0,1}] and Q[g=r][16ks + 4q + {2,3}].  4-bit:
+    // k-step ks = 2c + u pairs Q[r][b + 2u + {0,4}] and Q[r][b + 2u + {1,5}] with
+    // b = 32c + 8q.  q is scaled by 2^k so that its largest magnitude sits just
+    // below 2^15 (exact in f16).
     const int r = lane >> 2, qd = lane & 3;
     uint2 raw[C::NT][C::KS];
     float amax = 0.f;
@@ -152,8 +175,9 @@ __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint1
     for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
       for (int ks = 0; ks < C::KS; ++ks) {
-        raw[nt][ks] = *reinterpret_cast<const uint2 *>(qslot_ptr + (nt * 8 + r) * C::D +
-                                                       ks * 16 + qd * 4);
+        // 4-bit: the eight values b..b+7 of chunk c arrive as two uint2 (u = 0, 1)
+        const int off = C::INT4 ? (ks >> 1) * 32 + qd * 8 + (ks & 1) * 4 : ks * 16 + qd * 4;
+        raw[nt][ks] = *reinterpret_cast<const uint2 *>(qslot_ptr + (nt * 8 + r) * C::D + off);
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(raw[nt][ks].x)), fabsf(bf16_hi(raw[nt][ks].x))),
                                  fmaxf(fabsf(bf16_lo(raw[nt][ks].y)), fabsf(bf16_hi(raw[nt][ks].y)))));
       }
@@ -170,9 +194,19 @@ __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint1
     for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
       for (int ks = 0; ks < C::KS; ++ks) {
-        const uint2 v = raw[nt][ks];
-        st.qf[nt][ks][0] = pack_f16(bf16_lo(v.x) * up, bf16_hi(v.x) * up);
-        st.qf[nt][ks][1] = pack_f16(bf16_lo(v.y) * up, bf16_hi(v.y) * up);
+        if constexpr (C::INT4) {
+          // ks = 2c + u: values b + 2u + {0,1,2,3} sit in raw[.][2c] (u = 0: 0..3 of b)
+          // and raw[.][2c + 1] (4..7 of b); pair (2u, 2u + 4) and (2u + 1, 2u + 5)
+          const uint2 lo4 = raw[nt][ks & ~1], hi4 = raw[nt][ks | 1];
+          const uint32_t e = (ks & 1) ? lo4.y : lo4.x;   // values b+2u, b+2u+1
+          const uint32_t f = (ks & 1) ? hi4.y : hi4.x;   // values b+2u+4, b+2u+5
+          st.qf[nt][ks][0] = pack_f16(bf16_lo(e) * up, bf16_lo(f) * up);
+          st.qf[nt][ks][1] = pack_f16(bf16_hi(e) * up, bf16_hi(f) * up);
+        } else {
+          const uint2 v = raw[nt][ks];
+          st.qf[nt][ks][0] = pack_f16(bf16_lo(v.x) * up, bf16_hi(v.x) * up);
+          st.qf[nt][ks][1] = pack_f16(bf16_lo(v.y) * up, bf16_hi(v.y) * up);
+        }
       }
   }
 }
@@ -216,7 +250,7 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
     for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
 
   // ---- S^T = K Q^T
-  if constexpr (!C::FP8) {
+  if constexpr (!C::QUANT) {
     const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
     for (int ks = 0; ks < C::KS; ++ks) {
@@ -225,6 +259,28 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
       ldsm_x4(a, ktile + (ks >> 2) * (kTile * 128) + row * 128 + ((c ^ (row & 7)) << 4));
 #pragma unroll
       for (int nt = 0; nt < C::NT; ++nt) mma_bf16(s[nt], a, st.qf[nt][ks][0], st.qf[nt][ks][1]);
+    }
+  } else if constexpr (C::INT4) {
+    // 64-byte rows, 64-byte swizzle: lane (r, q) receives nibbles b..b+7 (b = 32c + 8q)
+    // of row r; int4_pair_f16 yields the pairs (b+i, b+i+4) that load_q mirrors.
+    const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+    for (int cc = 0; cc < C::D / 64; ++cc) {
+      const int c = 2 * cc + (lane >> 4);
+      uint32_t R[4];
+      ldsm_x4(R, ktile + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+#pragma unroll
+      for (int half = 0; half < 2; ++half)      // chunk 2cc + half: R[2 half] rows r, R[2 half + 1] rows r + 8
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * u),
+                                 int4_pair_f16(R[2 * half + 1], 2 * u),
+                                 int4_pair_f16(R[2 * half], 2 * u + 1),
+                                 int4_pair_f16(R[2 * half + 1], 2 * u + 1)};
+          const int ks = (2 * cc + half) * 2 + u;
+#pragma unroll
+          for (int nt = 0; nt < C::NT; ++nt) mma_f16(s[nt], a, st.qf[nt][ks][0], st.qf[nt][ks][1]);
+        }
     }
   } else {
     // ldmatrix on byte pairs: lane (r, q) receives codes 4q..4q+3 of a 16-code chunk;
@@ -270,14 +326,14 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
       p[nt][j] = ex2(x[j] - mnew);
       p[nt][j + 2] = ex2(x[j + 2] - mnew);
       st.l[nt][j] = st.l[nt][j] * alpha + (p[nt][j] + p[nt][j + 2]);
-      corr[nt][j] = C::FP8 ? alpha * (st.vs / vs) : alpha;
+      corr[nt][j] = C::QUANT ? alpha * (st.vs / vs) : alpha;
     }
 #pragma unroll
     for (int dt = 0; dt < C::DT; ++dt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) st.acc[nt][dt][i] *= corr[nt][i & 1];
   }
-  if constexpr (C::FP8) st.vs = vs;
+  if constexpr (C::QUANT) st.vs = vs;
 
   // ---- P^T fragments: hi + lo 16-bit parts, transposed in registers
   uint32_t bh[C::NT][2], bl[C::NT][2];
@@ -287,16 +343,17 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
     for (int h = 0; h < 2; ++h) {
       const float p0 = p[nt][2 * h], p1 = p[nt][2 * h + 1];
       uint32_t hi, lo;
-      if constexpr (!C::FP8) {
+      if constexpr (!C::QUANT) {
         hi = pack_bf16(p0, p1);
         lo = pack_bf16(p0 - bf16_lo(hi), p1 - bf16_hi(hi));
       } else {
-        // f16 keeps 11 significant bits of p: one term is enough for the FP8 tolerance
+        // f16 keeps 11 significant bits of p: one term is enough for the quantised
+        // caches' tolerance
         hi = pack_f16(p0, p1);
         lo = 0;
       }
       bh[nt][h] = movmatrix_trans(hi);
-      if constexpr (!C::FP8) bl[nt][h] = movmatrix_trans(lo);
+      if constexpr (!C::QUANT) bl[nt][h] = movmatrix_trans(lo);
     }
   }
 
@@ -309,7 +366,7 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
     m01 = (in(2 * qd) ? 0x0000FFFFu : 0u) | (in(2 * qd + 1) ? 0xFFFF0000u : 0u);
     m23 = (in(2 * qd + 8) ? 0x0000FFFFu : 0u) | (in(2 * qd + 9) ? 0xFFFF0000u : 0u);
   }
-  if constexpr (!C::FP8) {
+  if constexpr (!C::QUANT) {
     const int t = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
     for (int dt = 0; dt < C::DT; ++dt) {
@@ -327,6 +384,35 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
         mma_bf16(st.acc[nt][dt], a, bh[nt][0], bh[nt][1]);
         mma_bf16(st.acc[nt][dt], a, bl[nt][0], bl[nt][1]);
       }
+    }
+  } else if constexpr (C::INT4) {
+    // ldmatrix.trans on the byte-pair view gives lane (r, q) the nibbles d = 32c + 4r
+    // .. +3 of tokens 2q (low half) and 2q + 1 (high half): int4_pair_f16(., i) is
+    // V^T row d = 32c + 4r + i over tokens (2q, 2q + 1).
+    const int t = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+    for (int cc = 0; cc < C::D / 64; ++cc) {
+      const int c = 2 * cc + (lane >> 4);
+      uint32_t R[4];
+      ldsm_x4_trans(R, vtile + t * 64 + ((c ^ ((t >> 1) & 3)) << 4));
+#pragma unroll
+      for (int half = 0; half < 2; ++half)      // chunk 2cc + half
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {        // rows 4r + 2mt + {0, 1}
+          uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * mt),
+                           int4_pair_f16(R[2 * half], 2 * mt + 1),
+                           int4_pair_f16(R[2 * half + 1], 2 * mt),
+                           int4_pair_f16(R[2 * half + 1], 2 * mt + 1)};
+          if (partial) {
+            a[0] &= m01;
+            a[1] &= m01;
+            a[2] &= m23;
+            a[3] &= m23;
+          }
+          const int dt = (2 * cc + half) * 2 + mt;
+#pragma unroll
+          for (int nt = 0; nt < C::NT; ++nt) mma_f16(st.acc[nt][dt], a, bh[nt][0], bh[nt][1]);
+        }
     }
   } else {
     // ldmatrix.trans on byte pairs gives lane (r, q): bytes (t=2q: d=2r, 2r+1) and
@@ -386,7 +472,7 @@ __device__ __forceinline__ void write_normalised(const State<C> &st, float *dst,
     for (int j = 0; j < 2; ++j) {
       const int g = nt * 8 + 2 * qd + j;
       if (g >= G) continue;
-      const float f = (C::FP8 ? st.vs : 1.f) / ltot[nt][j];
+      const float f = (C::QUANT ? st.vs : 1.f) / ltot[nt][j];
 #pragma unroll
       for (int dt = 0; dt < C::DT; ++dt) {
         dst[g * C::D + acc_d<C>(dt, j, lane)] = st.acc[nt][dt][j] * f;
@@ -522,7 +608,7 @@ __device__ __forceinline__ void issue(const WarpSmem &ws, int s, int4 u, const P
   const int phys = u.x, pair = u.y, tile = u.z;
   const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
   ws.meta[2 * s] = u;
-  if constexpr (C::FP8) {
+  if constexpr (C::QUANT) {
     float *sc = reinterpret_cast<float *>(&ws.meta[2 * s + 1]);
     if (phys != kInvalidPhys) {
       cp_async_4(smem_u32(sc), p.k_scale + static_cast<size_t>(phys) * p.Hkv + kvh);
@@ -539,20 +625,22 @@ __device__ __forceinline__ void issue(const WarpSmem &ws, int s, int4 u, const P
   const uint32_t dst = smem_u32(stage);
   fence_proxy_async();
   mbar_arrive_expect_tx(bar, bytes);
+  // the row of KV head kvh starts at element kvh * (ROW / element bytes)
+  const int x0 = kvh * C::BOXES * C::BOX_X;
   if (u.w & (kHintShared | kHintPrivate)) {
     const uint64_t pol = (u.w & kHintShared) ? l2_policy_evict_last() : l2_policy_evict_first();
 #pragma unroll
-    for (int h = 0; h < C::HALVES; ++h) {
-      const int x = kvh * C::D + h * C::BOX_X;
-      tma_load_2d_hint(dst + h * (kTile * 128), tmK, x, y, bar, pol);
-      tma_load_2d_hint(dst + C::KV_BYTES + h * (kTile * 128), tmV, x, y, bar, pol);
+    for (int h = 0; h < C::BOXES; ++h) {
+      const int x = x0 + h * C::BOX_X;
+      tma_load_2d_hint(dst + h * (kTile * C::BOX_BYTES), tmK, x, y, bar, pol);
+      tma_load_2d_hint(dst + C::KV_BYTES + h * (kTile * C::BOX_BYTES), tmV, x, y, bar, pol);
     }
   } else {
 #pragma unroll
-    for (int h = 0; h < C::HALVES; ++h) {
-      const int x = kvh * C::D + h * C::BOX_X;
-      tma_load_2d(dst + h * (kTile * 128), tmK, x, y, bar);
-      tma_load_2d(dst + C::KV_BYTES + h * (kTile * 128), tmV, x, y, bar);
+    for (int h = 0; h < C::BOXES; ++h) {
+      const int x = x0 + h * C::BOX_X;
+      tma_load_2d(dst + h * (kTile * C::BOX_BYTES), tmK, x, y, bar);
+      tma_load_2d(dst + C::KV_BYTES + h * (kTile * C::BOX_BYTES), tmV, x, y, bar);
     }
   }
   if (with_q)
@@ -597,7 +685,7 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
                 reinterpret_cast<const uint16_t *>(stage + 2 * C::KV_BYTES), lane);
       piece_first = (u.w & kFirstOfPair) != 0;
     }
-    if constexpr (C::FP8) {
+    if constexpr (C::QUANT) {
       const float4 sc = *reinterpret_cast<const float4 *>(&ws.meta[2 * s + 1]);
       sscale = p.sl2 * sc.x * st.qshift;
       vs = sc.y;
@@ -623,7 +711,7 @@ __device__ __forceinline__ WarpSmem setup_smem(uint8_t *raw, int warp, int G, in
   ws.meta = reinterpret_cast<int4 *>(tail + C::WARPS * C::STAGES * 8) + warp * C::STAGES * 2;
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < C::STAGES; ++s) mbar_init(smem_u32(&ws.bar[s]), C::FP8 ? 2 : 1);
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(smem_u32(&ws.bar[s]), C::QUANT ? 2 : 1);
     fence_mbar_init();
   }
   // query rows G..8*NT-1 of every Q slot stay zero (the bulk copy writes G rows)
@@ -704,7 +792,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
           sm_m[warp * GP + g] = st.m[nt][j];
           sm_l[warp * GP + g] = ltot[nt][j];
         }
-        const float f = C::FP8 ? st.vs : 1.f;
+        const float f = C::QUANT ? st.vs : 1.f;
 #pragma unroll
         for (int dt = 0; dt < C::DT; ++dt) {
           sm_acc[(warp * GP + g) * C::D + acc_d<C>(dt, j, lane)] = st.acc[nt][dt][j] * f;
@@ -914,25 +1002,31 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D view of a pool: rows = nblocks * bs tokens, columns = Hkv * D elements;
-// box = 16 rows x 128 bytes, 128-byte swizzle.
+// 2D view of a pool: rows = nblocks * bs tokens, columns = one token's Hkv head rows
+// (bf16 elements, or bytes for the code pools); box = 16 rows x one head row of up to
+// 128 bytes, swizzled by the box width (128 or 64 bytes).
 static bool make_pool_map(CUtensorMap *map, const void *pool, const pa_shape &s) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
-  const int eb = fp8 ? 1 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.Hkv) * s.D,
+  const bool bf16 = s.kv_dtype == PA_KV_BF16;
+  const int row_bytes = s.kv_dtype == PA_KV_INT4 ? s.D / 2 : (bf16 ? 2 * s.D : s.D);
+  const int box_bytes = row_bytes < 128 ? row_bytes : 128;
+  const int eb = bf16 ? 2 : 1;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.Hkv) * row_bytes / eb,
                         static_cast<cuuint64_t>(s.nblocks) * s.block_size};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(s.Hkv) * s.D * eb};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(kTile)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(s.Hkv) * row_bytes};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / eb), static_cast<cuuint32_t>(kTile)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  // promote L2 fills to one head row: 256 B for bf16 D = 128, 128 B for 128-byte
+  // rows, none for 64-byte rows (a wider fill would pull in the next head's row)
+  const CUtensorMapL2promotion promo =
+      row_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                       : (row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                           : CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                   const_cast<void *>(pool), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  // promote L2 fills to one head row: 256 B for bf16 D = 128, else 128 B
-                  // (a wider fill would pull in the neighbouring KV head's row)
-                  s.D * eb >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
-                                  : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, promo,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -992,52 +1086,58 @@ static pa_status launch_segments(const Params &p, const CUtensorMap &mk, const C
 }
 
 // Dispatch on (D, n-tiles, dtype).
-#define PA_DISPATCH(D_, NT_, FP8_, FN, ...)                                   \
-  if (s.D == D_ && nt == NT_ && fp8 == FP8_) return FN<Cfg<D_, NT_, FP8_>>(__VA_ARGS__);
+#define PA_DISPATCH(D_, NT_, KIND_, FN, ...)                                  \
+  if (s.D == D_ && nt == NT_ && kind == KIND_) return FN<Cfg<D_, NT_, KIND_>>(__VA_ARGS__);
+
+static int kind_of(const pa_shape &s) {
+  return s.kv_dtype == PA_KV_FP8_E4M3 ? kKindFp8 : (s.kv_dtype == PA_KV_INT4 ? kKindInt4 : kKindBf16);
+}
+
+#define PA_DISPATCH_ALL(FN, ...)                      \
+  PA_DISPATCH(128, 1, kKindBf16, FN, __VA_ARGS__)     \
+  PA_DISPATCH(128, 2, kKindBf16, FN, __VA_ARGS__)     \
+  PA_DISPATCH(64, 1, kKindBf16, FN, __VA_ARGS__)      \
+  PA_DISPATCH(64, 2, kKindBf16, FN, __VA_ARGS__)      \
+  PA_DISPATCH(128, 1, kKindFp8, FN, __VA_ARGS__)      \
+  PA_DISPATCH(128, 2, kKindFp8, FN, __VA_ARGS__)      \
+  PA_DISPATCH(128, 1, kKindInt4, FN, __VA_ARGS__)     \
+  PA_DISPATCH(128, 2, kKindInt4, FN, __VA_ARGS__)
 
 static pa_status dispatch_pair(const pa_shape &s, const Params &p, const CUtensorMap &mk,
                                const CUtensorMap &mv, cudaStream_t st) {
   const int nt = (p.G + 7) / 8;
-  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
-  PA_DISPATCH(128, 1, false, launch_pair, p, mk, mv, st)
-  PA_DISPATCH(128, 2, false, launch_pair, p, mk, mv, st)
-  PA_DISPATCH(64, 1, false, launch_pair, p, mk, mv, st)
-  PA_DISPATCH(64, 2, false, launch_pair, p, mk, mv, st)
-  PA_DISPATCH(128, 1, true, launch_pair, p, mk, mv, st)
-  PA_DISPATCH(128, 2, true, launch_pair, p, mk, mv, st)
+  const int kind = kind_of(s);
+  PA_DISPATCH_ALL(launch_pair, p, mk, mv, st)
   return PA_ERR_UNSUPPORTED;
 }
 
 static pa_status dispatch_segments(const pa_shape &s, const Params &p, const CUtensorMap &mk,
                                    const CUtensorMap &mv, cudaStream_t st) {
   const int nt = (p.G + 7) / 8;
-  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
-  PA_DISPATCH(128, 1, false, launch_segments, p, mk, mv, st)
-  PA_DISPATCH(128, 2, false, launch_segments, p, mk, mv, st)
-  PA_DISPATCH(64, 1, false, launch_segments, p, mk, mv, st)
-  PA_DISPATCH(64, 2, false, launch_segments, p, mk, mv, st)
-  PA_DISPATCH(128, 1, true, launch_segments, p, mk, mv, st)
-  PA_DISPATCH(128, 2, true, launch_segments, p, mk, mv, st)
+  const int kind = kind_of(s);
+  PA_DISPATCH_ALL(launch_segments, p, mk, mv, st)
   return PA_ERR_UNSUPPORTED;
 }
 
+template <class C>
+static int cfg_split_smem(int B) { return split_smem<C>(B); }
+template <class C>
+static int cfg_min_blocks(int) { return C::MIN_BLOCKS; }
+
 int splitkv_smem_bytes(const pa_shape &s) {
   const int nt = (s.Hq / s.Hkv + 7) / 8;
-  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
-  if (fp8) return nt == 1 ? split_smem<Cfg<128, 1, true>>(s.B) : split_smem<Cfg<128, 2, true>>(s.B);
-  if (s.D == 64)
-    return nt == 1 ? split_smem<Cfg<64, 1, false>>(s.B) : split_smem<Cfg<64, 2, false>>(s.B);
-  return nt == 1 ? split_smem<Cfg<128, 1, false>>(s.B) : split_smem<Cfg<128, 2, false>>(s.B);
+  const int kind = kind_of(s);
+  PA_DISPATCH_ALL(cfg_split_smem, s.B)
+  return 0;
 }
 
 int decode_warps_per_cta() { return Cfg<128, 1, false>::WARPS; }
 
 int splitkv_min_blocks(const pa_shape &s) {
   const int nt = (s.Hq / s.Hkv + 7) / 8;
-  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
-  if (fp8) return nt == 1 ? Cfg<128, 1, true>::MIN_BLOCKS : Cfg<128, 2, true>::MIN_BLOCKS;
-  if (s.D == 64) return nt == 1 ? Cfg<64, 1, false>::MIN_BLOCKS : Cfg<64, 2, false>::MIN_BLOCKS;
-  return nt == 1 ? Cfg<128, 1, false>::MIN_BLOCKS : Cfg<128, 2, false>::MIN_BLOCKS;
+  const int kind = kind_of(s);
+  PA_DISPATCH_ALL(cfg_min_blocks, 0)
+  return 1;
 }
 
 WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits) {

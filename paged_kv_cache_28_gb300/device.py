@@ -24,11 +24,12 @@ class DeviceBatch:
         instead of uploading batch.k_pool / batch.v_pool (for large generated pools)."""
         self.batch = batch
         self.device = torch.device(device)
-        fp8 = batch.kv_dtype == "fp8_e4m3"
+        fp8 = batch.quantized            # code pools (E4M3 or 4-bit) with scales
         self.fp8 = fp8
+        kind = {"bf16": _lib.PA_KV_BF16, "fp8_e4m3": _lib.PA_KV_FP8_E4M3,
+                "int4": _lib.PA_KV_INT4}[batch.kv_dtype]
         self.shape = _lib.make_shape(batch.B, batch.Hq, batch.Hkv, batch.D, batch.block_size,
-                                     batch.nblocks, batch.max_blocks,
-                                     _lib.PA_KV_FP8_E4M3 if fp8 else _lib.PA_KV_BF16)
+                                     batch.nblocks, batch.max_blocks, kind)
         self.q = to_device_bf16(batch.q, self.device)
         self.k_new = to_device_bf16(batch.k_new, self.device)
         self.v_new = to_device_bf16(batch.v_new, self.device)

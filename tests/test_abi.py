@@ -59,6 +59,7 @@ def _decode(lib, s, **ptr):
     (dict(D=96), _lib.PA_ERR_UNSUPPORTED),
     (dict(block_size=8), _lib.PA_ERR_UNSUPPORTED),
     (dict(kv_dtype=_lib.PA_KV_FP8_E4M3), _lib.PA_ERR_UNSUPPORTED),   # FP8 needs D = 128
+    (dict(kv_dtype=_lib.PA_KV_INT4), _lib.PA_ERR_UNSUPPORTED),       # so does 4-bit
     (dict(kv_dtype=7), _lib.PA_ERR_INVALID_ARG),
     (dict(nblocks=0), _lib.PA_ERR_INVALID_ARG),
     (dict(B=-1), _lib.PA_ERR_INVALID_ARG),

@@ -17,7 +17,7 @@ from paged_kv_cache_28_gb300.device import DeviceBatch, default_num_splits
 pytestmark = pytest.mark.gpu
 
 TOL_BF16 = (1e-3, 1e-3)   # (atol, rtol)
-TOL_FP8 = (2e-2, 2e-2)
+TOL_FP8 = (2e-2, 2e-2)    # FP8 and 4-bit caches, against an oracle reading the same codes
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -28,7 +28,7 @@ def _cuda():
 
 
 def _tol(batch):
-    return TOL_FP8 if batch.kv_dtype == "fp8_e4m3" else TOL_BF16
+    return TOL_FP8 if batch.quantized else TOL_BF16
 
 
 def assert_close(gpu, ref, batch, what=""):
@@ -52,6 +52,9 @@ def oracle_after_write(batch, rows=None, write=True, window=0):
         if batch.kv_dtype == "fp8_e4m3":
             oracle.reshape_and_cache_fp8(batch.k_new, batch.v_new, kp, vp, ks, vs,
                                          batch.slot_mapping, batch.block_size)
+        elif batch.kv_dtype == "int4":
+            oracle.reshape_and_cache_int4(batch.k_new, batch.v_new, kp, vp, ks, vs,
+                                          batch.slot_mapping, batch.block_size)
         else:
             oracle.reshape_and_cache_bf16(batch.k_new, batch.v_new, kp, vp, batch.slot_mapping,
                                           batch.block_size)
@@ -118,14 +121,18 @@ def test_reshape_and_cache_bf16_canary_and_padding():
     assert _lib.pa_read_error_flag(err) == 0
 
 
-def _fp8_write_case(seed, T, Hkv, bs, nblocks, steps):
+def _fp8_write_case(seed, T, Hkv, bs, nblocks, steps, int4=False):
     """Several write calls; each writes one token into each of T distinct blocks at
     increasing offsets, so scales grow and rows get re-encoded."""
     rng = np.random.default_rng(seed)
     D = 128
-    k_pool = rng.integers(0, 256, (nblocks, bs, Hkv, D)).astype(np.uint8)
-    k_pool[k_pool == 0x7F] = 0
-    k_pool[k_pool == 0xFF] = 0
+    if int4:      # any nibbles 1..15 (codes -7..7)
+        k_pool = (rng.integers(1, 16, (nblocks, bs, Hkv, D // 2)) |
+                  (rng.integers(1, 16, (nblocks, bs, Hkv, D // 2)) << 4)).astype(np.uint8)
+    else:
+        k_pool = rng.integers(0, 256, (nblocks, bs, Hkv, D)).astype(np.uint8)
+        k_pool[k_pool == 0x7F] = 0
+        k_pool[k_pool == 0xFF] = 0
     v_pool = k_pool.copy()
     k_scale = rng.uniform(0.001, 0.01, (nblocks, Hkv)).astype(np.float32)
     v_scale = k_scale.copy()
@@ -133,7 +140,9 @@ def _fp8_write_case(seed, T, Hkv, bs, nblocks, steps):
     dks, dvs = torch.from_numpy(k_scale).cuda(), torch.from_numpy(v_scale).cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     blocks = rng.choice(nblocks, T, replace=False)
-    shape = _lib.make_shape(T, Hkv, Hkv, D, bs, nblocks, 1, _lib.PA_KV_FP8_E4M3)
+    shape = _lib.make_shape(T, Hkv, Hkv, D, bs, nblocks, 1,
+                            _lib.PA_KV_INT4 if int4 else _lib.PA_KV_FP8_E4M3)
+    write = oracle.reshape_and_cache_int4 if int4 else oracle.reshape_and_cache_fp8
     for step in range(steps):
         scale = rng.uniform(0.05, 4.0, (T, 1, 1)).astype(np.float32)
         x = rng.standard_normal((T, Hkv, D)).astype(np.float32) * scale
@@ -146,7 +155,7 @@ def _fp8_write_case(seed, T, Hkv, bs, nblocks, steps):
         _lib.pa_reshape_and_cache(shape, torch.from_numpy(k_new.view(np.int16)).cuda(),
                                   torch.from_numpy(v_new.view(np.int16)).cuda(), dk, dv, dks, dvs,
                                   torch.from_numpy(slots).cuda(), err)
-        oracle.reshape_and_cache_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, slots, bs)
+        write(k_new, v_new, k_pool, v_pool, k_scale, v_scale, slots, bs)
     torch.cuda.synchronize()
     assert _lib.pa_read_error_flag(err) == 0
     return (dk.cpu().numpy(), dv.cpu().numpy(), dks.cpu().numpy(), dvs.cpu().numpy()), \
@@ -157,6 +166,15 @@ def _fp8_write_case(seed, T, Hkv, bs, nblocks, steps):
                                                   (2, 9, 1, 32, 32)])
 def test_reshape_and_cache_fp8_bit_exact(seed, T, Hkv, bs, steps):
     got, want = _fp8_write_case(seed, T, Hkv, bs, 3 * T + 2, steps)
+    for g, w, name in zip(got, want, ("k_pool", "v_pool", "k_scale", "v_scale")):
+        assert np.array_equal(g.view(np.uint8) if g.dtype != np.float32 else g.view(np.uint32),
+                              w.view(np.uint8) if w.dtype != np.float32 else w.view(np.uint32)), name
+
+
+@pytest.mark.parametrize("seed,T,Hkv,bs,steps", [(3, 5, 2, 16, 16), (4, 64, 8, 16, 6),
+                                                  (5, 9, 1, 32, 32)])
+def test_reshape_and_cache_int4_bit_exact(seed, T, Hkv, bs, steps):
+    got, want = _fp8_write_case(seed, T, Hkv, bs, 3 * T + 2, steps, int4=True)
     for g, w, name in zip(got, want, ("k_pool", "v_pool", "k_scale", "v_scale")):
         assert np.array_equal(g.view(np.uint8) if g.dtype != np.float32 else g.view(np.uint32),
                               w.view(np.uint8) if w.dtype != np.float32 else w.view(np.uint32)), name
@@ -217,6 +235,27 @@ def test_fp8_small_all_modes():
     dev.reshape_and_cache()
     ref, _ = oracle_after_write(batch)
     _modes_run(dev, batch, ref, "fp8")
+
+
+def test_int4_small_all_modes():
+    batch = wl.build_batch("t", [1, 16, 17, 200, 33, 0, 1000], Hq=64, Hkv=8, D=128, block_size=16,
+                           seed=23, kv_dtype="int4")
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch)
+    _modes_run(dev, batch, ref, "int4")
+
+
+def test_int4_g16_bs32_window():
+    batch = wl.build_batch("t", [3, 64, 65, 400], Hq=32, Hkv=2, D=128, block_size=32, seed=24,
+                           kv_dtype="int4")
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch)
+    _modes_run(dev, batch, ref, "int4 G=16 bs=32")
+    ref, _ = oracle_after_write(batch, window=50)
+    for mode, ns in (("decode", None), ("split", 7)):
+        assert_close(run_gpu(dev, mode, ns, window=50), ref, batch, f"int4 window {mode}")
 
 
 def test_fp8_g16_and_bs32():
@@ -431,7 +470,8 @@ def _sample_rows(batch, rng, n_random=192):
     return np.array(rows, dtype=np.int32)
 
 
-@pytest.mark.parametrize("name", ["llama70b_layer", "prefix_sharing", "long_context", "fp8_mixed"])
+@pytest.mark.parametrize("name", ["llama70b_layer", "prefix_sharing", "long_context", "fp8_mixed",
+                                  "int4_mixed"])
 def test_full_size_config_sampled(name):
     """The bench's launch configuration (split-KV, default num_splits) at full size;
     every head of the longest, shortest and three random sequences plus 192
@@ -444,6 +484,6 @@ def test_full_size_config_sampled(name):
     rows = _sample_rows(batch, np.random.default_rng(7))
     ref, _ = oracle_after_write(batch, rows=rows)
     assert_close(out[rows[:, 0], rows[:, 1]], ref, batch, name)
-    if name == "fp8_mixed":      # unsplit kernel too, on the same rows
+    if name in ("fp8_mixed", "int4_mixed"):      # unsplit kernel too, on the same rows
         out2 = run_gpu(dev, "decode")
         assert_close(out2[rows[:, 0], rows[:, 1]], ref, batch, name + " decode")
