@@ -41,6 +41,13 @@ window_positions               the four-token window trace printed in
                                "KV Cache Engineering", sec. 3
 paged_decode(window=W)         numpy/scipy attention over the last W rows of
                                the contiguous K/V; W >= L equals no window
+page_summary / page_score /    the Quest example printed in "KV Cache
+select_pages                   Engineering", sec. 7 (scores 2.5, 6.0, 4.0,
+                               -1.0; pages [1, 2]); brute force over all
+                               key choices for the upper-bound property
+quest_decode                   textbook attention restricted to the chosen
+                               pages' tokens (numpy), topk >= pages equals
+                               full decode; selection by brute-force scores
 split_partials / merge_lse     merge(split(x)) == unsplit(x) to 1e-12 for
                                random splits; one split is the identity;
                                empty splits carry no weight
@@ -110,6 +117,14 @@ def _load():
             lib.oracle_reshape_and_cache_int4.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
             lib.oracle_int4_restore.restype = None
             lib.oracle_int4_restore.argtypes = [P, I, ctypes.c_float, P]
+            lib.oracle_page_summary.restype = None
+            lib.oracle_page_summary.argtypes = [P, I, I, P, P]
+            lib.oracle_page_score.restype = D
+            lib.oracle_page_score.argtypes = [P, P, P, I]
+            lib.oracle_select_pages.restype = I
+            lib.oracle_select_pages.argtypes = [P, I, I, P]
+            lib.oracle_quest_decode.restype = None
+            lib.oracle_quest_decode.argtypes = [I, I, I, I, I, I, P, P, P, P, P, D, I, P, P, I]
             lib.oracle_paged_decode.restype = None
             lib.oracle_paged_decode.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, D,
                                                 I, I, P, P, P, I]
@@ -287,6 +302,46 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, *, 
                             _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl), float(sm_scale),
                             int(window), rows.shape[0], _ptr(rb), _ptr(rh), _ptr(out), nthreads)
     return out
+
+
+def page_summary(keys):
+    """(min, max) per channel of keys [n, D]."""
+    lib = _load()
+    k = _c(keys, np.float64)
+    n, D = k.shape
+    mn, mx = np.zeros(D), np.zeros(D)
+    lib.oracle_page_summary(_ptr(k), n, D, _ptr(mn), _ptr(mx))
+    return mn, mx
+
+
+def page_score(q, mn, mx) -> float:
+    lib = _load()
+    q, mn, mx = _c(q, np.float64), _c(mn, np.float64), _c(mx, np.float64)
+    return lib.oracle_page_score(_ptr(q), _ptr(mn), _ptr(mx), q.size)
+
+
+def select_pages(scores, k: int) -> list[int]:
+    lib = _load()
+    s = _c(scores, np.float64)
+    out = np.zeros(max(1, s.size), dtype=np.int32)
+    m = lib.oracle_select_pages(_ptr(s), s.size, int(k), _ptr(out))
+    return out[:m].tolist()
+
+
+def quest_decode(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, *, Hkv: int,
+                 block_size: int, topk: int, nthreads: int | None = None):
+    """Query-aware sparse decode over bf16 pools; returns (out [B, Hq, D], sel [B, Hkv, topk])."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    B, Hq, D = q.shape
+    kp, vp = _c(k_pool, np.uint16), _c(v_pool, np.uint16)
+    bt, sl = _c(block_tables, np.int32), _c(seq_lens, np.int32)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    sel = np.zeros((B, Hkv, topk), dtype=np.int32)
+    lib.oracle_quest_decode(B, Hq, Hkv, D, block_size, bt.shape[1], _ptr(q), _ptr(kp), _ptr(vp),
+                            _ptr(bt), _ptr(sl), float(sm_scale), int(topk), _ptr(out), _ptr(sel),
+                            nthreads or os.cpu_count() or 1)
+    return out, sel
 
 
 def split_partials(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, b: int, h: int,

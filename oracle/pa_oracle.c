@@ -157,6 +157,56 @@ int oracle_window_positions(int len, int window, int *out)
 }
 
 /*
+ * [P3] section 7 (Quest): a page's summary is the per-channel minimum and maximum
+ * of its n keys; a query scores the page by sum_d max(q_d * min_d, q_d * max_d), an
+ * upper bound of q . k over the page's keys.  Pages are chosen by score.
+ */
+void oracle_page_summary(const double *keys, int n, int D, double *mn, double *mx)
+{
+    int i, d;
+    for (d = 0; d < D; d++) {
+        mn[d] = keys[d];
+        mx[d] = keys[d];
+    }
+    for (i = 1; i < n; i++)
+        for (d = 0; d < D; d++) {
+            if (keys[(size_t)i * D + d] < mn[d]) mn[d] = keys[(size_t)i * D + d];
+            if (keys[(size_t)i * D + d] > mx[d]) mx[d] = keys[(size_t)i * D + d];
+        }
+}
+
+double oracle_page_score(const double *q, const double *mn, const double *mx, int D)
+{
+    double s = 0.0;
+    int d;
+    for (d = 0; d < D; d++) {
+        double a = q[d] * mn[d], b = q[d] * mx[d];
+        s += (a > b) ? a : b;
+    }
+    return s;
+}
+
+/* The k highest-scoring of n pages (all of them when n <= k), ties to the lower
+ * page index, returned in increasing page order.  Returns how many were chosen. */
+int oracle_select_pages(const double *scores, int n, int k, int *out)
+{
+    int i, j, m = (n < k) ? n : k;
+    char *taken = (char *)calloc((size_t)(n > 0 ? n : 1), 1);
+    for (j = 0; j < m; j++) {
+        int best = -1;
+        for (i = 0; i < n; i++)
+            if (!taken[i] && (best < 0 || scores[i] > scores[best]))
+                best = i;
+        taken[best] = 1;
+    }
+    for (i = 0, j = 0; i < n; i++)
+        if (taken[i])
+            out[j++] = i;
+    free(taken);
+    return m;
+}
+
+/*
  * [P3] section 8: absmax quantiser onto signed integer codes.
  *   scale = max|x| / largest_code, largest_code = 2^(bits-1) - 1
  *   code  = clip(rint(x / scale), -largest_code, largest_code)   (rint: ties to even)
@@ -502,6 +552,94 @@ void oracle_paged_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks, 
         int first = (window > 0 && L > window) ? L - window : 0;
         attend_range(&p, &q[((size_t)b * Hq + h) * D], b, h, first, L, sm_scale,
                      &out[(size_t)i * D], &lse);
+    }
+}
+
+/*
+ * Query-aware sparse decode ([P3] section 7) over bf16 pools, pages of 16 tokens:
+ * for every (b, kv head) the pages of sequence b are summarised from their valid
+ * keys (oracle_page_summary), each page is scored with every query head of the
+ * group and keeps the largest score (the group shares one selection), the topk
+ * best pages are chosen (oracle_select_pages) and every query head of the group
+ * attends over the tokens of the chosen pages only (textbook softmax).  The
+ * chosen pages go to sel[b][kvh][0..topk) (-1 where fewer exist).
+ */
+void oracle_quest_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks,
+                         const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                         const int32_t *block_tables, const int32_t *seq_lens, double sm_scale,
+                         int topk, double *out, int32_t *sel, int nthreads)
+{
+    paged_kv p;
+    long long i;
+    int G = Hq / Hkv;
+    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_kind = 0;
+    p.k_pool = k_pool; p.v_pool = v_pool; p.k_scale = NULL; p.v_scale = NULL;
+    p.block_tables = block_tables;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+    for (i = 0; i < (long long)B * Hkv; i++) {
+        int b = (int)(i / Hkv), kvh = (int)(i % Hkv);
+        int L = seq_lens[b], np = (L + 15) / 16, j, t, g, d, m, c;
+        double *keys = (double *)malloc(sizeof(double) * 16 * (size_t)D);
+        double *mn = (double *)malloc(sizeof(double) * (size_t)D);
+        double *mx = (double *)malloc(sizeof(double) * (size_t)D);
+        double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+        double *row = (double *)malloc(sizeof(double) * (size_t)D);
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(np > 0 ? np : 1));
+        int *chosen = (int *)malloc(sizeof(int) * (size_t)(np > 0 ? np : 1));
+        for (j = 0; j < np; j++) {
+            int n = (L - 16 * j < 16) ? L - 16 * j : 16;
+            for (t = 0; t < n; t++)
+                kv_row(&p, 0, b, 16 * j + t, kvh, &keys[(size_t)t * D]);
+            oracle_page_summary(keys, n, D, mn, mx);
+            scores[j] = -INFINITY;
+            for (g = 0; g < G; g++) {
+                double sc;
+                for (d = 0; d < D; d++)
+                    qd[d] = oracle_bf16_to_double(q[((size_t)b * Hq + kvh * G + g) * D + d]);
+                sc = oracle_page_score(qd, mn, mx, D);
+                if (sc > scores[j]) scores[j] = sc;
+            }
+        }
+        m = oracle_select_pages(scores, np, topk, chosen);
+        for (c = 0; c < topk; c++)
+            sel[(size_t)i * topk + c] = (c < m) ? chosen[c] : -1;
+        for (g = 0; g < G; g++) {
+            int h = kvh * G + g, nt = 0;
+            double mxs = -INFINITY, sum = 0.0;
+            double *o = &out[((size_t)b * Hq + h) * D];
+            double *sv = (double *)malloc(sizeof(double) * 16 * (size_t)(m > 0 ? m : 1));
+            for (d = 0; d < D; d++) {
+                qd[d] = oracle_bf16_to_double(q[((size_t)b * Hq + h) * D + d]);
+                o[d] = 0.0;
+            }
+            for (c = 0; c < m; c++) {
+                int pg = chosen[c], n = (L - 16 * pg < 16) ? L - 16 * pg : 16;
+                for (t = 0; t < n; t++) {
+                    double acc = 0.0;
+                    kv_row(&p, 0, b, 16 * pg + t, kvh, row);
+                    for (d = 0; d < D; d++)
+                        acc += qd[d] * row[d];
+                    sv[nt] = sm_scale * acc;
+                    if (sv[nt] > mxs) mxs = sv[nt];
+                    nt++;
+                }
+            }
+            nt = 0;
+            for (c = 0; c < m; c++) {
+                int pg = chosen[c], n = (L - 16 * pg < 16) ? L - 16 * pg : 16;
+                for (t = 0; t < n; t++) {
+                    double w = exp(sv[nt++] - mxs);
+                    sum += w;
+                    kv_row(&p, 1, b, 16 * pg + t, kvh, row);
+                    for (d = 0; d < D; d++)
+                        o[d] += w * row[d];
+                }
+            }
+            for (d = 0; d < D; d++)
+                o[d] = (sum > 0.0) ? o[d] / sum : 0.0;
+            free(sv);
+        }
+        free(keys); free(mn); free(mx); free(qd); free(row); free(scores); free(chosen);
     }
 }
 

@@ -505,6 +505,89 @@ def test_decode_gqa_group_shares_kv():
     assert not np.array_equal(out[0, 0], out[0, 4])
 
 
+# ---------------------------------------------------------------- Quest page selection
+
+def test_quest_page_example(golden_dir):
+    g = _golden(golden_dir, "quest_pages.json")
+    pages = np.array(g["pages"], dtype=np.float64)
+    q = np.array(g["query"])
+    scores = []
+    for page in pages:
+        mn, mx = oracle.page_summary(page)
+        assert mn.tolist() == page.min(axis=0).tolist() and mx.tolist() == page.max(axis=0).tolist()
+        scores.append(oracle.page_score(q, mn, mx))
+    assert scores == g["page_scores"]
+    sel = oracle.select_pages(scores, 2)
+    assert sel == g["selected_pages"]
+    assert len(sel) * pages.shape[1] == g["kv_entries_read"]
+    assert pages.shape[0] * pages.shape[1] == g["kv_entries_stored"]
+
+
+def test_quest_score_bounds_every_key():
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        keys = rng.standard_normal((16, 8))
+        q = rng.standard_normal(8)
+        mn, mx = oracle.page_summary(keys)
+        s = oracle.page_score(q, mn, mx)
+        assert np.all(keys @ q <= s + 1e-12)                   # an upper bound of q . k
+        # and tight: the corner of the box it picks reaches it
+        corner = np.where(q >= 0, mx, mn)
+        assert abs(corner @ q - s) < 1e-12
+
+
+def test_select_pages_ties_and_short():
+    assert oracle.select_pages([1.0, 3.0, 3.0, 2.0], 2) == [1, 2]
+    assert oracle.select_pages([5.0, 5.0, 5.0], 2) == [0, 1]      # ties: lower index
+    assert oracle.select_pages([0.5, -1.0], 4) == [0, 1]          # fewer pages than k
+
+
+def _quest_reference(batch, topk):
+    """numpy restatement: summaries, group-max scores, top-k, attention on those tokens."""
+    B, Hq, Hkv, D, bs = batch.B, batch.Hq, batch.Hkv, batch.D, batch.block_size
+    G = Hq // Hkv
+    q = wl.bf16_to_float(batch.q).astype(np.float64)
+    kf = wl.bf16_to_float(batch.k_pool).astype(np.float64)
+    vf = wl.bf16_to_float(batch.v_pool).astype(np.float64)
+    out = np.zeros((B, Hq, D))
+    sel_all = np.full((B, Hkv, topk), -1)
+    for b in range(B):
+        L = int(batch.seq_lens[b])
+        t = np.arange(L)
+        K = kf[batch.block_tables[b, t // bs], t % bs]
+        V = vf[batch.block_tables[b, t // bs], t % bs]
+        npg = (L + 15) // 16
+        for kvh in range(Hkv):
+            sc = []
+            for j in range(npg):
+                kk = K[16 * j:16 * j + 16, kvh]
+                qs = q[b, kvh * G:(kvh + 1) * G]
+                sc.append(max(np.maximum(qs * kk.min(0), qs * kk.max(0)).sum(1)))
+            order = sorted(range(npg), key=lambda j: (-sc[j], j))[:topk]
+            sel = sorted(order)
+            sel_all[b, kvh, :len(sel)] = sel
+            idx = np.concatenate([np.arange(16 * j, min(L, 16 * j + 16)) for j in sel]) \
+                if sel else np.zeros(0, int)
+            for g in range(G):
+                h = kvh * G + g
+                if idx.size:
+                    out[b, h] = softmax(batch.sm_scale * K[idx, kvh] @ q[b, h]) @ V[idx, kvh]
+    return out, sel_all
+
+
+@pytest.mark.parametrize("topk", [1, 3, 8, 100])
+def test_quest_decode_vs_numpy(topk):
+    batch = wl.build_batch("t", [1, 15, 16, 17, 70, 200, 0], Hq=8, Hkv=2, D=64, block_size=32,
+                           seed=80 + topk)
+    out, sel = oracle.quest_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                   batch.seq_lens, batch.sm_scale, Hkv=2, block_size=32, topk=topk)
+    ref, ref_sel = _quest_reference(batch, topk)
+    assert np.array_equal(sel, ref_sel)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-13)
+    if topk >= 200 // 16 + 1:
+        assert np.allclose(out, _oracle(batch), rtol=1e-12, atol=1e-13)
+
+
 # ---------------------------------------------------------------- split + merge
 
 def test_split_merge_identity_random():
