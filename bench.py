@@ -210,14 +210,27 @@ def run_ours(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(0, args.steps, EVENT_EVERY)]
 
+    quest = args.quest_topk > 0
+    if quest:       # summaries of the whole cache, then per step: summarise the new
+        dev.quest_build_summaries(stream)      # token's page, select, sparse decode
+        dev.selected_pages = torch.empty((batch.B, batch.Hkv, args.quest_topk),
+                                         dtype=torch.int32, device=dev_id)
+
     def step(i=None):
         dev.reshape_and_cache(stream)
+        if quest:
+            _lib.pa_quest_summarize(dev.shape, dev.k_pool, dev.key_summaries, dev.slot_mapping,
+                                    dev.err, stream)
+            _lib.pa_quest_select(dev.shape, dev.q, dev.key_summaries, dev.block_tables,
+                                 dev.seq_lens, args.quest_topk, dev.selected_pages, dev.err,
+                                 stream)
         if i is not None:
             ev[i][0].record(stream)
         _lib.pa_decode_splitkv(dev.shape, dev.out, dev.workspace, ns, dev.q, dev.k_pool,
                                dev.v_pool, dev.k_scale, dev.v_scale, dev.block_tables,
                                dev.seq_lens, batch.sm_scale, dev.err, stream,
-                               dev.shared_prefix_lens, args.window)
+                               dev.shared_prefix_lens, args.window,
+                               dev.selected_pages if quest else None)
         if i is not None:
             ev[i][1].record(stream)
         _lib.pa_merge_lse(dev.shape, dev.out, dev.workspace, ns, stream)
@@ -277,13 +290,16 @@ def run_ours(args):
         raise RuntimeError("device error flag set during the timed steps")
 
     unique_tokens = batch.unique_kv_tokens(args.window)
+    if args.quest_topk > 0:     # the chosen pages' tokens (pages of 16; the last may be short)
+        unique_tokens = int(sum(min(int(L), 16 * args.quest_topk) if (int(L) + 15) // 16 <=
+                                args.quest_topk else 16 * args.quest_topk for L in batch.seq_lens))
     kv_bytes = unique_tokens * batch.kv_bytes_per_token()
     if batch.quantized:
         kv_bytes += sum(int(n) for n in (batch.seq_lens + batch.block_size - 1)
                         // batch.block_size) * batch.scale_bytes_per_block()
     peak, peak_kind = measured_peak_hbm()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
-    tr = TRAFFIC.get(args.config) if args.window == 0 else None
+    tr = TRAFFIC.get(args.config) if args.window == 0 and args.quest_topk == 0 else None
     traffic = tr["bytes"] if tr and tr.get("kernel_hash") == kernel_source_hash() else None
     result = {
         "metric": METRIC,
@@ -305,6 +321,7 @@ def run_ours(args):
             "seq_len_max": int(batch.seq_lens.max()),
             "unique_kv_tokens": unique_tokens, "num_splits": ns,
             "window": args.window,
+            "quest_topk": args.quest_topk,
             "l2": f"no flush: {kv_bytes / 1e9:.2f} GB of KV read per step >> 129 MB L2",
             "parallelism": f"replicas x{world}" if world > 1 else "single",
             "step": "pa_reshape_and_cache + pa_decode_splitkv + pa_merge_lse",
@@ -321,7 +338,7 @@ def run_ours(args):
             "algorithmic_bytes": kv_bytes,
             "peak_kind": peak_kind,
         },
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (5 if args.quest_topk > 0 else 3) * args.steps,
         "clocks": clock_info,
     }
     if e2e is not None:
@@ -427,6 +444,8 @@ def main(argv=None):
                     choices=["tiny", "llama70b_layer", "prefix_sharing", "long_context",
                              "fp8_mixed", "int4_mixed"])
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--quest-topk", type=int, default=0,
+                    help="query-aware sparse decode over the K best 16-token pages (0 = off)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding-window layer: attend over the last W positions (0 = all)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -109,7 +109,12 @@ typedef struct {
  *     [max(0, L - window), L) -- a sliding-window layer ("KV Cache Engineering
  *     for LLM Serving", section 3).  Block-table entries of blocks wholly before
  *     the window are never read (they may be freed and hold any value).  0 = all.
- *   reserved: must be 0.
+ *   topk, selected_pages: query-aware sparse decode (section 7, Quest): with
+ *     topk > 0, (sequence b, KV head h) attends only over the 16-token pages
+ *     selected_pages[b][h][0 .. min(topk, pages of b)) -- logical page indices in
+ *     increasing order, as pa_quest_select writes them (page j = tokens
+ *     [16 j, min(16 j + 16, L))).  An index outside the sequence sets
+ *     PA_DEVERR_BLOCK_ID and reads zeros.  Not combined with window.
  *   shared_prefix_lens: pa_decode_splitkv only (ignored by pa_decode); optional
  *     [B] int32 device array, a speed hint for batches with prefix sharing
  *     ("appendonly", "Prefix sharing is where the real win lives"): the number
@@ -121,8 +126,9 @@ typedef struct {
  */
 typedef struct {
     int32_t window;
-    int32_t reserved;
+    int32_t topk;
     const int32_t *shared_prefix_lens;
+    const int32_t *selected_pages;      /* [B, Hkv, topk] int32, with topk > 0 */
 } pa_decode_opts;
 
 /*
@@ -262,6 +268,39 @@ pa_status pa_decode_splitkv_noalloc(const pa_shape *shape, float *out, int32_t n
                                     const float *k_scale, const float *v_scale,
                                     const int32_t *block_tables, const int32_t *seq_lens,
                                     float sm_scale, int32_t *err_flag, pa_stream_t stream);
+
+/*
+ * Quest page summaries ("KV Cache Engineering for LLM Serving", section 7).  A page
+ * is a 16-token tile of the pool: page g holds pool rows [16 g, 16 g + 16), i.e.
+ * slots 16 g .. 16 g + 15 (a 32-token block is two pages).
+ *
+ * pa_quest_summarize -- for every token t < shape->B with slot s = slot_mapping[t]
+ * >= 0, set the summary of page s / 16 to the per-channel minimum and maximum of its
+ * keys in rows 0 .. s % 16:
+ *     key_summaries[s / 16][h][0][d] = min_r K[r][h][d],  [1][d] = max_r K[r][h][d]
+ * key_summaries: [nblocks * block_size / 16, Hkv, 2, D] bf16 (exact: bf16 keys).
+ * Call it after pa_reshape_and_cache with the same slots; to build every summary
+ * of a sequence, pass the slot of each page's last token.  When several listed
+ * slots share a page the one with the largest slot writes.  bf16 pools only.
+ */
+pa_status pa_quest_summarize(const pa_shape *shape, const void *k_pool, void *key_summaries,
+                             const int64_t *slot_mapping, int32_t *err_flag,
+                             pa_stream_t stream);
+
+/*
+ * pa_quest_select -- for every (sequence b, KV head h): score each 16-token page j of
+ * b (pages 0 .. ceil(L/16) - 1, reached through block_tables) with every query head
+ * g of the group as  sum_d max(q[b][g][d] * min_d, q[b][g][d] * max_d)  (fp32), keep
+ * the page's largest score over the group, and write the topk best pages (ties to
+ * the lower page index; all pages if there are at most topk) in increasing order to
+ * selected_pages[b][h][0 .. topk), -1 past the number of pages.  bf16 pools only;
+ * q [B, Hq, D] bf16.  Pass the result to pa_decode / pa_decode_splitkv through
+ * pa_decode_opts.  Page scores are fp32 sums, so pages whose scores agree to
+ * rounding may be ordered differently from an exact computation.
+ */
+pa_status pa_quest_select(const pa_shape *shape, const void *q, const void *key_summaries,
+                          const int32_t *block_tables, const int32_t *seq_lens, int32_t topk,
+                          int32_t *selected_pages, int32_t *err_flag, pa_stream_t stream);
 
 /* Human-readable name of a status. */
 const char *pa_status_string(pa_status status);

@@ -20,7 +20,8 @@ PA_DEVERR_FP8_CONFLICT, PA_DEVERR_TIMEOUT = 8, 16
 
 EXPORTED = ("pa_reshape_and_cache", "pa_decode", "pa_splitkv_workspace_bytes",
             "pa_default_num_splits", "pa_decode_splitkv", "pa_merge_lse", "pa_status_string",
-            "pa_read_error_flag", "pa_decode_splitkv_noalloc")
+            "pa_read_error_flag", "pa_decode_splitkv_noalloc", "pa_quest_summarize",
+            "pa_quest_select")
 PA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -32,15 +33,18 @@ class pa_shape(ctypes.Structure):
 
 
 class pa_decode_opts(ctypes.Structure):
-    _fields_ = [("window", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("shared_prefix_lens", ctypes.c_void_p)]
+    _fields_ = [("window", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("shared_prefix_lens", ctypes.c_void_p), ("selected_pages", ctypes.c_void_p)]
 
 
-def _opts(window: int = 0, shared_prefix_lens=None):
-    """A pa_decode_opts by reference, or None when every setting is the default."""
-    if not window and shared_prefix_lens is None:
+def _opts(window: int = 0, shared_prefix_lens=None, selected_pages=None):
+    """A pa_decode_opts by reference, or None when every setting is the default.
+    selected_pages: [B, Hkv, topk] int32 tensor (topk taken from its last dim)."""
+    if not window and shared_prefix_lens is None and selected_pages is None:
         return None
-    return ctypes.byref(pa_decode_opts(int(window), 0, _ptr(shared_prefix_lens)))
+    topk = 0 if selected_pages is None else int(selected_pages.shape[-1])
+    return ctypes.byref(pa_decode_opts(int(window), topk, _ptr(shared_prefix_lens),
+                                       _ptr(selected_pages)))
 
 
 class PAError(RuntimeError):
@@ -73,6 +77,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "pa_status_string": (ctypes.c_char_p, [I32]),
             "pa_read_error_flag": (I32, [P, ctypes.POINTER(I32), P]),
             "pa_decode_splitkv_noalloc": (I32, [S, P, I32, P, P, P, P, P, P, P, F, P, P]),
+            "pa_quest_summarize": (I32, [S, P, P, P, P, P]),
+            "pa_quest_select": (I32, [S, P, P, P, P, I32, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -133,12 +139,14 @@ def pa_reshape_and_cache(shape: pa_shape, k_new, v_new, k_pool, v_pool, k_scale,
 
 
 def pa_decode(shape: pa_shape, out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
-              seq_lens, sm_scale: float, err_flag=None, stream=None, window: int = 0) -> None:
+              seq_lens, sm_scale: float, err_flag=None, stream=None, window: int = 0,
+              selected_pages=None) -> None:
     lib = load()
     _check("pa_decode", lib.pa_decode(
         ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
-        _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), _opts(window), float(sm_scale),
-        _ptr(err_flag), _stream(stream)))
+        _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens),
+        _opts(window, selected_pages=selected_pages), float(sm_scale), _ptr(err_flag),
+        _stream(stream)))
 
 
 def pa_splitkv_workspace_bytes(shape: pa_shape, num_splits: int) -> int:
@@ -151,14 +159,15 @@ def pa_default_num_splits(shape: pa_shape, sm_count: int) -> int:
 
 def pa_decode_splitkv(shape: pa_shape, out, workspace, num_splits: int, q, k_pool, v_pool,
                       k_scale, v_scale, block_tables, seq_lens, sm_scale: float, err_flag=None,
-                      stream=None, shared_prefix_lens=None, window: int = 0) -> None:
+                      stream=None, shared_prefix_lens=None, window: int = 0,
+                      selected_pages=None) -> None:
     lib = load()
     nbytes = workspace.numel() * workspace.element_size()
     _check("pa_decode_splitkv", lib.pa_decode_splitkv(
         ctypes.byref(shape), _ptr(out), _ptr(workspace), nbytes, int(num_splits), _ptr(q),
         _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
-        _ptr(seq_lens), _opts(window, shared_prefix_lens), float(sm_scale), _ptr(err_flag),
-        _stream(stream)))
+        _ptr(seq_lens), _opts(window, shared_prefix_lens, selected_pages), float(sm_scale),
+        _ptr(err_flag), _stream(stream)))
 
 
 def pa_merge_lse(shape: pa_shape, out, workspace, num_splits: int, stream=None) -> None:
@@ -187,3 +196,19 @@ def pa_decode_splitkv_noalloc(shape: pa_shape, out, num_splits: int, q, k_pool, 
         ctypes.byref(shape), _ptr(out), int(num_splits), _ptr(q), _ptr(k_pool), _ptr(v_pool),
         _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), float(sm_scale),
         _ptr(err_flag), _stream(stream)))
+
+
+def pa_quest_summarize(shape: pa_shape, k_pool, key_summaries, slot_mapping, err_flag=None,
+                       stream=None) -> None:
+    lib = load()
+    _check("pa_quest_summarize", lib.pa_quest_summarize(
+        ctypes.byref(shape), _ptr(k_pool), _ptr(key_summaries), _ptr(slot_mapping),
+        _ptr(err_flag), _stream(stream)))
+
+
+def pa_quest_select(shape: pa_shape, q, key_summaries, block_tables, seq_lens, topk: int,
+                    selected_pages, err_flag=None, stream=None) -> None:
+    lib = load()
+    _check("pa_quest_select", lib.pa_quest_select(
+        ctypes.byref(shape), _ptr(q), _ptr(key_summaries), _ptr(block_tables), _ptr(seq_lens),
+        int(topk), _ptr(selected_pages), _ptr(err_flag), _stream(stream)))

@@ -53,8 +53,11 @@ pa_status check_decode_args(const pa_shape *shape, const float *out, const void 
   if (st != PA_OK) return st;
   if (shape->kv_dtype != PA_KV_BF16 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
   if (opts) {
-    if (opts->window < 0 || opts->reserved != 0) return PA_ERR_INVALID_ARG;
+    if (opts->window < 0 || opts->topk < 0) return PA_ERR_INVALID_ARG;
     if (opts->shared_prefix_lens && !aligned16(opts->shared_prefix_lens)) return PA_ERR_INVALID_ARG;
+    if ((opts->topk > 0) != (opts->selected_pages != nullptr)) return PA_ERR_INVALID_ARG;
+    if (opts->selected_pages && !aligned16(opts->selected_pages)) return PA_ERR_INVALID_ARG;
+    if (opts->topk > 0 && opts->window > 0) return PA_ERR_INVALID_ARG;
   }
   return PA_OK;
 }
@@ -141,6 +144,34 @@ pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,
     return PA_ERR_INVALID_ARG;
   if (num_splits < 1 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARG;
   return pa::run_merge(*shape, out, workspace, num_splits, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_quest_summarize(const pa_shape *shape, const void *k_pool, void *key_summaries,
+                             const int64_t *slot_mapping, int32_t *err_flag,
+                             pa_stream_t stream) {
+  pa_status st = check_shape(shape, false);
+  if (st != PA_OK) return st;
+  if (shape->kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
+  if (shape->B == 0) return PA_OK;
+  st = check_ptrs({k_pool, key_summaries, slot_mapping});
+  if (st != PA_OK) return st;
+  return pa::run_quest_summarize(*shape, k_pool, key_summaries, slot_mapping, err_flag,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_quest_select(const pa_shape *shape, const void *q, const void *key_summaries,
+                          const int32_t *block_tables, const int32_t *seq_lens, int32_t topk,
+                          int32_t *selected_pages, int32_t *err_flag, pa_stream_t stream) {
+  pa_status st = check_shape(shape, true);
+  if (st != PA_OK) return st;
+  if (shape->kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
+  if (topk < 1) return PA_ERR_INVALID_ARG;
+  if (shape->B == 0) return PA_OK;
+  st = check_ptrs({q, key_summaries, block_tables, seq_lens, selected_pages});
+  if (st != PA_OK) return st;
+  if (pa::quest_select_smem(*shape) > 200 * 1024) return PA_ERR_UNSUPPORTED;
+  return pa::run_quest_select(*shape, q, key_summaries, block_tables, seq_lens, topk,
+                              selected_pages, err_flag, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *pa_status_string(pa_status status) {

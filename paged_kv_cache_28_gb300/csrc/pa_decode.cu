@@ -84,6 +84,8 @@ struct Params {
   const int32_t *seq_lens;
   const int32_t *shared_prefix_lens;   // optional L2 hint per sequence (split kernel)
   int window;                          // > 0: attend over the last `window` positions only
+  int topk;                            // > 0: attend over the pages listed in sel only
+  const int32_t *sel;                  // [B, Hkv, topk] chosen 16-token pages (ascending)
   int32_t *err;
   int B, Hq, Hkv, G, bs, nblocks, max_blocks;
   float sl2;  // sm_scale * log2(e)
@@ -234,6 +236,12 @@ __device__ __forceinline__ SeqTiles seq_tiles(int L, int window) {
 }
 
 constexpr int kLoShift = 16;   // unit info bits 16..19: first valid token of the tile
+
+// Tiles attended per (sequence, KV head): the window's tiles, or the chosen pages.
+__device__ __forceinline__ int pair_tile_count(int L, int window, int topk) {
+  if (topk > 0) return min(topk, (L + kTile - 1) / kTile);
+  return seq_tiles(L, window).count;
+}
 
 // One 16-token tile: scores, online-softmax update, P V accumulation.
 // sscale: factor from raw mma scores to log2-domain scores; vs: FP8 V scale.
@@ -490,9 +498,11 @@ __device__ __forceinline__ void write_normalised(const State<C> &st, float *dst,
 // the block table.
 struct PairSource {
   const int32_t *row;
+  const int32_t *sel;   // this pair's chosen pages, or null
   int32_t *err;
   int pair, w, nw, bs, nblocks;
-  SeqTiles geo;
+  SeqTiles geo;         // with a selection: count = pages chosen, first = 0
+  int npages;           // 16-token pages of the sequence
   int base;
   int4 cur, nxt;
 
@@ -502,14 +512,23 @@ struct PairSource {
   __device__ __forceinline__ int4 load(int i) const {
     const int j = w + i * nw;
     if (j >= geo.count) return make_int4(kInvalidPhys, 0, 0, 0);
-    const int tile = geo.first + j;
-    int phys = __ldg(row + (tile * kTile) / bs);
+    int tile = geo.first + j, last_tile = geo.first + geo.count - 1;
+    if (sel) {
+      tile = __ldg(sel + j);
+      last_tile = npages - 1;
+    }
+    const bool bad_page = sel && (tile < 0 || tile >= npages);
+    if (bad_page) {
+      set_err(err, PA_DEVERR_BLOCK_ID);
+      tile = 0;
+    }
+    int phys = bad_page ? kInvalidPhys : __ldg(row + (tile * kTile) / bs);
     if (phys < 0 || phys >= nblocks) {
       set_err(err, PA_DEVERR_BLOCK_ID);
       phys = kInvalidPhys;
     }
-    int info = (j == geo.count - 1) ? geo.last_valid : kTile;
-    if (j == 0) info |= kFirstOfPair | (geo.first_skip << kLoShift);
+    int info = (tile == last_tile) ? geo.last_valid : kTile;
+    if (j == 0) info |= kFirstOfPair | (sel ? 0 : geo.first_skip << kLoShift);
     if (j == geo.count - 1) info |= kLastOfPair;
     if (i == 0) info |= kPieceStart;
     if (j + nw >= geo.count) info |= kPieceEnd;
@@ -538,8 +557,9 @@ struct SegmentSource {
   const int32_t *seq_lens;
   const int32_t *block_tables;
   const int32_t *shared_prefix_lens;   // may be null
+  const int32_t *sel;                  // [B, Hkv, topk] chosen pages, or null
   int32_t *err;
-  int B, Hkv, bs, nblocks, max_blocks, window;
+  int B, Hkv, bs, nblocks, max_blocks, window, topk;
   int begin, end;
   int base;
   int4 cur, nxt;
@@ -559,14 +579,26 @@ struct SegmentSource {
     const int kvh = r / nt, j = r - kvh * nt;
     const int L = min(max(__ldg(seq_lens + b), 0), max_blocks * bs);
     const SeqTiles geo = seq_tiles(L, window);
-    const int tile = geo.first + j;
-    int phys = __ldg(block_tables + static_cast<size_t>(b) * max_blocks + (tile * kTile) / bs);
+    int tile = geo.first + j, last_tile = geo.first + geo.count - 1;
+    bool bad_page = false;
+    if (sel) {
+      const int npages = (L + kTile - 1) / kTile;
+      tile = __ldg(sel + (static_cast<size_t>(b) * Hkv + kvh) * topk + j);
+      last_tile = npages - 1;
+      bad_page = tile < 0 || tile >= npages;
+      if (bad_page) {
+        set_err(err, PA_DEVERR_BLOCK_ID);
+        tile = 0;
+      }
+    }
+    int phys = bad_page ? kInvalidPhys
+                        : __ldg(block_tables + static_cast<size_t>(b) * max_blocks + (tile * kTile) / bs);
     if (phys < 0 || phys >= nblocks) {
       set_err(err, PA_DEVERR_BLOCK_ID);
       phys = kInvalidPhys;
     }
-    int info = (j == nt - 1) ? geo.last_valid : kTile;
-    if (j == 0) info |= kFirstOfPair | kPieceStart | (geo.first_skip << kLoShift);
+    int info = (tile == last_tile) ? geo.last_valid : kTile;
+    if (j == 0) info |= kFirstOfPair | kPieceStart | (sel ? 0 : geo.first_skip << kLoShift);
     if (j == nt - 1) info |= kLastOfPair | kPieceEnd;
     if (i == 0) info |= kPieceStart;
     if (f == end - 1) info |= kPieceEnd;
@@ -764,6 +796,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.err = p.err;
   src.pair = pair;
   src.geo = seq_tiles(L, p.window);
+  src.npages = (L + kTile - 1) / kTile;
+  src.sel = nullptr;
+  if (p.sel) {
+    src.sel = p.sel + static_cast<size_t>(pair) * p.topk;
+    src.geo.first = 0;
+    src.geo.count = pair_tile_count(L, 0, p.topk);
+  }
   src.w = warp;
   src.nw = C::WARPS;
   src.bs = p.bs;
@@ -846,7 +885,7 @@ __device__ void scan_lengths(const Params &p, int32_t *prefix) {
     if (i < p.B) {
       const int L0 = p.seq_lens[i];
       if ((L0 < 0 || L0 > cap) && blockIdx.x == 0) set_err(p.err, PA_DEVERR_SEQ_LEN);
-      v = p.Hkv * seq_tiles(clamp_len(L0, cap), p.window).count;
+      v = p.Hkv * pair_tile_count(clamp_len(L0, cap), p.window, p.topk);
     }
     int x = v;
 #pragma unroll
@@ -892,6 +931,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.nblocks = p.nblocks;
   src.max_blocks = p.max_blocks;
   src.window = p.window;
+  src.sel = p.sel;
+  src.topk = p.topk;
   src.begin = min(seg * W, total);
   src.end = (seg < p.num_splits) ? min(src.begin + W, total) : src.begin;
   src.init(lane);
@@ -1047,6 +1088,8 @@ static Params make_params(const pa_shape &s, float *out, const void *q, const fl
                           const pa_decode_opts *opts, float sm_scale, int32_t *err) {
   Params p{};
   p.window = opts ? opts->window : 0;
+  p.topk = (opts && opts->selected_pages) ? opts->topk : 0;
+  p.sel = p.topk > 0 ? opts->selected_pages : nullptr;
   p.out = out;
   p.q = static_cast<const uint16_t *>(q);
   p.k_scale = k_scale;

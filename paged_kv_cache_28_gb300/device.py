@@ -62,10 +62,10 @@ class DeviceBatch:
                                   self.k_scale, self.v_scale, self.slot_mapping, self.err,
                                   stream)
 
-    def decode(self, stream=None, window: int = 0):
+    def decode(self, stream=None, window: int = 0, selected_pages=None):
         _lib.pa_decode(self.shape, self.out, self.q, self.k_pool, self.v_pool, self.k_scale,
                        self.v_scale, self.block_tables, self.seq_lens, self.batch.sm_scale,
-                       self.err, stream, window)
+                       self.err, stream, window, selected_pages)
 
     def ensure_workspace(self, num_splits: int):
         nbytes = _lib.pa_splitkv_workspace_bytes(self.shape, num_splits)
@@ -76,7 +76,7 @@ class DeviceBatch:
         self.num_splits = num_splits
 
     def decode_splitkv(self, num_splits: int | None = None, stream=None, hints: bool = True,
-                       window: int = 0):
+                       window: int = 0, selected_pages=None):
         """Split-KV decode + merge; hints: pass the batch's shared-prefix lengths (if any)."""
         if num_splits is None:
             num_splits = default_num_splits(self.shape, self.device)
@@ -85,8 +85,40 @@ class DeviceBatch:
         _lib.pa_decode_splitkv(self.shape, self.out, self.workspace, num_splits, self.q,
                                self.k_pool, self.v_pool, self.k_scale, self.v_scale,
                                self.block_tables, self.seq_lens, self.batch.sm_scale, self.err,
-                               stream, self.shared_prefix_lens if hints else None, window)
+                               stream, self.shared_prefix_lens if hints else None, window,
+                               selected_pages)
         _lib.pa_merge_lse(self.shape, self.out, self.workspace, num_splits, stream)
+
+    # -- Quest page selection ------------------------------------------------------
+
+    def quest_summary_slots(self) -> torch.Tensor:
+        """Slots of every page's last valid token: summarising them builds all pages."""
+        b = self.batch
+        slots = []
+        for s in range(b.B):
+            L = int(b.seq_lens[s])
+            for j in range((L + 15) // 16):
+                t = min(L, 16 * (j + 1)) - 1
+                slots.append(int(b.block_tables[s, t // b.block_size]) * b.block_size +
+                             t % b.block_size)
+        return torch.tensor(slots if slots else [-1], dtype=torch.int64, device=self.device)
+
+    def quest_build_summaries(self, stream=None):
+        b = self.batch
+        npages = b.nblocks * b.block_size // 16
+        self.key_summaries = torch.zeros((npages, b.Hkv, 2, b.D), dtype=torch.bfloat16,
+                                         device=self.device)
+        slots = self.quest_summary_slots()
+        shape = _lib.make_shape(slots.numel(), b.Hq, b.Hkv, b.D, b.block_size, b.nblocks,
+                                b.max_blocks)
+        _lib.pa_quest_summarize(shape, self.k_pool, self.key_summaries, slots, self.err, stream)
+
+    def quest_select(self, topk: int, stream=None) -> torch.Tensor:
+        self.selected_pages = torch.empty((self.batch.B, self.batch.Hkv, topk), dtype=torch.int32,
+                                          device=self.device)
+        _lib.pa_quest_select(self.shape, self.q, self.key_summaries, self.block_tables,
+                             self.seq_lens, topk, self.selected_pages, self.err, stream)
+        return self.selected_pages
 
     def read_err(self, stream=None) -> int:
         return _lib.pa_read_error_flag(self.err, stream)

@@ -79,10 +79,14 @@ def test_decode_rejects_bad_pointers(lib):
     assert _decode(lib, fp8) == _lib.PA_ERR_INVALID_ARG                # scales missing
     assert lib.pa_decode(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, None, 0.1, None,
                          None) == _lib.PA_ERR_INVALID_ARG
-    bad = _lib.pa_decode_opts(-1, 0, None)
+    bad = _lib.pa_decode_opts(-1, 0, None, None)
     assert _decode(lib, s, opts=ctypes.byref(bad)) == _lib.PA_ERR_INVALID_ARG   # window < 0
-    bad = _lib.pa_decode_opts(8, 1, None)
-    assert _decode(lib, s, opts=ctypes.byref(bad)) == _lib.PA_ERR_INVALID_ARG   # reserved != 0
+    bad = _lib.pa_decode_opts(0, 4, None, None)
+    assert _decode(lib, s, opts=ctypes.byref(bad)) == _lib.PA_ERR_INVALID_ARG   # topk, no pages
+    bad = _lib.pa_decode_opts(0, 0, None, FAKE)
+    assert _decode(lib, s, opts=ctypes.byref(bad)) == _lib.PA_ERR_INVALID_ARG   # pages, topk 0
+    bad = _lib.pa_decode_opts(16, 4, None, FAKE)
+    assert _decode(lib, s, opts=ctypes.byref(bad)) == _lib.PA_ERR_INVALID_ARG   # window + topk
 
 
 def test_empty_batch_is_a_no_op(lib):
@@ -106,7 +110,7 @@ def test_splitkv_host_checks(lib):
     args[2] = FAKE + 16
     assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # workspace not 256-aligned
     args[2] = FAKE
-    args[12] = ctypes.byref(_lib.pa_decode_opts(0, 0, FAKE + 4))
+    args[12] = ctypes.byref(_lib.pa_decode_opts(0, 0, FAKE + 4, None))
     assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # hint array misaligned
     args[12] = None
     assert lib.pa_merge_lse(ctypes.byref(s), FAKE, FAKE, 0, None) == _lib.PA_ERR_INVALID_ARG
@@ -132,3 +136,15 @@ def test_reshape_rejects_bad_args(lib):
     fp8 = ctypes.byref(shape(D=128, kv_dtype=_lib.PA_KV_FP8_E4M3))
     assert lib.pa_reshape_and_cache(fp8, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None,
                                     None) == _lib.PA_ERR_INVALID_ARG
+
+
+def test_quest_host_checks(lib):
+    import ctypes
+    s = ctypes.byref(shape())
+    fp8 = ctypes.byref(shape(D=128, kv_dtype=_lib.PA_KV_FP8_E4M3))
+    assert lib.pa_quest_summarize(fp8, FAKE, FAKE, FAKE, None, None) == _lib.PA_ERR_UNSUPPORTED
+    assert lib.pa_quest_summarize(s, FAKE, None, FAKE, None, None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_quest_select(s, FAKE, FAKE, FAKE, FAKE, 0, FAKE, None, None) == \
+        _lib.PA_ERR_INVALID_ARG                                          # topk < 1
+    assert lib.pa_quest_select(fp8, FAKE, FAKE, FAKE, FAKE, 4, FAKE, None, None) == \
+        _lib.PA_ERR_UNSUPPORTED

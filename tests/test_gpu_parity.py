@@ -305,6 +305,109 @@ def test_window_one_returns_last_v_and_skips_old_blocks():
     assert dev.read_err() == 0
 
 
+# ---------------------------------------------------------------- Quest page selection
+
+def _quest_scores_numpy(batch):
+    """Exact page scores [B][Hkv] -> list over pages (group max), from the pool."""
+    bs, G = batch.block_size, batch.Hq // batch.Hkv
+    q = wl.bf16_to_float(batch.q).astype(np.float64)
+    kf = wl.bf16_to_float(batch.k_pool).astype(np.float64)
+    out = {}
+    for b in range(batch.B):
+        L = int(batch.seq_lens[b])
+        t = np.arange(L)
+        K = kf[batch.block_tables[b, t // bs], t % bs]
+        for kvh in range(batch.Hkv):
+            sc = []
+            for j in range((L + 15) // 16):
+                kk = K[16 * j:16 * j + 16, kvh]
+                qs = q[b, kvh * G:(kvh + 1) * G]
+                sc.append(np.max(np.maximum(qs * kk.min(0), qs * kk.max(0)).sum(1)))
+            out[b, kvh] = np.array(sc)
+    return out
+
+
+def _check_selection(batch, gpu_sel, ref_sel, topk):
+    """Selections agree wherever the exact k-th / (k+1)-th score gap exceeds fp32
+    rounding; elsewhere the GPU's choice must still be a valid top-k."""
+    scores = _quest_scores_numpy(batch)
+    agree = np.zeros(gpu_sel.shape[:2], bool)
+    for (b, kvh), sc in scores.items():
+        g, r = gpu_sel[b, kvh], ref_sel[b, kvh]
+        n = min(topk, sc.size)
+        assert np.all(g[n:] == -1) and np.all(np.diff(g[:n]) > 0)
+        if np.array_equal(g, r):
+            agree[b, kvh] = True
+            continue
+        srt = np.sort(sc)[::-1]
+        gap = srt[n - 1] - srt[n] if n < sc.size else np.inf
+        assert gap <= 1e-4 * max(1.0, abs(srt[n - 1])), (b, kvh, gap)
+        assert sc[g[:n]].min() >= srt[n - 1] - 1e-4 * max(1.0, abs(srt[n - 1]))
+    return agree
+
+
+def test_quest_summaries_bit_exact():
+    batch = wl.build_batch("t", [1, 15, 16, 17, 100, 333], Hq=16, Hkv=4, D=128, block_size=32,
+                           seed=90)
+    dev = DeviceBatch(batch)
+    dev.quest_build_summaries()
+    torch.cuda.synchronize()
+    got = dev.key_summaries.view(torch.int16).cpu().numpy().view(np.uint16)
+    kf = wl.bf16_to_float(batch.k_pool)
+    for b in range(batch.B):
+        L = int(batch.seq_lens[b])
+        for j in range((L + 15) // 16):
+            t = np.arange(16 * j, min(L, 16 * j + 16))
+            rows = kf[batch.block_tables[b, t // 32], t % 32]          # [n, Hkv, D]
+            page = batch.block_tables[b, 16 * j // 32] * 2 + (16 * j % 32) // 16
+            assert np.array_equal(got[page, :, 0], wl.bf16_bits(rows.min(0)))
+            assert np.array_equal(got[page, :, 1], wl.bf16_bits(rows.max(0)))
+    assert dev.read_err() == 0
+
+
+@pytest.mark.parametrize("topk,bs", [(1, 16), (4, 16), (13, 32), (64, 16)])
+def test_quest_select_and_sparse_decode(topk, bs):
+    lens = [1, 15, 16, 17, 100, 333, 1000, 2047, 0, 64]
+    batch = wl.build_batch("t", lens, Hq=64, Hkv=8, D=128, block_size=bs, seed=91 + topk)
+    dev = DeviceBatch(batch)
+    dev.quest_build_summaries()
+    sel = dev.quest_select(topk)
+    torch.cuda.synchronize()
+    gpu_sel = sel.cpu().numpy()
+    ref, ref_sel = oracle.quest_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                       batch.seq_lens, batch.sm_scale, Hkv=batch.Hkv,
+                                       block_size=bs, topk=topk)
+    agree = _check_selection(batch, gpu_sel, ref_sel, topk)
+    G = batch.Hq // batch.Hkv
+    rows = np.array([(b, h) for b in range(batch.B) for h in range(batch.Hq) if agree[b, h // G]])
+    for mode, ns in (("decode", None), ("split", 1), ("split", 11), ("split", 500)):
+        dev.out.fill_(float("nan"))
+        if mode == "decode":
+            dev.decode(selected_pages=sel)
+        else:
+            dev.decode_splitkv(ns, selected_pages=sel)
+        torch.cuda.synchronize()
+        out = dev.out.cpu().numpy()
+        assert_close(out[rows[:, 0], rows[:, 1]], ref[rows[:, 0], rows[:, 1]], batch,
+                     f"quest topk={topk} {mode} {ns}")
+    assert dev.read_err() == 0
+
+
+def test_quest_all_pages_equals_full_decode():
+    batch = wl.build_batch("t", [5, 70, 300], Hq=64, Hkv=8, D=128, block_size=16, seed=95)
+    dev = DeviceBatch(batch)
+    dev.quest_build_summaries()
+    sel = dev.quest_select(64)                    # more pages than any sequence has
+    ref, _ = oracle_after_write(batch, write=False)
+    for mode, ns in (("decode", None), ("split", 9)):
+        dev.out.fill_(float("nan"))
+        (dev.decode(selected_pages=sel) if mode == "decode"
+         else dev.decode_splitkv(ns, selected_pages=sel))
+        torch.cuda.synchronize()
+        assert_close(dev.out.cpu().numpy(), ref, batch, f"quest all pages {mode}")
+    assert dev.read_err() == 0
+
+
 # ---------------------------------------------------------------- invariants
 
 def _bits(x):
