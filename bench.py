@@ -38,8 +38,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic per decode launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum), with
 # the hash of the kernel sources it was measured on; reported only while they still match.
 TRAFFIC = {
-    "llama70b_layer": {"bytes": 1_338_525_000 + 5_267_712, "kernel_hash": "45a9972f6b80ccba"},
-    "fp8_mixed": {"bytes": 2_260_870_000 + 24_728_064, "kernel_hash": "45a9972f6b80ccba"},
+    "int4_mixed": {"bytes": 1_122_790_144 + 16_972_160, "kernel_hash": "1039cbd6dd7087aa"},
 }
 
 
@@ -136,14 +135,44 @@ class ClockSampler:
 # our arm
 # ----------------------------------------------------------------------------
 
+# the sources the decode kernel is compiled from
+DECODE_SOURCES = ("pa_common.cuh", "pa_decode.cu", "pa_internal.h")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_28_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in DECODE_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+L2_BYTES = 128 << 20                 # GB300 L2 (~129 MB)
+L2_FLUSH_BELOW = 4 * L2_BYTES        # steps reading less KV than this are timed flushed
+
+
+def step_kv_tokens(batch, args, selected=None) -> int:
+    """KV tokens one decode step reads once each (averaged over the KV heads): the
+    unique tokens, only the window's, or only the chosen pages' (pages of 16 tokens,
+    a sequence's last page may be short); selected: [B, Hkv, topk] page indices."""
+    if args.quest_topk > 0:
+        L = batch.seq_lens.astype(np.int64)[:, None, None]
+        pages = np.asarray(selected, dtype=np.int64)
+        rows = np.where(pages >= 0, np.minimum(16, L - 16 * pages), 0)
+        return int(rows.sum()) // batch.Hkv
+    return batch.unique_kv_tokens(args.window)
+
+
+def step_kv_bytes(batch, args, selected=None) -> int:
+    """Algorithmic bytes of one decode launch: KV rows (+ per-block scales of a
+    quantised pool)."""
+    n = step_kv_tokens(batch, args, selected) * batch.kv_bytes_per_token()
+    if batch.quantized:
+        n += sum(int(x) for x in (batch.seq_lens + batch.block_size - 1)
+                 // batch.block_size) * batch.scale_bytes_per_block()
+    return n
 
 
 def measured_peak_hbm():
@@ -213,8 +242,7 @@ def run_ours(args):
     quest = args.quest_topk > 0
     if quest:       # summaries of the whole cache, then per step: summarise the new
         dev.quest_build_summaries(stream)      # token's page, select, sparse decode
-        dev.selected_pages = torch.empty((batch.B, batch.Hkv, args.quest_topk),
-                                         dtype=torch.int32, device=dev_id)
+        dev.quest_buffers(args.quest_topk)
 
     def step(i=None):
         dev.reshape_and_cache(stream)
@@ -222,8 +250,8 @@ def run_ours(args):
             _lib.pa_quest_summarize(dev.shape, dev.k_pool, dev.key_summaries, dev.slot_mapping,
                                     dev.err, stream)
             _lib.pa_quest_select(dev.shape, dev.q, dev.key_summaries, dev.block_tables,
-                                 dev.seq_lens, args.quest_topk, dev.selected_pages, dev.err,
-                                 stream)
+                                 dev.seq_lens, args.quest_topk, dev.page_scores,
+                                 dev.selected_pages, dev.err, stream)
         if i is not None:
             ev[i][0].record(stream)
         _lib.pa_decode_splitkv(dev.shape, dev.out, dev.workspace, ns, dev.q, dev.k_pool,
@@ -241,6 +269,20 @@ def run_ours(args):
     if dev.read_err():
         raise RuntimeError("device error flag set during warm-up")
 
+    # a step that reads less than L2_FLUSH_BELOW bytes of KV would find part of it in
+    # L2 from the step before: read a buffer twice the L2 size between such steps (a
+    # read leaves L2 clean, as the weight reads of a model's other kernels would; a
+    # written buffer would leave dirty lines for the next step to write back) and time
+    # each step alone with events (the flush is not timed)
+    selected = dev.selected_pages.cpu().numpy() if quest else None
+    kv_bytes = step_kv_bytes(batch, args, selected)
+    flush = None
+    if kv_bytes < L2_FLUSH_BELOW:
+        flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev_id)
+        flush_sink = torch.empty((), dtype=torch.float32, device=dev_id)
+        st_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
@@ -249,12 +291,20 @@ def run_ours(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            torch.sum(flush, dim=0, out=flush_sink)
+            st_ev[i][0].record(stream)
         step(i // EVENT_EVERY if i % EVENT_EVERY == 0 else None)
+        if flush is not None:
+            st_ev[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop()
     barrier(world)
-    ms_total = t_start.elapsed_time(t_end)
+    if flush is None:
+        ms_total = t_start.elapsed_time(t_end)
+    else:
+        ms_total = sum(a.elapsed_time(b) for a, b in st_ev)
     ms_total = reduce_max(ms_total, world, dev_id)
     ms_per_step = ms_total / args.steps
     decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
@@ -289,14 +339,7 @@ def run_ours(args):
     if dev.read_err():
         raise RuntimeError("device error flag set during the timed steps")
 
-    unique_tokens = batch.unique_kv_tokens(args.window)
-    if args.quest_topk > 0:     # the chosen pages' tokens (pages of 16; the last may be short)
-        unique_tokens = int(sum(min(int(L), 16 * args.quest_topk) if (int(L) + 15) // 16 <=
-                                args.quest_topk else 16 * args.quest_topk for L in batch.seq_lens))
-    kv_bytes = unique_tokens * batch.kv_bytes_per_token()
-    if batch.quantized:
-        kv_bytes += sum(int(n) for n in (batch.seq_lens + batch.block_size - 1)
-                        // batch.block_size) * batch.scale_bytes_per_block()
+    unique_tokens = step_kv_tokens(batch, args, selected)
     peak, peak_kind = measured_peak_hbm()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
     tr = TRAFFIC.get(args.config) if args.window == 0 and args.quest_topk == 0 else None
@@ -322,9 +365,14 @@ def run_ours(args):
             "unique_kv_tokens": unique_tokens, "num_splits": ns,
             "window": args.window,
             "quest_topk": args.quest_topk,
-            "l2": f"no flush: {kv_bytes / 1e9:.2f} GB of KV read per step >> 129 MB L2",
+            "l2": (f"no flush: {kv_bytes / 1e9:.2f} GB of KV read per step >> 129 MB L2"
+                   if flush is None else
+                   f"flushed: {kv_bytes / 1e9:.3f} GB of KV per step, a {2 * L2_BYTES >> 20} MB "
+                   "buffer read between steps, each step timed alone with events"),
             "parallelism": f"replicas x{world}" if world > 1 else "single",
-            "step": "pa_reshape_and_cache + pa_decode_splitkv + pa_merge_lse",
+            "step": ("pa_reshape_and_cache + pa_quest_summarize + pa_quest_select + "
+                     "pa_decode_splitkv + pa_merge_lse" if args.quest_topk > 0 else
+                     "pa_reshape_and_cache + pa_decode_splitkv + pa_merge_lse"),
         },
         "roofline": {
             "bound": "hbm",

@@ -213,6 +213,10 @@ int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count);
  * concurrent calls; nothing in it needs initialising.  1 <= num_splits <= 65536.
  * opts (may be NULL): the window and the shared-prefix L2 hint, see
  * pa_decode_opts; with a window the partition runs over the attended tiles only.
+ * 4-bit pools with an even number of KV heads, 8 query heads per KV head and
+ * no Quest selection are read two adjacent KV heads at a time (their 64-byte
+ * rows form one 128-byte run per token): the partition's pairs are then
+ * (b, KV heads 2u and 2u + 1).  The result does not depend on it.
  * Batches of more than 16384 sequences return PA_ERR_UNSUPPORTED (each CTA
  * scans the sequence lengths in shared memory).
  */
@@ -288,19 +292,26 @@ pa_status pa_quest_summarize(const pa_shape *shape, const void *k_pool, void *ke
                              pa_stream_t stream);
 
 /*
- * pa_quest_select -- for every (sequence b, KV head h): score each 16-token page j of
- * b (pages 0 .. ceil(L/16) - 1, reached through block_tables) with every query head
- * g of the group as  sum_d max(q[b][g][d] * min_d, q[b][g][d] * max_d)  (fp32), keep
- * the page's largest score over the group, and write the topk best pages (ties to
- * the lower page index; all pages if there are at most topk) in increasing order to
- * selected_pages[b][h][0 .. topk), -1 past the number of pages.  bf16 pools only;
- * q [B, Hq, D] bf16.  Pass the result to pa_decode / pa_decode_splitkv through
- * pa_decode_opts.  Page scores are fp32 sums, so pages whose scores agree to
- * rounding may be ordered differently from an exact computation.
+ * pa_quest_select -- Quest's two steps for every (sequence b, KV head h): score
+ * each 16-token page j of b (pages 0 .. ceil(L/16) - 1, reached through
+ * block_tables) with every query head g of the group as
+ *     sum_d max(q[b][g][d] * min_d, q[b][g][d] * max_d)      (fp32)
+ * keep the page's largest score over the group in
+ *     page_scores[b][h][j],  page_scores: [B, Hkv, P] fp32, P = ceil(max_blocks *
+ *     block_size / 16), entries j >= pages of b left untouched,
+ * then write the topk best pages (ties to the lower page index; all pages if
+ * there are at most topk) in increasing order to selected_pages[b][h][0 .. topk),
+ * -1 past the number of pages.  A page whose block-table entry is outside
+ * [0, nblocks) sets PA_DEVERR_BLOCK_ID and scores -inf.  bf16 pools only; q
+ * [B, Hq, D] bf16; page_scores and selected_pages are caller-owned device memory
+ * (outputs).  Pass selected_pages to pa_decode / pa_decode_splitkv through
+ * pa_decode_opts.  Scores are fp32 sums, so pages whose scores agree to rounding
+ * may be ordered differently from an exact computation.
  */
 pa_status pa_quest_select(const pa_shape *shape, const void *q, const void *key_summaries,
                           const int32_t *block_tables, const int32_t *seq_lens, int32_t topk,
-                          int32_t *selected_pages, int32_t *err_flag, pa_stream_t stream);
+                          float *page_scores, int32_t *selected_pages, int32_t *err_flag,
+                          pa_stream_t stream);
 
 /* Human-readable name of a status. */
 const char *pa_status_string(pa_status status);

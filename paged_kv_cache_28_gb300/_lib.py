@@ -78,7 +78,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "pa_read_error_flag": (I32, [P, ctypes.POINTER(I32), P]),
             "pa_decode_splitkv_noalloc": (I32, [S, P, I32, P, P, P, P, P, P, P, F, P, P]),
             "pa_quest_summarize": (I32, [S, P, P, P, P, P]),
-            "pa_quest_select": (I32, [S, P, P, P, P, I32, P, P, P]),
+            "pa_quest_select": (I32, [S, P, P, P, P, I32, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -207,8 +207,8 @@ def pa_quest_summarize(shape: pa_shape, k_pool, key_summaries, slot_mapping, err
 
 
 def pa_quest_select(shape: pa_shape, q, key_summaries, block_tables, seq_lens, topk: int,
-                    selected_pages, err_flag=None, stream=None) -> None:
+                    page_scores, selected_pages, err_flag=None, stream=None) -> None:
     lib = load()
     _check("pa_quest_select", lib.pa_quest_select(
         ctypes.byref(shape), _ptr(q), _ptr(key_summaries), _ptr(block_tables), _ptr(seq_lens),
-        int(topk), _ptr(selected_pages), _ptr(err_flag), _stream(stream)))
+        int(topk), _ptr(page_scores), _ptr(selected_pages), _ptr(err_flag), _stream(stream)))

@@ -161,17 +161,23 @@ pa_status pa_quest_summarize(const pa_shape *shape, const void *k_pool, void *ke
 
 pa_status pa_quest_select(const pa_shape *shape, const void *q, const void *key_summaries,
                           const int32_t *block_tables, const int32_t *seq_lens, int32_t topk,
-                          int32_t *selected_pages, int32_t *err_flag, pa_stream_t stream) {
+                          float *page_scores, int32_t *selected_pages, int32_t *err_flag,
+                          pa_stream_t stream) {
   pa_status st = check_shape(shape, true);
   if (st != PA_OK) return st;
   if (shape->kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
   if (topk < 1) return PA_ERR_INVALID_ARG;
   if (shape->B == 0) return PA_OK;
-  st = check_ptrs({q, key_summaries, block_tables, seq_lens, selected_pages});
+  st = check_ptrs({q, key_summaries, block_tables, seq_lens, page_scores, selected_pages});
   if (st != PA_OK) return st;
-  if (pa::quest_select_smem(*shape) > 200 * 1024) return PA_ERR_UNSUPPORTED;
+  if (pa::quest_topk_smem(*shape) > 200 * 1024 || pa::quest_score_smem(*shape) > 200 * 1024)
+    return PA_ERR_UNSUPPORTED;
+  // (sequence, KV head, page) units are counted in int32
+  if (static_cast<int64_t>(shape->B) * shape->Hkv * pa::quest_max_pages(*shape) > INT32_MAX)
+    return PA_ERR_UNSUPPORTED;
   return pa::run_quest_select(*shape, q, key_summaries, block_tables, seq_lens, topk,
-                              selected_pages, err_flag, reinterpret_cast<cudaStream_t>(stream));
+                              page_scores, selected_pages, err_flag,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *pa_status_string(pa_status status) {

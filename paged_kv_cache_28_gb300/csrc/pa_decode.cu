@@ -44,6 +44,11 @@ namespace pa {
 constexpr int kKindBf16 = 0;
 constexpr int kKindFp8 = 1;   // E4M3 codes, one per byte
 constexpr int kKindInt4 = 2;  // 4-bit codes, two per byte (offset binary)
+// 4-bit codes with two adjacent KV heads per unit: their 64-byte rows sit side by
+// side in the pool, so one 128-byte box per token feeds both and every fetched
+// byte is used (a lone 64-byte row costs a 128-byte DRAM fetch); n-tile h serves
+// the group of KV head 2 u + h.
+constexpr int kKindInt4x2 = 3;
 
 template <int D_, int NT_, int KIND_>
 struct Cfg {
@@ -51,18 +56,20 @@ struct Cfg {
   static constexpr int NT = NT_;            // 8-head n-tiles (G <= 8 * NT)
   static constexpr int KIND = KIND_;
   static constexpr bool FP8 = KIND == kKindFp8;
-  static constexpr bool INT4 = KIND == kKindInt4;
+  static constexpr bool INT4 = KIND == kKindInt4 || KIND == kKindInt4x2;
+  static constexpr bool PAIRED = KIND == kKindInt4x2;
+  static constexpr int HEADS = PAIRED ? 2 : 1;      // KV heads per unit
   static constexpr bool QUANT = KIND != kKindBf16;   // codes x per-(block, head) scale
   static constexpr int KS = D / 16;         // QK k-steps of 16 elements
   static constexpr int DT = D / 16;         // PV 16-row output tiles
-  static constexpr int ROW = INT4 ? D / 2 : (FP8 ? D : 2 * D);  // bytes of one token's head row
+  static constexpr int ROW = HEADS * (INT4 ? D / 2 : (FP8 ? D : 2 * D));  // bytes of a unit's row
   static constexpr int BOX_BYTES = ROW < 128 ? ROW : 128;        // TMA box width (swizzle span)
   static constexpr int BOXES = ROW / BOX_BYTES;                  // boxes per tile row
   static constexpr int BOX_X = BOX_BYTES / (KIND == kKindBf16 ? 2 : 1);  // box width in elements
   static constexpr int KV_BYTES = kTile * ROW;
   static constexpr int Q_BYTES = 8 * NT * D * 2;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
-  static constexpr int STAGES = INT4 ? 4 : 2;
+  static constexpr int STAGES = PAIRED ? 3 : (INT4 ? 4 : 2);
   static constexpr int WARPS = 4;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int META_BYTES = 32;     // int4 unit + k/v scale
@@ -72,6 +79,7 @@ struct Cfg {
   static constexpr int MIN_BLOCKS_RAW = (227 * 1024) / (SMEM + 1024 + 4096);
   static constexpr int MIN_BLOCKS = MIN_BLOCKS_RAW < 1 ? 1 : (MIN_BLOCKS_RAW > 4 ? 4 : MIN_BLOCKS_RAW);
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(!PAIRED || (NT == 2 && D == 128), "paired heads: one n-tile per KV head");
   static_assert(KV_BYTES % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
 };
 
@@ -106,8 +114,8 @@ struct State {
   float m[C::NT][2];            // running max, log2 domain, heads 2q, 2q+1 of each n-tile
   float l[C::NT][2];            // this thread's share of the running sum
   uint32_t qf[C::NT][C::KS][2]; // Q^T B-fragments
-  float qshift;                 // FP8: 2^-k undoing the power-of-two scaling of q
-  float vs;                     // FP8: V scale the accumulator is expressed in
+  float qshift;                 // quantised: 2^-k undoing the power-of-two scaling of q
+  float vs[C::NT];              // quantised: V scale each n-tile's accumulator is expressed in
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -118,9 +126,9 @@ struct State {
         for (int i = 0; i < 4; ++i) acc[nt][dt][i] = 0.f;
       m[nt][0] = m[nt][1] = -INFINITY;
       l[nt][0] = l[nt][1] = 0.f;
+      vs[nt] = 1.f;
     }
     qshift = 1.f;
-    vs = 1.f;
   }
 };
 
@@ -244,11 +252,14 @@ __device__ __forceinline__ int pair_tile_count(int L, int window, int topk) {
 }
 
 // One 16-token tile: scores, online-softmax update, P V accumulation.
-// sscale: factor from raw mma scores to log2-domain scores; vs: FP8 V scale.
+// sscale[nt]: factor from raw mma scores to log2-domain scores; vs[nt]: V scale of a
+// quantised tile (the accumulator's unit; nonzero); vzero[h]: the tile's V scale of
+// the unit's KV head h is zero, so its V rows count as zeros.
 template <class C>
 __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint32_t vtile,
-                                             int lo, int nvalid, float sscale, float vs,
-                                             int lane) {
+                                             int lo, int nvalid, const float (&sscale)[C::NT],
+                                             const float (&vs)[C::NT],
+                                             const bool (&vzero)[C::HEADS], int lane) {
   // tokens lo <= t < nvalid of the tile are attended
   const int r = lane >> 2, qd = lane & 3;
   float s[C::NT][4];
@@ -269,27 +280,39 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
       for (int nt = 0; nt < C::NT; ++nt) mma_bf16(s[nt], a, st.qf[nt][ks][0], st.qf[nt][ks][1]);
     }
   } else if constexpr (C::INT4) {
-    // 64-byte rows, 64-byte swizzle: lane (r, q) receives nibbles b..b+7 (b = 32c + 8q)
-    // of row r; int4_pair_f16 yields the pairs (b+i, b+i+4) that load_q mirrors.
+    // 64-byte head rows: lane (r, q) receives nibbles b..b+7 (b = 32c + 8q) of row r;
+    // int4_pair_f16 yields the pairs (b+i, b+i+4) that load_q mirrors.  One head: a
+    // 64-byte-swizzled box; paired heads: head h is chunks 4h..4h+3 of a 128-byte-
+    // swizzled row and feeds n-tile h only.
     const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-    for (int cc = 0; cc < C::D / 64; ++cc) {
-      const int c = 2 * cc + (lane >> 4);
-      uint32_t R[4];
-      ldsm_x4(R, ktile + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+    for (int h = 0; h < C::HEADS; ++h)
 #pragma unroll
-      for (int half = 0; half < 2; ++half)      // chunk 2cc + half: R[2 half] rows r, R[2 half + 1] rows r + 8
+      for (int cc = 0; cc < C::D / 64; ++cc) {
+        const int c = 2 * cc + (lane >> 4);
+        uint32_t R[4];
+        if constexpr (C::PAIRED)
+          ldsm_x4(R, ktile + row * 128 + (((4 * h + c) ^ (row & 7)) << 4));
+        else
+          ldsm_x4(R, ktile + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * u),
-                                 int4_pair_f16(R[2 * half + 1], 2 * u),
-                                 int4_pair_f16(R[2 * half], 2 * u + 1),
-                                 int4_pair_f16(R[2 * half + 1], 2 * u + 1)};
-          const int ks = (2 * cc + half) * 2 + u;
+        for (int half = 0; half < 2; ++half)    // chunk 2cc + half: R[2 half] rows r, R[2 half + 1] rows r + 8
 #pragma unroll
-          for (int nt = 0; nt < C::NT; ++nt) mma_f16(s[nt], a, st.qf[nt][ks][0], st.qf[nt][ks][1]);
-        }
-    }
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * u),
+                                   int4_pair_f16(R[2 * half + 1], 2 * u),
+                                   int4_pair_f16(R[2 * half], 2 * u + 1),
+                                   int4_pair_f16(R[2 * half + 1], 2 * u + 1)};
+            const int ks = (2 * cc + half) * 2 + u;
+            if constexpr (C::PAIRED) {
+              mma_f16(s[h], a, st.qf[h][ks][0], st.qf[h][ks][1]);
+            } else {
+#pragma unroll
+              for (int nt = 0; nt < C::NT; ++nt)
+                mma_f16(s[nt], a, st.qf[nt][ks][0], st.qf[nt][ks][1]);
+            }
+          }
+      }
   } else {
     // ldmatrix on byte pairs: lane (r, q) receives codes 4q..4q+3 of a 16-code chunk;
     // the mma's k order is permuted accordingly (load_q applies the same order to q).
@@ -320,7 +343,7 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int t = r + ((i >> 1) << 3);
-      x[i] = (t >= lo && t < nvalid) ? s[nt][i] * sscale : -INFINITY;
+      x[i] = (t >= lo && t < nvalid) ? s[nt][i] * sscale[nt] : -INFINITY;
     }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -334,14 +357,17 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
       p[nt][j] = ex2(x[j] - mnew);
       p[nt][j + 2] = ex2(x[j + 2] - mnew);
       st.l[nt][j] = st.l[nt][j] * alpha + (p[nt][j] + p[nt][j + 2]);
-      corr[nt][j] = C::QUANT ? alpha * (st.vs / vs) : alpha;
+      corr[nt][j] = C::QUANT ? alpha * (st.vs[nt] / vs[nt]) : alpha;
     }
 #pragma unroll
     for (int dt = 0; dt < C::DT; ++dt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) st.acc[nt][dt][i] *= corr[nt][i & 1];
   }
-  if constexpr (C::QUANT) st.vs = vs;
+  if constexpr (C::QUANT) {
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt) st.vs[nt] = vs[nt];
+  }
 
   // ---- P^T fragments: hi + lo 16-bit parts, transposed in registers
   uint32_t bh[C::NT][2], bl[C::NT][2];
@@ -367,13 +393,16 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
 
   // ---- O^T += V^T P^T; rows of V beyond nvalid are zeroed in registers (the pool
   // may hold stale or non-finite values there)
-  const bool partial = nvalid < kTile || lo > 0;
+  const bool ragged = nvalid < kTile || lo > 0;
   uint32_t m01 = 0xFFFFFFFFu, m23 = 0xFFFFFFFFu;
-  if (partial) {
+  if (ragged) {
     auto in = [&](int t) { return t >= lo && t < nvalid; };
     m01 = (in(2 * qd) ? 0x0000FFFFu : 0u) | (in(2 * qd + 1) ? 0xFFFF0000u : 0u);
     m23 = (in(2 * qd + 8) ? 0x0000FFFFu : 0u) | (in(2 * qd + 9) ? 0xFFFF0000u : 0u);
   }
+  if constexpr (C::QUANT && !C::PAIRED)   // a zero V scale: the tile's V rows are zeros
+    if (vzero[0]) m01 = m23 = 0u;
+  const bool partial = ragged || (C::QUANT && !C::PAIRED && vzero[0]);
   if constexpr (!C::QUANT) {
     const int t = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
@@ -396,31 +425,47 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
   } else if constexpr (C::INT4) {
     // ldmatrix.trans on the byte-pair view gives lane (r, q) the nibbles d = 32c + 4r
     // .. +3 of tokens 2q (low half) and 2q + 1 (high half): int4_pair_f16(., i) is
-    // V^T row d = 32c + 4r + i over tokens (2q, 2q + 1).
+    // V^T row d = 32c + 4r + i over tokens (2q, 2q + 1).  Paired heads as for K.
     const int t = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-    for (int cc = 0; cc < C::D / 64; ++cc) {
-      const int c = 2 * cc + (lane >> 4);
-      uint32_t R[4];
-      ldsm_x4_trans(R, vtile + t * 64 + ((c ^ ((t >> 1) & 3)) << 4));
+    for (int h = 0; h < C::HEADS; ++h) {
+      uint32_t k01 = m01, k23 = m23;
+      bool mask = partial;
+      if constexpr (C::PAIRED) {
+        if (vzero[h]) k01 = k23 = 0u;
+        mask = ragged || vzero[h];
+      }
 #pragma unroll
-      for (int half = 0; half < 2; ++half)      // chunk 2cc + half
+      for (int cc = 0; cc < C::D / 64; ++cc) {
+        const int c = 2 * cc + (lane >> 4);
+        uint32_t R[4];
+        if constexpr (C::PAIRED)
+          ldsm_x4_trans(R, vtile + t * 128 + (((4 * h + c) ^ (t & 7)) << 4));
+        else
+          ldsm_x4_trans(R, vtile + t * 64 + ((c ^ ((t >> 1) & 3)) << 4));
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {        // rows 4r + 2mt + {0, 1}
-          uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * mt),
-                           int4_pair_f16(R[2 * half], 2 * mt + 1),
-                           int4_pair_f16(R[2 * half + 1], 2 * mt),
-                           int4_pair_f16(R[2 * half + 1], 2 * mt + 1)};
-          if (partial) {
-            a[0] &= m01;
-            a[1] &= m01;
-            a[2] &= m23;
-            a[3] &= m23;
+        for (int half = 0; half < 2; ++half)    // chunk 2cc + half
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {      // rows 4r + 2mt + {0, 1}
+            uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * mt),
+                             int4_pair_f16(R[2 * half], 2 * mt + 1),
+                             int4_pair_f16(R[2 * half + 1], 2 * mt),
+                             int4_pair_f16(R[2 * half + 1], 2 * mt + 1)};
+            if (mask) {
+              a[0] &= k01;
+              a[1] &= k01;
+              a[2] &= k23;
+              a[3] &= k23;
+            }
+            const int dt = (2 * cc + half) * 2 + mt;
+            if constexpr (C::PAIRED) {
+              mma_f16(st.acc[h][dt], a, bh[h][0], bh[h][1]);
+            } else {
+#pragma unroll
+              for (int nt = 0; nt < C::NT; ++nt) mma_f16(st.acc[nt][dt], a, bh[nt][0], bh[nt][1]);
+            }
           }
-          const int dt = (2 * cc + half) * 2 + mt;
-#pragma unroll
-          for (int nt = 0; nt < C::NT; ++nt) mma_f16(st.acc[nt][dt], a, bh[nt][0], bh[nt][1]);
-        }
+      }
     }
   } else {
     // ldmatrix.trans on byte pairs gives lane (r, q): bytes (t=2q: d=2r, 2r+1) and
@@ -480,7 +525,7 @@ __device__ __forceinline__ void write_normalised(const State<C> &st, float *dst,
     for (int j = 0; j < 2; ++j) {
       const int g = nt * 8 + 2 * qd + j;
       if (g >= G) continue;
-      const float f = (C::QUANT ? st.vs : 1.f) / ltot[nt][j];
+      const float f = (C::QUANT ? st.vs[nt] : 1.f) / ltot[nt][j];
 #pragma unroll
       for (int dt = 0; dt < C::DT; ++dt) {
         dst[g * C::D + acc_d<C>(dt, j, lane)] = st.acc[nt][dt][j] * f;
@@ -641,13 +686,18 @@ __device__ __forceinline__ void issue(const WarpSmem &ws, int s, int4 u, const P
   const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
   ws.meta[2 * s] = u;
   if constexpr (C::QUANT) {
+    // (k, v) scale of each KV head of the unit: heads kvh, or 2 kvh and 2 kvh + 1
     float *sc = reinterpret_cast<float *>(&ws.meta[2 * s + 1]);
     if (phys != kInvalidPhys) {
-      cp_async_4(smem_u32(sc), p.k_scale + static_cast<size_t>(phys) * p.Hkv + kvh);
-      cp_async_4(smem_u32(sc + 1), p.v_scale + static_cast<size_t>(phys) * p.Hkv + kvh);
+#pragma unroll
+      for (int h = 0; h < C::HEADS; ++h) {
+        const size_t i = (static_cast<size_t>(phys) * p.Hkv + kvh) * C::HEADS + h;
+        cp_async_4(smem_u32(sc + 2 * h), p.k_scale + i);
+        cp_async_4(smem_u32(sc + 2 * h + 1), p.v_scale + i);
+      }
     } else {
-      sc[0] = 0.f;
-      sc[1] = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2 * C::HEADS; ++h) sc[h] = 0.f;
     }
     cp_async_arrive(bar);
   }
@@ -710,7 +760,15 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
     const int4 u = ws.meta[2 * s];
     uint8_t *stage = ws.stage + s * C::STAGE_BYTES;
     const uint32_t ktile = smem_u32(stage);
-    float sscale = p.sl2, vs = 1.f;
+    float sscale[C::NT], vs[C::NT];
+    bool vzero[C::HEADS];
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt) {
+      sscale[nt] = p.sl2;
+      vs[nt] = 1.f;
+    }
+#pragma unroll
+    for (int h = 0; h < C::HEADS; ++h) vzero[h] = false;
     if (u.w & kPieceStart) {
       st.reset();
       load_q<C>(st, ktile + 2 * C::KV_BYTES,
@@ -718,13 +776,21 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
       piece_first = (u.w & kFirstOfPair) != 0;
     }
     if constexpr (C::QUANT) {
+      // n-tile nt reads KV head nt of the unit (paired) or the unit's one head; a zero
+      // V scale keeps the accumulator's unit and zeroes the tile's V rows instead
       const float4 sc = *reinterpret_cast<const float4 *>(&ws.meta[2 * s + 1]);
-      sscale = p.sl2 * sc.x * st.qshift;
-      vs = sc.y;
-      if (u.w & kPieceStart) st.vs = vs;
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt) {
+        const int h = C::PAIRED ? nt : 0;
+        const float ks = h ? sc.z : sc.x, v = h ? sc.w : sc.y;
+        sscale[nt] = p.sl2 * ks * st.qshift;
+        vzero[h] = !(v > 0.f);
+        vs[nt] = vzero[h] ? st.vs[nt] : v;
+        if ((u.w & kPieceStart) && !vzero[h]) st.vs[nt] = v;
+      }
     }
     process_tile<C>(st, ktile, ktile + C::KV_BYTES, (u.w >> kLoShift) & 0xF, u.w & 0xFF, sscale,
-                    vs, lane);
+                    vs, vzero, lane);
     if (u.w & kPieceEnd) on_piece_end(u, piece_first, st);
     __syncwarp();
     if (i + C::STAGES < n) issue<C>(ws, s, src.get(i + C::STAGES, lane), p, tmK, tmV, lane);
@@ -831,7 +897,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
           sm_m[warp * GP + g] = st.m[nt][j];
           sm_l[warp * GP + g] = ltot[nt][j];
         }
-        const float f = C::QUANT ? st.vs : 1.f;
+        const float f = C::QUANT ? st.vs[nt] : 1.f;
 #pragma unroll
         for (int dt = 0; dt < C::DT; ++dt) {
           sm_acc[(warp * GP + g) * C::D + acc_d<C>(dt, j, lane)] = st.acc[nt][dt][j] * f;
@@ -935,13 +1001,17 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.topk = p.topk;
   src.begin = min(seg * W, total);
   src.end = (seg < p.num_splits) ? min(src.begin + W, total) : src.begin;
+  // the chosen pages are written by the selection launched just before
+  if (p.sel) pdl_wait();
   src.init(lane);
-  // everything above reads only caller inputs (lengths, block tables); the pools
-  // (written by the cache write) and the workspace (read by the previous merge)
-  // are touched only after the previous grid has finished
+  // without a selection everything above reads only caller inputs (lengths, block
+  // tables); the pools (written by the cache write) and the workspace (read by the
+  // previous merge) are touched only after the previous grid has finished
   pdl_wait();
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i <= p.B; i += C::THREADS) p.prefix_out[i] = prefix[i];
+    if (threadIdx.x == 0) p.prefix_out[p.B + 1] = C::HEADS;   // KV heads per unit, for the merge
+  }
   State<C> st;
   st.reset();
   run_warp<C>(
@@ -961,7 +1031,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 }
 
 // One CTA per (b, kvh) pair; threads over (head, 4 consecutive d).  The pieces of a
-// pair are visited eight at a time with their loads issued together.
+// pair are visited eight at a time with their loads issued together.  The decode
+// leaves the number of KV heads per unit (1, or 2 for paired 4-bit heads) after
+// the tile prefix: head kvh's partials are then rows (kvh % 2) G .. of unit kvh / 2.
 __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *prefix,
                                                     const float *o_part, const float *lse_part,
                                                     int B, int Hq, int Hkv, int G, int D,
@@ -970,8 +1042,11 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
   pdl_wait();
   const int pair = blockIdx.x;
   const int b = pair / Hkv, kvh = pair - b * Hkv;
+  const int heads = prefix[B + 1] == 2 ? 2 : 1;
+  const int unit = kvh / heads, row0 = (kvh - unit * heads) * G;
+  const int Hu = Hkv / heads, Gu = G * heads;      // units per sequence, rows per unit
   const int start_b = prefix[b];
-  const int nt = (prefix[b + 1] - start_b) / Hkv;
+  const int nt = (prefix[b + 1] - start_b) / Hu;
   const int total = prefix[B];
   const int W = max(1, (total + num_splits - 1) / num_splits);
   float *o = out + (static_cast<size_t>(b) * Hq + kvh * G) * D;
@@ -981,19 +1056,19 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
       reinterpret_cast<float4 *>(o)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const int start = start_b + kvh * nt, end = start + nt;
+  const int start = start_b + unit * nt, end = start + nt;
   const int p0 = start / W, p1 = (end - 1) / W;
   if (p0 == p1) return;
   constexpr int U = 8;
   for (int e = threadIdx.x; e < G * D4; e += blockDim.x) {
-    const int g = e / D4, d4 = e - g * D4;
+    const int g = e / D4, d4 = e - g * D4, gu = row0 + g;
     auto slot = [&](int s) { return static_cast<size_t>(s) * 2 + (s == p0 ? 1 : 0); };
     float M = -INFINITY;
     for (int s0 = p0; s0 <= p1; s0 += U) {
       float v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        v[u] = (s0 + u <= p1) ? __ldg(lse_part + slot(s0 + u) * G + g) : -INFINITY;
+        v[u] = (s0 + u <= p1) ? __ldg(lse_part + slot(s0 + u) * Gu + gu) : -INFINITY;
 #pragma unroll
       for (int u = 0; u < U; ++u) M = fmaxf(M, v[u]);
     }
@@ -1005,8 +1080,8 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const bool ok = s0 + u <= p1;
-        l[u] = ok ? __ldg(lse_part + slot(s0 + u) * G + g) : -INFINITY;
-        x[u] = ok ? __ldg(reinterpret_cast<const float4 *>(o_part + (slot(s0 + u) * G + g) * D) + d4)
+        l[u] = ok ? __ldg(lse_part + slot(s0 + u) * Gu + gu) : -INFINITY;
+        x[u] = ok ? __ldg(reinterpret_cast<const float4 *>(o_part + (slot(s0 + u) * Gu + gu) * D) + d4)
                   : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
@@ -1046,11 +1121,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2D view of a pool: rows = nblocks * bs tokens, columns = one token's Hkv head rows
 // (bf16 elements, or bytes for the code pools); box = 16 rows x one head row of up to
 // 128 bytes, swizzled by the box width (128 or 64 bytes).
-static bool make_pool_map(CUtensorMap *map, const void *pool, const pa_shape &s) {
+// s: the decode's view of the shape (Hkv counts units of `heads` adjacent KV heads).
+static bool make_pool_map(CUtensorMap *map, const void *pool, const pa_shape &s, int heads) {
   auto fn = encode_fn();
   if (!fn) return false;
   const bool bf16 = s.kv_dtype == PA_KV_BF16;
-  const int row_bytes = s.kv_dtype == PA_KV_INT4 ? s.D / 2 : (bf16 ? 2 * s.D : s.D);
+  const int row_bytes = heads * (s.kv_dtype == PA_KV_INT4 ? s.D / 2 : (bf16 ? 2 * s.D : s.D));
   const int box_bytes = row_bytes < 128 ? row_bytes : 128;
   const int eb = bf16 ? 2 : 1;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.Hkv) * row_bytes / eb,
@@ -1132,8 +1208,27 @@ static pa_status launch_segments(const Params &p, const CUtensorMap &mk, const C
 #define PA_DISPATCH(D_, NT_, KIND_, FN, ...)                                  \
   if (s.D == D_ && nt == NT_ && kind == KIND_) return FN<Cfg<D_, NT_, KIND_>>(__VA_ARGS__);
 
-static int kind_of(const pa_shape &s) {
-  return s.kv_dtype == PA_KV_FP8_E4M3 ? kKindFp8 : (s.kv_dtype == PA_KV_INT4 ? kKindInt4 : kKindBf16);
+// 4-bit pools whose KV heads can be served two at a time: an even number of heads,
+// groups of 8 query heads (one n-tile each), D = 128.  A Quest selection is per KV
+// head, so a decode with one serves the heads singly.
+static bool int4_pairable(const pa_shape &s) {
+  return s.kv_dtype == PA_KV_INT4 && s.D == 128 && s.Hkv % 2 == 0 && s.Hq == 8 * s.Hkv;
+}
+
+static int heads_per_unit(const pa_shape &s, const pa_decode_opts *opts) {
+  return (int4_pairable(s) && !(opts && opts->topk > 0 && opts->selected_pages)) ? 2 : 1;
+}
+
+// The decode's view of the shape: units of `heads` adjacent KV heads.
+static pa_shape unit_view(const pa_shape &s, int heads) {
+  pa_shape v = s;
+  v.Hkv = s.Hkv / heads;
+  return v;
+}
+
+static int kind_of(const pa_shape &s, int heads) {
+  if (s.kv_dtype == PA_KV_INT4) return heads == 2 ? kKindInt4x2 : kKindInt4;
+  return s.kv_dtype == PA_KV_FP8_E4M3 ? kKindFp8 : kKindBf16;
 }
 
 #define PA_DISPATCH_ALL(FN, ...)                      \
@@ -1144,20 +1239,23 @@ static int kind_of(const pa_shape &s) {
   PA_DISPATCH(128, 1, kKindFp8, FN, __VA_ARGS__)      \
   PA_DISPATCH(128, 2, kKindFp8, FN, __VA_ARGS__)      \
   PA_DISPATCH(128, 1, kKindInt4, FN, __VA_ARGS__)     \
-  PA_DISPATCH(128, 2, kKindInt4, FN, __VA_ARGS__)
+  PA_DISPATCH(128, 2, kKindInt4, FN, __VA_ARGS__)     \
+  PA_DISPATCH(128, 2, kKindInt4x2, FN, __VA_ARGS__)
 
-static pa_status dispatch_pair(const pa_shape &s, const Params &p, const CUtensorMap &mk,
-                               const CUtensorMap &mv, cudaStream_t st) {
+// s: the unit view; p.G query heads per unit
+static pa_status dispatch_pair(const pa_shape &s, int heads, const Params &p,
+                               const CUtensorMap &mk, const CUtensorMap &mv, cudaStream_t st) {
   const int nt = (p.G + 7) / 8;
-  const int kind = kind_of(s);
+  const int kind = kind_of(s, heads);
   PA_DISPATCH_ALL(launch_pair, p, mk, mv, st)
   return PA_ERR_UNSUPPORTED;
 }
 
-static pa_status dispatch_segments(const pa_shape &s, const Params &p, const CUtensorMap &mk,
-                                   const CUtensorMap &mv, cudaStream_t st) {
+static pa_status dispatch_segments(const pa_shape &s, int heads, const Params &p,
+                                   const CUtensorMap &mk, const CUtensorMap &mv,
+                                   cudaStream_t st) {
   const int nt = (p.G + 7) / 8;
-  const int kind = kind_of(s);
+  const int kind = kind_of(s, heads);
   PA_DISPATCH_ALL(launch_segments, p, mk, mv, st)
   return PA_ERR_UNSUPPORTED;
 }
@@ -1167,28 +1265,35 @@ static int cfg_split_smem(int B) { return split_smem<C>(B); }
 template <class C>
 static int cfg_min_blocks(int) { return C::MIN_BLOCKS; }
 
-int splitkv_smem_bytes(const pa_shape &s) {
+// Sizing of the split kernel a decode without a Quest selection launches.
+int splitkv_smem_bytes(const pa_shape &shape) {
+  const int heads = heads_per_unit(shape, nullptr);
+  const pa_shape s = unit_view(shape, heads);
   const int nt = (s.Hq / s.Hkv + 7) / 8;
-  const int kind = kind_of(s);
+  const int kind = kind_of(s, heads);
   PA_DISPATCH_ALL(cfg_split_smem, s.B)
   return 0;
 }
 
 int decode_warps_per_cta() { return Cfg<128, 1, false>::WARPS; }
 
-int splitkv_min_blocks(const pa_shape &s) {
+int splitkv_min_blocks(const pa_shape &shape) {
+  const int heads = heads_per_unit(shape, nullptr);
+  const pa_shape s = unit_view(shape, heads);
   const int nt = (s.Hq / s.Hkv + 7) / 8;
-  const int kind = kind_of(s);
+  const int kind = kind_of(s, heads);
   PA_DISPATCH_ALL(cfg_min_blocks, 0)
   return 1;
 }
 
+// prefix int32[B + 2] (tile prefix, then KV heads per unit), lse f32[splits][2][Gu],
+// o_part f32[splits][2][Gu][D]; Gu = query heads of the largest unit the shape allows.
 WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits) {
   WorkspaceLayout w{};
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  const size_t G = static_cast<size_t>(s.Hq / s.Hkv);
+  const size_t G = static_cast<size_t>(s.Hq / s.Hkv) * (int4_pairable(s) ? 2 : 1);
   w.prefix = 0;
-  w.lse = up(w.prefix + (static_cast<size_t>(s.B) + 1) * 4);
+  w.lse = up(w.prefix + (static_cast<size_t>(s.B) + 2) * 4);
   w.o_part = up(w.lse + static_cast<size_t>(num_splits) * 2 * G * 4);
   w.total = up(w.o_part + static_cast<size_t>(num_splits) * 2 * G * s.D * 4);
   return w;
@@ -1198,10 +1303,13 @@ pa_status run_decode(const pa_shape &s, float *out, const void *q, const void *k
                      const void *v_pool, const float *k_scale, const float *v_scale,
                      const int32_t *bt, const int32_t *sl, const pa_decode_opts *opts,
                      float sm_scale, int32_t *err, cudaStream_t stream) {
+  const int heads = heads_per_unit(s, opts);
+  const pa_shape v = unit_view(s, heads);
   CUtensorMap mk, mv;
-  if (!make_pool_map(&mk, k_pool, s) || !make_pool_map(&mv, v_pool, s)) return PA_ERR_CUDA;
-  Params p = make_params(s, out, q, k_scale, v_scale, bt, sl, opts, sm_scale, err);
-  return dispatch_pair(s, p, mk, mv, stream);
+  if (!make_pool_map(&mk, k_pool, v, heads) || !make_pool_map(&mv, v_pool, v, heads))
+    return PA_ERR_CUDA;
+  Params p = make_params(v, out, q, k_scale, v_scale, bt, sl, opts, sm_scale, err);
+  return dispatch_pair(v, heads, p, mk, mv, stream);
 }
 
 pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int num_splits,
@@ -1211,15 +1319,18 @@ pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int
                              int32_t *err, cudaStream_t stream) {
   const WorkspaceLayout w = splitkv_layout(s, num_splits);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
+  const int heads = heads_per_unit(s, opts);
+  const pa_shape v = unit_view(s, heads);
   CUtensorMap mk, mv;
-  if (!make_pool_map(&mk, k_pool, s) || !make_pool_map(&mv, v_pool, s)) return PA_ERR_CUDA;
-  Params p = make_params(s, out, q, k_scale, v_scale, bt, sl, opts, sm_scale, err);
+  if (!make_pool_map(&mk, k_pool, v, heads) || !make_pool_map(&mv, v_pool, v, heads))
+    return PA_ERR_CUDA;
+  Params p = make_params(v, out, q, k_scale, v_scale, bt, sl, opts, sm_scale, err);
   p.shared_prefix_lens = opts ? opts->shared_prefix_lens : nullptr;
   p.prefix_out = reinterpret_cast<int32_t *>(ws + w.prefix);
   p.lse_part = reinterpret_cast<float *>(ws + w.lse);
   p.o_part = reinterpret_cast<float *>(ws + w.o_part);
   p.num_splits = num_splits;
-  return dispatch_segments(s, p, mk, mv, stream);
+  return dispatch_segments(v, heads, p, mk, mv, stream);
 }
 
 pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int num_splits,

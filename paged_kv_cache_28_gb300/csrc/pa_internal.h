@@ -68,9 +68,12 @@ pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int nu
 
 pa_status run_quest_summarize(const pa_shape &s, const void *k_pool, void *summaries,
                               const int64_t *slot_mapping, int32_t *err, cudaStream_t stream);
-size_t quest_select_smem(const pa_shape &s);
+int quest_max_pages(const pa_shape &s);
+size_t quest_score_smem(const pa_shape &s);
+size_t quest_topk_smem(const pa_shape &s);
 pa_status run_quest_select(const pa_shape &s, const void *q, const void *summaries,
                            const int32_t *block_tables, const int32_t *seq_lens, int topk,
-                           int32_t *selected, int32_t *err, cudaStream_t stream);
+                           float *page_scores, int32_t *selected, int32_t *err,
+                           cudaStream_t stream);
 
 }  // namespace pa

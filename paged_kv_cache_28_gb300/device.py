@@ -113,11 +113,21 @@ class DeviceBatch:
                                 b.max_blocks)
         _lib.pa_quest_summarize(shape, self.k_pool, self.key_summaries, slots, self.err, stream)
 
-    def quest_select(self, topk: int, stream=None) -> torch.Tensor:
-        self.selected_pages = torch.empty((self.batch.B, self.batch.Hkv, topk), dtype=torch.int32,
+    def quest_buffers(self, topk: int):
+        """page_scores [B, Hkv, pages per block-table row] and selected_pages [B, Hkv, topk]."""
+        b = self.batch
+        max_pages = (b.max_blocks * b.block_size + 15) // 16
+        self.page_scores = torch.zeros((b.B, b.Hkv, max_pages), dtype=torch.float32,
+                                       device=self.device)
+        self.selected_pages = torch.empty((b.B, b.Hkv, topk), dtype=torch.int32,
                                           device=self.device)
+
+    def quest_select(self, topk: int, stream=None) -> torch.Tensor:
+        if getattr(self, "selected_pages", None) is None or self.selected_pages.shape[2] != topk:
+            self.quest_buffers(topk)
         _lib.pa_quest_select(self.shape, self.q, self.key_summaries, self.block_tables,
-                             self.seq_lens, topk, self.selected_pages, self.err, stream)
+                             self.seq_lens, topk, self.page_scores, self.selected_pages,
+                             self.err, stream)
         return self.selected_pages
 
     def read_err(self, stream=None) -> int:

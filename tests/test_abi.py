@@ -103,6 +103,12 @@ def test_splitkv_host_checks(lib):
     assert expect_min <= nbytes <= expect_min + 3 * 256
     assert _lib.pa_splitkv_workspace_bytes(s, 0) == 0
     assert _lib.pa_splitkv_workspace_bytes(s, 70000) == 0
+    # 4-bit pools read two KV heads at a time: partials of 16 query heads per piece
+    s4 = shape(B=64, Hq=64, Hkv=8, D=128, max_blocks=2048, nblocks=30000,
+               kv_dtype=_lib.PA_KV_INT4)
+    n4 = _lib.pa_splitkv_workspace_bytes(s4, 1216)
+    expect4 = (66 * 4) + 1216 * 2 * 16 * 4 + 1216 * 2 * 16 * 128 * 4
+    assert expect4 <= n4 <= expect4 + 3 * 256
     args = [ctypes.byref(s), FAKE, FAKE, nbytes - 1, 1216, FAKE, FAKE, FAKE, None, None, FAKE,
             FAKE, None, 0.1, None, None]
     assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # workspace too small
@@ -144,7 +150,9 @@ def test_quest_host_checks(lib):
     fp8 = ctypes.byref(shape(D=128, kv_dtype=_lib.PA_KV_FP8_E4M3))
     assert lib.pa_quest_summarize(fp8, FAKE, FAKE, FAKE, None, None) == _lib.PA_ERR_UNSUPPORTED
     assert lib.pa_quest_summarize(s, FAKE, None, FAKE, None, None) == _lib.PA_ERR_INVALID_ARG
-    assert lib.pa_quest_select(s, FAKE, FAKE, FAKE, FAKE, 0, FAKE, None, None) == \
+    assert lib.pa_quest_select(s, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, None, None) == \
         _lib.PA_ERR_INVALID_ARG                                          # topk < 1
-    assert lib.pa_quest_select(fp8, FAKE, FAKE, FAKE, FAKE, 4, FAKE, None, None) == \
+    assert lib.pa_quest_select(s, FAKE, FAKE, FAKE, FAKE, 4, None, FAKE, None, None) == \
+        _lib.PA_ERR_INVALID_ARG                                          # no page_scores
+    assert lib.pa_quest_select(fp8, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, None, None) == \
         _lib.PA_ERR_UNSUPPORTED

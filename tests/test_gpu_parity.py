@@ -258,6 +258,64 @@ def test_int4_g16_bs32_window():
         assert_close(run_gpu(dev, mode, ns, window=50), ref, batch, f"int4 window {mode}")
 
 
+def test_int4_odd_kv_heads():
+    """G = 8 with an odd number of KV heads: 4-bit heads are served one at a time."""
+    batch = wl.build_batch("t", [1, 16, 17, 200, 0, 500], Hq=24, Hkv=3, D=128, block_size=16,
+                           seed=25, kv_dtype="int4")
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch)
+    _modes_run(dev, batch, ref, "int4 Hkv=3")
+
+
+def test_int4_selection_serves_heads_singly():
+    """A per-KV-head selection on a shape whose heads are otherwise read in pairs:
+    choosing every page must equal the full decode."""
+    batch = wl.build_batch("t", [5, 70, 300, 1], Hq=64, Hkv=8, D=128, block_size=16, seed=26,
+                           kv_dtype="int4")
+    dev = DeviceBatch(batch)
+    ref, _ = oracle_after_write(batch, write=False)
+    topk = 24
+    sel = np.full((batch.B, batch.Hkv, topk), -1, np.int32)
+    for b, L in enumerate(batch.seq_lens):
+        n = (int(L) + 15) // 16
+        sel[b, :, :n] = np.arange(n)
+    sel = torch.from_numpy(sel).to(dev.device)
+    for mode, ns in (("decode", None), ("split", 1), ("split", 9), ("split", 200)):
+        dev.out.fill_(float("nan"))
+        (dev.decode(selected_pages=sel) if mode == "decode"
+         else dev.decode_splitkv(ns, selected_pages=sel))
+        torch.cuda.synchronize()
+        assert_close(dev.out.cpu().numpy(), ref, batch, f"int4 all pages chosen {mode} {ns}")
+    assert dev.read_err() == 0
+
+
+@pytest.mark.parametrize("kv_dtype,Hq,Hkv", [("fp8_e4m3", 64, 8), ("int4", 64, 8),
+                                             ("int4", 24, 3)])
+def test_quantised_zero_scales(kv_dtype, Hq, Hkv):
+    """A (block, head) whose scale is 0 restores to zeros (the writer stores scale 0
+    for an all-zero block): its K rows score 0 and its V rows add nothing."""
+    batch = wl.build_batch("t", [40, 300, 17, 64], Hq=Hq, Hkv=Hkv, D=128, block_size=16,
+                           seed=27, kv_dtype=kv_dtype)
+    rng = np.random.default_rng(7)
+    for b, L in enumerate(batch.seq_lens):
+        for j in range((int(L) + 15) // 16):
+            blk = batch.block_tables[b, j]
+            for h in range(Hkv):
+                r = rng.integers(0, 4)           # 0: V scale 0, 1: K scale 0, 2: both, 3: none
+                if r in (0, 2):
+                    batch.v_scale[blk, h] = 0.0
+                if r in (1, 2):
+                    batch.k_scale[blk, h] = 0.0
+    dev = DeviceBatch(batch)
+    ref, _ = oracle_after_write(batch, write=False)
+    for mode, ns in (("decode", None), ("split", 1), ("split", 7), ("split", 100)):
+        out = run_gpu(dev, mode, ns)
+        assert np.isfinite(out).all(), (mode, ns)
+        assert_close(out, ref, batch, f"{kv_dtype} zero scales {mode} {ns}")
+    assert dev.read_err() == 0
+
+
 def test_fp8_g16_and_bs32():
     batch = wl.build_batch("t", [3, 64, 65, 400], Hq=32, Hkv=2, D=128, block_size=32, seed=22,
                            kv_dtype="fp8_e4m3")
@@ -362,6 +420,48 @@ def test_quest_summaries_bit_exact():
             page = batch.block_tables[b, 16 * j // 32] * 2 + (16 * j % 32) // 16
             assert np.array_equal(got[page, :, 0], wl.bf16_bits(rows.min(0)))
             assert np.array_equal(got[page, :, 1], wl.bf16_bits(rows.max(0)))
+    assert dev.read_err() == 0
+
+
+def _oracle_page_scores(batch):
+    """[B][Hkv] -> (scores over pages, fp32 error bound) from the oracle's page summary
+    and page score, group max taken here; the bound is 32 units of fp32 rounding of the
+    sum of |terms| (the kernel's sums are about nine additions deep)."""
+    bs, G = batch.block_size, batch.Hq // batch.Hkv
+    q = wl.bf16_to_float(batch.q).astype(np.float64)
+    kf = wl.bf16_to_float(batch.k_pool).astype(np.float64)
+    out = {}
+    for b in range(batch.B):
+        L = int(batch.seq_lens[b])
+        t = np.arange(L)
+        K = kf[batch.block_tables[b, t // bs], t % bs]
+        for kvh in range(batch.Hkv):
+            sc, tol = [], []
+            for j in range((L + 15) // 16):
+                mn, mx = oracle.page_summary(K[16 * j:16 * j + 16, kvh])
+                qs = q[b, kvh * G:(kvh + 1) * G]
+                sc.append(max(oracle.page_score(qs[g], mn, mx) for g in range(G)))
+                mag = np.abs(qs) @ np.maximum(np.abs(mn), np.abs(mx))
+                tol.append(32 * 2.0 ** -24 * mag.max())
+            out[b, kvh] = (np.array(sc), np.array(tol))
+    return out
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_quest_page_scores(bs):
+    lens = [1, 15, 16, 17, 100, 333, 1000, 2047, 0, 64, 4000]
+    batch = wl.build_batch("t", lens, Hq=32, Hkv=4, D=128, block_size=bs, seed=97 + bs)
+    dev = DeviceBatch(batch)
+    dev.quest_build_summaries()
+    dev.quest_buffers(8)
+    dev.page_scores.fill_(float("nan"))
+    dev.quest_select(8)
+    torch.cuda.synchronize()
+    got = dev.page_scores.cpu().numpy()
+    for (b, kvh), (sc, tol) in _oracle_page_scores(batch).items():
+        n = sc.size
+        assert np.all(np.abs(got[b, kvh, :n] - sc) <= tol), (b, kvh)
+        assert np.all(np.isnan(got[b, kvh, n:])), (b, kvh)            # untouched
     assert dev.read_err() == 0
 
 
