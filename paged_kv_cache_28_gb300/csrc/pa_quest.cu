@@ -37,22 +37,45 @@ __global__ void __launch_bounds__(128) quest_summarize_kernel(
   }
   if (__syncthreads_or(later)) return;
   const int rows = static_cast<int>(slot - page * kTile) + 1;
-  const int row_elems = Hkv * D;
-  for (int e = threadIdx.x; e < row_elems; e += blockDim.x) {
-    const int h = e / D, d = e - h * D;
-    float mn = INFINITY, mx = -INFINITY;
+  // eight consecutive channels of one KV head per thread and pass (16-byte loads of
+  // all 16 rows in flight; rows >= `rows` are not used)
+  const int row_vecs = Hkv * D / 8;
+  const uint4 *src = reinterpret_cast<const uint4 *>(k_pool + page * kTile * Hkv * D);
+  for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) {
+    uint4 x[kTile];
 #pragma unroll
-    for (int r = 0; r < kTile; ++r) {            // loads issued together, rows < `rows` used
+    for (int r = 0; r < kTile; ++r)
+      x[r] = r < rows ? __ldg(src + r * row_vecs + v) : make_uint4(0u, 0u, 0u, 0u);
+    float mn[8], mx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      mn[i] = INFINITY;
+      mx[i] = -INFINITY;
+    }
+#pragma unroll
+    for (int r = 0; r < kTile; ++r) {
       if (r < rows) {
-        const float v = __uint_as_float(
-            static_cast<uint32_t>(k_pool[(page * kTile + r) * row_elems + e]) << 16);
-        mn = fminf(mn, v);
-        mx = fmaxf(mx, v);
+        const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = bf16_lo(w[i]), hi = bf16_hi(w[i]);
+          mn[2 * i] = fminf(mn[2 * i], lo);
+          mx[2 * i] = fmaxf(mx[2 * i], lo);
+          mn[2 * i + 1] = fminf(mn[2 * i + 1], hi);
+          mx[2 * i + 1] = fmaxf(mx[2 * i + 1], hi);
+        }
       }
     }
-    uint16_t *dst = summ + ((page * Hkv + h) * 2) * D;
-    dst[d] = static_cast<uint16_t>(__float_as_uint(mn) >> 16);   // exact: bf16 inputs
-    dst[D + d] = static_cast<uint16_t>(__float_as_uint(mx) >> 16);
+    uint32_t pmn[4], pmx[4];                      // exact: the inputs are bf16
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      pmn[i] = (__float_as_uint(mn[2 * i]) >> 16) | (__float_as_uint(mn[2 * i + 1]) & 0xFFFF0000u);
+      pmx[i] = (__float_as_uint(mx[2 * i]) >> 16) | (__float_as_uint(mx[2 * i + 1]) & 0xFFFF0000u);
+    }
+    const int e = v * 8, h = e / D, d = e - h * D;
+    uint16_t *dst = summ + ((page * Hkv + h) * 2) * D + d;
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(pmn[0], pmn[1], pmn[2], pmn[3]);
+    *reinterpret_cast<uint4 *>(dst + D) = make_uint4(pmx[0], pmx[1], pmx[2], pmx[3]);
   }
 }
 
@@ -127,117 +150,212 @@ __device__ void scan_units(const int32_t *seq_lens, int B, int Hkv, int cap, int
   __syncthreads();
 }
 
-constexpr int kScoreThreads = 256;
-constexpr int kScorePages = 8;                   // pages in flight per warp
+// Page scoring as a tensor-core contraction.  Because min_d <= max_d,
+//     sum_d max(q_d min_d, q_d max_d) = sum_d q-_d min_d + sum_d q+_d max_d
+// with q+ = max(q, 0) and q- = min(q, 0): the product of a page's summary row
+// [min_0 .. min_{D-1}, max_0 .. max_{D-1}] (bf16, exactly as stored) with the
+// column [q-; q+] (bf16, exact).  A warp scores 16 pages of one (sequence, KV head)
+// against the group's 8 (or 16) query heads with m16n8k16 mma, fp32 accumulation.
+template <int D_, int NG_>
+struct ScoreCfg {
+  static constexpr int D = D_;
+  static constexpr int NG = NG_;                   // 8-head n-tiles (G <= 8 NG)
+  static constexpr int ROWB = 4 * D;               // one summary row: 2 D bf16
+  static constexpr int ROWP = ROWB + 16;           // padded row in shared memory: the 8 rows
+                                                   // an ldmatrix reads fall in distinct banks
+  static constexpr int CH = 16;                    // pages per chunk (the mma's m)
+  static constexpr int KSQ = D / 16;               // k-steps over one half of the row
+  static constexpr int QB = 8 * NG * D * 2;        // the group's query rows, zero-padded
+  static constexpr int BUF = CH * ROWP + QB;       // one stage
+  static constexpr int WARPS = 4;
+  static constexpr int THREADS = 32 * WARPS;
+  static constexpr int FIXED = WARPS * 2 * BUF + WARPS * 2 * 8;   // stages + mbarriers
+  static_assert(BUF % 16 == 0, "bulk copies need 16-byte aligned stages");
+};
 
-// Page scores.  The (sequence, KV head, page) units, pages fastest, are cut into
-// `nseg` equal contiguous segments, one per warp, so a long sequence spreads over
-// many warps.  Lane l covers channels [l E, l E + E), E = D / 32, and keeps the
-// group's queries for them in registers while its segment stays in one (sequence,
-// KV head); score[b][kvh][j] = max over the group of sum_d max(q_d min_d, q_d max_d).
-template <int NG>   // groups of 8 query heads (G <= 8 * NG)
-__global__ void __launch_bounds__(kScoreThreads, 2) quest_score_kernel(
+// The warp's share of the score workspace: a contiguous run of units cut into
+// chunks of at most 16 pages of one (sequence, KV head).
+struct ScoreChunk {
+  int b, kvh, j0, n;
+};
+
+template <class S>
+__global__ void __launch_bounds__(S::THREADS) quest_score_kernel(
     const uint16_t *q, const uint16_t *summ, const int32_t *block_tables,
-    const int32_t *seq_lens, int B, int Hq, int Hkv, int D, int bs, int nblocks, int max_blocks,
+    const int32_t *seq_lens, int B, int Hq, int Hkv, int bs, int nblocks, int max_blocks,
     int max_pages, int nseg, float *scores, int32_t *err) {
-  extern __shared__ int32_t prefix[];            // [B + 1]
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int D = S::D;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *stage = smem + warp * 2 * S::BUF;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::WARPS * 2 * S::BUF) + warp * 2;
+  int32_t *prefix = reinterpret_cast<int32_t *>(smem + S::FIXED);
+  const int G = Hq / Hkv;
   pdl_trigger();
+  if (lane == 0) {
+    mbar_init(smem_u32(&bar[0]), 1);
+    mbar_init(smem_u32(&bar[1]), 1);
+    fence_mbar_init();
+  }
+  for (int st = 0; st < 2; ++st) {                 // query rows G .. 8 NG - 1 stay zero
+    uint8_t *pad = stage + st * S::BUF + S::CH * S::ROWP + G * D * 2;
+    for (int o = lane * 16; o < (8 * S::NG - G) * D * 2; o += 32 * 16)
+      *reinterpret_cast<uint4 *>(pad + o) = make_uint4(0u, 0u, 0u, 0u);
+  }
   const int cap = max_blocks * bs;
-  scan_units<kScoreThreads>(seq_lens, B, Hkv, cap, prefix);
-  pdl_wait();                                    // summaries come from the launch before
-  const int lane = threadIdx.x & 31;
-  const int seg = blockIdx.x * (kScoreThreads / 32) + (threadIdx.x >> 5);
+  scan_units<S::THREADS>(seq_lens, B, Hkv, cap, prefix);
+  pdl_wait();                                      // summaries come from the launch before
+
+  const int seg = blockIdx.x * S::WARPS + warp;
   const int total = prefix[B];
   const int W = (total + nseg - 1) / nseg;
   int f = min(seg * W, total);
   const int end = min(f + W, total);
-  const int G = Hq / Hkv;
-  constexpr int E_MAX = 4;                       // D <= 128
-  const int E = D / 32;
-  while (f < end) {                              // warp-uniform
-    int lo = 0, hi = B - 1;                      // last sequence starting at or before f
+  auto take = [&](ScoreChunk &c) -> bool {         // next chunk of the segment
+    if (f >= end) return false;
+    int lo = 0, hi = B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (prefix[mid] <= f) lo = mid; else hi = mid - 1;
     }
-    const int b = lo;
-    const int npg = (prefix[b + 1] - prefix[b]) / Hkv;
-    const int r = f - prefix[b];
-    const int kvh = r / npg, j0 = r - kvh * npg;
-    const int run = min(end - f, npg - j0);
-    float qv[8 * NG][E_MAX];
+    const int npg = (prefix[lo + 1] - prefix[lo]) / Hkv;
+    const int r = f - prefix[lo];
+    c.b = lo;
+    c.kvh = r / npg;
+    c.j0 = r - c.kvh * npg;
+    c.n = min(min(S::CH, end - f), npg - c.j0);
+    f += c.n;
+    return true;
+  };
+  // copy chunk c's summary rows (and the group's query rows when with_q) into stage
+  // st; returns the mask of rows whose block-table entry is valid
+  auto issue = [&](const ScoreChunk &c, int st, bool with_q) -> unsigned {
+    uint8_t *buf = stage + st * S::BUF;
+    const uint32_t b = smem_u32(&bar[st]);
+    int page = 0;
+    bool ok = false;
+    if (lane < c.n) {
+      const int j = c.j0 + lane;
+      const int phys = __ldg(block_tables + static_cast<size_t>(c.b) * max_blocks + (j * kTile) / bs);
+      ok = phys >= 0 && phys < nblocks;
+      page = ok ? phys * (bs / kTile) + (j * kTile % bs) / kTile : 0;
+    }
+    const unsigned okm = __ballot_sync(0xffffffffu, ok);
+    const uint32_t bytes = __popc(okm) * S::ROWB + (with_q ? G * D * 2 : 0);
+    fence_proxy_async();                           // the stage was last read by ldmatrix
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(b, bytes);
+    __syncwarp();
+    if (ok)
+      bulk_load(smem_u32(buf + lane * S::ROWP),
+                summ + (static_cast<size_t>(page) * Hkv + c.kvh) * 2 * D, S::ROWB, b);
+    if (with_q && lane == 0)
+      bulk_load(smem_u32(buf + S::CH * S::ROWP),
+                q + (static_cast<size_t>(c.b) * Hq + c.kvh * G) * D, G * D * 2, b);
+    return okm;
+  };
+
+  uint32_t bneg[S::NG][S::KSQ][2], bpos[S::NG][S::KSQ][2];   // B fragments of q-, q+
+  ScoreChunk cur, nxt;
+  bool have = take(cur);
+  // per stage (held in scalars so that nothing is indexed by the runtime stage):
+  // valid-row masks, and bits 0/1 phase, 2/3 copies pending, 4/5 new query rows
+  unsigned okm0 = 0u, okm1 = 0u;
+  uint32_t flags = 0u;
+  int last_pair = -1;
+  if (have) {
+    okm0 = issue(cur, 0, true);
+    flags |= (1u << 2) | (1u << 4);
+    last_pair = cur.b * Hkv + cur.kvh;
+  }
+  int st = 0;
+  while (have) {
+    const int ot = st ^ 1;
+    const bool have_n = take(nxt);
+    if (have_n) {                                  // prefetch the next chunk
+      const int pr = nxt.b * Hkv + nxt.kvh;
+      const bool nq = pr != last_pair;
+      const unsigned m = issue(nxt, ot, nq);
+      if (ot) okm1 = m; else okm0 = m;
+      flags = (flags & ~(1u << (4 + ot))) | (1u << (2 + ot)) | (nq ? 1u << (4 + ot) : 0u);
+      last_pair = pr;
+    }
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar[st]), (flags >> st) & 1u))) {
+      if (lane == 0) set_err(err, PA_DEVERR_TIMEOUT);
+      if (flags & (1u << (2 + ot))) mbar_wait(smem_u32(&bar[ot]), (flags >> ot) & 1u);
+      return;
+    }
+    flags ^= 1u << st;                             // phase
+    flags &= ~(1u << (2 + st));                    // nothing pending
+    const unsigned okm_cur = st ? okm1 : okm0;
+    const uint8_t *buf = stage + st * S::BUF;
+    if (flags & (1u << (4 + st))) {                                // B fragments: q rows n, k pairs of the
+#pragma unroll                                     // chunk's channels, split by sign
+      for (int nt = 0; nt < S::NG; ++nt)
 #pragma unroll
-    for (int g = 0; g < 8 * NG; ++g)
+        for (int kq = 0; kq < S::KSQ; kq += 2) {
+          uint32_t r[4];
+          ldsm_x4(r, smem_u32(buf + S::CH * S::ROWP + (nt * 8 + (lane & 7)) * D * 2 +
+                              (2 * kq + (lane >> 3)) * 16));
 #pragma unroll
-      for (int e = 0; e < E_MAX; ++e)
-        qv[g][e] = (g < G && e < E)
-                       ? __uint_as_float(static_cast<uint32_t>(__ldg(
-                             q + (static_cast<size_t>(b) * Hq + kvh * G + g) * D + lane * E + e))
-                                         << 16)
-                       : 0.f;
-    const int32_t *row = block_tables + static_cast<size_t>(b) * max_blocks;
-    float *out = scores + (static_cast<size_t>(b) * Hkv + kvh) * max_pages;
-    for (int jb = j0; jb < j0 + run; jb += kScorePages) {
-      const int n = min(kScorePages, j0 + run - jb);
-      // lane k < n fetches the block-table entry of page jb + k
-      const int my_phys = lane < n ? __ldg(row + ((jb + lane) * kTile) / bs) : 0;
-      int phys[kScorePages];
-      uint2 mnv[kScorePages], mxv[kScorePages];
-#pragma unroll
-      for (int k = 0; k < kScorePages; ++k) {
-        phys[k] = __shfl_sync(0xffffffffu, my_phys, k);
-        mnv[k] = mxv[k] = make_uint2(0u, 0u);
-        if (k < n && phys[k] >= 0 && phys[k] < nblocks) {
-          const int j = jb + k;
-          const int64_t page =
-              static_cast<int64_t>(phys[k]) * (bs / kTile) + (j * kTile % bs) / kTile;
-          const uint16_t *sm = summ + ((page * Hkv + kvh) * 2) * D + lane * E;
-          if (E == 4) {
-            mnv[k] = __ldg(reinterpret_cast<const uint2 *>(sm));
-            mxv[k] = __ldg(reinterpret_cast<const uint2 *>(sm + D));
-          } else {                               // D = 64: two channels per lane
-            mnv[k].x = __ldg(reinterpret_cast<const uint32_t *>(sm));
-            mxv[k].x = __ldg(reinterpret_cast<const uint32_t *>(sm + D));
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t neg = ((r[i] >> 15) & 0x00010001u) * 0xFFFFu;   // halves with q < 0
+            bneg[nt][kq + (i >> 1)][i & 1] = r[i] & neg;
+            bpos[nt][kq + (i >> 1)][i & 1] = r[i] & ~neg;
           }
         }
-      }
+    }
+    float acc[S::NG][2][4];
 #pragma unroll
-      for (int k = 0; k < kScorePages; ++k) {
-        if (k >= n) break;
-        float best = -INFINITY;
-        if (phys[k] < 0 || phys[k] >= nblocks) {
-          if (lane == 0) set_err(err, PA_DEVERR_BLOCK_ID);
-        } else {
-          const float mn[E_MAX] = {bf16_lo(mnv[k].x), bf16_hi(mnv[k].x), bf16_lo(mnv[k].y),
-                                   bf16_hi(mnv[k].y)};
-          const float mx[E_MAX] = {bf16_lo(mxv[k].x), bf16_hi(mxv[k].x), bf16_lo(mxv[k].y),
-                                   bf16_hi(mxv[k].y)};
+    for (int nt = 0; nt < S::NG; ++nt)
 #pragma unroll
-          for (int ng = 0; ng < NG; ++ng) {
-            float acc[8];      // max(q mn, q mx) picks mx for q >= 0 and mn otherwise
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              acc[g] = 0.f;
+        for (int i = 0; i < 4; ++i) acc[nt][h][i] = 0.f;
+    const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-              for (int e = 0; e < E_MAX; ++e) {
-                const float qq = qv[ng * 8 + g][e];
-                acc[g] = fmaf(qq, qq >= 0.f ? mx[e] : mn[e], acc[g]);
-              }
-            }
-            const int head =
-                ng * 8 + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-            float tot = warp_sum8(acc, lane);
-            if (head >= G) tot = -INFINITY;
-            tot = fmaxf(tot, __shfl_xor_sync(0xffffffffu, tot, 4));
-            tot = fmaxf(tot, __shfl_xor_sync(0xffffffffu, tot, 8));
-            tot = fmaxf(tot, __shfl_xor_sync(0xffffffffu, tot, 16));
-            best = fmaxf(best, tot);
-          }
-        }
-        if (lane == k) out[jb + k] = best;       // spread the stores over the lanes
+    for (int ks = 0; ks < 2 * S::KSQ; ++ks) {      // ks < KSQ: the min half, else the max half
+      uint32_t a[4];
+      ldsm_x4(a, smem_u32(buf + row * S::ROWP + (2 * ks + (lane >> 4)) * 16));
+      const int kq = ks % S::KSQ;
+#pragma unroll
+      for (int nt = 0; nt < S::NG; ++nt) {
+        if (ks < S::KSQ)
+          mma_bf16(acc[nt][0], a, bneg[nt][kq][0], bneg[nt][kq][1]);
+        else
+          mma_bf16(acc[nt][1], a, bpos[nt][kq][0], bpos[nt][kq][1]);
       }
     }
-    f += run;
+    // element i of the accumulator: page (lane >> 2) + 8 (i >> 1), head 2 (lane & 3) + (i & 1)
+    float best[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < S::NG; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int head = nt * 8 + 2 * (lane & 3) + (i & 1);
+        if (head < G) best[i >> 1] = fmaxf(best[i >> 1], acc[nt][0][i] + acc[nt][1][i]);
+      }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      best[h] = fmaxf(best[h], __shfl_xor_sync(0xffffffffu, best[h], 1));
+      best[h] = fmaxf(best[h], __shfl_xor_sync(0xffffffffu, best[h], 2));
+    }
+    if ((lane & 3) == 0) {
+      float *out = scores + (static_cast<size_t>(cur.b) * Hkv + cur.kvh) * max_pages + cur.j0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = (lane >> 2) + 8 * h;
+        if (r < cur.n) {
+          const bool ok = (okm_cur >> r) & 1u;
+          if (!ok) set_err(err, PA_DEVERR_BLOCK_ID);
+          out[r] = ok ? best[h] : -INFINITY;
+        }
+      }
+    }
+    __syncwarp();
+    cur = nxt;
+    have = have_n;
+    st ^= 1;
   }
 }
 
@@ -362,7 +480,32 @@ int quest_max_pages(const pa_shape &s) {
 
 size_t quest_topk_smem(const pa_shape &s) { return static_cast<size_t>(quest_max_pages(s)) * 4; }
 
-size_t quest_score_smem(const pa_shape &s) { return (static_cast<size_t>(s.B) + 1) * 4; }
+template <int D, int NG>
+static size_t score_smem(int B) {
+  return ScoreCfg<D, NG>::FIXED + (static_cast<size_t>(B) + 1) * 4;
+}
+
+size_t quest_score_smem(const pa_shape &s) {
+  const bool two = s.Hq / s.Hkv > 8;
+  if (s.D == 64) return two ? score_smem<64, 2>(s.B) : score_smem<64, 1>(s.B);
+  return two ? score_smem<128, 2>(s.B) : score_smem<128, 1>(s.B);
+}
+
+template <class S>
+static cudaError_t launch_score(const pa_shape &s, int sms, const void *q, const void *summaries,
+                                const int32_t *block_tables, const int32_t *seq_lens,
+                                float *page_scores, int32_t *err, cudaStream_t stream) {
+  const size_t smem = S::FIXED + (static_cast<size_t>(s.B) + 1) * 4;
+  cudaError_t e = cudaFuncSetAttribute(quest_score_kernel<S>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = 2 * sms;                       // two CTAs per SM
+  return launch_pdl(quest_score_kernel<S>, dim3(grid), dim3(S::THREADS), smem, stream,
+                    static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(summaries),
+                    block_tables, seq_lens, s.B, s.Hq, s.Hkv, s.block_size, s.nblocks,
+                    s.max_blocks, quest_max_pages(s), grid * S::WARPS, page_scores, err);
+}
 
 pa_status run_quest_select(const pa_shape &s, const void *q, const void *summaries,
                            const int32_t *block_tables, const int32_t *seq_lens, int topk,
@@ -373,18 +516,19 @@ pa_status run_quest_select(const pa_shape &s, const void *q, const void *summari
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PA_ERR_CUDA;
   const int max_pages = quest_max_pages(s);
-  const size_t score_smem = quest_score_smem(s);
-  auto score = (s.Hq / s.Hkv <= 8) ? quest_score_kernel<1> : quest_score_kernel<2>;
-  if (cudaFuncSetAttribute(score, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(score_smem)) != cudaSuccess)
-    return PA_ERR_CUDA;
-  const int grid = 2 * sms;                      // two 8-warp CTAs per SM
-  const int nseg = grid * (kScoreThreads / 32);
-  if (launch_pdl(score, dim3(grid), dim3(kScoreThreads), score_smem, stream,
-                 static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(summaries),
-                 block_tables, seq_lens, s.B, s.Hq, s.Hkv, s.D, s.block_size, s.nblocks,
-                 s.max_blocks, max_pages, nseg, page_scores, err) != cudaSuccess)
-    return PA_ERR_CUDA;
+  const bool two = s.Hq / s.Hkv > 8;
+  cudaError_t e;
+  if (s.D == 64)
+    e = two ? launch_score<ScoreCfg<64, 2>>(s, sms, q, summaries, block_tables, seq_lens,
+                                             page_scores, err, stream)
+            : launch_score<ScoreCfg<64, 1>>(s, sms, q, summaries, block_tables, seq_lens,
+                                             page_scores, err, stream);
+  else
+    e = two ? launch_score<ScoreCfg<128, 2>>(s, sms, q, summaries, block_tables, seq_lens,
+                                              page_scores, err, stream)
+            : launch_score<ScoreCfg<128, 1>>(s, sms, q, summaries, block_tables, seq_lens,
+                                              page_scores, err, stream);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
   const size_t topk_smem = quest_topk_smem(s);
   if (cudaFuncSetAttribute(quest_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(topk_smem)) != cudaSuccess)
