@@ -207,6 +207,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
   return r;
 }
 
+// two E4M3 codes (high 16 bits) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t codes) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.f16x2.e4m3x2 %0, hi;\n}\n"
+      : "=r"(r)
+      : "r"(codes));
+  return r;
+}
+
 // two E4M3 codes (low 16 bits) -> two floats, exact
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t codes) {
   const uint32_t h = e4m3x2_to_f16x2(codes);

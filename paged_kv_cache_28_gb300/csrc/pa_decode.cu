@@ -69,7 +69,7 @@ struct Cfg {
   static constexpr int KV_BYTES = kTile * ROW;
   static constexpr int Q_BYTES = 8 * NT * D * 2;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
-  static constexpr int STAGES = PAIRED ? 3 : (INT4 ? 4 : 2);
+  static constexpr int STAGES = PAIRED ? 2 : (INT4 ? 4 : 2);
   static constexpr int WARPS = 4;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int META_BYTES = 32;     // int4 unit + k/v scale
@@ -115,7 +115,8 @@ struct State {
   float l[C::NT][2];            // this thread's share of the running sum
   uint32_t qf[C::NT][C::KS][2]; // Q^T B-fragments
   float qshift;                 // quantised: 2^-k undoing the power-of-two scaling of q
-  float vs[C::NT];              // quantised: V scale each n-tile's accumulator is expressed in
+  float vref[C::NT];            // quantised: V scale each n-tile's accumulator is expressed in
+  float vinv[C::NT];            // 1 / vref, or 0 before the piece's first nonzero V scale
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -126,7 +127,8 @@ struct State {
         for (int i = 0; i < 4; ++i) acc[nt][dt][i] = 0.f;
       m[nt][0] = m[nt][1] = -INFINITY;
       l[nt][0] = l[nt][1] = 0.f;
-      vs[nt] = 1.f;
+      vref[nt] = 1.f;
+      vinv[nt] = 0.f;
     }
     qshift = 1.f;
   }
@@ -253,8 +255,9 @@ __device__ __forceinline__ int pair_tile_count(int L, int window, int topk) {
 
 // One 16-token tile: scores, online-softmax update, P V accumulation.
 // sscale[nt]: factor from raw mma scores to log2-domain scores; vs[nt]: V scale of a
-// quantised tile (the accumulator's unit; nonzero); vzero[h]: the tile's V scale of
-// the unit's KV head h is zero, so its V rows count as zeros.
+// quantised tile; vzero[h]: the tile's V scale of the unit's KV head h is zero, so
+// its V rows count as zeros.  The accumulator stays in units of the piece's first
+// nonzero V scale: a tile with another scale enters through P scaled by the ratio.
 template <class C>
 __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint32_t vtile,
                                              int lo, int nvalid, const float (&sscale)[C::NT],
@@ -323,9 +326,9 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
       uint32_t R[4];
       ldsm_x4(R, ktile + row * 128 + ((c ^ (row & 7)) << 4));
       const uint32_t a0[4] = {e4m3x2_to_f16x2(R[0]), e4m3x2_to_f16x2(R[1]),
-                              e4m3x2_to_f16x2(R[0] >> 16), e4m3x2_to_f16x2(R[1] >> 16)};
+                              e4m3x2_hi_to_f16x2(R[0]), e4m3x2_hi_to_f16x2(R[1])};
       const uint32_t a1[4] = {e4m3x2_to_f16x2(R[2]), e4m3x2_to_f16x2(R[3]),
-                              e4m3x2_to_f16x2(R[2] >> 16), e4m3x2_to_f16x2(R[3] >> 16)};
+                              e4m3x2_hi_to_f16x2(R[2]), e4m3x2_hi_to_f16x2(R[3])};
 #pragma unroll
       for (int nt = 0; nt < C::NT; ++nt) {
         mma_f16(s[nt], a0, st.qf[nt][2 * kk][0], st.qf[nt][2 * kk][1]);
@@ -334,39 +337,75 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
     }
   }
 
-  // ---- online softmax (log2 domain); element i: token r + 8*(i>>1), head 2q + (i&1)
-  float p[C::NT][4];
-  float corr[C::NT][2];
+  // ---- V scale of a quantised tile relative to the accumulator's unit (warp-uniform).
+  // The piece starts with vinv = 0, so its first nonzero scale takes the rare branch
+  // that (re)expresses the accumulator in the tile's own scale.
+  float rat[C::NT];
 #pragma unroll
   for (int nt = 0; nt < C::NT; ++nt) {
-    float x[4];
+    rat[nt] = 1.f;
+    if constexpr (C::QUANT) {
+      rat[nt] = vs[nt] * st.vinv[nt];
+      if (!vzero[C::PAIRED ? nt : 0] && !(rat[nt] <= 4096.f && rat[nt] >= 1.f / 4096.f)) {
+        const float f = st.vref[nt] / vs[nt];   // keeps P * ratio well inside f16
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = r + ((i >> 1) << 3);
-      x[i] = (t >= lo && t < nvalid) ? s[nt][i] * sscale[nt] : -INFINITY;
+        for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) st.acc[nt][dt][i] *= f;
+        st.vref[nt] = vs[nt];
+        st.vinv[nt] = 1.f / vs[nt];
+        rat[nt] = 1.f;
+      }
     }
+  }
+
+  // ---- online softmax (log2 domain); element i: token r + 8*(i>>1), head 2q + (i&1)
+  const bool in0 = r >= lo && r < nvalid, in1 = r + 8 >= lo && r + 8 < nvalid;
+  float x[C::NT][4], mnew[C::NT][2];
+  bool grow = false;
+#pragma unroll
+  for (int nt = 0; nt < C::NT; ++nt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[nt][i] = ((i >> 1) ? in1 : in0) ? s[nt][i] * sscale[nt] : -INFINITY;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      float mx = fmaxf(x[j], x[j + 2]);
+      float mx = fmaxf(x[nt][j], x[nt][j + 2]);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const float mnew = fmaxf(st.m[nt][j], mx);
-      const float alpha = ex2(st.m[nt][j] - mnew);
-      st.m[nt][j] = mnew;
-      p[nt][j] = ex2(x[j] - mnew);
-      p[nt][j + 2] = ex2(x[j + 2] - mnew);
-      st.l[nt][j] = st.l[nt][j] * alpha + (p[nt][j] + p[nt][j + 2]);
-      corr[nt][j] = C::QUANT ? alpha * (st.vs[nt] / vs[nt]) : alpha;
+      mnew[nt][j] = fmaxf(st.m[nt][j], mx);
+      grow |= mnew[nt][j] > st.m[nt][j];
     }
-#pragma unroll
-    for (int dt = 0; dt < C::DT; ++dt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) st.acc[nt][dt][i] *= corr[nt][i & 1];
   }
-  if constexpr (C::QUANT) {
+  // the accumulator and the sums are rescaled only when some head's maximum grew
+  // (paired 4-bit units measured faster without the vote: they always rescale)
+  if constexpr (C::PAIRED)
+    grow = true;
+  else
+    grow = __any_sync(0xffffffffu, grow);
+  float p[C::NT][4];
 #pragma unroll
-    for (int nt = 0; nt < C::NT; ++nt) st.vs[nt] = vs[nt];
+  for (int nt = 0; nt < C::NT; ++nt) {
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      p[nt][j] = ex2(x[nt][j] - mnew[nt][j]);
+      p[nt][j + 2] = ex2(x[nt][j + 2] - mnew[nt][j]);
+      const float ps = p[nt][j] + p[nt][j + 2];
+      if (grow) {
+        alpha[j] = ex2(st.m[nt][j] - mnew[nt][j]);
+        st.l[nt][j] = st.l[nt][j] * alpha[j] + ps;
+      } else {
+        st.l[nt][j] += ps;
+      }
+      st.m[nt][j] = mnew[nt][j];
+    }
+    if (grow) {
+#pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st.acc[nt][dt][i] *= alpha[i & 1];
+    }
   }
 
   // ---- P^T fragments: hi + lo 16-bit parts, transposed in registers
@@ -382,8 +421,8 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
         lo = pack_bf16(p0 - bf16_lo(hi), p1 - bf16_hi(hi));
       } else {
         // f16 keeps 11 significant bits of p: one term is enough for the quantised
-        // caches' tolerance
-        hi = pack_f16(p0, p1);
+        // caches' tolerance; the ratio carries this tile's V scale
+        hi = pack_f16(p0 * rat[nt], p1 * rat[nt]);
         lo = 0;
       }
       bh[nt][h] = movmatrix_trans(hi);
@@ -525,7 +564,7 @@ __device__ __forceinline__ void write_normalised(const State<C> &st, float *dst,
     for (int j = 0; j < 2; ++j) {
       const int g = nt * 8 + 2 * qd + j;
       if (g >= G) continue;
-      const float f = (C::QUANT ? st.vs[nt] : 1.f) / ltot[nt][j];
+      const float f = (C::QUANT ? st.vref[nt] : 1.f) / ltot[nt][j];
 #pragma unroll
       for (int dt = 0; dt < C::DT; ++dt) {
         dst[g * C::D + acc_d<C>(dt, j, lane)] = st.acc[nt][dt][j] * f;
@@ -777,7 +816,7 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
     }
     if constexpr (C::QUANT) {
       // n-tile nt reads KV head nt of the unit (paired) or the unit's one head; a zero
-      // V scale keeps the accumulator's unit and zeroes the tile's V rows instead
+      // V scale zeroes the tile's V rows
       const float4 sc = *reinterpret_cast<const float4 *>(&ws.meta[2 * s + 1]);
 #pragma unroll
       for (int nt = 0; nt < C::NT; ++nt) {
@@ -785,8 +824,7 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
         const float ks = h ? sc.z : sc.x, v = h ? sc.w : sc.y;
         sscale[nt] = p.sl2 * ks * st.qshift;
         vzero[h] = !(v > 0.f);
-        vs[nt] = vzero[h] ? st.vs[nt] : v;
-        if ((u.w & kPieceStart) && !vzero[h]) st.vs[nt] = v;
+        vs[nt] = v;
       }
     }
     process_tile<C>(st, ktile, ktile + C::KV_BYTES, (u.w >> kLoShift) & 0xF, u.w & 0xFF, sscale,
@@ -897,7 +935,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
           sm_m[warp * GP + g] = st.m[nt][j];
           sm_l[warp * GP + g] = ltot[nt][j];
         }
-        const float f = C::QUANT ? st.vs[nt] : 1.f;
+        const float f = C::QUANT ? st.vref[nt] : 1.f;
 #pragma unroll
         for (int dt = 0; dt < C::DT; ++dt) {
           sm_acc[(warp * GP + g) * C::D + acc_d<C>(dt, j, lane)] = st.acc[nt][dt][j] * f;

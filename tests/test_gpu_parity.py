@@ -316,6 +316,43 @@ def test_quantised_zero_scales(kv_dtype, Hq, Hkv):
     assert dev.read_err() == 0
 
 
+def _abs_codes(pool, kv_dtype):
+    """Codes of |v| for every cached value v (same scales)."""
+    if kv_dtype == "fp8_e4m3":
+        return pool & np.uint8(0x7F)
+    lo, hi = (pool & 0x0F).astype(np.int16) - 8, (pool >> 4).astype(np.int16) - 8
+    return ((np.abs(lo) + 8) | ((np.abs(hi) + 8) << 4)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("kv_dtype,Hq,Hkv", [("fp8_e4m3", 64, 8), ("int4", 64, 8),
+                                             ("fp8_e4m3", 32, 2)])
+def test_quantised_scale_spread(kv_dtype, Hq, Hkv):
+    """Per-block V scales spread over six decades inside one sequence: the decode's
+    accumulator changes its V-scale unit along the way.  P reaches the PV product as
+    one f16 term (relative error <= 2^-11 per weight), so besides the quantised
+    tolerance each output may differ by 2^-9 sum_t p_t |v_t|; the oracle computes
+    that sum from a pool holding the codes of |v|."""
+    batch = wl.build_batch("t", [40, 700, 17, 1500], Hq=Hq, Hkv=Hkv, D=128, block_size=16,
+                           seed=28, kv_dtype=kv_dtype)
+    rng = np.random.default_rng(8)
+    batch.k_scale[:] *= (10.0 ** rng.uniform(-2, 1, batch.k_scale.shape)).astype(np.float32)
+    batch.v_scale[:] *= (10.0 ** rng.uniform(-3, 3, batch.v_scale.shape)).astype(np.float32)
+    dev = DeviceBatch(batch)
+    ref, _ = oracle_after_write(batch, write=False)
+    mag = oracle.paged_decode(batch.q, batch.k_pool, _abs_codes(batch.v_pool, kv_dtype),
+                              batch.block_tables, batch.seq_lens, batch.sm_scale, Hkv=Hkv,
+                              block_size=batch.block_size, k_scale=batch.k_scale,
+                              v_scale=batch.v_scale)
+    atol, rtol = TOL_FP8
+    for mode, ns in (("decode", None), ("split", 1), ("split", 5), ("split", 64)):
+        out = run_gpu(dev, mode, ns)
+        assert np.isfinite(out).all(), (mode, ns)
+        err = np.abs(out.astype(np.float64) - ref)
+        bound = atol + rtol * np.abs(ref) + 2.0 ** -9 * mag
+        assert np.all(err <= bound), (mode, ns, float((err - bound).max()))
+    assert dev.read_err() == 0
+
+
 def test_fp8_g16_and_bs32():
     batch = wl.build_batch("t", [3, 64, 65, 400], Hq=32, Hkv=2, D=128, block_size=32, seed=22,
                            kv_dtype="fp8_e4m3")
