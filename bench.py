@@ -239,6 +239,10 @@ def run_ours(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(0, args.steps, EVENT_EVERY)]
 
+    if args.cascade:            # shared prefixes attended once per group (prefix-aware decode)
+        if not batch.prefix_groups:
+            raise SystemExit("--cascade needs a workload with prefix groups (prefix_sharing)")
+        dev.enable_cascade()
     quest = args.quest_topk > 0
     if quest:       # summaries of the whole cache, then per step: summarise the new
         dev.quest_build_summaries(stream)      # token's page, select, sparse decode
@@ -258,7 +262,8 @@ def run_ours(args):
                                dev.v_pool, dev.k_scale, dev.v_scale, dev.block_tables,
                                dev.seq_lens, batch.sm_scale, dev.err, stream,
                                dev.shared_prefix_lens, args.window,
-                               dev.selected_pages if quest else None)
+                               dev.selected_pages if quest else None,
+                               dev.cascade if args.cascade else None)
         if i is not None:
             ev[i][1].record(stream)
         _lib.pa_merge_lse(dev.shape, dev.out, dev.workspace, ns, stream)
@@ -365,6 +370,7 @@ def run_ours(args):
             "unique_kv_tokens": unique_tokens, "num_splits": ns,
             "window": args.window,
             "quest_topk": args.quest_topk,
+            "cascade": bool(args.cascade),
             "l2": (f"no flush: {kv_bytes / 1e9:.2f} GB of KV read per step >> 129 MB L2"
                    if flush is None else
                    f"flushed: {kv_bytes / 1e9:.3f} GB of KV per step, a {2 * L2_BYTES >> 20} MB "
@@ -372,6 +378,8 @@ def run_ours(args):
             "parallelism": f"replicas x{world}" if world > 1 else "single",
             "step": ("pa_reshape_and_cache + pa_quest_summarize + pa_quest_select + "
                      "pa_decode_splitkv + pa_merge_lse" if args.quest_topk > 0 else
+                     "pa_reshape_and_cache + pa_decode_splitkv (cascade + split kernels) + "
+                     "pa_merge_lse" if args.cascade else
                      "pa_reshape_and_cache + pa_decode_splitkv + pa_merge_lse"),
         },
         "roofline": {
@@ -381,12 +389,13 @@ def run_ours(args):
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": traffic,
-            "kernel": "decode_segment_kernel (the pa_decode_splitkv call)",
+            "kernel": ("cascade_kernel + decode_segment_kernel (the pa_decode_splitkv call)"
+                       if args.cascade else "decode_segment_kernel (the pa_decode_splitkv call)"),
             "kernel_ms": decode_ms,
             "algorithmic_bytes": kv_bytes,
             "peak_kind": peak_kind,
         },
-        "gpu_launches": (5 if args.quest_topk > 0 else 3) * args.steps,
+        "gpu_launches": (5 if args.quest_topk > 0 else 4 if args.cascade else 3) * args.steps,
         "clocks": clock_info,
     }
     if e2e is not None:
@@ -490,8 +499,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="llama70b_layer",
                     choices=["tiny", "llama70b_layer", "prefix_sharing", "long_context",
-                             "fp8_mixed", "int4_mixed"])
+                             "fp8_mixed", "int4_mixed", "code_assistant_turns"])
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--cascade", action="store_true",
+                    help="prefix-aware decode: each prefix group's shared tokens attended once")
     ap.add_argument("--quest-topk", type=int, default=0,
                     help="query-aware sparse decode over the K best 16-token pages (0 = off)")
     ap.add_argument("--window", type=int, default=0,

@@ -123,12 +123,35 @@ typedef struct {
  *     fetched with an L2 evict-last policy, all other tiles evict-first, so a
  *     shared block stays in L2 for its other readers.  Any value gives the same
  *     result, bit for bit.
+ *   num_prefix_groups, group_offsets, group_seqs, group_prefix_len,
+ *     cascade_workspace: prefix-aware (cascade) decode, pa_decode_splitkv only
+ *     ("appendonly", "Prefix sharing is where the real win lives": many
+ *     sequences point at the same physical blocks).  Group g's members are
+ *     group_seqs[group_offsets[g] .. group_offsets[g + 1]) (device int32
+ *     arrays; group_offsets rises from 0, at most B members in all); their first
+ *     group_prefix_len[g] tokens (device int32, a multiple of 16) hold the same
+ *     keys and values, as when their block tables share those blocks.  A separate kernel attends over each group's shared tokens
+ *     once for all members and KV heads at a time (the members' query rows
+ *     stacked into one tensor-core contraction, reading the blocks through the
+ *     first member's table); the split kernel covers the rest of each sequence
+ *     and pa_merge_lse joins the two.  Each sequence belongs to at most one
+ *     group and every member holds at least group_prefix_len[g] tokens (a
+ *     member with fewer sets PA_DEVERR_SEQ_LEN and its output is undefined).
+ *     cascade_workspace: device memory of at least pa_cascade_workspace_bytes
+ *     bytes, 256-byte aligned, used by pa_decode_splitkv and read by the
+ *     following pa_merge_lse.  bf16 pools only; not combined with window or
+ *     topk.  The result equals the plain decode's up to rounding order.
  */
 typedef struct {
     int32_t window;
     int32_t topk;
     const int32_t *shared_prefix_lens;
     const int32_t *selected_pages;      /* [B, Hkv, topk] int32, with topk > 0 */
+    int32_t num_prefix_groups;          /* 0: no cascade */
+    const int32_t *group_offsets;       /* [num_prefix_groups + 1] */
+    const int32_t *group_seqs;          /* [group_offsets[num_prefix_groups]] */
+    const int32_t *group_prefix_len;    /* [num_prefix_groups] */
+    void *cascade_workspace;
 } pa_decode_opts;
 
 /*
@@ -190,6 +213,13 @@ pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void
  * shape and num_splits; 0 if the arguments are invalid.  Host only.
  */
 size_t pa_splitkv_workspace_bytes(const pa_shape *shape, int32_t num_splits);
+
+/*
+ * Bytes of device workspace a cascade decode (pa_decode_opts.num_prefix_groups
+ * > 0) needs for this shape, besides the split-KV workspace; 0 if the shape is
+ * invalid.  Host only.
+ */
+size_t pa_cascade_workspace_bytes(const pa_shape *shape);
 
 /*
  * A good num_splits for this shape on a GPU with sm_count SMs: the number of

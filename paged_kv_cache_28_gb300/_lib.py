@@ -21,7 +21,7 @@ PA_DEVERR_FP8_CONFLICT, PA_DEVERR_TIMEOUT = 8, 16
 EXPORTED = ("pa_reshape_and_cache", "pa_decode", "pa_splitkv_workspace_bytes",
             "pa_default_num_splits", "pa_decode_splitkv", "pa_merge_lse", "pa_status_string",
             "pa_read_error_flag", "pa_decode_splitkv_noalloc", "pa_quest_summarize",
-            "pa_quest_select")
+            "pa_quest_select", "pa_cascade_workspace_bytes")
 PA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -34,17 +34,25 @@ class pa_shape(ctypes.Structure):
 
 class pa_decode_opts(ctypes.Structure):
     _fields_ = [("window", ctypes.c_int32), ("topk", ctypes.c_int32),
-                ("shared_prefix_lens", ctypes.c_void_p), ("selected_pages", ctypes.c_void_p)]
+                ("shared_prefix_lens", ctypes.c_void_p), ("selected_pages", ctypes.c_void_p),
+                ("num_prefix_groups", ctypes.c_int32), ("group_offsets", ctypes.c_void_p),
+                ("group_seqs", ctypes.c_void_p), ("group_prefix_len", ctypes.c_void_p),
+                ("cascade_workspace", ctypes.c_void_p)]
 
 
-def _opts(window: int = 0, shared_prefix_lens=None, selected_pages=None):
+def _opts(window: int = 0, shared_prefix_lens=None, selected_pages=None, cascade=None):
     """A pa_decode_opts by reference, or None when every setting is the default.
-    selected_pages: [B, Hkv, topk] int32 tensor (topk taken from its last dim)."""
-    if not window and shared_prefix_lens is None and selected_pages is None:
+    selected_pages: [B, Hkv, topk] int32 tensor (topk taken from its last dim).
+    cascade: (group_offsets, group_seqs, group_prefix_len, cascade_workspace) tensors."""
+    if not window and shared_prefix_lens is None and selected_pages is None and cascade is None:
         return None
     topk = 0 if selected_pages is None else int(selected_pages.shape[-1])
+    groups = (0, None, None, None, None)
+    if cascade is not None:
+        offsets, seqs, plen, ws = cascade
+        groups = (int(offsets.numel()) - 1, _ptr(offsets), _ptr(seqs), _ptr(plen), _ptr(ws))
     return ctypes.byref(pa_decode_opts(int(window), topk, _ptr(shared_prefix_lens),
-                                       _ptr(selected_pages)))
+                                       _ptr(selected_pages), *groups))
 
 
 class PAError(RuntimeError):
@@ -79,6 +87,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "pa_decode_splitkv_noalloc": (I32, [S, P, I32, P, P, P, P, P, P, P, F, P, P]),
             "pa_quest_summarize": (I32, [S, P, P, P, P, P]),
             "pa_quest_select": (I32, [S, P, P, P, P, I32, P, P, P, P]),
+            "pa_cascade_workspace_bytes": (ctypes.c_size_t, [S]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -153,6 +162,10 @@ def pa_splitkv_workspace_bytes(shape: pa_shape, num_splits: int) -> int:
     return int(load().pa_splitkv_workspace_bytes(ctypes.byref(shape), int(num_splits)))
 
 
+def pa_cascade_workspace_bytes(shape: pa_shape) -> int:
+    return int(load().pa_cascade_workspace_bytes(ctypes.byref(shape)))
+
+
 def pa_default_num_splits(shape: pa_shape, sm_count: int) -> int:
     return int(load().pa_default_num_splits(ctypes.byref(shape), int(sm_count)))
 
@@ -160,14 +173,15 @@ def pa_default_num_splits(shape: pa_shape, sm_count: int) -> int:
 def pa_decode_splitkv(shape: pa_shape, out, workspace, num_splits: int, q, k_pool, v_pool,
                       k_scale, v_scale, block_tables, seq_lens, sm_scale: float, err_flag=None,
                       stream=None, shared_prefix_lens=None, window: int = 0,
-                      selected_pages=None) -> None:
+                      selected_pages=None, cascade=None) -> None:
+    """cascade: (group_offsets, group_seqs, group_prefix_len, cascade_workspace)."""
     lib = load()
     nbytes = workspace.numel() * workspace.element_size()
     _check("pa_decode_splitkv", lib.pa_decode_splitkv(
         ctypes.byref(shape), _ptr(out), _ptr(workspace), nbytes, int(num_splits), _ptr(q),
         _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
-        _ptr(seq_lens), _opts(window, shared_prefix_lens, selected_pages), float(sm_scale),
-        _ptr(err_flag), _stream(stream)))
+        _ptr(seq_lens), _opts(window, shared_prefix_lens, selected_pages, cascade),
+        float(sm_scale), _ptr(err_flag), _stream(stream)))
 
 
 def pa_merge_lse(shape: pa_shape, out, workspace, num_splits: int, stream=None) -> None:

@@ -58,6 +58,17 @@ pa_status check_decode_args(const pa_shape *shape, const float *out, const void 
     if ((opts->topk > 0) != (opts->selected_pages != nullptr)) return PA_ERR_INVALID_ARG;
     if (opts->selected_pages && !aligned16(opts->selected_pages)) return PA_ERR_INVALID_ARG;
     if (opts->topk > 0 && opts->window > 0) return PA_ERR_INVALID_ARG;
+    if (opts->num_prefix_groups < 0) return PA_ERR_INVALID_ARG;
+    if (opts->num_prefix_groups > 0) {              // cascade decode
+      auto aligned4 = [](const void *q) { return q && (reinterpret_cast<uintptr_t>(q) & 3u) == 0; };
+      if (!aligned4(opts->group_offsets) || !aligned4(opts->group_seqs) ||
+          !aligned4(opts->group_prefix_len) || !opts->cascade_workspace ||
+          (reinterpret_cast<uintptr_t>(opts->cascade_workspace) & 255u))
+        return PA_ERR_INVALID_ARG;
+      if (opts->window > 0 || opts->topk > 0) return PA_ERR_INVALID_ARG;
+      if (shape->kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
+      if (opts->num_prefix_groups > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
+    }
   }
   return PA_OK;
 }
@@ -99,6 +110,11 @@ pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void
 size_t pa_splitkv_workspace_bytes(const pa_shape *shape, int32_t num_splits) {
   if (check_shape(shape, true) != PA_OK || num_splits < 1 || num_splits > kMaxSplits) return 0;
   return pa::splitkv_layout(*shape, num_splits).total;
+}
+
+size_t pa_cascade_workspace_bytes(const pa_shape *shape) {
+  if (check_shape(shape, true) != PA_OK) return 0;
+  return pa::cascade_layout(shape->B, shape->Hq, shape->D).total;
 }
 
 int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count) {

@@ -24,6 +24,7 @@ constexpr int kPieceStart = 1 << 10;
 constexpr int kPieceEnd = 1 << 11;
 constexpr int kHintShared = 1 << 12;   // tile lies in a prefix other sequences share
 constexpr int kHintPrivate = 1 << 13;  // tile is private (hints given, not shared)
+constexpr int kCascade = 1 << 14;      // the sequence's shared prefix is done by the cascade
 constexpr int kInvalidPhys = -1;
 
 __device__ __forceinline__ void set_err(int32_t *flag, int bits) {
@@ -54,6 +55,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // Bounded wait for the phase with the given parity; false if it never completed.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   for (uint32_t it = 0; it < kWaitSpins; ++it) {
     uint32_t done;

@@ -94,6 +94,8 @@ struct Params {
   int window;                          // > 0: attend over the last `window` positions only
   int topk;                            // > 0: attend over the pages listed in sel only
   const int32_t *sel;                  // [B, Hkv, topk] chosen 16-token pages (ascending)
+  const int32_t *casc_tiles;           // [B] shared tiles done by the cascade kernel, or null
+  uint64_t casc_ws;                    // the cascade workspace address (0: none), for the merge
   int32_t *err;
   int B, Hq, Hkv, G, bs, nblocks, max_blocks;
   float sl2;  // sm_scale * log2(e)
@@ -234,8 +236,10 @@ struct SeqTiles {
   int first_skip;  // tokens before the window in the first tile (0..15)
 };
 
-__device__ __forceinline__ SeqTiles seq_tiles(int L, int window) {
-  const int start = (window > 0 && L > window) ? L - window : 0;
+__device__ __forceinline__ SeqTiles seq_tiles(int L, int window, int cascade_tiles = 0) {
+  int start = (window > 0 && L > window) ? L - window : 0;
+  // tiles of a shared prefix that the cascade kernel attends over are skipped here
+  start = max(start, min(cascade_tiles * kTile, L));
   const int end_tiles = (L + kTile - 1) / kTile;
   SeqTiles t;
   t.first = start / kTile;
@@ -247,10 +251,12 @@ __device__ __forceinline__ SeqTiles seq_tiles(int L, int window) {
 
 constexpr int kLoShift = 16;   // unit info bits 16..19: first valid token of the tile
 
-// Tiles attended per (sequence, KV head): the window's tiles, or the chosen pages.
-__device__ __forceinline__ int pair_tile_count(int L, int window, int topk) {
+// Tiles attended per (sequence, KV head): the window's tiles, the chosen pages, or
+// the tiles after a cascaded shared prefix.
+__device__ __forceinline__ int pair_tile_count(int L, int window, int topk,
+                                               int cascade_tiles = 0) {
   if (topk > 0) return min(topk, (L + kTile - 1) / kTile);
-  return seq_tiles(L, window).count;
+  return seq_tiles(L, window, cascade_tiles).count;
 }
 
 // One 16-token tile: scores, online-softmax update, P V accumulation.
@@ -574,6 +580,22 @@ __device__ __forceinline__ void write_normalised(const State<C> &st, float *dst,
     }
 }
 
+// The cascade partials of sequence b, KV head kvh: lse [pieces][G] and o
+// [pieces][G][D] in the cascade workspace at `cws` (0: none).  Returns the pieces.
+__device__ __forceinline__ int cascade_partials(uint64_t cws, int B, int Hq, int Hkv, int G,
+                                                int D, int b, int kvh, const float *&clse,
+                                                const float *&co) {
+  if (!cws) return 0;
+  const CascadeLayout cl = cascade_layout(B, Hq, D);
+  const uint8_t *cw = reinterpret_cast<const uint8_t *>(cws);
+  const int m = reinterpret_cast<const int32_t *>(cw + cl.member)[b];
+  if (m < 0) return 0;
+  const size_t c0 = (static_cast<size_t>(m) * Hkv + kvh) * kCascadePieces * G;
+  clse = reinterpret_cast<const float *>(cw + cl.lse) + c0;
+  co = reinterpret_cast<const float *>(cw + cl.o) + c0 * D;
+  return reinterpret_cast<const int32_t *>(cw + cl.pieces)[b];
+}
+
 // ----------------------------------------------------------------------------
 // unit sources: which tiles a warp processes, in order
 // ----------------------------------------------------------------------------
@@ -642,6 +664,7 @@ struct SegmentSource {
   const int32_t *block_tables;
   const int32_t *shared_prefix_lens;   // may be null
   const int32_t *sel;                  // [B, Hkv, topk] chosen pages, or null
+  const int32_t *casc_tiles;           // [B] cascaded shared tiles, or null
   int32_t *err;
   int B, Hkv, bs, nblocks, max_blocks, window, topk;
   int begin, end;
@@ -662,7 +685,8 @@ struct SegmentSource {
     const int r = f - start;
     const int kvh = r / nt, j = r - kvh * nt;
     const int L = min(max(__ldg(seq_lens + b), 0), max_blocks * bs);
-    const SeqTiles geo = seq_tiles(L, window);
+    const int ct = casc_tiles ? casc_tiles[b] : 0;
+    const SeqTiles geo = seq_tiles(L, window, ct);
     int tile = geo.first + j, last_tile = geo.first + geo.count - 1;
     bool bad_page = false;
     if (sel) {
@@ -688,6 +712,7 @@ struct SegmentSource {
     if (f == end - 1) info |= kPieceEnd;
     if (shared_prefix_lens)
       info |= ((tile + 1) * kTile <= __ldg(shared_prefix_lens + b)) ? kHintShared : kHintPrivate;
+    if (ct > 0) info |= kCascade;
     return make_int4(phys, b * Hkv + kvh, tile, info);
   }
   __device__ __forceinline__ void init(int lane) {
@@ -988,8 +1013,10 @@ __device__ void scan_lengths(const Params &p, int32_t *prefix) {
     int v = 0;
     if (i < p.B) {
       const int L0 = p.seq_lens[i];
-      if ((L0 < 0 || L0 > cap) && blockIdx.x == 0) set_err(p.err, PA_DEVERR_SEQ_LEN);
-      v = p.Hkv * pair_tile_count(clamp_len(L0, cap), p.window, p.topk);
+      const int ct = p.casc_tiles ? p.casc_tiles[i] : 0;
+      if ((L0 < 0 || L0 > cap || L0 < ct * kTile) && blockIdx.x == 0)
+        set_err(p.err, PA_DEVERR_SEQ_LEN);
+      v = p.Hkv * pair_tile_count(clamp_len(L0, cap), p.window, p.topk, ct);
     }
     int x = v;
 #pragma unroll
@@ -1019,6 +1046,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   pdl_trigger();
   WarpSmem ws = setup_smem<C>(smem_raw, warp, p.G, lane);
   int32_t *prefix = reinterpret_cast<int32_t *>(split_tail<C>(smem_raw));
+  if (p.casc_tiles) pdl_wait();   // the cascaded tiles are written by the cascade kernel
   scan_lengths<C::THREADS>(p, prefix);
   const int seg = blockIdx.x * C::WARPS + warp;
   const int total = prefix[p.B];
@@ -1037,6 +1065,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.window = p.window;
   src.sel = p.sel;
   src.topk = p.topk;
+  src.casc_tiles = p.casc_tiles;
   src.begin = min(seg * W, total);
   src.end = (seg < p.num_splits) ? min(src.begin + W, total) : src.begin;
   // the chosen pages are written by the selection launched just before
@@ -1048,7 +1077,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   pdl_wait();
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i <= p.B; i += C::THREADS) p.prefix_out[i] = prefix[i];
-    if (threadIdx.x == 0) p.prefix_out[p.B + 1] = C::HEADS;   // KV heads per unit, for the merge
+    if (threadIdx.x == 0) {                 // for the merge: KV heads per unit, cascade
+      p.prefix_out[p.B + 1] = C::HEADS;
+      p.prefix_out[p.B + 2] = static_cast<int32_t>(static_cast<uint32_t>(p.casc_ws));
+      p.prefix_out[p.B + 3] = static_cast<int32_t>(static_cast<uint32_t>(p.casc_ws >> 32));
+    }
   }
   State<C> st;
   st.reset();
@@ -1056,9 +1089,16 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       src, ws, st, p, &tmK, &tmV,
       [&](int4 u, bool piece_first, State<C> &s) {
         const int b = u.y / p.Hkv, kvh = u.y - b * p.Hkv;
-        if (piece_first && (u.w & kLastOfPair)) {
-          write_normalised<C>(s, p.out + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D,
-                              nullptr, p.G, lane);
+        if (piece_first && (u.w & kLastOfPair)) {   // the whole unit is in this segment
+          const size_t row = static_cast<size_t>(b) * p.Hq + kvh * p.G;
+          if (u.w & kCascade) {                     // joined with its shared prefix by the merge
+            const CascadeLayout cl = cascade_layout(p.B, p.Hq, C::D);
+            uint8_t *cw = reinterpret_cast<uint8_t *>(p.casc_ws);
+            write_normalised<C>(s, reinterpret_cast<float *>(cw + cl.uo) + row * C::D,
+                                reinterpret_cast<float *>(cw + cl.ulse) + row, p.G, lane);
+          } else {
+            write_normalised<C>(s, p.out + row * C::D, nullptr, p.G, lane);
+          }
         } else {
           const size_t slot = static_cast<size_t>(seg) * 2 + (piece_first ? 1 : 0);
           write_normalised<C>(s, p.o_part + slot * p.G * C::D, p.lse_part + slot * p.G, p.G,
@@ -1089,14 +1129,32 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
   const int W = max(1, (total + num_splits - 1) / num_splits);
   float *o = out + (static_cast<size_t>(b) * Hq + kvh * G) * D;
   const int D4 = D / 4;
-  if (nt == 0) {
+  // a cascaded sequence adds the partials of its shared prefix (cascade workspace);
+  // a unit finished inside one segment was joined with them there
+  const uint64_t cws = (static_cast<uint64_t>(static_cast<uint32_t>(prefix[B + 3])) << 32) |
+                       static_cast<uint32_t>(prefix[B + 2]);
+  const float *clse = nullptr, *co = nullptr;
+  const int cpieces = cascade_partials(cws, B, Hq, Hkv, G, D, b, kvh, clse, co);
+  if (nt == 0 && cpieces == 0) {
     for (int e = threadIdx.x; e < G * D4; e += blockDim.x)
       reinterpret_cast<float4 *>(o)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   const int start = start_b + unit * nt, end = start + nt;
-  const int p0 = start / W, p1 = (end - 1) / W;
-  if (p0 == p1) return;
+  // split pieces p0..p1 (none when the cascade covers the whole sequence)
+  int p0 = nt > 0 ? start / W : 0, p1 = nt > 0 ? (end - 1) / W : -1;
+  const bool inplace = nt > 0 && p0 == p1;         // finished inside one segment
+  if (inplace && cpieces == 0) return;
+  // a cascaded unit finished in place left its (o, lse) in the unit slots
+  const float *ulse = nullptr, *uo = nullptr;
+  if (inplace) {
+    const CascadeLayout cl = cascade_layout(B, Hq, D);
+    const uint8_t *cw = reinterpret_cast<const uint8_t *>(cws);
+    const size_t row = static_cast<size_t>(b) * Hq + kvh * G;
+    ulse = reinterpret_cast<const float *>(cw + cl.ulse) + row;
+    uo = reinterpret_cast<const float *>(cw + cl.uo) + row * D;
+    p1 = p0 - 1;                                   // no split pieces
+  }
   constexpr int U = 8;
   for (int e = threadIdx.x; e < G * D4; e += blockDim.x) {
     const int g = e / D4, d4 = e - g * D4, gu = row0 + g;
@@ -1110,8 +1168,25 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
 #pragma unroll
       for (int u = 0; u < U; ++u) M = fmaxf(M, v[u]);
     }
+    for (int c = 0; c < cpieces; ++c) M = fmaxf(M, clse[c * G + g]);
+    if (ulse) M = fmaxf(M, ulse[g]);
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
+    if (ulse) {
+      const float wgt = expf(ulse[g] - M);
+      const float4 x = reinterpret_cast<const float4 *>(uo + g * D)[d4];
+      num = make_float4(wgt * x.x, wgt * x.y, wgt * x.z, wgt * x.w);
+      den = wgt;
+    }
+    for (int c = 0; c < cpieces; ++c) {            // the cascade's pieces of the prefix
+      const float wgt = expf(clse[c * G + g] - M);
+      const float4 x = reinterpret_cast<const float4 *>(co + (c * G + g) * D)[d4];
+      num.x += wgt * x.x;
+      num.y += wgt * x.y;
+      num.z += wgt * x.z;
+      num.w += wgt * x.w;
+      den += wgt;
+    }
     for (int s0 = p0; s0 <= p1; s0 += U) {
       float l[U];
       float4 x[U];
@@ -1160,7 +1235,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // (bf16 elements, or bytes for the code pools); box = 16 rows x one head row of up to
 // 128 bytes, swizzled by the box width (128 or 64 bytes).
 // s: the decode's view of the shape (Hkv counts units of `heads` adjacent KV heads).
-static bool make_pool_map(CUtensorMap *map, const void *pool, const pa_shape &s, int heads) {
+bool make_pool_map(CUtensorMap *map, const void *pool, const pa_shape &s, int heads) {
   auto fn = encode_fn();
   if (!fn) return false;
   const bool bf16 = s.kv_dtype == PA_KV_BF16;
@@ -1324,14 +1399,15 @@ int splitkv_min_blocks(const pa_shape &shape) {
   return 1;
 }
 
-// prefix int32[B + 2] (tile prefix, then KV heads per unit), lse f32[splits][2][Gu],
+// prefix int32[B + 4] (tile prefix, KV heads per unit, cascade workspace address),
+// lse f32[splits][2][Gu],
 // o_part f32[splits][2][Gu][D]; Gu = query heads of the largest unit the shape allows.
 WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits) {
   WorkspaceLayout w{};
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t G = static_cast<size_t>(s.Hq / s.Hkv) * (int4_pairable(s) ? 2 : 1);
   w.prefix = 0;
-  w.lse = up(w.prefix + (static_cast<size_t>(s.B) + 2) * 4);
+  w.lse = up(w.prefix + (static_cast<size_t>(s.B) + 4) * 4);
   w.o_part = up(w.lse + static_cast<size_t>(num_splits) * 2 * G * 4);
   w.total = up(w.o_part + static_cast<size_t>(num_splits) * 2 * G * s.D * 4);
   return w;
@@ -1348,6 +1424,18 @@ pa_status run_decode(const pa_shape &s, float *out, const void *q, const void *k
     return PA_ERR_CUDA;
   Params p = make_params(v, out, q, k_scale, v_scale, bt, sl, opts, sm_scale, err);
   return dispatch_pair(v, heads, p, mk, mv, stream);
+}
+
+// A non-blocking stream per device for work a call runs beside the caller's stream
+// (created on first use, kept for the life of the process).
+static cudaStream_t side_stream(int dev) {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {};
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+    streams[dev] = nullptr;
+  return streams[dev];
 }
 
 pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int num_splits,
@@ -1368,7 +1456,49 @@ pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int
   p.lse_part = reinterpret_cast<float *>(ws + w.lse);
   p.o_part = reinterpret_cast<float *>(ws + w.o_part);
   p.num_splits = num_splits;
-  return dispatch_segments(v, heads, p, mk, mv, stream);
+  if (!opts || opts->num_prefix_groups <= 0) return dispatch_segments(v, heads, p, mk, mv, stream);
+
+  // Cascade: plan on the caller's stream, then fork.  The cascade kernel (tensor
+  // work on the shared prefixes) runs on a side stream with one CTA per SM, next to
+  // the split kernel (HBM streaming of the rest, two CTAs per SM); a second cascade
+  // launch after the split kernel takes the items still left at full occupancy; the
+  // caller's stream waits for both before anything it runs next (the merge).
+  pa_status st = run_cascade_plan(v, *opts, err, stream);
+  if (st != PA_OK) return st;
+  const CascadeLayout cl = cascade_layout(s.B, s.Hq, s.D);
+  p.casc_tiles =
+      reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(opts->cascade_workspace) + cl.tiles);
+  p.casc_ws = reinterpret_cast<uint64_t>(opts->cascade_workspace);
+  int dev = 0, sms = 0;
+  cudaStream_t side = nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      !(side = side_stream(dev)))
+    return PA_ERR_CUDA;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+    if (fork) cudaEventDestroy(fork);
+    return PA_ERR_CUDA;
+  }
+  // (an event destroyed before the GPU reaches it is released once it completes)
+  struct Events {
+    cudaEvent_t a, b;
+    ~Events() {
+      cudaEventDestroy(a);
+      cudaEventDestroy(b);
+    }
+  } ev{fork, join};
+  if (cudaEventRecord(fork, stream) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
+    return PA_ERR_CUDA;
+  st = run_cascade(v, mk, mv, q, bt, *opts, sm_scale, err, sms, side);
+  if (st != PA_OK) return st;
+  if (cudaEventRecord(join, side) != cudaSuccess) return PA_ERR_CUDA;
+  st = dispatch_segments(v, heads, p, mk, mv, stream);
+  if (st != PA_OK) return st;
+  st = run_cascade(v, mk, mv, q, bt, *opts, sm_scale, err, 3 * sms, stream);
+  if (st != PA_OK) return st;
+  return cudaStreamWaitEvent(stream, join, 0) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int num_splits,

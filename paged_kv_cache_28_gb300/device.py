@@ -10,7 +10,7 @@ import numpy as np
 import torch
 
 from . import _lib
-from .workload import Batch
+from .workload import Batch, cascade_groups
 
 
 def to_device_bf16(bits: np.ndarray, device) -> torch.Tensor:
@@ -54,6 +54,7 @@ class DeviceBatch:
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.workspace = None
         self.num_splits = None
+        self.cascade = None
 
     # -- calls -----------------------------------------------------------------
 
@@ -75,18 +76,30 @@ class DeviceBatch:
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
         self.num_splits = num_splits
 
+    def enable_cascade(self, groups=None):
+        """Prefix-aware decode for decode_splitkv: groups = (group_offsets, group_seqs,
+        group_prefix_len) int32 arrays, by default the batch's own prefix groups."""
+        offsets, seqs, plen = cascade_groups(self.batch) if groups is None else groups
+        ws = torch.empty(_lib.pa_cascade_workspace_bytes(self.shape), dtype=torch.uint8,
+                         device=self.device)
+        self.cascade = tuple(torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(
+            self.device) for a in (offsets, seqs, plen)) + (ws,)
+
     def decode_splitkv(self, num_splits: int | None = None, stream=None, hints: bool = True,
-                       window: int = 0, selected_pages=None):
-        """Split-KV decode + merge; hints: pass the batch's shared-prefix lengths (if any)."""
+                       window: int = 0, selected_pages=None, cascade: bool = False):
+        """Split-KV decode + merge; hints: pass the batch's shared-prefix lengths (if any);
+        cascade: attend over the prefix groups (enable_cascade) once per group."""
         if num_splits is None:
             num_splits = default_num_splits(self.shape, self.device)
         if self.workspace is None or self.num_splits != num_splits:
             self.ensure_workspace(num_splits)
+        if cascade and self.cascade is None:
+            self.enable_cascade()
         _lib.pa_decode_splitkv(self.shape, self.out, self.workspace, num_splits, self.q,
                                self.k_pool, self.v_pool, self.k_scale, self.v_scale,
                                self.block_tables, self.seq_lens, self.batch.sm_scale, self.err,
                                stream, self.shared_prefix_lens if hints else None, window,
-                               selected_pages)
+                               selected_pages, self.cascade if cascade else None)
         _lib.pa_merge_lse(self.shape, self.out, self.workspace, num_splits, stream)
 
     # -- Quest page selection ------------------------------------------------------

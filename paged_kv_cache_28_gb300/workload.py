@@ -87,6 +87,7 @@ class Batch:
     sm_scale: float
     seed: int
     shared_prefix_lens: np.ndarray | None = None   # int32 [B]: tokens in blocks shared with others
+    prefix_groups: tuple = ()          # ((prefix tokens, [member sequences]), ...) as built
 
     @property
     def quantized(self) -> bool:
@@ -289,7 +290,21 @@ def build_batch(name: str, seq_lens, *, Hq: int, Hkv: int, D: int, block_size: i
                  max_blocks=max_blocks, kv_dtype=kv_dtype, seq_lens=seq_lens,
                  block_tables=tables, slot_mapping=slot, q=q, k_new=k_new, v_new=v_new,
                  k_pool=k_pool, v_pool=v_pool, k_scale=k_scale, v_scale=v_scale,
-                 sm_scale=float(sm_scale), seed=seed, shared_prefix_lens=shared)
+                 sm_scale=float(sm_scale), seed=seed, shared_prefix_lens=shared,
+                 prefix_groups=tuple((int(plen), list(seqs)) for plen, seqs in prefix_groups))
+
+
+def cascade_groups(batch: Batch):
+    """The batch's prefix groups as cascade arrays: (group_offsets, group_seqs,
+    group_prefix_len) int32, each group's shared length cut down to whole 16-token
+    tiles (the copied tail block holds the same values, so it counts as shared)."""
+    offsets, seqs, plen = [0], [], []
+    for tokens, members in batch.prefix_groups:
+        seqs.extend(members)
+        offsets.append(len(seqs))
+        plen.append((tokens // 16) * 16)
+    return (np.asarray(offsets, np.int32), np.asarray(seqs, np.int32),
+            np.asarray(plen, np.int32))
 
 
 def lognormal_lens(rng, n: int, median: float, lo: int, hi: int) -> np.ndarray:
@@ -302,7 +317,7 @@ def lognormal_lens(rng, n: int, median: float, lo: int, hi: int) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 CONFIGS = ("tiny", "llama70b_layer", "prefix_sharing", "long_context", "fp8_mixed",
-           "int4_mixed")
+           "int4_mixed", "code_assistant_turns")
 
 
 def config_seq_lens(name: str, seed: int):
@@ -323,6 +338,15 @@ def config_seq_lens(name: str, seed: int):
     if name == "long_context":
         return (np.full(8, 131072, np.int32), (),
                 dict(Hq=64, Hkv=8, D=128, block_size=32, max_blocks=4096))
+    if name == "code_assistant_turns":
+        # 32 repositories, 8 turns each: a turn shares its repository's files (a
+        # LogNormal(8000) prefix) with the other turns and adds its own conversation
+        # (LogNormal(1500)); the shared KV (~1.4 GB) is far larger than L2
+        plen = lognormal_lens(rng, 32, 8000, 2048, 24576)
+        sfx = lognormal_lens(rng, 256, 1500, 1, 32768 - 24576)
+        lens = np.array([plen[i // 8] + sfx[i] for i in range(256)], np.int32)
+        groups = tuple((int(plen[g]), list(range(8 * g, 8 * g + 8))) for g in range(32))
+        return lens, groups, dict(Hq=64, Hkv=8, D=128, block_size=16, max_blocks=2048)
     if name in ("fp8_mixed", "int4_mixed"):
         return (rng.integers(1, 4097, 512).astype(np.int32), (),
                 dict(Hq=64, Hkv=8, D=128, block_size=16, max_blocks=256,
@@ -331,7 +355,7 @@ def config_seq_lens(name: str, seed: int):
 
 
 DEFAULT_SEEDS = {"tiny": 0, "llama70b_layer": 1, "prefix_sharing": 2, "long_context": 3,
-                 "fp8_mixed": 4, "int4_mixed": 5}
+                 "fp8_mixed": 4, "int4_mixed": 5, "code_assistant_turns": 6}
 
 
 def make(name: str, seed: int | None = None, with_pools: bool = True) -> Batch:

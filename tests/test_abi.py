@@ -144,6 +144,33 @@ def test_reshape_rejects_bad_args(lib):
                                     None) == _lib.PA_ERR_INVALID_ARG
 
 
+def test_cascade_host_checks(lib):
+    import ctypes
+    s = shape(B=8, Hq=64, Hkv=8, D=128, max_blocks=64, nblocks=512)
+    ws = _lib.pa_splitkv_workspace_bytes(s, 16)
+    cb = _lib.pa_cascade_workspace_bytes(s)
+    assert cb >= 8 * 64 * 4 * 129 * 4 and _lib.pa_cascade_workspace_bytes(shape(Hq=7)) == 0
+
+    def call(sh, opts):
+        return lib.pa_decode_splitkv(ctypes.byref(sh), FAKE, FAKE, ws, 16, FAKE, FAKE, FAKE,
+                                     None, None, FAKE, FAKE, ctypes.byref(opts), 0.1, None, None)
+
+    def opts(n=1, offs=FAKE, seqs=FAKE, plen=FAKE, cws=FAKE, window=0):
+        return _lib.pa_decode_opts(window, 0, None, None, n, offs, seqs, plen, cws)
+
+    assert call(s, opts(n=-1)) == _lib.PA_ERR_INVALID_ARG
+    assert call(s, opts(seqs=None)) == _lib.PA_ERR_INVALID_ARG          # no member list
+    assert call(s, opts(cws=None)) == _lib.PA_ERR_INVALID_ARG           # no workspace
+    assert call(s, opts(cws=FAKE + 16)) == _lib.PA_ERR_INVALID_ARG      # not 256-aligned
+    assert call(s, opts(offs=FAKE + 2)) == _lib.PA_ERR_INVALID_ARG      # misaligned int32
+    assert call(s, opts(window=64)) == _lib.PA_ERR_INVALID_ARG          # not with a window
+    fp8 = shape(B=8, Hq=64, Hkv=8, D=128, max_blocks=64, nblocks=512,
+                kv_dtype=_lib.PA_KV_FP8_E4M3)
+    assert lib.pa_decode_splitkv(ctypes.byref(fp8), FAKE, FAKE, ws, 16, FAKE, FAKE, FAKE, FAKE,
+                                 FAKE, FAKE, FAKE, ctypes.byref(opts()), 0.1, None,
+                                 None) == _lib.PA_ERR_UNSUPPORTED        # bf16 pools only
+
+
 def test_quest_host_checks(lib):
     import ctypes
     s = ctypes.byref(shape())

@@ -710,8 +710,92 @@ def _sample_rows(batch, rng, n_random=192):
     return np.array(rows, dtype=np.int32)
 
 
+# ---------------------------------------------------------------- cascade (shared prefixes)
+
+def _cascade_batch(Hq, Hkv, D, bs, groups, free_lens, seed, plens=None):
+    """groups: [(prefix tokens, [suffix lengths])]; members follow each other, then the
+    ungrouped sequences.  plens: the cascade lengths (default: prefix cut to tiles)."""
+    lens, pgroups, b = [], [], 0
+    for plen, suffixes in groups:
+        members = list(range(b, b + len(suffixes)))
+        lens += [plen + sfx for sfx in suffixes]
+        pgroups.append((plen, members))
+        b += len(suffixes)
+    lens += list(free_lens)
+    batch = wl.build_batch("t", lens, Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seed=seed,
+                           prefix_groups=pgroups)
+    offsets, seqs, plen = wl.cascade_groups(batch)
+    if plens is not None:
+        plen = np.asarray(plens, np.int32)
+    return batch, (offsets, seqs, plen)
+
+
+def _run_cascade(dev, num_splits):
+    dev.out.fill_(float("nan"))
+    dev.decode_splitkv(num_splits, cascade=True)
+    torch.cuda.synchronize()
+    return dev.out.cpu().numpy()
+
+
+CASCADE_CASES = [
+    # Hq, Hkv, D, bs, groups [(prefix, suffixes)], ungrouped lengths
+    (64, 8, 128, 16, [(900, [1, 5, 17, 300, 2, 64, 40, 1000]), (300, [3, 30])], [7, 500, 1]),
+    (64, 8, 128, 16, [(2000, [1, 2, 3])], [100]),                    # four pieces per member
+    (16, 4, 64, 32, [(97, [1, 31, 32, 200]), (64, [50])], [1, 70]),  # G = 4, bs = 32
+    (32, 2, 128, 16, [(500, [9, 90, 900]), (16, [1, 2])], [33]),     # G = 16 (two n-tiles)
+    (8, 8, 128, 16, [(160, [5, 6, 7, 8, 9])], []),                   # G = 1
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs,groups,free", CASCADE_CASES)
+def test_cascade_matches_oracle(Hq, Hkv, D, bs, groups, free):
+    """Shared prefixes attended once per group (stacked queries), the rest per
+    sequence, joined by the merge: equal to the plain decode of the oracle."""
+    batch, cg = _cascade_batch(Hq, Hkv, D, bs, groups, free, seed=Hq + D + bs)
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    dev.enable_cascade(cg)
+    ref, _ = oracle_after_write(batch)
+    for ns in (1, 3, 17, 64, 500, default_num_splits(dev.shape)):
+        assert_close(_run_cascade(dev, ns), ref, batch, f"cascade num_splits={ns}")
+    assert dev.read_err() == 0
+
+
+def test_cascade_prefix_is_whole_sequence():
+    """Members whose every token is in the shared prefix (nothing left for the split
+    kernel) and groups with a zero-length prefix."""
+    batch, cg = _cascade_batch(64, 8, 128, 16, [(320, [0, 0, 16, 1]), (48, [2, 3])], [5],
+                               seed=101)
+    dev = DeviceBatch(batch)
+    ref, _ = oracle_after_write(batch, write=False)
+    offsets, seqs, plen = cg
+    plen2 = plen.copy()
+    plen2[1] = 0                                    # the second group shares nothing
+    for groups in ((offsets, seqs, plen), (offsets, seqs, plen2)):
+        dev.enable_cascade(groups)
+        for ns in (1, 5, 77):
+            assert_close(_run_cascade(dev, ns), ref, batch, f"cascade whole prefix {ns}")
+    assert dev.read_err() == 0
+
+
+def test_cascade_bad_groups_set_error_flag():
+    """A member shorter than its group's prefix, or a sequence in two groups, is a
+    caller error: the device flag reports it, nothing faults."""
+    batch, (offsets, seqs, plen) = _cascade_batch(64, 8, 128, 16, [(64, [5, 6])], [9], seed=102)
+    dev = DeviceBatch(batch)
+    dev.enable_cascade((offsets, seqs, np.array([96], np.int32)))       # 96 > 64 + 5
+    _run_cascade(dev, 7)
+    assert dev.read_err() & _lib.PA_DEVERR_SEQ_LEN
+    dev.err.zero_()
+    two = (np.array([0, 2, 3], np.int32), np.array([0, 1, 0], np.int32),
+           np.array([64, 64], np.int32))                               # sequence 0 twice
+    dev.enable_cascade(two)
+    _run_cascade(dev, 7)
+    assert dev.read_err() & _lib.PA_DEVERR_SEQ_LEN
+
+
 @pytest.mark.parametrize("name", ["llama70b_layer", "prefix_sharing", "long_context", "fp8_mixed",
-                                  "int4_mixed"])
+                                  "int4_mixed", "code_assistant_turns"])
 def test_full_size_config_sampled(name):
     """The bench's launch configuration (split-KV, default num_splits) at full size;
     every head of the longest, shortest and three random sequences plus 192
@@ -727,3 +811,7 @@ def test_full_size_config_sampled(name):
     if name in ("fp8_mixed", "int4_mixed"):      # unsplit kernel too, on the same rows
         out2 = run_gpu(dev, "decode")
         assert_close(out2[rows[:, 0], rows[:, 1]], ref, batch, name + " decode")
+    if name in ("prefix_sharing", "code_assistant_turns"):   # the cascade (bench.py --cascade)
+        out3 = _run_cascade(dev, default_num_splits(dev.shape))
+        assert dev.read_err() == 0
+        assert_close(out3[rows[:, 0], rows[:, 1]], ref, batch, name + " cascade")
