@@ -38,7 +38,11 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic per decode launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum), with
 # the hash of the kernel sources it was measured on; reported only while they still match.
 TRAFFIC = {
-    "int4_mixed": {"bytes": 1_122_790_144 + 16_972_160, "kernel_hash": "1039cbd6dd7087aa"},
+    "llama70b_layer": {"bytes": 1_338_685_696 + 2_230_272, "kernel_hash": "1f6db4850c8ef2f3"},
+    "prefix_sharing": {"bytes": 2_545_070_848 + 2_917_120, "kernel_hash": "1f6db4850c8ef2f3"},
+    "long_context": {"bytes": 4_296_158_208 + 1_512_192, "kernel_hash": "1f6db4850c8ef2f3"},
+    "fp8_mixed": {"bytes": 2_260_587_008 + 22_075_136, "kernel_hash": "1f6db4850c8ef2f3"},
+    "int4_mixed": {"bytes": 1_124_507_648 + 20_538_112, "kernel_hash": "1f6db4850c8ef2f3"},
 }
 
 
@@ -347,7 +351,8 @@ def run_ours(args):
     unique_tokens = step_kv_tokens(batch, args, selected)
     peak, peak_kind = measured_peak_hbm()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
-    tr = TRAFFIC.get(args.config) if args.window == 0 and args.quest_topk == 0 else None
+    tr = (TRAFFIC.get(args.config)
+          if args.window == 0 and args.quest_topk == 0 and not args.cascade else None)
     traffic = tr["bytes"] if tr and tr.get("kernel_hash") == kernel_source_hash() else None
     result = {
         "metric": METRIC,
