@@ -794,6 +794,48 @@ def test_cascade_bad_groups_set_error_flag():
     assert dev.read_err() & _lib.PA_DEVERR_SEQ_LEN
 
 
+@pytest.mark.parametrize("mode", ["split", "cascade", "fp8"])
+def test_step_captured_in_cuda_graph(mode):
+    """One decode step (cache write, split decode, merge; with the cascade also its plan,
+    side-stream fork and join) captured into a CUDA graph and replayed: the replay
+    gives the oracle's result.  The step's launches chain by programmatic dependent
+    launch, which the graph keeps."""
+    if mode == "fp8":
+        batch = wl.build_batch("t", [1, 40, 300, 17], Hq=64, Hkv=8, D=128, block_size=16,
+                               seed=111, kv_dtype="fp8_e4m3")
+        cg = None
+    else:
+        batch, cg = _cascade_batch(64, 8, 128, 16, [(400, [3, 50, 7]), (96, [1, 2])], [33, 5],
+                                   seed=110)
+    dev = DeviceBatch(batch)
+    ns = 37
+    dev.ensure_workspace(ns)
+    if mode == "cascade":
+        dev.enable_cascade(cg)
+
+    def step():
+        dev.reshape_and_cache()
+        dev.decode_splitkv(ns, cascade=(mode == "cascade"))
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):                  # warm-up outside the capture
+        for _ in range(3):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    ref, _ = oracle_after_write(batch)
+    for _ in range(2):
+        dev.out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_close(dev.out.cpu().numpy(), ref, batch, f"graph replay {mode}")
+    assert dev.read_err() == 0
+
+
 @pytest.mark.parametrize("name", ["llama70b_layer", "prefix_sharing", "long_context", "fp8_mixed",
                                   "int4_mixed", "code_assistant_turns"])
 def test_full_size_config_sampled(name):
