@@ -252,25 +252,26 @@ def run_ours(args):
         dev.quest_build_summaries(stream)      # token's page, select, sparse decode
         dev.quest_buffers(args.quest_topk)
 
-    def step(i=None):
-        dev.reshape_and_cache(stream)
+    def step(i=None, st=None):
+        st = stream if st is None else st
+        dev.reshape_and_cache(st)
         if quest:
             _lib.pa_quest_summarize(dev.shape, dev.k_pool, dev.key_summaries, dev.slot_mapping,
-                                    dev.err, stream)
+                                    dev.err, st)
             _lib.pa_quest_select(dev.shape, dev.q, dev.key_summaries, dev.block_tables,
                                  dev.seq_lens, args.quest_topk, dev.page_scores,
-                                 dev.selected_pages, dev.err, stream)
+                                 dev.selected_pages, dev.err, st)
         if i is not None:
-            ev[i][0].record(stream)
+            ev[i][0].record(st)
         _lib.pa_decode_splitkv(dev.shape, dev.out, dev.workspace, ns, dev.q, dev.k_pool,
                                dev.v_pool, dev.k_scale, dev.v_scale, dev.block_tables,
-                               dev.seq_lens, batch.sm_scale, dev.err, stream,
+                               dev.seq_lens, batch.sm_scale, dev.err, st,
                                dev.shared_prefix_lens, args.window,
                                dev.selected_pages if quest else None,
                                dev.cascade if args.cascade else None)
         if i is not None:
-            ev[i][1].record(stream)
-        _lib.pa_merge_lse(dev.shape, dev.out, dev.workspace, ns, stream)
+            ev[i][1].record(st)
+        _lib.pa_merge_lse(dev.shape, dev.out, dev.workspace, ns, st)
 
     for _ in range(args.warmup):
         step()
@@ -322,18 +323,64 @@ def run_ours(args):
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        host = {name: getattr(dev, name).cpu().pin_memory()
-                for name in ("q", "k_new", "v_new", "slot_mapping", "seq_lens", "block_tables")}
+        # the step's inputs packed into one pinned host buffer and one device buffer (each
+        # input 256-byte aligned); the device batch's inputs become views of the latter,
+        # so one copy in and one copy out carry the whole step
+        inputs = {name: getattr(dev, name) for name in
+                  ("q", "k_new", "v_new", "slot_mapping", "seq_lens", "block_tables")}
+        if dev.shared_prefix_lens is not None:
+            inputs["shared_prefix_lens"] = dev.shared_prefix_lens
+        if args.cascade:                          # the prefix groups (not the workspace)
+            for k, t in zip(("group_offsets", "group_seqs", "group_prefix_len"), dev.cascade):
+                inputs[k] = t
+        parts, off = {}, 0
+        for name, t in inputs.items():
+            n = t.numel() * t.element_size()
+            parts[name] = (off, n, t.dtype, t.shape)
+            off = (off + n + 255) // 256 * 256
+        host_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+        dev_in = torch.empty(off, dtype=torch.uint8, device=dev_id)
+        views = {}
+        for name, (o, n, dt, shp) in parts.items():
+            host_in[o:o + n].view(dt).copy_(inputs[name].reshape(-1).cpu())
+            views[name] = dev_in[o:o + n].view(dt).view(shp)
+        for name in ("q", "k_new", "v_new", "slot_mapping", "seq_lens", "block_tables",
+                     "shared_prefix_lens"):
+            if name in views:
+                setattr(dev, name, views[name])
+        if args.cascade:
+            dev.cascade = (views["group_offsets"], views["group_seqs"],
+                           views["group_prefix_len"], dev.cascade[3])
         out_host = torch.empty(dev.out.shape, dtype=dev.out.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        h2d = sum(n for _, n, _, _ in parts.values())
         d2h = out_host.numel() * out_host.element_size()
 
-        def e2e_step():
-            for name, t in host.items():
-                getattr(dev, name).copy_(t, non_blocking=True)
-            step()
+        def e2e_body(st):
+            dev_in.copy_(host_in, non_blocking=True)
+            step(st=st)
             out_host.copy_(dev.out, non_blocking=True)
-            stream.synchronize()
+
+        if args.e2e_eager:
+            def e2e_step():
+                e2e_body(stream)
+                stream.synchronize()
+        else:
+            # the whole step -- input copies from pinned host memory, the launch chain,
+            # the read-back -- captured once into a CUDA graph and replayed per step
+            side = torch.cuda.Stream(dev_id)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    e2e_body(side)
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                e2e_body(torch.cuda.current_stream(dev_id))
+
+            def e2e_step():
+                graph.replay()
+                torch.cuda.current_stream(dev_id).synchronize()
 
         for _ in range(max(3, args.warmup)):
             e2e_step()
@@ -344,7 +391,8 @@ def run_ours(args):
             e2e_step()
         e2e_s = reduce_max((time.perf_counter() - t0) / n_e2e, world, dev_id)
         e2e = {"value": world * batch.B / e2e_s, "unit": "tokens/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "cuda_graph": not args.e2e_eager}
     if dev.read_err():
         raise RuntimeError("device error flag set during the timed steps")
 
@@ -506,6 +554,8 @@ def main(argv=None):
                     choices=["tiny", "llama70b_layer", "prefix_sharing", "long_context",
                              "fp8_mixed", "int4_mixed", "code_assistant_turns"])
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--e2e-eager", action="store_true",
+                    help="e2e leg: launch each call eagerly instead of replaying a CUDA graph")
     ap.add_argument("--cascade", action="store_true",
                     help="prefix-aware decode: each prefix group's shared tokens attended once")
     ap.add_argument("--quest-topk", type=int, default=0,
