@@ -794,6 +794,41 @@ def test_cascade_bad_groups_set_error_flag():
     assert dev.read_err() & _lib.PA_DEVERR_SEQ_LEN
 
 
+def test_largest_split_batch_and_split_count():
+    """16,384 sequences (the split kernel's largest batch: its length scan sits in shared
+    memory) of 1..48 tokens, then 65,536 splits (the largest count) on a small batch."""
+    rng = np.random.default_rng(120)
+    lens = rng.integers(1, 49, 16384)
+    batch = wl.build_batch("t", lens, Hq=16, Hkv=2, D=64, block_size=16, seed=120)
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    out = run_gpu(dev, "split", default_num_splits(dev.shape))
+    assert dev.read_err() == 0
+    rows = np.stack([rng.integers(0, batch.B, 512), rng.integers(0, batch.Hq, 512)], 1)
+    rows = np.concatenate([rows, [[0, 0], [batch.B - 1, batch.Hq - 1]]]).astype(np.int32)
+    ref, _ = oracle_after_write(batch, rows=rows)
+    assert_close(out[rows[:, 0], rows[:, 1]], ref, batch, "B = 16384")
+    small = wl.build_batch("t", [1, 700, 33], Hq=64, Hkv=8, D=128, block_size=16, seed=121)
+    dev = DeviceBatch(small)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(small)
+    assert_close(run_gpu(dev, "split", 65536), ref, small, "65536 splits")
+    assert dev.read_err() == 0
+
+
+def test_cascade_many_small_groups():
+    """500 groups of two sequences each (the cascade's group scan spans many groups)."""
+    groups = [(16 * (1 + g % 9), [1 + g % 5, 2]) for g in range(500)]
+    batch, cg = _cascade_batch(32, 4, 128, 16, groups, [3, 100], seed=122)
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    dev.enable_cascade(cg)
+    ref, _ = oracle_after_write(batch)
+    for ns in (7, default_num_splits(dev.shape)):
+        assert_close(_run_cascade(dev, ns), ref, batch, f"500 groups num_splits={ns}")
+    assert dev.read_err() == 0
+
+
 @pytest.mark.parametrize("mode", ["split", "cascade", "fp8"])
 def test_step_captured_in_cuda_graph(mode):
     """One decode step (cache write, split decode, merge; with the cascade also its plan,
