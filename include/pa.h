@@ -141,6 +141,13 @@ typedef struct {
  *     bytes, 256-byte aligned, used by pa_decode_splitkv and read by the
  *     following pa_merge_lse.  bf16 pools only; not combined with window or
  *     topk.  The result equals the plain decode's up to rounding order.
+ *   workspace, workspace_bytes, num_splits: pa_decode only.  With a workspace
+ *     (device memory of at least pa_splitkv_workspace_bytes(shape, n) bytes,
+ *     256-byte aligned; n = num_splits, or pa_default_num_splits for this GPU
+ *     when num_splits is 0) pa_decode runs the split decode and the merge
+ *     itself: one call, load-balanced however the lengths are spread.  Without
+ *     one it uses one CTA per (sequence, KV head), which needs no memory but is
+ *     held back by the longest sequence.
  */
 typedef struct {
     int32_t window;
@@ -152,6 +159,9 @@ typedef struct {
     const int32_t *group_seqs;          /* [group_offsets[num_prefix_groups]] */
     const int32_t *group_prefix_len;    /* [num_prefix_groups] */
     void *cascade_workspace;
+    void *workspace;                    /* pa_decode: split workspace, or NULL */
+    size_t workspace_bytes;
+    int32_t num_splits;                 /* pa_decode with a workspace; 0: default */
 } pa_decode_opts;
 
 /*
@@ -192,8 +202,9 @@ pa_status pa_reshape_and_cache(const pa_shape *shape, const void *k_new, const v
  */
 
 /*
- * pa_decode -- single-token decode attention over the paged cache, one CTA per
- * (sequence, KV head) serving the whole query group.
+ * pa_decode -- single-token decode attention over the paged cache: one CTA per
+ * (sequence, KV head) serving the whole query group, or, with a workspace in
+ * opts, the split decode and the merge in one call.
  * [P4] "Custom PagedAttention Kernels" (grid over sequence and head, block-table
  * walk, block staged in shared memory); [P3] section 1 (GQA grouping).
  *     out[b][h][:] = sum_t softmax_t(sm_scale * <q[b][h], K_b[t]>) V_b[t]

@@ -37,22 +37,28 @@ class pa_decode_opts(ctypes.Structure):
                 ("shared_prefix_lens", ctypes.c_void_p), ("selected_pages", ctypes.c_void_p),
                 ("num_prefix_groups", ctypes.c_int32), ("group_offsets", ctypes.c_void_p),
                 ("group_seqs", ctypes.c_void_p), ("group_prefix_len", ctypes.c_void_p),
-                ("cascade_workspace", ctypes.c_void_p)]
+                ("cascade_workspace", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("num_splits", ctypes.c_int32)]
 
 
-def _opts(window: int = 0, shared_prefix_lens=None, selected_pages=None, cascade=None):
+def _opts(window: int = 0, shared_prefix_lens=None, selected_pages=None, cascade=None,
+          workspace=None, num_splits: int = 0):
     """A pa_decode_opts by reference, or None when every setting is the default.
     selected_pages: [B, Hkv, topk] int32 tensor (topk taken from its last dim).
-    cascade: (group_offsets, group_seqs, group_prefix_len, cascade_workspace) tensors."""
-    if not window and shared_prefix_lens is None and selected_pages is None and cascade is None:
+    cascade: (group_offsets, group_seqs, group_prefix_len, cascade_workspace) tensors.
+    workspace: pa_decode's split workspace (uint8 tensor), num_splits (0: default)."""
+    if (not window and shared_prefix_lens is None and selected_pages is None and cascade is None
+            and workspace is None):
         return None
     topk = 0 if selected_pages is None else int(selected_pages.shape[-1])
     groups = (0, None, None, None, None)
     if cascade is not None:
         offsets, seqs, plen, ws = cascade
         groups = (int(offsets.numel()) - 1, _ptr(offsets), _ptr(seqs), _ptr(plen), _ptr(ws))
+    ws = (None, 0) if workspace is None else (_ptr(workspace),
+                                              workspace.numel() * workspace.element_size())
     return ctypes.byref(pa_decode_opts(int(window), topk, _ptr(shared_prefix_lens),
-                                       _ptr(selected_pages), *groups))
+                                       _ptr(selected_pages), *groups, *ws, int(num_splits)))
 
 
 class PAError(RuntimeError):
@@ -149,13 +155,15 @@ def pa_reshape_and_cache(shape: pa_shape, k_new, v_new, k_pool, v_pool, k_scale,
 
 def pa_decode(shape: pa_shape, out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
               seq_lens, sm_scale: float, err_flag=None, stream=None, window: int = 0,
-              selected_pages=None) -> None:
+              selected_pages=None, workspace=None, num_splits: int = 0,
+              shared_prefix_lens=None, cascade=None) -> None:
+    """workspace (uint8 device tensor): run the split decode and the merge in this call."""
     lib = load()
     _check("pa_decode", lib.pa_decode(
         ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
         _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens),
-        _opts(window, selected_pages=selected_pages), float(sm_scale), _ptr(err_flag),
-        _stream(stream)))
+        _opts(window, shared_prefix_lens, selected_pages, cascade, workspace, num_splits),
+        float(sm_scale), _ptr(err_flag), _stream(stream)))
 
 
 def pa_splitkv_workspace_bytes(shape: pa_shape, num_splits: int) -> int:

@@ -103,8 +103,28 @@ pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void
   pa_status st = check_decode_args(shape, out, q, k_pool, v_pool, k_scale, v_scale,
                                    block_tables, seq_lens, opts);
   if (st != PA_OK) return st;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (opts && opts->workspace) {                   // split decode + merge in one call
+    int ns = opts->num_splits;
+    if (ns <= 0) {
+      int dev = 0, sms = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+      ns = pa_default_num_splits(shape, sms);
+    }
+    if (ns > kMaxSplits) return PA_ERR_INVALID_ARG;
+    if (shape->B > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(opts->workspace) & 255u) ||
+        opts->workspace_bytes < pa::splitkv_layout(*shape, ns).total)
+      return PA_ERR_INVALID_ARG;
+    st = pa::run_decode_splitkv(*shape, out, opts->workspace, ns, q, k_pool, v_pool, k_scale,
+                                v_scale, block_tables, seq_lens, opts, sm_scale, err_flag, cs);
+    if (st != PA_OK) return st;
+    return pa::run_merge(*shape, out, opts->workspace, ns, cs);
+  }
   return pa::run_decode(*shape, out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
-                        opts, sm_scale, err_flag, reinterpret_cast<cudaStream_t>(stream));
+                        opts, sm_scale, err_flag, cs);
 }
 
 size_t pa_splitkv_workspace_bytes(const pa_shape *shape, int32_t num_splits) {

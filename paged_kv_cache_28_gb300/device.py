@@ -63,10 +63,17 @@ class DeviceBatch:
                                   self.k_scale, self.v_scale, self.slot_mapping, self.err,
                                   stream)
 
-    def decode(self, stream=None, window: int = 0, selected_pages=None):
+    def decode(self, stream=None, window: int = 0, selected_pages=None,
+               workspace: bool = False):
+        """pa_decode; workspace: hand it a split workspace (the default split count), so
+        that it runs the split decode and the merge itself."""
+        ws = None
+        if workspace:
+            self.ensure_workspace(default_num_splits(self.shape, self.device))
+            ws = self.workspace
         _lib.pa_decode(self.shape, self.out, self.q, self.k_pool, self.v_pool, self.k_scale,
                        self.v_scale, self.block_tables, self.seq_lens, self.batch.sm_scale,
-                       self.err, stream, window, selected_pages)
+                       self.err, stream, window, selected_pages, ws)
 
     def ensure_workspace(self, num_splits: int):
         nbytes = _lib.pa_splitkv_workspace_bytes(self.shape, num_splits)

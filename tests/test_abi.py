@@ -144,6 +144,21 @@ def test_reshape_rejects_bad_args(lib):
                                     None) == _lib.PA_ERR_INVALID_ARG
 
 
+def test_decode_workspace_host_checks(lib):
+    import ctypes
+    s = shape(B=8, Hq=64, Hkv=8, D=128, max_blocks=64, nblocks=512)
+    need = _lib.pa_splitkv_workspace_bytes(s, 16)
+
+    def call(ws, nbytes, ns):
+        o = _lib.pa_decode_opts(0, 0, None, None, 0, None, None, None, None, ws, nbytes, ns)
+        return lib.pa_decode(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE,
+                             ctypes.byref(o), 0.1, None, None)
+
+    assert call(FAKE, need - 1, 16) == _lib.PA_ERR_INVALID_ARG         # too small
+    assert call(FAKE + 16, need, 16) == _lib.PA_ERR_INVALID_ARG        # not 256-aligned
+    assert call(FAKE, need, 70000) == _lib.PA_ERR_INVALID_ARG          # too many splits
+
+
 def test_cascade_host_checks(lib):
     import ctypes
     s = shape(B=8, Hq=64, Hkv=8, D=128, max_blocks=64, nblocks=512)

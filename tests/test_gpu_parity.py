@@ -68,14 +68,16 @@ def run_gpu(dev, mode, num_splits=None, window=0):
     dev.out.fill_(float("nan"))
     if mode == "decode":
         dev.decode(window=window)
+    elif mode == "decode_ws":                    # pa_decode given a workspace: split + merge
+        dev.decode(window=window, workspace=True)
     else:
         dev.decode_splitkv(num_splits, window=window)
     torch.cuda.synchronize()
     return dev.out.cpu().numpy()
 
 
-MODES = [("decode", None), ("split", 1), ("split", 3), ("split", 7), ("split", 64),
-         ("split", 1000), ("split", "default")]
+MODES = [("decode", None), ("decode_ws", None), ("split", 1), ("split", 3), ("split", 7),
+         ("split", 64), ("split", 1000), ("split", "default")]
 
 
 def _modes_run(dev, batch, ref, label):
@@ -885,6 +887,9 @@ def test_full_size_config_sampled(name):
     rows = _sample_rows(batch, np.random.default_rng(7))
     ref, _ = oracle_after_write(batch, rows=rows)
     assert_close(out[rows[:, 0], rows[:, 1]], ref, batch, name)
+    out_ws = run_gpu(dev, "decode_ws")            # the one-call form of the same path
+    assert dev.read_err() == 0
+    assert_close(out_ws[rows[:, 0], rows[:, 1]], ref, batch, name + " pa_decode + workspace")
     if name in ("fp8_mixed", "int4_mixed"):      # unsplit kernel too, on the same rows
         out2 = run_gpu(dev, "decode")
         assert_close(out2[rows[:, 0], rows[:, 1]], ref, batch, name + " decode")
