@@ -38,11 +38,11 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic per decode launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum), with
 # the hash of the kernel sources it was measured on; reported only while they still match.
 TRAFFIC = {
-    "llama70b_layer": {"bytes": 1_338_685_696 + 2_230_272, "kernel_hash": "1f6db4850c8ef2f3"},
-    "prefix_sharing": {"bytes": 2_545_070_848 + 2_917_120, "kernel_hash": "1f6db4850c8ef2f3"},
-    "long_context": {"bytes": 4_296_158_208 + 1_512_192, "kernel_hash": "1f6db4850c8ef2f3"},
-    "fp8_mixed": {"bytes": 2_260_587_008 + 22_075_136, "kernel_hash": "1f6db4850c8ef2f3"},
-    "int4_mixed": {"bytes": 1_124_507_648 + 20_538_112, "kernel_hash": "1f6db4850c8ef2f3"},
+    "llama70b_layer": {"bytes": 1_338_533_888 + 2_068_480, "kernel_hash": "6a3acd4a383e0a85"},
+    "prefix_sharing": {"bytes": 2_545_011_712 + 2_945_536, "kernel_hash": "6a3acd4a383e0a85"},
+    "long_context": {"bytes": 4_296_138_752 + 975_616, "kernel_hash": "6a3acd4a383e0a85"},
+    "fp8_mixed": {"bytes": 2_261_636_096 + 19_598_592, "kernel_hash": "6a3acd4a383e0a85"},
+    "int4_mixed": {"bytes": 1_124_583_424 + 16_731_392, "kernel_hash": "6a3acd4a383e0a85"},
 }
 
 

@@ -148,13 +148,18 @@ __device__ __forceinline__ int acc_d(int dt, int i, int lane) {
 }
 
 // Four signed 4-bit codes stored as offset-binary nibbles at bits 4i.. and 4i+16..
-// of w (after w >> 4i): as f16 bits 0x6400 | u the halves are exactly 1024 + u, so
-// subtracting 1032 leaves the code.  Returns {nibble i, nibble i + 4} as f16x2.
+// of w: returns {nibble i, nibble i + 4} as f16x2.  Even i: the nibbles masked into
+// the low mantissa bits of 0x6400 (f16 1024 + u), minus 1032.  Odd i: masked in place
+// at bits 4..7 (1024 + 16u), times 1/16 minus 72.  Both are exact, and i >= 2 reads
+// w >> 8, so one shift serves four pairs.
 __device__ __forceinline__ uint32_t int4_pair_f16(uint32_t w, int i) {
   uint32_t h;
-  const uint32_t x = w >> (4 * i);
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(x), "r"(0x000F000Fu), "r"(0x64006400u));
-  const __half2 v = __hsub2(*reinterpret_cast<const __half2 *>(&h), __floats2half2_rn(1032.f, 1032.f));
+  const uint32_t x = i >= 2 ? w >> 8 : w;
+  const uint32_t mask = (i & 1) ? 0x00F000F0u : 0x000F000Fu;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(x), "r"(mask), "r"(0x64006400u));
+  const __half2 hv = *reinterpret_cast<const __half2 *>(&h);
+  const __half2 v = (i & 1) ? __hfma2(hv, __floats2half2_rn(0.0625f, 0.0625f), __floats2half2_rn(-72.f, -72.f))
+                            : __hsub2(hv, __floats2half2_rn(1032.f, 1032.f));
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
@@ -250,6 +255,13 @@ __device__ __forceinline__ SeqTiles seq_tiles(int L, int window, int cascade_til
 }
 
 constexpr int kLoShift = 16;   // unit info bits 16..19: first valid token of the tile
+
+// A head's reference maximum (log2 domain) moves only when a score exceeds it by more
+// than this, so every p stays <= 2^8.
+constexpr float kMaxSlack = 8.f;
+// Quantised caches: P enters the mma as f16 times the ratio of the tile's V scale to
+// the accumulator's; the ratio stays <= 2^7 so that 2^8 * 2^7 is well inside f16.
+constexpr float kRatMax = 128.f;
 
 // Tiles attended per (sequence, KV head): the window's tiles, the chosen pages, or
 // the tiles after a cascaded shared prefix.
@@ -352,7 +364,7 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
     rat[nt] = 1.f;
     if constexpr (C::QUANT) {
       rat[nt] = vs[nt] * st.vinv[nt];
-      if (!vzero[C::PAIRED ? nt : 0] && !(rat[nt] <= 4096.f && rat[nt] >= 1.f / 4096.f)) {
+      if (!vzero[C::PAIRED ? nt : 0] && !(rat[nt] <= kRatMax && rat[nt] >= 1.f / 4096.f)) {
         const float f = st.vref[nt] / vs[nt];   // keeps P * ratio well inside f16
 #pragma unroll
         for (int dt = 0; dt < C::DT; ++dt)
@@ -365,54 +377,51 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
     }
   }
 
-  // ---- online softmax (log2 domain); element i: token r + 8*(i>>1), head 2q + (i&1)
+  // ---- online softmax (log2 domain); element i: token r + 8*(i>>1), head 2q + (i&1).
+  // Each head's reference maximum st.m moves only when a score exceeds it by more than
+  // kMaxSlack, so p <= 2^kMaxSlack; the result is the same (o and l share the
+  // reference).  A tile that moves no reference needs no reduction across lanes and
+  // no rescaling of the accumulator: one compare per score and a warp vote.
   const bool in0 = r >= lo && r < nvalid, in1 = r + 8 >= lo && r + 8 < nvalid;
-  float x[C::NT][4], mnew[C::NT][2];
-  bool grow = false;
+  float x[C::NT][4];
+  bool over = false;
 #pragma unroll
-  for (int nt = 0; nt < C::NT; ++nt) {
+  for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x[nt][i] = ((i >> 1) ? in1 : in0) ? s[nt][i] * sscale[nt] : -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float mx = fmaxf(x[nt][j], x[nt][j + 2]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      mnew[nt][j] = fmaxf(st.m[nt][j], mx);
-      grow |= mnew[nt][j] > st.m[nt][j];
+    for (int i = 0; i < 4; ++i) {
+      x[nt][i] = ((i >> 1) ? in1 : in0) ? s[nt][i] * sscale[nt] : -INFINITY;
+      over |= x[nt][i] > st.m[nt][i & 1] + kMaxSlack;
     }
-  }
-  // the accumulator and the sums are rescaled only when some head's maximum grew
-  // (paired 4-bit units measured faster without the vote: they always rescale)
-  if constexpr (C::PAIRED)
-    grow = true;
-  else
-    grow = __any_sync(0xffffffffu, grow);
-  float p[C::NT][4];
+  if (__any_sync(0xffffffffu, over)) {
 #pragma unroll
-  for (int nt = 0; nt < C::NT; ++nt) {
-    float alpha[2];
+    for (int nt = 0; nt < C::NT; ++nt) {
+      float alpha[2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      p[nt][j] = ex2(x[nt][j] - mnew[nt][j]);
-      p[nt][j + 2] = ex2(x[nt][j + 2] - mnew[nt][j]);
-      const float ps = p[nt][j] + p[nt][j + 2];
-      if (grow) {
-        alpha[j] = ex2(st.m[nt][j] - mnew[nt][j]);
-        st.l[nt][j] = st.l[nt][j] * alpha[j] + ps;
-      } else {
-        st.l[nt][j] += ps;
+      for (int j = 0; j < 2; ++j) {
+        float mx = fmaxf(x[nt][j], x[nt][j + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(st.m[nt][j], mx);
+        alpha[j] = ex2(st.m[nt][j] - mnew);
+        st.l[nt][j] *= alpha[j];
+        st.m[nt][j] = mnew;
       }
-      st.m[nt][j] = mnew[nt][j];
-    }
-    if (grow) {
 #pragma unroll
       for (int dt = 0; dt < C::DT; ++dt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) st.acc[nt][dt][i] *= alpha[i & 1];
     }
   }
+  float p[C::NT][4];
+#pragma unroll
+  for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      p[nt][j] = ex2(x[nt][j] - st.m[nt][j]);
+      p[nt][j + 2] = ex2(x[nt][j + 2] - st.m[nt][j]);
+      st.l[nt][j] += p[nt][j] + p[nt][j + 2];
+    }
 
   // ---- P^T fragments: hi + lo 16-bit parts, transposed in registers
   uint32_t bh[C::NT][2], bl[C::NT][2];
@@ -524,11 +533,12 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
       ldsm_x4_trans(R, vtile + t * 128 + ((c ^ (t & 7)) << 4));
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t lo8 = R[2 * hh], hi8 = R[2 * hh + 1];
-        uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(lo8, 0, 0x4420)),
-                         e4m3x2_to_f16x2(__byte_perm(lo8, 0, 0x4431)),
-                         e4m3x2_to_f16x2(__byte_perm(hi8, 0, 0x4420)),
-                         e4m3x2_to_f16x2(__byte_perm(hi8, 0, 0x4431))};
+        // one permute per register: (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0,
+        // t0 d1, t1 d1); its low half is row 2r, its high half row 2r + 1
+        const uint32_t lo8 = __byte_perm(R[2 * hh], 0, 0x3120);
+        const uint32_t hi8 = __byte_perm(R[2 * hh + 1], 0, 0x3120);
+        uint32_t a[4] = {e4m3x2_to_f16x2(lo8), e4m3x2_hi_to_f16x2(lo8),
+                         e4m3x2_to_f16x2(hi8), e4m3x2_hi_to_f16x2(hi8)};
         if (partial) {
           a[0] &= m01;
           a[1] &= m01;

@@ -746,6 +746,9 @@ CASCADE_CASES = [
     (16, 4, 64, 32, [(97, [1, 31, 32, 200]), (64, [50])], [1, 70]),  # G = 4, bs = 32
     (32, 2, 128, 16, [(500, [9, 90, 900]), (16, [1, 2])], [33]),     # G = 16 (two n-tiles)
     (8, 8, 128, 16, [(160, [5, 6, 7, 8, 9])], []),                   # G = 1
+    # 160 stacked rows (two chunks of 128, the second part padding); two pieces
+    (64, 8, 128, 16, [(1100, [1 + i % 7 for i in range(20)])], [3]),
+    (32, 8, 128, 32, [(704, list(range(1, 41))), (32, [4, 4])], [9]),  # G = 4, bs = 32
 ]
 
 
