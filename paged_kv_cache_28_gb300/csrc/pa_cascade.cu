@@ -279,36 +279,46 @@ __global__ void __launch_bounds__(kCasThreads, 3)
           mma_bf16(sc[1], qa[ks], b[2], b[3]);
         }
       }
-      // ---- online softmax per row (log2 domain); element i: row g4 + 8 (i >> 1)
+      // ---- online softmax per row (log2 domain); element i: row g4 + 8 (i >> 1).  A
+      // row's reference maximum moves only when a score exceeds it by more than 8, so
+      // p <= 2^8 (o and l share the reference); a tile that moves none skips the
+      // reduction across lanes and the accumulator rescale.
       float pr[2][4];
+      bool over = false;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sc[nt][i] *= p.sl2;
+        for (int i = 0; i < 4; ++i) {
+          sc[nt][i] *= p.sl2;
+          over |= sc[nt][i] > m[i >> 1] + 8.f;
+        }
+      if (__any_sync(0xffffffffu, over)) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float mx = fmaxf(fmaxf(sc[0][2 * h], sc[0][2 * h + 1]), fmaxf(sc[1][2 * h], sc[1][2 * h + 1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mnew = fmaxf(m[h], mx);
-        const float alpha = ex2(m[h] - mnew);
-        m[h] = mnew;
-        float sum = 0.f;
+        for (int h = 0; h < 2; ++h) {
+          float mx = fmaxf(fmaxf(sc[0][2 * h], sc[0][2 * h + 1]), fmaxf(sc[1][2 * h], sc[1][2 * h + 1]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float mnew = fmaxf(m[h], mx);
+          const float alpha = ex2(m[h] - mnew);
+          m[h] = mnew;
+          l[h] *= alpha;
+#pragma unroll
+          for (int dt = 0; dt < C::DT; ++dt) {
+            acc[dt][2 * h] *= alpha;
+            acc[dt][2 * h + 1] *= alpha;
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float v = ex2(sc[nt][2 * h + e] - mnew);
+            const float v = ex2(sc[nt][2 * h + e] - m[h]);
             pr[nt][2 * h + e] = v;
-            sum += v;
+            l[h] += v;
           }
-        l[h] = l[h] * alpha + sum;
-#pragma unroll
-        for (int dt = 0; dt < C::DT; ++dt) {
-          acc[dt][2 * h] *= alpha;
-          acc[dt][2 * h + 1] *= alpha;
-        }
-      }
       // ---- P as the A operand (the accumulator layout is the A layout): bf16 hi + lo
       uint32_t ph[4], pl[4];
 #pragma unroll
