@@ -834,6 +834,98 @@ def test_cascade_many_small_groups():
     assert dev.read_err() == 0
 
 
+# ---------------------------------------------------------------- online-softmax reference
+
+def _staircase_keys(batch, seqs, steps, rng):
+    """Keys whose scores (log2 units) step by steps[i] from one 16-token tile to the
+    next in sequence seqs[i] (None: a random walk of up to +-6 per tile).  Every query
+    head of a KV head's group gets the same query u; a key is f u / (|u|^2 sm_scale
+    log2 e) plus noise, so its score is about f.  bf16 pools take the keys as they are;
+    FP8 and 4-bit pools get absmax codes and scales per (block, KV head) over the rows
+    written here, and their V scales are spread over 2^-5 .. 2^5 per block."""
+    G, D, bs = batch.Hq // batch.Hkv, batch.D, batch.block_size
+    l2 = batch.sm_scale * np.log2(np.e)
+    keys = {}
+    for b, step in zip(seqs, steps):
+        L = int(batch.seq_lens[b])
+        ntile = (L + 15) // 16
+        f = (np.arange(ntile) * step if step is not None
+             else np.cumsum(rng.uniform(-6, 6, ntile)))
+        for h in range(batch.Hkv):
+            ub = wl.bf16_bits(rng.standard_normal(D).astype(np.float32))
+            batch.q[b, h * G:(h + 1) * G] = ub
+            uf = wl.bf16_to_float(ub).astype(np.float64)
+            for t in range(L):
+                k = f[t // 16] / l2 * uf / uf.dot(uf) + 0.05 * rng.standard_normal(D)
+                keys.setdefault((int(batch.block_tables[b, t // bs]), h), {})[t % bs] = k
+    for (blk, h), rows in keys.items():
+        if batch.kv_dtype == "bf16":
+            for r, k in rows.items():
+                batch.k_pool[blk, r, h] = wl.bf16_bits(k.astype(np.float32))
+            continue
+        amax = max(np.abs(k).max() for k in rows.values())
+        if batch.kv_dtype == "fp8_e4m3":
+            scale = np.float32(amax / 448.0)
+            for r, k in rows.items():
+                batch.k_pool[blk, r, h] = oracle.e4m3_from_float((k / scale).astype(np.float32))
+        else:
+            scale = np.float32(amax / 7.0)
+            for r, k in rows.items():
+                c = np.clip(np.rint(k / scale), -7, 7).astype(np.int16) + 8
+                batch.k_pool[blk, r, h] = (c[0::2] | (c[1::2] << 4)).astype(np.uint8)
+        batch.k_scale[blk, h] = scale
+        batch.v_scale[blk, h] *= np.float32(2.0 ** rng.uniform(-5, 5))
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "int4"])
+def test_softmax_reference_staircase_scores(kv_dtype):
+    """Scores that climb by 10 per tile (the running maximum moves on every tile), by 3
+    per tile (it stays up to 2^8 above an older reference for several tiles), fall by
+    2 per tile, or wander: every decode path against the oracle.  Quantised pools add
+    V scales over ten octaves, so P times the V-scale ratio must stay inside f16 (the
+    allowance 2^-9 sum_t p_t |v_t| is the one f16 weights need, as in the spread test)."""
+    batch = wl.build_batch("t", [700, 900, 500, 800], Hq=32, Hkv=4, D=128, block_size=16,
+                           seed=140, kv_dtype=kv_dtype)
+    _staircase_keys(batch, [0, 1, 2, 3], [10.0, 3.0, -2.0, None], np.random.default_rng(140))
+    dev = DeviceBatch(batch)
+    ref, _ = oracle_after_write(batch, write=False)
+    extra = 0.0
+    if batch.quantized:
+        extra = 2.0 ** -9 * oracle.paged_decode(
+            batch.q, batch.k_pool, _abs_codes(batch.v_pool, kv_dtype), batch.block_tables,
+            batch.seq_lens, batch.sm_scale, Hkv=batch.Hkv, block_size=batch.block_size,
+            k_scale=batch.k_scale, v_scale=batch.v_scale)
+    atol, rtol = _tol(batch)
+    for mode, ns in MODES:
+        if ns == "default":
+            ns = default_num_splits(dev.shape)
+        out = run_gpu(dev, mode, ns).astype(np.float64)
+        assert np.isfinite(out).all(), (mode, ns)
+        err = np.abs(out - ref)
+        bound = atol + rtol * np.abs(ref) + extra
+        assert np.all(err <= bound), (mode, ns, float((err - bound).max()))
+    assert dev.read_err() == 0
+
+
+def test_cascade_staircase_prefix():
+    """The cascade kernel's running maximum per stacked row: a shared prefix whose
+    scores climb by 10 per tile (every tile moves it) and one whose scores climb by 3
+    (weights up to 2^8 against an older reference), joined with the suffixes."""
+    batch, cg = _cascade_batch(32, 4, 128, 16, [(1100, [1, 40, 7]), (640, [3, 300])], [50],
+                               seed=141)
+    # the prefix blocks are shared: one member per group writes them, the others take
+    # its query so the whole group sees the staircase
+    _staircase_keys(batch, [2, 4, 5], [10.0, 3.0, None], np.random.default_rng(141))
+    batch.q[[0, 1]] = batch.q[2]
+    batch.q[3] = batch.q[4]
+    dev = DeviceBatch(batch)
+    dev.enable_cascade(cg)
+    ref, _ = oracle_after_write(batch, write=False)
+    for ns in (1, 9, default_num_splits(dev.shape)):
+        assert_close(_run_cascade(dev, ns), ref, batch, f"staircase cascade num_splits={ns}")
+    assert dev.read_err() == 0
+
+
 @pytest.mark.parametrize("mode", ["split", "cascade", "fp8"])
 def test_step_captured_in_cuda_graph(mode):
     """One decode step (cache write, split decode, merge; with the cascade also its plan,
