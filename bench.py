@@ -38,11 +38,11 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic per decode launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum), with
 # the hash of the kernel sources it was measured on; reported only while they still match.
 TRAFFIC = {
-    "llama70b_layer": {"bytes": 1_338_533_888 + 2_068_480, "kernel_hash": "6a3acd4a383e0a85"},
-    "prefix_sharing": {"bytes": 2_545_011_712 + 2_945_536, "kernel_hash": "6a3acd4a383e0a85"},
-    "long_context": {"bytes": 4_296_138_752 + 975_616, "kernel_hash": "6a3acd4a383e0a85"},
-    "fp8_mixed": {"bytes": 2_261_636_096 + 19_598_592, "kernel_hash": "6a3acd4a383e0a85"},
-    "int4_mixed": {"bytes": 1_124_583_424 + 16_731_392, "kernel_hash": "6a3acd4a383e0a85"},
+    "llama70b_layer": {"bytes": 1_338_533_376 + 2_068_992, "kernel_hash": "5d7dac995d1c8495"},
+    "prefix_sharing": {"bytes": 2_545_005_824 + 2_937_856, "kernel_hash": "5d7dac995d1c8495"},
+    "long_context": {"bytes": 4_296_253_952 + 2_498_304, "kernel_hash": "5d7dac995d1c8495"},
+    "fp8_mixed": {"bytes": 2_261_472_000 + 19_795_712, "kernel_hash": "5d7dac995d1c8495"},
+    "int4_mixed": {"bytes": 1_124_528_128 + 16_987_648, "kernel_hash": "5d7dac995d1c8495"},
 }
 
 

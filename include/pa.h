@@ -45,7 +45,7 @@
  *    and reads it after synchronising (see pa_read_error_flag).  err_flag may
  *    be NULL only if the caller vouches that the data is valid.
  *  - Shapes: B sequences (or tokens, for the cache write), Hq query heads,
- *    Hkv KV heads (Hq % Hkv == 0, G = Hq / Hkv <= 16), head dim D in {64, 128},
+ *    Hkv <= 2048 KV heads (Hq % Hkv == 0, G = Hq / Hkv <= 16), head dim D in {64, 128},
  *    block_size in {16, 32}.  FP8 and 4-bit pools need D = 128.
  *  - Layouts:
  *      q            [B, Hq, D]                  bf16

@@ -18,6 +18,7 @@ pa_status check_shape(const pa_shape *s, bool need_q) {
   if (s->B < 0 || s->Hkv <= 0 || s->D <= 0 || s->block_size <= 0 || s->nblocks <= 0 ||
       s->max_blocks <= 0)
     return PA_ERR_INVALID_ARG;
+  if (s->Hkv > 2048) return PA_ERR_UNSUPPORTED;        // the decode packs the KV head in 11 bits
   if (s->kv_dtype != PA_KV_BF16 && s->kv_dtype != PA_KV_FP8_E4M3 && s->kv_dtype != PA_KV_INT4)
     return PA_ERR_INVALID_ARG;
   if (need_q) {

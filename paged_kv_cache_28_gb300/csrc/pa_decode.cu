@@ -255,13 +255,18 @@ __device__ __forceinline__ SeqTiles seq_tiles(int L, int window, int cascade_til
 }
 
 constexpr int kLoShift = 16;   // unit info bits 16..19: first valid token of the tile
+constexpr int kKvhShift = 20;  // unit info bits 20..30: the unit's KV head (of the unit view)
+constexpr int kKvhMask = 0x7FF;
 
 // A head's reference maximum (log2 domain) moves only when a score exceeds it by more
 // than this, so every p stays <= 2^8.
 constexpr float kMaxSlack = 8.f;
 // Quantised caches: P enters the mma as f16 times the ratio of the tile's V scale to
-// the accumulator's; the ratio stays <= 2^7 so that 2^8 * 2^7 is well inside f16.
+// the accumulator's.  The ratio stays <= 2^7, so that 2^8 * 2^7 is well inside f16, and
+// >= 2^-12, so that a tile's largest weights keep f16's normal range; outside that the
+// accumulator is re-expressed in the tile's scale.
 constexpr float kRatMax = 128.f;
+constexpr float kRatMin = 1.f / 4096.f;
 
 // Tiles attended per (sequence, KV head): the window's tiles, the chosen pages, or
 // the tiles after a cascaded shared prefix.
@@ -364,8 +369,8 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
     rat[nt] = 1.f;
     if constexpr (C::QUANT) {
       rat[nt] = vs[nt] * st.vinv[nt];
-      if (!vzero[C::PAIRED ? nt : 0] && !(rat[nt] <= kRatMax && rat[nt] >= 1.f / 4096.f)) {
-        const float f = st.vref[nt] / vs[nt];   // keeps P * ratio well inside f16
+      if (!vzero[C::PAIRED ? nt : 0] && !(rat[nt] <= kRatMax && rat[nt] >= kRatMin)) {
+        const float f = st.vref[nt] / vs[nt];
 #pragma unroll
         for (int dt = 0; dt < C::DT; ++dt)
 #pragma unroll
@@ -616,7 +621,7 @@ struct PairSource {
   const int32_t *row;
   const int32_t *sel;   // this pair's chosen pages, or null
   int32_t *err;
-  int pair, w, nw, bs, nblocks;
+  int pair, kvh, w, nw, bs, nblocks;
   SeqTiles geo;         // with a selection: count = pages chosen, first = 0
   int npages;           // 16-token pages of the sequence
   int base;
@@ -648,7 +653,7 @@ struct PairSource {
     if (j == geo.count - 1) info |= kLastOfPair;
     if (i == 0) info |= kPieceStart;
     if (j + nw >= geo.count) info |= kPieceEnd;
-    return make_int4(phys, pair, tile, info);
+    return make_int4(phys, pair, tile, info | (kvh << kKvhShift));
   }
   __device__ __forceinline__ void init(int lane) {
     base = 0;
@@ -723,7 +728,7 @@ struct SegmentSource {
     if (shared_prefix_lens)
       info |= ((tile + 1) * kTile <= __ldg(shared_prefix_lens + b)) ? kHintShared : kHintPrivate;
     if (ct > 0) info |= kCascade;
-    return make_int4(phys, b * Hkv + kvh, tile, info);
+    return make_int4(phys, b * Hkv + kvh, tile, info | (kvh << kKvhShift));
   }
   __device__ __forceinline__ void init(int lane) {
     base = 0;
@@ -756,8 +761,8 @@ __device__ __forceinline__ void issue(const WarpSmem &ws, int s, int4 u, const P
   if (lane != 0) return;
   uint8_t *stage = ws.stage + s * C::STAGE_BYTES;
   const uint32_t bar = smem_u32(&ws.bar[s]);
-  const int phys = u.x, pair = u.y, tile = u.z;
-  const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
+  const int phys = u.x, tile = u.z;
+  const int kvh = (u.w >> kKvhShift) & kKvhMask;
   ws.meta[2 * s] = u;
   if constexpr (C::QUANT) {
     // (k, v) scale of each KV head of the unit: heads kvh, or 2 kvh and 2 kvh + 1
@@ -777,7 +782,8 @@ __device__ __forceinline__ void issue(const WarpSmem &ws, int s, int4 u, const P
   }
   const bool with_q = (u.w & kPieceStart) != 0;
   const uint32_t bytes = 2 * C::KV_BYTES + (with_q ? p.G * C::D * 2 : 0);
-  const int y = (phys == kInvalidPhys) ? p.nblocks * p.bs : phys * p.bs + (tile * kTile) % p.bs;
+  // block_size is 16 or 32: the tile's first row in its block is a mask away
+  const int y = (phys == kInvalidPhys) ? p.nblocks * p.bs : phys * p.bs + ((tile * kTile) & (p.bs - 1));
   const uint32_t dst = smem_u32(stage);
   fence_proxy_async();
   mbar_arrive_expect_tx(bar, bytes);
@@ -799,9 +805,11 @@ __device__ __forceinline__ void issue(const WarpSmem &ws, int s, int4 u, const P
       tma_load_2d(dst + C::KV_BYTES + h * (kTile * C::BOX_BYTES), tmV, x, y, bar);
     }
   }
-  if (with_q)
+  if (with_q) {                                  // a piece starts: the group's query rows
+    const int b = u.y / p.Hkv;
     bulk_load(dst + 2 * C::KV_BYTES, p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D,
               p.G * C::D * 2, bar);
+  }
 }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
@@ -934,6 +942,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.row = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
   src.err = p.err;
   src.pair = pair;
+  src.kvh = kvh;
   src.geo = seq_tiles(L, p.window);
   src.npages = (L + kTile - 1) / kTile;
   src.sel = nullptr;

@@ -64,6 +64,7 @@ def _decode(lib, s, **ptr):
     (dict(nblocks=0), _lib.PA_ERR_INVALID_ARG),
     (dict(B=-1), _lib.PA_ERR_INVALID_ARG),
     (dict(nblocks=1 << 27, block_size=32), _lib.PA_ERR_INVALID_ARG),   # rows overflow int32
+    (dict(Hq=4096, Hkv=4096, nblocks=4), _lib.PA_ERR_UNSUPPORTED),     # KV heads > 2048
 ])
 def test_decode_rejects_bad_shapes(lib, kw, status):
     import ctypes
