@@ -58,9 +58,11 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Bounded wait for the phase with the given parity; false if it never completed.
+// Bounded wait for the phase with the given parity; false if it never completed
+// (after kSpins polls).
+template <uint32_t kSpins = kWaitSpins>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitSpins; ++it) {
+  for (uint32_t it = 0; it < kSpins; ++it) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"

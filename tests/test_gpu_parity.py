@@ -5,6 +5,8 @@ indexing invariants; |gpu - oracle| <= 1e-3 + 1e-3 |oracle| elementwise for
 bf16 caches and <= 2e-2 + 2e-2 |oracle| for FP8 caches (the oracle reads the
 same codes and scales).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -992,3 +994,34 @@ def test_full_size_config_sampled(name):
         out3 = _run_cascade(dev, default_num_splits(dev.shape))
         assert dev.read_err() == 0
         assert_close(out3[rows[:, 0], rows[:, 1]], ref, batch, name + " cascade")
+
+
+# ---------------------------------------------------------------- failure handling
+
+def test_bounded_wait_reports_timeout_and_context_survives(tmp_path):
+    """A pipeline wait that nothing completes: the library's bounded mbarrier wait (here
+    with a short bound) gives up, the kernel sets PA_DEVERR_TIMEOUT and returns, and
+    the same context then runs a decode that matches the oracle.  The kernel is built
+    here from tests/csrc/wait_timeout.cu against the library's own wait helper."""
+    import ctypes
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    so = str(tmp_path / "libwait_timeout.so")
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17",
+                    "-Xcompiler", "-fPIC", "-shared",
+                    "-I", os.path.join(root, "include"),
+                    "-I", os.path.join(root, "paged_kv_cache_28_gb300", "csrc"),
+                    os.path.join(root, "tests", "csrc", "wait_timeout.cu"), "-o", so], check=True)
+    lib = ctypes.CDLL(so)
+    lib.run_wait_nothing_arrives.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    flags = torch.zeros(2, dtype=torch.int32, device="cuda")
+    rc = lib.run_wait_nothing_arrives(flags.data_ptr(), flags.data_ptr() + 4)
+    assert rc == 0                                   # the kernel returned: no fault, no hang
+    err, finished = flags.cpu().tolist()
+    assert err & _lib.PA_DEVERR_TIMEOUT and finished == 1
+    batch = wl.make("tiny")
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch)
+    assert_close(run_gpu(dev, "split", 3), ref, batch, "after a timed-out wait")
+    assert dev.read_err() == 0
