@@ -38,11 +38,11 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic per decode launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum), with
 # the hash of the kernel sources it was measured on; reported only while they still match.
 TRAFFIC = {
-    "llama70b_layer": {"bytes": 1_338_533_376 + 2_068_992, "kernel_hash": "5d7dac995d1c8495"},
-    "prefix_sharing": {"bytes": 2_545_005_824 + 2_937_856, "kernel_hash": "5d7dac995d1c8495"},
-    "long_context": {"bytes": 4_296_253_952 + 2_498_304, "kernel_hash": "5d7dac995d1c8495"},
-    "fp8_mixed": {"bytes": 2_261_472_000 + 19_795_712, "kernel_hash": "5d7dac995d1c8495"},
-    "int4_mixed": {"bytes": 1_124_528_128 + 16_987_648, "kernel_hash": "5d7dac995d1c8495"},
+    "llama70b_layer": {"bytes": 1_338_532_608 + 2_160_896, "kernel_hash": "aef9d20c56b656ab"},
+    "prefix_sharing": {"bytes": 2_544_666_368 + 2_918_656, "kernel_hash": "aef9d20c56b656ab"},
+    "long_context": {"bytes": 4_296_211_712 + 3_141_376, "kernel_hash": "aef9d20c56b656ab"},
+    "fp8_mixed": {"bytes": 2_261_518_592 + 19_928_320, "kernel_hash": "aef9d20c56b656ab"},
+    "int4_mixed": {"bytes": 1_124_569_088 + 17_001_728, "kernel_hash": "aef9d20c56b656ab"},
 }
 
 
