@@ -996,6 +996,31 @@ def test_full_size_config_sampled(name):
         assert_close(out3[rows[:, 0], rows[:, 1]], ref, batch, name + " cascade")
 
 
+
+def test_two_streams_decode_concurrently():
+    """Two batches, each with its own workspace and cascade groups, decoded over and over
+    on two caller streams at once: the library-owned stream that runs the cascade beside
+    the split kernel is shared by both, and neither result may see the other's work."""
+    b1, cg1 = _cascade_batch(64, 8, 128, 16, [(900, [1, 5, 17, 300]), (300, [3, 30])], [7, 500],
+                             seed=150)
+    b2, cg2 = _cascade_batch(32, 4, 128, 16, [(1600, [2, 9, 40]), (64, [5])], [1000, 3],
+                             seed=151)
+    d1, d2 = DeviceBatch(b1), DeviceBatch(b2)
+    d1.enable_cascade(cg1)
+    d2.enable_cascade(cg2)
+    ref1, _ = oracle_after_write(b1, write=False)
+    ref2, _ = oracle_after_write(b2, write=False)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ns1, ns2 = default_num_splits(d1.shape), 77
+    torch.cuda.synchronize()
+    for _ in range(20):
+        d1.decode_splitkv(ns1, stream=s1.cuda_stream, cascade=True)
+        d2.decode_splitkv(ns2, stream=s2.cuda_stream, cascade=True)
+    torch.cuda.synchronize()
+    assert_close(d1.out.cpu().numpy(), ref1, b1, "stream 1")
+    assert_close(d2.out.cpu().numpy(), ref2, b2, "stream 2")
+    assert d1.read_err() == 0 and d2.read_err() == 0
+
 # ---------------------------------------------------------------- failure handling
 
 def test_bounded_wait_reports_timeout_and_context_survives(tmp_path):
