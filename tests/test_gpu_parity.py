@@ -368,7 +368,8 @@ def test_fp8_g16_and_bs32():
 
 # ---------------------------------------------------------------- sliding window
 
-@pytest.mark.parametrize("kv_dtype,bs", [("bf16", 16), ("bf16", 32), ("fp8_e4m3", 16)])
+@pytest.mark.parametrize("kv_dtype,bs", [("bf16", 16), ("bf16", 32), ("fp8_e4m3", 16),
+                                        ("fp8_e4m3", 32), ("int4", 16), ("int4", 32)])
 def test_window_all_modes(kv_dtype, bs):
     lens = [1, 15, 16, 17, 40, 97, 333, 1200, 0, 64]
     batch = wl.build_batch("t", lens, Hq=64, Hkv=8, D=128, block_size=bs, seed=70 + bs,
