@@ -115,7 +115,8 @@ typedef struct {
  *     increasing order, as pa_quest_select writes them (page j = tokens
  *     [16 j, min(16 j + 16, L))).  An index outside the sequence sets
  *     PA_DEVERR_BLOCK_ID and reads zeros.  Not combined with window.
- *   shared_prefix_lens: pa_decode_splitkv only (ignored by pa_decode); optional
+ *   shared_prefix_lens: pa_decode_splitkv, and pa_decode given a workspace (it
+ *     runs the split decode); pa_decode without one ignores it.  Optional
  *     [B] int32 device array, a speed hint for batches with prefix sharing
  *     ("appendonly", "Prefix sharing is where the real win lives"): the number
  *     of leading tokens of sequence b that lie in blocks other sequences of the
@@ -124,7 +125,9 @@ typedef struct {
  *     shared block stays in L2 for its other readers.  Any value gives the same
  *     result, bit for bit.
  *   num_prefix_groups, group_offsets, group_seqs, group_prefix_len,
- *     cascade_workspace: prefix-aware (cascade) decode, pa_decode_splitkv only
+ *     cascade_workspace: prefix-aware (cascade) decode, in pa_decode_splitkv and in
+ *     pa_decode given a workspace (pa_decode without one ignores them and attends
+ *     over every token itself)
  *     ("appendonly", "Prefix sharing is where the real win lives": many
  *     sequences point at the same physical blocks).  Group g's members are
  *     group_seqs[group_offsets[g] .. group_offsets[g + 1]) (device int32
@@ -138,8 +141,8 @@ typedef struct {
  *     group and every member holds at least group_prefix_len[g] tokens (a
  *     member with fewer sets PA_DEVERR_SEQ_LEN and its output is undefined).
  *     cascade_workspace: device memory of at least pa_cascade_workspace_bytes
- *     bytes, 256-byte aligned, used by pa_decode_splitkv and read by the
- *     following pa_merge_lse.  bf16 pools only; not combined with window or
+ *     bytes, 256-byte aligned, used by the split decode and read by the merge
+ *     (pa_merge_lse, or the merge pa_decode runs).  bf16 pools only; not combined with window or
  *     topk.  The result equals the plain decode's up to rounding order.
  *   workspace, workspace_bytes, num_splits: pa_decode only.  With a workspace
  *     (device memory of at least pa_splitkv_workspace_bytes(shape, n) bytes,

@@ -769,6 +769,28 @@ def test_cascade_matches_oracle(Hq, Hkv, D, bs, groups, free):
     assert dev.read_err() == 0
 
 
+
+def test_cascade_through_pa_decode():
+    """pa_decode with a workspace runs the split decode with the cascade and the merge in
+    one call; without a workspace it ignores the groups and attends over every token."""
+    batch, cg = _cascade_batch(64, 8, 128, 16, [(900, [1, 5, 17, 300]), (300, [3, 30])],
+                               [7, 500], seed=152)
+    dev = DeviceBatch(batch)
+    dev.enable_cascade(cg)
+    ref, _ = oracle_after_write(batch, write=False)
+    for ns in (0, 13):
+        dev.ensure_workspace(ns or default_num_splits(dev.shape))
+        for ws in (dev.workspace, None):
+            dev.out.fill_(float("nan"))
+            _lib.pa_decode(dev.shape, dev.out, dev.q, dev.k_pool, dev.v_pool, None, None,
+                           dev.block_tables, dev.seq_lens, batch.sm_scale, dev.err, None,
+                           workspace=ws, num_splits=ns, shared_prefix_lens=dev.shared_prefix_lens,
+                           cascade=dev.cascade)
+            torch.cuda.synchronize()
+            assert_close(dev.out.cpu().numpy(), ref, batch,
+                         f"pa_decode cascade workspace={ws is not None} num_splits={ns}")
+    assert dev.read_err() == 0
+
 def test_cascade_prefix_is_whole_sequence():
     """Members whose every token is in the shared prefix (nothing left for the split
     kernel) and groups with a zero-length prefix."""
