@@ -1073,3 +1073,37 @@ def test_bounded_wait_reports_timeout_and_context_survives(tmp_path):
     ref, _ = oracle_after_write(batch)
     assert_close(run_gpu(dev, "split", 3), ref, batch, "after a timed-out wait")
     assert dev.read_err() == 0
+
+
+def test_c_program_drives_the_abi(tmp_path):
+    """The C ABI from plain C99 and the CUDA runtime, no Python in the loop
+    (tests/c/decode_from_c.c): cache write, split decode + merge, and pa_decode on a
+    small bf16 batch, against the oracle."""
+    import shutil
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cuda = os.path.dirname(os.path.dirname(os.path.realpath(shutil.which("nvcc"))))
+    pkg = os.path.join(root, "paged_kv_cache_28_gb300")
+    exe = str(tmp_path / "decode_from_c")
+    subprocess.run(["gcc", "-std=c99", "-O2", "-I", os.path.join(root, "include"),
+                    "-I", os.path.join(cuda, "include"), os.path.join(root, "tests", "c", "decode_from_c.c"),
+                    "-L", pkg, "-lpa", "-L", os.path.join(cuda, "lib64"), "-lcudart",
+                    "-Wl,-rpath," + pkg, "-o", exe], check=True)
+    batch = wl.build_batch("t", [1, 17, 33, 100, 300], Hq=16, Hkv=2, D=128, block_size=16, seed=160)
+    inp, outp = tmp_path / "in.bin", tmp_path / "out.bin"
+    with open(inp, "wb") as f:
+        f.write(np.array([batch.B, batch.Hq, batch.Hkv, batch.D, batch.block_size, batch.nblocks,
+                          batch.max_blocks, 7], np.int32).tobytes())
+        f.write(np.array([batch.sm_scale], np.float32).tobytes())
+        for a in (batch.q, batch.k_pool, batch.v_pool, batch.k_new, batch.v_new,
+                  batch.block_tables.astype(np.int32), batch.seq_lens.astype(np.int32),
+                  batch.slot_mapping.astype(np.int64)):
+            f.write(np.ascontiguousarray(a).tobytes())
+    subprocess.run([exe, str(inp), str(outp)], check=True)
+    raw = np.fromfile(outp, dtype=np.uint8)
+    n = batch.B * batch.Hq * batch.D
+    outs = raw[:8 * n].view(np.float32).reshape(2, batch.B, batch.Hq, batch.D)
+    assert raw[8 * n:].view(np.int32)[0] == 0
+    ref, _ = oracle_after_write(batch)
+    assert_close(outs[0], ref, batch, "from C: split decode + merge")
+    assert_close(outs[1], ref, batch, "from C: pa_decode")
