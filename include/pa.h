@@ -44,6 +44,10 @@
  *    (or reads zeros), nothing traps.  The flag is sticky; the caller zeroes it
  *    and reads it after synchronising (see pa_read_error_flag).  err_flag may
  *    be NULL only if the caller vouches that the data is valid.
+ *  - Cached values must be finite in the rows a decode attends.  A NaN or Inf there
+ *    gives an undefined output (NaN, or a value that leaves those tokens out).  Rows
+ *    it does not attend -- past a sequence's length, before a window -- may hold
+ *    anything.
  *  - Shapes: B sequences (or tokens, for the cache write), Hq query heads,
  *    Hkv <= 2048 KV heads (Hq % Hkv == 0, G = Hq / Hkv <= 16), head dim D in {64, 128},
  *    block_size in {16, 32}.  FP8 and 4-bit pools need D = 128.

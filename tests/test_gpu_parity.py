@@ -859,6 +859,43 @@ def test_cascade_many_small_groups():
     assert dev.read_err() == 0
 
 
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_unattended_rows_hold_nonfinite_values(kv_dtype):
+    """Pool rows a decode does not attend -- past a sequence's length in its last block,
+    and before a window's start inside the first tile it keeps -- hold NaN and Inf
+    (E4M3 NaN codes for FP8).  Every decode path gives the same bits as with clean rows:
+    those rows are masked, not multiplied by a zero weight."""
+    lens = [5, 17, 31, 100, 333]
+    W = 20
+    batch = wl.build_batch("t", lens, Hq=32, Hkv=4, D=128, block_size=16, seed=170,
+                           kv_dtype=kv_dtype)
+    clean = DeviceBatch(batch)
+    runs = [(mode, ns, w) for w in (0, W) for mode, ns in (("decode", None), ("decode_ws", None),
+                                                            ("split", 1), ("split", 9))]
+    want = [run_gpu(clean, m, ns, w).copy() for m, ns, w in runs]
+    bad_k, bad_v = (0x7FC0, 0x7F80) if kv_dtype == "bf16" else (0x7F, 0xFF)   # NaN, Inf / NaN
+    for b, L in enumerate(lens):                                # past the length
+        blk = batch.block_tables[b, (L - 1) // 16]
+        batch.k_pool[blk, L % 16 or 16:] = bad_k
+        batch.v_pool[blk, L % 16 or 16:] = bad_v
+    for w in (0, W):
+        if w:                                                   # before the window, same tile
+            for b, L in enumerate(lens):
+                if L <= w:
+                    continue
+                for t in range(((L - w) // 16) * 16, L - w):
+                    batch.k_pool[batch.block_tables[b, t // 16], t % 16] = bad_k
+                    batch.v_pool[batch.block_tables[b, t // 16], t % 16] = bad_v
+        poisoned = DeviceBatch(batch)
+        for (m, ns, ww), ref in zip(runs, want):
+            if ww != w:
+                continue
+            got = run_gpu(poisoned, m, ns, w)
+            assert np.isfinite(got).all(), (m, ns, w)
+            assert np.array_equal(_bits(got), _bits(ref)), (m, ns, w)
+        assert poisoned.read_err() == 0
+
 # ---------------------------------------------------------------- online-softmax reference
 
 def _staircase_keys(batch, seqs, steps, rng):
