@@ -35,15 +35,18 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode-attn tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM traffic per decode launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum), with
-# the hash of the kernel sources it was measured on; reported only while they still match.
+# DRAM traffic per decode launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum), by
+# workload and kernel, with the hash of the kernel sources it was measured on; reported only
+# while they still match.
 TRAFFIC = {
-    "llama70b_layer": {"bytes": 1_338_532_608 + 2_160_896, "kernel_hash": "aef9d20c56b656ab"},
-    "prefix_sharing": {"bytes": 2_544_666_368 + 2_918_656, "kernel_hash": "aef9d20c56b656ab"},
-    "long_context": {"bytes": 4_296_211_712 + 3_141_376, "kernel_hash": "aef9d20c56b656ab"},
-    "fp8_mixed": {"bytes": 2_261_518_592 + 19_928_320, "kernel_hash": "aef9d20c56b656ab"},
-    "int4_mixed": {"bytes": 1_124_569_088 + 17_001_728, "kernel_hash": "aef9d20c56b656ab"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_532_608 + 2_160_896, "kernel_hash": "aef9d20c56b656ab"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_666_368 + 2_918_656, "kernel_hash": "aef9d20c56b656ab"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_211_712 + 3_141_376, "kernel_hash": "aef9d20c56b656ab"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_518_592 + 19_928_320, "kernel_hash": "aef9d20c56b656ab"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_057_344 + 15_580_672, "kernel_hash": "aef9d20c56b656ab"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_569_088 + 17_001_728, "kernel_hash": "aef9d20c56b656ab"},
 }
+
 
 
 # ----------------------------------------------------------------------------
@@ -243,6 +246,10 @@ def run_ours(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(0, args.steps, EVENT_EVERY)]
 
+    call = args.call if args.call != "auto" else (
+        "decode" if args.config == "fp8_mixed" else "splitkv")
+    if call == "decode" and args.cascade:
+        raise SystemExit("--cascade runs through the split decode (--call splitkv)")
     if args.cascade:            # shared prefixes attended once per group (prefix-aware decode)
         if not batch.prefix_groups:
             raise SystemExit("--cascade needs a workload with prefix groups (prefix_sharing)")
@@ -263,6 +270,13 @@ def run_ours(args):
                                  dev.selected_pages, dev.err, st)
         if i is not None:
             ev[i][0].record(st)
+        if call == "decode":
+            _lib.pa_decode(dev.shape, dev.out, dev.q, dev.k_pool, dev.v_pool, dev.k_scale,
+                           dev.v_scale, dev.block_tables, dev.seq_lens, batch.sm_scale, dev.err,
+                           st, args.window, dev.selected_pages if quest else None)
+            if i is not None:
+                ev[i][1].record(st)
+            return
         _lib.pa_decode_splitkv(dev.shape, dev.out, dev.workspace, ns, dev.q, dev.k_pool,
                                dev.v_pool, dev.k_scale, dev.v_scale, dev.block_tables,
                                dev.seq_lens, batch.sm_scale, dev.err, st,
@@ -399,9 +413,15 @@ def run_ours(args):
     unique_tokens = step_kv_tokens(batch, args, selected)
     peak, peak_kind = measured_peak_hbm()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
-    tr = (TRAFFIC.get(args.config)
+    kernel = ("decode_pair_kernel" if call == "decode" else "decode_segment_kernel")
+    tr = (TRAFFIC.get((args.config, kernel))
           if args.window == 0 and args.quest_topk == 0 and not args.cascade else None)
     traffic = tr["bytes"] if tr and tr.get("kernel_hash") == kernel_source_hash() else None
+    # our kernels per step: the cache write; Quest's summary, scores and top-k; then the
+    # pair kernel, or the split kernel and the merge (with the cascade also its plan and
+    # its two launches, beside and after the split kernel)
+    launches = (1 + (3 if args.quest_topk > 0 else 0) +
+                (1 if call == "decode" else 2 + (3 if args.cascade else 0)))
     result = {
         "metric": METRIC,
         "value": world * batch.B / (ms_per_step * 1e-3),
@@ -420,7 +440,8 @@ def run_ours(args):
             "B": batch.B, "Hq": batch.Hq, "Hkv": batch.Hkv, "D": batch.D,
             "block_size": batch.block_size, "seq_len_sum": batch.logical_tokens,
             "seq_len_max": int(batch.seq_lens.max()),
-            "unique_kv_tokens": unique_tokens, "num_splits": ns,
+            "unique_kv_tokens": unique_tokens,
+            "num_splits": ns if call == "splitkv" else None,
             "window": args.window,
             "quest_topk": args.quest_topk,
             "cascade": bool(args.cascade),
@@ -429,11 +450,11 @@ def run_ours(args):
                    f"flushed: {kv_bytes / 1e9:.3f} GB of KV per step, a {2 * L2_BYTES >> 20} MB "
                    "buffer read between steps, each step timed alone with events"),
             "parallelism": f"replicas x{world}" if world > 1 else "single",
-            "step": ("pa_reshape_and_cache + pa_quest_summarize + pa_quest_select + "
-                     "pa_decode_splitkv + pa_merge_lse" if args.quest_topk > 0 else
-                     "pa_reshape_and_cache + pa_decode_splitkv (cascade + split kernels) + "
-                     "pa_merge_lse" if args.cascade else
-                     "pa_reshape_and_cache + pa_decode_splitkv + pa_merge_lse"),
+            "step": ("pa_reshape_and_cache + "
+                     + ("pa_quest_summarize + pa_quest_select + " if args.quest_topk > 0 else "")
+                     + ("pa_decode (one CTA per sequence and KV head)" if call == "decode" else
+                        "pa_decode_splitkv (cascade + split kernels) + pa_merge_lse"
+                        if args.cascade else "pa_decode_splitkv + pa_merge_lse")),
         },
         "roofline": {
             "bound": "hbm",
@@ -442,13 +463,14 @@ def run_ours(args):
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": traffic,
-            "kernel": ("cascade_kernel + decode_segment_kernel (the pa_decode_splitkv call)"
+            "kernel": ("decode_pair_kernel (the pa_decode call)" if call == "decode" else
+                       "cascade_kernel + decode_segment_kernel (the pa_decode_splitkv call)"
                        if args.cascade else "decode_segment_kernel (the pa_decode_splitkv call)"),
             "kernel_ms": decode_ms,
             "algorithmic_bytes": kv_bytes,
             "peak_kind": peak_kind,
         },
-        "gpu_launches": (5 if args.quest_topk > 0 else 4 if args.cascade else 3) * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clock_info,
     }
     if e2e is not None:
@@ -554,6 +576,11 @@ def main(argv=None):
                     choices=["tiny", "llama70b_layer", "prefix_sharing", "long_context",
                              "fp8_mixed", "int4_mixed", "code_assistant_turns"])
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--call", choices=["auto", "splitkv", "decode"], default="auto",
+                    help="the decode entry point of each step: pa_decode_splitkv + pa_merge_lse, "
+                         "or pa_decode without a workspace (one CTA per sequence and KV head); "
+                         "auto: pa_decode for fp8_mixed, whose workload names that call, "
+                         "pa_decode_splitkv otherwise")
     ap.add_argument("--e2e-eager", action="store_true",
                     help="e2e leg: launch each call eagerly instead of replaying a CUDA graph")
     ap.add_argument("--cascade", action="store_true",
