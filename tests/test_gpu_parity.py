@@ -1033,9 +1033,10 @@ def test_step_captured_in_cuda_graph(mode):
 @pytest.mark.parametrize("name", ["llama70b_layer", "prefix_sharing", "long_context", "fp8_mixed",
                                   "int4_mixed", "code_assistant_turns"])
 def test_full_size_config_sampled(name):
-    """The bench's launch configuration (split-KV, default num_splits) at full size;
-    every head of the longest, shortest and three random sequences plus 192
-    random (b, h) rows are compared with the oracle."""
+    """The bench's launch configurations at full size (split-KV at the default
+    num_splits; for FP8 also pa_decode, the call its workload names); every head of the
+    longest, shortest and three random sequences plus 192 random (b, h) rows are
+    compared with the oracle."""
     batch = wl.make(name)
     dev = DeviceBatch(batch)
     dev.reshape_and_cache()
@@ -1047,7 +1048,7 @@ def test_full_size_config_sampled(name):
     out_ws = run_gpu(dev, "decode_ws")            # the one-call form of the same path
     assert dev.read_err() == 0
     assert_close(out_ws[rows[:, 0], rows[:, 1]], ref, batch, name + " pa_decode + workspace")
-    if name in ("fp8_mixed", "int4_mixed"):      # unsplit kernel too, on the same rows
+    if name in ("fp8_mixed", "int4_mixed"):      # pa_decode without a workspace, same rows
         out2 = run_gpu(dev, "decode")
         assert_close(out2[rows[:, 0], rows[:, 1]], ref, batch, name + " decode")
     if name in ("prefix_sharing", "code_assistant_turns"):   # the cascade (bench.py --cascade)
