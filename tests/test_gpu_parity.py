@@ -489,10 +489,13 @@ def _oracle_page_scores(batch):
     return out
 
 
-@pytest.mark.parametrize("bs", [16, 32])
-def test_quest_page_scores(bs):
+@pytest.mark.parametrize("bs,Hq,Hkv,D", [(16, 32, 4, 128), (32, 32, 4, 128),
+                                         (16, 32, 2, 128), (16, 16, 4, 64), (32, 32, 2, 64)])
+def test_quest_page_scores(bs, Hq, Hkv, D):
+    """Scores for every page, for G = 4, 8 and 16 (one or two 8-head n-tiles) and D = 64
+    and 128."""
     lens = [1, 15, 16, 17, 100, 333, 1000, 2047, 0, 64, 4000]
-    batch = wl.build_batch("t", lens, Hq=32, Hkv=4, D=128, block_size=bs, seed=97 + bs)
+    batch = wl.build_batch("t", lens, Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seed=97 + bs + Hq + D)
     dev = DeviceBatch(batch)
     dev.quest_build_summaries()
     dev.quest_buffers(8)
@@ -507,10 +510,12 @@ def test_quest_page_scores(bs):
     assert dev.read_err() == 0
 
 
-@pytest.mark.parametrize("topk,bs", [(1, 16), (4, 16), (13, 32), (64, 16)])
-def test_quest_select_and_sparse_decode(topk, bs):
+@pytest.mark.parametrize("topk,bs,Hq,Hkv,D", [(1, 16, 64, 8, 128), (4, 16, 64, 8, 128),
+                                              (13, 32, 64, 8, 128), (64, 16, 64, 8, 128),
+                                              (6, 16, 32, 2, 128), (9, 32, 16, 4, 64)])
+def test_quest_select_and_sparse_decode(topk, bs, Hq, Hkv, D):
     lens = [1, 15, 16, 17, 100, 333, 1000, 2047, 0, 64]
-    batch = wl.build_batch("t", lens, Hq=64, Hkv=8, D=128, block_size=bs, seed=91 + topk)
+    batch = wl.build_batch("t", lens, Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seed=91 + topk)
     dev = DeviceBatch(batch)
     dev.quest_build_summaries()
     sel = dev.quest_select(topk)
