@@ -1174,38 +1174,31 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
     uo = reinterpret_cast<const float *>(cw + cl.uo) + row * D;
     p1 = p0 - 1;                                   // no split pieces
   }
+  // one pass: each batch of up to U pieces' (lse, o) is loaded together, then folded into
+  // a running maximum M with num and den rescaled when it rises
   constexpr int U = 8;
   for (int e = threadIdx.x; e < G * D4; e += blockDim.x) {
     const int g = e / D4, d4 = e - g * D4, gu = row0 + g;
     auto slot = [&](int s) { return static_cast<size_t>(s) * 2 + (s == p0 ? 1 : 0); };
-    float M = -INFINITY;
-    for (int s0 = p0; s0 <= p1; s0 += U) {
-      float v[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        v[u] = (s0 + u <= p1) ? __ldg(lse_part + slot(s0 + u) * Gu + gu) : -INFINITY;
-#pragma unroll
-      for (int u = 0; u < U; ++u) M = fmaxf(M, v[u]);
-    }
-    for (int c = 0; c < cpieces; ++c) M = fmaxf(M, clse[c * G + g]);
-    if (ulse) M = fmaxf(M, ulse[g]);
+    float M = -INFINITY, den = 0.f;
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-    float den = 0.f;
-    if (ulse) {
-      const float wgt = expf(ulse[g] - M);
-      const float4 x = reinterpret_cast<const float4 *>(uo + g * D)[d4];
-      num = make_float4(wgt * x.x, wgt * x.y, wgt * x.z, wgt * x.w);
-      den = wgt;
-    }
-    for (int c = 0; c < cpieces; ++c) {            // the cascade's pieces of the prefix
-      const float wgt = expf(clse[c * G + g] - M);
-      const float4 x = reinterpret_cast<const float4 *>(co + (c * G + g) * D)[d4];
-      num.x += wgt * x.x;
-      num.y += wgt * x.y;
-      num.z += wgt * x.z;
-      num.w += wgt * x.w;
-      den += wgt;
-    }
+    auto fold = [&](float l, float4 x) {           // one piece; l = -inf adds nothing
+      if (l > M) {
+        const float r = expf(M - l);               // 0 while M is -inf
+        num = make_float4(num.x * r, num.y * r, num.z * r, num.w * r);
+        den *= r;
+        M = l;
+      }
+      const float w = l == -INFINITY ? 0.f : expf(l - M);
+      num.x += w * x.x;
+      num.y += w * x.y;
+      num.z += w * x.z;
+      num.w += w * x.w;
+      den += w;
+    };
+    if (ulse) fold(ulse[g], reinterpret_cast<const float4 *>(uo + g * D)[d4]);
+    for (int c = 0; c < cpieces; ++c)              // the cascade's pieces of the prefix
+      fold(clse[c * G + g], reinterpret_cast<const float4 *>(co + (c * G + g) * D)[d4]);
     for (int s0 = p0; s0 <= p1; s0 += U) {
       float l[U];
       float4 x[U];
@@ -1216,9 +1209,18 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
         x[u] = ok ? __ldg(reinterpret_cast<const float4 *>(o_part + (slot(s0 + u) * Gu + gu) * D) + d4)
                   : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      float bm = l[0];
+#pragma unroll
+      for (int u = 1; u < U; ++u) bm = fmaxf(bm, l[u]);
+      if (bm > M) {                                // raise M once per batch
+        const float r = expf(M - bm);
+        num = make_float4(num.x * r, num.y * r, num.z * r, num.w * r);
+        den *= r;
+        M = bm;
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const float w = expf(l[u] - M);
+        const float w = l[u] == -INFINITY ? 0.f : expf(l[u] - M);
         num.x += w * x[u].x;
         num.y += w * x[u].y;
         num.z += w * x[u].z;
