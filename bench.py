@@ -39,12 +39,12 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_532_608 + 2_160_896, "kernel_hash": "aef9d20c56b656ab"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_666_368 + 2_918_656, "kernel_hash": "aef9d20c56b656ab"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_211_712 + 3_141_376, "kernel_hash": "aef9d20c56b656ab"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_518_592 + 19_928_320, "kernel_hash": "aef9d20c56b656ab"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_057_344 + 15_580_672, "kernel_hash": "aef9d20c56b656ab"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_569_088 + 17_001_728, "kernel_hash": "aef9d20c56b656ab"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_548_480 + 2_331_648, "kernel_hash": "46e32444e70361e0"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_043_712 + 2_940_416, "kernel_hash": "46e32444e70361e0"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_186_880 + 2_533_888, "kernel_hash": "46e32444e70361e0"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_557_248 + 20_763_648, "kernel_hash": "46e32444e70361e0"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_105_984 + 15_867_136, "kernel_hash": "46e32444e70361e0"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_609_792 + 17_080_064, "kernel_hash": "46e32444e70361e0"},
 }
 
 
