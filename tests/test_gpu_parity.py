@@ -232,6 +232,39 @@ def test_random_shapes_all_modes(Hq, Hkv, D, bs, lens):
     _modes_run(dev, batch, ref, f"Hq={Hq} Hkv={Hkv} D={D} bs={bs}")
 
 
+
+def _fuzz_case(case):
+    """Seeded draw of one configuration: cache type, group size, head dim, block size,
+    lengths (zeros, tails and longer sequences), a window or none, and split counts."""
+    rng = np.random.default_rng(1000 + case)
+    kv = ["bf16", "fp8_e4m3", "int4"][case % 3]
+    D = 128 if kv != "bf16" else int(rng.choice([64, 128]))
+    Hkv = int(rng.choice([1, 2, 3, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 6, 8, 12, 16]))
+    bs = int(rng.choice([16, 32]))
+    B = int(rng.integers(1, 11))
+    lens = [int(x) for x in rng.choice([0, 1, 15, 16, 17, 33, 64, 129, 300, 777, 1500], B)]
+    window = int(rng.integers(1, 600)) if rng.random() < 0.3 else 0
+    splits = [int(x) for x in rng.choice([1, 2, 5, 17, 64, 333], 2, replace=False)]
+    return kv, D, Hkv, G, bs, lens, window, splits
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_fuzz_configurations(case):
+    """24 seeded random configurations, each through the cache write and every decode
+    path (pa_decode with and without a workspace, the split decode at two split counts),
+    against the oracle."""
+    kv, D, Hkv, G, bs, lens, window, splits = _fuzz_case(case)
+    batch = wl.build_batch("t", lens, Hq=G * Hkv, Hkv=Hkv, D=D, block_size=bs, seed=2000 + case,
+                           kv_dtype=kv, max_blocks=(max(lens) + bs - 1) // bs + 2)
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch, window=window)
+    label = f"case {case}: {kv} D={D} Hkv={Hkv} G={G} bs={bs} lens={lens} window={window}"
+    for mode, ns in [("decode", None), ("decode_ws", None)] + [("split", n) for n in splits]:
+        assert_close(run_gpu(dev, mode, ns, window), ref, batch, f"{label} {mode} {ns}")
+    assert dev.read_err() == 0
+
 def test_fp8_small_all_modes():
     batch = wl.build_batch("t", [1, 16, 17, 200, 33, 0, 1000], Hq=64, Hkv=8, D=128, block_size=16,
                            seed=21, kv_dtype="fp8_e4m3")
