@@ -30,6 +30,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -387,16 +388,25 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
   // kMaxSlack, so p <= 2^kMaxSlack; the result is the same (o and l share the
   // reference).  A tile that moves no reference needs no reduction across lanes and
   // no rescaling of the accumulator: one compare per score and a warp vote.
-  const bool in0 = r >= lo && r < nvalid, in1 = r + 8 >= lo && r + 8 < nvalid;
+  const bool ragged = nvalid < kTile || lo > 0;   // warp-uniform
   float x[C::NT][4];
+#pragma unroll
+  for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[nt][i] = s[nt][i] * sscale[nt];
+  if (ragged) {
+    const bool in0 = r >= lo && r < nvalid, in1 = r + 8 >= lo && r + 8 < nvalid;
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (!((i >> 1) ? in1 : in0)) x[nt][i] = -INFINITY;
+  }
   bool over = false;
 #pragma unroll
   for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[nt][i] = ((i >> 1) ? in1 : in0) ? s[nt][i] * sscale[nt] : -INFINITY;
-      over |= x[nt][i] > st.m[nt][i & 1] + kMaxSlack;
-    }
+    for (int i = 0; i < 4; ++i) over |= x[nt][i] > st.m[nt][i & 1] + kMaxSlack;
   if (__any_sync(0xffffffffu, over)) {
 #pragma unroll
     for (int nt = 0; nt < C::NT; ++nt) {
@@ -450,37 +460,41 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
     }
   }
 
-  // ---- O^T += V^T P^T; rows of V beyond nvalid are zeroed in registers (the pool
-  // may hold stale or non-finite values there)
-  const bool ragged = nvalid < kTile || lo > 0;
-  uint32_t m01 = 0xFFFFFFFFu, m23 = 0xFFFFFFFFu;
-  if (ragged) {
-    auto in = [&](int t) { return t >= lo && t < nvalid; };
-    m01 = (in(2 * qd) ? 0x0000FFFFu : 0u) | (in(2 * qd + 1) ? 0xFFFF0000u : 0u);
-    m23 = (in(2 * qd + 8) ? 0x0000FFFFu : 0u) | (in(2 * qd + 9) ? 0xFFFF0000u : 0u);
-  }
-  if constexpr (C::QUANT && !C::PAIRED)   // a zero V scale: the tile's V rows are zeros
-    if (vzero[0]) m01 = m23 = 0u;
-  const bool partial = ragged || (C::QUANT && !C::PAIRED && vzero[0]);
+  // ---- O^T += V^T P^T.  A masked token has p = 0 exactly, but stale bf16 or E4M3 rows
+  // may hold non-finite values (0 * NaN = NaN), so for those caches the V rows of a
+  // ragged tile (and of a tile whose V scale is zero) are zeroed in registers under
+  // one warp-uniform branch; full tiles skip it.  Every 4-bit code converts to a finite
+  // value and a zero V scale already makes P zero (rat = 0), so 4-bit tiles need no
+  // mask.
   if constexpr (!C::QUANT) {
-    const int t = (lane & 7) + ((lane >> 4) << 3);
-#pragma unroll
-    for (int dt = 0; dt < C::DT; ++dt) {
-      const int c = ((dt & 3) << 1) + ((lane >> 3) & 1);
-      uint32_t a[4];
-      ldsm_x4_trans(a, vtile + (dt >> 2) * (kTile * 128) + t * 128 + ((c ^ (t & 7)) << 4));
-      if (partial) {
-        a[0] &= m01;
-        a[1] &= m01;
-        a[2] &= m23;
-        a[3] &= m23;
+    auto pv = [&](auto masked) {
+      constexpr bool MASK = decltype(masked)::value;
+      uint32_t m01 = 0xFFFFFFFFu, m23 = 0xFFFFFFFFu;
+      if constexpr (MASK) {
+        auto in = [&](int t) { return t >= lo && t < nvalid; };
+        m01 = (in(2 * qd) ? 0x0000FFFFu : 0u) | (in(2 * qd + 1) ? 0xFFFF0000u : 0u);
+        m23 = (in(2 * qd + 8) ? 0x0000FFFFu : 0u) | (in(2 * qd + 9) ? 0xFFFF0000u : 0u);
       }
+      const int t = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
-      for (int nt = 0; nt < C::NT; ++nt) {
-        mma_bf16(st.acc[nt][dt], a, bh[nt][0], bh[nt][1]);
-        mma_bf16(st.acc[nt][dt], a, bl[nt][0], bl[nt][1]);
+      for (int dt = 0; dt < C::DT; ++dt) {
+        const int c = ((dt & 3) << 1) + ((lane >> 3) & 1);
+        uint32_t a[4];
+        ldsm_x4_trans(a, vtile + (dt >> 2) * (kTile * 128) + t * 128 + ((c ^ (t & 7)) << 4));
+        if constexpr (MASK) {
+          a[0] &= m01;
+          a[1] &= m01;
+          a[2] &= m23;
+          a[3] &= m23;
+        }
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+          mma_bf16(st.acc[nt][dt], a, bh[nt][0], bh[nt][1]);
+          mma_bf16(st.acc[nt][dt], a, bl[nt][0], bl[nt][1]);
+        }
       }
-    }
+    };
+    if (ragged) pv(std::true_type{}); else pv(std::false_type{});
   } else if constexpr (C::INT4) {
     // ldmatrix.trans on the byte-pair view gives lane (r, q) the nibbles d = 32c + 4r
     // .. +3 of tokens 2q (low half) and 2q + 1 (high half): int4_pair_f16(., i) is
@@ -488,12 +502,6 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
     const int t = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
     for (int h = 0; h < C::HEADS; ++h) {
-      uint32_t k01 = m01, k23 = m23;
-      bool mask = partial;
-      if constexpr (C::PAIRED) {
-        if (vzero[h]) k01 = k23 = 0u;
-        mask = ragged || vzero[h];
-      }
 #pragma unroll
       for (int cc = 0; cc < C::D / 64; ++cc) {
         const int c = 2 * cc + (lane >> 4);
@@ -506,16 +514,10 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
         for (int half = 0; half < 2; ++half)    // chunk 2cc + half
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {      // rows 4r + 2mt + {0, 1}
-            uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * mt),
-                             int4_pair_f16(R[2 * half], 2 * mt + 1),
-                             int4_pair_f16(R[2 * half + 1], 2 * mt),
-                             int4_pair_f16(R[2 * half + 1], 2 * mt + 1)};
-            if (mask) {
-              a[0] &= k01;
-              a[1] &= k01;
-              a[2] &= k23;
-              a[3] &= k23;
-            }
+            const uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * mt),
+                                   int4_pair_f16(R[2 * half], 2 * mt + 1),
+                                   int4_pair_f16(R[2 * half + 1], 2 * mt),
+                                   int4_pair_f16(R[2 * half + 1], 2 * mt + 1)};
             const int dt = (2 * cc + half) * 2 + mt;
             if constexpr (C::PAIRED) {
               mma_f16(st.acc[h][dt], a, bh[h][0], bh[h][1]);
@@ -530,30 +532,44 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
     // ldmatrix.trans on byte pairs gives lane (r, q): bytes (t=2q: d=2r, 2r+1) and
     // (t=2q+1: d=2r, 2r+1); regrouping by d yields V^T rows d = 2r (even) and 2r+1
     // (odd) -- the tile's 16 output rows in the order (2r, 2r+1).
-    const int t = (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-    for (int cc = 0; cc < C::D / 32; ++cc) {
-      const int c = 2 * cc + (lane >> 4);
-      uint32_t R[4];
-      ldsm_x4_trans(R, vtile + t * 128 + ((c ^ (t & 7)) << 4));
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        // one permute per register: (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0,
-        // t0 d1, t1 d1); its low half is row 2r, its high half row 2r + 1
-        const uint32_t lo8 = __byte_perm(R[2 * hh], 0, 0x3120);
-        const uint32_t hi8 = __byte_perm(R[2 * hh + 1], 0, 0x3120);
-        uint32_t a[4] = {e4m3x2_to_f16x2(lo8), e4m3x2_hi_to_f16x2(lo8),
-                         e4m3x2_to_f16x2(hi8), e4m3x2_hi_to_f16x2(hi8)};
-        if (partial) {
-          a[0] &= m01;
-          a[1] &= m01;
-          a[2] &= m23;
-          a[3] &= m23;
+    auto pv = [&](auto masked) {
+      constexpr bool MASK = decltype(masked)::value;
+      uint32_t m01 = 0xFFFFFFFFu, m23 = 0xFFFFFFFFu;
+      if constexpr (MASK) {
+        if (vzero[0]) {
+          m01 = m23 = 0u;
+        } else {
+          auto in = [&](int t) { return t >= lo && t < nvalid; };
+          m01 = (in(2 * qd) ? 0x0000FFFFu : 0u) | (in(2 * qd + 1) ? 0xFFFF0000u : 0u);
+          m23 = (in(2 * qd + 8) ? 0x0000FFFFu : 0u) | (in(2 * qd + 9) ? 0xFFFF0000u : 0u);
         }
-#pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt) mma_f16(st.acc[nt][2 * cc + hh], a, bh[nt][0], bh[nt][1]);
       }
-    }
+      const int t = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+      for (int cc = 0; cc < C::D / 32; ++cc) {
+        const int c = 2 * cc + (lane >> 4);
+        uint32_t R[4];
+        ldsm_x4_trans(R, vtile + t * 128 + ((c ^ (t & 7)) << 4));
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          // one permute per register: (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0,
+          // t0 d1, t1 d1); its low half is row 2r, its high half row 2r + 1
+          const uint32_t lo8 = __byte_perm(R[2 * hh], 0, 0x3120);
+          const uint32_t hi8 = __byte_perm(R[2 * hh + 1], 0, 0x3120);
+          uint32_t a[4] = {e4m3x2_to_f16x2(lo8), e4m3x2_hi_to_f16x2(lo8),
+                           e4m3x2_to_f16x2(hi8), e4m3x2_hi_to_f16x2(hi8)};
+          if constexpr (MASK) {
+            a[0] &= m01;
+            a[1] &= m01;
+            a[2] &= m23;
+            a[3] &= m23;
+          }
+#pragma unroll
+          for (int nt = 0; nt < C::NT; ++nt) mma_f16(st.acc[nt][2 * cc + hh], a, bh[nt][0], bh[nt][1]);
+        }
+      }
+    };
+    if (ragged || vzero[0]) pv(std::true_type{}); else pv(std::false_type{});
   }
 }
 
