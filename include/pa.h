@@ -50,7 +50,10 @@
  *    anything.
  *  - Shapes: B sequences (or tokens, for the cache write), Hq query heads,
  *    Hkv <= 2048 KV heads (Hq % Hkv == 0, G = Hq / Hkv <= 16), head dim D in {64, 128},
- *    block_size in {16, 32}.  FP8 and 4-bit pools need D = 128.
+ *    block_size in {16, 32}.  FP8 and 4-bit pools need D = 128.  Indices stay in
+ *    int32: nblocks * block_size, B * max_blocks, B * Hkv * ceil(max_blocks *
+ *    block_size / 16) and, for code pools, nblocks * Hkv must be below 2^31
+ *    (else PA_ERR_INVALID_ARG).
  *  - Layouts:
  *      q            [B, Hq, D]                  bf16
  *      out          [B, Hq, D]                  fp32

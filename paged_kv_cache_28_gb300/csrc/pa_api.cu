@@ -32,6 +32,8 @@ pa_status check_shape(const pa_shape *s, bool need_q) {
   if (static_cast<int64_t>(s->nblocks) * s->block_size >= (int64_t(1) << 31))
     return PA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(s->B) * s->max_blocks >= (int64_t(1) << 31)) return PA_ERR_INVALID_ARG;
+  if (s->kv_dtype != PA_KV_BF16 && static_cast<int64_t>(s->nblocks) * s->Hkv >= (int64_t(1) << 31))
+    return PA_ERR_INVALID_ARG;                          // scale indices
   const int64_t max_tiles = (static_cast<int64_t>(s->max_blocks) * s->block_size + 15) / 16;
   if (static_cast<int64_t>(s->B) * s->Hkv * max_tiles >= (int64_t(1) << 31))
     return PA_ERR_INVALID_ARG;

@@ -125,6 +125,11 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Both addresses 8-byte aligned.
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // Make `bar` wait for this thread's outstanding cp.async copies (no count increment:
 // the barrier's expected arrival count must include this arrival).
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {

@@ -633,11 +633,22 @@ __device__ __forceinline__ int cascade_partials(uint64_t cws, int B, int Hq, int
 
 // Tiles w, w + NW, ... of one (b, kvh) pair's attended tiles, read straight from
 // the block table.
+// The copy record of one tile, built lane-parallel when a source loads 32 tiles:
+// (row of the tile's first token in the pools' 2-D view, unit, scale index
+// phys * Hkv + kvh of the unit view or -1 for a bad block, info bits).  A bad block
+// reads the rows past the pool, which the copy fills with zeros.
+__device__ __forceinline__ int4 tile_record(int phys, int tile, int unit, int kvh, int hkv,
+                                            int bs, int nblocks, int info) {
+  if (phys == kInvalidPhys) return make_int4(nblocks * bs, unit, -1, info);
+  // block_size is 16 or 32: the tile's first row in its block is a mask away
+  return make_int4(phys * bs + ((tile * kTile) & (bs - 1)), unit, phys * hkv + kvh, info);
+}
+
 struct PairSource {
   const int32_t *row;
   const int32_t *sel;   // this pair's chosen pages, or null
   int32_t *err;
-  int pair, kvh, w, nw, bs, nblocks;
+  int pair, kvh, hkv, w, nw, bs, nblocks;
   SeqTiles geo;         // with a selection: count = pages chosen, first = 0
   int npages;           // 16-token pages of the sequence
   int base;
@@ -648,7 +659,7 @@ struct PairSource {
   }
   __device__ __forceinline__ int4 load(int i) const {
     const int j = w + i * nw;
-    if (j >= geo.count) return make_int4(kInvalidPhys, 0, 0, 0);
+    if (j >= geo.count) return make_int4(0, 0, -1, 0);   // never issued
     int tile = geo.first + j, last_tile = geo.first + geo.count - 1;
     if (sel) {
       tile = __ldg(sel + j);
@@ -669,7 +680,7 @@ struct PairSource {
     if (j == geo.count - 1) info |= kLastOfPair;
     if (i == 0) info |= kPieceStart;
     if (j + nw >= geo.count) info |= kPieceEnd;
-    return make_int4(phys, pair, tile, info | (kvh << kKvhShift));
+    return tile_record(phys, tile, pair, kvh, hkv, bs, nblocks, info | (kvh << kKvhShift));
   }
   __device__ __forceinline__ void init(int lane) {
     base = 0;
@@ -705,7 +716,7 @@ struct SegmentSource {
   __device__ __forceinline__ int count() const { return end - begin; }
   __device__ __forceinline__ int4 load(int i) const {
     const int f = begin + i;
-    if (f >= end) return make_int4(kInvalidPhys, 0, 0, 0);
+    if (f >= end) return make_int4(0, 0, -1, 0);   // never issued
     int lo = 0, hi = B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -744,7 +755,8 @@ struct SegmentSource {
     if (shared_prefix_lens)
       info |= ((tile + 1) * kTile <= __ldg(shared_prefix_lens + b)) ? kHintShared : kHintPrivate;
     if (ct > 0) info |= kCascade;
-    return make_int4(phys, b * Hkv + kvh, tile, info | (kvh << kKvhShift));
+    return tile_record(phys, tile, b * Hkv + kvh, kvh, Hkv, bs, nblocks,
+                       info | (kvh << kKvhShift));
   }
   __device__ __forceinline__ void init(int lane) {
     base = 0;
@@ -777,29 +789,30 @@ __device__ __forceinline__ void issue(const WarpSmem &ws, int s, int4 u, const P
   if (lane != 0) return;
   uint8_t *stage = ws.stage + s * C::STAGE_BYTES;
   const uint32_t bar = smem_u32(&ws.bar[s]);
-  const int phys = u.x, tile = u.z;
+  const int y = u.x, sidx = u.z;
   const int kvh = (u.w >> kKvhShift) & kKvhMask;
   ws.meta[2 * s] = u;
   if constexpr (C::QUANT) {
-    // (k, v) scale of each KV head of the unit: heads kvh, or 2 kvh and 2 kvh + 1
+    // the k scales of the unit's KV heads (kvh, or 2 kvh and 2 kvh + 1), then their
+    // v scales
     float *sc = reinterpret_cast<float *>(&ws.meta[2 * s + 1]);
-    if (phys != kInvalidPhys) {
-#pragma unroll
-      for (int h = 0; h < C::HEADS; ++h) {
-        const size_t i = (static_cast<size_t>(phys) * p.Hkv + kvh) * C::HEADS + h;
-        cp_async_4(smem_u32(sc + 2 * h), p.k_scale + i);
-        cp_async_4(smem_u32(sc + 2 * h + 1), p.v_scale + i);
+    if (sidx >= 0) {
+      const size_t i = static_cast<size_t>(sidx) * C::HEADS;
+      if constexpr (C::PAIRED) {
+        cp_async_8(smem_u32(sc), p.k_scale + i);
+        cp_async_8(smem_u32(sc + 2), p.v_scale + i);
+      } else {
+        cp_async_4(smem_u32(sc), p.k_scale + i);
+        cp_async_4(smem_u32(sc + 2), p.v_scale + i);
       }
     } else {
 #pragma unroll
-      for (int h = 0; h < 2 * C::HEADS; ++h) sc[h] = 0.f;
+      for (int h = 0; h < 4; ++h) sc[h] = 0.f;
     }
     cp_async_arrive(bar);
   }
   const bool with_q = (u.w & kPieceStart) != 0;
   const uint32_t bytes = 2 * C::KV_BYTES + (with_q ? p.G * C::D * 2 : 0);
-  // block_size is 16 or 32: the tile's first row in its block is a mask away
-  const int y = (phys == kInvalidPhys) ? p.nblocks * p.bs : phys * p.bs + ((tile * kTile) & (p.bs - 1));
   const uint32_t dst = smem_u32(stage);
   fence_proxy_async();
   mbar_arrive_expect_tx(bar, bytes);
@@ -880,7 +893,7 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
 #pragma unroll
       for (int nt = 0; nt < C::NT; ++nt) {
         const int h = C::PAIRED ? nt : 0;
-        const float ks = h ? sc.z : sc.x, v = h ? sc.w : sc.y;
+        const float ks = h ? sc.y : sc.x, v = h ? sc.w : sc.z;
         sscale[nt] = p.sl2 * ks * st.qshift;
         vzero[h] = !(v > 0.f);
         vs[nt] = v;
@@ -959,6 +972,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.err = p.err;
   src.pair = pair;
   src.kvh = kvh;
+  src.hkv = p.Hkv;
   src.geo = seq_tiles(L, p.window);
   src.npages = (L + kTile - 1) / kTile;
   src.sel = nullptr;

@@ -71,6 +71,14 @@ def test_decode_rejects_bad_shapes(lib, kw, status):
     assert _decode(lib, ctypes.byref(shape(**kw))) == status
 
 
+def test_decode_rejects_scale_indices_past_int32(lib):
+    # FP8 pool of 2^20 blocks x 2048 KV heads: every other bound holds, but the
+    # [nblocks, Hkv] scale arrays have 2^31 entries
+    import ctypes
+    s = shape(kv_dtype=_lib.PA_KV_FP8_E4M3, D=128, Hq=2048, Hkv=2048, nblocks=1 << 20)
+    assert _decode(lib, ctypes.byref(s), ks=FAKE, vs=FAKE) == _lib.PA_ERR_INVALID_ARG
+
+
 def test_decode_rejects_bad_pointers(lib):
     import ctypes
     s = ctypes.byref(shape())
