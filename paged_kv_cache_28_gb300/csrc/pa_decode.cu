@@ -68,20 +68,35 @@ struct Cfg {
   static constexpr int BOXES = ROW / BOX_BYTES;                  // boxes per tile row
   static constexpr int BOX_X = BOX_BYTES / (KIND == kKindBf16 ? 2 : 1);  // box width in elements
   static constexpr int KV_BYTES = kTile * ROW;
-  static constexpr int Q_BYTES = 8 * NT * D * 2;
+  // Paired 4-bit units read a piece's query rows straight from global memory and keep
+  // the Q^T fragments in a per-warp shared-memory area: no Q slot in the stages (a
+  // quarter less shared memory) and 32 registers freed for the tile loop, which made
+  // pa_decode on these pools 8 % faster.  Other kinds carry the query rows in the
+  // stage that starts a piece and hold the fragments in registers.
+  static constexpr bool QSMEM = PAIRED;
+  static constexpr int Q_BYTES = QSMEM ? 0 : 8 * NT * D * 2;
+  static constexpr int QF_BYTES = QSMEM ? NT * KS * 32 * 8 : 0;   // per warp: uint2 per lane
   static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
   static constexpr int STAGES = PAIRED ? 2 : (INT4 ? 4 : 2);
   static constexpr int WARPS = 4;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int META_BYTES = 32;     // int4 unit + k/v scale
-  static constexpr int SMEM = 1024 + WARPS * STAGES * (STAGE_BYTES + 8 + META_BYTES);
+  static constexpr int SMEM = 1024 + WARPS * (STAGES * (STAGE_BYTES + 8 + META_BYTES) + QF_BYTES);
   // CTAs per SM that shared memory allows (227 KB usable, 1 KB reserved per CTA, 4 KB
-  // left for the split kernel's length scan); the register budget is held to it
+  // left for the split kernel's length scan); the register budget is held to it.
+  // Paired 4-bit units stop at three: four would fit in shared memory, but their
+  // 128-register budget spills and measured slower than three CTAs at up to 168.
   static constexpr int MIN_BLOCKS_RAW = (227 * 1024) / (SMEM + 1024 + 4096);
-  static constexpr int MIN_BLOCKS = MIN_BLOCKS_RAW < 1 ? 1 : (MIN_BLOCKS_RAW > 4 ? 4 : MIN_BLOCKS_RAW);
+  static constexpr int MIN_BLOCKS =
+      QSMEM ? 3 : (MIN_BLOCKS_RAW < 1 ? 1 : (MIN_BLOCKS_RAW > 4 ? 4 : MIN_BLOCKS_RAW));
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(!PAIRED || (NT == 2 && D == 128), "paired heads: one n-tile per KV head");
   static_assert(KV_BYTES % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
+  static_assert(!QSMEM || PAIRED, "query rows from global memory: paired 4-bit units only");
+  // pa_decode's CTA merges its warps' accumulators in the stage area; their m and l go
+  // after every per-warp area (mbarrier memory is never reused)
+  static_assert(WARPS * 8 * NT * D * 4 <= WARPS * STAGES * STAGE_BYTES, "pair merge must fit");
+  static constexpr int PAIR_SMEM = SMEM + 2 * WARPS * 8 * NT * 4;
 };
 
 struct Params {
@@ -116,7 +131,7 @@ struct State {
   float acc[C::NT][C::DT][4];   // O^T fragments (d x heads)
   float m[C::NT][2];            // running max, log2 domain, heads 2q, 2q+1 of each n-tile
   float l[C::NT][2];            // this thread's share of the running sum
-  uint32_t qf[C::NT][C::KS][2]; // Q^T B-fragments
+  uint32_t qf[C::QSMEM ? 1 : C::NT][C::QSMEM ? 1 : C::KS][2]; // Q^T B-fragments (else in smem)
   float qshift;                 // quantised: 2^-k undoing the power-of-two scaling of q
   float vref[C::NT];            // quantised: V scale each n-tile's accumulator is expressed in
   float vinv[C::NT];            // 1 / vref, or 0 before the piece's first nonzero V scale
@@ -164,10 +179,12 @@ __device__ __forceinline__ uint32_t int4_pair_f16(uint32_t w, int i) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Load the group's Q^T fragments from the stage's Q slot ([8*NT rows][D] bf16).
+// Load the group's Q^T fragments from the stage's Q slot ([8*NT rows][D] bf16), or,
+// with C::QSMEM, from the query rows in global memory into the warp's fragment area
+// qfs (lane-private: each lane reads back only what it wrote).
 template <class C>
 __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint16_t *qslot_ptr,
-                                       int lane) {
+                                       uint4 *qfs, int lane) {
   if constexpr (!C::QUANT) {
 #pragma unroll
     for (int nt = 0; nt < C::NT; ++nt)
@@ -197,7 +214,11 @@ __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint1
       for (int ks = 0; ks < C::KS; ++ks) {
         // 4-bit: the eight values b..b+7 of chunk c arrive as two uint2 (u = 0, 1)
         const int off = C::INT4 ? (ks >> 1) * 32 + qd * 8 + (ks & 1) * 4 : ks * 16 + qd * 4;
-        raw[nt][ks] = *reinterpret_cast<const uint2 *>(qslot_ptr + (nt * 8 + r) * C::D + off);
+        const uint2 *src = reinterpret_cast<const uint2 *>(qslot_ptr + (nt * 8 + r) * C::D + off);
+        if constexpr (C::QSMEM)
+          raw[nt][ks] = __ldg(src);
+        else
+          raw[nt][ks] = *src;
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(raw[nt][ks].x)), fabsf(bf16_hi(raw[nt][ks].x))),
                                  fmaxf(fabsf(bf16_lo(raw[nt][ks].y)), fabsf(bf16_hi(raw[nt][ks].y)))));
       }
@@ -220,8 +241,21 @@ __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint1
           const uint2 lo4 = raw[nt][ks & ~1], hi4 = raw[nt][ks | 1];
           const uint32_t e = (ks & 1) ? lo4.y : lo4.x;   // values b+2u, b+2u+1
           const uint32_t f = (ks & 1) ? hi4.y : hi4.x;   // values b+2u+4, b+2u+5
-          st.qf[nt][ks][0] = pack_f16(bf16_lo(e) * up, bf16_lo(f) * up);
-          st.qf[nt][ks][1] = pack_f16(bf16_hi(e) * up, bf16_hi(f) * up);
+          const uint32_t f0 = pack_f16(bf16_lo(e) * up, bf16_lo(f) * up);
+          const uint32_t f1 = pack_f16(bf16_hi(e) * up, bf16_hi(f) * up);
+          if constexpr (C::QSMEM) {   // k-steps 2j and 2j + 1 share one 16-byte entry
+            uint4 &q4 = qfs[(nt * (C::KS / 2) + (ks >> 1)) * 32 + lane];
+            if (ks & 1) {
+              q4.z = f0;
+              q4.w = f1;
+            } else {
+              q4.x = f0;
+              q4.y = f1;
+            }
+          } else {
+            st.qf[nt][ks][0] = f0;
+            st.qf[nt][ks][1] = f1;
+          }
         } else {
           const uint2 v = raw[nt][ks];
           st.qf[nt][ks][0] = pack_f16(bf16_lo(v.x) * up, bf16_hi(v.x) * up);
@@ -283,8 +317,9 @@ __device__ __forceinline__ int pair_tile_count(int L, int window, int topk,
 // its V rows count as zeros.  The accumulator stays in units of the piece's first
 // nonzero V scale: a tile with another scale enters through P scaled by the ratio.
 template <class C>
-__device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint32_t vtile,
-                                             int lo, int nvalid, const float (&sscale)[C::NT],
+__device__ __forceinline__ void process_tile(State<C> &st, const uint4 *qfs, uint32_t ktile,
+                                             uint32_t vtile, int lo, int nvalid,
+                                             const float (&sscale)[C::NT],
                                              const float (&vs)[C::NT],
                                              const bool (&vzero)[C::HEADS], int lane) {
   // tokens lo <= t < nvalid of the tile are attended
@@ -323,7 +358,9 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
         else
           ldsm_x4(R, ktile + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
 #pragma unroll
-        for (int half = 0; half < 2; ++half)    // chunk 2cc + half: R[2 half] rows r, R[2 half + 1] rows r + 8
+        for (int half = 0; half < 2; ++half) {  // chunk 2cc + half: R[2 half] rows r, R[2 half + 1] rows r + 8
+          uint4 q4 = make_uint4(0u, 0u, 0u, 0u);
+          if constexpr (C::QSMEM) q4 = qfs[(h * (C::KS / 2) + 2 * cc + half) * 32 + lane];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * u),
@@ -331,7 +368,9 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
                                    int4_pair_f16(R[2 * half], 2 * u + 1),
                                    int4_pair_f16(R[2 * half + 1], 2 * u + 1)};
             const int ks = (2 * cc + half) * 2 + u;
-            if constexpr (C::PAIRED) {
+            if constexpr (C::QSMEM) {
+              mma_f16(s[h], a, u ? q4.z : q4.x, u ? q4.w : q4.y);
+            } else if constexpr (C::PAIRED) {
               mma_f16(s[h], a, st.qf[h][ks][0], st.qf[h][ks][1]);
             } else {
 #pragma unroll
@@ -339,6 +378,7 @@ __device__ __forceinline__ void process_tile(State<C> &st, uint32_t ktile, uint3
                 mma_f16(s[nt], a, st.qf[nt][ks][0], st.qf[nt][ks][1]);
             }
           }
+        }
       }
   } else {
     // ldmatrix on byte pairs: lane (r, q) receives codes 4q..4q+3 of a 16-code chunk;
@@ -780,7 +820,8 @@ struct SegmentSource {
 struct WarpSmem {
   uint8_t *stage;     // STAGES * STAGE_BYTES, 1024-aligned
   uint64_t *bar;      // STAGES mbarriers
-  int4 *meta;         // STAGES * 2 int4: unit, then (k scale, v scale) as floats
+  int4 *meta;         // STAGES * 2 int4: unit, then the unit's k scales and v scales
+  uint4 *qf;          // Q^T fragments when they live in shared memory, else null
 };
 
 template <class C>
@@ -811,7 +852,7 @@ __device__ __forceinline__ void issue(const WarpSmem &ws, int s, int4 u, const P
     }
     cp_async_arrive(bar);
   }
-  const bool with_q = (u.w & kPieceStart) != 0;
+  const bool with_q = !C::QSMEM && (u.w & kPieceStart) != 0;
   const uint32_t bytes = 2 * C::KV_BYTES + (with_q ? p.G * C::D * 2 : 0);
   const uint32_t dst = smem_u32(stage);
   fence_proxy_async();
@@ -882,8 +923,14 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
     for (int h = 0; h < C::HEADS; ++h) vzero[h] = false;
     if (u.w & kPieceStart) {
       st.reset();
-      load_q<C>(st, ktile + 2 * C::KV_BYTES,
-                reinterpret_cast<const uint16_t *>(stage + 2 * C::KV_BYTES), lane);
+      if constexpr (C::QSMEM) {   // the group's query rows, straight from global memory
+        const int b = u.y / p.Hkv, kvh = (u.w >> kKvhShift) & kKvhMask;
+        load_q<C>(st, 0u, p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D, ws.qf,
+                  lane);
+      } else {
+        load_q<C>(st, ktile + 2 * C::KV_BYTES,
+                  reinterpret_cast<const uint16_t *>(stage + 2 * C::KV_BYTES), nullptr, lane);
+      }
       piece_first = (u.w & kFirstOfPair) != 0;
     }
     if constexpr (C::QUANT) {
@@ -899,7 +946,7 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
         vs[nt] = v;
       }
     }
-    process_tile<C>(st, ktile, ktile + C::KV_BYTES, (u.w >> kLoShift) & 0xF, u.w & 0xFF, sscale,
+    process_tile<C>(st, ws.qf, ktile, ktile + C::KV_BYTES, (u.w >> kLoShift) & 0xF, u.w & 0xFF, sscale,
                     vs, vzero, lane);
     if (u.w & kPieceEnd) on_piece_end(u, piece_first, st);
     __syncwarp();
@@ -917,27 +964,35 @@ __device__ __forceinline__ WarpSmem setup_smem(uint8_t *raw, int warp, int G, in
   uint8_t *tail = base + C::WARPS * C::STAGES * C::STAGE_BYTES;
   ws.bar = reinterpret_cast<uint64_t *>(tail) + warp * C::STAGES;
   ws.meta = reinterpret_cast<int4 *>(tail + C::WARPS * C::STAGES * 8) + warp * C::STAGES * 2;
+  ws.qf = nullptr;
+  if constexpr (C::QSMEM)
+    ws.qf = reinterpret_cast<uint4 *>(tail + C::WARPS * C::STAGES * (8 + C::META_BYTES) +
+                                      warp * C::QF_BYTES);
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < C::STAGES; ++s) mbar_init(smem_u32(&ws.bar[s]), C::QUANT ? 2 : 1);
     fence_mbar_init();
   }
   // query rows G..8*NT-1 of every Q slot stay zero (the bulk copy writes G rows)
-  const int pad = (8 * C::NT - G) * C::D * 2;
-  for (int s = 0; s < C::STAGES; ++s) {
-    uint8_t *qs = ws.stage + s * C::STAGE_BYTES + 2 * C::KV_BYTES + G * C::D * 2;
-    for (int o = lane * 16; o < pad; o += 32 * 16) *reinterpret_cast<uint4 *>(qs + o) = make_uint4(0, 0, 0, 0);
+  if constexpr (!C::QSMEM) {
+    const int pad = (8 * C::NT - G) * C::D * 2;
+    for (int s = 0; s < C::STAGES; ++s) {
+      uint8_t *qs = ws.stage + s * C::STAGE_BYTES + 2 * C::KV_BYTES + G * C::D * 2;
+      for (int o = lane * 16; o < pad; o += 32 * 16)
+        *reinterpret_cast<uint4 *>(qs + o) = make_uint4(0, 0, 0, 0);
+    }
   }
   __syncwarp();
   return ws;
 }
 
-// First byte after the per-warp stages, barriers and metadata (16-byte aligned).
+// First byte after the per-warp stages, barriers, metadata and Q^T fragment areas
+// (16-byte aligned).
 template <class C>
 __device__ __forceinline__ uint8_t *split_tail(uint8_t *raw) {
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  return base + C::WARPS * C::STAGES * (C::STAGE_BYTES + 8 + C::META_BYTES);
+  return base + C::WARPS * (C::STAGES * (C::STAGE_BYTES + 8 + C::META_BYTES) + C::QF_BYTES);
 }
 
 // Dynamic shared memory of the split kernel: stages plus the length scan.
@@ -993,9 +1048,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   constexpr int GP = 8 * C::NT;
-  float *sm_m = reinterpret_cast<float *>(base);                 // [WARPS][GP]
+  float *sm_acc = reinterpret_cast<float *>(base);               // [WARPS][GP][D], stage area
+  float *sm_m = reinterpret_cast<float *>(split_tail<C>(smem_raw));   // [WARPS][GP]
   float *sm_l = sm_m + C::WARPS * GP;                            // [WARPS][GP]
-  float *sm_acc = sm_l + C::WARPS * GP;                          // [WARPS][GP][D]
   {
     float ltot[C::NT][2];
     reduce_l<C>(st, ltot);
@@ -1351,8 +1406,8 @@ static Params make_params(const pa_shape &s, float *out, const void *q, const fl
 template <class C>
 static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
                              cudaStream_t stream) {
-  if (prep_kernel(decode_pair_kernel<C>, C::SMEM) != cudaSuccess) return PA_ERR_CUDA;
-  decode_pair_kernel<C><<<p.B * p.Hkv, C::THREADS, C::SMEM, stream>>>(mk, mv, p);
+  if (prep_kernel(decode_pair_kernel<C>, C::PAIR_SMEM) != cudaSuccess) return PA_ERR_CUDA;
+  decode_pair_kernel<C><<<p.B * p.Hkv, C::THREADS, C::PAIR_SMEM, stream>>>(mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
