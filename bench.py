@@ -39,12 +39,12 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_548_480 + 2_331_648, "kernel_hash": "46e32444e70361e0"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_043_712 + 2_940_416, "kernel_hash": "46e32444e70361e0"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_186_880 + 2_533_888, "kernel_hash": "46e32444e70361e0"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_557_248 + 20_763_648, "kernel_hash": "46e32444e70361e0"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_105_984 + 15_867_136, "kernel_hash": "46e32444e70361e0"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_609_792 + 17_080_064, "kernel_hash": "46e32444e70361e0"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_530_560 + 2_071_552, "kernel_hash": "d079e65729300462"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_732_160 + 2_910_976, "kernel_hash": "d079e65729300462"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_249_600 + 2_041_856, "kernel_hash": "d079e65729300462"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_476_608 + 20_132_352, "kernel_hash": "d079e65729300462"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_261_120 + 15_911_680, "kernel_hash": "d079e65729300462"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_563_968 + 16_166_144, "kernel_hash": "d079e65729300462"},
 }
 
 
