@@ -8,6 +8,8 @@
 // it holds; a query scores it by sum_d max(q_d min_d, q_d max_d), an upper bound of
 // q . k over the page.  A GQA group shares one selection: each page keeps its best
 // score over the group's query heads.
+#include <algorithm>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -165,11 +167,12 @@ struct ScoreCfg {
                                                    // an ldmatrix reads fall in distinct banks
   static constexpr int CH = 16;                    // pages per chunk (the mma's m)
   static constexpr int KSQ = D / 16;               // k-steps over one half of the row
-  static constexpr int QB = 8 * NG * D * 2;        // the group's query rows, zero-padded
-  static constexpr int BUF = CH * ROWP + QB;       // one stage
+  static constexpr int BUF = CH * ROWP;            // one stage: a chunk's summary rows
+  static constexpr int STAGES = 2;                 // one chunk in flight while one is scored
   static constexpr int WARPS = 4;
   static constexpr int THREADS = 32 * WARPS;
-  static constexpr int FIXED = WARPS * 2 * BUF + WARPS * 2 * 8;   // stages + mbarriers
+  // per warp: stages, then mbarriers, chunk descriptors (int4) and valid-row masks
+  static constexpr int FIXED = WARPS * STAGES * (BUF + 8 + 16 + 4);
   static_assert(BUF % 16 == 0, "bulk copies need 16-byte aligned stages");
 };
 
@@ -185,23 +188,21 @@ __global__ void __launch_bounds__(S::THREADS) quest_score_kernel(
     const int32_t *seq_lens, int B, int Hq, int Hkv, int bs, int nblocks, int max_blocks,
     int max_pages, int nseg, float *scores, int32_t *err) {
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int D = S::D;
+  constexpr int D = S::D, ST = S::STAGES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t *stage = smem + warp * 2 * S::BUF;
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::WARPS * 2 * S::BUF) + warp * 2;
+  uint8_t *stage = smem + warp * ST * S::BUF;
+  uint8_t *tail = smem + S::WARPS * ST * S::BUF;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(tail) + warp * ST;
+  int4 *desc = reinterpret_cast<int4 *>(tail + S::WARPS * ST * 8) + warp * ST;
+  unsigned *okms = reinterpret_cast<unsigned *>(tail + S::WARPS * ST * 24) + warp * ST;
   int32_t *prefix = reinterpret_cast<int32_t *>(smem + S::FIXED);
   const int G = Hq / Hkv;
   pdl_trigger();
   if (lane == 0) {
-    mbar_init(smem_u32(&bar[0]), 1);
-    mbar_init(smem_u32(&bar[1]), 1);
+    for (int st = 0; st < ST; ++st) mbar_init(smem_u32(&bar[st]), 1);
     fence_mbar_init();
   }
-  for (int st = 0; st < 2; ++st) {                 // query rows G .. 8 NG - 1 stay zero
-    uint8_t *pad = stage + st * S::BUF + S::CH * S::ROWP + G * D * 2;
-    for (int o = lane * 16; o < (8 * S::NG - G) * D * 2; o += 32 * 16)
-      *reinterpret_cast<uint4 *>(pad + o) = make_uint4(0u, 0u, 0u, 0u);
-  }
+  __syncwarp();
   const int cap = max_blocks * bs;
   scan_units<S::THREADS>(seq_lens, B, Hkv, cap, prefix);
   pdl_wait();                                      // summaries come from the launch before
@@ -211,99 +212,108 @@ __global__ void __launch_bounds__(S::THREADS) quest_score_kernel(
   const int W = (total + nseg - 1) / nseg;
   int f = min(seg * W, total);
   const int end = min(f + W, total);
+  // the unit (sequence b, KV head kvh) holding position f: [ustart, uend) of npg pages;
+  // the next unit is the next KV head of the same sequence unless that was the last
+  int ub = -1, ukvh = 0, unpg = 0, ustart = 0, uend = 0;
   auto take = [&](ScoreChunk &c) -> bool {         // next chunk of the segment
     if (f >= end) return false;
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= f) lo = mid; else hi = mid - 1;
+    if (f >= uend) {
+      if (ub >= 0 && ukvh + 1 < Hkv) {
+        ++ukvh;
+        ustart = uend;
+        uend += unpg;
+      } else {
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (prefix[mid] <= f) lo = mid; else hi = mid - 1;
+        }
+        ub = lo;
+        unpg = (prefix[lo + 1] - prefix[lo]) / Hkv;
+        ukvh = (f - prefix[lo]) / unpg;
+        ustart = prefix[lo] + ukvh * unpg;
+        uend = ustart + unpg;
+      }
     }
-    const int npg = (prefix[lo + 1] - prefix[lo]) / Hkv;
-    const int r = f - prefix[lo];
-    c.b = lo;
-    c.kvh = r / npg;
-    c.j0 = r - c.kvh * npg;
-    c.n = min(min(S::CH, end - f), npg - c.j0);
+    c.b = ub;
+    c.kvh = ukvh;
+    c.j0 = f - ustart;
+    c.n = min(min(S::CH, end - f), uend - f);
     f += c.n;
     return true;
   };
-  // copy chunk c's summary rows (and the group's query rows when with_q) into stage
-  // st; returns the mask of rows whose block-table entry is valid
-  auto issue = [&](const ScoreChunk &c, int st, bool with_q) -> unsigned {
+  const int pshift = bs == 32 ? 1 : 0;             // 16-token pages per block: 1 or 2
+  auto qrows = [&](int b, int kvh) { return q + (static_cast<size_t>(b) * Hq + kvh * G) * D; };
+  // copy chunk c's summary rows into stage st and record its descriptor and the mask of
+  // rows whose block-table entry is valid; a chunk that starts its unit also pulls the
+  // group's query rows into L2 for the fragments built when it is scored
+  int last_pair = -1;
+  auto issue = [&](const ScoreChunk &c, int st) {
     uint8_t *buf = stage + st * S::BUF;
-    const uint32_t b = smem_u32(&bar[st]);
+    const uint32_t bb = smem_u32(&bar[st]);
     int page = 0;
     bool ok = false;
     if (lane < c.n) {
       const int j = c.j0 + lane;
-      const int phys = __ldg(block_tables + static_cast<size_t>(c.b) * max_blocks + (j * kTile) / bs);
+      const int phys = __ldg(block_tables + static_cast<size_t>(c.b) * max_blocks + (j >> pshift));
       ok = phys >= 0 && phys < nblocks;
-      page = ok ? phys * (bs / kTile) + (j * kTile % bs) / kTile : 0;
+      page = ok ? (phys << pshift) + (j & pshift) : 0;
     }
     const unsigned okm = __ballot_sync(0xffffffffu, ok);
-    const uint32_t bytes = __popc(okm) * S::ROWB + (with_q ? G * D * 2 : 0);
+    const int pair = c.b * Hkv + c.kvh;
+    if (pair != last_pair && lane * 128 < G * D * 2)
+      prefetch_l2(reinterpret_cast<const uint8_t *>(qrows(c.b, c.kvh)) + lane * 128);
+    last_pair = pair;
     fence_proxy_async();                           // the stage was last read by ldmatrix
     __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(b, bytes);
+    if (lane == 0) {
+      desc[st] = make_int4(c.b, c.kvh, c.j0, c.n);
+      okms[st] = okm;
+      mbar_arrive_expect_tx(bb, __popc(okm) * S::ROWB);
+    }
     __syncwarp();
     if (ok)
       bulk_load(smem_u32(buf + lane * S::ROWP),
-                summ + (static_cast<size_t>(page) * Hkv + c.kvh) * 2 * D, S::ROWB, b);
-    if (with_q && lane == 0)
-      bulk_load(smem_u32(buf + S::CH * S::ROWP),
-                q + (static_cast<size_t>(c.b) * Hq + c.kvh * G) * D, G * D * 2, b);
-    return okm;
+                summ + (static_cast<size_t>(page) * Hkv + c.kvh) * 2 * D, S::ROWB, bb);
   };
 
   uint32_t bneg[S::NG][S::KSQ][2], bpos[S::NG][S::KSQ][2];   // B fragments of q-, q+
-  ScoreChunk cur, nxt;
-  bool have = take(cur);
-  // per stage (held in scalars so that nothing is indexed by the runtime stage):
-  // valid-row masks, and bits 0/1 phase, 2/3 copies pending, 4/5 new query rows
-  unsigned okm0 = 0u, okm1 = 0u;
-  uint32_t flags = 0u;
-  int last_pair = -1;
-  if (have) {
-    okm0 = issue(cur, 0, true);
-    flags |= (1u << 2) | (1u << 4);
-    last_pair = cur.b * Hkv + cur.kvh;
+  int issued = 0;
+  {
+    ScoreChunk c;
+    while (issued < ST && take(c)) issue(c, issued++);
   }
-  int st = 0;
-  while (have) {
-    const int ot = st ^ 1;
-    const bool have_n = take(nxt);
-    if (have_n) {                                  // prefetch the next chunk
-      const int pr = nxt.b * Hkv + nxt.kvh;
-      const bool nq = pr != last_pair;
-      const unsigned m = issue(nxt, ot, nq);
-      if (ot) okm1 = m; else okm0 = m;
-      flags = (flags & ~(1u << (4 + ot))) | (1u << (2 + ot)) | (nq ? 1u << (4 + ot) : 0u);
-      last_pair = pr;
-    }
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar[st]), (flags >> st) & 1u))) {
+  int frag_pair = -1;
+  for (int k = 0; k < issued; ++k) {
+    const int st = k % ST;
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar[st]), (k / ST) & 1))) {
       if (lane == 0) set_err(err, PA_DEVERR_TIMEOUT);
-      if (flags & (1u << (2 + ot))) mbar_wait(smem_u32(&bar[ot]), (flags >> ot) & 1u);
+      for (int j = k; j < issued && j < k + ST; ++j)   // copies still in flight
+        mbar_wait(smem_u32(&bar[j % ST]), (j / ST) & 1);
       return;
     }
-    flags ^= 1u << st;                             // phase
-    flags &= ~(1u << (2 + st));                    // nothing pending
-    const unsigned okm_cur = st ? okm1 : okm0;
+    const int4 cd = desc[st];
+    const unsigned okm_cur = okms[st];
     const uint8_t *buf = stage + st * S::BUF;
-    if (flags & (1u << (4 + st))) {                                // B fragments: q rows n, k pairs of the
-#pragma unroll                                     // chunk's channels, split by sign
-      for (int nt = 0; nt < S::NG; ++nt)
+    if (cd.x * Hkv + cd.y != frag_pair) {          // a new unit: B fragments from q rows,
+      frag_pair = cd.x * Hkv + cd.y;               // k pairs of the channels split by sign
+      const uint16_t *qr = qrows(cd.x, cd.y);
 #pragma unroll
-        for (int kq = 0; kq < S::KSQ; kq += 2) {
-          uint32_t r[4];
-          ldsm_x4(r, smem_u32(buf + S::CH * S::ROWP + (nt * 8 + (lane & 7)) * D * 2 +
-                              (2 * kq + (lane >> 3)) * 16));
+      for (int nt = 0; nt < S::NG; ++nt) {
+        const int g = nt * 8 + (lane >> 2);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t neg = ((r[i] >> 15) & 0x00010001u) * 0xFFFFu;   // halves with q < 0
-            bneg[nt][kq + (i >> 1)][i & 1] = r[i] & neg;
-            bpos[nt][kq + (i >> 1)][i & 1] = r[i] & ~neg;
+        for (int kk = 0; kk < S::KSQ; ++kk)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t v =
+                g < G ? __ldg(reinterpret_cast<const uint32_t *>(qr + g * D + 16 * kk + 8 * j +
+                                                                 2 * (lane & 3)))
+                      : 0u;
+            const uint32_t neg = ((v >> 15) & 0x00010001u) * 0xFFFFu;   // halves with q < 0
+            bneg[nt][kk][j] = v & neg;
+            bpos[nt][kk][j] = v & ~neg;
           }
-        }
+      }
     }
     float acc[S::NG][2][4];
 #pragma unroll
@@ -341,21 +351,20 @@ __global__ void __launch_bounds__(S::THREADS) quest_score_kernel(
       best[h] = fmaxf(best[h], __shfl_xor_sync(0xffffffffu, best[h], 2));
     }
     if ((lane & 3) == 0) {
-      float *out = scores + (static_cast<size_t>(cur.b) * Hkv + cur.kvh) * max_pages + cur.j0;
+      float *out = scores + (static_cast<size_t>(cd.x) * Hkv + cd.y) * max_pages + cd.z;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int r = (lane >> 2) + 8 * h;
-        if (r < cur.n) {
+        if (r < cd.w) {
           const bool ok = (okm_cur >> r) & 1u;
           if (!ok) set_err(err, PA_DEVERR_BLOCK_ID);
           out[r] = ok ? best[h] : -INFINITY;
         }
       }
     }
-    __syncwarp();
-    cur = nxt;
-    have = have_n;
-    st ^= 1;
+    __syncwarp();                                  // the stage and its record are consumed
+    ScoreChunk c;
+    if (issued < k + 1 + ST && take(c)) issue(c, issued++ % ST);
   }
 }
 
@@ -364,13 +373,15 @@ constexpr int kTopkThreads = 512;
 // Top-k of one (sequence, KV head) per CTA: the topk best pages by score (ties to
 // the lower page index), written in increasing page order to sel[b][kvh][0..topk),
 // -1 past the number of pages.  Radix select of the topk-th largest order key, eight
-// bits a pass from the top, then an ordered compaction by warp ballots.
+// bits a pass from the top (two histograms, so that clearing the next one costs no
+// barrier), then one ordered compaction: each thread owns a contiguous run of pages,
+// and a block-wide scan of its (above, equal) counts places its chosen pages.
 __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
     const float *scores, const int32_t *seq_lens, int Hkv, int cap, int max_pages, int topk,
     int32_t *sel) {
   extern __shared__ uint32_t key[];              // [npg] order keys of the page scores
-  __shared__ int hist[256];
-  __shared__ int warp_cnt[2][kTopkThreads / 32];
+  __shared__ int hist[2][256];
+  __shared__ unsigned long long warp_tot[kTopkThreads / 32];
   __shared__ uint32_t s_prefix;
   __shared__ int s_kleft;
   pdl_trigger();
@@ -387,17 +398,21 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
   pdl_wait();
   const float *sc = scores + static_cast<size_t>(pair) * max_pages;
   for (int j = tid; j < npg; j += kTopkThreads) key[j] = order_key(sc[j]);
+  for (int i = tid; i < 256; i += kTopkThreads) hist[0][i] = 0;
   if (tid == 0) {
     s_prefix = 0u;
     s_kleft = topk;
   }
+  __syncthreads();
   uint32_t mask = 0u;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    int *h = hist[pass & 1];
     const uint32_t prefix = s_prefix;
     for (int j = tid; j < npg; j += kTopkThreads)
-      if ((key[j] & mask) == prefix) atomicAdd(&hist[(key[j] >> shift) & 0xFF], 1);
+      if ((key[j] & mask) == prefix) atomicAdd(&h[(key[j] >> shift) & 0xFF], 1);
+    // the other histogram was last read by warp 0 in the pass before: clear it for the next
+    for (int i = tid; i < 256; i += kTopkThreads) hist[(pass + 1) & 1][i] = 0;
     __syncthreads();
     if (warp == 0) {
       // the highest bin whose count from the top reaches kleft: lane l holds bins
@@ -406,7 +421,7 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
       int c[8], mine = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        c[i] = hist[lane * 8 + i];
+        c[i] = h[lane * 8 + i];
         mine += c[i];
       }
       int suf = mine;                            // sum over lanes >= lane
@@ -431,36 +446,42 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
   // threshold T: every key > T and the first s_kleft keys == T (lowest pages)
   const uint32_t T = s_prefix;
   const int take_equal = s_kleft;
-  int count = 0, eq_seen = 0;                    // identical in every thread
-  for (int base = 0; base < npg; base += kTopkThreads) {
-    const int j = base + tid;
-    const bool gt = j < npg && key[j] > T, eq = j < npg && key[j] == T;
-    const unsigned eq_bal = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) warp_cnt[0][warp] = __popc(eq_bal);
-    __syncthreads();
-    int eq_before = eq_seen, eq_chunk = 0;
+  const int per = (npg + kTopkThreads - 1) / kTopkThreads;
+  const int j0 = min(npg, tid * per), j1 = min(npg, j0 + per);
+  int gt = 0, eq = 0;
+  for (int j = j0; j < j1; ++j) {
+    gt += key[j] > T;
+    eq += key[j] == T;
+  }
+  // exclusive block scan of (eq, gt) packed as the high and low halves of 64 bits
+  const unsigned long long mineq = (static_cast<unsigned long long>(eq) << 32) | static_cast<unsigned>(gt);
+  unsigned long long inc = mineq;
 #pragma unroll
-    for (int w = 0; w < kTopkThreads / 32; ++w) {
-      const int v = warp_cnt[0][w];
-      eq_before += w < warp ? v : 0;
-      eq_chunk += v;
-    }
-    eq_before += __popc(eq_bal & ((1u << lane) - 1u));
-    const bool take = gt || (eq && eq_before < take_equal);
-    const unsigned tk_bal = __ballot_sync(0xffffffffu, take);
-    if (lane == 0) warp_cnt[1][warp] = __popc(tk_bal);
-    __syncthreads();
-    int pos = count, chunk = 0;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long t = lane < kTopkThreads / 32 ? warp_tot[lane] : 0ull;
+    const unsigned long long own = t;
 #pragma unroll
-    for (int w = 0; w < kTopkThreads / 32; ++w) {
-      const int v = warp_cnt[1][w];
-      pos += w < warp ? v : 0;
-      chunk += v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long v = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += v;
     }
-    if (take) out[pos + __popc(tk_bal & ((1u << lane) - 1u))] = j;
-    count += chunk;
-    eq_seen += eq_chunk;
-    __syncthreads();                             // warp_cnt is rewritten next chunk
+    if (lane < kTopkThreads / 32) warp_tot[lane] = t - own;
+  }
+  __syncthreads();
+  const unsigned long long before = warp_tot[warp] + inc - mineq;
+  const int gt_before = static_cast<int>(before & 0xFFFFFFFFull);
+  int eq_seen = static_cast<int>(before >> 32);
+  // equal keys are taken in page order until take_equal of them are in
+  int pos = gt_before + min(eq_seen, take_equal);
+  for (int j = j0; j < j1; ++j) {
+    const uint32_t k = key[j];
+    if (k > T || (k == T && eq_seen++ < take_equal)) out[pos++] = j;
   }
 }
 
@@ -500,7 +521,9 @@ static cudaError_t launch_score(const pa_shape &s, int sms, const void *q, const
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int grid = 2 * sms;                       // two CTAs per SM
+  // as many CTAs per SM as shared memory holds (227 KB usable, 1 KB reserved per CTA)
+  const int per_sm = std::max(1, std::min(4, static_cast<int>((227 * 1024) / (smem + 1024))));
+  const int grid = per_sm * sms;
   return launch_pdl(quest_score_kernel<S>, dim3(grid), dim3(S::THREADS), smem, stream,
                     static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(summaries),
                     block_tables, seq_lens, s.B, s.Hq, s.Hkv, s.block_size, s.nblocks,
