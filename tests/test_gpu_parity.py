@@ -265,6 +265,24 @@ def test_fuzz_configurations(case):
         assert_close(run_gpu(dev, mode, ns, window), ref, batch, f"{label} {mode} {ns}")
     assert dev.read_err() == 0
 
+@pytest.mark.parametrize("kv,D,G", [("bf16", 64, 1), ("fp8_e4m3", 128, 1), ("int4", 128, 8)])
+def test_largest_kv_head_count(kv, D, G):
+    """Hkv = 2048, the most the decode's tile records can name (the KV head sits in 11
+    bits): ragged lengths through the cache write and every decode path.  The 4-bit case
+    reads its heads in pairs (G = 8), so its unit view has 1024 KV heads of 16 query rows."""
+    lens = [1, 17, 40]
+    batch = wl.build_batch("max_hkv", lens, Hq=G * 2048, Hkv=2048, D=D, block_size=16, seed=77,
+                           kv_dtype=kv, max_blocks=4)
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch)
+    for mode, ns in [("decode", None), ("decode_ws", None), ("split", 5), ("split", "default")]:
+        if ns == "default":
+            ns = default_num_splits(dev.shape)
+        assert_close(run_gpu(dev, mode, ns), ref, batch, f"Hkv=2048 {kv} {mode} {ns}")
+    assert dev.read_err() == 0
+
+
 def test_fp8_small_all_modes():
     batch = wl.build_batch("t", [1, 16, 17, 200, 33, 0, 1000], Hq=64, Hkv=8, D=128, block_size=16,
                            seed=21, kv_dtype="fp8_e4m3")
