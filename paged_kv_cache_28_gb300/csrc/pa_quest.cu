@@ -15,6 +15,11 @@
 
 namespace pa {
 
+// Pull the 128-byte line holding `p` into L2 (a hint: no data comes back).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Summaries [pages, Hkv, 2 (min, max), D] bf16, for the pages the listed slots were
 // written to: min/max over the page's rows 0 .. slot % 16.  When several listed
 // slots fall in one page only the last of them (largest slot, then largest index)
