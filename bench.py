@@ -39,12 +39,12 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_530_560 + 2_071_552, "kernel_hash": "d079e65729300462"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_732_160 + 2_910_976, "kernel_hash": "d079e65729300462"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_249_600 + 2_041_856, "kernel_hash": "d079e65729300462"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_476_608 + 20_132_352, "kernel_hash": "d079e65729300462"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_261_120 + 15_911_680, "kernel_hash": "d079e65729300462"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_563_968 + 16_166_144, "kernel_hash": "d079e65729300462"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_536_448 + 2_179_584, "kernel_hash": "f61cedbb60351bb0"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_727_552 + 2_932_480, "kernel_hash": "f61cedbb60351bb0"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_233_728 + 2_018_816, "kernel_hash": "f61cedbb60351bb0"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_360_640 + 20_046_592, "kernel_hash": "f61cedbb60351bb0"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_120_832 + 15_784_960, "kernel_hash": "f61cedbb60351bb0"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_674_560 + 16_124_416, "kernel_hash": "f61cedbb60351bb0"},
 }
 
 

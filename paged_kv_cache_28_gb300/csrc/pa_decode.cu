@@ -1612,7 +1612,10 @@ pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int nu
   const WorkspaceLayout w = splitkv_layout(s, num_splits);
   const uint8_t *ws = static_cast<const uint8_t *>(workspace);
   const int G = s.Hq / s.Hkv;
-  const int threads = min(256, max(32, ((G * s.D / 4) + 31) / 32 * 32));
+  // a CTA per (sequence, KV head); with thousands of them (large batches, where most
+  // units finished inside one segment and exit at once) smaller CTAs keep more resident
+  const int cap = s.B * s.Hkv >= 2048 ? 128 : 256;
+  const int threads = min(cap, max(32, ((G * s.D / 4) + 31) / 32 * 32));
   return launch_pdl(merge_kernel, dim3(s.B * s.Hkv), dim3(threads), 0, stream, out,
                     reinterpret_cast<const int32_t *>(ws + w.prefix),
                     reinterpret_cast<const float *>(ws + w.o_part),
