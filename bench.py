@@ -273,7 +273,8 @@ def run_ours(args):
         if call == "decode":
             _lib.pa_decode(dev.shape, dev.out, dev.q, dev.k_pool, dev.v_pool, dev.k_scale,
                            dev.v_scale, dev.block_tables, dev.seq_lens, batch.sm_scale, dev.err,
-                           st, args.window, dev.selected_pages if quest else None)
+                           st, args.window, dev.selected_pages if quest else None,
+                           shared_prefix_lens=dev.shared_prefix_lens)
             if i is not None:
                 ev[i][1].record(st)
             return

@@ -122,10 +122,10 @@ typedef struct {
  *     increasing order, as pa_quest_select writes them (page j = tokens
  *     [16 j, min(16 j + 16, L))).  An index outside the sequence sets
  *     PA_DEVERR_BLOCK_ID and reads zeros.  Not combined with window.
- *   shared_prefix_lens: pa_decode_splitkv, and pa_decode given a workspace (it
- *     runs the split decode); pa_decode without one ignores it.  Optional
- *     [B] int32 device array, a speed hint for batches with prefix sharing
- *     ("appendonly", "Prefix sharing is where the real win lives"): the number
+ *   shared_prefix_lens: pa_decode (with or without a workspace) and
+ *     pa_decode_splitkv.  Optional [B] int32 device array, a speed hint for
+ *     batches with prefix sharing ("appendonly", "Prefix sharing is where the
+ *     real win lives"): the number
  *     of leading tokens of sequence b that lie in blocks other sequences of the
  *     batch also reference.  Whole 16-token tiles inside that prefix are
  *     fetched with an L2 evict-last policy, all other tiles evict-first, so a
@@ -156,8 +156,13 @@ typedef struct {
  *     256-byte aligned; n = num_splits, or pa_default_num_splits for this GPU
  *     when num_splits is 0) pa_decode runs the split decode and the merge
  *     itself: one call, load-balanced however the lengths are spread.  Without
- *     one it uses one CTA per (sequence, KV head), which needs no memory but is
- *     held back by the longest sequence.
+ *     one it needs no memory: one CTA per (sequence, KV head) unit, or, when the
+ *     batch has at most two units per CTA the GPU holds at once, a cluster of
+ *     four CTAs per unit that share its tiles (at least 16 per warp; a short
+ *     unit leaves the extra CTAs idle) and merge through distributed shared
+ *     memory.  Batches of up to 256 sequences start their longest sequences
+ *     first.  A batch whose longest sequence outweighs the rest is still held
+ *     back by it; the split decode is not.
  */
 typedef struct {
     int32_t window;
@@ -212,9 +217,10 @@ pa_status pa_reshape_and_cache(const pa_shape *shape, const void *k_new, const v
  */
 
 /*
- * pa_decode -- single-token decode attention over the paged cache: one CTA per
- * (sequence, KV head) serving the whole query group, or, with a workspace in
- * opts, the split decode and the merge in one call.
+ * pa_decode -- single-token decode attention over the paged cache: one CTA (or,
+ * for batches of few units, a cluster of CTAs) per (sequence, KV head) serving
+ * the whole query group, or, with a workspace in opts, the split decode and the
+ * merge in one call.
  * [P4] "Custom PagedAttention Kernels" (grid over sequence and head, block-table
  * walk, block staged in shared memory); [P3] section 1 (GQA grouping).
  *     out[b][h][:] = sum_t softmax_t(sm_scale * <q[b][h], K_b[t]>) V_b[t]

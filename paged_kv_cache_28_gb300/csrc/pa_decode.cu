@@ -96,7 +96,8 @@ struct Cfg {
   // pa_decode's CTA merges its warps' accumulators in the stage area; their m and l go
   // after every per-warp area (mbarrier memory is never reused)
   static_assert(WARPS * 8 * NT * D * 4 <= WARPS * STAGES * STAGE_BYTES, "pair merge must fit");
-  static constexpr int PAIR_SMEM = SMEM + 2 * WARPS * 8 * NT * 4;
+  // after them: the CTA's folded m and l (cluster launches) and one cluster mbarrier
+  static constexpr int PAIR_SMEM = SMEM + (2 * WARPS + 2) * 8 * NT * 4 + 16;
 };
 
 struct Params {
@@ -106,7 +107,7 @@ struct Params {
   const float *v_scale;
   const int32_t *block_tables;
   const int32_t *seq_lens;
-  const int32_t *shared_prefix_lens;   // optional L2 hint per sequence (split kernel)
+  const int32_t *shared_prefix_lens;   // optional L2 hint per sequence
   int window;                          // > 0: attend over the last `window` positions only
   int topk;                            // > 0: attend over the pages listed in sel only
   const int32_t *sel;                  // [B, Hkv, topk] chosen 16-token pages (ascending)
@@ -691,6 +692,7 @@ struct PairSource {
   int pair, kvh, hkv, w, nw, bs, nblocks;
   SeqTiles geo;         // with a selection: count = pages chosen, first = 0
   int npages;           // 16-token pages of the sequence
+  int shared_len;       // L2 hint: leading tokens in shared blocks, or -1 (no hint)
   int base;
   int4 cur, nxt;
 
@@ -720,6 +722,7 @@ struct PairSource {
     if (j == geo.count - 1) info |= kLastOfPair;
     if (i == 0) info |= kPieceStart;
     if (j + nw >= geo.count) info |= kPieceEnd;
+    if (shared_len >= 0) info |= ((tile + 1) * kTile <= shared_len) ? kHintShared : kHintPrivate;
     return tile_record(phys, tile, pair, kvh, hkv, bs, nblocks, info | (kvh << kKvhShift));
   }
   __device__ __forceinline__ void init(int lane) {
@@ -1002,15 +1005,103 @@ __host__ __device__ constexpr int split_smem(int B) {
 }
 
 // ----------------------------------------------------------------------------
-// pa_decode: one CTA per (sequence, KV head)
+// pa_decode: one CTA per (sequence, KV head), or a cluster of CTAs per unit
 // ----------------------------------------------------------------------------
 
-template <class C>
+// Thread-block clusters.  When a batch has few (sequence, KV head) units, pa_decode
+// launches clusters of CTAs, one cluster per unit: the cluster's CTAs share the unit's
+// tiles and CTA 0 merges their states through distributed shared memory.
+__device__ __forceinline__ int cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return static_cast<int>(r);
+}
+__device__ __forceinline__ int cluster_ctas() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return static_cast<int>(r);
+}
+// Every thread of every CTA of the cluster arrives, then waits for all the others.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// The shared::cluster address of `addr` (this CTA's shared memory) in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Arrive on an mbarrier in another CTA of the cluster, releasing this thread's prior
+// writes (and those ordered before them by a CTA barrier) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// Bounded wait with acquire at cluster scope; false if the phase never completed.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kWaitSpins; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// Fewest tiles a warp takes when a cluster shares a unit: a unit of n tiles keeps
+// ceil(n / (kClusterWarpTiles * WARPS)) of the cluster's CTAs (at least one, at most
+// all); the others leave at once.
+constexpr int kClusterWarpTiles = 16;
+// Batches up to this many sequences are served longest first (the ordering costs
+// O(B^2 / threads) per CTA).
+constexpr int kLongestFirstMaxB = 256;
+
+// Unit slot c (a CTA, or a cluster) serves the sequence of rank c / Hkv when the
+// sequences are ordered by attended tiles, most first (ties by index), so that the
+// longest units start first and do not end the launch alone.  counts: shared
+// scratch of B + 1 ints, free again on return.
+__device__ int longest_first(const Params &p, int pair, int *counts) {
+  const int cap = p.max_blocks * p.bs;
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x)
+    counts[b] = pair_tile_count(min(max(__ldg(p.seq_lens + b), 0), cap), p.window, p.topk);
+  __syncthreads();
+  const int want = pair / p.Hkv;
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    const int cb = counts[b];
+    int rank = 0;
+    for (int j = 0; j < p.B; ++j) {
+      const int cj = counts[j];
+      rank += (cj > cb) || (cj == cb && j < b);
+    }
+    if (rank == want) counts[p.B] = b;   // ranks are a permutation: exactly one writer
+  }
+  __syncthreads();
+  const int seq = counts[p.B];
+  __syncthreads();   // every thread has read it before the stages are filled
+  return seq * p.Hkv + (pair - want * p.Hkv);
+}
+
+// CLUSTER: launched in clusters, one per unit (else one CTA per unit).
+template <class C, bool CLUSTER>
 __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  const int pair = blockIdx.x;
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const int ncl = CLUSTER ? cluster_ctas() : 1, crank = CLUSTER ? cluster_rank() : 0;
+  int pair = blockIdx.x / ncl;
+  if (p.B <= kLongestFirstMaxB) pair = longest_first(p, pair, reinterpret_cast<int *>(base));
   const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int L = p.seq_lens[b];
@@ -1030,14 +1121,34 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.hkv = p.Hkv;
   src.geo = seq_tiles(L, p.window);
   src.npages = (L + kTile - 1) / kTile;
+  src.shared_len = p.shared_prefix_lens ? __ldg(p.shared_prefix_lens + b) : -1;
   src.sel = nullptr;
   if (p.sel) {
     src.sel = p.sel + static_cast<size_t>(pair) * p.topk;
     src.geo.first = 0;
     src.geo.count = pair_tile_count(L, 0, p.topk);
   }
-  src.w = warp;
-  src.nw = C::WARPS;
+  constexpr int GP = 8 * C::NT;
+  float *sm_acc = reinterpret_cast<float *>(base);               // [WARPS][GP][D], stage area
+  float *sm_m = reinterpret_cast<float *>(split_tail<C>(smem_raw));   // [WARPS][GP]
+  float *sm_l = sm_m + C::WARPS * GP;                            // [WARPS][GP]
+  float *cta_m = sm_l + C::WARPS * GP;                           // [GP] folded over warps
+  float *cta_l = cta_m + GP;                                     // [GP]
+  const uint32_t cl_bar = smem_u32(cta_l + GP);                  // cluster mbarrier
+  // A cluster shares the unit's tiles among its first `active` CTAs; the others leave.
+  int active = 1;
+  if (ncl > 1) {
+    const int per_cta = kClusterWarpTiles * C::WARPS;
+    active = min(ncl, max(1, (src.geo.count + per_cta - 1) / per_cta));
+    if (threadIdx.x == 0) {   // CTA 0 hears from the other active CTAs, each of them from CTA 0
+      mbar_init(cl_bar, crank == 0 ? max(active - 1, 1) : 1);
+      fence_mbar_init();
+    }
+    cluster_barrier();   // every CTA's cluster mbarrier is initialised
+    if (crank >= active) return;
+  }
+  src.w = crank * C::WARPS + warp;
+  src.nw = active * C::WARPS;
   src.bs = p.bs;
   src.nblocks = p.nblocks;
   src.init(lane);
@@ -1045,12 +1156,6 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 
   // ---- merge the warps' states: warp w leaves m, l, acc (in absolute units)
   __syncthreads();
-  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
-  constexpr int GP = 8 * C::NT;
-  float *sm_acc = reinterpret_cast<float *>(base);               // [WARPS][GP][D], stage area
-  float *sm_m = reinterpret_cast<float *>(split_tail<C>(smem_raw));   // [WARPS][GP]
-  float *sm_l = sm_m + C::WARPS * GP;                            // [WARPS][GP]
   {
     float ltot[C::NT][2];
     reduce_l<C>(st, ltot);
@@ -1090,8 +1195,54 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         den += f * sm_l[w * GP + g];
       }
     }
+    if (ncl == 1) {
+      out[e] = den > 0.f ? num / den : 0.f;
+    } else {   // this CTA's state, relative to its own maximum M, for CTA 0 to merge
+      sm_acc[g * C::D + d] = num;   // warp 0's entry (g, d): no other thread touches it
+      if (d == 0) {
+        cta_m[g] = M;
+        cta_l[g] = den;
+      }
+    }
+  }
+  if (ncl == 1) return;
+
+  // ---- cluster: CTA 0 merges the active CTAs' states through distributed shared memory
+  __syncthreads();
+  if (crank > 0) {
+    if (threadIdx.x == 0) mbar_arrive_cluster(cluster_map(cl_bar, 0));
+    // stay until CTA 0 has read this CTA's shared memory
+    if (!mbar_wait_cluster(cl_bar, 0) && threadIdx.x == 0) set_err(p.err, PA_DEVERR_TIMEOUT);
+    return;
+  }
+  if (active > 1 && !mbar_wait_cluster(cl_bar, 0) && threadIdx.x == 0)
+    set_err(p.err, PA_DEVERR_TIMEOUT);
+  constexpr int kMaxCluster = 8;
+  for (int e = threadIdx.x; e < p.G * C::D; e += C::THREADS) {
+    const int g = e / C::D, d = e - g * C::D;
+    const uint32_t am = smem_u32(&cta_m[g]), al = smem_u32(&cta_l[g]);
+    const uint32_t aa = smem_u32(&sm_acc[g * C::D + d]);
+    float mc[kMaxCluster];
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+      mc[c] = c < active ? ld_cluster_f32(cluster_map(am, c)) : -INFINITY;
+      M = fmaxf(M, mc[c]);
+    }
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) {
+        if (mc[c] == -INFINITY) continue;
+        const float f = ex2(mc[c] - M);
+        num += f * ld_cluster_f32(cluster_map(aa, c));
+        den += f * ld_cluster_f32(cluster_map(al, c));
+      }
+    }
     out[e] = den > 0.f ? num / den : 0.f;
   }
+  __syncthreads();   // every read of the other CTAs' shared memory is done: release them
+  if (threadIdx.x > 0 && threadIdx.x < active) mbar_arrive_cluster(cluster_map(cl_bar, threadIdx.x));
 }
 
 // ----------------------------------------------------------------------------
@@ -1403,12 +1554,44 @@ static Params make_params(const pa_shape &s, float *out, const void *q, const fl
   return p;
 }
 
+// CTAs per (sequence, KV head) unit in pa_decode.  With at most two units per resident
+// CTA, one long sequence would be left to a single CTA at the end of the launch: such
+// batches get a cluster of four CTAs per unit (of which a short unit keeps only as
+// many as it has tiles for).  Larger batches keep one CTA per unit.
+static int pair_cluster_ctas(int units, int resident_ctas) {
+  return units <= 2 * resident_ctas ? 4 : 1;
+}
+
 template <class C>
 static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
                              cudaStream_t stream) {
-  if (prep_kernel(decode_pair_kernel<C>, C::PAIR_SMEM) != cudaSuccess) return PA_ERR_CUDA;
-  decode_pair_kernel<C><<<p.B * p.Hkv, C::THREADS, C::PAIR_SMEM, stream>>>(mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const int units = p.B * p.Hkv;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PA_ERR_CUDA;
+  const int ncl = pair_cluster_ctas(units, sms * C::MIN_BLOCKS);
+  if (ncl == 1) {
+    if (prep_kernel(decode_pair_kernel<C, false>, C::PAIR_SMEM) != cudaSuccess) return PA_ERR_CUDA;
+    decode_pair_kernel<C, false><<<units, C::THREADS, C::PAIR_SMEM, stream>>>(mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
+  if (prep_kernel(decode_pair_kernel<C, true>, C::PAIR_SMEM) != cudaSuccess) return PA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(units * ncl);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::PAIR_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ncl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_pair_kernel<C, true>, mk, mv, p) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 template <class C>
@@ -1529,6 +1712,7 @@ pa_status run_decode(const pa_shape &s, float *out, const void *q, const void *k
   if (!make_pool_map(&mk, k_pool, v, heads) || !make_pool_map(&mv, v_pool, v, heads))
     return PA_ERR_CUDA;
   Params p = make_params(v, out, q, k_scale, v_scale, bt, sl, opts, sm_scale, err);
+  p.shared_prefix_lens = opts ? opts->shared_prefix_lens : nullptr;
   return dispatch_pair(v, heads, p, mk, mv, stream);
 }
 

@@ -64,16 +64,18 @@ class DeviceBatch:
                                   stream)
 
     def decode(self, stream=None, window: int = 0, selected_pages=None,
-               workspace: bool = False):
+               workspace: bool = False, hints: bool = False):
         """pa_decode; workspace: hand it a split workspace (the default split count), so
-        that it runs the split decode and the merge itself."""
+        that it runs the split decode and the merge itself; hints: pass the batch's
+        shared-prefix lengths (if any)."""
         ws = None
         if workspace:
             self.ensure_workspace(default_num_splits(self.shape, self.device))
             ws = self.workspace
         _lib.pa_decode(self.shape, self.out, self.q, self.k_pool, self.v_pool, self.k_scale,
                        self.v_scale, self.block_tables, self.seq_lens, self.batch.sm_scale,
-                       self.err, stream, window, selected_pages, ws)
+                       self.err, stream, window, selected_pages, ws,
+                       shared_prefix_lens=self.shared_prefix_lens if hints else None)
 
     def ensure_workspace(self, num_splits: int):
         nbytes = _lib.pa_splitkv_workspace_bytes(self.shape, num_splits)

@@ -283,6 +283,29 @@ def test_largest_kv_head_count(kv, D, G):
     assert dev.read_err() == 0
 
 
+@pytest.mark.parametrize("kv_dtype,Hq,Hkv,bs", [("bf16", 64, 8, 16), ("bf16", 32, 2, 32),
+                                                  ("bf16", 16, 1, 16), ("fp8_e4m3", 64, 8, 16),
+                                                  ("int4", 64, 8, 16), ("int4", 16, 2, 32)])
+def test_pa_decode_cluster_split_skewed(kv_dtype, Hq, Hkv, bs):
+    """pa_decode without a workspace on a small, skewed batch.  With few (sequence, KV
+    head) units each is served by a cluster of CTAs: a long sequence's tiles spread over
+    all of them and CTA 0 merges their states through distributed shared memory; a short
+    one keeps CTA 0 alone and the others leave.  Clusters take the sequences longest
+    first.  Windows shorten the long sequences' tile lists."""
+    lens = [5000, 1, 17, 300, 0, 1025, 64, 3333]
+    batch = wl.build_batch("cl", lens, Hq=Hq, Hkv=Hkv, D=128, block_size=bs, seed=77,
+                           kv_dtype=kv_dtype)
+    dev = DeviceBatch(batch)
+    ref, _ = oracle_after_write(batch, write=False)
+    out = run_gpu(dev, "decode")
+    assert_close(out, ref, batch, "cluster decode")
+    for w in (1, 100, 2000):
+        ref_w, _ = oracle_after_write(batch, write=False, window=w)
+        assert_close(run_gpu(dev, "decode", window=w), ref_w, batch, f"cluster decode window {w}")
+    assert np.array_equal(_bits(run_gpu(dev, "decode")), _bits(out)), "not repeatable"
+    assert dev.read_err() == 0
+
+
 def test_fp8_small_all_modes():
     batch = wl.build_batch("t", [1, 16, 17, 200, 33, 0, 1000], Hq=64, Hkv=8, D=128, block_size=16,
                            seed=21, kv_dtype="fp8_e4m3")
@@ -693,6 +716,15 @@ def test_shared_prefix_hint_changes_nothing_bitwise():
     dev.decode_splitkv(23)
     torch.cuda.synchronize()
     assert np.array_equal(_bits(dev.out.cpu().numpy()), _bits(outs[0]))
+    # pa_decode without a workspace (one CTA per sequence and KV head) takes the hint too
+    pair = []
+    for hints in (False, True):
+        dev.out.fill_(float("nan"))
+        dev.decode(hints=hints)
+        torch.cuda.synchronize()
+        pair.append(dev.out.cpu().numpy())
+        assert_close(pair[-1], ref, batch, f"pa_decode hints={hints}")
+    assert np.array_equal(_bits(pair[0]), _bits(pair[1]))
     assert dev.read_err() == 0
 
 
@@ -1090,9 +1122,10 @@ def test_step_captured_in_cuda_graph(mode):
                                   "int4_mixed", "code_assistant_turns"])
 def test_full_size_config_sampled(name):
     """The bench's launch configurations at full size (split-KV at the default
-    num_splits; for FP8 also pa_decode, the call its workload names); every head of the
-    longest, shortest and three random sequences plus 192 random (b, h) rows are
-    compared with the oracle."""
+    num_splits) and pa_decode without a workspace (the call the FP8 workload names; a
+    cluster of CTAs per unit on the 70B and long-context batches, longest sequences
+    first on the prefix batch); every head of the longest, shortest and three random
+    sequences plus 192 random (b, h) rows are compared with the oracle."""
     batch = wl.make(name)
     dev = DeviceBatch(batch)
     dev.reshape_and_cache()
@@ -1104,13 +1137,13 @@ def test_full_size_config_sampled(name):
     out_ws = run_gpu(dev, "decode_ws")            # the one-call form of the same path
     assert dev.read_err() == 0
     assert_close(out_ws[rows[:, 0], rows[:, 1]], ref, batch, name + " pa_decode + workspace")
-    if name in ("fp8_mixed", "int4_mixed"):      # pa_decode without a workspace, same rows
-        out2 = run_gpu(dev, "decode")
-        assert dev.read_err() == 0
-        assert_close(out2[rows[:, 0], rows[:, 1]], ref, batch, name + " decode")
-        # its CTAs merge their warps' states through shared memory: a second call must
-        # give the same bits everywhere (a race there shows up as a few stray values)
-        assert np.array_equal(run_gpu(dev, "decode"), out2), name + " decode not repeatable"
+    out2 = run_gpu(dev, "decode")                 # pa_decode without a workspace, same rows
+    assert dev.read_err() == 0
+    assert_close(out2[rows[:, 0], rows[:, 1]], ref, batch, name + " decode")
+    # its CTAs merge their warps' states through shared memory (and a cluster's CTAs
+    # through distributed shared memory): a second call must give the same bits
+    # everywhere (a race there shows up as a few stray values)
+    assert np.array_equal(_bits(run_gpu(dev, "decode")), _bits(out2)), name + " decode not repeatable"
     if name in ("prefix_sharing", "code_assistant_turns"):   # the cascade (bench.py --cascade)
         out3 = _run_cascade(dev, default_num_splits(dev.shape))
         assert dev.read_err() == 0
