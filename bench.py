@@ -39,12 +39,12 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_536_448 + 2_179_584, "kernel_hash": "f61cedbb60351bb0"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_727_552 + 2_932_480, "kernel_hash": "f61cedbb60351bb0"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_233_728 + 2_018_816, "kernel_hash": "f61cedbb60351bb0"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_360_640 + 20_046_592, "kernel_hash": "f61cedbb60351bb0"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_120_832 + 15_784_960, "kernel_hash": "f61cedbb60351bb0"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_674_560 + 16_124_416, "kernel_hash": "f61cedbb60351bb0"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_529_024 + 2_014_720, "kernel_hash": "31bb1e2df53193f5"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_188_608 + 3_005_952, "kernel_hash": "31bb1e2df53193f5"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_612_352 + 2_729_216, "kernel_hash": "31bb1e2df53193f5"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_492_480 + 19_506_944, "kernel_hash": "31bb1e2df53193f5"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_142_080 + 15_558_144, "kernel_hash": "31bb1e2df53193f5"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_562_432 + 16_075_776, "kernel_hash": "31bb1e2df53193f5"},
 }
 
 
