@@ -44,6 +44,7 @@ TRAFFIC = {
     ("long_context", "decode_segment_kernel"): {"bytes": 4_296_612_352 + 2_729_216, "kernel_hash": "31bb1e2df53193f5"},
     ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_492_480 + 19_506_944, "kernel_hash": "31bb1e2df53193f5"},
     ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_142_080 + 15_558_144, "kernel_hash": "31bb1e2df53193f5"},
+    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_570_560 + 1_184_512, "kernel_hash": "31bb1e2df53193f5"},
     ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_562_432 + 16_075_776, "kernel_hash": "31bb1e2df53193f5"},
 }
 
@@ -453,7 +454,7 @@ def run_ours(args):
             "parallelism": f"replicas x{world}" if world > 1 else "single",
             "step": ("pa_reshape_and_cache + "
                      + ("pa_quest_summarize + pa_quest_select + " if args.quest_topk > 0 else "")
-                     + ("pa_decode (one CTA per sequence and KV head)" if call == "decode" else
+                     + ("pa_decode (no workspace: one CTA, or a cluster of CTAs, per sequence and KV head)" if call == "decode" else
                         "pa_decode_splitkv (cascade + split kernels) + pa_merge_lse"
                         if args.cascade else "pa_decode_splitkv + pa_merge_lse")),
         },
@@ -579,7 +580,7 @@ def main(argv=None):
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--call", choices=["auto", "splitkv", "decode"], default="auto",
                     help="the decode entry point of each step: pa_decode_splitkv + pa_merge_lse, "
-                         "or pa_decode without a workspace (one CTA per sequence and KV head); "
+                         "or pa_decode without a workspace (a CTA or a cluster of CTAs per sequence and KV head); "
                          "auto: pa_decode for fp8_mixed, whose workload names that call, "
                          "pa_decode_splitkv otherwise")
     ap.add_argument("--e2e-eager", action="store_true",
