@@ -1571,11 +1571,12 @@ static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUten
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PA_ERR_CUDA;
   const int ncl = pair_cluster_ctas(units, sms * C::MIN_BLOCKS);
-  if (ncl == 1) {
+  auto one_cta_per_unit = [&]() {
     if (prep_kernel(decode_pair_kernel<C, false>, C::PAIR_SMEM) != cudaSuccess) return PA_ERR_CUDA;
     decode_pair_kernel<C, false><<<units, C::THREADS, C::PAIR_SMEM, stream>>>(mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
-  }
+  };
+  if (ncl == 1) return one_cta_per_unit();
   if (prep_kernel(decode_pair_kernel<C, true>, C::PAIR_SMEM) != cudaSuccess) return PA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units * ncl);
@@ -1589,9 +1590,11 @@ static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUten
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_pair_kernel<C, true>, mk, mv, p) == cudaSuccess
-             ? PA_OK
-             : PA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, decode_pair_kernel<C, true>, mk, mv, p) == cudaSuccess) return PA_OK;
+  // a device (or a partition of one) that cannot place the cluster: the same
+  // decode with one CTA per unit (the failed launch left no sticky error)
+  (void)cudaGetLastError();
+  return one_cta_per_unit();
 }
 
 template <class C>
