@@ -39,13 +39,13 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_529_024 + 2_014_720, "kernel_hash": "31bb1e2df53193f5"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_188_608 + 3_005_952, "kernel_hash": "31bb1e2df53193f5"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_612_352 + 2_729_216, "kernel_hash": "31bb1e2df53193f5"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_492_480 + 19_506_944, "kernel_hash": "31bb1e2df53193f5"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_142_080 + 15_558_144, "kernel_hash": "31bb1e2df53193f5"},
-    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_570_560 + 1_184_512, "kernel_hash": "31bb1e2df53193f5"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_562_432 + 16_075_776, "kernel_hash": "31bb1e2df53193f5"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_531_328 + 2_179_584, "kernel_hash": "36f40f7601e914f3"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_073_152 + 3_331_072, "kernel_hash": "36f40f7601e914f3"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_201_984 + 1_786_368, "kernel_hash": "36f40f7601e914f3"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_383_936 + 20_606_720, "kernel_hash": "36f40f7601e914f3"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_141_824 + 15_580_672, "kernel_hash": "36f40f7601e914f3"},
+    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_551_360 + 1_225_472, "kernel_hash": "36f40f7601e914f3"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_549_376 + 16_105_216, "kernel_hash": "36f40f7601e914f3"},
 }
 
 
