@@ -1076,12 +1076,13 @@ def test_cascade_staircase_prefix():
     assert dev.read_err() == 0
 
 
-@pytest.mark.parametrize("mode", ["split", "cascade", "fp8"])
+@pytest.mark.parametrize("mode", ["split", "cascade", "fp8", "decode"])
 def test_step_captured_in_cuda_graph(mode):
     """One decode step (cache write, split decode, merge; with the cascade also its plan,
-    side-stream fork and join) captured into a CUDA graph and replayed: the replay
-    gives the oracle's result.  The step's launches chain by programmatic dependent
-    launch, which the graph keeps."""
+    side-stream fork and join; "decode": pa_decode without a workspace, here a cluster
+    launch) captured into a CUDA graph and replayed: the replay gives the oracle's
+    result.  The step's launches chain by programmatic dependent launch, which the graph
+    keeps."""
     if mode == "fp8":
         batch = wl.build_batch("t", [1, 40, 300, 17], Hq=64, Hkv=8, D=128, block_size=16,
                                seed=111, kv_dtype="fp8_e4m3")
@@ -1097,7 +1098,10 @@ def test_step_captured_in_cuda_graph(mode):
 
     def step():
         dev.reshape_and_cache()
-        dev.decode_splitkv(ns, cascade=(mode == "cascade"))
+        if mode == "decode":
+            dev.decode()
+        else:
+            dev.decode_splitkv(ns, cascade=(mode == "cascade"))
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
