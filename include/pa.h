@@ -160,8 +160,9 @@ typedef struct {
  *     batch has at most two units per CTA the GPU holds at once, a cluster of
  *     four CTAs per unit that share its tiles (at least 16 per warp; a short
  *     unit leaves the extra CTAs idle) and merge through distributed shared
- *     memory.  Batches of up to 256 sequences start their longest sequences
- *     first.  A batch whose longest sequence outweighs the rest is still held
+ *     memory; a window or topk that bounds every unit keeps one CTA per unit
+ *     when the units fill the GPU or fit one CTA.  Batches of up to 256
+ *     sequences start their longest sequences first.  A batch whose longest sequence outweighs the rest is still held
  *     back by it; the split decode is not.
  */
 typedef struct {

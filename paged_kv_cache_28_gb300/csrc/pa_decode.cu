@@ -1557,9 +1557,18 @@ static Params make_params(const pa_shape &s, float *out, const void *q, const fl
 // CTAs per (sequence, KV head) unit in pa_decode.  With at most two units per resident
 // CTA, one long sequence would be left to a single CTA at the end of the launch: such
 // batches get a cluster of four CTAs per unit (of which a short unit keeps only as
-// many as it has tiles for).  Larger batches keep one CTA per unit.
-static int pair_cluster_ctas(int units, int resident_ctas) {
-  return units <= 2 * resident_ctas ? 4 : 1;
+// many as it has tiles for).  Larger batches keep one CTA per unit.  So do launches
+// whose window or page selection bounds every unit's tiles when the units fill the GPU
+// (bounded units are near-uniform: a cluster would only add CTAs), and launches whose
+// bound is one CTA's share (the cluster's other CTAs would all sit idle).
+template <class C>
+static int pair_cluster_ctas(int units, int resident_ctas, int window, int topk) {
+  if (units > 2 * resident_ctas) return 1;
+  const bool bounded = topk > 0 || window > 0;
+  if (bounded && units >= resident_ctas) return 1;
+  const int share = kClusterWarpTiles * C::WARPS;   // tiles one CTA takes before another joins
+  const int max_tiles = topk > 0 ? topk : (window > 0 ? (window + kTile - 2) / kTile + 1 : 1 << 30);
+  return max_tiles <= share ? 1 : 4;
 }
 
 template <class C>
@@ -1570,7 +1579,7 @@ static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUten
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PA_ERR_CUDA;
-  const int ncl = pair_cluster_ctas(units, sms * C::MIN_BLOCKS);
+  const int ncl = pair_cluster_ctas<C>(units, sms * C::MIN_BLOCKS, p.window, p.topk);
   auto one_cta_per_unit = [&]() {
     if (prep_kernel(decode_pair_kernel<C, false>, C::PAIR_SMEM) != cudaSuccess) return PA_ERR_CUDA;
     decode_pair_kernel<C, false><<<units, C::THREADS, C::PAIR_SMEM, stream>>>(mk, mv, p);
