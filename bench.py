@@ -39,13 +39,13 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_531_328 + 2_179_584, "kernel_hash": "36f40f7601e914f3"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_073_152 + 3_331_072, "kernel_hash": "36f40f7601e914f3"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_201_984 + 1_786_368, "kernel_hash": "36f40f7601e914f3"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_383_936 + 20_606_720, "kernel_hash": "36f40f7601e914f3"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_141_824 + 15_580_672, "kernel_hash": "36f40f7601e914f3"},
-    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_551_360 + 1_225_472, "kernel_hash": "36f40f7601e914f3"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_549_376 + 16_105_216, "kernel_hash": "36f40f7601e914f3"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_519_296 + 2_271_744, "kernel_hash": "0621e6781f8c81cd"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_632_320 + 2_694_656, "kernel_hash": "0621e6781f8c81cd"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_283_904 + 1_697_536, "kernel_hash": "0621e6781f8c81cd"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_423_360 + 20_029_440, "kernel_hash": "0621e6781f8c81cd"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_151_808 + 15_585_280, "kernel_hash": "0621e6781f8c81cd"},
+    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_559_296 + 1_239_808, "kernel_hash": "0621e6781f8c81cd"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_557_824 + 16_058_624, "kernel_hash": "0621e6781f8c81cd"},
 }
 
 
