@@ -39,13 +39,13 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_519_296 + 2_271_744, "kernel_hash": "0621e6781f8c81cd"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_632_320 + 2_694_656, "kernel_hash": "0621e6781f8c81cd"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_283_904 + 1_697_536, "kernel_hash": "0621e6781f8c81cd"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_423_360 + 20_029_440, "kernel_hash": "0621e6781f8c81cd"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_151_808 + 15_585_280, "kernel_hash": "0621e6781f8c81cd"},
-    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_559_296 + 1_239_808, "kernel_hash": "0621e6781f8c81cd"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_557_824 + 16_058_624, "kernel_hash": "0621e6781f8c81cd"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_517_504 + 2_066_176, "kernel_hash": "1743392616c67833"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_059_840 + 3_015_936, "kernel_hash": "1743392616c67833"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_179_456 + 2_199_552, "kernel_hash": "1743392616c67833"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_233_664 + 21_535_488, "kernel_hash": "1743392616c67833"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_152_832 + 15_639_552, "kernel_hash": "1743392616c67833"},
+    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_564_160 + 1_169_408, "kernel_hash": "1743392616c67833"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_574_976 + 16_071_424, "kernel_hash": "1743392616c67833"},
 }
 
 

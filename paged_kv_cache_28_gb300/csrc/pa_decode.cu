@@ -1063,30 +1063,47 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
 // all); the others leave at once.
 constexpr int kClusterWarpTiles = 16;
 // Batches up to this many sequences are served longest first (the ordering costs
-// O(B^2 / threads) per CTA).
+// B^2 / threads key comparisons per CTA).
 constexpr int kLongestFirstMaxB = 256;
 
 // Unit slot c (a CTA, or a cluster) serves the sequence of rank c / Hkv when the
 // sequences are ordered by attended tiles, most first (ties by index), so that the
-// longest units start first and do not end the launch alone.  counts: shared
-// scratch of B + 1 ints, free again on return.
-__device__ int longest_first(const Params &p, int pair, int *counts) {
+// longest units start first and do not end the launch alone.  Each sequence gets one
+// 32-bit key, tiles above its index (larger = earlier, all distinct), and its rank
+// is the number of larger keys: every thread ranks two candidates in one pass over
+// the keys, four at a time.  keys: shared scratch of 4 * (round4(B) + 1) bytes,
+// 16-byte aligned, free again on return.
+__device__ int longest_first(const Params &p, int pair, uint32_t *keys) {
+  static_assert(kLongestFirstMaxB <= 512, "keys hold the sequence index in 9 bits");
   const int cap = p.max_blocks * p.bs;
-  for (int b = threadIdx.x; b < p.B; b += blockDim.x)
-    counts[b] = pair_tile_count(min(max(__ldg(p.seq_lens + b), 0), cap), p.window, p.topk);
-  __syncthreads();
-  const int want = pair / p.Hkv;
-  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const int cb = counts[b];
-    int rank = 0;
-    for (int j = 0; j < p.B; ++j) {
-      const int cj = counts[j];
-      rank += (cj > cb) || (cj == cb && j < b);
+  const int nb4 = (p.B + 3) >> 2;
+  for (int b = threadIdx.x; b < 4 * nb4; b += blockDim.x) {
+    uint32_t key = 0u;   // padding: counted by no rank
+    if (b < p.B) {
+      const int c = pair_tile_count(min(max(__ldg(p.seq_lens + b), 0), cap), p.window, p.topk);
+      key = (static_cast<uint32_t>(min(c, (1 << 23) - 1)) << 9) | static_cast<uint32_t>(511 - b);
     }
-    if (rank == want) counts[p.B] = b;   // ranks are a permutation: exactly one writer
+    keys[b] = key;
   }
   __syncthreads();
-  const int seq = counts[p.B];
+  const int want = pair / p.Hkv;
+  int *chosen = reinterpret_cast<int *>(keys + 4 * nb4);
+  const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
+  for (int b0 = threadIdx.x; b0 < p.B; b0 += 2 * blockDim.x) {
+    const int b1 = b0 + blockDim.x;
+    const uint32_t c0 = keys[b0], c1 = b1 < p.B ? keys[b1] : 0xFFFFFFFFu;
+    int r0 = 0, r1 = 0;
+    for (int j = 0; j < nb4; ++j) {
+      const uint4 k = k4[j];
+      r0 += (k.x > c0) + (k.y > c0) + (k.z > c0) + (k.w > c0);
+      r1 += (k.x > c1) + (k.y > c1) + (k.z > c1) + (k.w > c1);
+    }
+    // ranks are a permutation of 0..B-1: exactly one thread writes
+    if (r0 == want) *chosen = b0;
+    if (b1 < p.B && r1 == want) *chosen = b1;
+  }
+  __syncthreads();
+  const int seq = *chosen;
   __syncthreads();   // every thread has read it before the stages are filled
   return seq * p.Hkv + (pair - want * p.Hkv);
 }
@@ -1101,7 +1118,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
                                               ~static_cast<uintptr_t>(1023));
   const int ncl = CLUSTER ? cluster_ctas() : 1, crank = CLUSTER ? cluster_rank() : 0;
   int pair = blockIdx.x / ncl;
-  if (p.B <= kLongestFirstMaxB) pair = longest_first(p, pair, reinterpret_cast<int *>(base));
+  if (p.B <= kLongestFirstMaxB) pair = longest_first(p, pair, reinterpret_cast<uint32_t *>(base));
   const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int L = p.seq_lens[b];
