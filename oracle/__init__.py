@@ -51,6 +51,14 @@ quest_decode                   textbook attention restricted to the chosen
 split_partials / merge_lse     merge(split(x)) == unsplit(x) to 1e-12 for
                                random splits; one split is the identity;
                                empty splits carry no weight
+token_partials                 block-aligned cuts equal split_partials;
+                               merge over random token cuts (16-token and
+                               ragged) == unsplit to 1e-12; a one-token
+                               piece has lse = score, o = its V row
+paged_decode_pages             every page chosen == paged_decode; one page ==
+                               numpy softmax over that page's rows; chosen
+                               pages == merge of one-page partials; the
+                               pages quest_decode chooses give its output
 =============================  ==============================================
 
 No function is left unpinned.
@@ -133,6 +141,12 @@ def _load():
             lib.oracle_split_partials.restype = None
             lib.oracle_split_partials.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, D,
                                                   I, I, I, P, P, P]
+            lib.oracle_token_partials.restype = None
+            lib.oracle_token_partials.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, D,
+                                                  I, I, I, P, P, P]
+            lib.oracle_paged_decode_pages.restype = None
+            lib.oracle_paged_decode_pages.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P,
+                                                      D, I, P, P, I]
             lib.oracle_merge_lse.restype = None
             lib.oracle_merge_lse.argtypes = [I, I, P, P, P]
             _lib = lib
@@ -366,6 +380,56 @@ def split_partials(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, b
                               _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl), float(sm_scale),
                               b, h, S, _ptr(beg), _ptr(o), _ptr(lse))
     return o, lse
+
+
+def token_partials(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, b: int, h: int,
+                   tok_begin, *, Hkv: int, block_size: int, k_scale=None, v_scale=None):
+    """Partials (o [S, D], lse [S]) of (b, h) for token pieces [tok_begin[i], tok_begin[i+1])."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    B, Hq, D = q.shape
+    kind = _kv_kind(k_pool, D)
+    fp8 = kind != 0
+    kp = np.ascontiguousarray(k_pool)
+    vp = np.ascontiguousarray(v_pool)
+    ks = _c(k_scale, np.float32) if fp8 else None
+    vs = _c(v_scale, np.float32) if fp8 else None
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    beg = _c(tok_begin, np.int32)
+    S = beg.size - 1
+    o = np.zeros((S, D), dtype=np.float64)
+    lse = np.zeros(S, dtype=np.float64)
+    lib.oracle_token_partials(Hq, Hkv, D, block_size, bt.shape[1], kind, _ptr(q), _ptr(kp),
+                              _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl), float(sm_scale),
+                              b, h, S, _ptr(beg), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def paged_decode_pages(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float,
+                       selected_pages, *, Hkv: int, block_size: int, k_scale=None, v_scale=None,
+                       nthreads: int | None = None) -> np.ndarray:
+    """Decode over chosen 16-token pages: selected_pages int32 [B, Hkv, topk] (-1 = none);
+    returns out [B, Hq, D] in fp64."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    B, Hq, D = q.shape
+    kind = _kv_kind(k_pool, D)
+    fp8 = kind != 0
+    kp = np.ascontiguousarray(k_pool)
+    vp = np.ascontiguousarray(v_pool)
+    ks = _c(k_scale, np.float32) if fp8 else None
+    vs = _c(v_scale, np.float32) if fp8 else None
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    sel = _c(selected_pages, np.int32)
+    topk = sel.shape[-1]
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lib.oracle_paged_decode_pages(B, Hq, Hkv, D, block_size, bt.shape[1], kind, _ptr(q), _ptr(kp),
+                                  _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl),
+                                  float(sm_scale), int(topk), _ptr(sel), _ptr(out),
+                                  nthreads or os.cpu_count() or 1)
+    return out
 
 
 def merge_lse(o_parts, lse) -> np.ndarray:

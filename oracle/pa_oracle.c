@@ -671,6 +671,100 @@ void oracle_split_partials(int Hq, int Hkv, int D, int bs, int max_blocks, int k
 }
 
 /*
+ * Split-KV partials of one (b, h) over token ranges: piece i covers tokens
+ * [tok_begin[i], tok_begin[i+1]) of the sequence, clipped to its length, attended on
+ * its own (attend_range): o_i normalised, lse_i natural log; an empty piece gives
+ * o_i = 0 and lse_i = -inf.  (oracle_split_partials is the block-aligned case.)
+ */
+void oracle_token_partials(int Hq, int Hkv, int D, int bs, int max_blocks, int kv_kind,
+                           const uint16_t *q, const void *k_pool, const void *v_pool,
+                           const float *k_scale, const float *v_scale,
+                           const int32_t *block_tables, const int32_t *seq_lens,
+                           double sm_scale, int b, int h, int npiece,
+                           const int32_t *tok_begin, double *o_parts, double *lse)
+{
+    paged_kv p;
+    int i, L = seq_lens[b];
+    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_kind = kv_kind;
+    p.k_pool = k_pool; p.v_pool = v_pool; p.k_scale = k_scale; p.v_scale = v_scale;
+    p.block_tables = block_tables;
+    for (i = 0; i < npiece; i++) {
+        int t0 = tok_begin[i], t1 = tok_begin[i + 1];
+        if (t1 > L) t1 = L;
+        if (t0 > L) t0 = L;
+        attend_range(&p, &q[((size_t)b * Hq + h) * D], b, h, t0, t1, sm_scale,
+                     &o_parts[(size_t)i * D], &lse[i]);
+    }
+}
+
+/*
+ * Decode over chosen pages ([P3] section 7, the read that follows the selection):
+ * query head h of sequence b attends over the tokens of the 16-token pages
+ * sel[b][h / G][0 .. topk) only -- page j holds tokens [16 j, min(16 j + 16, L)) --
+ * with textbook softmax (max-subtracted, in double).  Entries that name no page of
+ * the sequence (-1, or j * 16 >= L) are skipped; a head with no token gets zeros.
+ * Pages are visited in the order given.
+ */
+void oracle_paged_decode_pages(int B, int Hq, int Hkv, int D, int bs, int max_blocks,
+                               int kv_kind, const uint16_t *q, const void *k_pool,
+                               const void *v_pool, const float *k_scale, const float *v_scale,
+                               const int32_t *block_tables, const int32_t *seq_lens,
+                               double sm_scale, int topk, const int32_t *sel, double *out,
+                               int nthreads)
+{
+    paged_kv p;
+    long long i;
+    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_kind = kv_kind;
+    p.k_pool = k_pool; p.v_pool = v_pool; p.k_scale = k_scale; p.v_scale = v_scale;
+    p.block_tables = block_tables;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+    for (i = 0; i < (long long)B * Hq; i++) {
+        int b = (int)(i / Hq), h = (int)(i % Hq), kvh = oracle_kv_head(h, Hq, Hkv);
+        int L = seq_lens[b], c, t, d, n = 0;
+        const int32_t *pages = &sel[((size_t)b * Hkv + kvh) * topk];
+        double mx = -INFINITY, sum = 0.0;
+        double *o = &out[(size_t)i * D];
+        double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+        double *row = (double *)malloc(sizeof(double) * (size_t)D);
+        double *sv = (double *)malloc(sizeof(double) * 16 * (size_t)(topk > 0 ? topk : 1));
+        for (d = 0; d < D; d++) {
+            qd[d] = oracle_bf16_to_double(q[(size_t)i * D + d]);
+            o[d] = 0.0;
+        }
+        for (c = 0; c < topk; c++) {            /* scores of the chosen tokens */
+            int pg = pages[c], t0 = 16 * pg, t1 = 16 * pg + 16;
+            if (pg < 0 || t0 >= L) continue;
+            if (t1 > L) t1 = L;
+            for (t = t0; t < t1; t++) {
+                double acc = 0.0;
+                kv_row(&p, 0, b, t, kvh, row);
+                for (d = 0; d < D; d++)
+                    acc += qd[d] * row[d];
+                sv[n] = sm_scale * acc;
+                if (sv[n] > mx) mx = sv[n];
+                n++;
+            }
+        }
+        n = 0;
+        for (c = 0; c < topk; c++) {            /* weights and values, same order */
+            int pg = pages[c], t0 = 16 * pg, t1 = 16 * pg + 16;
+            if (pg < 0 || t0 >= L) continue;
+            if (t1 > L) t1 = L;
+            for (t = t0; t < t1; t++) {
+                double w = exp(sv[n++] - mx);
+                sum += w;
+                kv_row(&p, 1, b, t, kvh, row);
+                for (d = 0; d < D; d++)
+                    o[d] += w * row[d];
+            }
+        }
+        for (d = 0; d < D; d++)
+            o[d] = (sum > 0.0) ? o[d] / sum : 0.0;
+        free(qd); free(row); free(sv);
+    }
+}
+
+/*
  * Log-sum-exp merge of split partials of one head:
  *   M = max_i lse_i,  w_i = exp(lse_i - M),  out = sum_i w_i o_i / sum_i w_i
  * Splits with lse_i = -inf carry no weight; if all are -inf the output is 0.

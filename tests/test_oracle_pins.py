@@ -614,3 +614,119 @@ def test_merge_empty_splits_carry_no_weight():
     lse = np.array([0.0, -np.inf, math.log(3.0)])
     assert np.allclose(oracle.merge_lse(o, lse), [(1 + 9) / 4, (2 + 12) / 4], rtol=1e-15)
     assert np.array_equal(oracle.merge_lse(o[1:2], lse[1:2]), [0.0, 0.0])
+
+
+def test_token_partials_block_cuts_equal_split_partials():
+    """Token pieces at block multiples are the block-aligned split: the same numbers."""
+    batch = wl.build_batch("t", [1, 40, 100, 0], Hq=8, Hkv=2, D=64, block_size=32, seed=17)
+    rng = np.random.default_rng(3)
+    for b in range(batch.B):
+        nb = (int(batch.seq_lens[b]) + 31) // 32
+        cuts = np.sort(rng.integers(0, nb + 1, 2))
+        beg = np.concatenate([[0], cuts, [nb]]).astype(np.int32)
+        o1, l1 = oracle.split_partials(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                       batch.seq_lens, batch.sm_scale, b, 3, beg, Hkv=2,
+                                       block_size=32)
+        o2, l2 = oracle.token_partials(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                       batch.seq_lens, batch.sm_scale, b, 3, beg * 32, Hkv=2,
+                                       block_size=32)
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_token_partials_merge_identity_and_single_token():
+    """Merging pieces cut anywhere (16-token and ragged cuts, empty pieces) gives the
+    unsplit attention; a one-token piece has lse = its score and o = its V row."""
+    batch = wl.build_batch("t", [1, 33, 200, 0, 97], Hq=8, Hkv=2, D=64, block_size=16, seed=18)
+    full = _oracle(batch)
+    rng = np.random.default_rng(4)
+    kf = wl.bf16_to_float(batch.k_pool).astype(np.float64)
+    vf = wl.bf16_to_float(batch.v_pool).astype(np.float64)
+    q = wl.bf16_to_float(batch.q).astype(np.float64)
+    for b in range(batch.B):
+        L = int(batch.seq_lens[b])
+        for h in (0, 6):
+            for S in (1, 3, 6):
+                cuts = np.sort(rng.integers(0, L + 1, S - 1))
+                if S == 6 and L > 32:
+                    cuts[:2] = (cuts[:2] // 16) * 16            # some 16-token cuts
+                beg = np.concatenate([[0], np.sort(cuts), [L]]).astype(np.int32)
+                o, lse = oracle.token_partials(batch.q, batch.k_pool, batch.v_pool,
+                                               batch.block_tables, batch.seq_lens,
+                                               batch.sm_scale, b, h, beg, Hkv=2, block_size=16)
+                assert np.allclose(oracle.merge_lse(o, lse), full[b, h], rtol=1e-12, atol=1e-13)
+                for i in range(S):
+                    if beg[i] == beg[i + 1]:
+                        assert lse[i] == -np.inf and not o[i].any()
+            if L > 5:
+                t = 5
+                o, lse = oracle.token_partials(batch.q, batch.k_pool, batch.v_pool,
+                                               batch.block_tables, batch.seq_lens,
+                                               batch.sm_scale, b, h,
+                                               np.array([t, t + 1], np.int32), Hkv=2,
+                                               block_size=16)
+                blk = batch.block_tables[b, t // 16]
+                assert np.array_equal(o[0], vf[blk, t % 16, h // 4])
+                assert math.isclose(lse[0], batch.sm_scale * (kf[blk, t % 16, h // 4] @ q[b, h]),
+                                    rel_tol=1e-12, abs_tol=1e-12)
+
+
+def test_paged_decode_pages_all_pages_one_page_and_merge():
+    """Every page chosen equals the full decode; one page equals softmax attention over
+    that page's rows (numpy on contiguous rows); several pages equal the merge of their
+    one-page partials; -1 entries and pages past the end are skipped."""
+    batch = wl.build_batch("t", [1, 15, 16, 17, 100, 0], Hq=8, Hkv=2, D=64, block_size=32,
+                           seed=19)
+    B, Hkv, G = batch.B, 2, 4
+    npg = (batch.seq_lens + 15) // 16
+    allp = np.full((B, Hkv, 8), -1, np.int32)
+    for b in range(B):
+        allp[b, :, :npg[b]] = np.arange(npg[b])
+    full = _oracle(batch)
+    got = oracle.paged_decode_pages(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                    batch.seq_lens, batch.sm_scale, allp, Hkv=Hkv, block_size=32)
+    assert np.allclose(got, full, rtol=1e-12, atol=1e-13)
+    kf = wl.bf16_to_float(batch.k_pool).astype(np.float64)
+    vf = wl.bf16_to_float(batch.v_pool).astype(np.float64)
+    q = wl.bf16_to_float(batch.q).astype(np.float64)
+    rng = np.random.default_rng(5)
+    sel = np.full((B, Hkv, 3), -1, np.int32)
+    for b in range(B):
+        for kvh in range(Hkv):
+            k = min(3, int(npg[b]))
+            sel[b, kvh, :k] = np.sort(rng.choice(npg[b], k, replace=False))
+    sel[4, 1, 2] = 99                                           # past the end: skipped
+    got = oracle.paged_decode_pages(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                    batch.seq_lens, batch.sm_scale, sel, Hkv=Hkv, block_size=32)
+    for b in range(B):
+        L = int(batch.seq_lens[b])
+        for h in range(batch.Hq):
+            pages = [int(p) for p in sel[b, h // G] if 0 <= p and 16 * p < L]
+            if not pages:
+                assert not got[b, h].any()
+                continue
+            t = np.concatenate([np.arange(16 * p, min(L, 16 * p + 16)) for p in pages])
+            K = kf[batch.block_tables[b, t // 32], t % 32, h // G]
+            V = vf[batch.block_tables[b, t // 32], t % 32, h // G]
+            ref = softmax(batch.sm_scale * (K @ q[b, h])) @ V
+            assert np.allclose(got[b, h], ref, rtol=1e-12, atol=1e-13)
+            beg = [16 * p for p in pages]
+            parts = [oracle.token_partials(batch.q, batch.k_pool, batch.v_pool,
+                                           batch.block_tables, batch.seq_lens, batch.sm_scale,
+                                           b, h, np.array([s, min(L, s + 16)], np.int32),
+                                           Hkv=Hkv, block_size=32) for s in beg]
+            o = np.concatenate([p[0] for p in parts])
+            lse = np.concatenate([p[1] for p in parts])
+            assert np.allclose(oracle.merge_lse(o, lse), got[b, h], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("topk", [1, 4])
+def test_paged_decode_pages_on_quest_selection(topk):
+    """The pages quest_decode chooses, read by paged_decode_pages, give quest_decode's
+    output."""
+    batch = wl.build_batch("t", [1, 15, 16, 17, 70, 200, 0], Hq=8, Hkv=2, D=64, block_size=32,
+                           seed=90 + topk)
+    out, sel = oracle.quest_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                   batch.seq_lens, batch.sm_scale, Hkv=2, block_size=32, topk=topk)
+    got = oracle.paged_decode_pages(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                    batch.seq_lens, batch.sm_scale, sel, Hkv=2, block_size=32)
+    assert np.allclose(got, out, rtol=1e-12, atol=1e-13)
