@@ -4,9 +4,12 @@
 A step is one pass of the whole hot path over one decode batch of the
 70B-class layer workload (B=64, Hq=64, Hkv=8, D=128, bf16, 16-token blocks,
 lognormal lengths with median 2,400 / p95 ~18,000): the slot-mapped cache
-write of the step's new K/V, split-KV paged decode attention, and the
-log-sum-exp merge.  Inputs are resident in HBM when the timed region starts;
-the KV read per step (~1.3 GB) is far larger than L2, so no flush is needed.
+write of the step's new K/V (pa_reshape_and_cache), split-KV paged decode
+attention into caller-visible partials (pa_decode_splitkv) and their
+log-sum-exp merge (pa_merge_lse).  Inputs are resident in HBM when the timed
+region starts; the KV read per step (~1.3 GB) is far larger than L2, so no
+flush is needed.  The line also carries "per_config": the prefix-sharing,
+long-context, FP8 and 4-bit workloads timed the same way in the same process.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
@@ -215,12 +218,241 @@ def cpu_baseline(batch, cores: int) -> dict:
                       f"sequences x {batch.Hq} heads), fp64 C with OpenMP, {dt:.2f} s wall"}
 
 
+# the decode kernel is bracketed by events on every EVENT_EVERY-th timed step (an event
+# between two kernels of the launch chain stops the next one from starting early, so
+# bracketing every step would slow the steps being measured)
+EVENT_EVERY = 8
+
+
+def resolve_call(config: str, call: str, window: int, quest_topk: int, cascade: bool) -> str:
+    """The decode entry point of a step: "splitkv" (pa_decode_splitkv + pa_merge_lse),
+    "segments" (pa_decode given a workspace: the same split kernel and a merge, with the
+    options pa_decode_splitkv does not take) or "decode" (pa_decode, no workspace)."""
+    if call != "auto":
+        if call == "splitkv" and cascade:
+            raise SystemExit("the cascade goes through --call segments (pa_decode with a "
+                             "workspace)")
+        if call == "decode" and cascade:
+            raise SystemExit("--cascade needs a workspace (--call segments)")
+        return call
+    if config == "fp8_mixed":          # that workload's description names pa_decode
+        return "decode"
+    return "segments" if cascade else "splitkv"
+
+
+def device_pools(batch, seed: int, device):
+    """Seeded random pools generated on the GPU (for the per-workload lines, whose host
+    pools would take a minute to draw): the value distributions of workload.py --
+    N(0,1) bf16; E4M3 codes of N(0,1) * 112; 4-bit codes rint(N(0,1) * 7/3) clipped to
+    +-7; scales base * U(0.8, 1.2).  Timing does not depend on the values."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    shape = (batch.nblocks, batch.block_size, batch.Hkv, batch.D)
+
+    def pool():
+        if batch.kv_dtype == "bf16":
+            return torch.randn(shape, generator=g, device=device, dtype=torch.bfloat16)
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        if batch.kv_dtype == "fp8_e4m3":
+            return (x * 112.0).clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        c = (x * (7.0 / 3.0)).round_().clamp_(-7, 7).to(torch.int16) + 8
+        return (c[..., 0::2] | (c[..., 1::2] << 4)).to(torch.uint8).contiguous()
+
+    def scale(base):
+        u = torch.rand((batch.nblocks, batch.Hkv), generator=g, device=device)
+        return (base * (0.8 + 0.4 * u)).to(torch.float32).contiguous()
+
+    kp, vp = pool(), pool()
+    if batch.kv_dtype == "bf16":
+        return kp, vp, None, None
+    base = 4.0 / 448.0 if batch.kv_dtype == "fp8_e4m3" else 3.0 / 7.0
+    return kp, vp, scale(base), scale(base)
+
+
+class StepRunner:
+    """One decode step of a workload on the GPU -- the cache write, (Quest's summary and
+    selection,) the decode call -- with the decode call bracketed by events on demand."""
+
+    def __init__(self, dev, batch, call, args, ns_segments, ns_splits, stream):
+        from paged_kv_cache_28_gb300 import _lib
+        self._lib = _lib
+        self.dev, self.batch, self.call, self.args = dev, batch, call, args
+        self.ns_segments, self.ns_splits, self.stream = ns_segments, ns_splits, stream
+        self.quest = args.quest_topk > 0
+        if call == "segments":
+            dev.ensure_workspace(ns_segments)
+        if call == "splitkv":
+            dev.ensure_parts(ns_splits)
+        if args.cascade:        # shared prefixes attended once per group (prefix-aware decode)
+            if not batch.prefix_groups:
+                raise SystemExit("--cascade needs a workload with prefix groups (prefix_sharing)")
+            dev.enable_cascade()
+        if self.quest:          # summaries of the whole cache, then per step: summarise the
+            dev.quest_build_summaries(stream)       # new token's page, select, sparse decode
+            dev.quest_buffers(args.quest_topk)
+
+    def __call__(self, ev=None, st=None):
+        dev, b, args, _lib = self.dev, self.batch, self.args, self._lib
+        st = self.stream if st is None else st
+        dev.reshape_and_cache(st)
+        if self.quest:
+            _lib.pa_quest_summarize(dev.shape, dev.k_pool, dev.key_summaries, dev.slot_mapping,
+                                    dev.err, st)
+            _lib.pa_quest_select(dev.shape, dev.q, dev.key_summaries, dev.block_tables,
+                                 dev.seq_lens, args.quest_topk, dev.page_scores,
+                                 dev.selected_pages, dev.err, st)
+        if ev is not None:
+            ev[0].record(st)
+        sel = dev.selected_pages if self.quest else None
+        if self.call == "splitkv":
+            _lib.pa_decode_splitkv(dev.shape, dev.o_part, dev.lse, self.ns_splits, dev.q,
+                                   dev.k_pool, dev.v_pool, dev.k_scale, dev.v_scale,
+                                   dev.block_tables, dev.seq_lens, b.sm_scale, dev.err, st,
+                                   args.window, sel, dev.shared_prefix_lens)
+            if ev is not None:
+                ev[1].record(st)
+            _lib.pa_merge_lse(dev.shape, dev.out, dev.o_part, dev.lse, self.ns_splits, st)
+            return
+        ws = dev.workspace if self.call == "segments" else None
+        _lib.pa_decode(dev.shape, dev.out, dev.q, dev.k_pool, dev.v_pool, dev.k_scale,
+                       dev.v_scale, dev.block_tables, dev.seq_lens, b.sm_scale, dev.err, st,
+                       args.window, sel, ws, self.ns_segments if ws is not None else 0,
+                       shared_prefix_lens=dev.shared_prefix_lens,
+                       cascade=dev.cascade if args.cascade else None)
+        if ev is not None:
+            ev[1].record(st)
+
+    def kernel_label(self):
+        if self.call == "splitkv":
+            return "decode_segment_kernel (the pa_decode_splitkv call)"
+        if self.call == "decode":
+            return "decode_pair_kernel (the pa_decode call, no workspace)"
+        return ("pa_decode call with a workspace: "
+                + ("cascade_kernel + " if self.args.cascade else "")
+                + "decode_segment_kernel + merge_kernel")
+
+    def step_label(self):
+        quest = "pa_quest_summarize + pa_quest_select + " if self.quest else ""
+        if self.call == "splitkv":
+            return "pa_reshape_and_cache + " + quest + "pa_decode_splitkv + pa_merge_lse"
+        if self.call == "decode":
+            return ("pa_reshape_and_cache + " + quest + "pa_decode (no workspace: one CTA, "
+                    "or a cluster of CTAs, per sequence and KV head)")
+        return ("pa_reshape_and_cache + " + quest + "pa_decode with a workspace ("
+                + ("cascade + " if self.args.cascade else "") + "split kernel + merge)")
+
+    def launches(self):
+        # our kernels per step: the cache write; Quest's summary, scores and top-k; then
+        # the pair kernel, or the split kernel and a merge (with the cascade also its plan
+        # and its two launches, beside and after the split kernel)
+        return (1 + (3 if self.quest else 0) +
+                (1 if self.call == "decode" else 2 + (3 if self.args.cascade else 0)))
+
+
+def time_steps(run, steps: int, warmup: int, kv_bytes: int, device, world: int, clocks=None):
+    """Warm up, then time `steps` steps with CUDA events (max over ranks): returns
+    (ms per step, mean ms of the bracketed decode call, clock record or None)."""
+    import torch
+    stream = run.stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(0, steps, EVENT_EVERY)]
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    if run.dev.read_err():
+        raise RuntimeError("device error flag set during warm-up")
+    # a step that reads less than L2_FLUSH_BELOW bytes of KV would find part of it in
+    # L2 from the step before: read a buffer twice the L2 size between such steps (a
+    # read leaves L2 clean, as the weight reads of a model's other kernels would; a
+    # written buffer would leave dirty lines for the next step to write back) and time
+    # each step alone with events (the flush is not timed)
+    flush = None
+    if kv_bytes < L2_FLUSH_BELOW:
+        flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+        flush_sink = torch.empty((), dtype=torch.float32, device=device)
+        st_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            torch.sum(flush, dim=0, out=flush_sink)
+            st_ev[i][0].record(stream)
+        run(ev[i // EVENT_EVERY] if i % EVENT_EVERY == 0 else None)
+        if flush is not None:
+            st_ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop() if clocks is not None else None
+    barrier(world)
+    if flush is None:
+        ms_total = t_start.elapsed_time(t_end)
+    else:
+        ms_total = sum(a.elapsed_time(b) for a, b in st_ev)
+    ms_per_step = reduce_max(ms_total, world, device) / steps
+    decode_ms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in ev), world, device)
+    if run.dev.read_err():
+        raise RuntimeError("device error flag set during the timed steps")
+    return ms_per_step, decode_ms, clock_info
+
+
+def traffic_for(config: str, kernel: str):
+    tr = TRAFFIC.get((config, kernel))
+    return tr["bytes"] if tr and tr.get("kernel_hash") == kernel_source_hash() else None
+
+
+# The per-workload lines: the other workloads of the measurement plan, each timed in
+# the same process as the headline, through the call named (the cross-sequence prefix
+# batch through both the split decode and pa_decode without a workspace).
+PER_CONFIG = (("prefix_sharing", "splitkv"), ("prefix_sharing", "decode"),
+              ("long_context", "splitkv"), ("fp8_mixed", "decode"), ("int4_mixed", "splitkv"))
+
+
+def per_config_lines(args, device, world, rank):
+    import torch
+
+    from paged_kv_cache_28_gb300 import workload as wl
+    from paged_kv_cache_28_gb300.device import (DeviceBatch, default_num_segments,
+                                                default_num_splits)
+    peak, _ = measured_peak_hbm()
+    out = {}
+    for config, call in PER_CONFIG:
+        seed = rank_seed(wl.DEFAULT_SEEDS[config], rank)
+        batch = wl.make(config, seed=seed, with_pools=False)
+        dev = DeviceBatch(batch, device=device, pools=device_pools(batch, seed, device))
+        sub = argparse.Namespace(window=0, quest_topk=0, cascade=False)
+        run = StepRunner(dev, batch, call, sub, default_num_segments(dev.shape, device),
+                         default_num_splits(dev.shape, device), torch.cuda.current_stream(device))
+        kv_bytes = step_kv_bytes(batch, sub)
+        steps = max(EVENT_EVERY, args.steps)
+        ms, kms, _ = time_steps(run, steps, args.warmup, kv_bytes, device, world)
+        achieved = kv_bytes / (kms * 1e-3) / 1e9
+        kernel = "decode_pair_kernel" if call == "decode" else "decode_segment_kernel"
+        out[f"{config}/{call}"] = {
+            "call": run.step_label(), "kernel": run.kernel_label(),
+            "tokens_per_s": world * batch.B / (ms * 1e-3), "ms_per_step": ms, "kernel_ms": kms,
+            "algorithmic_bytes": kv_bytes, "achieved_gbs": achieved, "frac": achieved / peak,
+            "traffic": traffic_for(config, kernel),
+            "num_splits": run.ns_splits if call == "splitkv" else None,
+            "steps": steps, "pools": "seeded on the GPU (torch.Generator), values as workload.py"}
+        del run, dev
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
 
     from paged_kv_cache_28_gb300 import _lib
     from paged_kv_cache_28_gb300 import workload as wl
-    from paged_kv_cache_28_gb300.device import DeviceBatch, default_num_splits, to_device_bf16
+    from paged_kv_cache_28_gb300.device import (DeviceBatch, default_num_segments,
+                                                default_num_splits)
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -236,105 +468,20 @@ def run_ours(args):
     seed = rank_seed(wl.DEFAULT_SEEDS[args.config], rank)
     batch = wl.make(args.config, seed=seed)
     dev = DeviceBatch(batch, device=dev_id)
-    ns = args.num_splits or default_num_splits(dev.shape, dev_id)
-    dev.ensure_workspace(ns)
+    call = resolve_call(args.config, args.call, args.window, args.quest_topk, args.cascade)
     stream = torch.cuda.current_stream(dev_id)
-
-    # the decode kernel is bracketed by events on every EVENT_EVERY-th timed step (an
-    # event between two kernels of the launch chain stops the next one from starting
-    # early, so bracketing every step would slow the steps being measured)
-    EVENT_EVERY = 8
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(0, args.steps, EVENT_EVERY)]
-
-    call = args.call if args.call != "auto" else (
-        "decode" if args.config == "fp8_mixed" else "splitkv")
-    if call == "decode" and args.cascade:
-        raise SystemExit("--cascade runs through the split decode (--call splitkv)")
-    if args.cascade:            # shared prefixes attended once per group (prefix-aware decode)
-        if not batch.prefix_groups:
-            raise SystemExit("--cascade needs a workload with prefix groups (prefix_sharing)")
-        dev.enable_cascade()
-    quest = args.quest_topk > 0
-    if quest:       # summaries of the whole cache, then per step: summarise the new
-        dev.quest_build_summaries(stream)      # token's page, select, sparse decode
-        dev.quest_buffers(args.quest_topk)
-
-    def step(i=None, st=None):
-        st = stream if st is None else st
-        dev.reshape_and_cache(st)
-        if quest:
-            _lib.pa_quest_summarize(dev.shape, dev.k_pool, dev.key_summaries, dev.slot_mapping,
-                                    dev.err, st)
-            _lib.pa_quest_select(dev.shape, dev.q, dev.key_summaries, dev.block_tables,
-                                 dev.seq_lens, args.quest_topk, dev.page_scores,
-                                 dev.selected_pages, dev.err, st)
-        if i is not None:
-            ev[i][0].record(st)
-        if call == "decode":
-            _lib.pa_decode(dev.shape, dev.out, dev.q, dev.k_pool, dev.v_pool, dev.k_scale,
-                           dev.v_scale, dev.block_tables, dev.seq_lens, batch.sm_scale, dev.err,
-                           st, args.window, dev.selected_pages if quest else None,
-                           shared_prefix_lens=dev.shared_prefix_lens)
-            if i is not None:
-                ev[i][1].record(st)
-            return
-        _lib.pa_decode_splitkv(dev.shape, dev.out, dev.workspace, ns, dev.q, dev.k_pool,
-                               dev.v_pool, dev.k_scale, dev.v_scale, dev.block_tables,
-                               dev.seq_lens, batch.sm_scale, dev.err, st,
-                               dev.shared_prefix_lens, args.window,
-                               dev.selected_pages if quest else None,
-                               dev.cascade if args.cascade else None)
-        if i is not None:
-            ev[i][1].record(st)
-        _lib.pa_merge_lse(dev.shape, dev.out, dev.workspace, ns, st)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if dev.read_err():
-        raise RuntimeError("device error flag set during warm-up")
-
-    # a step that reads less than L2_FLUSH_BELOW bytes of KV would find part of it in
-    # L2 from the step before: read a buffer twice the L2 size between such steps (a
-    # read leaves L2 clean, as the weight reads of a model's other kernels would; a
-    # written buffer would leave dirty lines for the next step to write back) and time
-    # each step alone with events (the flush is not timed)
-    selected = dev.selected_pages.cpu().numpy() if quest else None
+    run = StepRunner(dev, batch, call, args,
+                     args.num_segments or default_num_segments(dev.shape, dev_id),
+                     args.num_splits or default_num_splits(dev.shape, dev_id), stream)
+    selected = None
+    if args.quest_topk > 0:
+        run()                                   # one step so the selection exists
+        torch.cuda.synchronize()
+        selected = dev.selected_pages.cpu().numpy()
     kv_bytes = step_kv_bytes(batch, args, selected)
-    flush = None
-    if kv_bytes < L2_FLUSH_BELOW:
-        flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev_id)
-        flush_sink = torch.empty((), dtype=torch.float32, device=dev_id)
-        st_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(args.steps)]
-
     clocks = ClockSampler(local)
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        if flush is not None:
-            torch.sum(flush, dim=0, out=flush_sink)
-            st_ev[i][0].record(stream)
-        step(i // EVENT_EVERY if i % EVENT_EVERY == 0 else None)
-        if flush is not None:
-            st_ev[i][1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clock_info = clocks.stop()
-    barrier(world)
-    if flush is None:
-        ms_total = t_start.elapsed_time(t_end)
-    else:
-        ms_total = sum(a.elapsed_time(b) for a, b in st_ev)
-    ms_total = reduce_max(ms_total, world, dev_id)
-    ms_per_step = ms_total / args.steps
-    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    decode_ms = reduce_max(decode_ms, world, dev_id)
+    ms_per_step, decode_ms, clock_info = time_steps(run, args.steps, args.warmup, kv_bytes,
+                                                    dev_id, world, clocks)
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -366,14 +513,14 @@ def run_ours(args):
                 setattr(dev, name, views[name])
         if args.cascade:
             dev.cascade = (views["group_offsets"], views["group_seqs"],
-                           views["group_prefix_len"], dev.cascade[3])
+                           views["group_prefix_len"]) + tuple(dev.cascade[3:])
         out_host = torch.empty(dev.out.shape, dtype=dev.out.dtype).pin_memory()
         h2d = sum(n for _, n, _, _ in parts.values())
         d2h = out_host.numel() * out_host.element_size()
 
         def e2e_body(st):
             dev_in.copy_(host_in, non_blocking=True)
-            step(st=st)
+            run(st=st)
             out_host.copy_(dev.out, non_blocking=True)
 
         if args.e2e_eager:
@@ -409,21 +556,15 @@ def run_ours(args):
         e2e = {"value": world * batch.B / e2e_s, "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "cuda_graph": not args.e2e_eager}
-    if dev.read_err():
-        raise RuntimeError("device error flag set during the timed steps")
+        if dev.read_err():
+            raise RuntimeError("device error flag set during the end-to-end steps")
 
     unique_tokens = step_kv_tokens(batch, args, selected)
     peak, peak_kind = measured_peak_hbm()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
-    kernel = ("decode_pair_kernel" if call == "decode" else "decode_segment_kernel")
-    tr = (TRAFFIC.get((args.config, kernel))
-          if args.window == 0 and args.quest_topk == 0 and not args.cascade else None)
-    traffic = tr["bytes"] if tr and tr.get("kernel_hash") == kernel_source_hash() else None
-    # our kernels per step: the cache write; Quest's summary, scores and top-k; then the
-    # pair kernel, or the split kernel and the merge (with the cascade also its plan and
-    # its two launches, beside and after the split kernel)
-    launches = (1 + (3 if args.quest_topk > 0 else 0) +
-                (1 if call == "decode" else 2 + (3 if args.cascade else 0)))
+    kernel = "decode_pair_kernel" if call == "decode" else "decode_segment_kernel"
+    plain = args.window == 0 and args.quest_topk == 0 and not args.cascade
+    traffic = traffic_for(args.config, kernel) if plain and call != "segments" else None
     result = {
         "metric": METRIC,
         "value": world * batch.B / (ms_per_step * 1e-3),
@@ -443,20 +584,17 @@ def run_ours(args):
             "block_size": batch.block_size, "seq_len_sum": batch.logical_tokens,
             "seq_len_max": int(batch.seq_lens.max()),
             "unique_kv_tokens": unique_tokens,
-            "num_splits": ns if call == "splitkv" else None,
+            "num_splits": run.ns_splits if call == "splitkv" else None,
+            "num_segments": run.ns_segments if call == "segments" else None,
             "window": args.window,
             "quest_topk": args.quest_topk,
             "cascade": bool(args.cascade),
             "l2": (f"no flush: {kv_bytes / 1e9:.2f} GB of KV read per step >> 129 MB L2"
-                   if flush is None else
+                   if kv_bytes >= L2_FLUSH_BELOW else
                    f"flushed: {kv_bytes / 1e9:.3f} GB of KV per step, a {2 * L2_BYTES >> 20} MB "
                    "buffer read between steps, each step timed alone with events"),
             "parallelism": f"replicas x{world}" if world > 1 else "single",
-            "step": ("pa_reshape_and_cache + "
-                     + ("pa_quest_summarize + pa_quest_select + " if args.quest_topk > 0 else "")
-                     + ("pa_decode (no workspace: one CTA, or a cluster of CTAs, per sequence and KV head)" if call == "decode" else
-                        "pa_decode_splitkv (cascade + split kernels) + pa_merge_lse"
-                        if args.cascade else "pa_decode_splitkv + pa_merge_lse")),
+            "step": run.step_label(),
         },
         "roofline": {
             "bound": "hbm",
@@ -465,18 +603,20 @@ def run_ours(args):
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": traffic,
-            "kernel": ("decode_pair_kernel (the pa_decode call)" if call == "decode" else
-                       "cascade_kernel + decode_segment_kernel (the pa_decode_splitkv call)"
-                       if args.cascade else "decode_segment_kernel (the pa_decode_splitkv call)"),
+            "kernel": run.kernel_label(),
             "kernel_ms": decode_ms,
             "algorithmic_bytes": kv_bytes,
             "peak_kind": peak_kind,
         },
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": run.launches() * args.steps,
         "clocks": clock_info,
     }
     if e2e is not None:
         result["e2e"] = e2e
+    del run, dev
+    torch.cuda.empty_cache()
+    if not args.no_per_config and plain and args.config == "llama70b_layer":
+        result["per_config"] = per_config_lines(args, dev_id, world, rank)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(batch, os.cpu_count() or 1)
     if rank == 0:
@@ -577,12 +717,17 @@ def main(argv=None):
     ap.add_argument("--config", default="llama70b_layer",
                     choices=["tiny", "llama70b_layer", "prefix_sharing", "long_context",
                              "fp8_mixed", "int4_mixed", "code_assistant_turns"])
-    ap.add_argument("--num-splits", type=int, default=0)
-    ap.add_argument("--call", choices=["auto", "splitkv", "decode"], default="auto",
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="pa_decode_splitkv's partial slots per head (0: pa_default_num_splits)")
+    ap.add_argument("--num-segments", type=int, default=0,
+                    help="segments of pa_decode's split decode (0: pa_default_num_segments)")
+    ap.add_argument("--call", choices=["auto", "splitkv", "segments", "decode"], default="auto",
                     help="the decode entry point of each step: pa_decode_splitkv + pa_merge_lse, "
-                         "or pa_decode without a workspace (a CTA or a cluster of CTAs per sequence and KV head); "
-                         "auto: pa_decode for fp8_mixed, whose workload names that call, "
-                         "pa_decode_splitkv otherwise")
+                         "pa_decode with a workspace (the same split kernel and its own merge; "
+                         "the cascade goes this way), or pa_decode without a workspace (a CTA "
+                         "or a cluster of CTAs per sequence and KV head); auto: pa_decode for "
+                         "fp8_mixed, whose workload names that call, the workspace form with "
+                         "the cascade, pa_decode_splitkv otherwise")
     ap.add_argument("--e2e-eager", action="store_true",
                     help="e2e leg: launch each call eagerly instead of replaying a CUDA graph")
     ap.add_argument("--cascade", action="store_true",
@@ -593,6 +738,9 @@ def main(argv=None):
                     help="sliding-window layer: attend over the last W positions (0 = all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload lines (prefix sharing, long context, FP8, "
+                         "4-bit) added to the default 70B line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -38,8 +38,8 @@
  *    argument returns PA_ERR_INVALID_ARG or PA_ERR_UNSUPPORTED and launches
  *    nothing.  A failed launch returns PA_ERR_CUDA.
  *  - Errors that depend on device data (a block id outside the pool, a
- *    sequence longer than its block table, a slot outside the pool, two FP8
- *    writes into one block) are reported through `err_flag`: a device int32
+ *    sequence longer than its block table, a slot outside the pool, two
+ *    quantised writes into one slot) are reported through `err_flag`: a device int32
  *    that the kernels OR a PA_DEVERR_* bit into.  The affected unit is skipped
  *    (or reads zeros), nothing traps.  The flag is sticky; the caller zeroes it
  *    and reads it after synchronising (see pa_read_error_flag).  err_flag may
@@ -77,6 +77,7 @@ extern "C" {
 #endif
 
 typedef struct CUstream_st *pa_stream_t;   /* same type as cudaStream_t */
+typedef struct CUevent_st *pa_event_t;     /* same type as cudaEvent_t */
 
 typedef enum {
     PA_OK = 0,
@@ -92,11 +93,11 @@ typedef enum {
 typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1, PA_KV_INT4 = 2 } pa_kv_dtype;
 
 /* Device error bits ORed into *err_flag (PA_DEVERR_FP8_CONFLICT also covers 4-bit
- * pools: two tokens of one write call in one block). */
+ * pools: two tokens of one write call with the same slot). */
 #define PA_DEVERR_BLOCK_ID     1   /* block table entry outside [0, nblocks)        */
 #define PA_DEVERR_SEQ_LEN      2   /* seq_len < 0 or > max_blocks * block_size      */
 #define PA_DEVERR_SLOT         4   /* slot_mapping entry >= nblocks * block_size    */
-#define PA_DEVERR_FP8_CONFLICT 8   /* two tokens of one FP8 write hit one block     */
+#define PA_DEVERR_FP8_CONFLICT 8   /* two tokens of one FP8/4-bit write, one slot    */
 #define PA_DEVERR_TIMEOUT      16  /* an internal pipeline wait gave up             */
 
 typedef struct {
@@ -122,48 +123,59 @@ typedef struct {
  *     increasing order, as pa_quest_select writes them (page j = tokens
  *     [16 j, min(16 j + 16, L))).  An index outside the sequence sets
  *     PA_DEVERR_BLOCK_ID and reads zeros.  Not combined with window.
- *   shared_prefix_lens: pa_decode (with or without a workspace) and
- *     pa_decode_splitkv.  Optional [B] int32 device array, a speed hint for
- *     batches with prefix sharing ("appendonly", "Prefix sharing is where the
- *     real win lives"): the number
+ *   shared_prefix_lens: pa_decode (with or without a workspace).  Optional [B]
+ *     int32 device array, a speed hint for batches with prefix sharing
+ *     ("appendonly", "Prefix sharing is where the real win lives"): the number
  *     of leading tokens of sequence b that lie in blocks other sequences of the
  *     batch also reference.  Whole 16-token tiles inside that prefix are
  *     fetched with an L2 evict-last policy, all other tiles evict-first, so a
  *     shared block stays in L2 for its other readers.  Any value gives the same
  *     result, bit for bit.
  *   num_prefix_groups, group_offsets, group_seqs, group_prefix_len,
- *     cascade_workspace: prefix-aware (cascade) decode, in pa_decode_splitkv and in
- *     pa_decode given a workspace (pa_decode without one ignores them and attends
- *     over every token itself)
- *     ("appendonly", "Prefix sharing is where the real win lives": many
- *     sequences point at the same physical blocks).  Group g's members are
+ *     cascade_workspace: prefix-aware (cascade) decode, in pa_decode given a
+ *     workspace (pa_decode without one ignores them and attends over every
+ *     token itself) ("appendonly", "Prefix sharing is where the real win lives":
+ *     many sequences point at the same physical blocks).  Group g's members are
  *     group_seqs[group_offsets[g] .. group_offsets[g + 1]) (device int32
  *     arrays; group_offsets rises from 0, at most B members in all); their first
  *     group_prefix_len[g] tokens (device int32, a multiple of 16) hold the same
- *     keys and values, as when their block tables share those blocks.  A separate kernel attends over each group's shared tokens
- *     once for all members and KV heads at a time (the members' query rows
- *     stacked into one tensor-core contraction, reading the blocks through the
- *     first member's table); the split kernel covers the rest of each sequence
- *     and pa_merge_lse joins the two.  Each sequence belongs to at most one
- *     group and every member holds at least group_prefix_len[g] tokens (a
- *     member with fewer sets PA_DEVERR_SEQ_LEN and its output is undefined).
- *     cascade_workspace: device memory of at least pa_cascade_workspace_bytes
- *     bytes, 256-byte aligned, used by the split decode and read by the merge
- *     (pa_merge_lse, or the merge pa_decode runs).  bf16 pools only; not combined with window or
- *     topk.  The result equals the plain decode's up to rounding order.
- *   workspace, workspace_bytes, num_splits: pa_decode only.  With a workspace
- *     (device memory of at least pa_splitkv_workspace_bytes(shape, n) bytes,
- *     256-byte aligned; n = num_splits, or pa_default_num_splits for this GPU
- *     when num_splits is 0) pa_decode runs the split decode and the merge
- *     itself: one call, load-balanced however the lengths are spread.  Without
- *     one it needs no memory: one CTA per (sequence, KV head) unit, or, when the
- *     batch has at most two units per CTA the GPU holds at once, a cluster of
- *     four CTAs per unit that share its tiles (at least 16 per warp; a short
- *     unit leaves the extra CTAs idle) and merge through distributed shared
- *     memory; a window or topk that bounds every unit keeps one CTA per unit
- *     when the units fill the GPU or fit one CTA.  Batches of up to 256
- *     sequences start their longest sequences first.  A batch whose longest sequence outweighs the rest is still held
- *     back by it; the split decode is not.
+ *     keys and values, as when their block tables share those blocks.  A
+ *     separate kernel attends over each group's shared tokens once for all
+ *     members and KV heads at a time (the members' query rows stacked into one
+ *     tensor-core contraction, reading the blocks through the first member's
+ *     table); the split kernel covers the rest of each sequence and the merge
+ *     joins the two.  Each sequence belongs to at most one group and every
+ *     member holds at least group_prefix_len[g] tokens (a member with fewer sets
+ *     PA_DEVERR_SEQ_LEN and its output is undefined).  cascade_workspace:
+ *     device memory of at least pa_cascade_workspace_bytes bytes, 256-byte
+ *     aligned.  bf16 pools only; not combined with window or topk.  The result
+ *     equals the plain decode's up to rounding order.
+ *   cascade_stream, cascade_events: where the cascade kernel runs.  NULL: on
+ *     `stream`, after the split kernel.  Otherwise a caller-owned stream of the
+ *     same device, on which the cascade kernel runs beside the split kernel (it
+ *     does tensor work while the split kernel streams HBM), joined back before
+ *     the merge: the call records cascade_events[0] on `stream`, makes
+ *     cascade_stream wait for it, launches there, records cascade_events[1] on
+ *     cascade_stream and makes `stream` wait for it.  The two events are
+ *     caller-created (cudaEventDisableTiming is enough) and may be reused by the
+ *     next call on the same streams.  The results are the same either way.
+ *   workspace, workspace_bytes, num_segments: pa_decode only.  With a workspace
+ *     (device memory of at least pa_decode_workspace_bytes(shape, n) bytes,
+ *     256-byte aligned; n = num_segments, or pa_default_num_segments for this
+ *     GPU when num_segments is 0) pa_decode runs the load-balanced split decode
+ *     and the merge itself: the 16-token tiles of all (sequence, KV head) units,
+ *     laid end to end, are cut into n equal segments, one per split worker; a
+ *     unit inside one segment is finished there, a unit cut by segment bounds
+ *     leaves one partial per piece in the workspace for the merge.  Without a
+ *     workspace it needs no memory: one CTA per (sequence, KV head) unit, or,
+ *     when the batch has at most two units per CTA the GPU holds at once, a
+ *     cluster of four CTAs per unit that share its tiles (at least 16 per warp;
+ *     a short unit leaves the extra CTAs idle) and merge through distributed
+ *     shared memory; a window or topk that bounds every unit keeps one CTA per
+ *     unit when the units fill the GPU or fit one CTA.  Batches of up to 256
+ *     sequences start their longest sequences first.  A batch whose longest
+ *     sequence outweighs the rest is still held back by it; the split decode is
+ *     not.
  */
 typedef struct {
     int32_t window;
@@ -177,7 +189,9 @@ typedef struct {
     void *cascade_workspace;
     void *workspace;                    /* pa_decode: split workspace, or NULL */
     size_t workspace_bytes;
-    int32_t num_splits;                 /* pa_decode with a workspace; 0: default */
+    int32_t num_segments;               /* pa_decode with a workspace; 0: default */
+    pa_stream_t cascade_stream;         /* NULL: the cascade runs after the split kernel */
+    pa_event_t cascade_events[2];       /* fork, join (with cascade_stream) */
 } pa_decode_opts;
 
 /*
@@ -200,8 +214,10 @@ typedef struct {
  *   - a write that raises the scale re-encodes the codes at offsets below it:
  *     code' = E4M3((E4M3 value of code * old scale) / new scale), fp32 product
  *     and division.
- *   Two tokens of one call that land in the same block set
- *   PA_DEVERR_FP8_CONFLICT and neither is written.
+ *   Tokens of one call that land in the same block (a prompt, several appended
+ *   tokens) are applied one after the other in token order, exactly as separate
+ *   calls would apply them.  Two tokens of one call with the same slot are both
+ *   applied, the later one last, and set PA_DEVERR_FP8_CONFLICT.
  * A slot beyond the pool sets PA_DEVERR_SLOT and is skipped.
  */
 pa_status pa_reshape_and_cache(const pa_shape *shape, const void *k_new, const void *v_new,
@@ -237,68 +253,101 @@ pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void
                     pa_stream_t stream);
 
 /*
- * Bytes of device workspace pa_decode_splitkv / pa_merge_lse need for this
- * shape and num_splits; 0 if the arguments are invalid.  Host only.
+ * Bytes of the optional split workspace of pa_decode (pa_decode_opts.workspace)
+ * for this shape and num_segments; 0 if the arguments are invalid.  Host only.
  */
-size_t pa_splitkv_workspace_bytes(const pa_shape *shape, int32_t num_splits);
+size_t pa_decode_workspace_bytes(const pa_shape *shape, int32_t num_segments);
+
+/*
+ * The number of segments pa_decode's split decode uses when num_segments is 0: the
+ * split workers a GPU with sm_count SMs keeps resident at once.  Host only, no CUDA
+ * call.
+ */
+int32_t pa_default_num_segments(const pa_shape *shape, int32_t sm_count);
 
 /*
  * Bytes of device workspace a cascade decode (pa_decode_opts.num_prefix_groups
- * > 0) needs for this shape, besides the split-KV workspace; 0 if the shape is
+ * > 0) needs for this shape, besides the split workspace; 0 if the shape is
  * invalid.  Host only.
  */
 size_t pa_cascade_workspace_bytes(const pa_shape *shape);
 
 /*
- * A good num_splits for this shape on a GPU with sm_count SMs: the number of
- * split workers that are resident at once.  Host only, no CUDA call.
+ * Split-KV decode with caller-visible partials (flash-decoding), and the
+ * log-sum-exp merge of such partials.  Not on the pages: the standard extension
+ * of their per-(sequence, head) attention ("Taming the Token Torrent", "Custom
+ * PagedAttention Kernels") to several workers per sequence.
+ *
+ * Partials of query head h of sequence b, S = num_splits slots:
+ *     o_part [B, Hq, S, D] fp32   o_part[b][h][i][:] = sum_t e^(s_t - m_i) V_t / l_i
+ *     lse    [B, Hq, S]    fp32   lse[b][h][i]       = m_i + ln l_i (natural log)
+ * over the tokens t of piece i (s_t = sm_scale <q[b][h], K_b[t]>, m_i their
+ * largest score, l_i = sum_t e^(s_t - m_i)).  An empty slot has lse = -inf and
+ * its o_part row is not read (it may hold anything).  Merging every slot gives
+ * the attention of pa_decode.
+ */
+
+/*
+ * Bytes of o_part and lse together for num_splits slots, B * Hq * num_splits *
+ * (D + 1) * 4 (o_part first, then lse, when both come from one allocation);
+ * 0 if the arguments are invalid.  Host only.
+ */
+size_t pa_splitkv_workspace_bytes(const pa_shape *shape, int32_t num_splits);
+
+/*
+ * A num_splits for pa_decode_splitkv: the most slots (2 to 64) whose o_part fits
+ * in 64 MiB, and no more than a sequence of max_blocks blocks has 16-token
+ * tiles.  Host only, no CUDA call; sm_count is checked (> 0) but a GPU's size does
+ * not change the slots a sequence needs.
  */
 int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count);
 
 /*
- * pa_decode_splitkv -- the same attention as pa_decode, with the KV of each
- * (sequence, KV head) split across SMs (flash-decoding).  Partition: the
- * 16-token tiles of all (b, kvh) pairs, in (b, kvh, position) order, are cut
- * into num_splits contiguous segments of ceil(total / num_splits) tiles; each
- * segment is one split worker.  A pair that lies inside one segment is finished
- * there and written to out.  A pair cut by segment boundaries leaves one
- * partial per piece in the workspace:
- *     o_i = sum_t e^(s_t - m_i) V_t / l_i,  lse_i = m_i + ln l_i  (natural log)
- * and pa_merge_lse completes it.  out is complete only after pa_merge_lse on
- * the same stream with the same shape, workspace and num_splits.
- * workspace: device memory of at least pa_splitkv_workspace_bytes(shape,
- * num_splits) bytes, 256-byte aligned, owned by the caller, not shared with
- * concurrent calls; nothing in it needs initialising.  1 <= num_splits <= 65536.
- * opts (may be NULL): the window and the shared-prefix L2 hint, see
- * pa_decode_opts; with a window the partition runs over the attended tiles only.
- * 4-bit pools with an even number of KV heads, 8 query heads per KV head and
- * no Quest selection are read two adjacent KV heads at a time (their 64-byte
- * rows form one 128-byte run per token): the partition's pairs are then
- * (b, KV heads 2u and 2u + 1).  The result does not depend on it.
- * Batches of more than 16384 sequences return PA_ERR_UNSUPPORTED (each CTA
- * scans the sequence lengths in shared memory).
+ * pa_decode_splitkv -- write the partials of every query head (layout above),
+ * 1 <= num_splits <= 65536.  How the tokens are cut: the 16-token tiles of all
+ * (sequence, KV head) units, in (b, kvh, position) order, are laid end to end
+ * and cut into equal segments of W tiles, one per split worker (the workers this
+ * GPU keeps resident), W = max(ceil(total / workers), ceil((n_max - 1) /
+ * (S - 1))) with n_max the tiles of the longest unit: the second bound keeps
+ * every unit within S pieces (a unit of n tiles spans at most ceil((n - 1) / W)
+ * + 1 segments).  Piece i of a unit is its part in the i-th segment that holds
+ * it; slots after its last piece, and all slots of a sequence with seq_len 0,
+ * get lse = -inf.  With S = 1 a segment's bounds move up to the next unit start,
+ * so every unit is one piece.  4-bit pools with an even number of KV heads and 8
+ * query heads per KV head are read two adjacent KV heads at a time (a unit is then
+ * (b, KV heads 2u, 2u + 1)) unless opts selects Quest pages; the result does not
+ * depend on it.  opts (may be NULL): window, topk + selected_pages and
+ * shared_prefix_lens as for pa_decode, the cut then running over the attended tiles
+ * only; the workspace fields are ignored, and a cascade (num_prefix_groups > 0)
+ * returns PA_ERR_UNSUPPORTED (its shared-prefix partials are merged by pa_decode's
+ * own merge).
+ * All arrays are caller-owned device memory; o_part and lse are outputs,
+ * nothing in them needs initialising.  Batches of more than 16384 sequences
+ * return PA_ERR_UNSUPPORTED (each CTA scans the lengths in shared memory).
  */
-pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
-                            size_t workspace_bytes, int32_t num_splits, const void *q,
-                            const void *k_pool, const void *v_pool, const float *k_scale,
-                            const float *v_scale, const int32_t *block_tables,
-                            const int32_t *seq_lens, const pa_decode_opts *opts,
-                            float sm_scale, int32_t *err_flag, pa_stream_t stream);
+pa_status pa_decode_splitkv(const pa_shape *shape, float *o_part, float *lse, int32_t num_splits,
+                            const void *q, const void *k_pool, const void *v_pool,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *block_tables, const int32_t *seq_lens,
+                            const pa_decode_opts *opts, float sm_scale, int32_t *err_flag,
+                            pa_stream_t stream);
 
 /*
- * pa_merge_lse -- log-sum-exp merge of the split partials left by
- * pa_decode_splitkv, per query head:
+ * pa_merge_lse -- per query head (b, h), over the slots i < num_splits of
+ * o_part [B, Hq, S, D] and lse [B, Hq, S] (fp32, caller-owned, from
+ * pa_decode_splitkv or from anywhere else, e.g. partials of a prefix attended
+ * elsewhere; lse = -inf marks an empty slot):
  *     M = max_i lse_i,  w_i = e^(lse_i - M),  out = sum_i w_i o_i / sum_i w_i
- * Pairs with seq_len 0 get zeros; pairs finished inside one segment are left
- * untouched.
+ * A head with every slot empty gets zeros.  out [B, Hq, D] fp32.
  */
-pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,
+pa_status pa_merge_lse(const pa_shape *shape, float *out, const float *o_part, const float *lse,
                        int32_t num_splits, pa_stream_t stream);
 
 /*
- * pa_decode_splitkv_noalloc -- pa_decode_splitkv followed by pa_merge_lse, for
- * callers that cannot allocate device memory.  The pages describe no such
- * call; it exists for users of this library who may not call cudaMalloc: a
+ * pa_decode_splitkv_noalloc -- pa_decode's load-balanced split decode and merge
+ * (pa_decode with opts.workspace and opts.num_segments = num_segments, no other
+ * option), for callers that cannot allocate device memory.  The pages describe no
+ * such call; it exists for users of this library who may not call cudaMalloc: a
  * plugin inside a host framework that owns all device memory through its own
  * pool, a latency-critical path where cudaMalloc's implicit device-wide
  * synchronisation is not acceptable, or a deployment whose memory budget is
@@ -307,17 +356,19 @@ pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,
  * Instead of a caller workspace it uses a scratch array of
  * PA_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library: every GPU that
  * loads libpa.so holds that array until the process exits.  The call allocates
- * nothing and frees nothing.  Arguments and results are those of
- * pa_decode_splitkv (with opts = NULL: full attention, no hint) + pa_merge_lse:
- * out [B, Hq, D] is complete when the work enqueued on `stream` has finished.
+ * nothing and frees nothing.  out [B, Hq, D] is complete when the work enqueued
+ * on `stream` has finished.
  *
  * Limits and sharing:
  *   - returns PA_ERR_INVALID_ARG (launching nothing) when
- *     pa_splitkv_workspace_bytes(shape, num_splits) exceeds
- *     PA_NOALLOC_SCRATCH_BYTES, or for any argument pa_decode_splitkv rejects;
- *   - the first call on a device looks up the array's device address on that
- *     device (cudaGetSymbolAddress) and caches it; make that first call before
- *     any stream capture;
+ *     pa_decode_workspace_bytes(shape, num_segments) exceeds
+ *     PA_NOALLOC_SCRATCH_BYTES, or for any argument pa_decode rejects;
+ *   - num_segments = 0 takes pa_default_num_segments for the current GPU;
+ *   - the array's device address is looked up (cudaGetSymbolAddress, on the
+ *     current device) by every call made while `stream` is not being captured,
+ *     so it stays right after cudaDeviceReset; a call made during stream capture
+ *     reuses the address the last call on that device found, so make one call on
+ *     each device before capturing;
  *   - all calls share the one array per device and it keeps the last call's
  *     contents (nothing in it needs to start at zero); calls whose work
  *     overlaps on the GPU -- on different streams, or from different threads --
@@ -325,7 +376,7 @@ pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,
  */
 #define PA_NOALLOC_SCRATCH_BYTES (64u << 20)
 
-pa_status pa_decode_splitkv_noalloc(const pa_shape *shape, float *out, int32_t num_splits,
+pa_status pa_decode_splitkv_noalloc(const pa_shape *shape, float *out, int32_t num_segments,
                                     const void *q, const void *k_pool, const void *v_pool,
                                     const float *k_scale, const float *v_scale,
                                     const int32_t *block_tables, const int32_t *seq_lens,

@@ -21,7 +21,8 @@ PA_DEVERR_FP8_CONFLICT, PA_DEVERR_TIMEOUT = 8, 16
 EXPORTED = ("pa_reshape_and_cache", "pa_decode", "pa_splitkv_workspace_bytes",
             "pa_default_num_splits", "pa_decode_splitkv", "pa_merge_lse", "pa_status_string",
             "pa_read_error_flag", "pa_decode_splitkv_noalloc", "pa_quest_summarize",
-            "pa_quest_select", "pa_cascade_workspace_bytes")
+            "pa_quest_select", "pa_cascade_workspace_bytes", "pa_decode_workspace_bytes",
+            "pa_default_num_segments")
 PA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -38,27 +39,35 @@ class pa_decode_opts(ctypes.Structure):
                 ("num_prefix_groups", ctypes.c_int32), ("group_offsets", ctypes.c_void_p),
                 ("group_seqs", ctypes.c_void_p), ("group_prefix_len", ctypes.c_void_p),
                 ("cascade_workspace", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t), ("num_splits", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_size_t), ("num_segments", ctypes.c_int32),
+                ("cascade_stream", ctypes.c_void_p), ("cascade_events", ctypes.c_void_p * 2)]
 
 
 def _opts(window: int = 0, shared_prefix_lens=None, selected_pages=None, cascade=None,
-          workspace=None, num_splits: int = 0):
+          workspace=None, num_segments: int = 0):
     """A pa_decode_opts by reference, or None when every setting is the default.
     selected_pages: [B, Hkv, topk] int32 tensor (topk taken from its last dim).
-    cascade: (group_offsets, group_seqs, group_prefix_len, cascade_workspace) tensors.
-    workspace: pa_decode's split workspace (uint8 tensor), num_splits (0: default)."""
+    cascade: (group_offsets, group_seqs, group_prefix_len, cascade_workspace) tensors,
+    optionally followed by (side stream, fork event, join event) for a cascade that runs
+    beside the split kernel (torch.cuda.Stream / torch.cuda.Event or raw handles).
+    workspace: pa_decode's split workspace (uint8 tensor), num_segments (0: default)."""
     if (not window and shared_prefix_lens is None and selected_pages is None and cascade is None
             and workspace is None):
         return None
     topk = 0 if selected_pages is None else int(selected_pages.shape[-1])
     groups = (0, None, None, None, None)
+    side = (None, (ctypes.c_void_p * 2)())
     if cascade is not None:
-        offsets, seqs, plen, ws = cascade
+        offsets, seqs, plen, ws = cascade[:4]
         groups = (int(offsets.numel()) - 1, _ptr(offsets), _ptr(seqs), _ptr(plen), _ptr(ws))
+        if len(cascade) > 4 and cascade[4] is not None:
+            stream, fork, join = cascade[4:7]
+            side = (_stream(stream), (ctypes.c_void_p * 2)(_event(fork), _event(join)))
     ws = (None, 0) if workspace is None else (_ptr(workspace),
                                               workspace.numel() * workspace.element_size())
     return ctypes.byref(pa_decode_opts(int(window), topk, _ptr(shared_prefix_lens),
-                                       _ptr(selected_pages), *groups, *ws, int(num_splits)))
+                                       _ptr(selected_pages), *groups, *ws, int(num_segments),
+                                       *side))
 
 
 class PAError(RuntimeError):
@@ -85,9 +94,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "pa_decode": (I32, [S, P, P, P, P, P, P, P, P, P, F, P, P]),
             "pa_splitkv_workspace_bytes": (ctypes.c_size_t, [S, I32]),
             "pa_default_num_splits": (I32, [S, I32]),
-            "pa_decode_splitkv": (I32, [S, P, P, ctypes.c_size_t, I32, P, P, P, P, P, P, P, P,
-                                        F, P, P]),
-            "pa_merge_lse": (I32, [S, P, P, I32, P]),
+            "pa_decode_workspace_bytes": (ctypes.c_size_t, [S, I32]),
+            "pa_default_num_segments": (I32, [S, I32]),
+            "pa_decode_splitkv": (I32, [S, P, P, I32, P, P, P, P, P, P, P, P, F, P, P]),
+            "pa_merge_lse": (I32, [S, P, P, P, I32, P]),
             "pa_status_string": (ctypes.c_char_p, [I32]),
             "pa_read_error_flag": (I32, [P, ctypes.POINTER(I32), P]),
             "pa_decode_splitkv_noalloc": (I32, [S, P, I32, P, P, P, P, P, P, P, F, P, P]),
@@ -131,6 +141,16 @@ def _stream(stream):
     return stream if isinstance(stream, int) else stream.cuda_stream
 
 
+def _event(event):
+    """cudaEvent_t of a torch.cuda.Event (created on first use) or a raw handle."""
+    if event is None or isinstance(event, int):
+        return event
+    if event.cuda_event == 0:          # torch creates the event lazily: record it once
+        import torch
+        event.record(torch.cuda.current_stream())
+    return event.cuda_event
+
+
 def make_shape(B, Hq, Hkv, D, block_size, nblocks, max_blocks, kv_dtype=PA_KV_BF16) -> pa_shape:
     return pa_shape(int(B), int(Hq), int(Hkv), int(D), int(block_size), int(nblocks),
                     int(max_blocks), int(kv_dtype))
@@ -155,15 +175,24 @@ def pa_reshape_and_cache(shape: pa_shape, k_new, v_new, k_pool, v_pool, k_scale,
 
 def pa_decode(shape: pa_shape, out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
               seq_lens, sm_scale: float, err_flag=None, stream=None, window: int = 0,
-              selected_pages=None, workspace=None, num_splits: int = 0,
+              selected_pages=None, workspace=None, num_segments: int = 0,
               shared_prefix_lens=None, cascade=None) -> None:
-    """workspace (uint8 device tensor): run the split decode and the merge in this call."""
+    """workspace (uint8 device tensor): run the split decode and the merge in this call
+    (cascade, see _opts, needs one)."""
     lib = load()
     _check("pa_decode", lib.pa_decode(
         ctypes.byref(shape), _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
         _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens),
-        _opts(window, shared_prefix_lens, selected_pages, cascade, workspace, num_splits),
+        _opts(window, shared_prefix_lens, selected_pages, cascade, workspace, num_segments),
         float(sm_scale), _ptr(err_flag), _stream(stream)))
+
+
+def pa_decode_workspace_bytes(shape: pa_shape, num_segments: int) -> int:
+    return int(load().pa_decode_workspace_bytes(ctypes.byref(shape), int(num_segments)))
+
+
+def pa_default_num_segments(shape: pa_shape, sm_count: int) -> int:
+    return int(load().pa_default_num_segments(ctypes.byref(shape), int(sm_count)))
 
 
 def pa_splitkv_workspace_bytes(shape: pa_shape, num_splits: int) -> int:
@@ -178,24 +207,23 @@ def pa_default_num_splits(shape: pa_shape, sm_count: int) -> int:
     return int(load().pa_default_num_splits(ctypes.byref(shape), int(sm_count)))
 
 
-def pa_decode_splitkv(shape: pa_shape, out, workspace, num_splits: int, q, k_pool, v_pool,
+def pa_decode_splitkv(shape: pa_shape, o_part, lse, num_splits: int, q, k_pool, v_pool,
                       k_scale, v_scale, block_tables, seq_lens, sm_scale: float, err_flag=None,
-                      stream=None, shared_prefix_lens=None, window: int = 0,
-                      selected_pages=None, cascade=None) -> None:
-    """cascade: (group_offsets, group_seqs, group_prefix_len, cascade_workspace)."""
+                      stream=None, window: int = 0, selected_pages=None,
+                      shared_prefix_lens=None) -> None:
+    """Partials o_part [B, Hq, S, D] and lse [B, Hq, S] (fp32 device tensors), S = num_splits."""
     lib = load()
-    nbytes = workspace.numel() * workspace.element_size()
     _check("pa_decode_splitkv", lib.pa_decode_splitkv(
-        ctypes.byref(shape), _ptr(out), _ptr(workspace), nbytes, int(num_splits), _ptr(q),
-        _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
-        _ptr(seq_lens), _opts(window, shared_prefix_lens, selected_pages, cascade),
-        float(sm_scale), _ptr(err_flag), _stream(stream)))
+        ctypes.byref(shape), _ptr(o_part), _ptr(lse), int(num_splits), _ptr(q), _ptr(k_pool),
+        _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens),
+        _opts(window, shared_prefix_lens, selected_pages), float(sm_scale), _ptr(err_flag),
+        _stream(stream)))
 
 
-def pa_merge_lse(shape: pa_shape, out, workspace, num_splits: int, stream=None) -> None:
+def pa_merge_lse(shape: pa_shape, out, o_part, lse, num_splits: int, stream=None) -> None:
     lib = load()
-    _check("pa_merge_lse", lib.pa_merge_lse(ctypes.byref(shape), _ptr(out), _ptr(workspace),
-                                            int(num_splits), _stream(stream)))
+    _check("pa_merge_lse", lib.pa_merge_lse(ctypes.byref(shape), _ptr(out), _ptr(o_part),
+                                            _ptr(lse), int(num_splits), _stream(stream)))
 
 
 def pa_read_error_flag(err_flag, stream=None) -> int:
@@ -208,14 +236,14 @@ def pa_read_error_flag(err_flag, stream=None) -> int:
     return int(v.value)
 
 
-def pa_decode_splitkv_noalloc(shape: pa_shape, out, num_splits: int, q, k_pool, v_pool,
+def pa_decode_splitkv_noalloc(shape: pa_shape, out, num_segments: int, q, k_pool, v_pool,
                               k_scale, v_scale, block_tables, seq_lens, sm_scale: float,
                               err_flag=None, stream=None) -> None:
     """Split-KV decode + merge with the library's own fixed scratch array, for
     callers that may not allocate device memory (see include/pa.h)."""
     lib = load()
     _check("pa_decode_splitkv_noalloc", lib.pa_decode_splitkv_noalloc(
-        ctypes.byref(shape), _ptr(out), int(num_splits), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        ctypes.byref(shape), _ptr(out), int(num_segments), _ptr(q), _ptr(k_pool), _ptr(v_pool),
         _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), float(sm_scale),
         _ptr(err_flag), _stream(stream)))
 

@@ -69,6 +69,8 @@ pa_status check_decode_args(const pa_shape *shape, const float *out, const void 
           (reinterpret_cast<uintptr_t>(opts->cascade_workspace) & 255u))
         return PA_ERR_INVALID_ARG;
       if (opts->window > 0 || opts->topk > 0) return PA_ERR_INVALID_ARG;
+      if (opts->cascade_stream && (!opts->cascade_events[0] || !opts->cascade_events[1]))
+        return PA_ERR_INVALID_ARG;
       if (shape->kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
       if (opts->num_prefix_groups > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
     }
@@ -77,6 +79,27 @@ pa_status check_decode_args(const pa_shape *shape, const float *out, const void 
 }
 
 constexpr int kMaxSplits = 65536;
+
+// Split workers resident at once: CTAs per SM by shared memory (227 KB usable per SM,
+// 1 KB reserved per CTA), capped by what the kernel's register budget was compiled
+// for, times warps per CTA.
+int resident_segments(const pa_shape *shape, int sm_count) {
+  const int per_cta = pa::splitkv_smem_bytes(*shape) + 1024;
+  const int warps = pa::decode_warps_per_cta();
+  int ctas = (227 * 1024) / per_cta;
+  if (ctas > pa::splitkv_min_blocks(*shape)) ctas = pa::splitkv_min_blocks(*shape);
+  if (ctas < 1) ctas = 1;
+  const int64_t n = static_cast<int64_t>(sm_count) * ctas * warps;
+  return static_cast<int>(n > kMaxSplits ? kMaxSplits : n);
+}
+
+pa_status current_sm_count(int *sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
 
 }  // namespace
 
@@ -108,13 +131,11 @@ pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void
   if (st != PA_OK) return st;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (opts && opts->workspace) {                   // split decode + merge in one call
-    int ns = opts->num_splits;
+    int ns = opts->num_segments;
     if (ns <= 0) {
-      int dev = 0, sms = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return PA_ERR_CUDA;
-      ns = pa_default_num_splits(shape, sms);
+      int sms = 0;
+      if (current_sm_count(&sms) != PA_OK) return PA_ERR_CUDA;
+      ns = resident_segments(shape, sms);
     }
     if (ns > kMaxSplits) return PA_ERR_INVALID_ARG;
     if (shape->B > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
@@ -130,9 +151,20 @@ pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void
                         opts, sm_scale, err_flag, cs);
 }
 
+size_t pa_decode_workspace_bytes(const pa_shape *shape, int32_t num_segments) {
+  if (check_shape(shape, true) != PA_OK || num_segments < 1 || num_segments > kMaxSplits)
+    return 0;
+  return pa::splitkv_layout(*shape, num_segments).total;
+}
+
+int32_t pa_default_num_segments(const pa_shape *shape, int32_t sm_count) {
+  if (check_shape(shape, true) != PA_OK || sm_count <= 0) return 1;
+  return resident_segments(shape, sm_count);
+}
+
 size_t pa_splitkv_workspace_bytes(const pa_shape *shape, int32_t num_splits) {
   if (check_shape(shape, true) != PA_OK || num_splits < 1 || num_splits > kMaxSplits) return 0;
-  return pa::splitkv_layout(*shape, num_splits).total;
+  return static_cast<size_t>(shape->B) * shape->Hq * num_splits * (shape->D + 1) * sizeof(float);
 }
 
 size_t pa_cascade_workspace_bytes(const pa_shape *shape) {
@@ -142,47 +174,50 @@ size_t pa_cascade_workspace_bytes(const pa_shape *shape) {
 
 int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count) {
   if (check_shape(shape, true) != PA_OK || sm_count <= 0) return 1;
-  // resident split workers: CTAs per SM by shared memory (227 KB usable per SM,
-  // 1 KB reserved per CTA), capped by what the kernel's register budget was
-  // compiled for, times warps per CTA
-  const int per_cta = pa::splitkv_smem_bytes(*shape) + 1024;
-  const int warps = pa::decode_warps_per_cta();
-  int ctas = (227 * 1024) / per_cta;
-  if (ctas > pa::splitkv_min_blocks(*shape)) ctas = pa::splitkv_min_blocks(*shape);
-  if (ctas < 1) ctas = 1;
-  const int64_t n = static_cast<int64_t>(sm_count) * ctas * warps;
-  return static_cast<int32_t>(n > kMaxSplits ? kMaxSplits : n);
+  // partial slots per query head: as many as 64 MiB of o_part holds, between 2 and 64,
+  // and no more than a sequence has 16-token tiles
+  const int64_t per_slot = static_cast<int64_t>(shape->B) * shape->Hq * shape->D * 4;
+  const int64_t max_tiles = (static_cast<int64_t>(shape->max_blocks) * shape->block_size + 15) / 16;
+  int64_t n = per_slot > 0 ? (int64_t(64) << 20) / per_slot : 64;
+  if (n > 64) n = 64;
+  if (n < 2) n = 2;
+  if (n > max_tiles) n = max_tiles;
+  return static_cast<int32_t>(n < 1 ? 1 : n);
 }
 
-pa_status pa_decode_splitkv(const pa_shape *shape, float *out, void *workspace,
-                            size_t workspace_bytes, int32_t num_splits, const void *q,
-                            const void *k_pool, const void *v_pool, const float *k_scale,
-                            const float *v_scale, const int32_t *block_tables,
-                            const int32_t *seq_lens, const pa_decode_opts *opts,
-                            float sm_scale, int32_t *err_flag, pa_stream_t stream) {
+pa_status pa_decode_splitkv(const pa_shape *shape, float *o_part, float *lse, int32_t num_splits,
+                            const void *q, const void *k_pool, const void *v_pool,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *block_tables, const int32_t *seq_lens,
+                            const pa_decode_opts *opts, float sm_scale, int32_t *err_flag,
+                            pa_stream_t stream) {
   if (!shape) return PA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARG;
   if (shape->B == 0) return check_shape(shape, true);
-  pa_status st = check_decode_args(shape, out, q, k_pool, v_pool, k_scale, v_scale,
+  pa_status st = check_decode_args(shape, o_part, q, k_pool, v_pool, k_scale, v_scale,
                                    block_tables, seq_lens, opts);
   if (st != PA_OK) return st;
-  if (num_splits < 1 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARG;
+  st = check_ptrs({lse});
+  if (st != PA_OK) return st;
+  if (opts && opts->num_prefix_groups > 0) return PA_ERR_UNSUPPORTED;
   if (shape->B > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
-  if (workspace_bytes < pa::splitkv_layout(*shape, num_splits).total) return PA_ERR_INVALID_ARG;
-  return pa::run_decode_splitkv(*shape, out, workspace, num_splits, q, k_pool, v_pool, k_scale,
-                                v_scale, block_tables, seq_lens, opts, sm_scale, err_flag,
-                                reinterpret_cast<cudaStream_t>(stream));
+  int sms = 0;
+  if (current_sm_count(&sms) != PA_OK) return PA_ERR_CUDA;
+  return pa::run_decode_parts(*shape, o_part, lse, num_splits, resident_segments(shape, sms), q,
+                              k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, opts,
+                              sm_scale, err_flag, reinterpret_cast<cudaStream_t>(stream));
 }
 
-pa_status pa_merge_lse(const pa_shape *shape, float *out, const void *workspace,
+pa_status pa_merge_lse(const pa_shape *shape, float *out, const float *o_part, const float *lse,
                        int32_t num_splits, pa_stream_t stream) {
   pa_status st = check_shape(shape, true);
   if (st != PA_OK) return st;
-  if (shape->B == 0) return PA_OK;
-  if (!out || !aligned16(out) || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return PA_ERR_INVALID_ARG;
   if (num_splits < 1 || num_splits > kMaxSplits) return PA_ERR_INVALID_ARG;
-  return pa::run_merge(*shape, out, workspace, num_splits, reinterpret_cast<cudaStream_t>(stream));
+  if (shape->B == 0) return PA_OK;
+  st = check_ptrs({out, o_part, lse});
+  if (st != PA_OK) return st;
+  return pa::run_merge_parts(*shape, out, o_part, lse, num_splits,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 pa_status pa_quest_summarize(const pa_shape *shape, const void *k_pool, void *key_summaries,

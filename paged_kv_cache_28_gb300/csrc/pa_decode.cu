@@ -120,7 +120,13 @@ struct Params {
   int32_t *prefix_out;   // workspace copy of the tile prefix, read by the merge
   float *o_part;
   float *lse_part;
-  int num_splits;
+  int num_splits;        // segments (split workers)
+  // pa_decode_splitkv: every piece goes to caller arrays parts_o [B, Hq, S, D] and
+  // parts_lse [B, Hq, S] (S = parts_S slots per query head, unused slots -inf);
+  // parts_S = 0: workspace mode (units finished in one segment go straight to out)
+  int parts_S;
+  float *parts_o;
+  float *parts_lse;
 };
 
 // ----------------------------------------------------------------------------
@@ -185,7 +191,7 @@ __device__ __forceinline__ uint32_t int4_pair_f16(uint32_t w, int i) {
 // qfs (lane-private: each lane reads back only what it wrote).
 template <class C>
 __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint16_t *qslot_ptr,
-                                       uint4 *qfs, int lane) {
+                                       uint4 *qfs, int G, int lane) {
   if constexpr (!C::QUANT) {
 #pragma unroll
     for (int nt = 0; nt < C::NT; ++nt)
@@ -216,8 +222,8 @@ __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint1
         // 4-bit: the eight values b..b+7 of chunk c arrive as two uint2 (u = 0, 1)
         const int off = C::INT4 ? (ks >> 1) * 32 + qd * 8 + (ks & 1) * 4 : ks * 16 + qd * 4;
         const uint2 *src = reinterpret_cast<const uint2 *>(qslot_ptr + (nt * 8 + r) * C::D + off);
-        if constexpr (C::QSMEM)
-          raw[nt][ks] = __ldg(src);
+        if constexpr (C::QSMEM)   // global memory: rows past the group read as zeros
+          raw[nt][ks] = nt * 8 + r < G ? __ldg(src) : make_uint2(0u, 0u);
         else
           raw[nt][ks] = *src;
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(raw[nt][ks].x)), fabsf(bf16_hi(raw[nt][ks].x))),
@@ -303,6 +309,10 @@ constexpr float kMaxSlack = 8.f;
 // accumulator is re-expressed in the tile's scale.
 constexpr float kRatMax = 128.f;
 constexpr float kRatMin = 1.f / 4096.f;
+// Quantised caches: largest restored |V| of a tile (V scale x largest code) for which P
+// enters the PV product as one f16 term; the term's rounding then adds at most
+// 2^-12 * 16 < 4e-3 to an output, a fifth of the quantised tolerance 2e-2.
+constexpr float kOneTermV = 16.f;
 
 // Tiles attended per (sequence, KV head): the window's tiles, the chosen pages, or
 // the tiles after a cascaded shared prefix.
@@ -317,7 +327,7 @@ __device__ __forceinline__ int pair_tile_count(int L, int window, int topk,
 // quantised tile; vzero[h]: the tile's V scale of the unit's KV head h is zero, so
 // its V rows count as zeros.  The accumulator stays in units of the piece's first
 // nonzero V scale: a tile with another scale enters through P scaled by the ratio.
-template <class C>
+template <class C, bool LO>
 __device__ __forceinline__ void process_tile(State<C> &st, const uint4 *qfs, uint32_t ktile,
                                              uint32_t vtile, int lo, int nvalid,
                                              const float (&sscale)[C::NT],
@@ -479,27 +489,43 @@ __device__ __forceinline__ void process_tile(State<C> &st, const uint4 *qfs, uin
       st.l[nt][j] += p[nt][j] + p[nt][j + 2];
     }
 
-  // ---- P^T fragments: hi + lo 16-bit parts, transposed in registers
+  // ---- P^T fragments, transposed in registers.  bf16 caches split p into two bf16
+  // terms, hi + lo (16 significant bits).  Quantised caches feed p times the tile's
+  // V-scale ratio as one f16 term (relative rounding <= 2^-12).  With LO (tiles whose
+  // restored V values exceed kOneTermV, chosen by the caller) the f16 remainder follows
+  // as a second term, 22 significant bits in all: its fragments are parked in the tile's
+  // K area (free once S is computed) and the same PV code runs a second time with them,
+  // so this rare instantiation needs no more registers than the common one.
   uint32_t bh[C::NT][2], bl[C::NT][2];
+  if constexpr (C::QUANT && LO) __syncwarp();   // every lane is done reading the K tile
 #pragma unroll
-  for (int nt = 0; nt < C::NT; ++nt) {
+  for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const float p0 = p[nt][2 * h], p1 = p[nt][2 * h + 1];
-      uint32_t hi, lo;
       if constexpr (!C::QUANT) {
-        hi = pack_bf16(p0, p1);
-        lo = pack_bf16(p0 - bf16_lo(hi), p1 - bf16_hi(hi));
+        const float p0 = p[nt][2 * h], p1 = p[nt][2 * h + 1];
+        const uint32_t hi = pack_bf16(p0, p1);
+        bh[nt][h] = movmatrix_trans(hi);
+        bl[nt][h] = movmatrix_trans(pack_bf16(p0 - bf16_lo(hi), p1 - bf16_hi(hi)));
       } else {
-        // f16 keeps 11 significant bits of p: one term is enough for the quantised
-        // caches' tolerance; the ratio carries this tile's V scale
-        hi = pack_f16(p0 * rat[nt], p1 * rat[nt]);
-        lo = 0;
+        const float p0 = p[nt][2 * h] * rat[nt], p1 = p[nt][2 * h + 1] * rat[nt];
+        const uint32_t hi = pack_f16(p0, p1);
+        bh[nt][h] = movmatrix_trans(hi);
+        if constexpr (LO) {
+          const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+          sts_u32(ktile + ((nt * 2 + h) * 32 + lane) * 4,
+                  movmatrix_trans(pack_f16(p0 - hf.x, p1 - hf.y)));
+        }
       }
-      bh[nt][h] = movmatrix_trans(hi);
-      if constexpr (!C::QUANT) bl[nt][h] = movmatrix_trans(lo);
     }
-  }
+  // the second pass of a quantised LO tile: the parked remainders become the P fragments
+  auto take_lo = [&]() {
+    __syncwarp();
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) bh[nt][h] = lds_u32(ktile + ((nt * 2 + h) * 32 + lane) * 4);
+  };
 
   // ---- O^T += V^T P^T.  A masked token has p = 0 exactly, but stale bf16 or E4M3 rows
   // may hold non-finite values (0 * NaN = NaN), so for those caches the V rows of a
@@ -541,33 +567,40 @@ __device__ __forceinline__ void process_tile(State<C> &st, const uint4 *qfs, uin
     // .. +3 of tokens 2q (low half) and 2q + 1 (high half): int4_pair_f16(., i) is
     // V^T row d = 32c + 4r + i over tokens (2q, 2q + 1).  Paired heads as for K.
     const int t = (lane & 7) + (((lane >> 3) & 1) << 3);
+    auto pv = [&]() {
 #pragma unroll
-    for (int h = 0; h < C::HEADS; ++h) {
+      for (int h = 0; h < C::HEADS; ++h) {
 #pragma unroll
-      for (int cc = 0; cc < C::D / 64; ++cc) {
-        const int c = 2 * cc + (lane >> 4);
-        uint32_t R[4];
-        if constexpr (C::PAIRED)
-          ldsm_x4_trans(R, vtile + t * 128 + (((4 * h + c) ^ (t & 7)) << 4));
-        else
-          ldsm_x4_trans(R, vtile + t * 64 + ((c ^ ((t >> 1) & 3)) << 4));
+        for (int cc = 0; cc < C::D / 64; ++cc) {
+          const int c = 2 * cc + (lane >> 4);
+          uint32_t R[4];
+          if constexpr (C::PAIRED)
+            ldsm_x4_trans(R, vtile + t * 128 + (((4 * h + c) ^ (t & 7)) << 4));
+          else
+            ldsm_x4_trans(R, vtile + t * 64 + ((c ^ ((t >> 1) & 3)) << 4));
 #pragma unroll
-        for (int half = 0; half < 2; ++half)    // chunk 2cc + half
+          for (int half = 0; half < 2; ++half)    // chunk 2cc + half
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {      // rows 4r + 2mt + {0, 1}
-            const uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * mt),
-                                   int4_pair_f16(R[2 * half], 2 * mt + 1),
-                                   int4_pair_f16(R[2 * half + 1], 2 * mt),
-                                   int4_pair_f16(R[2 * half + 1], 2 * mt + 1)};
-            const int dt = (2 * cc + half) * 2 + mt;
-            if constexpr (C::PAIRED) {
-              mma_f16(st.acc[h][dt], a, bh[h][0], bh[h][1]);
-            } else {
+            for (int mt = 0; mt < 2; ++mt) {      // rows 4r + 2mt + {0, 1}
+              const uint32_t a[4] = {int4_pair_f16(R[2 * half], 2 * mt),
+                                     int4_pair_f16(R[2 * half], 2 * mt + 1),
+                                     int4_pair_f16(R[2 * half + 1], 2 * mt),
+                                     int4_pair_f16(R[2 * half + 1], 2 * mt + 1)};
+              const int dt = (2 * cc + half) * 2 + mt;
+              if constexpr (C::PAIRED) {
+                mma_f16(st.acc[h][dt], a, bh[h][0], bh[h][1]);
+              } else {
 #pragma unroll
-              for (int nt = 0; nt < C::NT; ++nt) mma_f16(st.acc[nt][dt], a, bh[nt][0], bh[nt][1]);
+                for (int nt = 0; nt < C::NT; ++nt) mma_f16(st.acc[nt][dt], a, bh[nt][0], bh[nt][1]);
+              }
             }
-          }
+        }
       }
+    };
+    pv();
+    if constexpr (LO) {
+      take_lo();
+      pv();
     }
   } else {
     // ldmatrix.trans on byte pairs gives lane (r, q): bytes (t=2q: d=2r, 2r+1) and
@@ -611,6 +644,10 @@ __device__ __forceinline__ void process_tile(State<C> &st, const uint4 *qfs, uin
       }
     };
     if (ragged || vzero[0]) pv(std::true_type{}); else pv(std::false_type{});
+    if constexpr (LO) {
+      take_lo();
+      if (ragged || vzero[0]) pv(std::true_type{}); else pv(std::false_type{});
+    }
   }
 }
 
@@ -629,10 +666,12 @@ __device__ __forceinline__ void reduce_l(const State<C> &st, float (&ltot)[C::NT
     }
 }
 
-// Write o = acc / l (normalised) for heads < G to dst[g * D + d]; and lse if requested.
+// Write o = acc / l (normalised) for heads g < G to dst[g * hstride + d]; and, if
+// requested, lse to lse_dst[g * lstride].
 template <class C>
 __device__ __forceinline__ void write_normalised(const State<C> &st, float *dst, float *lse_dst,
-                                                 int G, int lane) {
+                                                 int G, int lane, size_t hstride = C::D,
+                                                 size_t lstride = 1) {
   float ltot[C::NT][2];
   reduce_l<C>(st, ltot);
   const int qd = lane & 3;
@@ -645,10 +684,11 @@ __device__ __forceinline__ void write_normalised(const State<C> &st, float *dst,
       const float f = (C::QUANT ? st.vref[nt] : 1.f) / ltot[nt][j];
 #pragma unroll
       for (int dt = 0; dt < C::DT; ++dt) {
-        dst[g * C::D + acc_d<C>(dt, j, lane)] = st.acc[nt][dt][j] * f;
-        dst[g * C::D + acc_d<C>(dt, j + 2, lane)] = st.acc[nt][dt][j + 2] * f;
+        dst[g * hstride + acc_d<C>(dt, j, lane)] = st.acc[nt][dt][j] * f;
+        dst[g * hstride + acc_d<C>(dt, j + 2, lane)] = st.acc[nt][dt][j + 2] * f;
       }
-      if (lse_dst && (lane >> 2) == 0) lse_dst[g] = (st.m[nt][j] + __log2f(ltot[nt][j])) * kLn2;
+      if (lse_dst && (lane >> 2) == 0)
+        lse_dst[g * lstride] = (st.m[nt][j] + __log2f(ltot[nt][j])) * kLn2;
     }
 }
 
@@ -929,10 +969,11 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
       if constexpr (C::QSMEM) {   // the group's query rows, straight from global memory
         const int b = u.y / p.Hkv, kvh = (u.w >> kKvhShift) & kKvhMask;
         load_q<C>(st, 0u, p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D, ws.qf,
-                  lane);
+                  p.G, lane);
       } else {
         load_q<C>(st, ktile + 2 * C::KV_BYTES,
-                  reinterpret_cast<const uint16_t *>(stage + 2 * C::KV_BYTES), nullptr, lane);
+                  reinterpret_cast<const uint16_t *>(stage + 2 * C::KV_BYTES), nullptr, p.G,
+                  lane);
       }
       piece_first = (u.w & kFirstOfPair) != 0;
     }
@@ -949,8 +990,18 @@ __device__ __forceinline__ bool run_warp(Src &src, const WarpSmem &ws, State<C> 
         vs[nt] = v;
       }
     }
-    process_tile<C>(st, ws.qf, ktile, ktile + C::KV_BYTES, (u.w >> kLoShift) & 0xF, u.w & 0xFF, sscale,
-                    vs, vzero, lane);
+    // quantised tiles whose restored V values exceed kOneTermV take the two-term weights
+    bool lo = false;
+    if constexpr (C::QUANT) {
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt) lo |= vs[nt] * (C::FP8 ? 448.f : 7.f) > kOneTermV;
+    }
+    if (lo)
+      process_tile<C, true>(st, ws.qf, ktile, ktile + C::KV_BYTES, (u.w >> kLoShift) & 0xF,
+                            u.w & 0xFF, sscale, vs, vzero, lane);
+    else
+      process_tile<C, false>(st, ws.qf, ktile, ktile + C::KV_BYTES, (u.w >> kLoShift) & 0xF,
+                             u.w & 0xFF, sscale, vs, vzero, lane);
     if (u.w & kPieceEnd) on_piece_end(u, piece_first, st);
     __syncwarp();
     if (i + C::STAGES < n) issue<C>(ws, s, src.get(i + C::STAGES, lane), p, tmK, tmV, lane);
@@ -1044,8 +1095,9 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 // Bounded wait with acquire at cluster scope; false if the phase never completed.
+template <uint32_t kSpins = kWaitSpins>
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitSpins; ++it) {
+  for (uint32_t it = 0; it < kSpins; ++it) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
@@ -1228,12 +1280,20 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   __syncthreads();
   if (crank > 0) {
     if (threadIdx.x == 0) mbar_arrive_cluster(cluster_map(cl_bar, 0));
-    // stay until CTA 0 has read this CTA's shared memory
-    if (!mbar_wait_cluster(cl_bar, 0) && threadIdx.x == 0) set_err(p.err, PA_DEVERR_TIMEOUT);
+    // stay until CTA 0 has read this CTA's shared memory; this wait is bounded four times
+    // longer than CTA 0's, so a CTA 0 that gave up (and reads nothing) is the only way
+    // it runs out
+    if (!mbar_wait_cluster<4 * kWaitSpins>(cl_bar, 0) && threadIdx.x == 0)
+      set_err(p.err, PA_DEVERR_TIMEOUT);
     return;
   }
-  if (active > 1 && !mbar_wait_cluster(cl_bar, 0) && threadIdx.x == 0)
-    set_err(p.err, PA_DEVERR_TIMEOUT);
+  // the other CTAs' states are complete once the phase completed for any thread
+  const bool merged = __syncthreads_or(active <= 1 || mbar_wait_cluster(cl_bar, 0));
+  if (!merged) {                     // no remote read: report, write zeros, release nobody
+    if (threadIdx.x == 0) set_err(p.err, PA_DEVERR_TIMEOUT);
+    for (int e = threadIdx.x; e < p.G * C::D; e += C::THREADS) out[e] = 0.f;
+    return;
+  }
   constexpr int kMaxCluster = 8;
   for (int e = threadIdx.x; e < p.G * C::D; e += C::THREADS) {
     const int g = e / C::D, d = e - g * C::D;
@@ -1271,14 +1331,15 @@ __device__ __forceinline__ int clamp_len(int L, int cap) { return min(max(L, 0),
 // Block-wide scan of the sequence lengths into shared memory:
 //   prefix[b] = Hkv * sum_{b' < b} count(b'),  prefix[B] = total tiles,
 // where count(b) is the number of 16-token tiles sequence b attends over.
-// Out-of-range lengths are clamped (and reported once, by CTA 0).
+// Out-of-range lengths are clamped (and reported once, by CTA 0).  Returns the
+// largest count (the longest unit).
 template <int THREADS>
-__device__ void scan_lengths(const Params &p, int32_t *prefix) {
+__device__ int scan_lengths(const Params &p, int32_t *prefix) {
   __shared__ int warp_sums[THREADS / 32];
-  __shared__ int carry_s;
+  __shared__ int carry_s, nmax_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cap = p.max_blocks * p.bs;
-  if (tid == 0) carry_s = 0;
+  if (tid == 0) carry_s = nmax_s = 0;
   __syncthreads();
   for (int base = 0; base < p.B; base += THREADS) {
     const int i = base + tid;
@@ -1288,7 +1349,9 @@ __device__ void scan_lengths(const Params &p, int32_t *prefix) {
       const int ct = p.casc_tiles ? p.casc_tiles[i] : 0;
       if ((L0 < 0 || L0 > cap || L0 < ct * kTile) && blockIdx.x == 0)
         set_err(p.err, PA_DEVERR_SEQ_LEN);
-      v = p.Hkv * pair_tile_count(clamp_len(L0, cap), p.window, p.topk, ct);
+      const int c = pair_tile_count(clamp_len(L0, cap), p.window, p.topk, ct);
+      if (c > 0) atomicMax(&nmax_s, c);
+      v = p.Hkv * c;
     }
     int x = v;
 #pragma unroll
@@ -1307,6 +1370,7 @@ __device__ void scan_lengths(const Params &p, int32_t *prefix) {
   }
   if (tid == 0) prefix[p.B] = carry_s;
   __syncthreads();
+  return nmax_s;
 }
 
 template <class C>
@@ -1319,10 +1383,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   WarpSmem ws = setup_smem<C>(smem_raw, warp, p.G, lane);
   int32_t *prefix = reinterpret_cast<int32_t *>(split_tail<C>(smem_raw));
   if (p.casc_tiles) pdl_wait();   // the cascaded tiles are written by the cascade kernel
-  scan_lengths<C::THREADS>(p, prefix);
+  const int nmax = scan_lengths<C::THREADS>(p, prefix);
   const int seg = blockIdx.x * C::WARPS + warp;
   const int total = prefix[p.B];
-  const int W = max(1, (total + p.num_splits - 1) / p.num_splits);
+  int W = max(1, (total + p.num_splits - 1) / p.num_splits);
+  // pa_decode_splitkv: a unit of n tiles is cut into at most ceil((n - 1) / W) + 1
+  // pieces, so W >= (nmax - 1) / (S - 1) keeps every unit within its S slots; with
+  // S = 1 the segment bounds move to the next unit start, so no unit is cut
+  const int S = p.parts_S;
+  if (S >= 2) W = max(W, (nmax - 1 + S - 2) / (S - 1));
   SegmentSource src;
   src.prefix = prefix;
   src.seq_lens = p.seq_lens;
@@ -1340,6 +1409,21 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   src.casc_tiles = p.casc_tiles;
   src.begin = min(seg * W, total);
   src.end = (seg < p.num_splits) ? min(src.begin + W, total) : src.begin;
+  if (S == 1) {
+    auto unit_start_at_or_after = [&](int f) {   // f <= total
+      if (f >= total) return total;
+      int lo = 0, hi = p.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= f) lo = mid; else hi = mid - 1;
+      }
+      const int nt = (prefix[lo + 1] - prefix[lo]) / p.Hkv;
+      const int us = prefix[lo] + (f - prefix[lo]) / nt * nt;
+      return us < f ? us + nt : us;
+    };
+    src.begin = unit_start_at_or_after(src.begin);
+    src.end = unit_start_at_or_after(src.end);
+  }
   // the chosen pages are written by the selection launched just before
   if (p.sel) pdl_wait();
   src.init(lane);
@@ -1347,7 +1431,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   // tables); the pools (written by the cache write) and the workspace (read by the
   // previous merge) are touched only after the previous grid has finished
   pdl_wait();
-  if (blockIdx.x == 0) {
+  if (S > 0) {
+    // sequences with no tile to attend have no piece: all their slots are empty
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+      if (prefix[b + 1] != prefix[b]) continue;
+      float *l = p.parts_lse + static_cast<size_t>(b) * p.Hq * S;
+      const size_t n = static_cast<size_t>(p.Hq) * S;
+      for (size_t i = threadIdx.x; i < n; i += C::THREADS) l[i] = -INFINITY;
+    }
+  } else if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i <= p.B; i += C::THREADS) p.prefix_out[i] = prefix[i];
     if (threadIdx.x == 0) {                 // for the merge: KV heads per unit, cascade
       p.prefix_out[p.B + 1] = C::HEADS;
@@ -1361,8 +1453,21 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       src, ws, st, p, &tmK, &tmV,
       [&](int4 u, bool piece_first, State<C> &s) {
         const int b = u.y / p.Hkv, kvh = u.y - b * p.Hkv;
-        if (piece_first && (u.w & kLastOfPair)) {   // the whole unit is in this segment
-          const size_t row = static_cast<size_t>(b) * p.Hq + kvh * p.G;
+        const size_t row = static_cast<size_t>(b) * p.Hq + kvh * p.G;
+        if (S > 0) {
+          // piece k of the unit: the segments before this one that hold its tiles
+          const int nt = (prefix[b + 1] - prefix[b]) / p.Hkv;
+          const int k = S == 1 ? 0 : seg - (prefix[b] + kvh * nt) / W;
+          write_normalised<C>(s, p.parts_o + (row * S + k) * C::D, p.parts_lse + row * S + k,
+                              p.G, lane, static_cast<size_t>(S) * C::D, S);
+          if (u.w & kLastOfPair) {              // the unit's last piece: later slots are empty
+            const int rest = S - 1 - k;
+            for (int i = lane; i < p.G * rest; i += 32) {
+              const int g = i / rest;
+              p.parts_lse[(row + g) * S + k + 1 + (i - g * rest)] = -INFINITY;
+            }
+          }
+        } else if (piece_first && (u.w & kLastOfPair)) {   // the whole unit is in this segment
           if (u.w & kCascade) {                     // joined with its shared prefix by the merge
             const CascadeLayout cl = cascade_layout(p.B, p.Hq, C::D);
             uint8_t *cw = reinterpret_cast<uint8_t *>(p.casc_ws);
@@ -1484,6 +1589,60 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
     const float inv = 1.f / den;
     reinterpret_cast<float4 *>(o)[e] = make_float4(num.x * inv, num.y * inv, num.z * inv,
                                                    num.w * inv);
+  }
+}
+
+// pa_merge_lse: one CTA per (sequence, KV head) group of query heads, threads over
+// (head, 4 consecutive d).  Partials of head (b, h) are o_part[b][h][i][:], lse[b][h][i]
+// for i < S; an lse of -inf marks an empty slot, whose o row is not read.  The slots
+// are visited eight at a time with their loads issued together and folded into a
+// running maximum; a head with no partial gets zeros.
+__global__ void __launch_bounds__(256) merge_parts_kernel(float *out, const float *o_part,
+                                                          const float *lse, int Hq, int G, int D,
+                                                          int S) {
+  pdl_trigger();
+  pdl_wait();
+  const size_t row0 = static_cast<size_t>(blockIdx.x) * G;   // first head b * Hq + kvh * G
+  const int D4 = D / 4;
+  constexpr int U = 8;
+  for (int e = threadIdx.x; e < G * D4; e += blockDim.x) {
+    const int g = e / D4, d4 = e - g * D4;
+    const size_t r = row0 + g;
+    const float *lr = lse + r * S;
+    const float4 *orow = reinterpret_cast<const float4 *>(o_part + r * S * D) + d4;
+    float M = -INFINITY, den = 0.f;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += U) {
+      float l[U];
+      float4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) l[u] = s0 + u < S ? __ldg(lr + s0 + u) : -INFINITY;
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        x[u] = l[u] != -INFINITY ? __ldg(orow + static_cast<size_t>(s0 + u) * D4)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+      float bm = l[0];
+#pragma unroll
+      for (int u = 1; u < U; ++u) bm = fmaxf(bm, l[u]);
+      if (bm > M) {                                // raise M once per batch
+        const float f = expf(M - bm);              // 0 while M is -inf
+        num = make_float4(num.x * f, num.y * f, num.z * f, num.w * f);
+        den *= f;
+        M = bm;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float w = l[u] == -INFINITY ? 0.f : expf(l[u] - M);
+        num.x += w * x[u].x;
+        num.y += w * x[u].y;
+        num.z += w * x[u].z;
+        num.w += w * x[u].w;
+        den += w;
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    reinterpret_cast<float4 *>(out + r * D)[d4] =
+        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
   }
 }
 
@@ -1745,18 +1904,6 @@ pa_status run_decode(const pa_shape &s, float *out, const void *q, const void *k
   return dispatch_pair(v, heads, p, mk, mv, stream);
 }
 
-// A non-blocking stream per device for work a call runs beside the caller's stream
-// (created on first use, kept for the life of the process).
-static cudaStream_t side_stream(int dev) {
-  static std::mutex mu;
-  static cudaStream_t streams[64] = {};
-  if (dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
-    streams[dev] = nullptr;
-  return streams[dev];
-}
-
 pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int num_splits,
                              const void *q, const void *k_pool, const void *v_pool,
                              const float *k_scale, const float *v_scale, const int32_t *bt,
@@ -1777,11 +1924,12 @@ pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int
   p.num_splits = num_splits;
   if (!opts || opts->num_prefix_groups <= 0) return dispatch_segments(v, heads, p, mk, mv, stream);
 
-  // Cascade: plan on the caller's stream, then fork.  The cascade kernel (tensor
-  // work on the shared prefixes) runs on a side stream with one CTA per SM, next to
-  // the split kernel (HBM streaming of the rest, two CTAs per SM); a second cascade
+  // Cascade: plan on the caller's stream.  Given a side stream, fork: the cascade
+  // kernel (tensor work on the shared prefixes) runs there with one CTA per SM, next
+  // to the split kernel (HBM streaming of the rest, two CTAs per SM); a second cascade
   // launch after the split kernel takes the items still left at full occupancy; the
-  // caller's stream waits for both before anything it runs next (the merge).
+  // caller's stream waits for both before anything it runs next (the merge).  Without
+  // one, the cascade runs after the split kernel on the caller's stream.
   pa_status st = run_cascade_plan(v, *opts, err, stream);
   if (st != PA_OK) return st;
   const CascadeLayout cl = cascade_layout(s.B, s.Hq, s.D);
@@ -1789,35 +1937,54 @@ pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int
       reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(opts->cascade_workspace) + cl.tiles);
   p.casc_ws = reinterpret_cast<uint64_t>(opts->cascade_workspace);
   int dev = 0, sms = 0;
-  cudaStream_t side = nullptr;
   if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      !(side = side_stream(dev)))
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PA_ERR_CUDA;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
-    if (fork) cudaEventDestroy(fork);
-    return PA_ERR_CUDA;
+  cudaStream_t side = reinterpret_cast<cudaStream_t>(opts->cascade_stream);
+  cudaEvent_t fork = reinterpret_cast<cudaEvent_t>(opts->cascade_events[0]);
+  cudaEvent_t join = reinterpret_cast<cudaEvent_t>(opts->cascade_events[1]);
+  if (side) {
+    if (cudaEventRecord(fork, stream) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
+      return PA_ERR_CUDA;
+    st = run_cascade(v, mk, mv, q, bt, *opts, sm_scale, err, sms, side);
+    if (st != PA_OK) return st;
+    if (cudaEventRecord(join, side) != cudaSuccess) return PA_ERR_CUDA;
   }
-  // (an event destroyed before the GPU reaches it is released once it completes)
-  struct Events {
-    cudaEvent_t a, b;
-    ~Events() {
-      cudaEventDestroy(a);
-      cudaEventDestroy(b);
-    }
-  } ev{fork, join};
-  if (cudaEventRecord(fork, stream) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
-    return PA_ERR_CUDA;
-  st = run_cascade(v, mk, mv, q, bt, *opts, sm_scale, err, sms, side);
-  if (st != PA_OK) return st;
-  if (cudaEventRecord(join, side) != cudaSuccess) return PA_ERR_CUDA;
   st = dispatch_segments(v, heads, p, mk, mv, stream);
   if (st != PA_OK) return st;
   st = run_cascade(v, mk, mv, q, bt, *opts, sm_scale, err, 3 * sms, stream);
   if (st != PA_OK) return st;
-  return cudaStreamWaitEvent(stream, join, 0) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  if (side && cudaStreamWaitEvent(stream, join, 0) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+pa_status run_decode_parts(const pa_shape &s, float *o_part, float *lse, int S, int workers,
+                           const void *q, const void *k_pool, const void *v_pool,
+                           const float *k_scale, const float *v_scale, const int32_t *bt,
+                           const int32_t *sl, const pa_decode_opts *opts, float sm_scale,
+                           int32_t *err, cudaStream_t stream) {
+  const int heads = heads_per_unit(s, opts);
+  const pa_shape v = unit_view(s, heads);
+  CUtensorMap mk, mv;
+  if (!make_pool_map(&mk, k_pool, v, heads) || !make_pool_map(&mv, v_pool, v, heads))
+    return PA_ERR_CUDA;
+  Params p = make_params(v, nullptr, q, k_scale, v_scale, bt, sl, opts, sm_scale, err);
+  p.shared_prefix_lens = opts ? opts->shared_prefix_lens : nullptr;
+  p.num_splits = workers;
+  p.parts_S = S;
+  p.parts_o = o_part;
+  p.parts_lse = lse;
+  return dispatch_segments(v, heads, p, mk, mv, stream);
+}
+
+pa_status run_merge_parts(const pa_shape &s, float *out, const float *o_part, const float *lse,
+                          int S, cudaStream_t stream) {
+  const int G = s.Hq / s.Hkv;
+  const int threads = min(256, max(32, ((G * s.D / 4) + 31) / 32 * 32));
+  return launch_pdl(merge_parts_kernel, dim3(s.B * s.Hkv), dim3(threads), 0, stream, out, o_part,
+                    lse, s.Hq, G, s.D, S) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int num_splits,

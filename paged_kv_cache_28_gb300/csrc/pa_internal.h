@@ -118,6 +118,16 @@ pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int
 pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int num_splits,
                     cudaStream_t stream);
 
+// pa_decode_splitkv / pa_merge_lse: the split kernel over `workers` segments with every
+// piece written to caller arrays o_part [B, Hq, S, D] / lse [B, Hq, S], and their merge.
+pa_status run_decode_parts(const pa_shape &s, float *o_part, float *lse, int S, int workers,
+                           const void *q, const void *k_pool, const void *v_pool,
+                           const float *k_scale, const float *v_scale, const int32_t *bt,
+                           const int32_t *sl, const pa_decode_opts *opts, float sm_scale,
+                           int32_t *err, cudaStream_t stream);
+pa_status run_merge_parts(const pa_shape &s, float *out, const float *o_part, const float *lse,
+                          int S, cudaStream_t stream);
+
 pa_status run_quest_summarize(const pa_shape &s, const void *k_pool, void *summaries,
                               const int64_t *slot_mapping, int32_t *err, cudaStream_t stream);
 int quest_max_pages(const pa_shape &s);

@@ -53,8 +53,9 @@ class DeviceBatch:
                                device=self.device)
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.workspace = None
-        self.num_splits = None
+        self.num_segments = None
         self.cascade = None
+        self.o_part = self.lse = None
 
     # -- calls -----------------------------------------------------------------
 
@@ -64,52 +65,84 @@ class DeviceBatch:
                                   stream)
 
     def decode(self, stream=None, window: int = 0, selected_pages=None,
-               workspace: bool = False, hints: bool = False):
-        """pa_decode; workspace: hand it a split workspace (the default split count), so
-        that it runs the split decode and the merge itself; hints: pass the batch's
-        shared-prefix lengths (if any)."""
+               workspace: bool = False, hints: bool = False, num_segments: int | None = None,
+               cascade: bool = False):
+        """pa_decode; workspace: hand it a split workspace (num_segments, default: the
+        resident split workers), so that it runs the split decode and the merge itself;
+        hints: pass the batch's shared-prefix lengths (if any); cascade: attend over the
+        prefix groups (enable_cascade) once per group (needs the workspace)."""
         ws = None
-        if workspace:
-            self.ensure_workspace(default_num_splits(self.shape, self.device))
+        if workspace or cascade:
+            ns = default_num_segments(self.shape, self.device) if num_segments is None else num_segments
+            if self.workspace is None or self.num_segments != ns:
+                self.ensure_workspace(ns)
             ws = self.workspace
+        if cascade and self.cascade is None:
+            self.enable_cascade()
         _lib.pa_decode(self.shape, self.out, self.q, self.k_pool, self.v_pool, self.k_scale,
                        self.v_scale, self.block_tables, self.seq_lens, self.batch.sm_scale,
                        self.err, stream, window, selected_pages, ws,
-                       shared_prefix_lens=self.shared_prefix_lens if hints else None)
+                       self.num_segments if ws is not None else 0,
+                       shared_prefix_lens=self.shared_prefix_lens if hints else None,
+                       cascade=self.cascade if cascade else None)
 
-    def ensure_workspace(self, num_splits: int):
-        nbytes = _lib.pa_splitkv_workspace_bytes(self.shape, num_splits)
+    def ensure_workspace(self, num_segments: int):
+        nbytes = _lib.pa_decode_workspace_bytes(self.shape, num_segments)
         if nbytes == 0:
-            raise ValueError("invalid shape or num_splits for split-KV")
+            raise ValueError("invalid shape or num_segments for the split decode")
         if self.workspace is None or self.workspace.numel() < nbytes:
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
-        self.num_splits = num_splits
+        self.num_segments = num_segments
 
-    def enable_cascade(self, groups=None):
-        """Prefix-aware decode for decode_splitkv: groups = (group_offsets, group_seqs,
-        group_prefix_len) int32 arrays, by default the batch's own prefix groups."""
+    def enable_cascade(self, groups=None, side_stream: bool = True):
+        """Prefix-aware decode: groups = (group_offsets, group_seqs, group_prefix_len) int32
+        arrays, by default the batch's own prefix groups; side_stream: run the cascade
+        kernel beside the split kernel on a stream of its own (else after it)."""
         offsets, seqs, plen = cascade_groups(self.batch) if groups is None else groups
         ws = torch.empty(_lib.pa_cascade_workspace_bytes(self.shape), dtype=torch.uint8,
                          device=self.device)
         self.cascade = tuple(torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(
             self.device) for a in (offsets, seqs, plen)) + (ws,)
+        if side_stream:
+            events = []
+            for _ in range(2):           # created now (recorded once), reused by every call
+                e = torch.cuda.Event()
+                e.record(torch.cuda.current_stream(self.device))
+                events.append(e)
+            self.cascade = self.cascade + (torch.cuda.Stream(self.device), *events)
 
-    def decode_splitkv(self, num_splits: int | None = None, stream=None, hints: bool = True,
-                       window: int = 0, selected_pages=None, cascade: bool = False):
-        """Split-KV decode + merge; hints: pass the batch's shared-prefix lengths (if any);
-        cascade: attend over the prefix groups (enable_cascade) once per group."""
+    def decode_segments(self, num_segments: int | None = None, stream=None, hints: bool = True,
+                        window: int = 0, selected_pages=None, cascade: bool = False):
+        """pa_decode with a workspace of num_segments (the load-balanced split decode and
+        its merge); hints: pass the batch's shared-prefix lengths (if any); cascade: attend
+        over the prefix groups (enable_cascade) once per group."""
+        self.decode(stream, window, selected_pages, workspace=True, hints=hints,
+                    num_segments=num_segments, cascade=cascade)
+
+    def ensure_parts(self, num_splits: int):
+        """Caller-visible partials o_part [B, Hq, S, D] and lse [B, Hq, S]."""
+        b = self.batch
+        if getattr(self, "o_part", None) is None or self.o_part.shape[2] != num_splits:
+            self.o_part = torch.empty((b.B, b.Hq, num_splits, b.D), dtype=torch.float32,
+                                      device=self.device)
+            self.lse = torch.empty((b.B, b.Hq, num_splits), dtype=torch.float32,
+                                   device=self.device)
+
+    def decode_splitkv(self, num_splits: int | None = None, stream=None, merge: bool = True,
+                       window: int = 0, selected_pages=None, hints: bool = False):
+        """pa_decode_splitkv into o_part / lse (num_splits slots per query head, default
+        pa_default_num_splits), then pa_merge_lse into out; hints: pass the batch's
+        shared-prefix lengths (if any)."""
         if num_splits is None:
             num_splits = default_num_splits(self.shape, self.device)
-        if self.workspace is None or self.num_splits != num_splits:
-            self.ensure_workspace(num_splits)
-        if cascade and self.cascade is None:
-            self.enable_cascade()
-        _lib.pa_decode_splitkv(self.shape, self.out, self.workspace, num_splits, self.q,
+        self.ensure_parts(num_splits)
+        _lib.pa_decode_splitkv(self.shape, self.o_part, self.lse, num_splits, self.q,
                                self.k_pool, self.v_pool, self.k_scale, self.v_scale,
                                self.block_tables, self.seq_lens, self.batch.sm_scale, self.err,
-                               stream, self.shared_prefix_lens if hints else None, window,
-                               selected_pages, self.cascade if cascade else None)
-        _lib.pa_merge_lse(self.shape, self.out, self.workspace, num_splits, stream)
+                               stream, window, selected_pages,
+                               self.shared_prefix_lens if hints else None)
+        if merge:
+            _lib.pa_merge_lse(self.shape, self.out, self.o_part, self.lse, num_splits, stream)
 
     # -- Quest page selection ------------------------------------------------------
 
@@ -165,6 +198,15 @@ class DeviceBatch:
                 self.v_pool.view(torch.int16).cpu().numpy().view(np.uint16), None, None)
 
 
+def _sm_count(device=None) -> int:
+    return torch.cuda.get_device_properties(device or 0).multi_processor_count
+
+
+def default_num_segments(shape, device=None) -> int:
+    """Segments of pa_decode's split decode: the resident split workers."""
+    return _lib.pa_default_num_segments(shape, _sm_count(device))
+
+
 def default_num_splits(shape, device=None) -> int:
-    sms = torch.cuda.get_device_properties(device or 0).multi_processor_count
-    return _lib.pa_default_num_splits(shape, sms)
+    """Partial slots per query head of pa_decode_splitkv."""
+    return _lib.pa_default_num_splits(shape, _sm_count(device))

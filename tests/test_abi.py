@@ -103,44 +103,73 @@ def test_empty_batch_is_a_no_op(lib):
     assert _decode(lib, ctypes.byref(shape(B=0)), q=None) == _lib.PA_OK
 
 
-def test_splitkv_host_checks(lib):
-    import ctypes
+def test_decode_workspace_bytes(lib):
     s = shape(B=64, Hq=64, Hkv=8, D=128, max_blocks=2048, nblocks=30000)
-    nbytes = _lib.pa_splitkv_workspace_bytes(s, 1216)
+    nbytes = _lib.pa_decode_workspace_bytes(s, 1216)
     G = 8
-    expect_min = (65 * 4) + 1216 * 2 * G * 4 + 1216 * 2 * G * 128 * 4
+    expect_min = (68 * 4) + 1216 * 2 * G * 4 + 1216 * 2 * G * 128 * 4
     assert expect_min <= nbytes <= expect_min + 3 * 256
-    assert _lib.pa_splitkv_workspace_bytes(s, 0) == 0
-    assert _lib.pa_splitkv_workspace_bytes(s, 70000) == 0
+    assert _lib.pa_decode_workspace_bytes(s, 0) == 0
+    assert _lib.pa_decode_workspace_bytes(s, 70000) == 0
     # 4-bit pools read two KV heads at a time: partials of 16 query heads per piece
     s4 = shape(B=64, Hq=64, Hkv=8, D=128, max_blocks=2048, nblocks=30000,
                kv_dtype=_lib.PA_KV_INT4)
-    n4 = _lib.pa_splitkv_workspace_bytes(s4, 1216)
-    expect4 = (66 * 4) + 1216 * 2 * 16 * 4 + 1216 * 2 * 16 * 128 * 4
+    n4 = _lib.pa_decode_workspace_bytes(s4, 1216)
+    expect4 = (68 * 4) + 1216 * 2 * 16 * 4 + 1216 * 2 * 16 * 128 * 4
     assert expect4 <= n4 <= expect4 + 3 * 256
-    args = [ctypes.byref(s), FAKE, FAKE, nbytes - 1, 1216, FAKE, FAKE, FAKE, None, None, FAKE,
-            FAKE, None, 0.1, None, None]
-    assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # workspace too small
-    args[3] = nbytes
-    args[2] = FAKE + 16
-    assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # workspace not 256-aligned
-    args[2] = FAKE
-    args[12] = ctypes.byref(_lib.pa_decode_opts(0, 0, FAKE + 4, None))
-    assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_INVALID_ARG    # hint array misaligned
-    args[12] = None
-    assert lib.pa_merge_lse(ctypes.byref(s), FAKE, FAKE, 0, None) == _lib.PA_ERR_INVALID_ARG
-    big = _lib.make_shape(16385, 8, 8, 128, 16, 30000, 4)
-    args[0] = ctypes.byref(big)
-    args[3] = _lib.pa_splitkv_workspace_bytes(big, 1216)
-    args[2] = FAKE
-    assert lib.pa_decode_splitkv(*args) == _lib.PA_ERR_UNSUPPORTED      # B > 16384
 
 
-def test_default_num_splits_is_resident_warps(lib):
+def test_splitkv_partials_host_checks(lib):
+    import ctypes
     s = shape(B=64, Hq=64, Hkv=8, D=128, max_blocks=2048, nblocks=30000)
-    n = _lib.pa_default_num_splits(s, 152)
+    assert _lib.pa_splitkv_workspace_bytes(s, 16) == 64 * 64 * 16 * 129 * 4   # o_part + lse
+    assert _lib.pa_splitkv_workspace_bytes(s, 0) == 0
+    assert _lib.pa_splitkv_workspace_bytes(s, 70000) == 0
+
+    def call(sh, o=FAKE, lse=FAKE, S=16, opts=None):
+        return lib.pa_decode_splitkv(ctypes.byref(sh), o, lse, S, FAKE, FAKE, FAKE, None, None,
+                                     FAKE, FAKE, opts, 0.1, None, None)
+
+    assert call(s, lse=None) == _lib.PA_ERR_INVALID_ARG          # no lse array
+    assert call(s, lse=FAKE + 4) == _lib.PA_ERR_INVALID_ARG      # misaligned
+    assert call(s, o=None) == _lib.PA_ERR_INVALID_ARG
+    assert call(s, S=0) == _lib.PA_ERR_INVALID_ARG
+    assert call(s, S=70000) == _lib.PA_ERR_INVALID_ARG
+    assert call(shape(B=0), o=None, lse=None) == _lib.PA_OK      # nothing to do
+    assert call(_lib.make_shape(16385, 8, 8, 128, 16, 30000, 4)) == _lib.PA_ERR_UNSUPPORTED
+    cascade = _lib.pa_decode_opts(0, 0, None, None, 1, FAKE, FAKE, FAKE, FAKE)
+    assert call(s, opts=ctypes.byref(cascade)) == _lib.PA_ERR_UNSUPPORTED   # no cascade here
+    window = _lib.pa_decode_opts(-1, 0, None, None)
+    assert call(s, opts=ctypes.byref(window)) == _lib.PA_ERR_INVALID_ARG
+
+    def merge(sh, out=FAKE, o=FAKE, lse=FAKE, S=16):
+        return lib.pa_merge_lse(ctypes.byref(sh), out, o, lse, S, None)
+
+    assert merge(s, S=0) == _lib.PA_ERR_INVALID_ARG
+    assert merge(s, o=None) == _lib.PA_ERR_INVALID_ARG
+    assert merge(s, lse=FAKE + 8) == _lib.PA_ERR_INVALID_ARG
+    assert merge(shape(Hq=6, Hkv=4)) == _lib.PA_ERR_INVALID_ARG
+    assert merge(shape(B=0), out=None, o=None, lse=None) == _lib.PA_OK
+
+
+def test_default_num_segments_is_resident_warps(lib):
+    s = shape(B=64, Hq=64, Hkv=8, D=128, max_blocks=2048, nblocks=30000)
+    n = _lib.pa_default_num_segments(s, 152)
     assert n % 152 == 0 and 152 * 4 <= n <= 152 * 16
-    assert _lib.pa_default_num_splits(s, 0) == 1
+    assert _lib.pa_default_num_segments(s, 0) == 1
+
+
+def test_default_num_splits_fills_64_mib_of_partials(lib):
+    # one slot of o_part is B * Hq * D * 4 bytes: the most slots in 64 MiB, 2..64, and at
+    # most the 16-token tiles of a full block table
+    def ns(**kw):
+        return _lib.pa_default_num_splits(shape(**kw), 152)
+    assert ns(B=64, Hq=64, Hkv=8, D=128, max_blocks=2048, nblocks=30000) == 32     # 2 MiB/slot
+    assert ns(B=8, Hq=64, Hkv=8, D=128, max_blocks=4096, nblocks=30000, block_size=32) == 64
+    assert ns(B=512, Hq=64, Hkv=8, D=128, max_blocks=256, nblocks=30000) == 4      # 16 MiB/slot
+    assert ns(B=4096, Hq=64, Hkv=8, D=128, max_blocks=256, nblocks=30000) == 2
+    assert ns(B=4, max_blocks=1) == 1                                              # one tile
+    assert _lib.pa_default_num_splits(shape(), 0) == 1
 
 
 def test_reshape_rejects_bad_args(lib):
@@ -156,7 +185,7 @@ def test_reshape_rejects_bad_args(lib):
 def test_decode_workspace_host_checks(lib):
     import ctypes
     s = shape(B=8, Hq=64, Hkv=8, D=128, max_blocks=64, nblocks=512)
-    need = _lib.pa_splitkv_workspace_bytes(s, 16)
+    need = _lib.pa_decode_workspace_bytes(s, 16)
 
     def call(ws, nbytes, ns):
         o = _lib.pa_decode_opts(0, 0, None, None, 0, None, None, None, None, ws, nbytes, ns)
@@ -165,22 +194,28 @@ def test_decode_workspace_host_checks(lib):
 
     assert call(FAKE, need - 1, 16) == _lib.PA_ERR_INVALID_ARG         # too small
     assert call(FAKE + 16, need, 16) == _lib.PA_ERR_INVALID_ARG        # not 256-aligned
-    assert call(FAKE, need, 70000) == _lib.PA_ERR_INVALID_ARG          # too many splits
+    assert call(FAKE, need, 70000) == _lib.PA_ERR_INVALID_ARG          # too many segments
+    big = _lib.make_shape(16385, 8, 8, 128, 16, 30000, 4)
+    o = _lib.pa_decode_opts(0, 0, None, None, 0, None, None, None, None, FAKE,
+                            _lib.pa_decode_workspace_bytes(big, 16), 16)
+    assert lib.pa_decode(ctypes.byref(big), FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE,
+                         ctypes.byref(o), 0.1, None, None) == _lib.PA_ERR_UNSUPPORTED   # B > 16384
 
 
 def test_cascade_host_checks(lib):
     import ctypes
     s = shape(B=8, Hq=64, Hkv=8, D=128, max_blocks=64, nblocks=512)
-    ws = _lib.pa_splitkv_workspace_bytes(s, 16)
+    ws = _lib.pa_decode_workspace_bytes(s, 16)
     cb = _lib.pa_cascade_workspace_bytes(s)
     assert cb >= 8 * 64 * 4 * 129 * 4 and _lib.pa_cascade_workspace_bytes(shape(Hq=7)) == 0
 
     def call(sh, opts):
-        return lib.pa_decode_splitkv(ctypes.byref(sh), FAKE, FAKE, ws, 16, FAKE, FAKE, FAKE,
-                                     None, None, FAKE, FAKE, ctypes.byref(opts), 0.1, None, None)
+        return lib.pa_decode(ctypes.byref(sh), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             ctypes.byref(opts), 0.1, None, None)
 
-    def opts(n=1, offs=FAKE, seqs=FAKE, plen=FAKE, cws=FAKE, window=0):
-        return _lib.pa_decode_opts(window, 0, None, None, n, offs, seqs, plen, cws)
+    def opts(n=1, offs=FAKE, seqs=FAKE, plen=FAKE, cws=FAKE, window=0, stream=None, events=(None, None)):
+        return _lib.pa_decode_opts(window, 0, None, None, n, offs, seqs, plen, cws, FAKE, ws, 16,
+                                   stream, (ctypes.c_void_p * 2)(*events))
 
     assert call(s, opts(n=-1)) == _lib.PA_ERR_INVALID_ARG
     assert call(s, opts(seqs=None)) == _lib.PA_ERR_INVALID_ARG          # no member list
@@ -188,11 +223,11 @@ def test_cascade_host_checks(lib):
     assert call(s, opts(cws=FAKE + 16)) == _lib.PA_ERR_INVALID_ARG      # not 256-aligned
     assert call(s, opts(offs=FAKE + 2)) == _lib.PA_ERR_INVALID_ARG      # misaligned int32
     assert call(s, opts(window=64)) == _lib.PA_ERR_INVALID_ARG          # not with a window
+    assert call(s, opts(stream=FAKE)) == _lib.PA_ERR_INVALID_ARG        # side stream, no events
+    assert call(s, opts(stream=FAKE, events=(FAKE, None))) == _lib.PA_ERR_INVALID_ARG
     fp8 = shape(B=8, Hq=64, Hkv=8, D=128, max_blocks=64, nblocks=512,
                 kv_dtype=_lib.PA_KV_FP8_E4M3)
-    assert lib.pa_decode_splitkv(ctypes.byref(fp8), FAKE, FAKE, ws, 16, FAKE, FAKE, FAKE, FAKE,
-                                 FAKE, FAKE, FAKE, ctypes.byref(opts()), 0.1, None,
-                                 None) == _lib.PA_ERR_UNSUPPORTED        # bf16 pools only
+    assert call(fp8, opts()) == _lib.PA_ERR_UNSUPPORTED                 # bf16 pools only
 
 
 def test_quest_host_checks(lib):
