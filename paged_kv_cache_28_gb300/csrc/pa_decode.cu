@@ -1592,58 +1592,50 @@ __global__ void __launch_bounds__(256) merge_kernel(float *out, const int32_t *p
   }
 }
 
-// pa_merge_lse: one CTA per (sequence, KV head) group of query heads, threads over
-// (head, 4 consecutive d).  Partials of head (b, h) are o_part[b][h][i][:], lse[b][h][i]
-// for i < S; an lse of -inf marks an empty slot, whose o row is not read.  The slots
-// are visited eight at a time with their loads issued together and folded into a
-// running maximum; a head with no partial gets zeros.
-__global__ void __launch_bounds__(256) merge_parts_kernel(float *out, const float *o_part,
-                                                          const float *lse, int Hq, int G, int D,
-                                                          int S) {
+// pa_merge_lse: one warp per query head (b, h), a CTA per (sequence, KV head) group.
+// Partials of the head are o_part[b][h][i][:], lse[b][h][i] for i < S; an lse of -inf
+// (or a weight that underflows to 0) marks an empty slot, whose o row is not read.
+// Lane i reads slot i of each 32-slot chunk: the running maximum and the normaliser take
+// warp reductions, and only the non-empty slots' o rows are read (each row coalesced
+// over the warp, D / 32 elements per lane).  A head with no partial gets zeros.
+template <int D>
+__global__ void __launch_bounds__(512) merge_parts_kernel(float *out, const float *o_part,
+                                                          const float *lse, int G, int S) {
   pdl_trigger();
   pdl_wait();
-  const size_t row0 = static_cast<size_t>(blockIdx.x) * G;   // first head b * Hq + kvh * G
-  const int D4 = D / 4;
-  constexpr int U = 8;
-  for (int e = threadIdx.x; e < G * D4; e += blockDim.x) {
-    const int g = e / D4, d4 = e - g * D4;
-    const size_t r = row0 + g;
-    const float *lr = lse + r * S;
-    const float4 *orow = reinterpret_cast<const float4 *>(o_part + r * S * D) + d4;
-    float M = -INFINITY, den = 0.f;
-    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < S; s0 += U) {
-      float l[U];
-      float4 x[U];
+  constexpr int E = D / 32;   // elements per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t r = static_cast<size_t>(blockIdx.x) * G + warp;   // head row b * Hq + h
+  const float *lr = lse + r * S;
+  const float *orow = o_part + r * S * D;
+  float M = -INFINITY;
+  for (int s0 = 0; s0 < S; s0 += 32)
+    M = fmaxf(M, s0 + lane < S ? __ldg(lr + s0 + lane) : -INFINITY);
 #pragma unroll
-      for (int u = 0; u < U; ++u) l[u] = s0 + u < S ? __ldg(lr + s0 + u) : -INFINITY;
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float acc[E];
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        x[u] = l[u] != -INFINITY ? __ldg(orow + static_cast<size_t>(s0 + u) * D4)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-      float bm = l[0];
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float den = 0.f;
+  if (M != -INFINITY) {
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const float l = s0 + lane < S ? __ldg(lr + s0 + lane) : -INFINITY;
+      const float w = l == -INFINITY ? 0.f : expf(l - M);
+      den += w;
+      for (uint32_t live = __ballot_sync(0xffffffffu, w > 0.f); live; live &= live - 1) {
+        const int j = __ffs(live) - 1;
+        const float wj = __shfl_sync(0xffffffffu, w, j);
+        const float *x = orow + static_cast<size_t>(s0 + j) * D;
 #pragma unroll
-      for (int u = 1; u < U; ++u) bm = fmaxf(bm, l[u]);
-      if (bm > M) {                                // raise M once per batch
-        const float f = expf(M - bm);              // 0 while M is -inf
-        num = make_float4(num.x * f, num.y * f, num.z * f, num.w * f);
-        den *= f;
-        M = bm;
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const float w = l[u] == -INFINITY ? 0.f : expf(l[u] - M);
-        num.x += w * x[u].x;
-        num.y += w * x[u].y;
-        num.z += w * x[u].z;
-        num.w += w * x[u].w;
-        den += w;
+        for (int e = 0; e < E; ++e) acc[e] += wj * __ldg(x + e * 32 + lane);
       }
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    reinterpret_cast<float4 *>(out + r * D)[d4] =
-        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) out[r * D + e * 32 + lane] = acc[e] * inv;
 }
 
 // ----------------------------------------------------------------------------
@@ -1979,12 +1971,12 @@ pa_status run_decode_parts(const pa_shape &s, float *o_part, float *lse, int S, 
 
 pa_status run_merge_parts(const pa_shape &s, float *out, const float *o_part, const float *lse,
                           int S, cudaStream_t stream) {
-  const int G = s.Hq / s.Hkv;
-  const int threads = min(256, max(32, ((G * s.D / 4) + 31) / 32 * 32));
-  return launch_pdl(merge_parts_kernel, dim3(s.B * s.Hkv), dim3(threads), 0, stream, out, o_part,
-                    lse, s.Hq, G, s.D, S) == cudaSuccess
-             ? PA_OK
-             : PA_ERR_CUDA;
+  const int G = s.Hq / s.Hkv;   // <= 16: a CTA of at most 512 threads
+  const dim3 grid(s.B * s.Hkv), block(32 * G);
+  const cudaError_t e =
+      s.D == 128 ? launch_pdl(merge_parts_kernel<128>, grid, block, 0, stream, out, o_part, lse, G, S)
+                 : launch_pdl(merge_parts_kernel<64>, grid, block, 0, stream, out, o_part, lse, G, S);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status run_merge(const pa_shape &s, float *out, const void *workspace, int num_splits,
