@@ -911,6 +911,42 @@ def _cascade_batch(Hq, Hkv, D, bs, groups, free_lens, seed, plens=None):
     return batch, (offsets, seqs, plen)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,lens_kind", [(64, 8, 128, "mixed"), (48, 8, 128, "mixed"),
+                                                 (64, 8, 64, "mixed"), (64, 64, 128, "short")])
+def test_pa_decode_many_units(Hq, Hkv, D, lens_kind):
+    """pa_decode without a workspace on bf16 batches of at most 256 sequences with more
+    (sequence, KV head) units than CTAs at once (one CTA per unit, longest sequences
+    first): lengths from 0 up with a few long ones; G = 8 and 6 (a padded group); D = 128
+    and 64; and 12,800 short units.  Against the oracle, with a window and with Quest
+    pages too, and repeatable bit for bit."""
+    rng = np.random.default_rng(500 + Hq + Hkv + D)
+    if lens_kind == "mixed":
+        lens = list(rng.integers(0, 600, 110)) + [0, 1, 15, 16, 17] + [4000, 2500]
+    else:
+        lens = list(rng.integers(1, 40, 200))          # 12,800 units
+    batch = wl.build_batch("t", lens, Hq=Hq, Hkv=Hkv, D=D, block_size=16, seed=510 + D)
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    for window in (0, 100):
+        ref, _ = oracle_after_write(batch, window=window)
+        out = run_gpu(dev, "decode", window=window)
+        assert_close(out, ref, batch, f"many units window={window}")
+        assert np.array_equal(_bits(run_gpu(dev, "decode", window=window)), _bits(out))
+    assert dev.read_err() == 0
+    if D == 128 and lens_kind == "mixed":
+        dev.quest_build_summaries()
+        sel = dev.quest_select(5)
+        torch.cuda.synchronize()
+        ref = oracle.paged_decode_pages(batch.q, dev.pools_numpy()[0], dev.pools_numpy()[1],
+                                        batch.block_tables, batch.seq_lens, batch.sm_scale,
+                                        sel.cpu().numpy(), Hkv=Hkv, block_size=16)
+        dev.out.fill_(float("nan"))
+        dev.decode(selected_pages=sel)
+        torch.cuda.synchronize()
+        assert_close(dev.out.cpu().numpy(), ref, batch, "many units quest")
+        assert dev.read_err() == 0
+
+
 # ---------------------------------------------------------------- caller-visible partials
 
 def _splitkv_pieces(batch, S, workers):
