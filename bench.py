@@ -42,13 +42,14 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_517_504 + 2_066_176, "kernel_hash": "1743392616c67833"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_059_840 + 3_015_936, "kernel_hash": "1743392616c67833"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_179_456 + 2_199_552, "kernel_hash": "1743392616c67833"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_233_664 + 21_535_488, "kernel_hash": "1743392616c67833"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_152_832 + 15_639_552, "kernel_hash": "1743392616c67833"},
-    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_564_160 + 1_169_408, "kernel_hash": "1743392616c67833"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_574_976 + 16_071_424, "kernel_hash": "1743392616c67833"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_771_456 + 2_599_168, "kernel_hash": "42843030ac5f6736"},
+    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_563_392 + 1_250_304, "kernel_hash": "42843030ac5f6736"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_057_536 + 2_975_488, "kernel_hash": "42843030ac5f6736"},
+    ("prefix_sharing", "decode_pair_kernel"): {"bytes": 2_541_372_160 + 180_736, "kernel_hash": "42843030ac5f6736"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_274_944 + 2_595_840, "kernel_hash": "42843030ac5f6736"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_230_912 + 15_663_616, "kernel_hash": "42843030ac5f6736"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_885_440 + 20_257_792, "kernel_hash": "42843030ac5f6736"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_996_096 + 16_524_032, "kernel_hash": "42843030ac5f6736"},
 }
 
 

@@ -1022,14 +1022,15 @@ def test_splitkv_partials_match_oracle_per_slot(kv_dtype, Hq, Hkv, bs, lens, S):
     assert dev.read_err() == 0
 
 
-def test_merge_lse_of_oracle_partials():
+@pytest.mark.parametrize("S,D", [(6, 128), (40, 128), (33, 64)])
+def test_merge_lse_of_oracle_partials(S, D):
     """pa_merge_lse fed with partials it did not write: the oracle's partials over random
     token cuts (empty pieces included), in random slots, with NaN in the o rows of empty
     slots (which must not be read); against the oracle's merge of the same fp32 inputs and
-    its plain decode."""
-    batch = wl.build_batch("t", [1, 40, 300, 0, 777, 16], Hq=16, Hkv=4, D=128, block_size=16,
-                           seed=310)
-    B, Hq, D, S = batch.B, batch.Hq, batch.D, 6
+    its plain decode.  More than 32 slots take the merge's chunk loop."""
+    batch = wl.build_batch("t", [1, 40, 300, 0, 777, 16], Hq=16, Hkv=4, D=D, block_size=16,
+                           seed=310 + S)
+    B, Hq = batch.B, batch.Hq
     full = oracle.paged_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
                                batch.seq_lens, batch.sm_scale, Hkv=4, block_size=16)
     rng = np.random.default_rng(11)
