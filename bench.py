@@ -447,6 +447,148 @@ def per_config_lines(args, device, world, rank):
     return out
 
 
+def end_to_end(args, run, dev, batch, stream, dev_id, world):
+    """Steps timed on the host clock from pinned host buffers: every step copies its
+    inputs in, runs the step's C-ABI calls and reads its output back.
+
+    Default (pipelined): two sets of input and output buffers, as a serving loop keeps
+    them; step i's upload and step i-1's read-back run on copy streams beside step i-1's
+    and step i's kernels, and the host waits for each step's output one step later.
+    --e2e-serial: one set, copy in -> step -> copy out -> wait, per step (a CUDA graph
+    replay, or eager launches with --e2e-eager)."""
+    import torch
+
+    # the step's inputs packed into one pinned host buffer and one device buffer (each
+    # input 256-byte aligned); the device batch's inputs become views of the latter, so
+    # one copy in and one copy out carry the whole step
+    inputs = {name: getattr(dev, name) for name in
+              ("q", "k_new", "v_new", "slot_mapping", "seq_lens", "block_tables")}
+    if dev.shared_prefix_lens is not None:
+        inputs["shared_prefix_lens"] = dev.shared_prefix_lens
+    if args.cascade:                          # the prefix groups (not the workspace)
+        for k, t in zip(("group_offsets", "group_seqs", "group_prefix_len"), dev.cascade):
+            inputs[k] = t
+    parts, off = {}, 0
+    for name, t in inputs.items():
+        n = t.numel() * t.element_size()
+        parts[name] = (off, n, t.dtype, t.shape)
+        off = (off + n + 255) // 256 * 256
+    host_inputs = {name: t.reshape(-1).cpu() for name, t in inputs.items()}
+    cascade_tail = tuple(dev.cascade[3:]) if args.cascade else ()
+
+    def make_set():
+        host_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+        dev_in = torch.empty(off, dtype=torch.uint8, device=dev_id)
+        views = {}
+        for name, (o, n, dt, shp) in parts.items():
+            host_in[o:o + n].view(dt).copy_(host_inputs[name])
+            views[name] = dev_in[o:o + n].view(dt).view(shp)
+        out = torch.empty_like(dev.out)
+        out_host = torch.empty(dev.out.shape, dtype=dev.out.dtype).pin_memory()
+        return {"host_in": host_in, "dev_in": dev_in, "views": views, "out": out,
+                "out_host": out_host}
+
+    def bind(st):
+        views = st["views"]
+        for name in ("q", "k_new", "v_new", "slot_mapping", "seq_lens", "block_tables",
+                     "shared_prefix_lens"):
+            if name in views:
+                setattr(dev, name, views[name])
+        if args.cascade:
+            dev.cascade = (views["group_offsets"], views["group_seqs"],
+                           views["group_prefix_len"]) + cascade_tail
+        dev.out = st["out"]
+
+    sets = [make_set() for _ in range(1 if args.e2e_serial else 2)]
+    h2d = sum(n for _, n, _, _ in parts.values())
+    d2h = sets[0]["out_host"].numel() * sets[0]["out_host"].element_size()
+
+    if args.e2e_serial:
+        st0 = sets[0]
+        bind(st0)
+
+        def e2e_body(s):
+            st0["dev_in"].copy_(st0["host_in"], non_blocking=True)
+            run(st=s)
+            st0["out_host"].copy_(st0["out"], non_blocking=True)
+
+        if args.e2e_eager:
+            def e2e_step(i):
+                e2e_body(stream)
+                stream.synchronize()
+        else:
+            # the whole step -- input copies from pinned host memory, the launch chain,
+            # the read-back -- captured once into a CUDA graph and replayed per step
+            side = torch.cuda.Stream(dev_id)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    e2e_body(side)
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                e2e_body(torch.cuda.current_stream(dev_id))
+
+            def e2e_step(i):
+                graph.replay()
+                torch.cuda.current_stream(dev_id).synchronize()
+
+        def e2e_finish():
+            pass
+    else:
+        copy_in, copy_out = torch.cuda.Stream(dev_id), torch.cuda.Stream(dev_id)
+        ev = {k: [torch.cuda.Event() for _ in sets] for k in ("in", "comp", "out")}
+        for k in ev:                              # every event starts out recorded
+            for e in ev[k]:
+                e.record(stream)
+        torch.cuda.synchronize()
+
+        def e2e_step(i):
+            j = i % 2
+            st = sets[j]
+            copy_in.wait_event(ev["comp"][j])     # step i-2 has read this input set
+            with torch.cuda.stream(copy_in):
+                st["dev_in"].copy_(st["host_in"], non_blocking=True)
+            ev["in"][j].record(copy_in)
+            stream.wait_event(ev["in"][j])
+            stream.wait_event(ev["out"][j])       # step i-2's output has been read back
+            bind(st)
+            run(st=stream)
+            ev["comp"][j].record(stream)
+            copy_out.wait_event(ev["comp"][j])
+            with torch.cuda.stream(copy_out):
+                st["out_host"].copy_(st["out"], non_blocking=True)
+            ev["out"][j].record(copy_out)
+            ev["out"][1 - j].synchronize()        # the host has step i-1's output
+
+        def e2e_finish():
+            torch.cuda.synchronize()
+
+    for i in range(max(3, args.warmup)):
+        e2e_step(i)
+    e2e_finish()
+    barrier(world)
+    t0 = time.perf_counter()
+    n_e2e = max(3, min(args.steps, 200))
+    for i in range(n_e2e):
+        e2e_step(i)
+    e2e_finish()
+    e2e_s = reduce_max((time.perf_counter() - t0) / n_e2e, world, dev_id)
+    if dev.read_err():
+        raise RuntimeError("device error flag set during the end-to-end steps")
+    for st in sets:                                # each set's output is the decode's
+        if not torch.equal(st["out"], sets[0]["out"]):
+            raise RuntimeError("end-to-end output sets differ")
+    return {"value": world * batch.B / e2e_s, "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "mode": ("serial: copy in, step, copy out, wait"
+                     + (" (eager launches)" if args.e2e_eager else " (CUDA graph replay)"))
+            if args.e2e_serial else
+            "pipelined: two input/output sets; uploads and read-backs on copy streams "
+            "beside the neighbouring steps' kernels, each output waited for one step later"}
+
+
 def run_ours(args):
     import torch
 
@@ -487,78 +629,7 @@ def run_ours(args):
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        # the step's inputs packed into one pinned host buffer and one device buffer (each
-        # input 256-byte aligned); the device batch's inputs become views of the latter,
-        # so one copy in and one copy out carry the whole step
-        inputs = {name: getattr(dev, name) for name in
-                  ("q", "k_new", "v_new", "slot_mapping", "seq_lens", "block_tables")}
-        if dev.shared_prefix_lens is not None:
-            inputs["shared_prefix_lens"] = dev.shared_prefix_lens
-        if args.cascade:                          # the prefix groups (not the workspace)
-            for k, t in zip(("group_offsets", "group_seqs", "group_prefix_len"), dev.cascade):
-                inputs[k] = t
-        parts, off = {}, 0
-        for name, t in inputs.items():
-            n = t.numel() * t.element_size()
-            parts[name] = (off, n, t.dtype, t.shape)
-            off = (off + n + 255) // 256 * 256
-        host_in = torch.empty(off, dtype=torch.uint8).pin_memory()
-        dev_in = torch.empty(off, dtype=torch.uint8, device=dev_id)
-        views = {}
-        for name, (o, n, dt, shp) in parts.items():
-            host_in[o:o + n].view(dt).copy_(inputs[name].reshape(-1).cpu())
-            views[name] = dev_in[o:o + n].view(dt).view(shp)
-        for name in ("q", "k_new", "v_new", "slot_mapping", "seq_lens", "block_tables",
-                     "shared_prefix_lens"):
-            if name in views:
-                setattr(dev, name, views[name])
-        if args.cascade:
-            dev.cascade = (views["group_offsets"], views["group_seqs"],
-                           views["group_prefix_len"]) + tuple(dev.cascade[3:])
-        out_host = torch.empty(dev.out.shape, dtype=dev.out.dtype).pin_memory()
-        h2d = sum(n for _, n, _, _ in parts.values())
-        d2h = out_host.numel() * out_host.element_size()
-
-        def e2e_body(st):
-            dev_in.copy_(host_in, non_blocking=True)
-            run(st=st)
-            out_host.copy_(dev.out, non_blocking=True)
-
-        if args.e2e_eager:
-            def e2e_step():
-                e2e_body(stream)
-                stream.synchronize()
-        else:
-            # the whole step -- input copies from pinned host memory, the launch chain,
-            # the read-back -- captured once into a CUDA graph and replayed per step
-            side = torch.cuda.Stream(dev_id)
-            side.wait_stream(stream)
-            with torch.cuda.stream(side):
-                for _ in range(3):
-                    e2e_body(side)
-            stream.wait_stream(side)
-            torch.cuda.synchronize()
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                e2e_body(torch.cuda.current_stream(dev_id))
-
-            def e2e_step():
-                graph.replay()
-                torch.cuda.current_stream(dev_id).synchronize()
-
-        for _ in range(max(3, args.warmup)):
-            e2e_step()
-        barrier(world)
-        t0 = time.perf_counter()
-        n_e2e = max(3, min(args.steps, 200))
-        for _ in range(n_e2e):
-            e2e_step()
-        e2e_s = reduce_max((time.perf_counter() - t0) / n_e2e, world, dev_id)
-        e2e = {"value": world * batch.B / e2e_s, "unit": "tokens/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "cuda_graph": not args.e2e_eager}
-        if dev.read_err():
-            raise RuntimeError("device error flag set during the end-to-end steps")
+        e2e = end_to_end(args, run, dev, batch, stream, dev_id, world)
 
     unique_tokens = step_kv_tokens(batch, args, selected)
     peak, peak_kind = measured_peak_hbm()
@@ -729,8 +800,11 @@ def main(argv=None):
                          "or a cluster of CTAs per sequence and KV head); auto: pa_decode for "
                          "fp8_mixed, whose workload names that call, the workspace form with "
                          "the cascade, pa_decode_splitkv otherwise")
+    ap.add_argument("--e2e-serial", action="store_true",
+                    help="e2e leg: one buffer set, copy in -> step -> copy out -> wait per step")
     ap.add_argument("--e2e-eager", action="store_true",
-                    help="e2e leg: launch each call eagerly instead of replaying a CUDA graph")
+                    help="with --e2e-serial: launch each call eagerly instead of replaying "
+                         "a CUDA graph")
     ap.add_argument("--cascade", action="store_true",
                     help="prefix-aware decode: each prefix group's shared tokens attended once")
     ap.add_argument("--quest-topk", type=int, default=0,
