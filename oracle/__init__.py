@@ -47,7 +47,18 @@ select_pages                   Engineering", sec. 7 (scores 2.5, 6.0, 4.0,
                                key choices for the upper-bound property
 quest_decode                   textbook attention restricted to the chosen
                                pages' tokens (numpy), topk >= pages equals
-                               full decode; selection by brute-force scores
+                               full decode; selection by brute-force scores;
+                               on E4M3 / 4-bit pools with power-of-two scales
+                               equal to Quest over bf16 pools of the restored
+                               values; with other scales the top-k of numpy
+                               scores over outward-rounded summaries
+quest_page_summary             numpy min / max of the page's restored keys
+                               (torch E4M3 decode, nibbles by hand), rounded
+                               outward by a search of the neighbouring bf16
+                               bit patterns, element-exact
+bf16_round_down / _up          the neighbouring bf16 bit patterns of x (the
+                               largest <= x, the smallest >= x); bf16 values
+                               are fixed points; round_down(-x) = -round_up(x)
 split_partials / merge_lse     merge(split(x)) == unsplit(x) to 1e-12 for
                                random splits; one split is the identity;
                                empty splits carry no weight
@@ -132,7 +143,15 @@ def _load():
             lib.oracle_select_pages.restype = I
             lib.oracle_select_pages.argtypes = [P, I, I, P]
             lib.oracle_quest_decode.restype = None
-            lib.oracle_quest_decode.argtypes = [I, I, I, I, I, I, P, P, P, P, P, D, I, P, P, I]
+            lib.oracle_quest_decode.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, D, I,
+                                                P, P, I]
+            lib.oracle_quest_page_summary.restype = None
+            lib.oracle_quest_page_summary.argtypes = [I, I, I, I, P, P, ctypes.c_longlong, I, I,
+                                                      P, P]
+            lib.oracle_bf16_round_down.restype = D
+            lib.oracle_bf16_round_down.argtypes = [D]
+            lib.oracle_bf16_round_up.restype = D
+            lib.oracle_bf16_round_up.argtypes = [D]
             lib.oracle_paged_decode.restype = None
             lib.oracle_paged_decode.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, D,
                                                 I, I, P, P, P, I]
@@ -343,19 +362,57 @@ def select_pages(scores, k: int) -> list[int]:
 
 
 def quest_decode(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, *, Hkv: int,
-                 block_size: int, topk: int, nthreads: int | None = None):
-    """Query-aware sparse decode over bf16 pools; returns (out [B, Hq, D], sel [B, Hkv, topk])."""
+                 block_size: int, topk: int, k_scale=None, v_scale=None,
+                 nthreads: int | None = None):
+    """Query-aware sparse decode over bf16, E4M3 or 4-bit pools (codes with per-(block,
+    head) scales); returns (out [B, Hq, D], sel [B, Hkv, topk])."""
     lib = _load()
     q = _c(q, np.uint16)
     B, Hq, D = q.shape
-    kp, vp = _c(k_pool, np.uint16), _c(v_pool, np.uint16)
+    kind = _kv_kind(k_pool, D)
+    quant = kind != 0
+    kp = np.ascontiguousarray(k_pool)
+    vp = np.ascontiguousarray(v_pool)
+    ks = _c(k_scale, np.float32) if quant else None
+    vs = _c(v_scale, np.float32) if quant else None
     bt, sl = _c(block_tables, np.int32), _c(seq_lens, np.int32)
     out = np.zeros((B, Hq, D), dtype=np.float64)
     sel = np.zeros((B, Hkv, topk), dtype=np.int32)
-    lib.oracle_quest_decode(B, Hq, Hkv, D, block_size, bt.shape[1], _ptr(q), _ptr(kp), _ptr(vp),
-                            _ptr(bt), _ptr(sl), float(sm_scale), int(topk), _ptr(out), _ptr(sel),
-                            nthreads or os.cpu_count() or 1)
+    lib.oracle_quest_decode(B, Hq, Hkv, D, block_size, bt.shape[1], kind, _ptr(q), _ptr(kp),
+                            _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl), float(sm_scale),
+                            int(topk), _ptr(out), _ptr(sel), nthreads or os.cpu_count() or 1)
     return out, sel
+
+
+def bf16_round_down(x: float) -> float:
+    """The largest bf16 value <= x (finite x)."""
+    return _load().oracle_bf16_round_down(float(x))
+
+
+def bf16_round_up(x: float) -> float:
+    """The smallest bf16 value >= x (finite x)."""
+    return _load().oracle_bf16_round_up(float(x))
+
+
+def quest_page_summary(k_pool, page: int, rows: int, kvh: int, *, Hkv: int, D: int,
+                       block_size: int, k_scale=None):
+    """Quest's stored summary of pool page `page` (pool rows 16 page .. 16 page + rows - 1)
+    for KV head kvh: (min rounded down, max rounded up) to bf16, from the restored keys."""
+    lib = _load()
+    kind = _kv_kind(k_pool, D)
+    kp = np.ascontiguousarray(k_pool)
+    ks = _c(k_scale, np.float32) if kind != 0 else None
+    mn, mx = np.zeros(D), np.zeros(D)
+    lib.oracle_quest_page_summary(Hkv, D, block_size, kind, _ptr(kp), _ptr(ks), int(page),
+                                  int(rows), int(kvh), _ptr(mn), _ptr(mx))
+    return mn, mx
+
+
+def page_summary_bf16(keys):
+    """Quest's stored summary of keys [n, D]: (min rounded down, max rounded up) to bf16."""
+    mn, mx = page_summary(keys)
+    return (np.array([bf16_round_down(v) for v in mn]),
+            np.array([bf16_round_up(v) for v in mx]))
 
 
 def split_partials(q, k_pool, v_pool, block_tables, seq_lens, sm_scale: float, b: int, h: int,

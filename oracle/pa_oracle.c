@@ -175,6 +175,37 @@ void oracle_page_summary(const double *keys, int n, int D, double *mn, double *m
         }
 }
 
+/*
+ * Directed rounding of a finite double to the bf16 grid: 8 significant bits with
+ * fp32's exponent range, subnormal spacing 2^-133.  down: the largest bf16 value
+ * <= x; up: the smallest bf16 value >= x.  Used for Quest summaries of quantised
+ * pools, whose restored keys (code * scale) are not bf16 values: the minimum is
+ * rounded down and the maximum up, so the page score stays an upper bound of q . k.
+ */
+static double bf16_ulp(double x)
+{
+    int e;
+    (void)frexp(x, &e);                 /* |x| in [2^(e-1), 2^e) */
+    if (e < -125) e = -125;             /* below 2^-126: subnormal spacing */
+    return ldexp(1.0, e - 8);
+}
+
+double oracle_bf16_round_down(double x)
+{
+    double u;
+    if (x == 0.0) return 0.0;
+    u = bf16_ulp(x);
+    return floor(x / u) * u;
+}
+
+double oracle_bf16_round_up(double x)
+{
+    double u;
+    if (x == 0.0) return 0.0;
+    u = bf16_ulp(x);
+    return ceil(x / u) * u;
+}
+
 double oracle_page_score(const double *q, const double *mn, const double *mx, int D)
 {
     double s = 0.0;
@@ -448,25 +479,55 @@ typedef struct {
  * written into dst[0..D) as doubles.  FP8 and 4-bit pools are restored as
  * code value * scale[block][kvh], exactly in double (kv_kind: 0 bf16, 1 E4M3,
  * 2 4-bit). */
+/* Row (blk, off, kvh) of one pool, restored into dst[0..D) as doubles. */
+static void pool_row(int Hkv, int D, int bs, int kv_kind, const void *pool, const float *sc,
+                     long long blk, int off, int kvh, double *dst)
+{
+    size_t idx = (((size_t)blk * bs + (size_t)off) * Hkv + kvh) * D;
+    int d;
+    if (kv_kind == 0) {
+        for (d = 0; d < D; d++)
+            dst[d] = oracle_bf16_to_double(((const uint16_t *)pool)[idx + d]);
+    } else if (kv_kind == 2) {
+        oracle_int4_restore(&((const uint8_t *)pool)[idx / 2], D, sc[(size_t)blk * Hkv + kvh],
+                            dst);
+    } else {
+        double scale = (double)sc[(size_t)blk * Hkv + kvh];
+        for (d = 0; d < D; d++)
+            dst[d] = oracle_e4m3_to_double(((const uint8_t *)pool)[idx + d]) * scale;
+    }
+}
+
 static void kv_row(const paged_kv *p, int is_v, int b, int t, int kvh, double *dst)
 {
     int32_t blk = p->block_tables[(size_t)b * p->max_blocks + t / p->bs];
-    size_t idx = (((size_t)blk * p->bs + (size_t)(t % p->bs)) * p->Hkv + kvh) * p->D;
-    const void *pool = is_v ? p->v_pool : p->k_pool;
-    int d;
-    if (p->kv_kind == 0) {
-        for (d = 0; d < p->D; d++)
-            dst[d] = oracle_bf16_to_double(((const uint16_t *)pool)[idx + d]);
-    } else if (p->kv_kind == 2) {
-        const float *sc = is_v ? p->v_scale : p->k_scale;
-        oracle_int4_restore(&((const uint8_t *)pool)[idx / 2], p->D,
-                            sc[(size_t)blk * p->Hkv + kvh], dst);
-    } else {
-        const float *sc = is_v ? p->v_scale : p->k_scale;
-        double scale = (double)sc[(size_t)blk * p->Hkv + kvh];
-        for (d = 0; d < p->D; d++)
-            dst[d] = oracle_e4m3_to_double(((const uint8_t *)pool)[idx + d]) * scale;
+    pool_row(p->Hkv, p->D, p->bs, p->kv_kind, is_v ? p->v_pool : p->k_pool,
+             is_v ? p->v_scale : p->k_scale, blk, t % p->bs, kvh, dst);
+}
+
+/*
+ * Quest's stored summary ([P3] section 7) of pool page `page` (pool rows
+ * 16 page .. 16 page + rows - 1, i.e. slots of one block) for KV head kvh: the
+ * per-channel minimum and maximum of the restored keys (oracle_page_summary),
+ * the minimum rounded down and the maximum up to bf16.
+ */
+void oracle_quest_page_summary(int Hkv, int D, int bs, int kv_kind, const void *k_pool,
+                               const float *k_scale, long long page, int rows, int kvh,
+                               double *mn, double *mx)
+{
+    double *keys = (double *)malloc(sizeof(double) * 16 * (size_t)D);
+    int t, d;
+    for (t = 0; t < rows; t++) {
+        long long r = 16 * page + t;
+        pool_row(Hkv, D, bs, kv_kind, k_pool, k_scale, r / bs, (int)(r % bs), kvh,
+                 &keys[(size_t)t * D]);
     }
+    oracle_page_summary(keys, rows, D, mn, mx);
+    for (d = 0; d < D; d++) {
+        mn[d] = oracle_bf16_round_down(mn[d]);
+        mx[d] = oracle_bf16_round_up(mx[d]);
+    }
+    free(keys);
 }
 
 /*
@@ -556,24 +617,27 @@ void oracle_paged_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks, 
 }
 
 /*
- * Query-aware sparse decode ([P3] section 7) over bf16 pools, pages of 16 tokens:
+ * Query-aware sparse decode ([P3] section 7), pages of 16 tokens, over bf16, E4M3 or
+ * 4-bit pools (kv_kind as in kv_row; keys and values restored exactly):
  * for every (b, kv head) the pages of sequence b are summarised from their valid
- * keys (oracle_page_summary), each page is scored with every query head of the
- * group and keeps the largest score (the group shares one selection), the topk
- * best pages are chosen (oracle_select_pages) and every query head of the group
- * attends over the tokens of the chosen pages only (textbook softmax).  The
- * chosen pages go to sel[b][kvh][0..topk) (-1 where fewer exist).
+ * keys (oracle_page_summary), the summary stored as bf16 with the minimum rounded
+ * down and the maximum up (a no-op on bf16 keys), each page is scored with every
+ * query head of the group and keeps the largest score (the group shares one
+ * selection), the topk best pages are chosen (oracle_select_pages) and every query
+ * head of the group attends over the tokens of the chosen pages only (textbook
+ * softmax).  The chosen pages go to sel[b][kvh][0..topk) (-1 where fewer exist).
  */
-void oracle_quest_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks,
-                         const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+void oracle_quest_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks, int kv_kind,
+                         const uint16_t *q, const void *k_pool, const void *v_pool,
+                         const float *k_scale, const float *v_scale,
                          const int32_t *block_tables, const int32_t *seq_lens, double sm_scale,
                          int topk, double *out, int32_t *sel, int nthreads)
 {
     paged_kv p;
     long long i;
     int G = Hq / Hkv;
-    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_kind = 0;
-    p.k_pool = k_pool; p.v_pool = v_pool; p.k_scale = NULL; p.v_scale = NULL;
+    p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.bs = bs; p.max_blocks = max_blocks; p.kv_kind = kv_kind;
+    p.k_pool = k_pool; p.v_pool = v_pool; p.k_scale = k_scale; p.v_scale = v_scale;
     p.block_tables = block_tables;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
     for (i = 0; i < (long long)B * Hkv; i++) {
@@ -588,9 +652,10 @@ void oracle_quest_decode(int B, int Hq, int Hkv, int D, int bs, int max_blocks,
         int *chosen = (int *)malloc(sizeof(int) * (size_t)(np > 0 ? np : 1));
         for (j = 0; j < np; j++) {
             int n = (L - 16 * j < 16) ? L - 16 * j : 16;
-            for (t = 0; t < n; t++)
-                kv_row(&p, 0, b, 16 * j + t, kvh, &keys[(size_t)t * D]);
-            oracle_page_summary(keys, n, D, mn, mx);
+            /* logical page j: 16 rows of one block, at pool page blk * bs / 16 + ... */
+            long long blk = block_tables[(size_t)b * max_blocks + 16 * j / bs];
+            oracle_quest_page_summary(Hkv, D, bs, kv_kind, k_pool, k_scale,
+                                      blk * (bs / 16) + (16 * j % bs) / 16, n, kvh, mn, mx);
             scores[j] = -INFINITY;
             for (g = 0; g < G; g++) {
                 double sc;

@@ -588,6 +588,175 @@ def test_quest_decode_vs_numpy(topk):
         assert np.allclose(out, _oracle(batch), rtol=1e-12, atol=1e-13)
 
 
+def _bf16_neighbours(x):
+    """bf16 values (as doubles) near x, found from the bit patterns around float32(x)."""
+    b = int(np.float32(x).view(np.uint32)) >> 16
+    out = []
+    for pat in range(b - 3, b + 4):
+        pat &= 0xFFFF
+        v = float(np.uint32(pat << 16).view(np.float32))
+        if math.isfinite(v):
+            out.append(v)
+        v = float(np.uint32((pat ^ 0x8000) << 16).view(np.float32))   # across zero
+        if math.isfinite(v):
+            out.append(v)
+    return out + [0.0]
+
+
+def test_bf16_directed_rounding():
+    """round_down(x) is the largest bf16 value <= x and round_up(x) the smallest >= x,
+    checked against the bf16 patterns next to x; bf16 values are fixed points."""
+    rng = np.random.default_rng(5)
+    xs = [1.0 + 2.0 ** -9, -(1.0 + 2.0 ** -9), 3.0, -0.0, 2.0 ** -130 * 1.3, -2.0 ** -128 * 1.7,
+          448.0 * 0.37, 1e-3, -7.0 * 0.4321]
+    xs += list(rng.standard_normal(300) * np.exp(rng.uniform(-40, 40, 300)))
+    for x in xs:
+        lo, hi = oracle.bf16_round_down(x), oracle.bf16_round_up(x)
+        cand = _bf16_neighbours(x)
+        assert lo == max(c for c in cand if c <= x), x
+        assert hi == min(c for c in cand if c >= x), x
+        assert oracle.bf16_round_down(-x) == -hi and oracle.bf16_round_up(-x) == -lo
+    assert oracle.bf16_round_down(1.0 + 2.0 ** -9) == 1.0
+    assert oracle.bf16_round_up(1.0 + 2.0 ** -9) == 1.0 + 2.0 ** -7
+    for bits in rng.integers(0, 0x7F80, 200):
+        v = float(np.uint32(int(bits) << 16).view(np.float32))
+        assert oracle.bf16_round_down(v) == v == oracle.bf16_round_up(v)
+
+
+def test_page_summary_bf16_bounds():
+    """Stored summaries bound every key and are the tightest bf16 bounds; on bf16 keys
+    they are the exact minimum and maximum."""
+    rng = np.random.default_rng(6)
+    keys = rng.integers(-7, 8, (16, 64)) * 0.0137           # restored 4-bit-like keys
+    mn, mx = oracle.page_summary_bf16(keys)
+    assert np.all(mn[None] <= keys) and np.all(mx[None] >= keys)
+    emn, emx = keys.min(0), keys.max(0)
+    for d in range(64):
+        assert max(c for c in _bf16_neighbours(emn[d]) if c <= emn[d]) == mn[d]
+        assert min(c for c in _bf16_neighbours(emx[d]) if c >= emx[d]) == mx[d]
+    kb = wl.bf16_to_float(wl.bf16_bits(rng.standard_normal((9, 32)))).astype(np.float64)
+    mn, mx = oracle.page_summary_bf16(kb)
+    assert np.array_equal(mn, kb.min(0)) and np.array_equal(mx, kb.max(0))
+
+
+def _restored_bf16_batch(batch):
+    """The same batch with its quantised pools replaced by bf16 pools of the restored
+    values (exact when every scale is a power of two), codes decoded by torch / by hand."""
+    import copy
+    out = copy.copy(batch)
+    pools = []
+    for pool, sc in ((batch.k_pool, batch.k_scale), (batch.v_pool, batch.v_scale)):
+        if batch.kv_dtype == "fp8_e4m3":
+            vals = torch.from_numpy(pool).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        else:
+            lo = (pool & 0xF).astype(np.int64) - 8
+            hi = (pool >> 4).astype(np.int64) - 8
+            vals = np.stack([lo, hi], -1).reshape(pool.shape[:-1] + (pool.shape[-1] * 2,))
+        vals = vals * sc.astype(np.float64)[:, None, :, None]
+        bits = wl.bf16_bits(vals.astype(np.float32))
+        assert np.array_equal(wl.bf16_to_float(bits).astype(np.float64), vals)   # exact
+        pools.append(bits)
+    out.k_pool, out.v_pool = pools
+    out.k_scale = out.v_scale = None
+    out.kv_dtype = "bf16"
+    return out
+
+
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "int4"])
+def test_quest_decode_quantised_pools(kv_dtype):
+    """Quest over E4M3 / 4-bit pools: with power-of-two scales the restored keys are
+    bf16 values, so it must equal Quest over bf16 pools holding them (selection and
+    output, exactly); choosing every page must equal the full decode of the pools."""
+    batch = wl.build_batch("t", [1, 15, 16, 17, 70, 200, 0], Hq=16, Hkv=2, D=128, block_size=16,
+                           seed=83, kv_dtype=kv_dtype)
+    rng = np.random.default_rng(7)
+    for sc in (batch.k_scale, batch.v_scale):
+        sc[...] = 2.0 ** rng.integers(-4, 3, sc.shape)
+    plain = _restored_bf16_batch(batch)
+    for topk in (1, 4, 100):
+        out, sel = oracle.quest_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                       batch.seq_lens, batch.sm_scale, Hkv=2, block_size=16,
+                                       topk=topk, k_scale=batch.k_scale, v_scale=batch.v_scale)
+        ref, ref_sel = oracle.quest_decode(plain.q, plain.k_pool, plain.v_pool,
+                                           plain.block_tables, plain.seq_lens, plain.sm_scale,
+                                           Hkv=2, block_size=16, topk=topk)
+        assert np.array_equal(sel, ref_sel), topk
+        assert np.array_equal(out, ref), topk
+    full = oracle.paged_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                               batch.seq_lens, batch.sm_scale, Hkv=2, block_size=16,
+                               k_scale=batch.k_scale, v_scale=batch.v_scale)
+    assert np.allclose(out, full, rtol=1e-12, atol=1e-13)
+
+
+def _restored_keys(batch):
+    """Restored key pool [nblocks, bs, Hkv, D] in fp64: E4M3 codes decoded by torch,
+    4-bit nibbles by hand (element 2j in the low nibble of byte j), times the scale."""
+    if batch.kv_dtype == "bf16":
+        return wl.bf16_to_float(batch.k_pool).astype(np.float64)
+    if batch.kv_dtype == "fp8_e4m3":
+        kv = torch.from_numpy(batch.k_pool).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    else:
+        lo = (batch.k_pool & 0xF).astype(np.int64) - 8
+        hi = (batch.k_pool >> 4).astype(np.int64) - 8
+        kv = np.stack([lo, hi], -1).reshape(batch.k_pool.shape[:-1] + (batch.D,))
+    return kv.astype(np.float64) * batch.k_scale.astype(np.float64)[:, None, :, None]
+
+
+@pytest.mark.parametrize("kv_dtype,bs", [("fp8_e4m3", 16), ("int4", 32), ("bf16", 32),
+                                         ("fp8_e4m3", 32)])
+def test_quest_page_summary_from_pool(kv_dtype, bs):
+    """The stored summary of a pool page: min and max of the page's restored keys over
+    its first `rows` rows, rounded down / up to bf16 (neighbour search), element-exact;
+    on bf16 pools the plain minimum and maximum."""
+    batch = wl.build_batch("t", [40, 97], Hq=16, Hkv=2, D=128, block_size=bs, seed=85,
+                           kv_dtype=kv_dtype)
+    kv = _restored_keys(batch)
+    down = np.vectorize(lambda x: max(c for c in _bf16_neighbours(x) if c <= x))
+    up = np.vectorize(lambda x: min(c for c in _bf16_neighbours(x) if c >= x))
+    rows_all = kv.reshape(-1, 2, 128)                   # pool rows in order
+    inexact = 0
+    for page, rows, kvh in ((0, 16, 0), (1, 7, 1), (3, 1, 0), (5, 16, 1), (2, 12, 1)):
+        mn, mx = oracle.quest_page_summary(batch.k_pool, page, rows, kvh, Hkv=2, D=128,
+                                           block_size=bs, k_scale=batch.k_scale)
+        kk = rows_all[16 * page:16 * page + rows, kvh]
+        assert np.array_equal(mn, down(kk.min(0))) and np.array_equal(mx, up(kk.max(0)))
+        inexact += int(np.sum(mn != kk.min(0)) + np.sum(mx != kk.max(0)))
+    assert (inexact == 0) == (kv_dtype == "bf16")
+
+
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "int4"])
+def test_quest_selection_quantised_rounded_summaries(kv_dtype):
+    """With arbitrary scales the restored keys are not bf16 values: the selection must be
+    the top-k of scores over summaries whose minimum is rounded down and maximum up to
+    bf16 (restated here with the neighbour search and numpy)."""
+    batch = wl.build_batch("t", [40, 97, 200, 333], Hq=16, Hkv=2, D=128, block_size=32,
+                           seed=84, kv_dtype=kv_dtype)
+    topk = 5
+    _, sel = oracle.quest_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                 batch.seq_lens, batch.sm_scale, Hkv=2, block_size=32,
+                                 topk=topk, k_scale=batch.k_scale, v_scale=batch.v_scale)
+    kv = _restored_keys(batch)
+    q = wl.bf16_to_float(batch.q).astype(np.float64)
+    down = np.vectorize(lambda x: max(c for c in _bf16_neighbours(x) if c <= x))
+    up = np.vectorize(lambda x: min(c for c in _bf16_neighbours(x) if c >= x))
+    inexact = 0
+    for b in range(batch.B):
+        L = int(batch.seq_lens[b])
+        t = np.arange(L)
+        K = kv[batch.block_tables[b, t // 32], t % 32]
+        for kvh in range(2):
+            sc = []
+            for j in range((L + 15) // 16):
+                kk = K[16 * j:16 * j + 16, kvh]
+                mn, mx = down(kk.min(0)), up(kk.max(0))
+                inexact += int(np.sum(mn != kk.min(0)) + np.sum(mx != kk.max(0)))
+                qs = q[b, kvh * 8:(kvh + 1) * 8]
+                sc.append(np.max(np.maximum(qs * mn, qs * mx).sum(1)))
+            want = sorted(sorted(range(len(sc)), key=lambda j: (-sc[j], j))[:topk])
+            assert list(sel[b, kvh, :len(want)]) == want, (b, kvh)
+    assert inexact > 0          # the rounding was exercised
+
+
 # ---------------------------------------------------------------- split + merge
 
 def test_split_merge_identity_random():
