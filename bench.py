@@ -298,8 +298,8 @@ class StepRunner:
         st = self.stream if st is None else st
         dev.reshape_and_cache(st)
         if self.quest:
-            _lib.pa_quest_summarize(dev.shape, dev.k_pool, dev.key_summaries, dev.slot_mapping,
-                                    dev.err, st)
+            _lib.pa_quest_summarize(dev.shape, dev.k_pool, dev.k_scale, dev.key_summaries,
+                                    dev.slot_mapping, dev.err, st)
             _lib.pa_quest_select(dev.shape, dev.q, dev.key_summaries, dev.block_tables,
                                  dev.seq_lens, args.quest_topk, dev.page_scores,
                                  dev.selected_pages, dev.err, st)

@@ -391,13 +391,17 @@ pa_status pa_decode_splitkv_noalloc(const pa_shape *shape, float *out, int32_t n
  * >= 0, set the summary of page s / 16 to the per-channel minimum and maximum of its
  * keys in rows 0 .. s % 16:
  *     key_summaries[s / 16][h][0][d] = min_r K[r][h][d],  [1][d] = max_r K[r][h][d]
- * key_summaries: [nblocks * block_size / 16, Hkv, 2, D] bf16 (exact: bf16 keys).
+ * key_summaries: [nblocks * block_size / 16, Hkv, 2, D] bf16.  bf16 pools: exact.
+ * FP8-E4M3 and 4-bit pools (section 8): K is the restored key code * k_scale[block]
+ * [h] (k_scale [nblocks, Hkv] fp32, required), which bf16 may not hold, so the
+ * minimum is stored rounded toward -inf and the maximum toward +inf: the page score
+ * stays an upper bound of q . k (k_scale is ignored for bf16 pools).
  * Call it after pa_reshape_and_cache with the same slots; to build every summary
  * of a sequence, pass the slot of each page's last token.  When several listed
- * slots share a page the one with the largest slot writes.  bf16 pools only.
+ * slots share a page the one with the largest slot writes.
  */
-pa_status pa_quest_summarize(const pa_shape *shape, const void *k_pool, void *key_summaries,
-                             const int64_t *slot_mapping, int32_t *err_flag,
+pa_status pa_quest_summarize(const pa_shape *shape, const void *k_pool, const float *k_scale,
+                             void *key_summaries, const int64_t *slot_mapping, int32_t *err_flag,
                              pa_stream_t stream);
 
 /*
@@ -411,11 +415,11 @@ pa_status pa_quest_summarize(const pa_shape *shape, const void *k_pool, void *ke
  * then write the topk best pages (ties to the lower page index; all pages if
  * there are at most topk) in increasing order to selected_pages[b][h][0 .. topk),
  * -1 past the number of pages.  A page whose block-table entry is outside
- * [0, nblocks) sets PA_DEVERR_BLOCK_ID and scores -inf.  bf16 pools only; q
- * [B, Hq, D] bf16; page_scores and selected_pages are caller-owned device memory
- * (outputs).  Pass selected_pages to pa_decode / pa_decode_splitkv through
- * pa_decode_opts.  Scores are fp32 sums, so pages whose scores agree to rounding
- * may be ordered differently from an exact computation.
+ * [0, nblocks) sets PA_DEVERR_BLOCK_ID and scores -inf.  Any pool dtype (the
+ * summaries are bf16); q [B, Hq, D] bf16; page_scores and selected_pages are
+ * caller-owned device memory (outputs).  Pass selected_pages to pa_decode /
+ * pa_decode_splitkv through pa_decode_opts.  Scores are fp32 sums, so pages whose
+ * scores agree to rounding may be ordered differently from an exact computation.
  */
 pa_status pa_quest_select(const pa_shape *shape, const void *q, const void *key_summaries,
                           const int32_t *block_tables, const int32_t *seq_lens, int32_t topk,

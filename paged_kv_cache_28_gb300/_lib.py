@@ -101,7 +101,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "pa_status_string": (ctypes.c_char_p, [I32]),
             "pa_read_error_flag": (I32, [P, ctypes.POINTER(I32), P]),
             "pa_decode_splitkv_noalloc": (I32, [S, P, I32, P, P, P, P, P, P, P, F, P, P]),
-            "pa_quest_summarize": (I32, [S, P, P, P, P, P]),
+            "pa_quest_summarize": (I32, [S, P, P, P, P, P, P]),
             "pa_quest_select": (I32, [S, P, P, P, P, I32, P, P, P, P]),
             "pa_cascade_workspace_bytes": (ctypes.c_size_t, [S]),
         }
@@ -248,12 +248,12 @@ def pa_decode_splitkv_noalloc(shape: pa_shape, out, num_segments: int, q, k_pool
         _ptr(err_flag), _stream(stream)))
 
 
-def pa_quest_summarize(shape: pa_shape, k_pool, key_summaries, slot_mapping, err_flag=None,
-                       stream=None) -> None:
+def pa_quest_summarize(shape: pa_shape, k_pool, k_scale, key_summaries, slot_mapping,
+                       err_flag=None, stream=None) -> None:
     lib = load()
     _check("pa_quest_summarize", lib.pa_quest_summarize(
-        ctypes.byref(shape), _ptr(k_pool), _ptr(key_summaries), _ptr(slot_mapping),
-        _ptr(err_flag), _stream(stream)))
+        ctypes.byref(shape), _ptr(k_pool), _ptr(k_scale), _ptr(key_summaries),
+        _ptr(slot_mapping), _ptr(err_flag), _stream(stream)))
 
 
 def pa_quest_select(shape: pa_shape, q, key_summaries, block_tables, seq_lens, topk: int,

@@ -220,16 +220,16 @@ pa_status pa_merge_lse(const pa_shape *shape, float *out, const float *o_part, c
                              reinterpret_cast<cudaStream_t>(stream));
 }
 
-pa_status pa_quest_summarize(const pa_shape *shape, const void *k_pool, void *key_summaries,
-                             const int64_t *slot_mapping, int32_t *err_flag,
+pa_status pa_quest_summarize(const pa_shape *shape, const void *k_pool, const float *k_scale,
+                             void *key_summaries, const int64_t *slot_mapping, int32_t *err_flag,
                              pa_stream_t stream) {
   pa_status st = check_shape(shape, false);
   if (st != PA_OK) return st;
-  if (shape->kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
   if (shape->B == 0) return PA_OK;
   st = check_ptrs({k_pool, key_summaries, slot_mapping});
   if (st != PA_OK) return st;
-  return pa::run_quest_summarize(*shape, k_pool, key_summaries, slot_mapping, err_flag,
+  if (shape->kv_dtype != PA_KV_BF16 && !k_scale) return PA_ERR_INVALID_ARG;
+  return pa::run_quest_summarize(*shape, k_pool, k_scale, key_summaries, slot_mapping, err_flag,
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -239,7 +239,6 @@ pa_status pa_quest_select(const pa_shape *shape, const void *q, const void *key_
                           pa_stream_t stream) {
   pa_status st = check_shape(shape, true);
   if (st != PA_OK) return st;
-  if (shape->kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
   if (topk < 1) return PA_ERR_INVALID_ARG;
   if (shape->B == 0) return PA_OK;
   st = check_ptrs({q, key_summaries, block_tables, seq_lens, page_scores, selected_pages});

@@ -128,7 +128,8 @@ pa_status run_decode_parts(const pa_shape &s, float *o_part, float *lse, int S, 
 pa_status run_merge_parts(const pa_shape &s, float *out, const float *o_part, const float *lse,
                           int S, cudaStream_t stream);
 
-pa_status run_quest_summarize(const pa_shape &s, const void *k_pool, void *summaries,
+pa_status run_quest_summarize(const pa_shape &s, const void *k_pool, const float *k_scale,
+                              void *summaries,
                               const int64_t *slot_mapping, int32_t *err, cudaStream_t stream);
 int quest_max_pages(const pa_shape &s);
 size_t quest_score_smem(const pa_shape &s);

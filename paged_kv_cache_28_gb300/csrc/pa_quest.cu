@@ -20,13 +20,84 @@ __device__ __forceinline__ void prefetch_l2(const void *p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// A finite float rounded to bf16 toward +inf (UP) or -inf, as bits; -0 comes out as +0.
+template <bool UP>
+__device__ __forceinline__ uint32_t bf16_directed(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  const uint32_t t = u >> 16;
+  if ((u & 0xFFFFu) == 0u) return t;              // a bf16 value already
+  const bool neg = (u >> 31) != 0u;
+  return neg != UP ? t + 1u : t;                  // away from zero, or toward it
+}
+
+// Quantised pools (KIND 1: E4M3 codes, one byte each; 2: 4-bit offset-binary codes,
+// element 2j in the low nibble of byte j): eight consecutive channels of one KV head
+// per thread and pass.  The restored keys code * scale are not bf16 values, so each
+// product is taken rounded down for the minimum and up for the maximum, and the
+// stored bf16 bounds are rounded the same way: the minimum never exceeds a key and
+// the maximum is never below one, so the page score stays an upper bound.  (Directed
+// rounding to fp32 and then to bf16 equals directed rounding to bf16.)
+template <int KIND>
+__device__ __forceinline__ void summarize_quant(const uint8_t *k_pool, const float *k_scale,
+                                                uint16_t *summ, int64_t page, int rows, int Hkv,
+                                                int D, int bs) {
+  constexpr int kCodeBytes = KIND == 1 ? 8 : 4;   // bytes of eight codes
+  const int row_vecs = Hkv * D / 8;
+  const int64_t blk = page * kTile / bs;          // a page lies inside one block
+  for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) {
+    const int e = v * 8, h = e / D, d = e - h * D;
+    const float sc = __ldg(k_scale + blk * Hkv + h);
+    float mn[8], mx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      mn[i] = INFINITY;
+      mx[i] = -INFINITY;
+    }
+#pragma unroll
+    for (int r = 0; r < kTile; ++r) {
+      if (r < rows) {
+        const uint8_t *src = k_pool + ((page * kTile + r) * row_vecs + v) * kCodeBytes;
+        float c[8];
+        if constexpr (KIND == 1) {
+          const uint2 w = __ldg(reinterpret_cast<const uint2 *>(src));
+          const float2 a = e4m3x2_to_float2(w.x), b = e4m3x2_to_float2(w.x >> 16);
+          const float2 x = e4m3x2_to_float2(w.y), y = e4m3x2_to_float2(w.y >> 16);
+          c[0] = a.x; c[1] = a.y; c[2] = b.x; c[3] = b.y;
+          c[4] = x.x; c[5] = x.y; c[6] = y.x; c[7] = y.y;
+        } else {
+          const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(src));
+#pragma unroll
+          for (int i = 0; i < 8; ++i) c[i] = static_cast<float>(static_cast<int>((w >> (4 * i)) & 0xFu) - 8);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          mn[i] = fminf(mn[i], __fmul_rd(c[i], sc));
+          mx[i] = fmaxf(mx[i], __fmul_ru(c[i], sc));
+        }
+      }
+    }
+    uint32_t pmn[4], pmx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      pmn[i] = bf16_directed<false>(mn[2 * i]) | (bf16_directed<false>(mn[2 * i + 1]) << 16);
+      pmx[i] = bf16_directed<true>(mx[2 * i]) | (bf16_directed<true>(mx[2 * i + 1]) << 16);
+    }
+    uint16_t *dst = summ + ((page * Hkv + h) * 2) * D + d;
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(pmn[0], pmn[1], pmn[2], pmn[3]);
+    *reinterpret_cast<uint4 *>(dst + D) = make_uint4(pmx[0], pmx[1], pmx[2], pmx[3]);
+  }
+}
+
 // Summaries [pages, Hkv, 2 (min, max), D] bf16, for the pages the listed slots were
 // written to: min/max over the page's rows 0 .. slot % 16.  When several listed
 // slots fall in one page only the last of them (largest slot, then largest index)
-// writes.  One CTA per listed token.
+// writes.  One CTA per listed token.  KIND 0: bf16 keys (exact min/max); 1, 2:
+// quantised keys restored with their (block, head) scale (summarize_quant).
+template <int KIND>
 __global__ void __launch_bounds__(128) quest_summarize_kernel(
-    const uint16_t *k_pool, uint16_t *summ, const int64_t *slot_mapping, int T, int Hkv, int D,
-    int64_t nrows, int32_t *err) {
+    const void *k_pool_raw, const float *k_scale, uint16_t *summ, const int64_t *slot_mapping,
+    int T, int Hkv, int D, int bs, int64_t nrows, int32_t *err) {
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x;
@@ -44,6 +115,12 @@ __global__ void __launch_bounds__(128) quest_summarize_kernel(
   }
   if (__syncthreads_or(later)) return;
   const int rows = static_cast<int>(slot - page * kTile) + 1;
+  if constexpr (KIND != 0) {
+    summarize_quant<KIND>(static_cast<const uint8_t *>(k_pool_raw), k_scale, summ, page, rows,
+                          Hkv, D, bs);
+    return;
+  }
+  const uint16_t *k_pool = static_cast<const uint16_t *>(k_pool_raw);
   // eight consecutive channels of one KV head per thread and pass (16-byte loads of
   // all 16 rows in flight; rows >= `rows` are not used)
   const int row_vecs = Hkv * D / 8;
@@ -490,14 +567,18 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
   }
 }
 
-pa_status run_quest_summarize(const pa_shape &s, const void *k_pool, void *summaries,
-                              const int64_t *slot_mapping, int32_t *err, cudaStream_t stream) {
-  return launch_pdl(quest_summarize_kernel, dim3(s.B), dim3(128), 0, stream,
-                    static_cast<const uint16_t *>(k_pool), static_cast<uint16_t *>(summaries),
-                    slot_mapping, s.B, s.Hkv, s.D,
-                    static_cast<int64_t>(s.nblocks) * s.block_size, err) == cudaSuccess
-             ? PA_OK
-             : PA_ERR_CUDA;
+pa_status run_quest_summarize(const pa_shape &s, const void *k_pool, const float *k_scale,
+                              void *summaries, const int64_t *slot_mapping, int32_t *err,
+                              cudaStream_t stream) {
+  auto launch = [&](auto kernel) {
+    return launch_pdl(kernel, dim3(s.B), dim3(128), 0, stream, k_pool, k_scale,
+                      static_cast<uint16_t *>(summaries), slot_mapping, s.B, s.Hkv, s.D,
+                      s.block_size, static_cast<int64_t>(s.nblocks) * s.block_size, err);
+  };
+  const cudaError_t e = s.kv_dtype == PA_KV_FP8_E4M3 ? launch(quest_summarize_kernel<1>)
+                        : s.kv_dtype == PA_KV_INT4   ? launch(quest_summarize_kernel<2>)
+                                                     : launch(quest_summarize_kernel<0>);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int quest_max_pages(const pa_shape &s) {

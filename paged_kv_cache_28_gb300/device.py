@@ -165,8 +165,9 @@ class DeviceBatch:
                                          device=self.device)
         slots = self.quest_summary_slots()
         shape = _lib.make_shape(slots.numel(), b.Hq, b.Hkv, b.D, b.block_size, b.nblocks,
-                                b.max_blocks)
-        _lib.pa_quest_summarize(shape, self.k_pool, self.key_summaries, slots, self.err, stream)
+                                b.max_blocks, self.shape.kv_dtype)
+        _lib.pa_quest_summarize(shape, self.k_pool, self.k_scale, self.key_summaries, slots,
+                                self.err, stream)
 
     def quest_buffers(self, topk: int):
         """page_scores [B, Hkv, pages per block-table row] and selected_pages [B, Hkv, topk]."""

@@ -234,11 +234,11 @@ def test_quest_host_checks(lib):
     import ctypes
     s = ctypes.byref(shape())
     fp8 = ctypes.byref(shape(D=128, kv_dtype=_lib.PA_KV_FP8_E4M3))
-    assert lib.pa_quest_summarize(fp8, FAKE, FAKE, FAKE, None, None) == _lib.PA_ERR_UNSUPPORTED
-    assert lib.pa_quest_summarize(s, FAKE, None, FAKE, None, None) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_quest_summarize(fp8, FAKE, None, FAKE, FAKE, None, None) == \
+        _lib.PA_ERR_INVALID_ARG                                          # no k_scale
+    assert lib.pa_quest_summarize(s, FAKE, None, None, FAKE, None, None) == \
+        _lib.PA_ERR_INVALID_ARG                                          # no summaries
     assert lib.pa_quest_select(s, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, None, None) == \
         _lib.PA_ERR_INVALID_ARG                                          # topk < 1
     assert lib.pa_quest_select(s, FAKE, FAKE, FAKE, FAKE, 4, None, FAKE, None, None) == \
         _lib.PA_ERR_INVALID_ARG                                          # no page_scores
-    assert lib.pa_quest_select(fp8, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, None, None) == \
-        _lib.PA_ERR_UNSUPPORTED

@@ -693,6 +693,102 @@ def test_quest_select_and_sparse_decode(topk, bs, Hq, Hkv, D):
     assert dev.read_err() == 0
 
 
+@pytest.mark.parametrize("kv_dtype,bs", [("fp8_e4m3", 16), ("fp8_e4m3", 32), ("int4", 16),
+                                         ("int4", 32)])
+def test_quest_summaries_quantised_bit_exact(kv_dtype, bs):
+    """Summaries of E4M3 / 4-bit pools: the oracle's outward-rounded bf16 bounds of the
+    restored keys, bit for bit, for every page of every sequence (full and partial pages,
+    pages sharing a block)."""
+    batch = wl.build_batch("t", [1, 15, 16, 17, 100, 333], Hq=16, Hkv=4, D=128, block_size=bs,
+                           seed=92 + bs, kv_dtype=kv_dtype)
+    dev = DeviceBatch(batch)
+    dev.quest_build_summaries()
+    torch.cuda.synchronize()
+    got = dev.key_summaries.view(torch.int16).cpu().numpy().view(np.uint16)
+    checked = 0
+    for b in range(batch.B):
+        L = int(batch.seq_lens[b])
+        for j in range((L + 15) // 16):
+            rows = min(16, L - 16 * j)
+            page = batch.block_tables[b, 16 * j // bs] * (bs // 16) + (16 * j % bs) // 16
+            for h in range(batch.Hkv):
+                mn, mx = oracle.quest_page_summary(batch.k_pool, page, rows, h, Hkv=batch.Hkv,
+                                                   D=128, block_size=bs, k_scale=batch.k_scale)
+                assert np.array_equal(got[page, h, 0], wl.bf16_bits(mn.astype(np.float32))), \
+                    (b, j, h)
+                assert np.array_equal(got[page, h, 1], wl.bf16_bits(mx.astype(np.float32))), \
+                    (b, j, h)
+                checked += 1
+    assert checked > 40 and dev.read_err() == 0
+
+
+def _oracle_quant_page_scores(batch):
+    """[B][Hkv] -> exact page scores (group max) over the oracle's stored summaries."""
+    bs, G = batch.block_size, batch.Hq // batch.Hkv
+    q = wl.bf16_to_float(batch.q).astype(np.float64)
+    out = {}
+    for b in range(batch.B):
+        L = int(batch.seq_lens[b])
+        for kvh in range(batch.Hkv):
+            sc = []
+            for j in range((L + 15) // 16):
+                page = batch.block_tables[b, 16 * j // bs] * (bs // 16) + (16 * j % bs) // 16
+                mn, mx = oracle.quest_page_summary(batch.k_pool, page, min(16, L - 16 * j), kvh,
+                                                   Hkv=batch.Hkv, D=batch.D, block_size=bs,
+                                                   k_scale=batch.k_scale)
+                qs = q[b, kvh * G:(kvh + 1) * G]
+                sc.append(max(oracle.page_score(qs[g], mn, mx) for g in range(G)))
+            out[b, kvh] = np.array(sc)
+    return out
+
+
+@pytest.mark.parametrize("kv_dtype,topk,bs", [("fp8_e4m3", 4, 16), ("fp8_e4m3", 13, 32),
+                                              ("int4", 4, 16), ("int4", 9, 32)])
+def test_quest_quantised_select_and_sparse_decode(kv_dtype, topk, bs):
+    """Quest end to end on E4M3 / 4-bit pools: the selection is the oracle's wherever the
+    k-th / (k+1)-th score gap exceeds fp32 rounding (else a valid top-k), and every row's
+    output matches the oracle's decode over the GPU's selection (quantised tolerance)."""
+    lens = [1, 15, 16, 17, 100, 333, 1000, 0, 64]
+    batch = wl.build_batch("t", lens, Hq=64, Hkv=8, D=128, block_size=bs, seed=93 + topk,
+                           kv_dtype=kv_dtype)
+    dev = DeviceBatch(batch)
+    dev.quest_build_summaries()
+    sel = dev.quest_select(topk)
+    torch.cuda.synchronize()
+    gpu_sel = sel.cpu().numpy()
+    _, ref_sel = oracle.quest_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                     batch.seq_lens, batch.sm_scale, Hkv=batch.Hkv,
+                                     block_size=bs, topk=topk, k_scale=batch.k_scale,
+                                     v_scale=batch.v_scale)
+    same = 0
+    for (b, kvh), sc in _oracle_quant_page_scores(batch).items():
+        g, r = gpu_sel[b, kvh], ref_sel[b, kvh]
+        n = min(topk, sc.size)
+        assert np.all(g[n:] == -1) and np.all(np.diff(g[:n]) > 0)
+        if np.array_equal(g, r):
+            same += 1
+            continue
+        srt = np.sort(sc)[::-1]
+        gap = srt[n - 1] - srt[n] if n < sc.size else np.inf
+        assert gap <= 1e-4 * max(1.0, abs(srt[n - 1])), (b, kvh, gap)
+        assert sc[g[:n]].min() >= srt[n - 1] - 1e-4 * max(1.0, abs(srt[n - 1]))
+    assert same >= 0.9 * batch.B * batch.Hkv
+    ref = oracle.paged_decode_pages(batch.q, batch.k_pool, batch.v_pool, batch.block_tables,
+                                    batch.seq_lens, batch.sm_scale, gpu_sel, Hkv=batch.Hkv,
+                                    block_size=bs, k_scale=batch.k_scale, v_scale=batch.v_scale)
+    for mode, ns in (("decode", None), ("split", 1), ("split", 11), ("parts", 4)):
+        dev.out.fill_(float("nan"))
+        if mode == "decode":
+            dev.decode(selected_pages=sel)
+        elif mode == "parts":
+            dev.decode_splitkv(ns, selected_pages=sel)
+        else:
+            dev.decode_segments(ns, selected_pages=sel)
+        torch.cuda.synchronize()
+        assert_close(dev.out.cpu().numpy(), ref, batch, f"{kv_dtype} quest topk={topk} {mode} {ns}")
+    assert dev.read_err() == 0
+
+
 def test_quest_all_pages_equals_full_decode():
     batch = wl.build_batch("t", [5, 70, 300], Hq=64, Hkv=8, D=128, block_size=16, seed=95)
     dev = DeviceBatch(batch)
