@@ -1622,12 +1622,25 @@ __global__ void __launch_bounds__(512) merge_parts_kernel(float *out, const floa
       const float l = s0 + lane < S ? __ldg(lr + s0 + lane) : -INFINITY;
       const float w = l == -INFINITY ? 0.f : expf(l - M);
       den += w;
-      for (uint32_t live = __ballot_sync(0xffffffffu, w > 0.f); live; live &= live - 1) {
-        const int j = __ffs(live) - 1;
-        const float wj = __shfl_sync(0xffffffffu, w, j);
-        const float *x = orow + static_cast<size_t>(s0 + j) * D;
+      // the live slots' rows in increasing slot order, four rows' loads in flight at
+      // once (a head of a long sequence has tens of live slots)
+      for (uint32_t live = __ballot_sync(0xffffffffu, w > 0.f); live;) {
+        constexpr int U = 4;
+        float wj[U], x[U][E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] += wj * __ldg(x + e * 32 + lane);
+        for (int u = 0; u < U; ++u) {
+          const int j = live ? __ffs(live) - 1 : -1;   // warp-uniform
+          live &= live - 1;
+          wj[u] = __shfl_sync(0xffffffffu, w, j < 0 ? 0 : j);
+          const float *row = orow + static_cast<size_t>(s0 + (j < 0 ? 0 : j)) * D;
+#pragma unroll
+          for (int e = 0; e < E; ++e) x[u][e] = j < 0 ? 0.f : __ldg(row + e * 32 + lane);
+          if (j < 0) wj[u] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] += wj[u] * x[u][e];
       }
     }
 #pragma unroll
