@@ -22,21 +22,29 @@ constexpr int kCasWarps = 4;
 constexpr int kCasThreads = 32 * kCasWarps;
 constexpr int kCasStages = 4;
 
-template <int D_>
+// FP8: E4M3 code pools ("KV Cache Engineering for LLM Serving", section 8) with one
+// fp32 scale per (block, KV head) for K and for V, D = 128.
+template <int D_, bool FP8_>
 struct CasCfg {
   static constexpr int D = D_;
-  static constexpr int ROW = 2 * D;             // bytes of one token's head row (bf16)
+  static constexpr bool FP8 = FP8_;
+  static constexpr int ROW = FP8 ? D : 2 * D;   // bytes of one token's head row
   static constexpr int BOXES = ROW / 128;       // 128-byte TMA boxes per row
   static constexpr int KV_BYTES = kTile * ROW;  // one 16-token tile of K (or V)
   static constexpr int STAGE = 2 * KV_BYTES;
   static constexpr int KS = D / 16;             // QK k-steps
   static constexpr int DT = D / 8;              // PV n-tiles (8 output channels each)
-  static constexpr int FIXED = 1024 + kCasStages * STAGE + 2 * kCasStages * 8;
+  // stages, full and empty barriers, each stage's (k scale, v scale)
+  static constexpr int FIXED = 1024 + kCasStages * STAGE + 2 * kCasStages * 8 + kCasStages * 8;
   static_assert(ROW % 128 == 0, "rows are whole 128-byte boxes");
+  static_assert(STAGE % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
+  static_assert(!FP8 || D == 128, "E4M3 pools have D = 128");
 };
 
 struct CascadeParams {
   const uint16_t *q;
+  const float *k_scale;     // E4M3 pools: [nblocks, Hkv] scales, else null
+  const float *v_scale;
   const int32_t *block_tables;
   const int32_t *group_offsets;
   const int32_t *group_seqs;
@@ -108,24 +116,35 @@ __global__ void __launch_bounds__(256) cascade_plan_kernel(const CascadeParams p
   }
 }
 
-template <int D>
+// E4M3 tiles: the mma's k order within a 16-channel step is permuted so that a lane's
+// four consecutive codes (one ldmatrix byte-pair word) give both of its K^T fragment
+// registers: k slots 2t, 2t+1 <- channels 4t, 4t+1 and 2t+8, 2t+9 <- 4t+2, 4t+3.  The
+// query rows (A operand) take the same order.  P V reads V codes by ldmatrix.trans on
+// the byte-pair view: lane (r, t) receives tokens 2t, 2t+1 of channels 2r, 2r+1; one
+// byte permute splits them into channel 2r (even n-tile) and 2r+1 (odd n-tile).
+__device__ __forceinline__ uint32_t f16x2_of_bf16x2(uint32_t w, float up) {
+  return pack_f16(bf16_lo(w) * up, bf16_hi(w) * up);
+}
+
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kCasThreads, 3)
     cascade_kernel(const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const CascadeParams p) {
-  using C = CasCfg<D>;
+  using C = CasCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *stages = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(stages + kCasStages * C::STAGE);
   uint64_t *empty = full + kCasStages;            // all four warps are done with the stage
-  int32_t *gprefix = reinterpret_cast<int32_t *>(empty + kCasStages);  // [num_groups + 1]
+  float *scl = reinterpret_cast<float *>(empty + kCasStages);   // [stage][k scale, v scale]
+  int32_t *gprefix = reinterpret_cast<int32_t *>(scl + 2 * kCasStages);  // [num_groups + 1]
   __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g4 = lane >> 2, tig = lane & 3;
   pdl_trigger();
   if (tid == 0) {
     for (int s = 0; s < kCasStages; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&full[s]), FP8 ? 2 : 1);   // E4M3: plus the scales' cp.async
       mbar_init(smem_u32(&empty[s]), kCasWarps);
     }
     fence_mbar_init();
@@ -201,11 +220,22 @@ __global__ void __launch_bounds__(kCasThreads, 3)
       const int y = (phys == kInvalidPhys) ? p.nblocks * p.bs : phys * p.bs + (t * kTile) % p.bs;
       const uint32_t bar = smem_u32(&full[s]);
       const uint32_t dst = smem_u32(stages + s * C::STAGE);
+      if constexpr (FP8) {                       // the tile's block scales, with the tile
+        float *sc = scl + 2 * s;
+        if (phys != kInvalidPhys) {
+          cp_async_4(smem_u32(sc), p.k_scale + static_cast<size_t>(phys) * p.Hkv + kvh);
+          cp_async_4(smem_u32(sc + 1), p.v_scale + static_cast<size_t>(phys) * p.Hkv + kvh);
+        } else {
+          sc[0] = sc[1] = 0.f;
+        }
+        cp_async_arrive(bar);
+      }
       fence_proxy_async();
       mbar_arrive_expect_tx(bar, 2 * C::KV_BYTES);
+      constexpr int kBoxElems = FP8 ? 128 : 64;  // elements of one 128-byte box
 #pragma unroll
       for (int h = 0; h < C::BOXES; ++h) {
-        const int x = kvh * D + h * 64;
+        const int x = kvh * D + h * kBoxElems;
         tma_load_2d(dst + h * (kTile * 128), &tmK, x, y, bar);
         tma_load_2d(dst + C::KV_BYTES + h * (kTile * 128), &tmV, x, y, bar);
       }
@@ -232,6 +262,7 @@ __global__ void __launch_bounds__(kCasThreads, 3)
       // rows past the members pad the last chunk; member slots are bounded by B
       if (rmember[h] >= w.members || off + rmember[h] >= p.B) rmember[h] = -1;
     }
+    float qshift[2] = {1.f, 1.f};                // E4M3: 2^-k undoing each row's scaling
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint32_t *qr = nullptr;
@@ -241,10 +272,39 @@ __global__ void __launch_bounds__(kCasThreads, 3)
           qr = reinterpret_cast<const uint32_t *>(
               p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G + rhead[h]) * D);
       }
+      if constexpr (!FP8) {
 #pragma unroll
-      for (int ks = 0; ks < C::KS; ++ks) {
-        qa[ks][h] = qr ? __ldg(qr + ks * 8 + tig) : 0u;         // channels 16ks + 2tig..
-        qa[ks][h + 2] = qr ? __ldg(qr + ks * 8 + 4 + tig) : 0u; // 16ks + 8 + 2tig..
+        for (int ks = 0; ks < C::KS; ++ks) {
+          qa[ks][h] = qr ? __ldg(qr + ks * 8 + tig) : 0u;         // channels 16ks + 2tig..
+          qa[ks][h + 2] = qr ? __ldg(qr + ks * 8 + 4 + tig) : 0u; // 16ks + 8 + 2tig..
+        }
+      } else {
+        // channels 16ks + 4tig + {0,1} and + {2,3} (the permuted k order), scaled by 2^k
+        // so that the row's largest magnitude sits just below 2^15: exact in f16
+        uint32_t raw[C::KS][2];
+        float amax = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < C::KS; ++ks) {
+          raw[ks][0] = qr ? __ldg(qr + ks * 8 + 2 * tig) : 0u;
+          raw[ks][1] = qr ? __ldg(qr + ks * 8 + 2 * tig + 1) : 0u;
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(raw[ks][e])), fabsf(bf16_hi(raw[ks][e]))));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));   // the row's quad
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int k = 0;
+        if (amax > 0.f) {
+          const int e = ((__float_as_uint(amax) >> 23) & 0xFF) - 126;   // amax < 2^e
+          k = min(max(15 - e, -100), 100);
+        }
+        const float up = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+        qshift[h] = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+#pragma unroll
+        for (int ks = 0; ks < C::KS; ++ks) {
+          qa[ks][h] = f16x2_of_bf16x2(raw[ks][0], up);
+          qa[ks][h + 2] = f16x2_of_bf16x2(raw[ks][1], up);
+        }
       }
     }
     float acc[C::DT][4];
@@ -253,6 +313,9 @@ __global__ void __launch_bounds__(kCasThreads, 3)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[dt][i] = 0.f;
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    // E4M3: the accumulator is in units of vref (the item's first nonzero V scale, or
+    // a later one when the ratio leaves [kRatMin, kRatMax]); vinv = 0 before it
+    float vref = 1.f, vinv = 0.f;
 
     __syncthreads();                             // s_abort from the first issues
     int j = 0;
@@ -268,7 +331,7 @@ __global__ void __launch_bounds__(kCasThreads, 3)
 
       // ---- S = Q K^T for 16 rows x 16 tokens (two n-tiles of 8 tokens)
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
+      if constexpr (!FP8) {
         const int tok = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
@@ -278,6 +341,21 @@ __global__ void __launch_bounds__(kCasThreads, 3)
           mma_bf16(sc[0], qa[ks], b[0], b[1]);
           mma_bf16(sc[1], qa[ks], b[2], b[3]);
         }
+      } else {
+        // matrices: tokens 0-7 / 8-15 of 16-code chunks ks and ks + 1
+        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int ks = 0; ks < C::KS; ks += 2) {
+          const int c = ks + (lane >> 4);
+          uint32_t b[4];
+          ldsm_x4(b, kt + tok * 128 + ((c ^ (tok & 7)) << 4));
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+              mma_f16(sc[nt], qa[ks + u], e4m3x2_to_f16x2(b[2 * u + nt]),
+                      e4m3x2_hi_to_f16x2(b[2 * u + nt]));
+        }
       }
       // ---- online softmax per row (log2 domain); element i: row g4 + 8 (i >> 1).  A
       // row's reference maximum moves only when a score exceeds it by more than 8, so
@@ -285,11 +363,29 @@ __global__ void __launch_bounds__(kCasThreads, 3)
       // reduction across lanes and the accumulator rescale.
       float pr[2][4];
       bool over = false;
+      float ssc[2] = {p.sl2, p.sl2};             // raw mma score -> log2-domain score
+      float rat = 1.f;                           // E4M3: tile V scale / accumulator's
+      if constexpr (FP8) {
+        const float2 tsc = *reinterpret_cast<const float2 *>(scl + 2 * s);   // k, v scale
+        ssc[0] = p.sl2 * tsc.x * qshift[0];
+        ssc[1] = p.sl2 * tsc.x * qshift[1];
+        rat = tsc.y * vinv;                      // warp-uniform; 0 for a zero V scale
+        if (tsc.y > 0.f && !(rat <= kRatMax && rat >= kRatMin)) {
+          const float f = vref / tsc.y;          // re-express in the tile's scale
+#pragma unroll
+          for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[dt][i] *= f;
+          vref = tsc.y;
+          vinv = 1.f / tsc.y;
+          rat = 1.f;
+        }
+      }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          sc[nt][i] *= p.sl2;
+          sc[nt][i] *= ssc[i >> 1];
           over |= sc[nt][i] > m[i >> 1] + 8.f;
         }
       if (__any_sync(0xffffffffu, over)) {
@@ -319,17 +415,46 @@ __global__ void __launch_bounds__(kCasThreads, 3)
             pr[nt][2 * h + e] = v;
             l[h] += v;
           }
-      // ---- P as the A operand (the accumulator layout is the A layout): bf16 hi + lo
+      // ---- P as the A operand (the accumulator layout is the A layout), hi + lo terms:
+      // bf16 against bf16 V; f16 times the V-scale ratio against E4M3 V
       uint32_t ph[4], pl[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int nt = i >> 1, h = i & 1;        // a0: row g4, tokens 0-7; a1: row g4 + 8; ...
         const float p0 = pr[nt][2 * h], p1 = pr[nt][2 * h + 1];
-        ph[i] = pack_bf16(p0, p1);
-        pl[i] = pack_bf16(p0 - bf16_lo(ph[i]), p1 - bf16_hi(ph[i]));
+        if constexpr (!FP8) {
+          ph[i] = pack_bf16(p0, p1);
+          pl[i] = pack_bf16(p0 - bf16_lo(ph[i]), p1 - bf16_hi(ph[i]));
+        } else {
+          const float a0 = p0 * rat, a1 = p1 * rat;
+          ph[i] = pack_f16(a0, a1);
+          const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&ph[i]));
+          pl[i] = pack_f16(a0 - hf.x, a1 - hf.y);
+        }
       }
       // ---- O += P V: V^T fragments by ldmatrix.trans on the token rows
-      {
+      if constexpr (FP8) {
+        // n-tile 2c + e: channels 16c + 2r + e (r = lane / 4) of 16-code chunk c
+        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int jc = 0; jc < D / 16; jc += 2) {
+          const int c = jc + (lane >> 4);
+          uint32_t b[4];
+          ldsm_x4_trans(b, vt + tok * 128 + ((c ^ (tok & 7)) << 4));
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t x0 = __byte_perm(b[2 * u], 0u, 0x3120);       // tokens 2t, 2t+1
+            const uint32_t x1 = __byte_perm(b[2 * u + 1], 0u, 0x3120);   // tokens 2t+8, 2t+9
+            const int n0 = 2 * (jc + u);
+            const uint32_t e0 = e4m3x2_to_f16x2(x0), e1 = e4m3x2_to_f16x2(x1);
+            const uint32_t o0 = e4m3x2_hi_to_f16x2(x0), o1 = e4m3x2_hi_to_f16x2(x1);
+            mma_f16(acc[n0], ph, e0, e1);
+            mma_f16(acc[n0], pl, e0, e1);
+            mma_f16(acc[n0 + 1], ph, o0, o1);
+            mma_f16(acc[n0 + 1], pl, o0, o1);
+          }
+        }
+      } else {
         const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
         for (int jd = 0; jd < C::DT / 2; ++jd) {
@@ -373,34 +498,46 @@ __global__ void __launch_bounds__(kCasThreads, 3)
       const size_t slot =
           ((static_cast<size_t>(off + rmember[h]) * p.Hkv + kvh) * kCascadePieces + piece) * p.G +
           rhead[h];
-      const float inv = 1.f / lt;
+      const float inv = (FP8 ? vref : 1.f) / lt;
       float *orow = p.o + slot * D;
+      if constexpr (FP8) {   // n-tiles 2c, 2c + 1 hold channels 16c + 4tig + {0, 2} and {1, 3}
 #pragma unroll
-      for (int dt = 0; dt < C::DT; ++dt)
-        *reinterpret_cast<float2 *>(orow + dt * 8 + 2 * tig) =
-            make_float2(acc[dt][2 * h] * inv, acc[dt][2 * h + 1] * inv);
+        for (int c = 0; c < D / 16; ++c)
+          *reinterpret_cast<float4 *>(orow + 16 * c + 4 * tig) =
+              make_float4(acc[2 * c][2 * h] * inv, acc[2 * c + 1][2 * h] * inv,
+                          acc[2 * c][2 * h + 1] * inv, acc[2 * c + 1][2 * h + 1] * inv);
+      } else {
+#pragma unroll
+        for (int dt = 0; dt < C::DT; ++dt)
+          *reinterpret_cast<float2 *>(orow + dt * 8 + 2 * tig) =
+              make_float2(acc[dt][2 * h] * inv, acc[dt][2 * h + 1] * inv);
+      }
       if (tig == 0) p.lse[slot] = (m[h] + __log2f(lt)) * kLn2;
     }
   }
 }
 
 static CascadeParams cascade_params(const pa_shape &s, const void *q, const int32_t *bt,
+                                    const float *k_scale, const float *v_scale,
                                     const pa_decode_opts &opts, float sm_scale, int32_t *err);
 
 pa_status run_cascade_plan(const pa_shape &s, const pa_decode_opts &opts, int32_t *err,
                            cudaStream_t stream) {
-  const CascadeParams p = cascade_params(s, nullptr, nullptr, opts, 1.f, err);
+  const CascadeParams p = cascade_params(s, nullptr, nullptr, nullptr, nullptr, opts, 1.f, err);
   return launch_pdl(cascade_plan_kernel, dim3(1), dim3(256), 0, stream, p) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }
 
 static CascadeParams cascade_params(const pa_shape &s, const void *q, const int32_t *bt,
+                                    const float *k_scale, const float *v_scale,
                                     const pa_decode_opts &opts, float sm_scale, int32_t *err) {
   const CascadeLayout cl = cascade_layout(s.B, s.Hq, s.D);
   uint8_t *ws = static_cast<uint8_t *>(opts.cascade_workspace);
   CascadeParams p{};
   p.q = static_cast<const uint16_t *>(q);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.block_tables = bt;
   p.group_offsets = opts.group_offsets;
   p.group_seqs = opts.group_seqs;
@@ -424,29 +561,30 @@ static CascadeParams cascade_params(const pa_shape &s, const void *q, const int3
   return p;
 }
 
+template <int D, bool FP8>
+static cudaError_t launch_cascade(const CUtensorMap &mk, const CUtensorMap &mv,
+                                  const CascadeParams &p, int grid, cudaStream_t stream) {
+  const size_t smem = CasCfg<D, FP8>::FIXED + (static_cast<size_t>(p.num_groups) + 1) * 4;
+  cudaError_t e = cudaFuncSetAttribute(cascade_kernel<D, FP8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cascade_kernel<D, FP8><<<grid, kCasThreads, smem, stream>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
 pa_status run_cascade(const pa_shape &s, const CUtensorMap &mk, const CUtensorMap &mv,
-                      const void *q, const int32_t *bt, const pa_decode_opts &opts,
-                      float sm_scale, int32_t *err, int ctas, cudaStream_t stream) {
-  const CascadeParams p = cascade_params(s, q, bt, opts, sm_scale, err);
-  const int grid = ctas;
+                      const void *q, const int32_t *bt, const float *k_scale,
+                      const float *v_scale, const pa_decode_opts &opts, float sm_scale,
+                      int32_t *err, int ctas, cudaStream_t stream) {
+  const CascadeParams p = cascade_params(s, q, bt, k_scale, v_scale, opts, sm_scale, err);
   cudaError_t e;
-  if (s.D == 128) {
-    const size_t smem = CasCfg<128>::FIXED + (static_cast<size_t>(p.num_groups) + 1) * 4;
-    e = cudaFuncSetAttribute(cascade_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e == cudaSuccess) {
-      cascade_kernel<128><<<grid, kCasThreads, smem, stream>>>(mk, mv, p);
-      e = cudaGetLastError();
-    }
-  } else {
-    const size_t smem = CasCfg<64>::FIXED + (static_cast<size_t>(p.num_groups) + 1) * 4;
-    e = cudaFuncSetAttribute(cascade_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e == cudaSuccess) {
-      cascade_kernel<64><<<grid, kCasThreads, smem, stream>>>(mk, mv, p);
-      e = cudaGetLastError();
-    }
-  }
+  if (s.kv_dtype == PA_KV_FP8_E4M3)
+    e = launch_cascade<128, true>(mk, mv, p, ctas, stream);
+  else if (s.D == 128)
+    e = launch_cascade<128, false>(mk, mv, p, ctas, stream);
+  else
+    e = launch_cascade<64, false>(mk, mv, p, ctas, stream);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

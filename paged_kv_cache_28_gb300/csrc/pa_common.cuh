@@ -26,6 +26,12 @@ constexpr int kHintShared = 1 << 12;   // tile lies in a prefix other sequences 
 constexpr int kHintPrivate = 1 << 13;  // tile is private (hints given, not shared)
 constexpr int kCascade = 1 << 14;      // the sequence's shared prefix is done by the cascade
 constexpr int kInvalidPhys = -1;
+// Quantised caches: P enters the PV mma as f16 times the ratio of the tile's V scale to
+// the accumulator's.  The ratio stays <= 2^7, so that a weight <= 2^8 times it is well
+// inside f16, and >= 2^-12, so that a tile's largest weights keep f16's normal range;
+// outside that the accumulator is re-expressed in the tile's scale.
+constexpr float kRatMax = 128.f;
+constexpr float kRatMin = 1.f / 4096.f;
 
 __device__ __forceinline__ void set_err(int32_t *flag, int bits) {
   if (flag) atomicOr(flag, bits);

@@ -303,12 +303,6 @@ constexpr int kKvhMask = 0x7FF;
 // A head's reference maximum (log2 domain) moves only when a score exceeds it by more
 // than this, so every p stays <= 2^8.
 constexpr float kMaxSlack = 8.f;
-// Quantised caches: P enters the mma as f16 times the ratio of the tile's V scale to
-// the accumulator's.  The ratio stays <= 2^7, so that 2^8 * 2^7 is well inside f16, and
-// >= 2^-12, so that a tile's largest weights keep f16's normal range; outside that the
-// accumulator is re-expressed in the tile's scale.
-constexpr float kRatMax = 128.f;
-constexpr float kRatMin = 1.f / 4096.f;
 // Quantised caches: largest restored |V| of a tile (V scale x largest code) for which P
 // enters the PV product as one f16 term; the term's rounding then adds at most
 // 2^-12 * 16 < 4e-3 to an output, a fifth of the quantised tolerance 2e-2.
@@ -1951,13 +1945,13 @@ pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int
   if (side) {
     if (cudaEventRecord(fork, stream) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
       return PA_ERR_CUDA;
-    st = run_cascade(v, mk, mv, q, bt, *opts, sm_scale, err, sms, side);
+    st = run_cascade(v, mk, mv, q, bt, k_scale, v_scale, *opts, sm_scale, err, sms, side);
     if (st != PA_OK) return st;
     if (cudaEventRecord(join, side) != cudaSuccess) return PA_ERR_CUDA;
   }
   st = dispatch_segments(v, heads, p, mk, mv, stream);
   if (st != PA_OK) return st;
-  st = run_cascade(v, mk, mv, q, bt, *opts, sm_scale, err, 3 * sms, stream);
+  st = run_cascade(v, mk, mv, q, bt, k_scale, v_scale, *opts, sm_scale, err, 3 * sms, stream);
   if (st != PA_OK) return st;
   if (side && cudaStreamWaitEvent(stream, join, 0) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;

@@ -88,8 +88,9 @@ bool make_pool_map(CUtensorMap *map, const void *pool, const pa_shape &s, int he
 pa_status run_cascade_plan(const pa_shape &s, const pa_decode_opts &opts, int32_t *err,
                            cudaStream_t stream);
 pa_status run_cascade(const pa_shape &s, const CUtensorMap &mk, const CUtensorMap &mv,
-                      const void *q, const int32_t *bt, const pa_decode_opts &opts,
-                      float sm_scale, int32_t *err, int ctas, cudaStream_t stream);
+                      const void *q, const int32_t *bt, const float *k_scale,
+                      const float *v_scale, const pa_decode_opts &opts, float sm_scale,
+                      int32_t *err, int ctas, cudaStream_t stream);
 
 // Largest batch the split-KV kernel accepts (its length scan lives in shared memory).
 constexpr int kMaxSplitBatch = 16384;

@@ -989,7 +989,7 @@ def _sample_rows(batch, rng, n_random=192):
 
 # ---------------------------------------------------------------- cascade (shared prefixes)
 
-def _cascade_batch(Hq, Hkv, D, bs, groups, free_lens, seed, plens=None):
+def _cascade_batch(Hq, Hkv, D, bs, groups, free_lens, seed, plens=None, kv_dtype="bf16"):
     """groups: [(prefix tokens, [suffix lengths])]; members follow each other, then the
     ungrouped sequences.  plens: the cascade lengths (default: prefix cut to tiles)."""
     lens, pgroups, b = [], [], 0
@@ -1000,7 +1000,7 @@ def _cascade_batch(Hq, Hkv, D, bs, groups, free_lens, seed, plens=None):
         b += len(suffixes)
     lens += list(free_lens)
     batch = wl.build_batch("t", lens, Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seed=seed,
-                           prefix_groups=pgroups)
+                           prefix_groups=pgroups, kv_dtype=kv_dtype)
     offsets, seqs, plen = wl.cascade_groups(batch)
     if plens is not None:
         plen = np.asarray(plens, np.int32)
@@ -1196,6 +1196,51 @@ def test_cascade_matches_oracle(Hq, Hkv, D, bs, groups, free):
             assert_close(_run_cascade(dev, ns), ref, batch, f"cascade side={side} segments={ns}")
     assert dev.read_err() == 0
 
+
+
+FP8_CASCADE_CASES = [
+    (64, 8, 16, [(900, [1, 5, 17, 300, 2, 64, 40, 1000]), (300, [3, 30])], [7, 500, 1]),
+    (64, 8, 16, [(2000, [1, 2, 3])], [100]),                          # four pieces per member
+    (32, 2, 16, [(500, [9, 90, 900]), (16, [1, 2])], [33]),           # G = 16 (two n-tiles)
+    (8, 8, 16, [(160, [5, 6, 7, 8, 9])], []),                         # G = 1
+    (32, 8, 32, [(704, list(range(1, 41))), (32, [4, 4])], [9]),      # G = 4, bs = 32
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,bs,groups,free", FP8_CASCADE_CASES)
+def test_cascade_fp8_matches_oracle(Hq, Hkv, bs, groups, free):
+    """The cascade over E4M3 pools (codes restored with their block scales, this step's
+    quantised cache write applied first): equal to the oracle's plain decode at the
+    quantised tolerance, beside or after the split kernel, at several segment counts."""
+    batch, cg = _cascade_batch(Hq, Hkv, 128, bs, groups, free, seed=300 + Hq + bs,
+                               kv_dtype="fp8_e4m3")
+    dev = DeviceBatch(batch)
+    dev.reshape_and_cache()
+    ref, _ = oracle_after_write(batch)
+    for side in (True, False):
+        dev.enable_cascade(cg, side_stream=side)
+        for ns in (1, 17, 500, default_num_segments(dev.shape)):
+            assert_close(_run_cascade(dev, ns), ref, batch,
+                         f"fp8 cascade side={side} segments={ns}")
+    assert dev.read_err() == 0
+
+
+def test_cascade_fp8_scale_spread():
+    """E4M3 cascade with K and V block scales spread over 2^-12 .. 2^6 (the accumulator
+    is re-expressed when a tile's V-scale ratio leaves [2^-12, 2^7]; large restored V
+    values), a zero V scale on some blocks, and a staircase of scores in the prefix."""
+    batch, cg = _cascade_batch(64, 8, 128, 16, [(1200, [1, 9, 300]), (320, [4, 60])], [77],
+                               seed=311, kv_dtype="fp8_e4m3")
+    rng = np.random.default_rng(311)
+    batch.k_scale[...] = (2.0 ** rng.uniform(-12, 2, batch.k_scale.shape)).astype(np.float32)
+    batch.v_scale[...] = (2.0 ** rng.uniform(-12, 6, batch.v_scale.shape)).astype(np.float32)
+    batch.v_scale[rng.random(batch.v_scale.shape) < 0.05] = 0.0
+    dev = DeviceBatch(batch)
+    ref, _ = oracle_after_write(batch, write=False)
+    dev.enable_cascade(cg)
+    for ns in (1, 9, default_num_segments(dev.shape)):
+        assert_close(_run_cascade(dev, ns), ref, batch, f"fp8 cascade scale spread {ns}")
+    assert dev.read_err() == 0
 
 
 def test_cascade_through_pa_decode():
