@@ -148,10 +148,10 @@ typedef struct {
  *     member holds at least group_prefix_len[g] tokens (a member with fewer sets
  *     PA_DEVERR_SEQ_LEN and its output is undefined).  cascade_workspace:
  *     device memory of at least pa_cascade_workspace_bytes bytes, 256-byte
- *     aligned.  bf16 and FP8-E4M3 pools (E4M3 codes are restored with their
- *     block scales as in the decode); 4-bit pools return PA_ERR_UNSUPPORTED.  Not
- *     combined with window or topk.  The result equals the plain decode's up to
- *     rounding order.
+ *     aligned.  Every pool kind: FP8-E4M3 and 4-bit codes are restored with
+ *     their block scales as in the decode (a cascade decode on 4-bit pools reads
+ *     the KV heads one at a time, not in pairs).  Not combined with window or
+ *     topk.  The result equals the plain decode's up to rounding order.
  *   cascade_stream, cascade_events: where the cascade kernel runs.  NULL: on
  *     `stream`, after the split kernel.  Otherwise a caller-owned stream of the
  *     same device, on which the cascade kernel runs beside the split kernel (it

@@ -71,7 +71,6 @@ pa_status check_decode_args(const pa_shape *shape, const float *out, const void 
       if (opts->window > 0 || opts->topk > 0) return PA_ERR_INVALID_ARG;
       if (opts->cascade_stream && (!opts->cascade_events[0] || !opts->cascade_events[1]))
         return PA_ERR_INVALID_ARG;
-      if (shape->kv_dtype == PA_KV_INT4) return PA_ERR_UNSUPPORTED;   // bf16 and E4M3 pools
       if (opts->num_prefix_groups > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
     }
   }

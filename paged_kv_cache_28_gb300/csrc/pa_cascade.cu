@@ -22,23 +22,26 @@ constexpr int kCasWarps = 4;
 constexpr int kCasThreads = 32 * kCasWarps;
 constexpr int kCasStages = 4;
 
-// FP8: E4M3 code pools ("KV Cache Engineering for LLM Serving", section 8) with one
-// fp32 scale per (block, KV head) for K and for V, D = 128.
-template <int D_, bool FP8_>
+// KIND 0: bf16 pools.  1: E4M3 code pools, 2: 4-bit code pools (offset-binary nibbles,
+// element 2j in the low nibble of byte j), each with one fp32 scale per (block, KV
+// head) for K and for V ("KV Cache Engineering for LLM Serving", section 8), D = 128.
+template <int D_, int KIND_>
 struct CasCfg {
   static constexpr int D = D_;
-  static constexpr bool FP8 = FP8_;
-  static constexpr int ROW = FP8 ? D : 2 * D;   // bytes of one token's head row
-  static constexpr int BOXES = ROW / 128;       // 128-byte TMA boxes per row
+  static constexpr int KIND = KIND_;
+  static constexpr bool FP8 = KIND == 1, INT4 = KIND == 2, QUANT = KIND != 0;
+  static constexpr int ROW = INT4 ? D / 2 : (FP8 ? D : 2 * D);   // bytes of a head row
+  static constexpr int BOX = ROW < 128 ? ROW : 128;   // TMA box width (= swizzle span)
+  static constexpr int BOXES = ROW / BOX;
   static constexpr int KV_BYTES = kTile * ROW;  // one 16-token tile of K (or V)
   static constexpr int STAGE = 2 * KV_BYTES;
   static constexpr int KS = D / 16;             // QK k-steps
   static constexpr int DT = D / 8;              // PV n-tiles (8 output channels each)
   // stages, full and empty barriers, each stage's (k scale, v scale)
   static constexpr int FIXED = 1024 + kCasStages * STAGE + 2 * kCasStages * 8 + kCasStages * 8;
-  static_assert(ROW % 128 == 0, "rows are whole 128-byte boxes");
+  static_assert(ROW % BOX == 0 && (BOX == 128 || (INT4 && BOX == 64)), "whole boxes");
   static_assert(STAGE % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
-  static_assert(!FP8 || D == 128, "E4M3 pools have D = 128");
+  static_assert(!QUANT || D == 128, "quantised pools have D = 128");
 };
 
 struct CascadeParams {
@@ -126,11 +129,22 @@ __device__ __forceinline__ uint32_t f16x2_of_bf16x2(uint32_t w, float up) {
   return pack_f16(bf16_lo(w) * up, bf16_hi(w) * up);
 }
 
-template <int D, bool FP8>
+// 4-bit tiles (64-byte rows, 64-byte swizzle): a lane's ldmatrix byte-pair word holds
+// eight consecutive channels 8t..8t+7 of one token; int4_pair_f16 gives the pairs
+// (i, i+4), which fill k-step 2c with (0,4), (1,5) and k-step 2c+1 with (2,6), (3,7)
+// (chunk c: channels 32c..32c+31); the query rows take the same order.  For P V the
+// transposed word holds channels 4r..4r+3 of tokens 2t and 2t+1, so int4_pair_f16(., j)
+// is the fragment of channel 4r + j: n-tile 4c + j covers channels 32c + 4r + j.
+__device__ __forceinline__ uint32_t swz64(uint32_t tile, int row, int c) {
+  return tile + row * 64 + ((c ^ ((row >> 1) & 3)) << 4);
+}
+
+template <int D, int KIND>
 __global__ void __launch_bounds__(kCasThreads, 3)
     cascade_kernel(const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const CascadeParams p) {
-  using C = CasCfg<D, FP8>;
+  using C = CasCfg<D, KIND>;
+  constexpr bool FP8 = C::FP8, INT4 = C::INT4, QUANT = C::QUANT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *stages = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -144,7 +158,7 @@ __global__ void __launch_bounds__(kCasThreads, 3)
   pdl_trigger();
   if (tid == 0) {
     for (int s = 0; s < kCasStages; ++s) {
-      mbar_init(smem_u32(&full[s]), FP8 ? 2 : 1);   // E4M3: plus the scales' cp.async
+      mbar_init(smem_u32(&full[s]), QUANT ? 2 : 1);  // codes: plus the scales' cp.async
       mbar_init(smem_u32(&empty[s]), kCasWarps);
     }
     fence_mbar_init();
@@ -220,7 +234,7 @@ __global__ void __launch_bounds__(kCasThreads, 3)
       const int y = (phys == kInvalidPhys) ? p.nblocks * p.bs : phys * p.bs + (t * kTile) % p.bs;
       const uint32_t bar = smem_u32(&full[s]);
       const uint32_t dst = smem_u32(stages + s * C::STAGE);
-      if constexpr (FP8) {                       // the tile's block scales, with the tile
+      if constexpr (QUANT) {                     // the tile's block scales, with the tile
         float *sc = scl + 2 * s;
         if (phys != kInvalidPhys) {
           cp_async_4(smem_u32(sc), p.k_scale + static_cast<size_t>(phys) * p.Hkv + kvh);
@@ -232,12 +246,12 @@ __global__ void __launch_bounds__(kCasThreads, 3)
       }
       fence_proxy_async();
       mbar_arrive_expect_tx(bar, 2 * C::KV_BYTES);
-      constexpr int kBoxElems = FP8 ? 128 : 64;  // elements of one 128-byte box
+      constexpr int kEB = QUANT ? 1 : 2;          // bytes per tensor-map element
 #pragma unroll
       for (int h = 0; h < C::BOXES; ++h) {
-        const int x = kvh * D + h * kBoxElems;
-        tma_load_2d(dst + h * (kTile * 128), &tmK, x, y, bar);
-        tma_load_2d(dst + C::KV_BYTES + h * (kTile * 128), &tmV, x, y, bar);
+        const int x = (kvh * C::ROW + h * C::BOX) / kEB;
+        tma_load_2d(dst + h * (kTile * C::BOX), &tmK, x, y, bar);
+        tma_load_2d(dst + C::KV_BYTES + h * (kTile * C::BOX), &tmV, x, y, bar);
       }
       return true;
     };
@@ -262,7 +276,7 @@ __global__ void __launch_bounds__(kCasThreads, 3)
       // rows past the members pad the last chunk; member slots are bounded by B
       if (rmember[h] >= w.members || off + rmember[h] >= p.B) rmember[h] = -1;
     }
-    float qshift[2] = {1.f, 1.f};                // E4M3: 2^-k undoing each row's scaling
+    float qshift[2] = {1.f, 1.f};                // codes: 2^-k undoing each row's scaling
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint32_t *qr = nullptr;
@@ -272,21 +286,24 @@ __global__ void __launch_bounds__(kCasThreads, 3)
           qr = reinterpret_cast<const uint32_t *>(
               p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G + rhead[h]) * D);
       }
-      if constexpr (!FP8) {
+      if constexpr (!QUANT) {
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
           qa[ks][h] = qr ? __ldg(qr + ks * 8 + tig) : 0u;         // channels 16ks + 2tig..
           qa[ks][h + 2] = qr ? __ldg(qr + ks * 8 + 4 + tig) : 0u; // 16ks + 8 + 2tig..
         }
       } else {
-        // channels 16ks + 4tig + {0,1} and + {2,3} (the permuted k order), scaled by 2^k
-        // so that the row's largest magnitude sits just below 2^15: exact in f16
+        // the permuted k order, scaled by 2^k so that the row's largest magnitude sits
+        // just below 2^15: exact in f16.  E4M3: raw[ks] = channels 16ks + 4tig + {0,1},
+        // {2,3}.  4-bit: raw[2c], raw[2c + 1] = channels 32c + 8tig + {0,1}, {2,3} and
+        // {4,5}, {6,7}.
         uint32_t raw[C::KS][2];
         float amax = 0.f;
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
-          raw[ks][0] = qr ? __ldg(qr + ks * 8 + 2 * tig) : 0u;
-          raw[ks][1] = qr ? __ldg(qr + ks * 8 + 2 * tig + 1) : 0u;
+          const int w = INT4 ? (ks >> 1) * 16 + 4 * tig + (ks & 1) * 2 : ks * 8 + 2 * tig;
+          raw[ks][0] = qr ? __ldg(qr + w) : 0u;
+          raw[ks][1] = qr ? __ldg(qr + w + 1) : 0u;
 #pragma unroll
           for (int e = 0; e < 2; ++e)
             amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(raw[ks][e])), fabsf(bf16_hi(raw[ks][e]))));
@@ -302,8 +319,17 @@ __global__ void __launch_bounds__(kCasThreads, 3)
         qshift[h] = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
-          qa[ks][h] = f16x2_of_bf16x2(raw[ks][0], up);
-          qa[ks][h + 2] = f16x2_of_bf16x2(raw[ks][1], up);
+          if constexpr (INT4) {
+            // k-step 2c: (0,4), (1,5); 2c + 1: (2,6), (3,7) of the lane's eight channels
+            const uint32_t lo4 = raw[ks & ~1][0], lo6 = raw[ks & ~1][1];   // 0,1 / 2,3
+            const uint32_t hi4 = raw[ks | 1][0], hi6 = raw[ks | 1][1];     // 4,5 / 6,7
+            const uint32_t e = (ks & 1) ? lo6 : lo4, f = (ks & 1) ? hi6 : hi4;
+            qa[ks][h] = pack_f16(bf16_lo(e) * up, bf16_lo(f) * up);
+            qa[ks][h + 2] = pack_f16(bf16_hi(e) * up, bf16_hi(f) * up);
+          } else {
+            qa[ks][h] = f16x2_of_bf16x2(raw[ks][0], up);
+            qa[ks][h + 2] = f16x2_of_bf16x2(raw[ks][1], up);
+          }
         }
       }
     }
@@ -313,7 +339,7 @@ __global__ void __launch_bounds__(kCasThreads, 3)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[dt][i] = 0.f;
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    // E4M3: the accumulator is in units of vref (the item's first nonzero V scale, or
+    // codes: the accumulator is in units of vref (the item's first nonzero V scale, or
     // a later one when the ratio leaves [kRatMin, kRatMax]); vinv = 0 before it
     float vref = 1.f, vinv = 0.f;
 
@@ -331,7 +357,7 @@ __global__ void __launch_bounds__(kCasThreads, 3)
 
       // ---- S = Q K^T for 16 rows x 16 tokens (two n-tiles of 8 tokens)
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      if constexpr (!FP8) {
+      if constexpr (!QUANT) {
         const int tok = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
@@ -340,6 +366,23 @@ __global__ void __launch_bounds__(kCasThreads, 3)
           ldsm_x4(b, kt + (c16 >> 3) * (kTile * 128) + tok * 128 + (((c16 & 7) ^ (tok & 7)) << 4));
           mma_bf16(sc[0], qa[ks], b[0], b[1]);
           mma_bf16(sc[1], qa[ks], b[2], b[3]);
+        }
+      } else if constexpr (INT4) {
+        // matrices: tokens 0-7 / 8-15 of 32-code chunks c and c + 1
+        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int c0 = 0; c0 < D / 32; c0 += 2) {
+          uint32_t b[4];
+          ldsm_x4(b, swz64(kt, tok, c0 + (lane >> 4)));
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              const uint32_t w = b[2 * u + nt];
+              const int ks = 2 * (c0 + u);
+              mma_f16(sc[nt], qa[ks], int4_pair_f16(w, 0), int4_pair_f16(w, 1));
+              mma_f16(sc[nt], qa[ks + 1], int4_pair_f16(w, 2), int4_pair_f16(w, 3));
+            }
         }
       } else {
         // matrices: tokens 0-7 / 8-15 of 16-code chunks ks and ks + 1
@@ -364,8 +407,8 @@ __global__ void __launch_bounds__(kCasThreads, 3)
       float pr[2][4];
       bool over = false;
       float ssc[2] = {p.sl2, p.sl2};             // raw mma score -> log2-domain score
-      float rat = 1.f;                           // E4M3: tile V scale / accumulator's
-      if constexpr (FP8) {
+      float rat = 1.f;                           // codes: tile V scale / accumulator's
+      if constexpr (QUANT) {
         const float2 tsc = *reinterpret_cast<const float2 *>(scl + 2 * s);   // k, v scale
         ssc[0] = p.sl2 * tsc.x * qshift[0];
         ssc[1] = p.sl2 * tsc.x * qshift[1];
@@ -416,13 +459,13 @@ __global__ void __launch_bounds__(kCasThreads, 3)
             l[h] += v;
           }
       // ---- P as the A operand (the accumulator layout is the A layout), hi + lo terms:
-      // bf16 against bf16 V; f16 times the V-scale ratio against E4M3 V
+      // bf16 against bf16 V; f16 times the V-scale ratio against code V
       uint32_t ph[4], pl[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int nt = i >> 1, h = i & 1;        // a0: row g4, tokens 0-7; a1: row g4 + 8; ...
         const float p0 = pr[nt][2 * h], p1 = pr[nt][2 * h + 1];
-        if constexpr (!FP8) {
+        if constexpr (!QUANT) {
           ph[i] = pack_bf16(p0, p1);
           pl[i] = pack_bf16(p0 - bf16_lo(ph[i]), p1 - bf16_hi(ph[i]));
         } else {
@@ -433,7 +476,23 @@ __global__ void __launch_bounds__(kCasThreads, 3)
         }
       }
       // ---- O += P V: V^T fragments by ldmatrix.trans on the token rows
-      if constexpr (FP8) {
+      if constexpr (INT4) {
+        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int c0 = 0; c0 < D / 32; c0 += 2) {
+          uint32_t b[4];
+          ldsm_x4_trans(b, swz64(vt, tok, c0 + (lane >> 4)));
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int n = 4 * (c0 + u) + j;
+              const uint32_t v0 = int4_pair_f16(b[2 * u], j), v1 = int4_pair_f16(b[2 * u + 1], j);
+              mma_f16(acc[n], ph, v0, v1);
+              mma_f16(acc[n], pl, v0, v1);
+            }
+        }
+      } else if constexpr (FP8) {
         // n-tile 2c + e: channels 16c + 2r + e (r = lane / 4) of 16-code chunk c
         const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
@@ -498,9 +557,20 @@ __global__ void __launch_bounds__(kCasThreads, 3)
       const size_t slot =
           ((static_cast<size_t>(off + rmember[h]) * p.Hkv + kvh) * kCascadePieces + piece) * p.G +
           rhead[h];
-      const float inv = (FP8 ? vref : 1.f) / lt;
+      const float inv = (QUANT ? vref : 1.f) / lt;
       float *orow = p.o + slot * D;
-      if constexpr (FP8) {   // n-tiles 2c, 2c + 1 hold channels 16c + 4tig + {0, 2} and {1, 3}
+      if constexpr (INT4) {  // n-tile 4c + j holds channels 32c + 8tig + j and + 4 + j
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float *o8 = orow + 32 * c + 8 * tig;
+          *reinterpret_cast<float4 *>(o8) =
+              make_float4(acc[4 * c][2 * h] * inv, acc[4 * c + 1][2 * h] * inv,
+                          acc[4 * c + 2][2 * h] * inv, acc[4 * c + 3][2 * h] * inv);
+          *reinterpret_cast<float4 *>(o8 + 4) =
+              make_float4(acc[4 * c][2 * h + 1] * inv, acc[4 * c + 1][2 * h + 1] * inv,
+                          acc[4 * c + 2][2 * h + 1] * inv, acc[4 * c + 3][2 * h + 1] * inv);
+        }
+      } else if constexpr (FP8) {   // n-tiles 2c, 2c + 1 hold channels 16c + 4tig + {0, 2} and {1, 3}
 #pragma unroll
         for (int c = 0; c < D / 16; ++c)
           *reinterpret_cast<float4 *>(orow + 16 * c + 4 * tig) =
@@ -561,15 +631,15 @@ static CascadeParams cascade_params(const pa_shape &s, const void *q, const int3
   return p;
 }
 
-template <int D, bool FP8>
+template <int D, int KIND>
 static cudaError_t launch_cascade(const CUtensorMap &mk, const CUtensorMap &mv,
                                   const CascadeParams &p, int grid, cudaStream_t stream) {
-  const size_t smem = CasCfg<D, FP8>::FIXED + (static_cast<size_t>(p.num_groups) + 1) * 4;
-  cudaError_t e = cudaFuncSetAttribute(cascade_kernel<D, FP8>,
+  const size_t smem = CasCfg<D, KIND>::FIXED + (static_cast<size_t>(p.num_groups) + 1) * 4;
+  cudaError_t e = cudaFuncSetAttribute(cascade_kernel<D, KIND>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  cascade_kernel<D, FP8><<<grid, kCasThreads, smem, stream>>>(mk, mv, p);
+  cascade_kernel<D, KIND><<<grid, kCasThreads, smem, stream>>>(mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -580,11 +650,13 @@ pa_status run_cascade(const pa_shape &s, const CUtensorMap &mk, const CUtensorMa
   const CascadeParams p = cascade_params(s, q, bt, k_scale, v_scale, opts, sm_scale, err);
   cudaError_t e;
   if (s.kv_dtype == PA_KV_FP8_E4M3)
-    e = launch_cascade<128, true>(mk, mv, p, ctas, stream);
+    e = launch_cascade<128, 1>(mk, mv, p, ctas, stream);
+  else if (s.kv_dtype == PA_KV_INT4)
+    e = launch_cascade<128, 2>(mk, mv, p, ctas, stream);
   else if (s.D == 128)
-    e = launch_cascade<128, false>(mk, mv, p, ctas, stream);
+    e = launch_cascade<128, 0>(mk, mv, p, ctas, stream);
   else
-    e = launch_cascade<64, false>(mk, mv, p, ctas, stream);
+    e = launch_cascade<64, 0>(mk, mv, p, ctas, stream);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

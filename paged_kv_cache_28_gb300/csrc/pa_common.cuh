@@ -245,6 +245,22 @@ __device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t codes) {
 }
 
 // two E4M3 codes (low 16 bits) -> two floats, exact
+// Four signed 4-bit codes stored as offset-binary nibbles at bits 4i.. and 4i+16..
+// of w: returns {nibble i, nibble i + 4} as f16x2.  Even i: the nibbles masked into
+// the low mantissa bits of 0x6400 (f16 1024 + u), minus 1032.  Odd i: masked in place
+// at bits 4..7 (1024 + 16u), times 1/16 minus 72.  Both are exact, and i >= 2 reads
+// w >> 8, so one shift serves four pairs.
+__device__ __forceinline__ uint32_t int4_pair_f16(uint32_t w, int i) {
+  uint32_t h;
+  const uint32_t x = i >= 2 ? w >> 8 : w;
+  const uint32_t mask = (i & 1) ? 0x00F000F0u : 0x000F000Fu;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(x), "r"(mask), "r"(0x64006400u));
+  const __half2 hv = *reinterpret_cast<const __half2 *>(&h);
+  const __half2 v = (i & 1) ? __hfma2(hv, __floats2half2_rn(0.0625f, 0.0625f), __floats2half2_rn(-72.f, -72.f))
+                            : __hsub2(hv, __floats2half2_rn(1032.f, 1032.f));
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t codes) {
   const uint32_t h = e4m3x2_to_f16x2(codes);
   return __half22float2(*reinterpret_cast<const __half2 *>(&h));

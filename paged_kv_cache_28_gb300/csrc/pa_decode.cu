@@ -170,22 +170,6 @@ __device__ __forceinline__ int acc_d(int dt, int i, int lane) {
     return dt * 16 + (lane >> 2) + (i >> 1) * 8;
 }
 
-// Four signed 4-bit codes stored as offset-binary nibbles at bits 4i.. and 4i+16..
-// of w: returns {nibble i, nibble i + 4} as f16x2.  Even i: the nibbles masked into
-// the low mantissa bits of 0x6400 (f16 1024 + u), minus 1032.  Odd i: masked in place
-// at bits 4..7 (1024 + 16u), times 1/16 minus 72.  Both are exact, and i >= 2 reads
-// w >> 8, so one shift serves four pairs.
-__device__ __forceinline__ uint32_t int4_pair_f16(uint32_t w, int i) {
-  uint32_t h;
-  const uint32_t x = i >= 2 ? w >> 8 : w;
-  const uint32_t mask = (i & 1) ? 0x00F000F0u : 0x000F000Fu;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(x), "r"(mask), "r"(0x64006400u));
-  const __half2 hv = *reinterpret_cast<const __half2 *>(&h);
-  const __half2 v = (i & 1) ? __hfma2(hv, __floats2half2_rn(0.0625f, 0.0625f), __floats2half2_rn(-72.f, -72.f))
-                            : __hsub2(hv, __floats2half2_rn(1032.f, 1032.f));
-  return *reinterpret_cast<const uint32_t *>(&v);
-}
-
 // Load the group's Q^T fragments from the stage's Q slot ([8*NT rows][D] bf16), or,
 // with C::QSMEM, from the query rows in global memory into the warp's fragment area
 // qfs (lane-private: each lane reads back only what it wrote).
@@ -1799,13 +1783,16 @@ static pa_status launch_segments(const Params &p, const CUtensorMap &mk, const C
 
 // 4-bit pools whose KV heads can be served two at a time: an even number of heads,
 // groups of 8 query heads (one n-tile each), D = 128.  A Quest selection is per KV
-// head, so a decode with one serves the heads singly.
+// head, and the cascade stacks one KV head's query rows, so a decode with either
+// serves the heads singly.
 static bool int4_pairable(const pa_shape &s) {
   return s.kv_dtype == PA_KV_INT4 && s.D == 128 && s.Hkv % 2 == 0 && s.Hq == 8 * s.Hkv;
 }
 
 static int heads_per_unit(const pa_shape &s, const pa_decode_opts *opts) {
-  return (int4_pairable(s) && !(opts && opts->topk > 0 && opts->selected_pages)) ? 2 : 1;
+  const bool per_head = opts && ((opts->topk > 0 && opts->selected_pages) ||
+                                 opts->num_prefix_groups > 0);
+  return (int4_pairable(s) && !per_head) ? 2 : 1;
 }
 
 // The decode's view of the shape: units of `heads` adjacent KV heads.

@@ -225,9 +225,6 @@ def test_cascade_host_checks(lib):
     assert call(s, opts(window=64)) == _lib.PA_ERR_INVALID_ARG          # not with a window
     assert call(s, opts(stream=FAKE)) == _lib.PA_ERR_INVALID_ARG        # side stream, no events
     assert call(s, opts(stream=FAKE, events=(FAKE, None))) == _lib.PA_ERR_INVALID_ARG
-    int4 = shape(B=8, Hq=64, Hkv=8, D=128, max_blocks=64, nblocks=512,
-                 kv_dtype=_lib.PA_KV_INT4)
-    assert call(int4, opts()) == _lib.PA_ERR_UNSUPPORTED                # bf16 and E4M3 only
 
 
 def test_quest_host_checks(lib):

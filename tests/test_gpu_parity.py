@@ -1198,7 +1198,7 @@ def test_cascade_matches_oracle(Hq, Hkv, D, bs, groups, free):
 
 
 
-FP8_CASCADE_CASES = [
+QUANT_CASCADE_CASES = [
     (64, 8, 16, [(900, [1, 5, 17, 300, 2, 64, 40, 1000]), (300, [3, 30])], [7, 500, 1]),
     (64, 8, 16, [(2000, [1, 2, 3])], [100]),                          # four pieces per member
     (32, 2, 16, [(500, [9, 90, 900]), (16, [1, 2])], [33]),           # G = 16 (two n-tiles)
@@ -1207,13 +1207,15 @@ FP8_CASCADE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("Hq,Hkv,bs,groups,free", FP8_CASCADE_CASES)
-def test_cascade_fp8_matches_oracle(Hq, Hkv, bs, groups, free):
-    """The cascade over E4M3 pools (codes restored with their block scales, this step's
-    quantised cache write applied first): equal to the oracle's plain decode at the
-    quantised tolerance, beside or after the split kernel, at several segment counts."""
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "int4"])
+@pytest.mark.parametrize("Hq,Hkv,bs,groups,free", QUANT_CASCADE_CASES)
+def test_cascade_quantised_matches_oracle(kv_dtype, Hq, Hkv, bs, groups, free):
+    """The cascade over E4M3 and 4-bit pools (codes restored with their block scales,
+    this step's quantised cache write applied first): equal to the oracle's plain decode
+    at the quantised tolerance, beside or after the split kernel, at several segment
+    counts."""
     batch, cg = _cascade_batch(Hq, Hkv, 128, bs, groups, free, seed=300 + Hq + bs,
-                               kv_dtype="fp8_e4m3")
+                               kv_dtype=kv_dtype)
     dev = DeviceBatch(batch)
     dev.reshape_and_cache()
     ref, _ = oracle_after_write(batch)
@@ -1221,16 +1223,17 @@ def test_cascade_fp8_matches_oracle(Hq, Hkv, bs, groups, free):
         dev.enable_cascade(cg, side_stream=side)
         for ns in (1, 17, 500, default_num_segments(dev.shape)):
             assert_close(_run_cascade(dev, ns), ref, batch,
-                         f"fp8 cascade side={side} segments={ns}")
+                         f"{kv_dtype} cascade side={side} segments={ns}")
     assert dev.read_err() == 0
 
 
-def test_cascade_fp8_scale_spread():
-    """E4M3 cascade with K and V block scales spread over 2^-12 .. 2^6 (the accumulator
-    is re-expressed when a tile's V-scale ratio leaves [2^-12, 2^7]; large restored V
-    values), a zero V scale on some blocks, and a staircase of scores in the prefix."""
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "int4"])
+def test_cascade_quantised_scale_spread(kv_dtype):
+    """Quantised cascade with K and V block scales spread over 2^-12 .. 2^6 (the
+    accumulator is re-expressed when a tile's V-scale ratio leaves [2^-12, 2^7]; large
+    restored V values) and a zero V scale on some blocks."""
     batch, cg = _cascade_batch(64, 8, 128, 16, [(1200, [1, 9, 300]), (320, [4, 60])], [77],
-                               seed=311, kv_dtype="fp8_e4m3")
+                               seed=311, kv_dtype=kv_dtype)
     rng = np.random.default_rng(311)
     batch.k_scale[...] = (2.0 ** rng.uniform(-12, 2, batch.k_scale.shape)).astype(np.float32)
     batch.v_scale[...] = (2.0 ** rng.uniform(-12, 6, batch.v_scale.shape)).astype(np.float32)
@@ -1239,7 +1242,7 @@ def test_cascade_fp8_scale_spread():
     ref, _ = oracle_after_write(batch, write=False)
     dev.enable_cascade(cg)
     for ns in (1, 9, default_num_segments(dev.shape)):
-        assert_close(_run_cascade(dev, ns), ref, batch, f"fp8 cascade scale spread {ns}")
+        assert_close(_run_cascade(dev, ns), ref, batch, f"{kv_dtype} cascade scale spread {ns}")
     assert dev.read_err() == 0
 
 
