@@ -1092,19 +1092,24 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
 // ceil(n / (kClusterWarpTiles * WARPS)) of the cluster's CTAs (at least one, at most
 // all); the others leave at once.
 constexpr int kClusterWarpTiles = 16;
-// Batches up to this many sequences are served longest first (the ordering costs
-// B^2 / threads key comparisons per CTA).
-constexpr int kLongestFirstMaxB = 256;
+// Batches up to this many sequences are served longest first: up to kExactRankMaxB by an
+// exact ranking (B^2 / threads key comparisons per CTA), above it by quarter-octave
+// buckets of the tile count (linear in B; one byte per sequence in the stage area).
+constexpr int kLongestFirstMaxB = 16384;
+constexpr int kExactRankMaxB = 128;
+constexpr int kRankBuckets = 256;
+// Shared scratch of longest_first: bucket counts, the count above each bucket, the
+// search's results and per-warp counts, then one bucket byte per sequence.
+constexpr int kRankScratch = (2 * kRankBuckets + 8) * 4 + kLongestFirstMaxB;
 
-// Unit slot c (a CTA, or a cluster) serves the sequence of rank c / Hkv when the
-// sequences are ordered by attended tiles, most first (ties by index), so that the
-// longest units start first and do not end the launch alone.  Each sequence gets one
+// Small batches: unit slot c serves the sequence of rank c / Hkv when the sequences
+// are ordered by attended tiles, most first (ties by index).  Each sequence gets one
 // 32-bit key, tiles above its index (larger = earlier, all distinct), and its rank
 // is the number of larger keys: every thread ranks two candidates in one pass over
 // the keys, four at a time.  keys: shared scratch of 4 * (round4(B) + 1) bytes,
 // 16-byte aligned, free again on return.
-__device__ int longest_first(const Params &p, int pair, uint32_t *keys) {
-  static_assert(kLongestFirstMaxB <= 512, "keys hold the sequence index in 9 bits");
+__device__ int longest_first_exact(const Params &p, int pair, uint32_t *keys) {
+  static_assert(kExactRankMaxB <= 512, "keys hold the sequence index in 9 bits");
   const int cap = p.max_blocks * p.bs;
   const int nb4 = (p.B + 3) >> 2;
   for (int b = threadIdx.x; b < 4 * nb4; b += blockDim.x) {
@@ -1138,17 +1143,119 @@ __device__ int longest_first(const Params &p, int pair, uint32_t *keys) {
   return seq * p.Hkv + (pair - want * p.Hkv);
 }
 
+// Unit slot c (a CTA, or a cluster) serves the sequence of rank c / Hkv when the
+// sequences are ordered by their bucket of attended tiles, fullest first, then by index:
+// the longest units start first and do not end the launch alone.  Buckets are quarter
+// octaves (n tiles: 4 floor(log2 n) + the next two bits of n, plus one), so a wave of
+// CTAs mixes lengths within about a fifth of each other: on batches of near-equal
+// lengths an exact order makes whole waves start and finish in step, with the DRAM idle
+// at each boundary.  A histogram of the buckets and a scan from the top give the bucket
+// holding the rank; a scan over runs of consecutive sequences finds its member.  The
+// cost is linear in B.  scratch: kRankScratch bytes of shared memory, 16-byte
+// aligned, free again on return.
+__device__ __forceinline__ int tile_bucket(int n) {
+  if (n <= 0) return 0;
+  const int e = 31 - __clz(n);                                 // n in [2^e, 2^(e+1))
+  const int frac = e >= 2 ? (n >> (e - 2)) & 3 : (n << (2 - e)) & 3;
+  return 4 * e + frac + 1;                                     // <= 4 * 30 + 3 + 1
+}
+
+__device__ int longest_first_bucketed(const Params &p, int pair, uint8_t *scratch) {
+  constexpr int NB = kRankBuckets;
+  static_assert(NB == 2 * 128, "two buckets per thread of a 128-thread CTA");
+  int *hist = reinterpret_cast<int *>(scratch);
+  int *above = hist + NB;                        // sequences in higher buckets
+  int *sel = above + NB;                         // bucket, rank within it, the sequence
+  int *wcnt = sel + 4;                           // per-warp counts
+  uint8_t *bucket = reinterpret_cast<uint8_t *>(wcnt + 4);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cap = p.max_blocks * p.bs;
+  static_assert(4 * 30 + 3 + 1 < NB, "every tile count has a bucket");
+  for (int k = tid; k < NB; k += blockDim.x) hist[k] = 0;
+  __syncthreads();
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    const int c = pair_tile_count(min(max(__ldg(p.seq_lens + b), 0), cap), p.window, p.topk);
+    const int k = tile_bucket(c);
+    bucket[b] = static_cast<uint8_t>(k);
+    atomicAdd(&hist[k], 1);
+  }
+  __syncthreads();
+  // above[k] = sum of hist[k'] over k' > k: thread t holds buckets NB-1-2t and NB-2-2t
+  {
+    const int k0 = NB - 1 - 2 * tid, k1 = k0 - 1;
+    const int v = hist[k0] + hist[k1];
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
+    }
+    if (lane == 31) wcnt[warp] = inc;
+    __syncthreads();
+    int ex = inc - v;
+    for (int w = 0; w < warp; ++w) ex += wcnt[w];
+    above[k0] = ex;
+    above[k1] = ex + hist[k0];
+  }
+  __syncthreads();
+  const int want = pair / p.Hkv;                 // < B: exactly one bucket holds it
+  for (int k = tid; k < NB; k += blockDim.x)
+    if (above[k] <= want && want < above[k] + hist[k]) {
+      sel[0] = k;
+      sel[1] = want - above[k];
+    }
+  __syncthreads();
+  // the j-th member of bucket kb in index order: each thread counts the members in its
+  // own run of consecutive sequences, a scan over the threads finds the run holding it
+  {
+    const int kb = sel[0], j = sel[1];
+    const int per = (p.B + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+    const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
+    int mine = 0;
+    for (int b = lo; b < hi; ++b) mine += bucket[b] == kb;
+    int inc = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
+    }
+    if (lane == 31) wcnt[warp] = inc;
+    __syncthreads();
+    int ex = inc - mine;
+    for (int w = 0; w < warp; ++w) ex += wcnt[w];
+    if (j >= ex && j < ex + mine) {
+      int r = j - ex;
+      for (int b = lo; b < hi; ++b)
+        if (bucket[b] == kb && r-- == 0) {
+          sel[2] = b;
+          break;
+        }
+    }
+    __syncthreads();
+  }
+  const int seq = sel[2];
+  __syncthreads();   // every thread has read it before the stages are filled
+  return seq * p.Hkv + (pair - want * p.Hkv);
+}
+
+__device__ __forceinline__ int longest_first(const Params &p, int pair, uint8_t *scratch) {
+  return p.B <= kExactRankMaxB ? longest_first_exact(p, pair, reinterpret_cast<uint32_t *>(scratch))
+                               : longest_first_bucketed(p, pair, scratch);
+}
+
 // CLUSTER: launched in clusters, one per unit (else one CTA per unit).
 template <class C, bool CLUSTER>
 __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const Params p) {
+  static_assert(kRankScratch <= C::WARPS * C::STAGES * C::STAGE_BYTES && C::THREADS == 128,
+                "the ordering's scratch lives in the stage area");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const int ncl = CLUSTER ? cluster_ctas() : 1, crank = CLUSTER ? cluster_rank() : 0;
   int pair = blockIdx.x / ncl;
-  if (p.B <= kLongestFirstMaxB) pair = longest_first(p, pair, reinterpret_cast<uint32_t *>(base));
+  if (p.B <= kLongestFirstMaxB) pair = longest_first(p, pair, base);
   const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int L = p.seq_lens[b];
