@@ -42,14 +42,14 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_771_456 + 2_599_168, "kernel_hash": "4b28388e69e8d4fa"},
-    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_563_392 + 1_250_304, "kernel_hash": "4b28388e69e8d4fa"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_057_536 + 2_975_488, "kernel_hash": "4b28388e69e8d4fa"},
-    ("prefix_sharing", "decode_pair_kernel"): {"bytes": 2_541_372_160 + 180_736, "kernel_hash": "4b28388e69e8d4fa"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_274_944 + 2_595_840, "kernel_hash": "4b28388e69e8d4fa"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_230_912 + 15_663_616, "kernel_hash": "4b28388e69e8d4fa"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_885_440 + 20_257_792, "kernel_hash": "4b28388e69e8d4fa"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_996_096 + 16_524_032, "kernel_hash": "4b28388e69e8d4fa"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_658_048 + 2_637_312, "kernel_hash": "adfbb6f5e47b3a4e"},
+    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_594_624 + 1_302_016, "kernel_hash": "adfbb6f5e47b3a4e"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_891_136 + 2_928_640, "kernel_hash": "adfbb6f5e47b3a4e"},
+    ("prefix_sharing", "decode_pair_kernel"): {"bytes": 2_541_424_384 + 120_832, "kernel_hash": "adfbb6f5e47b3a4e"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_368_384 + 2_218_240, "kernel_hash": "adfbb6f5e47b3a4e"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_168_704 + 12_585_728, "kernel_hash": "adfbb6f5e47b3a4e"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_897_984 + 20_838_656, "kernel_hash": "adfbb6f5e47b3a4e"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_125_199_616 + 16_246_272, "kernel_hash": "adfbb6f5e47b3a4e"},
 }
 
 

@@ -1008,16 +1008,20 @@ def _cascade_batch(Hq, Hkv, D, bs, groups, free_lens, seed, plens=None, kv_dtype
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,lens_kind", [(64, 8, 128, "mixed"), (48, 8, 128, "mixed"),
-                                                 (64, 8, 64, "mixed"), (64, 64, 128, "short")])
+                                                 (64, 8, 64, "mixed"), (64, 64, 128, "short"),
+                                                 (32, 4, 128, "wide")])
 def test_pa_decode_many_units(Hq, Hkv, D, lens_kind):
-    """pa_decode without a workspace on bf16 batches of at most 256 sequences with more
-    (sequence, KV head) units than CTAs at once (one CTA per unit, longest sequences
-    first): lengths from 0 up with a few long ones; G = 8 and 6 (a padded group); D = 128
-    and 64; and 12,800 short units.  Against the oracle, with a window and with Quest
-    pages too, and repeatable bit for bit."""
+    """pa_decode without a workspace on bf16 batches with more (sequence, KV head) units
+    than CTAs at once (one CTA per unit, longest sequences first): lengths from 0 up with
+    a few long ones; G = 8 and 6 (a padded group); D = 128 and 64; 12,800 short units (200
+    sequences); 300 sequences over five orders of magnitude (the bucketed order, several
+    sequences per thread in its search).  Against the oracle, with a window and with
+    Quest pages too, and repeatable bit for bit."""
     rng = np.random.default_rng(500 + Hq + Hkv + D)
     if lens_kind == "mixed":
         lens = list(rng.integers(0, 600, 110)) + [0, 1, 15, 16, 17] + [4000, 2500]
+    elif lens_kind == "wide":
+        lens = list((10 ** rng.uniform(0, 3.8, 296)).astype(int)) + [0, 0, 1, 16]
     else:
         lens = list(rng.integers(1, 40, 200))          # 12,800 units
     batch = wl.build_batch("t", lens, Hq=Hq, Hkv=Hkv, D=D, block_size=16, seed=510 + D)
@@ -1029,7 +1033,7 @@ def test_pa_decode_many_units(Hq, Hkv, D, lens_kind):
         assert_close(out, ref, batch, f"many units window={window}")
         assert np.array_equal(_bits(run_gpu(dev, "decode", window=window)), _bits(out))
     assert dev.read_err() == 0
-    if D == 128 and lens_kind == "mixed":
+    if D == 128 and lens_kind in ("mixed", "wide"):
         dev.quest_build_summaries()
         sel = dev.quest_select(5)
         torch.cuda.synchronize()
