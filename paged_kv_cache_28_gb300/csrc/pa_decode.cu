@@ -1896,9 +1896,9 @@ static bool int4_pairable(const pa_shape &s) {
   return s.kv_dtype == PA_KV_INT4 && s.D == 128 && s.Hkv % 2 == 0 && s.Hq == 8 * s.Hkv;
 }
 
-static int heads_per_unit(const pa_shape &s, const pa_decode_opts *opts) {
-  const bool per_head = opts && ((opts->topk > 0 && opts->selected_pages) ||
-                                 opts->num_prefix_groups > 0);
+// cascade: the decode runs the cascade (only pa_decode given a workspace does).
+static int heads_per_unit(const pa_shape &s, const pa_decode_opts *opts, bool cascade = false) {
+  const bool per_head = (opts && opts->topk > 0 && opts->selected_pages) || cascade;
   return (int4_pairable(s) && !per_head) ? 2 : 1;
 }
 
@@ -2004,7 +2004,7 @@ pa_status run_decode_splitkv(const pa_shape &s, float *out, void *workspace, int
                              int32_t *err, cudaStream_t stream) {
   const WorkspaceLayout w = splitkv_layout(s, num_splits);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  const int heads = heads_per_unit(s, opts);
+  const int heads = heads_per_unit(s, opts, opts && opts->num_prefix_groups > 0);
   const pa_shape v = unit_view(s, heads);
   CUtensorMap mk, mv;
   if (!make_pool_map(&mk, k_pool, v, heads) || !make_pool_map(&mv, v_pool, v, heads))

@@ -1250,11 +1250,13 @@ def test_cascade_quantised_scale_spread(kv_dtype):
     assert dev.read_err() == 0
 
 
-def test_cascade_through_pa_decode():
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int4"])
+def test_cascade_through_pa_decode(kv_dtype):
     """pa_decode with a workspace runs the split decode with the cascade and the merge in
-    one call; without a workspace it ignores the groups and attends over every token."""
+    one call; without a workspace it ignores the groups and attends over every token (on
+    4-bit pools: heads read in pairs without the cascade, one at a time with it)."""
     batch, cg = _cascade_batch(64, 8, 128, 16, [(900, [1, 5, 17, 300]), (300, [3, 30])],
-                               [7, 500], seed=152)
+                               [7, 500], seed=152, kv_dtype=kv_dtype)
     dev = DeviceBatch(batch)
     dev.enable_cascade(cg)
     ref, _ = oracle_after_write(batch, write=False)
@@ -1262,14 +1264,16 @@ def test_cascade_through_pa_decode():
         dev.ensure_workspace(ns or default_num_segments(dev.shape))
         for ws in (dev.workspace, None):
             dev.out.fill_(float("nan"))
-            _lib.pa_decode(dev.shape, dev.out, dev.q, dev.k_pool, dev.v_pool, None, None,
-                           dev.block_tables, dev.seq_lens, batch.sm_scale, dev.err, None,
+            _lib.pa_decode(dev.shape, dev.out, dev.q, dev.k_pool, dev.v_pool, dev.k_scale,
+                           dev.v_scale, dev.block_tables, dev.seq_lens, batch.sm_scale, dev.err,
+                           None,
                            workspace=ws, num_segments=ns, shared_prefix_lens=dev.shared_prefix_lens,
                            cascade=dev.cascade)
             torch.cuda.synchronize()
             assert_close(dev.out.cpu().numpy(), ref, batch,
-                         f"pa_decode cascade workspace={ws is not None} segments={ns}")
+                         f"{kv_dtype} pa_decode cascade workspace={ws is not None} segments={ns}")
     assert dev.read_err() == 0
+
 
 def test_cascade_prefix_is_whole_sequence():
     """Members whose every token is in the shared prefix (nothing left for the split
@@ -1306,7 +1310,8 @@ def test_cascade_bad_groups_set_error_flag():
 
 def test_largest_split_batch_and_split_count():
     """16,384 sequences (the split kernel's largest batch: its length scan sits in shared
-    memory) of 1..48 tokens, then 65,536 splits (the largest count) on a small batch."""
+    memory; also pa_decode's largest longest-first batch, 128 sequences per thread in its
+    search) of 1..48 tokens, then 65,536 splits (the largest count) on a small batch."""
     rng = np.random.default_rng(120)
     lens = rng.integers(1, 49, 16384)
     batch = wl.build_batch("t", lens, Hq=16, Hkv=2, D=64, block_size=16, seed=120)
@@ -1318,6 +1323,9 @@ def test_largest_split_batch_and_split_count():
     rows = np.concatenate([rows, [[0, 0], [batch.B - 1, batch.Hq - 1]]]).astype(np.int32)
     ref, _ = oracle_after_write(batch, rows=rows)
     assert_close(out[rows[:, 0], rows[:, 1]], ref, batch, "B = 16384")
+    out = run_gpu(dev, "decode")
+    assert dev.read_err() == 0
+    assert_close(out[rows[:, 0], rows[:, 1]], ref, batch, "B = 16384, pa_decode")
     small = wl.build_batch("t", [1, 700, 33], Hq=64, Hkv=8, D=128, block_size=16, seed=121)
     dev = DeviceBatch(small)
     dev.reshape_and_cache()
