@@ -42,14 +42,14 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_658_048 + 2_637_312, "kernel_hash": "adfbb6f5e47b3a4e"},
-    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_594_624 + 1_302_016, "kernel_hash": "adfbb6f5e47b3a4e"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_891_136 + 2_928_640, "kernel_hash": "adfbb6f5e47b3a4e"},
-    ("prefix_sharing", "decode_pair_kernel"): {"bytes": 2_541_424_384 + 120_832, "kernel_hash": "adfbb6f5e47b3a4e"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_368_384 + 2_218_240, "kernel_hash": "adfbb6f5e47b3a4e"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_168_704 + 12_585_728, "kernel_hash": "adfbb6f5e47b3a4e"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_261_897_984 + 20_838_656, "kernel_hash": "adfbb6f5e47b3a4e"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_125_199_616 + 16_246_272, "kernel_hash": "adfbb6f5e47b3a4e"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_667_264 + 2_657_024, "kernel_hash": "8840ba5514389ad5"},
+    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_565_440 + 1_198_080, "kernel_hash": "8840ba5514389ad5"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_876_288 + 2_954_752, "kernel_hash": "8840ba5514389ad5"},
+    ("prefix_sharing", "decode_pair_kernel"): {"bytes": 2_541_487_616 + 93_696, "kernel_hash": "8840ba5514389ad5"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_533_760 + 2_196_480, "kernel_hash": "8840ba5514389ad5"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_210_432 + 12_521_472, "kernel_hash": "8840ba5514389ad5"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_262_064_896 + 19_605_760, "kernel_hash": "8840ba5514389ad5"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_983_040 + 16_243_456, "kernel_hash": "8840ba5514389ad5"},
 }
 
 
