@@ -174,7 +174,7 @@ typedef struct {
  *     cluster of four CTAs per unit that share its tiles (at least 16 per warp;
  *     a short unit leaves the extra CTAs idle) and merge through distributed
  *     shared memory; a window or topk that bounds every unit keeps one CTA per
- *     unit when the units fill the GPU or fit one CTA.  Batches of up to 256
+ *     unit when the units fill the GPU or fit one CTA.  Batches of up to 16384
  *     sequences start their longest sequences first.  A batch whose longest
  *     sequence outweighs the rest is still held back by it; the split decode is
  *     not.
@@ -315,10 +315,10 @@ int32_t pa_default_num_splits(const pa_shape *shape, int32_t sm_count);
  * + 1 segments).  Piece i of a unit is its part in the i-th segment that holds
  * it; slots after its last piece, and all slots of a sequence with seq_len 0,
  * get lse = -inf.  With S = 1 a segment's bounds move up to the next unit start,
- * so every unit is one piece.  4-bit pools with an even number of KV heads and 8
- * query heads per KV head are read two adjacent KV heads at a time (a unit is then
- * (b, KV heads 2u, 2u + 1)) unless opts selects Quest pages; the result does not
- * depend on it.  opts (may be NULL): window, topk + selected_pages and
+ * so every unit is one piece.  4-bit and FP8-E4M3 pools with an even number of KV
+ * heads and 8 query heads per KV head are read two adjacent KV heads at a time (a unit
+ * is then (b, KV heads 2u, 2u + 1)) unless opts selects Quest pages; the result does
+ * not depend on it.  opts (may be NULL): window, topk + selected_pages and
  * shared_prefix_lens as for pa_decode, the cut then running over the attended tiles
  * only; the workspace fields are ignored, and a cascade (num_prefix_groups > 0)
  * returns PA_ERR_UNSUPPORTED (its shared-prefix partials are merged by pa_decode's

@@ -82,11 +82,13 @@ constexpr int kMaxSplits = 65536;
 // Split workers resident at once: CTAs per SM by shared memory (227 KB usable per SM,
 // 1 KB reserved per CTA), capped by what the kernel's register budget was compiled
 // for, times warps per CTA.
-int resident_segments(const pa_shape *shape, int sm_count) {
-  const int per_cta = pa::splitkv_smem_bytes(*shape) + 1024;
+// Split workers resident at once for the split kernel a decode with these options
+// (NULL: none) launches: a Quest selection or a cascade reads quantised heads singly.
+int resident_segments(const pa_shape *shape, int sm_count, const pa_decode_opts *opts = nullptr) {
+  const int per_cta = pa::splitkv_smem_bytes(*shape, opts) + 1024;
   const int warps = pa::decode_warps_per_cta();
   int ctas = (227 * 1024) / per_cta;
-  if (ctas > pa::splitkv_min_blocks(*shape)) ctas = pa::splitkv_min_blocks(*shape);
+  if (ctas > pa::splitkv_min_blocks(*shape, opts)) ctas = pa::splitkv_min_blocks(*shape, opts);
   if (ctas < 1) ctas = 1;
   const int64_t n = static_cast<int64_t>(sm_count) * ctas * warps;
   return static_cast<int>(n > kMaxSplits ? kMaxSplits : n);
@@ -134,7 +136,7 @@ pa_status pa_decode(const pa_shape *shape, float *out, const void *q, const void
     if (ns <= 0) {
       int sms = 0;
       if (current_sm_count(&sms) != PA_OK) return PA_ERR_CUDA;
-      ns = resident_segments(shape, sms);
+      ns = resident_segments(shape, sms);   // pa_default_num_segments: the caller sized for it
     }
     if (ns > kMaxSplits) return PA_ERR_INVALID_ARG;
     if (shape->B > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
@@ -202,7 +204,7 @@ pa_status pa_decode_splitkv(const pa_shape *shape, float *o_part, float *lse, in
   if (shape->B > pa::kMaxSplitBatch) return PA_ERR_UNSUPPORTED;
   int sms = 0;
   if (current_sm_count(&sms) != PA_OK) return PA_ERR_CUDA;
-  return pa::run_decode_parts(*shape, o_part, lse, num_splits, resident_segments(shape, sms), q,
+  return pa::run_decode_parts(*shape, o_part, lse, num_splits, resident_segments(shape, sms, opts), q,
                               k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, opts,
                               sm_scale, err_flag, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -50,15 +50,22 @@ constexpr int kKindInt4 = 2;  // 4-bit codes, two per byte (offset binary)
 // byte is used (a lone 64-byte row costs a 128-byte DRAM fetch); n-tile h serves
 // the group of KV head 2 u + h.
 constexpr int kKindInt4x2 = 3;
+// E4M3 units of two adjacent KV heads, in the split decode: a token row holds both heads'
+// 128-byte rows (two TMA boxes); n-tile h serves the group of KV head 2 u + h.  Per byte
+// of codes, the tile bookkeeping (records, barrier waits, copy issue) is shared by two
+// heads and each warp keeps twice the bytes in flight.  pa_decode without a workspace
+// keeps one E4M3 head per unit: there the paired form's three CTAs per SM (against
+// four) measured slower.
+constexpr int kKindFp8x2 = 4;
 
 template <int D_, int NT_, int KIND_>
 struct Cfg {
   static constexpr int D = D_;
   static constexpr int NT = NT_;            // 8-head n-tiles (G <= 8 * NT)
   static constexpr int KIND = KIND_;
-  static constexpr bool FP8 = KIND == kKindFp8;
+  static constexpr bool FP8 = KIND == kKindFp8 || KIND == kKindFp8x2;
   static constexpr bool INT4 = KIND == kKindInt4 || KIND == kKindInt4x2;
-  static constexpr bool PAIRED = KIND == kKindInt4x2;
+  static constexpr bool PAIRED = KIND == kKindInt4x2 || KIND == kKindFp8x2;
   static constexpr int HEADS = PAIRED ? 2 : 1;      // KV heads per unit
   static constexpr bool QUANT = KIND != kKindBf16;   // codes x per-(block, head) scale
   static constexpr int KS = D / 16;         // QK k-steps of 16 elements
@@ -92,7 +99,7 @@ struct Cfg {
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(!PAIRED || (NT == 2 && D == 128), "paired heads: one n-tile per KV head");
   static_assert(KV_BYTES % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
-  static_assert(!QSMEM || PAIRED, "query rows from global memory: paired 4-bit units only");
+  static_assert(!QSMEM || PAIRED, "query rows from global memory: paired units only");
   // pa_decode's CTA merges its warps' accumulators in the stage area; their m and l go
   // after every per-warp area (mbarrier memory is never reused)
   static_assert(WARPS * 8 * NT * D * 4 <= WARPS * STAGES * STAGE_BYTES, "pair merge must fit");
@@ -249,8 +256,21 @@ __device__ __forceinline__ void load_q(State<C> &st, uint32_t qslot, const uint1
           }
         } else {
           const uint2 v = raw[nt][ks];
-          st.qf[nt][ks][0] = pack_f16(bf16_lo(v.x) * up, bf16_hi(v.x) * up);
-          st.qf[nt][ks][1] = pack_f16(bf16_lo(v.y) * up, bf16_hi(v.y) * up);
+          const uint32_t f0 = pack_f16(bf16_lo(v.x) * up, bf16_hi(v.x) * up);
+          const uint32_t f1 = pack_f16(bf16_lo(v.y) * up, bf16_hi(v.y) * up);
+          if constexpr (C::QSMEM) {   // k-steps 2j and 2j + 1 share one 16-byte entry
+            uint4 &q4 = qfs[(nt * (C::KS / 2) + (ks >> 1)) * 32 + lane];
+            if (ks & 1) {
+              q4.z = f0;
+              q4.w = f1;
+            } else {
+              q4.x = f0;
+              q4.y = f1;
+            }
+          } else {
+            st.qf[nt][ks][0] = f0;
+            st.qf[nt][ks][1] = f1;
+          }
         }
       }
   }
@@ -372,22 +392,31 @@ __device__ __forceinline__ void process_tile(State<C> &st, const uint4 *qfs, uin
   } else {
     // ldmatrix on byte pairs: lane (r, q) receives codes 4q..4q+3 of a 16-code chunk;
     // the mma's k order is permuted accordingly (load_q applies the same order to q).
+    // Paired heads: head h is box h of the tile and feeds n-tile h only.
     const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-    for (int kk = 0; kk < C::D / 32; ++kk) {
-      const int c = 2 * kk + (lane >> 4);
-      uint32_t R[4];
-      ldsm_x4(R, ktile + row * 128 + ((c ^ (row & 7)) << 4));
-      const uint32_t a0[4] = {e4m3x2_to_f16x2(R[0]), e4m3x2_to_f16x2(R[1]),
-                              e4m3x2_hi_to_f16x2(R[0]), e4m3x2_hi_to_f16x2(R[1])};
-      const uint32_t a1[4] = {e4m3x2_to_f16x2(R[2]), e4m3x2_to_f16x2(R[3]),
-                              e4m3x2_hi_to_f16x2(R[2]), e4m3x2_hi_to_f16x2(R[3])};
+    for (int h = 0; h < C::HEADS; ++h)
 #pragma unroll
-      for (int nt = 0; nt < C::NT; ++nt) {
-        mma_f16(s[nt], a0, st.qf[nt][2 * kk][0], st.qf[nt][2 * kk][1]);
-        mma_f16(s[nt], a1, st.qf[nt][2 * kk + 1][0], st.qf[nt][2 * kk + 1][1]);
+      for (int kk = 0; kk < C::D / 32; ++kk) {
+        const int c = 2 * kk + (lane >> 4);
+        uint32_t R[4];
+        ldsm_x4(R, ktile + h * (kTile * 128) + row * 128 + ((c ^ (row & 7)) << 4));
+        const uint32_t a0[4] = {e4m3x2_to_f16x2(R[0]), e4m3x2_to_f16x2(R[1]),
+                                e4m3x2_hi_to_f16x2(R[0]), e4m3x2_hi_to_f16x2(R[1])};
+        const uint32_t a1[4] = {e4m3x2_to_f16x2(R[2]), e4m3x2_to_f16x2(R[3]),
+                                e4m3x2_hi_to_f16x2(R[2]), e4m3x2_hi_to_f16x2(R[3])};
+        if constexpr (C::PAIRED) {
+          const uint4 q4 = qfs[(h * (C::KS / 2) + kk) * 32 + lane];
+          mma_f16(s[h], a0, q4.x, q4.y);
+          mma_f16(s[h], a1, q4.z, q4.w);
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < C::NT; ++nt) {
+            mma_f16(s[nt], a0, st.qf[nt][2 * kk][0], st.qf[nt][2 * kk][1]);
+            mma_f16(s[nt], a1, st.qf[nt][2 * kk + 1][0], st.qf[nt][2 * kk + 1][1]);
+          }
+        }
       }
-    }
   }
 
   // ---- V scale of a quantised tile relative to the accumulator's unit (warp-uniform).
@@ -584,47 +613,62 @@ __device__ __forceinline__ void process_tile(State<C> &st, const uint4 *qfs, uin
     // ldmatrix.trans on byte pairs gives lane (r, q): bytes (t=2q: d=2r, 2r+1) and
     // (t=2q+1: d=2r, 2r+1); regrouping by d yields V^T rows d = 2r (even) and 2r+1
     // (odd) -- the tile's 16 output rows in the order (2r, 2r+1).
+    // Paired heads: head h is box h of the tile and feeds n-tile h only.
     auto pv = [&](auto masked) {
       constexpr bool MASK = decltype(masked)::value;
-      uint32_t m01 = 0xFFFFFFFFu, m23 = 0xFFFFFFFFu;
-      if constexpr (MASK) {
-        if (vzero[0]) {
-          m01 = m23 = 0u;
-        } else {
-          auto in = [&](int t) { return t >= lo && t < nvalid; };
-          m01 = (in(2 * qd) ? 0x0000FFFFu : 0u) | (in(2 * qd + 1) ? 0xFFFF0000u : 0u);
-          m23 = (in(2 * qd + 8) ? 0x0000FFFFu : 0u) | (in(2 * qd + 9) ? 0xFFFF0000u : 0u);
+      uint32_t m01[C::HEADS], m23[C::HEADS];
+#pragma unroll
+      for (int h = 0; h < C::HEADS; ++h) {
+        m01[h] = m23[h] = 0xFFFFFFFFu;
+        if constexpr (MASK) {
+          if (vzero[h]) {
+            m01[h] = m23[h] = 0u;
+          } else {
+            auto in = [&](int t) { return t >= lo && t < nvalid; };
+            m01[h] = (in(2 * qd) ? 0x0000FFFFu : 0u) | (in(2 * qd + 1) ? 0xFFFF0000u : 0u);
+            m23[h] = (in(2 * qd + 8) ? 0x0000FFFFu : 0u) | (in(2 * qd + 9) ? 0xFFFF0000u : 0u);
+          }
         }
       }
       const int t = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-      for (int cc = 0; cc < C::D / 32; ++cc) {
-        const int c = 2 * cc + (lane >> 4);
-        uint32_t R[4];
-        ldsm_x4_trans(R, vtile + t * 128 + ((c ^ (t & 7)) << 4));
+      for (int h = 0; h < C::HEADS; ++h)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          // one permute per register: (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0,
-          // t0 d1, t1 d1); its low half is row 2r, its high half row 2r + 1
-          const uint32_t lo8 = __byte_perm(R[2 * hh], 0, 0x3120);
-          const uint32_t hi8 = __byte_perm(R[2 * hh + 1], 0, 0x3120);
-          uint32_t a[4] = {e4m3x2_to_f16x2(lo8), e4m3x2_hi_to_f16x2(lo8),
-                           e4m3x2_to_f16x2(hi8), e4m3x2_hi_to_f16x2(hi8)};
-          if constexpr (MASK) {
-            a[0] &= m01;
-            a[1] &= m01;
-            a[2] &= m23;
-            a[3] &= m23;
+        for (int cc = 0; cc < C::D / 32; ++cc) {
+          const int c = 2 * cc + (lane >> 4);
+          uint32_t R[4];
+          ldsm_x4_trans(R, vtile + h * (kTile * 128) + t * 128 + ((c ^ (t & 7)) << 4));
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            // one permute per register: (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0,
+            // t0 d1, t1 d1); its low half is row 2r, its high half row 2r + 1
+            const uint32_t lo8 = __byte_perm(R[2 * hh], 0, 0x3120);
+            const uint32_t hi8 = __byte_perm(R[2 * hh + 1], 0, 0x3120);
+            uint32_t a[4] = {e4m3x2_to_f16x2(lo8), e4m3x2_hi_to_f16x2(lo8),
+                             e4m3x2_to_f16x2(hi8), e4m3x2_hi_to_f16x2(hi8)};
+            if constexpr (MASK) {
+              a[0] &= m01[h];
+              a[1] &= m01[h];
+              a[2] &= m23[h];
+              a[3] &= m23[h];
+            }
+            if constexpr (C::PAIRED) {
+              mma_f16(st.acc[h][2 * cc + hh], a, bh[h][0], bh[h][1]);
+            } else {
+#pragma unroll
+              for (int nt = 0; nt < C::NT; ++nt)
+                mma_f16(st.acc[nt][2 * cc + hh], a, bh[nt][0], bh[nt][1]);
+            }
           }
-#pragma unroll
-          for (int nt = 0; nt < C::NT; ++nt) mma_f16(st.acc[nt][2 * cc + hh], a, bh[nt][0], bh[nt][1]);
         }
-      }
     };
-    if (ragged || vzero[0]) pv(std::true_type{}); else pv(std::false_type{});
+    bool zmask = false;
+#pragma unroll
+    for (int h = 0; h < C::HEADS; ++h) zmask |= vzero[h];
+    if (ragged || zmask) pv(std::true_type{}); else pv(std::false_type{});
     if constexpr (LO) {
       take_lo();
-      if (ragged || vzero[0]) pv(std::true_type{}); else pv(std::false_type{});
+      if (ragged || zmask) pv(std::true_type{}); else pv(std::false_type{});
     }
   }
 }
@@ -1255,7 +1299,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
                                               ~static_cast<uintptr_t>(1023));
   const int ncl = CLUSTER ? cluster_ctas() : 1, crank = CLUSTER ? cluster_rank() : 0;
   int pair = blockIdx.x / ncl;
-  if (p.B <= kLongestFirstMaxB) pair = longest_first(p, pair, base);
+  // a window or a Quest selection bounds every unit's tiles: near-uniform units gain
+  // nothing from an order that costs more than the exact ranking of a small batch
+  const bool bounded = p.window > 0 || p.topk > 0;
+  if (p.B <= (bounded ? kExactRankMaxB : kLongestFirstMaxB))
+    pair = longest_first(p, pair, base);
   const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int L = p.seq_lens[b];
@@ -1838,8 +1886,8 @@ static int pair_cluster_ctas(int units, int resident_ctas, int window, int topk)
 }
 
 template <class C>
-static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
-                             cudaStream_t stream) {
+static pa_status launch_pair_units(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
+                                   cudaStream_t stream) {
   const int units = p.B * p.Hkv;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1872,6 +1920,17 @@ static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUten
   return one_cta_per_unit();
 }
 
+// pa_decode without a workspace reads E4M3 heads singly (heads_per_unit), so the paired
+// E4M3 kind has no instantiation of its kernel.
+template <class C>
+static pa_status launch_pair(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
+                             cudaStream_t stream) {
+  if constexpr (C::KIND == kKindFp8x2)
+    return PA_ERR_UNSUPPORTED;
+  else
+    return launch_pair_units<C>(p, mk, mv, stream);
+}
+
 template <class C>
 static pa_status launch_segments(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
                                  cudaStream_t stream) {
@@ -1895,11 +1954,19 @@ static pa_status launch_segments(const Params &p, const CUtensorMap &mk, const C
 static bool int4_pairable(const pa_shape &s) {
   return s.kv_dtype == PA_KV_INT4 && s.D == 128 && s.Hkv % 2 == 0 && s.Hq == 8 * s.Hkv;
 }
+// E4M3 pools on the same rule.
+static bool fp8_pairable(const pa_shape &s) {
+  return s.kv_dtype == PA_KV_FP8_E4M3 && s.D == 128 && s.Hkv % 2 == 0 && s.Hq == 8 * s.Hkv;
+}
+static bool pairable(const pa_shape &s) { return int4_pairable(s) || fp8_pairable(s); }
 
-// cascade: the decode runs the cascade (only pa_decode given a workspace does).
-static int heads_per_unit(const pa_shape &s, const pa_decode_opts *opts, bool cascade = false) {
+// cascade: the decode runs the cascade (only pa_decode given a workspace does);
+// cta_per_unit: pa_decode without a workspace (it pairs 4-bit heads, not E4M3 ones).
+static int heads_per_unit(const pa_shape &s, const pa_decode_opts *opts, bool cascade = false,
+                          bool cta_per_unit = false) {
   const bool per_head = (opts && opts->topk > 0 && opts->selected_pages) || cascade;
-  return (int4_pairable(s) && !per_head) ? 2 : 1;
+  const bool pair = int4_pairable(s) || (fp8_pairable(s) && !cta_per_unit);
+  return (pair && !per_head) ? 2 : 1;
 }
 
 // The decode's view of the shape: units of `heads` adjacent KV heads.
@@ -1911,7 +1978,8 @@ static pa_shape unit_view(const pa_shape &s, int heads) {
 
 static int kind_of(const pa_shape &s, int heads) {
   if (s.kv_dtype == PA_KV_INT4) return heads == 2 ? kKindInt4x2 : kKindInt4;
-  return s.kv_dtype == PA_KV_FP8_E4M3 ? kKindFp8 : kKindBf16;
+  if (s.kv_dtype == PA_KV_FP8_E4M3) return heads == 2 ? kKindFp8x2 : kKindFp8;
+  return kKindBf16;
 }
 
 #define PA_DISPATCH_ALL(FN, ...)                      \
@@ -1923,7 +1991,8 @@ static int kind_of(const pa_shape &s, int heads) {
   PA_DISPATCH(128, 2, kKindFp8, FN, __VA_ARGS__)      \
   PA_DISPATCH(128, 1, kKindInt4, FN, __VA_ARGS__)     \
   PA_DISPATCH(128, 2, kKindInt4, FN, __VA_ARGS__)     \
-  PA_DISPATCH(128, 2, kKindInt4x2, FN, __VA_ARGS__)
+  PA_DISPATCH(128, 2, kKindInt4x2, FN, __VA_ARGS__)   \
+  PA_DISPATCH(128, 2, kKindFp8x2, FN, __VA_ARGS__)
 
 // s: the unit view; p.G query heads per unit
 static pa_status dispatch_pair(const pa_shape &s, int heads, const Params &p,
@@ -1948,9 +2017,9 @@ static int cfg_split_smem(int B) { return split_smem<C>(B); }
 template <class C>
 static int cfg_min_blocks(int) { return C::MIN_BLOCKS; }
 
-// Sizing of the split kernel a decode without a Quest selection launches.
-int splitkv_smem_bytes(const pa_shape &shape) {
-  const int heads = heads_per_unit(shape, nullptr);
+// Sizing of the split kernel a decode with these options (NULL: none) launches.
+int splitkv_smem_bytes(const pa_shape &shape, const pa_decode_opts *opts) {
+  const int heads = heads_per_unit(shape, opts, opts && opts->num_prefix_groups > 0);
   const pa_shape s = unit_view(shape, heads);
   const int nt = (s.Hq / s.Hkv + 7) / 8;
   const int kind = kind_of(s, heads);
@@ -1960,8 +2029,8 @@ int splitkv_smem_bytes(const pa_shape &shape) {
 
 int decode_warps_per_cta() { return Cfg<128, 1, false>::WARPS; }
 
-int splitkv_min_blocks(const pa_shape &shape) {
-  const int heads = heads_per_unit(shape, nullptr);
+int splitkv_min_blocks(const pa_shape &shape, const pa_decode_opts *opts) {
+  const int heads = heads_per_unit(shape, opts, opts && opts->num_prefix_groups > 0);
   const pa_shape s = unit_view(shape, heads);
   const int nt = (s.Hq / s.Hkv + 7) / 8;
   const int kind = kind_of(s, heads);
@@ -1975,7 +2044,7 @@ int splitkv_min_blocks(const pa_shape &shape) {
 WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits) {
   WorkspaceLayout w{};
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  const size_t G = static_cast<size_t>(s.Hq / s.Hkv) * (int4_pairable(s) ? 2 : 1);
+  const size_t G = static_cast<size_t>(s.Hq / s.Hkv) * (pairable(s) ? 2 : 1);
   w.prefix = 0;
   w.lse = up(w.prefix + (static_cast<size_t>(s.B) + 4) * 4);
   w.o_part = up(w.lse + static_cast<size_t>(num_splits) * 2 * G * 4);
@@ -1987,7 +2056,7 @@ pa_status run_decode(const pa_shape &s, float *out, const void *q, const void *k
                      const void *v_pool, const float *k_scale, const float *v_scale,
                      const int32_t *bt, const int32_t *sl, const pa_decode_opts *opts,
                      float sm_scale, int32_t *err, cudaStream_t stream) {
-  const int heads = heads_per_unit(s, opts);
+  const int heads = heads_per_unit(s, opts, false, true);
   const pa_shape v = unit_view(s, heads);
   CUtensorMap mk, mv;
   if (!make_pool_map(&mk, k_pool, v, heads) || !make_pool_map(&mv, v_pool, v, heads))

@@ -96,10 +96,10 @@ pa_status run_cascade(const pa_shape &s, const CUtensorMap &mk, const CUtensorMa
 constexpr int kMaxSplitBatch = 16384;
 
 WorkspaceLayout splitkv_layout(const pa_shape &s, int num_splits);
-int splitkv_smem_bytes(const pa_shape &s);
+int splitkv_smem_bytes(const pa_shape &s, const pa_decode_opts *opts = nullptr);
 int decode_warps_per_cta();
 // CTAs per SM the split kernel is compiled for (registers capped accordingly).
-int splitkv_min_blocks(const pa_shape &s);
+int splitkv_min_blocks(const pa_shape &s, const pa_decode_opts *opts = nullptr);
 
 pa_status run_reshape_and_cache(const pa_shape &s, const void *k_new, const void *v_new,
                                 void *k_pool, void *v_pool, float *k_scale, float *v_scale,

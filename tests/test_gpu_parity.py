@@ -1054,9 +1054,9 @@ def _splitkv_pieces(batch, S, workers):
     cut of pa_decode_splitkv (no window): segments of W tiles over the (b, unit,
     position) tile stream, W = max(ceil(total / workers), ceil((n_max - 1) / (S - 1)));
     with S = 1 every unit is one piece.  A unit is (b, KV head), or (b, KV heads 2u,
-    2u + 1) for 4-bit pools read in pairs."""
-    paired = (batch.kv_dtype == "int4" and batch.D == 128 and batch.Hkv % 2 == 0
-              and batch.Hq == 8 * batch.Hkv)
+    2u + 1) for 4-bit and E4M3 pools read in pairs."""
+    paired = (batch.kv_dtype in ("int4", "fp8_e4m3") and batch.D == 128
+              and batch.Hkv % 2 == 0 and batch.Hq == 8 * batch.Hkv)
     Hu = batch.Hkv // (2 if paired else 1)
     n = [(int(L) + 15) // 16 for L in batch.seq_lens]
     prefix = np.concatenate([[0], np.cumsum([Hu * x for x in n])]).astype(np.int64)
