@@ -42,14 +42,14 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_667_264 + 2_657_024, "kernel_hash": "8840ba5514389ad5"},
-    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_565_440 + 1_198_080, "kernel_hash": "8840ba5514389ad5"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_544_876_288 + 2_954_752, "kernel_hash": "8840ba5514389ad5"},
-    ("prefix_sharing", "decode_pair_kernel"): {"bytes": 2_541_487_616 + 93_696, "kernel_hash": "8840ba5514389ad5"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_533_760 + 2_196_480, "kernel_hash": "8840ba5514389ad5"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_210_432 + 12_521_472, "kernel_hash": "8840ba5514389ad5"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_262_064_896 + 19_605_760, "kernel_hash": "8840ba5514389ad5"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_124_983_040 + 16_243_456, "kernel_hash": "8840ba5514389ad5"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_639_104 + 2_482_176, "kernel_hash": "2bdd123281d86a86"},
+    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_725_184 + 1_241_088, "kernel_hash": "2bdd123281d86a86"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_019_136 + 3_275_520, "kernel_hash": "2bdd123281d86a86"},
+    ("prefix_sharing", "decode_pair_kernel"): {"bytes": 2_541_345_536 + 164_864, "kernel_hash": "2bdd123281d86a86"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_333_056 + 2_892_800, "kernel_hash": "2bdd123281d86a86"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_232_448 + 12_568_320, "kernel_hash": "2bdd123281d86a86"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_248_185_344 + 17_004_544, "kernel_hash": "2bdd123281d86a86"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_125_042_432 + 16_304_640, "kernel_hash": "2bdd123281d86a86"},
 }
 
 
@@ -410,9 +410,11 @@ def traffic_for(config: str, kernel: str):
 
 # The per-workload lines: the other workloads of the measurement plan, each timed in
 # the same process as the headline, through the call named (the cross-sequence prefix
-# batch through both the split decode and pa_decode without a workspace).
+# batch and the FP8 batch through both the split decode and pa_decode without a
+# workspace).
 PER_CONFIG = (("prefix_sharing", "splitkv"), ("prefix_sharing", "decode"),
-              ("long_context", "splitkv"), ("fp8_mixed", "decode"), ("int4_mixed", "splitkv"))
+              ("long_context", "splitkv"), ("fp8_mixed", "decode"), ("fp8_mixed", "splitkv"),
+              ("int4_mixed", "splitkv"))
 
 
 def per_config_lines(args, device, world, rank):
