@@ -27,6 +27,7 @@ import math
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -94,11 +95,23 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 
 
 class ClockSampler:
+    """nvidia-smi sampling the SM clocks and throttle reasons every 100 ms.  start() waits
+    for its first sample, so that its start-up (driver queries) is over before a timed
+    region begins; mark() at the region's start drops the samples taken before it."""
+
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.lines = []
+        self.first = 0
+        self.reader = None
 
-    def start(self):
+    def _pump(self):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self.lines.append(ln)
+
+    def start(self, wait_s: float = 3.0):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_QUERY}",
@@ -106,17 +119,27 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        self.reader = threading.Thread(target=self._pump, daemon=True)
+        self.reader.start()
+        t0 = time.perf_counter()
+        while not self.lines and time.perf_counter() - t0 < wait_s:
+            time.sleep(0.005)
+
+    def mark(self):
+        self.first = len(self.lines)
 
     def stop(self) -> dict:
         lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            lines = [ln for ln in out.splitlines() if ln.strip()]
+                self.proc.wait()
+            self.reader.join(timeout=5)
+            lines = self.lines[self.first:]
         if not lines:     # the timed region was shorter than one sample: take one now
             try:
                 lines = subprocess.run(
@@ -358,6 +381,8 @@ def time_steps(run, steps: int, warmup: int, kv_bytes: int, device, world: int, 
     stream = run.stream
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(0, steps, EVENT_EVERY)]
+    if clocks is not None:
+        clocks.start()       # before the warm-up: its start-up is over by the timed region
     for _ in range(warmup):
         run()
     torch.cuda.synchronize()
@@ -377,7 +402,7 @@ def time_steps(run, steps: int, warmup: int, kv_bytes: int, device, world: int, 
     barrier(world)
     torch.cuda.synchronize()
     if clocks is not None:
-        clocks.start()
+        clocks.mark()        # samples from here on
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
