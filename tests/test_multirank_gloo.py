@@ -54,3 +54,17 @@ def test_single_rank_defaults(monkeypatch):
     assert bench.dist_env() == (0, 1, 0)
     assert bench.reduce_max(3.5, 1) == 3.5
     assert bench.rank_seed(1, 0) == 1 and np.unique([bench.rank_seed(1, r) for r in range(8)]).size == 8
+
+
+def test_decode_time_sample_is_stratified():
+    """The decode kernel's mean over K timed steps from events on step 0 and the middle of
+    each later block of 8: step 0 counts once, the other samples stand for the rest."""
+    assert bench.sampled_steps(1) == [0]
+    assert bench.sampled_steps(20) == [0, 4, 12]
+    s = bench.sampled_steps(2000)
+    assert s[0] == 0 and len(s) == 1 + 250 and all(i % 8 == 4 for i in s[1:])
+    # equal times give that time; a slow first step weighs 1/K, not 1/len(sample)
+    assert bench.mean_decode_ms({0: 3.0, 4: 3.0, 12: 3.0}, 20) == 3.0
+    got = bench.mean_decode_ms({0: 230.0, 4: 210.0, 12: 210.0}, 20)
+    assert abs(got - (230.0 + 19 * 210.0) / 20) < 1e-9
+    assert bench.mean_decode_ms({0: 7.0}, 1) == 7.0
