@@ -364,11 +364,16 @@ class StepRunner:
         if ev is not None:
             ev[1].record(st)
 
+    def kernel_name(self):
+        if self.call == "decode":
+            return decode_kernel(self.batch, self.args.window, self.quest, self.dev.device)
+        return "decode_segment_kernel"
+
     def kernel_label(self):
         if self.call == "splitkv":
             return "decode_segment_kernel (the pa_decode_splitkv call)"
         if self.call == "decode":
-            return "decode_pair_kernel (the pa_decode call, no workspace)"
+            return self.kernel_name() + " (the pa_decode call, no workspace)"
         return ("pa_decode call with a workspace: "
                 + ("cascade_kernel + " if self.args.cascade else "")
                 + "decode_segment_kernel + merge_kernel")
@@ -378,8 +383,8 @@ class StepRunner:
         if self.call == "splitkv":
             return "pa_reshape_and_cache + " + quest + "pa_decode_splitkv + pa_merge_lse"
         if self.call == "decode":
-            return ("pa_reshape_and_cache + " + quest + "pa_decode (no workspace: one CTA, "
-                    "or a cluster of CTAs, per sequence and KV head)")
+            return ("pa_reshape_and_cache + " + quest + "pa_decode (no workspace: persistent "
+                    "CTAs, or one CTA or a cluster of CTAs per sequence and KV head)")
         return ("pa_reshape_and_cache + " + quest + "pa_decode with a workspace ("
                 + ("cascade + " if self.args.cascade else "") + "split kernel + merge)")
 
@@ -446,6 +451,21 @@ def time_steps(run, steps: int, warmup: int, kv_bytes: int, device, world: int, 
     return ms_per_step, decode_ms, clock_info
 
 
+def decode_kernel(batch, window: int, quest: bool, device) -> str:
+    """The kernel pa_decode without a workspace runs (the library's choice): persistent
+    CTAs for bf16 batches of up to 8 query heads per KV head with more (sequence, KV head)
+    units than two per resident CTA, at most 2,048, and no window or page selection; one
+    CTA (or a cluster of CTAs) per unit otherwise."""
+    import torch
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    units, g = batch.B * batch.Hkv, batch.Hq // batch.Hkv
+    per_sm = {128: 2, 64: 4}.get(batch.D, 0)     # resident CTAs of the per-unit kernel
+    if (batch.kv_dtype == "bf16" and g <= 8 and per_sm and window == 0 and not quest
+            and 2 * sms * per_sm < units <= 2048):
+        return "decode_persist_kernel"
+    return "decode_pair_kernel"
+
+
 def traffic_for(config: str, kernel: str):
     tr = TRAFFIC.get((config, kernel))
     return tr["bytes"] if tr and tr.get("kernel_hash") == kernel_source_hash() else None
@@ -479,7 +499,7 @@ def per_config_lines(args, device, world, rank):
         steps = max(EVENT_EVERY, args.steps)
         ms, kms, _ = time_steps(run, steps, args.warmup, kv_bytes, device, world)
         achieved = kv_bytes / (kms * 1e-3) / 1e9
-        kernel = "decode_pair_kernel" if call == "decode" else "decode_segment_kernel"
+        kernel = run.kernel_name()
         out[f"{config}/{call}"] = {
             "call": run.step_label(), "kernel": run.kernel_label(),
             "tokens_per_s": world * batch.B / (ms * 1e-3), "ms_per_step": ms, "kernel_ms": kms,
@@ -679,7 +699,7 @@ def run_ours(args):
     unique_tokens = step_kv_tokens(batch, args, selected)
     peak, peak_kind = measured_peak_hbm()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
-    kernel = "decode_pair_kernel" if call == "decode" else "decode_segment_kernel"
+    kernel = run.kernel_name()
     plain = args.window == 0 and args.quest_topk == 0 and not args.cascade
     traffic = traffic_for(args.config, kernel) if plain and call != "segments" else None
     result = {

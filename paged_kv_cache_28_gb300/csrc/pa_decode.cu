@@ -1456,6 +1456,467 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 }
 
 // ----------------------------------------------------------------------------
+// pa_decode without a workspace on many units: persistent CTAs
+// ----------------------------------------------------------------------------
+
+// A bf16 batch with more (sequence, KV head) units than two per resident CTA, and no
+// window or page selection, runs one CTA of eight warps per SM instead of one CTA per
+// unit.  Every CTA computes the same static schedule from the lengths ("water
+// filling"): the units, longest first, are dealt out in rounds; each round's units
+// fill the least loaded CTAs up to a common level, a unit going to the CTA in whose
+// share the midpoint of its tiles falls.  Each CTA so gets about the mean number of
+// tiles, and no unit is split across CTAs (there is no memory to merge them in).  A
+// CTA's units form one stream of tiles, cut into eight equal contiguous segments, one
+// per warp: each warp's ring runs on from one unit into the next, a long unit is read
+// by several warps, and a unit inside one segment is finished by its warp alone.  A
+// unit that crosses segments is joined in shared memory: each warp before the last
+// that holds part of it leaves its state in its mailbox (a warp's only part that ends
+// before the unit does), and the warp holding the unit's last tile folds those parts,
+// in warp order, into its own and writes the output.  The schedule, the segments and
+// the fold order are fixed by the inputs, so results repeat bit for bit.
+constexpr int kPersistWarps = 8;
+constexpr int kPersistMaxUnits = 2048;   // the unit list's capacity: any batch's units fit
+constexpr int kPersistMaxBins = 256;     // CTAs of the launch (one per SM)
+constexpr int kPersistMaxRounds = 24;    // rounds of the water filling (at least U / 16 units each)
+
+template <class B>
+struct PersistCfg : B {
+  static constexpr int WARPS = kPersistWarps;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int GP = 8 * B::NT;
+  static constexpr int RING = 1024 + WARPS * (B::STAGES * (B::STAGE_BYTES + 8 + B::META_BYTES) +
+                                              B::QF_BYTES);
+  static constexpr int MAILBOX_BYTES = WARPS * GP * (B::D + 2) * 4;   // acc, m, l per warp
+  static constexpr int LIST_BYTES = (2 * kPersistMaxUnits + 1 + WARPS + 4) * 4;
+  static constexpr int SMEM = RING + MAILBOX_BYTES + LIST_BYTES;
+  static_assert(!B::QUANT && B::NT == 1, "persistent CTAs serve bf16 units of up to 8 heads");
+  static_assert(SMEM <= 227 * 1024, "one persistent CTA per SM");
+};
+
+// Shared scratch of the schedule (in the stage area, before any copy is issued).
+template <int NW>
+struct PersistScratch {
+  static constexpr int NB = kRankBuckets;
+  int32_t gp[kPersistMaxUnits + 1];         // tiles of the units before position k
+  int32_t lo[kPersistMaxBins];              // a round's first unit of each CTA
+  int32_t tiles[kPersistMaxUnits];          // attended tiles per sequence
+  int32_t order[kPersistMaxUnits];          // longest-first position -> sequence
+  int32_t uid[kPersistMaxUnits];            // longest-first position -> unit
+  int32_t hist[NW][NB];                     // per-warp bucket counts, then sort bases
+  int32_t wsum[NW];                         // block scans: per-warp totals
+  long long wsum64[NW];
+  long long red[2][NW];                     // the fill level's reductions (two in turn)
+  int32_t mine[kPersistMaxRounds][2];       // this CTA's unit range of each round
+  uint8_t bucket[kPersistMaxUnits];
+};
+
+// Block-wide exclusive scan of one value per thread (every thread gets the total).
+template <int THREADS, class T>
+__device__ __forceinline__ T block_scan_excl(T v, T *wsum, T &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  T off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < THREADS / 32; ++w) {
+    off += w < warp ? wsum[w] : 0;
+    tot += wsum[w];
+  }
+  __syncthreads();   // wsum is free again
+  total = tot;
+  return off + inc - v;
+}
+
+// The schedule: this CTA's units (ids sequence * Hkv + KV head) in stream order, with
+// starts[k] = tiles of the units before unit k (starts[n] = the CTA's tiles).  Returns n.
+// The launch keeps every sum of tiles below 2^30.
+template <int THREADS>
+__device__ int persist_schedule(const Params &p, PersistScratch<THREADS / 32> &s,
+                                int32_t *units, int32_t *starts) {
+  constexpr int NW = THREADS / 32, NB = PersistScratch<NW>::NB;
+  static_assert(THREADS >= NB && THREADS >= kPersistMaxBins, "a bucket and a CTA per thread");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = p.B, H = p.Hkv, U = B * H, bins = gridDim.x;
+  const int cap = p.max_blocks * p.bs;
+  for (int b = tid; b < B; b += THREADS) {
+    const int L = __ldg(p.seq_lens + b);
+    if ((L < 0 || L > cap) && blockIdx.x == 0) set_err(p.err, PA_DEVERR_SEQ_LEN);
+    const int n = seq_tiles(min(max(L, 0), cap), 0).count;
+    s.tiles[b] = n;
+    s.bucket[b] = static_cast<uint8_t>(tile_bucket(n));
+  }
+  for (int i = tid; i < NW * NB; i += THREADS) (&s.hist[0][0])[i] = 0;
+  __syncthreads();
+  // ---- stable order of the sequences: bucket descending, then index.  Warp w counts
+  // and places the sequences of its own contiguous range.
+  const int per = (B + NW - 1) / NW;
+  const int lo = min(B, warp * per), hi = min(B, lo + per);
+  for (int b = lo + lane; b < hi; b += 32) atomicAdd(&s.hist[warp][s.bucket[b]], 1);
+  __syncthreads();
+  {
+    // first position of bucket k: the sequences in higher buckets (thread t: bucket NB-1-t)
+    const int k = NB - 1 - tid;
+    int cnt = 0;
+    if (tid < NB)
+#pragma unroll
+      for (int w = 0; w < NW; ++w) cnt += s.hist[w][k];
+    int total;
+    int first = block_scan_excl<THREADS>(cnt, s.wsum, total);
+    if (tid < NB)
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {   // warp w's first position in bucket k
+        const int c = s.hist[w][k];
+        s.hist[w][k] = first;
+        first += c;
+      }
+  }
+  __syncthreads();
+  for (int b0 = lo; b0 < hi; b0 += 32) {
+    const int b = b0 + lane;
+    const int key = b < hi ? s.bucket[b] : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    const uint32_t below = peers & ((1u << lane) - 1u);
+    if (b < hi) s.order[s.hist[warp][key] + __popc(below)] = b;
+    __syncwarp();
+    if (b < hi && below == 0) s.hist[warp][key] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // ---- the units in that order (KV heads in turn) and the prefix of their tiles
+  {
+    const int run = (U + THREADS - 1) / THREADS;
+    const int k0 = min(U, tid * run), k1 = min(U, k0 + run);
+    int mine = 0;
+    for (int k = k0; k < k1; ++k) {
+      const int q = k / H, b = s.order[q];
+      s.uid[k] = b * H + (k - q * H);
+      mine += s.tiles[b];
+    }
+    int total;
+    int at = block_scan_excl<THREADS>(mine, s.wsum, total);
+    for (int k = k0; k < k1; ++k) {
+      s.gp[k] = at;
+      at += s.tiles[s.uid[k] / H];
+    }
+    if (tid == 0) s.gp[U] = total;
+  }
+  __syncthreads();
+  // ---- water filling.  Round r deals the next max(bins * (r + 1), U / 16) units of the
+  // order; thread b < bins keeps CTA b's load.
+  const bool has_bin = tid < bins;
+  int lb = 0;
+  int rounds = 0;
+  for (int next = 0, r = 0; next < U; ++r) {
+    const int c = min(U - next, max(bins * (r + 1), (U + 15) / 16));
+    const int base = s.gp[next], tot = s.gp[next + c] - base;
+    // The fill level: the CTAs S below it take the round's tiles, h = (tot + their
+    // loads) / |S|.  From S = every CTA, dropping those at or above the level lowers
+    // it; S is final when none drops (a round of no tiles keeps the least loaded).
+    bool in = has_bin;
+    long long A = 0;
+    int m = 0;
+    for (int it = 0;; ++it) {
+      long long v = in ? ((1ll << 40) | lb) : 0ll;   // members in bits 40.., loads below
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) s.red[it & 1][warp] = v;
+      __syncthreads();
+      long long t = 0;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) t += s.red[it & 1][w];
+      m = static_cast<int>(t >> 40);
+      A = tot + (t & ((1ll << 40) - 1));
+      const bool stay = in && static_cast<long long>(lb) * m < A;
+      const int nm = __syncthreads_count(stay);
+      if (nm == m || nm == 0) break;
+      in = stay;
+    }
+    // shares in CTA order: h - load for each member, one tile more for its first rem
+    // members, so that they add up to tot; CTA b's share is [cum, cum + share)
+    const long long h = A / m, rem = A - h * m;
+    long long shares;
+    const long long px = block_scan_excl<THREADS>(in ? ((1ll << 40) | (h - lb)) : 0ll, s.wsum64,
+                                                  shares);
+    // CTA b takes the units whose tile midpoints fall in its share: from the first unit
+    // whose midpoint reaches cum up to the next CTA's first (CTAs without a share take none)
+    if (has_bin) {
+      const long long cum2 = 2 * ((px & ((1ll << 40) - 1)) + min(px >> 40, rem));
+      int a = next, z = next + c;   // first k in [next, next + c) with 2 mid(k) >= cum2
+      while (a < z) {
+        const int md = (a + z) >> 1;
+        if (static_cast<long long>(s.gp[md]) + s.gp[md + 1] - 2ll * base >= cum2) z = md;
+        else a = md + 1;
+      }
+      s.lo[tid] = a;
+    }
+    __syncthreads();
+    if (has_bin) {
+      const int k0 = tid == 0 ? next : s.lo[tid], k1 = tid + 1 < bins ? s.lo[tid + 1] : next + c;
+      lb += s.gp[k1] - s.gp[k0];
+      if (tid == static_cast<int>(blockIdx.x)) {
+        s.mine[r][0] = k0;
+        s.mine[r][1] = k1;
+      }
+    }
+    __syncthreads();   // lo is read before the next round writes it
+    next += c;
+    rounds = r + 1;
+  }
+  // ---- this CTA's list: its ranges of the order, round by round
+  int n = 0;
+  for (int r = 0; r < rounds; ++r) {
+    const int k0 = s.mine[r][0], k1 = s.mine[r][1];
+    for (int k = k0 + tid; k < k1; k += THREADS) {
+      units[n + k - k0] = s.uid[k];
+      starts[n + k - k0] = s.gp[k] - s.gp[k0];   // within the range, made absolute below
+    }
+    n += k1 - k0;
+  }
+  __syncthreads();
+  for (int r = 0, at = 0, off = 0; r < rounds; ++r) {   // ranges' tile offsets
+    const int k0 = s.mine[r][0], k1 = s.mine[r][1];
+    for (int k = k0 + tid; k < k1; k += THREADS) starts[at + k - k0] += off;
+    at += k1 - k0;
+    off += s.gp[k1] - s.gp[k0];
+    if (r == rounds - 1 && tid == 0) starts[n] = off;
+  }
+  __syncthreads();
+  return n;
+}
+
+// Warp w's segment [begin, end) of its CTA's tile stream.
+struct PersistSource {
+  const int32_t *units, *starts;   // shared: the CTA's list
+  const int32_t *seq_lens, *block_tables, *shared_prefix_lens;
+  int32_t *err;
+  int n, begin, end, Hkv, bs, nblocks, max_blocks;
+  int base;
+  int4 cur, nxt;
+
+  __device__ __forceinline__ int count() const { return end - begin; }
+  __device__ __forceinline__ int4 load(int i) const {
+    const int g = begin + i;
+    if (g >= end) return make_int4(0, 0, -1, 0);   // never issued
+    int a = 0, z = n - 1;   // the unit holding position g: largest k with starts[k] <= g
+    while (a < z) {
+      const int md = (a + z + 1) >> 1;
+      if (starts[md] <= g) a = md; else z = md - 1;
+    }
+    const int unit = units[a], b = unit / Hkv, kvh = unit - b * Hkv;
+    const int nk = starts[a + 1] - starts[a], j = g - starts[a];
+    const int L = min(max(__ldg(seq_lens + b), 0), max_blocks * bs);
+    const SeqTiles geo = seq_tiles(L, 0);
+    int phys = __ldg(block_tables + static_cast<size_t>(b) * max_blocks + (j * kTile) / bs);
+    if (phys < 0 || phys >= nblocks) {
+      set_err(err, PA_DEVERR_BLOCK_ID);
+      phys = kInvalidPhys;
+    }
+    int info = (j == nk - 1) ? geo.last_valid : kTile;
+    if (j == 0) info |= kFirstOfPair | kPieceStart;
+    if (j == nk - 1) info |= kLastOfPair | kPieceEnd;
+    if (i == 0) info |= kPieceStart;
+    if (g == end - 1) info |= kPieceEnd;
+    if (shared_prefix_lens)
+      info |= ((j + 1) * kTile <= __ldg(shared_prefix_lens + b)) ? kHintShared : kHintPrivate;
+    return tile_record(phys, j, unit, kvh, Hkv, bs, nblocks, info | (kvh << kKvhShift));
+  }
+  __device__ __forceinline__ void init(int lane) {
+    base = 0;
+    cur = load(lane);
+    nxt = load(32 + lane);
+  }
+  __device__ __forceinline__ int4 get(int i, int lane) {
+    while (i >= base + 32) {
+      cur = nxt;
+      base += 32;
+      nxt = load(base + 32 + lane);
+    }
+    return shfl_int4(cur, i - base);
+  }
+};
+
+// Lane 0 polls a shared flag until it reads nonzero (bounded: a wait that runs out sets
+// the error flag and returns false).  Returns for the whole warp.
+__device__ __forceinline__ bool persist_wait(const volatile int32_t *flag, int32_t *err, int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    uint32_t i = 0;
+    while (*flag == 0) {
+      if (++i == kWaitSpins) {
+        ok = 0;
+        set_err(err, PA_DEVERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __threadfence_block();
+  return ok != 0;
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    decode_persist_kernel(const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const Params p) {
+  constexpr int GP = C::GP, W = C::WARPS;
+  using Scratch = PersistScratch<C::THREADS / 32>;
+  static_assert(sizeof(Scratch) <= W * C::STAGES * C::STAGE_BYTES,
+                "the schedule's scratch lives in the stage area");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  float *box_acc = reinterpret_cast<float *>(split_tail<C>(smem_raw));   // [W][GP][D]
+  float *box_m = box_acc + W * GP * C::D;                                 // [W][GP]
+  float *box_l = box_m + W * GP;                                          // [W][GP]
+  int32_t *units = reinterpret_cast<int32_t *>(box_l + W * GP);          // [max units]
+  int32_t *starts = units + kPersistMaxUnits;                             // [max units + 1]
+  int32_t *filled = starts + kPersistMaxUnits + 1;                        // [W] mailbox flags
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int n = persist_schedule<C::THREADS>(p, *reinterpret_cast<Scratch *>(base), units, starts);
+  if (threadIdx.x < W) filled[threadIdx.x] = 0;
+  // units without tiles (empty sequences) have no warp to write them
+  for (int k = warp; k < n; k += W) {
+    if (starts[k + 1] > starts[k]) continue;
+    const int unit = units[k], b = unit / p.Hkv, kvh = unit - b * p.Hkv;
+    float *out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D;
+    for (int e = lane; e < p.G * C::D; e += 32) out[e] = 0.f;
+  }
+  __syncthreads();   // the scratch is read: the stages may be filled
+
+  const int T = starts[n];
+  auto seg = [&](int w) { return static_cast<int>(static_cast<long long>(w) * T / W); };
+  WarpSmem ws = setup_smem<C>(smem_raw, warp, p.G, lane);
+  State<C> st, held;
+  st.reset();
+  held.reset();
+  PersistSource src;
+  src.units = units;
+  src.starts = starts;
+  src.seq_lens = p.seq_lens;
+  src.block_tables = p.block_tables;
+  src.shared_prefix_lens = p.shared_prefix_lens;
+  src.err = p.err;
+  src.n = n;
+  src.begin = seg(warp);
+  src.end = seg(warp + 1);
+  src.Hkv = p.Hkv;
+  src.bs = p.bs;
+  src.nblocks = p.nblocks;
+  src.max_blocks = p.max_blocks;
+  src.init(lane);
+  auto out_of = [&](int unit) {
+    const int b = unit / p.Hkv, kvh = unit - b * p.Hkv;
+    return p.out + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * C::D;
+  };
+  const int qd = lane & 3;
+  // this warp's mailbox: m, l (totals over the warp) and acc of a state
+  auto deposit = [&](const float (&m)[2], const float (&l)[2], auto &&acc_of) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int g = 2 * qd + j;
+      if ((lane >> 2) == 0) {
+        box_m[warp * GP + g] = m[j];
+        box_l[warp * GP + g] = l[j];
+      }
+#pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          box_acc[(warp * GP + g) * C::D + acc_d<C>(dt, j + 2 * h, lane)] = acc_of(dt, j + 2 * h);
+    }
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) *reinterpret_cast<volatile int32_t *>(&filled[warp]) = 1;
+  };
+  int held_unit = -1;
+  bool held_last = false;
+  auto on_end = [&](int4 u, bool piece_first, State<C> &s) {
+    const bool last = (u.w & kLastOfPair) != 0;
+    if (piece_first && last) {              // a whole unit: finished here
+      write_normalised<C>(s, out_of(u.y), nullptr, p.G, lane);
+    } else if (!piece_first) {              // the unit came from the warps before
+      held = s;
+      held_unit = u.y;
+      held_last = last;
+    } else {                                // the unit goes on into the next warp
+      float lt[1][2];
+      reduce_l<C>(s, lt);
+      const float mm[2] = {s.m[0][0], s.m[0][1]}, ll[2] = {lt[0][0], lt[0][1]};
+      deposit(mm, ll, [&](int dt, int i) { return s.acc[0][dt][i]; });
+    }
+  };
+  const bool ok = run_warp<C>(src, ws, st, p, &tmK, &tmV, on_end, lane);
+  if (held_unit < 0 || !ok) return;
+  float lt[1][2];
+  reduce_l<C>(held, lt);
+  if (!held_last) {   // the unit goes on past this segment: its last warp folds this part
+    const float mm[2] = {held.m[0][0], held.m[0][1]}, ll[2] = {lt[0][0], lt[0][1]};
+    deposit(mm, ll, [&](int dt, int i) { return held.acc[0][dt][i]; });
+    return;
+  }
+  // ---- the unit's last warp: fold the parts the warps before left in their mailboxes,
+  // in warp order, then its own, and write the output
+  int k = 0;   // the unit: the one holding this segment's first tile
+  for (int z = n - 1; k < z;) {
+    const int md = (k + z + 1) >> 1;
+    if (starts[md] <= src.begin) k = md; else z = md - 1;
+  }
+  float M[2] = {-INFINITY, -INFINITY}, L[2] = {0.f, 0.f}, acc[C::DT][4];
+#pragma unroll
+  for (int dt = 0; dt < C::DT; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
+  auto fold = [&](const float (&mo)[2], const float (&lo)[2], auto &&acc_of) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float Mn = fmaxf(M[j], mo[j]);
+      const float fa = M[j] == -INFINITY ? 0.f : ex2(M[j] - Mn);
+      const float fb = mo[j] == -INFINITY ? 0.f : ex2(mo[j] - Mn);
+#pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) acc[dt][j + 2 * h] = acc[dt][j + 2 * h] * fa + acc_of(dt, j + 2 * h) * fb;
+      L[j] = L[j] * fa + lo[j] * fb;
+      M[j] = Mn;
+    }
+  };
+  for (int w = 0; w < warp; ++w) {
+    if (seg(w + 1) <= starts[k] || seg(w) == seg(w + 1)) continue;   // holds none of the unit
+    if (!persist_wait(&filled[w], p.err, lane)) return;
+    float mo[2], lo[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      mo[j] = box_m[w * GP + 2 * qd + j];
+      lo[j] = box_l[w * GP + 2 * qd + j];
+    }
+    fold(mo, lo, [&](int dt, int i) {
+      return box_acc[(w * GP + 2 * qd + (i & 1)) * C::D + acc_d<C>(dt, i, lane)];
+    });
+  }
+  {
+    const float mo[2] = {held.m[0][0], held.m[0][1]}, lo[2] = {lt[0][0], lt[0][1]};
+    fold(mo, lo, [&](int dt, int i) { return held.acc[0][dt][i]; });
+  }
+  float *out = out_of(held_unit);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int g = 2 * qd + j;
+    if (g >= p.G) continue;
+    const float inv = L[j] > 0.f ? 1.f / L[j] : 0.f;
+#pragma unroll
+    for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) out[g * C::D + acc_d<C>(dt, j + 2 * h, lane)] = acc[dt][j + 2 * h] * inv;
+  }
+}
+
+// ----------------------------------------------------------------------------
 // pa_decode_splitkv: plan (scan + unit list), segmented decode, merge
 // ----------------------------------------------------------------------------
 
@@ -1885,6 +2346,18 @@ static int pair_cluster_ctas(int units, int resident_ctas, int window, int topk)
   return max_tiles <= share ? 1 : 4;
 }
 
+// pa_decode without a workspace on a bf16 batch of more units than two per resident
+// CTA (and at most kPersistMaxUnits), with no window or page selection: one persistent
+// CTA of eight warps per SM on a static water-filled schedule.
+template <class C>
+static pa_status launch_persist(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
+                                cudaStream_t stream, int sms) {
+  using P = PersistCfg<C>;
+  if (prep_kernel(decode_persist_kernel<P>, P::SMEM) != cudaSuccess) return PA_ERR_CUDA;
+  decode_persist_kernel<P><<<sms, P::THREADS, P::SMEM, stream>>>(mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 template <class C>
 static pa_status launch_pair_units(const Params &p, const CUtensorMap &mk, const CUtensorMap &mv,
                                    cudaStream_t stream) {
@@ -1893,6 +2366,13 @@ static pa_status launch_pair_units(const Params &p, const CUtensorMap &mk, const
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PA_ERR_CUDA;
+  if constexpr (C::KIND == kKindBf16 && C::NT == 1) {
+    // (every sum of tiles the schedule forms stays below 2^31)
+    const long long max_tiles = (static_cast<long long>(p.max_blocks) * p.bs + kTile - 1) / kTile;
+    if (units > 2 * sms * C::MIN_BLOCKS && units <= kPersistMaxUnits && sms <= kPersistMaxBins &&
+        p.window == 0 && p.topk == 0 && units * max_tiles < (1ll << 30))
+      return launch_persist<C>(p, mk, mv, stream, sms);
+  }
   const int ncl = pair_cluster_ctas<C>(units, sms * C::MIN_BLOCKS, p.window, p.topk);
   auto one_cta_per_unit = [&]() {
     if (prep_kernel(decode_pair_kernel<C, false>, C::PAIR_SMEM) != cudaSuccess) return PA_ERR_CUDA;
