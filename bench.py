@@ -454,14 +454,14 @@ def time_steps(run, steps: int, warmup: int, kv_bytes: int, device, world: int, 
 def decode_kernel(batch, window: int, quest: bool, device) -> str:
     """The kernel pa_decode without a workspace runs (the library's choice): persistent
     CTAs for bf16 batches of up to 8 query heads per KV head with more (sequence, KV head)
-    units than two per resident CTA, at most 2,048, and no window or page selection; one
+    units than two per resident CTA, at most 4,096, and no window or page selection; one
     CTA (or a cluster of CTAs) per unit otherwise."""
     import torch
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     units, g = batch.B * batch.Hkv, batch.Hq // batch.Hkv
     per_sm = {128: 2, 64: 4}.get(batch.D, 0)     # resident CTAs of the per-unit kernel
     if (batch.kv_dtype == "bf16" and g <= 8 and per_sm and window == 0 and not quest
-            and 2 * sms * per_sm < units <= 2048):
+            and 2 * sms * per_sm < units <= 4096):
         return "decode_persist_kernel"
     return "decode_pair_kernel"
 

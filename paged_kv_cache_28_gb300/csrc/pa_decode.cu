@@ -1475,7 +1475,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 // in warp order, into its own and writes the output.  The schedule, the segments and
 // the fold order are fixed by the inputs, so results repeat bit for bit.
 constexpr int kPersistWarps = 8;
-constexpr int kPersistMaxUnits = 2048;   // the unit list's capacity: any batch's units fit
+constexpr int kPersistMaxUnits = 4096;   // the unit list's capacity: any batch's units fit
 constexpr int kPersistMaxBins = 256;     // CTAs of the launch (one per SM)
 constexpr int kPersistMaxRounds = 24;    // rounds of the water filling (at least U / 16 units each)
 
@@ -1487,7 +1487,7 @@ struct PersistCfg : B {
   static constexpr int RING = 1024 + WARPS * (B::STAGES * (B::STAGE_BYTES + 8 + B::META_BYTES) +
                                               B::QF_BYTES);
   static constexpr int MAILBOX_BYTES = WARPS * GP * (B::D + 2) * 4;   // acc, m, l per warp
-  static constexpr int LIST_BYTES = (2 * kPersistMaxUnits + 1 + WARPS + 4) * 4;
+  static constexpr int LIST_BYTES = kPersistMaxUnits * 2 + (kPersistMaxUnits + 1 + WARPS + 4) * 4;
   static constexpr int SMEM = RING + MAILBOX_BYTES + LIST_BYTES;
   static_assert(!B::QUANT && B::NT == 1, "persistent CTAs serve bf16 units of up to 8 heads");
   static_assert(SMEM <= 227 * 1024, "one persistent CTA per SM");
@@ -1538,7 +1538,7 @@ __device__ __forceinline__ T block_scan_excl(T v, T *wsum, T &total) {
 // The launch keeps every sum of tiles below 2^30.
 template <int THREADS>
 __device__ int persist_schedule(const Params &p, PersistScratch<THREADS / 32> &s,
-                                int32_t *units, int32_t *starts) {
+                                uint16_t *units, int32_t *starts) {
   constexpr int NW = THREADS / 32, NB = PersistScratch<NW>::NB;
   static_assert(THREADS >= NB && THREADS >= kPersistMaxBins, "a bucket and a CTA per thread");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1673,7 +1673,7 @@ __device__ int persist_schedule(const Params &p, PersistScratch<THREADS / 32> &s
   for (int r = 0; r < rounds; ++r) {
     const int k0 = s.mine[r][0], k1 = s.mine[r][1];
     for (int k = k0 + tid; k < k1; k += THREADS) {
-      units[n + k - k0] = s.uid[k];
+      units[n + k - k0] = static_cast<uint16_t>(s.uid[k]);
       starts[n + k - k0] = s.gp[k] - s.gp[k0];   // within the range, made absolute below
     }
     n += k1 - k0;
@@ -1692,7 +1692,8 @@ __device__ int persist_schedule(const Params &p, PersistScratch<THREADS / 32> &s
 
 // Warp w's segment [begin, end) of its CTA's tile stream.
 struct PersistSource {
-  const int32_t *units, *starts;   // shared: the CTA's list
+  const uint16_t *units;           // shared: the CTA's list
+  const int32_t *starts;
   const int32_t *seq_lens, *block_tables, *shared_prefix_lens;
   int32_t *err;
   int n, begin, end, Hkv, bs, nblocks, max_blocks;
@@ -1775,12 +1776,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   float *box_acc = reinterpret_cast<float *>(split_tail<C>(smem_raw));   // [W][GP][D]
   float *box_m = box_acc + W * GP * C::D;                                 // [W][GP]
   float *box_l = box_m + W * GP;                                          // [W][GP]
-  int32_t *units = reinterpret_cast<int32_t *>(box_l + W * GP);          // [max units]
-  int32_t *starts = units + kPersistMaxUnits;                             // [max units + 1]
+  uint16_t *units = reinterpret_cast<uint16_t *>(box_l + W * GP);        // [max units]
+  int32_t *starts = reinterpret_cast<int32_t *>(units + kPersistMaxUnits); // [max units + 1]
   int32_t *filled = starts + kPersistMaxUnits + 1;                        // [W] mailbox flags
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
+  pdl_trigger();
+  // the schedule reads only caller inputs (lengths); the output and the pools (written
+  // by the cache write) are touched only after the previous grid has finished
   const int n = persist_schedule<C::THREADS>(p, *reinterpret_cast<Scratch *>(base), units, starts);
+  pdl_wait();
   if (threadIdx.x < W) filled[threadIdx.x] = 0;
   // units without tiles (empty sequences) have no warp to write them
   for (int k = warp; k < n; k += W) {
@@ -2354,8 +2358,10 @@ static pa_status launch_persist(const Params &p, const CUtensorMap &mk, const CU
                                 cudaStream_t stream, int sms) {
   using P = PersistCfg<C>;
   if (prep_kernel(decode_persist_kernel<P>, P::SMEM) != cudaSuccess) return PA_ERR_CUDA;
-  decode_persist_kernel<P><<<sms, P::THREADS, P::SMEM, stream>>>(mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return launch_pdl(decode_persist_kernel<P>, dim3(sms), dim3(P::THREADS), P::SMEM, stream, mk, mv,
+                    p) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 template <class C>

@@ -1047,18 +1047,20 @@ def test_pa_decode_many_units(Hq, Hkv, D, lens_kind):
         assert dev.read_err() == 0
 
 
-@pytest.mark.parametrize("kind", ["prefix", "one_long", "tiny_units", "max_units", "g6_d64"])
+@pytest.mark.parametrize("kind", ["prefix", "one_long", "tiny_units", "max_units", "g6_d64",
+                                  "mixed_4000"])
 def test_pa_decode_persistent(kind):
     """pa_decode without a workspace on bf16 batches of more units than two per resident
-    CTA and at most 2,048, with no window or page selection: persistent CTAs of eight
-    warps on a water-filled schedule, the units' states merged through mailboxes in
-    shared memory.  A shared 900-token prefix with the L2 hints (800 units); one
-    30,000-token sequence among short ones (its units outweigh a CTA's mean share);
-    2,048 units of 0 to 40 tokens (empty units, units read by fewer than eight warps);
-    2,048 single-head sequences; G = 6 at D = 64.  Against the oracle, and repeatable
-    bit for bit."""
+    CTA and at most 4,096, with no window or page selection: persistent CTAs of eight
+    warps on a water-filled schedule, each CTA's tiles cut into one contiguous segment per
+    warp, units that cross segments joined in shared memory.  A shared 900-token prefix
+    with the L2 hints (800 units); one 30,000-token sequence among short ones (its units
+    outweigh a CTA's mean share and cross every segment of their CTAs); 2,048 units of 0
+    to 40 tokens (empty units, segments of a few tiles); 4,096 single-head sequences (the
+    largest list); G = 6 at D = 64; 4,000 units of up to 1,500 tokens.  Against the
+    oracle, and repeatable bit for bit."""
     rng = np.random.default_rng({"prefix": 601, "one_long": 602, "tiny_units": 603,
-                                 "max_units": 604, "g6_d64": 605}[kind])
+                                 "max_units": 604, "g6_d64": 605, "mixed_4000": 606}[kind])
     Hq, Hkv, D, groups = 64, 8, 128, ()
     if kind == "prefix":
         lens = [900 + int(x) for x in wl.lognormal_lens(rng, 100, 600, 1, 6000)]
@@ -1069,13 +1071,15 @@ def test_pa_decode_persistent(kind):
         lens = list(rng.integers(0, 41, 256))
     elif kind == "max_units":
         Hq, Hkv = 8, 1
-        lens = list(rng.integers(1, 700, 2048))
+        lens = list(rng.integers(1, 700, 4096))
+    elif kind == "mixed_4000":
+        lens = list(rng.integers(0, 1501, 500))
     else:
         Hq, Hkv, D = 48, 8, 64          # four CTAs per SM otherwise: 1,216 resident
         lens = list(rng.integers(0, 1500, 196)) + [0, 1, 16, 17]
     batch = wl.build_batch("t", lens, Hq=Hq, Hkv=Hkv, D=D, block_size=16, seed=610,
                            prefix_groups=groups)
-    assert 2 * (4 if D == 64 else 2) * 152 < batch.B * Hkv <= 2048
+    assert 2 * (4 if D == 64 else 2) * 152 < batch.B * Hkv <= 4096
     dev = DeviceBatch(batch)
     dev.reshape_and_cache()
     ref, _ = oracle_after_write(batch)
