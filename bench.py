@@ -43,14 +43,14 @@ FALLBACK_HBM_GBS = 6800.0
 # workload and kernel, with the hash of the kernel sources it was measured on; reported only
 # while they still match.
 TRAFFIC = {
-    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_639_104 + 2_482_176, "kernel_hash": "2bdd123281d86a86"},
-    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_725_184 + 1_241_088, "kernel_hash": "2bdd123281d86a86"},
-    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_019_136 + 3_275_520, "kernel_hash": "2bdd123281d86a86"},
-    ("prefix_sharing", "decode_pair_kernel"): {"bytes": 2_541_345_536 + 164_864, "kernel_hash": "2bdd123281d86a86"},
-    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_333_056 + 2_892_800, "kernel_hash": "2bdd123281d86a86"},
-    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_232_448 + 12_568_320, "kernel_hash": "2bdd123281d86a86"},
-    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_248_185_344 + 17_004_544, "kernel_hash": "2bdd123281d86a86"},
-    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_125_042_432 + 16_304_640, "kernel_hash": "2bdd123281d86a86"},
+    ("llama70b_layer", "decode_segment_kernel"): {"bytes": 1_338_623_488 + 2_550_528, "kernel_hash": "e2f9552a00f0b381"},
+    ("llama70b_layer", "decode_pair_kernel"): {"bytes": 1_337_551_104 + 1_244_928, "kernel_hash": "e2f9552a00f0b381"},
+    ("prefix_sharing", "decode_segment_kernel"): {"bytes": 2_545_307_392 + 3_103_232, "kernel_hash": "e2f9552a00f0b381"},
+    ("prefix_sharing", "decode_persist_kernel"): {"bytes": 2_551_124_992 + 1_275_648, "kernel_hash": "e2f9552a00f0b381"},
+    ("long_context", "decode_segment_kernel"): {"bytes": 4_296_252_928 + 2_440_192, "kernel_hash": "e2f9552a00f0b381"},
+    ("fp8_mixed", "decode_pair_kernel"): {"bytes": 2_216_397_056 + 12_930_816, "kernel_hash": "e2f9552a00f0b381"},
+    ("fp8_mixed", "decode_segment_kernel"): {"bytes": 2_248_222_464 + 17_221_120, "kernel_hash": "e2f9552a00f0b381"},
+    ("int4_mixed", "decode_segment_kernel"): {"bytes": 1_125_001_984 + 16_473_856, "kernel_hash": "e2f9552a00f0b381"},
 }
 
 

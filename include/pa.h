@@ -175,9 +175,15 @@ typedef struct {
  *     a short unit leaves the extra CTAs idle) and merge through distributed
  *     shared memory; a window or topk that bounds every unit keeps one CTA per
  *     unit when the units fill the GPU or fit one CTA.  Batches of up to 16384
- *     sequences start their longest sequences first.  A batch whose longest
+ *     sequences start their longest sequences first.  A bf16 batch of up to 8
+ *     query heads per KV head with more units than two per CTA the GPU holds at
+ *     once (and at most 4096), and no window or topk, runs one persistent CTA per
+ *     SM instead: every CTA computes the same static schedule from seq_lens
+ *     (whole units dealt out longest first so that each CTA gets about the mean
+ *     number of tiles), cuts its tiles into one contiguous segment per warp, and
+ *     joins units that cross segments in shared memory.  A batch whose longest
  *     sequence outweighs the rest is still held back by it; the split decode is
- *     not.
+ *     not.  Every form gives the same result on every call, bit for bit.
  */
 typedef struct {
     int32_t window;
@@ -238,8 +244,8 @@ pa_status pa_reshape_and_cache(const pa_shape *shape, const void *k_new, const v
 /*
  * pa_decode -- single-token decode attention over the paged cache: one CTA (or,
  * for batches of few units, a cluster of CTAs) per (sequence, KV head) serving
- * the whole query group, or, with a workspace in opts, the split decode and the
- * merge in one call.
+ * the whole query group, persistent CTAs for bf16 batches of many units, or,
+ * with a workspace in opts, the split decode and the merge in one call.
  * [P4] "Custom PagedAttention Kernels" (grid over sequence and head, block-table
  * walk, block staged in shared memory); [P3] section 1 (GQA grouping).
  *     out[b][h][:] = sum_t softmax_t(sm_scale * <q[b][h], K_b[t]>) V_b[t]
