@@ -110,9 +110,12 @@ __global__ void __launch_bounds__(256) cache_write_quant_kernel(
   }
   const int64_t blk = slot / bs;
   auto in_block = [&](int64_t o) { return o >= 0 && o < nslots && o / bs == blk; };
-  // only the block's first token of the call goes on
+  // only the block's first token of the call goes on.  A token right after another of
+  // its block (a prompt's tokens fill their blocks in order) leaves at once; the others
+  // look through every earlier token.
+  if (t > 0 && in_block(slot_mapping[t - 1])) return;
   int earlier = 0;
-  for (int u = tid; u < t; u += blockDim.x) earlier |= in_block(slot_mapping[u]);
+  for (int u = tid; u < t - 1; u += blockDim.x) earlier |= in_block(slot_mapping[u]);
   if (__syncthreads_or(earlier)) return;
   if (tid == 0) offsets_seen = 0u;
   for (int c0 = t; c0 < T; c0 += blockDim.x) {

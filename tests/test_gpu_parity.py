@@ -263,6 +263,32 @@ def test_quantised_prompt_written_in_one_call(bs, int4):
 
 
 @pytest.mark.parametrize("int4", [False, True])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_quantised_long_prompt_in_order(bs, int4):
+    """A 3,000-token prompt written in one call in token order (each block's later tokens
+    follow one of their own block, so they leave without scanning the call), after a
+    block already half full, with a second sequence's tokens and padding rows between
+    some of them.  Codes and scales bit for bit against the oracle."""
+    rng = np.random.default_rng(450 + bs + int4)
+    Hkv, nblocks = 2, 3200 // bs + 16
+    pools = _quant_pools(rng, nblocks, bs, Hkv, int4)
+    blocks = rng.permutation(nblocks)
+    start = bs // 2
+    slots = [int(blocks[(start + p) // bs]) * bs + (start + p) % bs for p in range(3000)]
+    other = [int(blocks[-1]) * bs + j for j in range(5)]
+    for j, at in enumerate(sorted(rng.choice(3000, 5, replace=False))[::-1]):
+        slots.insert(int(at), other[j])
+    slots.insert(1234, -1)
+    T = len(slots)
+    mag = rng.uniform(0.05, 4.0, T)
+    x = (rng.standard_normal((T, Hkv, 128)) * mag[:, None, None]).astype(np.float32)
+    k_new, v_new = wl.bf16_bits(x), wl.bf16_bits(x[::-1].copy())
+    got, want, flag = _quant_write(pools, k_new, v_new, np.asarray(slots, np.int64), bs, int4)
+    _assert_pools_equal(got, want)
+    assert flag == 0
+
+
+@pytest.mark.parametrize("int4", [False, True])
 def test_quantised_duplicate_slot_applied_in_order_and_flagged(int4):
     """Two tokens of one call with the same slot: both applied, the later one last (the
     oracle's order), and PA_DEVERR_FP8_CONFLICT set; distinct slots of a block are not
