@@ -1074,7 +1074,7 @@ def test_pa_decode_many_units(Hq, Hkv, D, lens_kind):
 
 
 @pytest.mark.parametrize("kind", ["prefix", "one_long", "tiny_units", "max_units", "g6_d64",
-                                  "mixed_4000"])
+                                  "mixed_4000", "bs32"])
 def test_pa_decode_persistent(kind):
     """pa_decode without a workspace on bf16 batches of more units than two per resident
     CTA and at most 4,096, with no window or page selection: persistent CTAs of eight
@@ -1083,11 +1083,13 @@ def test_pa_decode_persistent(kind):
     with the L2 hints (800 units); one 30,000-token sequence among short ones (its units
     outweigh a CTA's mean share and cross every segment of their CTAs); 2,048 units of 0
     to 40 tokens (empty units, segments of a few tiles); 4,096 single-head sequences (the
-    largest list); G = 6 at D = 64; 4,000 units of up to 1,500 tokens.  Against the
-    oracle, and repeatable bit for bit."""
+    largest list); G = 6 at D = 64; 4,000 units of up to 1,500 tokens; 32-token blocks.
+    Against the oracle, repeatable bit for bit, and (on the shared prefix) the same bits
+    for any hint values."""
     rng = np.random.default_rng({"prefix": 601, "one_long": 602, "tiny_units": 603,
-                                 "max_units": 604, "g6_d64": 605, "mixed_4000": 606}[kind])
-    Hq, Hkv, D, groups = 64, 8, 128, ()
+                                 "max_units": 604, "g6_d64": 605, "mixed_4000": 606,
+                                 "bs32": 607}[kind])
+    Hq, Hkv, D, groups, bs = 64, 8, 128, (), 16
     if kind == "prefix":
         lens = [900 + int(x) for x in wl.lognormal_lens(rng, 100, 600, 1, 6000)]
         groups = ((900, list(range(100))),)
@@ -1100,10 +1102,13 @@ def test_pa_decode_persistent(kind):
         lens = list(rng.integers(1, 700, 4096))
     elif kind == "mixed_4000":
         lens = list(rng.integers(0, 1501, 500))
+    elif kind == "bs32":                           # 32-token blocks: two tiles per block
+        bs = 32
+        lens = list(rng.integers(0, 2000, 120)) + [31, 32, 33, 4000]
     else:
         Hq, Hkv, D = 48, 8, 64          # four CTAs per SM otherwise: 1,216 resident
         lens = list(rng.integers(0, 1500, 196)) + [0, 1, 16, 17]
-    batch = wl.build_batch("t", lens, Hq=Hq, Hkv=Hkv, D=D, block_size=16, seed=610,
+    batch = wl.build_batch("t", lens, Hq=Hq, Hkv=Hkv, D=D, block_size=bs, seed=610,
                            prefix_groups=groups)
     assert 2 * (4 if D == 64 else 2) * 152 < batch.B * Hkv <= 4096
     dev = DeviceBatch(batch)
@@ -1117,6 +1122,13 @@ def test_pa_decode_persistent(kind):
     assert dev.read_err() == 0
     for _ in range(2):
         assert np.array_equal(_bits(run_gpu(dev, "decode")), _bits(out)), f"{kind} not repeatable"
+    if kind == "prefix":   # any hint values (random, past the end too) give the same bits
+        dev.shared_prefix_lens = torch.from_numpy(
+            rng.integers(0, 8000, batch.B).astype(np.int32)).cuda()
+        dev.out.fill_(float("nan"))
+        dev.decode(hints=True)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(dev.out.cpu().numpy()), _bits(out))
     assert dev.read_err() == 0
 
 
