@@ -253,8 +253,9 @@ struct ScoreCfg {
   static constexpr int STAGES = 2;                 // one chunk in flight while one is scored
   static constexpr int WARPS = 4;
   static constexpr int THREADS = 32 * WARPS;
-  // per warp: stages, then mbarriers, chunk descriptors (int4) and valid-row masks
-  static constexpr int FIXED = WARPS * STAGES * (BUF + 8 + 16 + 4);
+  // per warp: stages, then chunk descriptors (int4), mbarriers and valid-row masks, each
+  // array after the stages at a multiple of its own alignment
+  static constexpr int FIXED = WARPS * STAGES * (BUF + 16 + 8 + 4);
   static_assert(BUF % 16 == 0, "bulk copies need 16-byte aligned stages");
 };
 
@@ -274,8 +275,8 @@ __global__ void __launch_bounds__(S::THREADS) quest_score_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t *stage = smem + warp * ST * S::BUF;
   uint8_t *tail = smem + S::WARPS * ST * S::BUF;
-  uint64_t *bar = reinterpret_cast<uint64_t *>(tail) + warp * ST;
-  int4 *desc = reinterpret_cast<int4 *>(tail + S::WARPS * ST * 8) + warp * ST;
+  int4 *desc = reinterpret_cast<int4 *>(tail) + warp * ST;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(tail + S::WARPS * ST * 16) + warp * ST;
   unsigned *okms = reinterpret_cast<unsigned *>(tail + S::WARPS * ST * 24) + warp * ST;
   int32_t *prefix = reinterpret_cast<int32_t *>(smem + S::FIXED);
   const int G = Hq / Hkv;
