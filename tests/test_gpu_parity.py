@@ -1074,7 +1074,7 @@ def test_pa_decode_many_units(Hq, Hkv, D, lens_kind):
 
 
 @pytest.mark.parametrize("kind", ["prefix", "one_long", "tiny_units", "max_units", "g6_d64",
-                                  "mixed_4000", "bs32"])
+                                  "mixed_4000", "bs32", "g1", "g2"])
 def test_pa_decode_persistent(kind):
     """pa_decode without a workspace on bf16 batches of more units than two per resident
     CTA and at most 4,096, with no window or page selection: persistent CTAs of eight
@@ -1083,12 +1083,13 @@ def test_pa_decode_persistent(kind):
     with the L2 hints (800 units); one 30,000-token sequence among short ones (its units
     outweigh a CTA's mean share and cross every segment of their CTAs); 2,048 units of 0
     to 40 tokens (empty units, segments of a few tiles); 4,096 single-head sequences (the
-    largest list); G = 6 at D = 64; 4,000 units of up to 1,500 tokens; 32-token blocks.
+    largest list); G = 6 at D = 64; 4,000 units of up to 1,500 tokens; 32-token blocks;
+    G = 1 and 2.
     Against the oracle, repeatable bit for bit, and (on the shared prefix) the same bits
     for any hint values."""
     rng = np.random.default_rng({"prefix": 601, "one_long": 602, "tiny_units": 603,
                                  "max_units": 604, "g6_d64": 605, "mixed_4000": 606,
-                                 "bs32": 607}[kind])
+                                 "bs32": 607, "g1": 608, "g2": 609}[kind])
     Hq, Hkv, D, groups, bs = 64, 8, 128, (), 16
     if kind == "prefix":
         lens = [900 + int(x) for x in wl.lognormal_lens(rng, 100, 600, 1, 6000)]
@@ -1105,6 +1106,9 @@ def test_pa_decode_persistent(kind):
     elif kind == "bs32":                           # 32-token blocks: two tiles per block
         bs = 32
         lens = list(rng.integers(0, 2000, 120)) + [31, 32, 33, 4000]
+    elif kind in ("g1", "g2"):                     # one or two query heads per KV head
+        Hq = 8 if kind == "g1" else 16
+        lens = list(rng.integers(0, 1200, 96)) + [1, 16, 17, 3000]
     else:
         Hq, Hkv, D = 48, 8, 64          # four CTAs per SM otherwise: 1,216 resident
         lens = list(rng.integers(0, 1500, 196)) + [0, 1, 16, 17]
